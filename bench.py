@@ -1,0 +1,469 @@
+#!/usr/bin/env python
+"""Benchmark of the KDA gated delta-rule serving path on GB300.
+
+One step is one pass of every phase of the path, each on its own synthetic
+workload at 16 heads x 128 (the pages' single-GPU microbenchmark setting,
+"[KDA] Support Helion MTP verification and harden prefill, decode", sglang
+PR #42857, Speed Tests and Profiling):
+  prefill   1 sequence x 4096 tokens, 16-slot FP32 pool      (the headline)
+  decode    48 requests x 1 token, 240-slot pool
+  verify    16 requests x 6 draft tokens, chain and tree, with snapshots
+  commit    16 requests, accepted prefix copied into the pool
+`value` is prefill tokens/s (the metric's first term) over the prefill phase
+time; every phase is timed with CUDA events on the launching stream, and L2
+is flushed (a 512 MiB write) before each phase.  `phases` carries the
+per-layer-call microseconds of every phase.  `e2e` repeats the prefill with
+its inputs copied from pinned host memory and its output copied back inside
+the timed region.
+
+Multi-GPU: the path has no exchange step, so N ranks run N independent
+replicas (weak scaling); `value` is the tokens of all ranks over the slowest
+rank's time.
+
+--impl reference times the FP64 CPU oracle (the slow reference program) on a
+bounded sample of the same prefill workload, on this machine's host cores.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+H, K = 16, 128
+CHUNK = 64
+METRIC = "KDA prefill tok/s @16h×128; decode/verify µs/layer; % HBM/TC roofline"
+PREFILL_T = 4096
+DECODE_B = 48
+VERIFY_B, VERIFY_T = 16, 6
+COMMIT_B = VERIFY_B
+FLUSH_BYTES = 512 << 20
+
+# DRAM traffic per launch from ncu (dram__bytes_read.sum + dram__bytes_write.sum),
+# keyed by kernel; valid only while the kernel sources hash to the recorded value.
+NCU_TRAFFIC = {}
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p.get("sm_max_mhz", 2070.0)), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, 1900.0, 2070.0, "fallback"
+
+
+def _source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "linear_attention_serving_gated_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+# --------------------------------------------------------------------------- #
+# algorithmic work per launch (bytes moved at minimum, or flops of the chunk form)
+
+def prefill_bytes(T, nseq=1):
+    # q, k, v, gate input a, o (BF16, T x H x 128 each), beta (BF16), state read+write
+    return 5 * T * H * K * 2 + T * H * 2 + nseq * 2 * H * K * K * 4
+
+
+def transform_flops(T):
+    # A, P, W, Util (C^2 K each, triangular) and the inverse (C^3 / 3) per chunk-head
+    n = (T + CHUNK - 1) // CHUNK * H
+    return n * (4 * CHUNK * CHUNK * K + CHUNK ** 3 / 3)
+
+
+def pass_flops(T):
+    # P U (C^2 V) and W S, Qtil S, Khat^T U (2 C K V each) per chunk-head
+    n = (T + CHUNK - 1) // CHUNK * H
+    return n * (CHUNK * CHUNK * K + 3 * 2 * CHUNK * K * K)
+
+
+def token_io_bytes():
+    # one packed row (q, k, v), gate input, beta, output, all BF16
+    return (3 * H * K + H * K + H + H * K) * 2
+
+
+def decode_bytes(B):
+    return B * (2 * H * K * K * 4 + token_io_bytes())
+
+
+def verify_bytes(B, T):
+    return B * (H * K * K * 4 + T * H * K * K * 4 + T * token_io_bytes())
+
+
+def commit_bytes(B):
+    return B * 2 * H * K * K * 4
+
+
+# --------------------------------------------------------------------------- #
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples every 200 ms while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = str(gpu_index)
+        self.proc = None
+        self.t_start = self.t_stop = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        mhz, max_mhz, reasons = [], 0.0, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in out.splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                mhz.append(float(f[1]))
+                max_mhz = max(max_mhz, float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not mhz:
+            return None
+        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": max_mhz,
+                "reasons": sorted(reasons), "samples": len(mhz)}
+
+
+def physical_gpu_index(local_rank):
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        ids = [x.strip() for x in vis.split(",") if x.strip()]
+        if local_rank < len(ids):
+            return ids[local_rank]
+    return local_rank
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    from linear_attention_serving_gated_gb300 import build as kbuild
+    from linear_attention_serving_gated_gb300 import inputs, kda
+
+    torch.cuda.set_device(local_rank)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    if rank == 0:
+        kbuild.build()
+    if world > 1:
+        dist.barrier()
+    kda.load()
+    dev = torch.device("cuda", local_rank)
+    stream = torch.cuda.current_stream()
+
+    def bf(x):
+        return torch.from_numpy(np.ascontiguousarray(x)).to(dev).view(torch.bfloat16)
+
+    def t(x):
+        return torch.from_numpy(np.ascontiguousarray(x)).to(dev)
+
+    # ---- workloads (seeded, synthetic; per-rank seed so replicas differ) ----
+    pf = inputs.prefill_inputs(seed=rank, lengths=[PREFILL_T], H=H, slots=16)
+    gate = kda.Gate(A_log=t(pf["A_log"]), dt_bias=t(pf["dt_bias"]), lower_bound=-5.0)
+    D = kda.dims(H)
+    P = {n: bf(pf[n]) for n in ("q", "k", "v", "g", "beta")}
+    p_pool = t(pf["pool"])
+    p_idx = t(pf["state_idx"])
+    p_cu = t(pf["cu_seqlens"])
+    p_o = torch.empty((PREFILL_T, H, K), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(kda.kda_prefill_workspace_size(D, 1, PREFILL_T), dtype=torch.uint8, device=dev)
+
+    dd = inputs.decode_inputs(seed=100 + rank, B=DECODE_B, H=H, slots=240)
+    DX = {n: bf(dd[n]) for n in ("mixed_qkv", "a", "b")}
+    d_pool = t(dd["pool"])
+    d_idx = t(dd["state_idx"])
+    d_o = torch.empty((DECODE_B, H, K), dtype=torch.bfloat16, device=dev)
+
+    vd = inputs.verify_inputs(seed=200 + rank, B=VERIFY_B, T=VERIFY_T, H=H, slots=240)
+    VX = {n: bf(vd[n]) for n in ("mixed_qkv", "a", "b")}
+    v_pool = t(vd["pool"])
+    v_idx = t(vd["state_idx"])
+    v_par = t(vd["parent"])
+    v_o = torch.empty((VERIFY_B, VERIFY_T, H, K), dtype=torch.bfloat16, device=dev)
+    v_snap = torch.empty((VERIFY_B, VERIFY_T, H, K, K), device=dev)
+    v_snap2 = torch.empty_like(v_snap)
+    accepted = t(np.random.default_rng(rank).integers(-1, VERIFY_T, size=COMMIT_B).astype(np.int32))
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    phases = ["prefill", "decode", "verify_chain", "verify_tree", "commit"]
+    kernels = ["prefill_transform", "prefill_pass", "decode", "verify_chain", "verify_tree", "commit"]
+    stage = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    kda.kda_prefill_set_stage_events(stage)
+
+    def run_phase(name):
+        if name == "prefill":
+            kda.kda_prefill(D, gate, P["q"], P["k"], P["v"], P["g"], P["beta"], p_pool, p_idx, p_cu, 1,
+                            p_o, workspace=ws)
+        elif name == "decode":
+            kda.kda_decode_packed(D, gate, DX["mixed_qkv"], DX["a"], DX["b"], d_pool, d_idx, d_o)
+        elif name == "verify_chain":
+            kda.kda_verify_chain(D, gate, VX["mixed_qkv"], VX["a"], VX["b"], VERIFY_B, VERIFY_T, v_pool,
+                                 v_idx, v_o, v_snap)
+        elif name == "verify_tree":
+            kda.kda_verify_tree(D, gate, VX["mixed_qkv"], VX["a"], VX["b"], VERIFY_B, VERIFY_T, v_par,
+                                v_pool, v_idx, v_o, v_snap2)
+        elif name == "commit":
+            kda.kda_commit(D, v_snap, COMMIT_B, VERIFY_T, accepted, v_pool, v_idx)
+
+    def one_step(record):
+        times = {}
+        for name in phases:
+            flush.zero_()
+            if record:
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+            run_phase(name)
+            if record:
+                e1.record(stream)
+                times[name] = (e0, e1)
+        return times
+
+    for _ in range(max(args.warmup, 3)):
+        one_step(False)
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(physical_gpu_index(local_rank)) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.5)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    records = []
+    for _ in range(args.steps):
+        # fresh stage events per step: the prefill records its two kernels' bounds into them
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        kda.kda_prefill_set_stage_events(ev)
+        rec = one_step(True)
+        rec["_stage"] = ev
+        records.append(rec)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    wall = time.perf_counter() - wall0
+    clocks = sampler.stop() if sampler else None
+    kda.kda_prefill_set_stage_events(None)
+
+    ph_ms = {n: [r[n][0].elapsed_time(r[n][1]) for r in records] for n in phases}
+    k_ms = {
+        "prefill_transform": [r["_stage"][0].elapsed_time(r["_stage"][1]) for r in records],
+        "prefill_pass": [r["_stage"][1].elapsed_time(r["_stage"][2]) for r in records],
+        "decode": ph_ms["decode"], "verify_chain": ph_ms["verify_chain"],
+        "verify_tree": ph_ms["verify_tree"], "commit": ph_ms["commit"],
+    }
+    tot = {n: sum(v) for n, v in ph_ms.items()}
+    if world > 1:
+        vec = torch.tensor([tot[n] for n in phases], device=dev, dtype=torch.float64)
+        dist.all_reduce(vec, op=dist.ReduceOp.MAX)
+        tot = {n: float(vec[i]) for i, n in enumerate(phases)}
+
+    # ---- e2e: prefill through the C ABI with host buffers ----
+    host = {n: torch.from_numpy(np.ascontiguousarray(pf[n])).pin_memory()
+            for n in ("q", "k", "v", "g", "beta", "state_idx", "cu_seqlens")}
+    o_host = torch.empty((PREFILL_T, H, K), dtype=torch.int16).pin_memory()
+    dbuf = {n: torch.empty(host[n].shape, dtype=host[n].dtype, device=dev) for n in host}
+    h2d = sum(x.numel() * x.element_size() for x in host.values())
+    d2h = o_host.numel() * o_host.element_size()
+    e2e_steps = max(3, min(args.steps, 50))
+    ev_e2e = []
+    for i in range(e2e_steps + 3):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for n in host:
+            dbuf[n].copy_(host[n], non_blocking=True)
+        kda.kda_prefill(D, gate, *(dbuf[n].view(torch.bfloat16) for n in ("q", "k", "v", "g", "beta")),
+                        p_pool, dbuf["state_idx"], dbuf["cu_seqlens"], 1, p_o, workspace=ws)
+        o_host.copy_(p_o.view(torch.int16), non_blocking=True)
+        e1.record(stream)
+        if i >= 3:
+            ev_e2e.append((e0, e1))
+    torch.cuda.synchronize()
+    e2e_ms = sum(a.elapsed_time(b) for a, b in ev_e2e)
+    if world > 1:
+        x = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(x, op=dist.ReduceOp.MAX)
+        e2e_ms = float(x.item())
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    hbm, bf16_tf, sm_max, peak_kind = _peaks()
+    steps = args.steps
+    prefill_s = tot["prefill"] / 1e3
+    value = PREFILL_T * steps * world / prefill_s
+    mean_k = {n: statistics.mean(v) for n, v in k_ms.items()}
+    # FP32 CUDA-core peak: 152 SMs x 128 FMA lanes x 2 flops x max SM clock
+    alu_peak = 152 * 128 * 2 * sm_max * 1e6 / 1e12
+    work = {
+        "prefill_transform": ("alu", transform_flops(PREFILL_T) / 1e12, alu_peak, "TFLOP/s"),
+        "prefill_pass": ("alu", pass_flops(PREFILL_T) / 1e12, alu_peak, "TFLOP/s"),
+        "decode": ("hbm", decode_bytes(DECODE_B) / 1e9, hbm, "GB/s"),
+        "verify_chain": ("hbm", verify_bytes(VERIFY_B, VERIFY_T) / 1e9, hbm, "GB/s"),
+        "verify_tree": ("hbm", verify_bytes(VERIFY_B, VERIFY_T) / 1e9, hbm, "GB/s"),
+        "commit": ("hbm", commit_bytes(COMMIT_B) / 1e9, hbm, "GB/s"),
+    }
+    dom = max(mean_k, key=mean_k.get)
+    bound, per_launch, peak, unit = work[dom]
+    achieved = per_launch / (mean_k[dom] / 1e3)
+    src = _source_hash()
+    tr = NCU_TRAFFIC.get(dom)
+    traffic = tr["bytes"] if tr and tr.get("src") == src else None
+    roofline = {"kernel": dom, "bound": bound, "achieved": round(achieved, 3), "peak": peak,
+                "unit": unit, "frac": round(achieved / peak, 4), "traffic": traffic,
+                "peak_source": peak_kind if bound != "alu" else "derived: 152 SM x 128 FP32 lanes x 2 x max SM clock"}
+    kern = {}
+    for n in kernels:
+        b_, w_, p_, u_ = work[n]
+        a_ = w_ / (mean_k[n] / 1e3)
+        kern[n] = {"us": round(mean_k[n] * 1e3, 2), "bound": b_, "achieved": round(a_, 2), "unit": u_,
+                   "frac": round(a_ / p_, 4)}
+    phase_out = {
+        "prefill_1x4096": {"us": round(statistics.mean(ph_ms["prefill"]) * 1e3, 2),
+                           "tok_s": round(value / world, 1),
+                           "hbm_frac_of_call": round(prefill_bytes(PREFILL_T) / (statistics.mean(ph_ms["prefill"]) / 1e3) / 1e9 / hbm, 4)},
+        "decode_b48": {"us": round(statistics.mean(ph_ms["decode"]) * 1e3, 2)},
+        "verify_chain_b16x6": {"us": round(statistics.mean(ph_ms["verify_chain"]) * 1e3, 2)},
+        "verify_tree_b16x6": {"us": round(statistics.mean(ph_ms["verify_tree"]) * 1e3, 2)},
+        "commit_b16": {"us": round(statistics.mean(ph_ms["commit"]) * 1e3, 2)},
+        "kernels": kern,
+    }
+    out = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+        "steps": steps, "warmup": args.warmup,
+        "ms_per_step": round(sum(tot.values()) / steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16 in / fp32 state",
+        "data": "synthetic (seeded; q,k,v,a,beta ~N(0,1) BF16, A_log~U(-1,1), dt_bias~N(0,0.1), state~N(0,0.02))",
+        "config": {"workload": "KDA prefill 1x4096 tokens, 16 heads x 128 (+ decode B=48, verify 16x6 chain/tree, commit 16)",
+                   "global_batch": world, "seq_len": PREFILL_T, "heads": H, "head_dim": K,
+                   "parallelism": f"replicas x{world}", "l2": "flushed (512 MiB write) before every phase"},
+        "gpu_launches": steps * len(kernels),
+        "phases": phase_out,
+        "roofline": roofline,
+        "e2e": {"value": round(PREFILL_T * e2e_steps * world / (e2e_ms / 1e3), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "clocks": clocks, "wall_s_timed": round(wall, 3), "source_hash": src,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(pf, budget_s=10.0)
+    print(json.dumps(out), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def cpu_baseline(pf, budget_s=10.0, tokens=None):
+    """The oracle, as it stands, on this host's cores."""
+    from oracle import kda_oracle as ko
+
+    T = PREFILL_T if tokens is None else tokens
+    gate = ko.Gate(H, K, K, A_log=pf["A_log"], dt_bias=pf["dt_bias"], lower_bound=-5.0)
+    cores = os.cpu_count() or 1
+    sl = {n: np.ascontiguousarray(pf[n][:T]) for n in ("q", "k", "v", "g", "beta")}
+    runs, t0 = 0, time.perf_counter()
+    while True:
+        pool = pf["pool"].astype(np.float64)
+        ko.prefill(gate, sl["q"], sl["k"], sl["v"], sl["g"], sl["beta"], pool, pf["state_idx"],
+                   np.array([0, T], np.int32), nthreads=cores)
+        runs += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or runs >= 50:
+            break
+    return {"value": round(T * runs / el, 1), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"prefill 1x{T} tokens x 16 heads, full call, {runs} run(s) in {el:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    from oracle import kda_oracle as ko
+    from linear_attention_serving_gated_gb300 import inputs
+
+    ko.build()
+    pf = inputs.prefill_inputs(seed=0, lengths=[PREFILL_T], H=H, slots=16)
+    sample_T = 512  # bounded sample of the 1x4096 workload per step
+    gate = ko.Gate(H, K, K, A_log=pf["A_log"], dt_bias=pf["dt_bias"], lower_bound=-5.0)
+    cores = os.cpu_count() or 1
+    sl = {n: np.ascontiguousarray(pf[n][:sample_T]) for n in ("q", "k", "v", "g", "beta")}
+
+    def step():
+        pool = pf["pool"].astype(np.float64)
+        ko.prefill(gate, sl["q"], sl["k"], sl["v"], sl["g"], sl["beta"], pool, pf["state_idx"],
+                   np.array([0, sample_T], np.int32), nthreads=cores)
+
+    for _ in range(max(args.warmup, 1)):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    el = time.perf_counter() - t0
+    value = sample_T * args.steps / el
+    out = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(el / args.steps * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded, same generator)",
+        "config": {"workload": "KDA prefill 1x4096 tokens, 16 heads x 128 (oracle on a 512-token sample per step)",
+                   "seq_len": PREFILL_T, "heads": H, "head_dim": K},
+        "cpu_baseline": {"value": round(value, 1), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"first {sample_T} tokens of the 1x4096 x 16-head prefill per step"},
+        "e2e": {"value": round(value, 1), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", args.gpus if "RANK" in os.environ else 1))
+    local_rank = int(os.environ.get("LOCAL_RANK", 0))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()

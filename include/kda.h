@@ -1,0 +1,191 @@
+/*
+ * kda.h -- C ABI of the KDA (Kimi Delta Attention) gated delta-rule serving
+ * path on one NVIDIA GB300 (sm_103a).
+ *
+ * The rule, per head, with S a K x V FP32 state:
+ *   S_t = (I - beta_t k_t k_t^T) Diag(exp(g_t)) S_{t-1} + beta_t k_t v_t^T
+ *   o_t = scale * S_t^T q_t
+ * with q, k optionally L2-normalised (x / sqrt(sum x^2 + 1e-6)), beta
+ * optionally sigmoid(raw beta), and g either given (a log-decay) or the
+ * bounded gate g = lower_bound * sigmoid(exp(A_log[h]) * (a + dt_bias[h,:])).
+ *
+ * The three serving phases and their contracts come from the pages:
+ *   prefill  -- chunk_kda in "PR #35197 report: fix(kernel) Fix Helion
+ *               small-token prefill bug" (key source snippet of
+ *               kda_prefill.py; implementation steps 1-2),
+ *   decode   -- validate_packed_decode_inputs in the same report (snippet of
+ *               kda_decode.py; implementation step 3),
+ *   verify   -- "[KDA] Support Helion MTP verification and harden prefill,
+ *               decode" (sglang PR #42857), Modifications: chain/tree
+ *               verification with per-candidate state snapshots; its review
+ *               thread: commit a partially accepted prefix, then replay.
+ *
+ * Conventions shared by every entry point:
+ *   - Every tensor pointer is a DEVICE pointer owned by the caller.  The
+ *     library allocates nothing, never synchronises and never reads device
+ *     memory from the host, so each call can be captured in a CUDA graph and
+ *     replayed with new device-resident indices.
+ *   - BF16 tensors are passed as raw 16-bit patterns (kda_bf16).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy stream).
+ *   - Host-checkable errors return a status and launch nothing.
+ *   - Device-resident index errors (a state slot outside [-1, pool_slots), a
+ *     tree parent outside [-1, i), a malformed cu_seqlens, an accepted index
+ *     >= T) set bits in *err_flag when err_flag is non-NULL and the affected
+ *     unit (sequence or request) is skipped; kernels never trap.  The caller
+ *     zeroes *err_flag.
+ *   - A state slot of -1 marks a padding sequence/request: it is skipped,
+ *     its output rows are written as zero and its pool slot is not touched.
+ *   - Slots within one call must be distinct (a caller error otherwise).
+ *   - This build supports H == HV and K == V == 128; other shapes return
+ *     KDA_ERR_UNSUPPORTED (non-power-of-two K or V are always rejected, as
+ *     the packed-decode validator does).
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t kda_bf16; /* raw BF16 bits */
+
+typedef enum {
+  KDA_OK = 0,
+  KDA_ERR_NULL_ARG = 1,    /* a required pointer is NULL (e.g. no pool or no indices) */
+  KDA_ERR_SHAPE = 2,       /* inconsistent sizes (e.g. gate/beta rows < tokens) */
+  KDA_ERR_UNSUPPORTED = 3, /* a shape or option this build does not implement */
+  KDA_ERR_WORKSPACE = 4,   /* workspace missing or smaller than required */
+  KDA_ERR_CUDA = 5,        /* a CUDA launch failed; see cudaGetLastError */
+  KDA_ERR_ALIGNMENT = 6    /* a pointer or stride is not 16-byte aligned */
+} kda_status;
+
+/* device-side error bits written to *err_flag */
+#define KDA_DEVERR_SLOT 1     /* state slot outside [-1, pool_slots) */
+#define KDA_DEVERR_PARENT 2   /* tree parent outside [-1, i) */
+#define KDA_DEVERR_SEQLENS 4  /* cu_seqlens not 0 .. total_tokens, non-decreasing */
+#define KDA_DEVERR_ACCEPTED 8 /* accepted index >= T */
+
+typedef struct {
+  int H;  /* q/k heads */
+  int HV; /* value heads (== H in this build) */
+  int K;  /* key head dim (128) */
+  int V;  /* value head dim (128) */
+} kda_dims;
+
+typedef struct {
+  const float *A_log;   /* device [HV] FP32, or NULL: g is already a log-decay */
+  const float *dt_bias; /* device [HV*K] FP32, or NULL (zero bias) */
+  float lower_bound;    /* bound of the gate (e.g. -5); NaN = none.  Required
+                           when A_log is given: the unbounded gate formula is
+                           not supported (KDA_ERR_UNSUPPORTED). */
+  int beta_is_raw;      /* 1: beta <- sigmoid(beta) */
+  int use_qk_l2norm;    /* 1: q, k <- x / sqrt(sum x^2 + 1e-6) */
+  float scale;          /* output scale, usually K^-0.5 */
+} kda_gate;
+
+/* Human-readable name of a status. */
+const char *kda_status_string(kda_status s);
+
+/* Bytes of device workspace kda_prefill needs for this call shape (an upper
+ * bound over every cu_seqlens with this many sequences and tokens). */
+size_t kda_prefill_workspace_size(kda_dims dims, int num_seqs, int64_t total_tokens);
+
+/*
+ * Chunked varlen prefill from an indexed initial-state pool (chunk_kda).
+ *   q, k          [total_tokens, H, K]    BF16
+ *   v             [total_tokens, HV, V]   BF16
+ *   g             [gb_rows, HV, K] BF16: gate input a (A_log given) or log-decay
+ *   beta          [gb_rows, HV]    BF16: raw beta (beta_is_raw) or beta
+ *   gb_rows       >= total_tokens (else KDA_ERR_SHAPE).  Rows past
+ *                 total_tokens are CUDA-graph bucket padding and never read.
+ *   state_pool    [pool_slots, HV, V, K] FP32, updated in place: sequence n
+ *                 starts from slot state_idx[n] and its final state is
+ *                 written back there.  NULL pool or indices: KDA_ERR_NULL_ARG.
+ *   state_idx     [num_seqs] int32 (device)
+ *   cu_seqlens    [num_seqs+1] int32 (device) or NULL for the fixed layout
+ *                 (num_seqs equal lengths, total_tokens % num_seqs == 0).
+ *                 A sequence of length 0 leaves its state unchanged.
+ *   o             [total_tokens, HV, V] BF16 (round to nearest even)
+ *   intermediate  NULL, or [sum_n ceil(T_n/64), HV, V, K] FP32: the state at
+ *                 the start of every 64-token chunk of every sequence,
+ *                 sequence-major.
+ *   workspace     >= kda_prefill_workspace_size(...) bytes, 256-byte aligned.
+ * T = 1 takes the same kernels as any other length.
+ */
+kda_status kda_prefill(kda_dims dims, kda_gate gate, const kda_bf16 *q, const kda_bf16 *k,
+                       const kda_bf16 *v, const kda_bf16 *g, const kda_bf16 *beta,
+                       int64_t gb_rows, float *state_pool, int pool_slots,
+                       const int32_t *state_idx, const int32_t *cu_seqlens, int num_seqs,
+                       int64_t total_tokens, kda_bf16 *o, float *intermediate,
+                       void *workspace, size_t workspace_bytes, int32_t *err_flag,
+                       void *stream);
+
+/*
+ * Packed single-token decode (one token per request), state updated in place.
+ *   mixed_qkv     [B, row_stride] BF16, each row [q (H*K) | k (H*K) | v (HV*V)];
+ *                 row_stride >= 2*H*K + HV*V and a multiple of 8 elements.
+ *   a             [B, HV*K] BF16 gate input (or log-decay when A_log is NULL)
+ *   b             [B, HV]   BF16 raw beta (or beta)
+ *   state_pool    [pool_slots, HV, V, K] FP32, slot state_idx[r] read and
+ *                 written in place.
+ *   o             [B, HV, V] BF16
+ */
+kda_status kda_decode_packed(kda_dims dims, kda_gate gate, const kda_bf16 *mixed_qkv,
+                             int64_t row_stride, const kda_bf16 *a, const kda_bf16 *b, int B,
+                             float *state_pool, int pool_slots, const int32_t *state_idx,
+                             kda_bf16 *o, int32_t *err_flag, void *stream);
+
+/*
+ * Speculative chain verify: T draft tokens per request, request-major rows
+ * (row r*T + i is draft token i of request r) in mixed_qkv, a and b, laid out
+ * as for decode.  The pool is READ ONLY.
+ *   o             [B, T, HV, V] BF16
+ *   snapshots     [B, T, HV, V, K] FP32: snapshots[r][i] is the state after
+ *                 draft token i (the per-candidate state snapshot).
+ */
+kda_status kda_verify_chain(kda_dims dims, kda_gate gate, const kda_bf16 *mixed_qkv,
+                            int64_t row_stride, const kda_bf16 *a, const kda_bf16 *b, int B,
+                            int T, const float *state_pool, int pool_slots,
+                            const int32_t *state_idx, kda_bf16 *o, float *snapshots,
+                            int32_t *err_flag, void *stream);
+
+/*
+ * Speculative tree verify: as kda_verify_chain, but node i of request r
+ * continues from node parent_idx[r*T+i] (parent < i; -1 = the pool state).
+ *   parent_idx    [B, T] int32 (device)
+ */
+kda_status kda_verify_tree(kda_dims dims, kda_gate gate, const kda_bf16 *mixed_qkv,
+                           int64_t row_stride, const kda_bf16 *a, const kda_bf16 *b, int B,
+                           int T, const int32_t *parent_idx, const float *state_pool,
+                           int pool_slots, const int32_t *state_idx, kda_bf16 *o,
+                           float *snapshots, int32_t *err_flag, void *stream);
+
+/*
+ * Commit of the accepted draft prefix: for each request r with
+ * accepted[r] >= 0, state_pool[state_idx[r]] <- snapshots[r][accepted[r]]
+ * (a bit-exact copy).  accepted[r] = -1 keeps the pool state.
+ *   snapshots     [B, T, HV, V, K] FP32 as written by verify
+ *   accepted      [B] int32 (device)
+ */
+kda_status kda_commit(kda_dims dims, const float *snapshots, int B, int T,
+                      const int32_t *accepted, float *state_pool, int pool_slots,
+                      const int32_t *state_idx, int32_t *err_flag, void *stream);
+
+/*
+ * Profiling aid (not part of the pages' contract): per-stage timing of
+ * kda_prefill.  After kda_prefill_set_stage_events(ev) with three cudaEvent_t
+ * handles passed as void*, every kda_prefill call records ev[0] on its stream
+ * before its first kernel, ev[1] between the chunk-transform and the
+ * state-pass kernels, and ev[2] after the state pass.  NULL clears it.  The
+ * setting is process-wide and not meant for concurrent callers.
+ */
+void kda_prefill_set_stage_events(void *const *events);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */

@@ -1,0 +1,350 @@
+// kda_recurrent.cu -- packed decode, chain/tree speculative verify and commit.
+//
+// Phases (pages): packed single-token decode with the bounded gate routed to
+// the packed kernel, and chain/tree target verification that writes a
+// per-candidate state snapshot after every draft token ("[KDA] Support Helion
+// MTP verification and harden prefill, decode", sglang PR #42857,
+// Motivation and Modifications); the decode input contract of
+// validate_packed_decode_inputs ("PR #35197 report: fix(kernel) Fix Helion
+// small-token prefill bug", kda_decode.py snippet); commit of an accepted
+// prefix between verify rounds (PR #42857 review thread).
+//
+// Design (GB300): these phases move each 64 KiB FP32 head state once per call
+// and do ~6 flops per state element per token, so they are HBM-bound.  Every
+// thread keeps its share of the state in registers for the whole call:
+//   * one CTA = 4 warps covers 16*GROUPS rows j of S^T ([V][K], K contiguous);
+//   * a warp works on 4 rows at once, 8 lanes per row, each lane holding 16
+//     key channels c = i*32 + sub*4 + {0..3} (i < 4) as four float4, so each
+//     128-bit load instruction reads four full 128-byte row segments;
+//   * k^T x and S^T q are 16-term packed-FP32 (f32x2) partial dots finished
+//     with three xor-shuffles inside the 8-lane row group;
+//   * the fold (L2 norm, gate, sigmoid beta) is recomputed per CTA from the
+//     16 channels a lane owns, so no shared memory and no __syncthreads;
+//   * verify keeps the state in registers across the T draft tokens and
+//     writes each snapshot straight from registers; a tree node whose parent
+//     is not the previous node reloads the parent's snapshot, which this same
+//     thread wrote (so it is visible to it without any barrier).
+#include "kda_host.h"
+
+namespace kda {
+namespace {
+
+enum Mode { kDecode = 0, kChain = 1, kTree = 2 };
+
+struct StepArgs {
+  GateArgs gate;
+  int H, HV;
+  const kda_bf16* mixed_qkv;
+  int64_t row_stride;
+  const kda_bf16* a;
+  const kda_bf16* b;
+  int B, T;
+  const int32_t* parent;
+  float* pool;
+  int pool_slots;
+  const int32_t* state_idx;
+  kda_bf16* o;
+  float* snapshots;
+  int32_t* err_flag;
+};
+
+__device__ __forceinline__ float group_sum8(float x) {
+  x += __shfl_xor_sync(0xffffffffu, x, 1);
+  x += __shfl_xor_sync(0xffffffffu, x, 2);
+  x += __shfl_xor_sync(0xffffffffu, x, 4);
+  return x;
+}
+
+__device__ __forceinline__ float dot16(const float4 (&x)[4], const float4 (&y)[4]) {
+  float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    acc = fma2(make_float2(x[i].x, x[i].y), make_float2(y[i].x, y[i].y), acc);
+    acc = fma2(make_float2(x[i].z, x[i].w), make_float2(y[i].z, y[i].w), acc);
+  }
+  return acc.x + acc.y;
+}
+
+template <int MODE, int GROUPS>
+__global__ void __launch_bounds__(128) recurrent_kernel(const StepArgs args) {
+  constexpr int K = kHeadDim, V = kHeadDim;
+  const int r = blockIdx.z, h = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int sub = lane & 7;
+  const int row0 = blockIdx.x * (16 * GROUPS) + warp * (4 * GROUPS) + (lane >> 3);
+  const int T = MODE == kDecode ? 1 : args.T;
+  const int HV = args.HV;
+  const bool reporter = threadIdx.x == 0 && blockIdx.x == 0 && h == 0;
+
+  const int slot = args.state_idx[r];
+  bool ok = slot >= -1 && slot < args.pool_slots;
+  if (!ok && reporter) set_error(args.err_flag, KDA_DEVERR_SLOT);
+  if (MODE == kTree && ok) {
+    for (int i = 0; i < T; ++i) {
+      const int p = args.parent[(int64_t)r * T + i];
+      if (p < -1 || p >= i) {
+        ok = false;
+        if (reporter) set_error(args.err_flag, KDA_DEVERR_PARENT);
+      }
+    }
+  }
+  if (!ok || slot < 0) {  // padding or rejected request: zero outputs, touch no state
+    if (sub == 0)
+      for (int i = 0; i < T; ++i)
+#pragma unroll
+        for (int gi = 0; gi < GROUPS; ++gi)
+          args.o[(((int64_t)r * T + i) * HV + h) * V + row0 + gi * 4] = 0;
+    return;
+  }
+
+  const size_t head_elems = (size_t)V * K;
+  float* root = args.pool + ((size_t)slot * HV + h) * head_elems;
+  const int lane_col = sub * 4;
+
+  float4 S[GROUPS][4];
+#pragma unroll
+  for (int gi = 0; gi < GROUPS; ++gi)
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      S[gi][i] = *reinterpret_cast<const float4*>(root + (size_t)(row0 + gi * 4) * K + i * 32 +
+                                                  lane_col);
+
+  const GateArgs& ga = args.gate;
+  const float exp_alog = ga.A_log ? expf(ga.A_log[h]) : 0.f;
+  float4 bias[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    bias[i] = ga.dt_bias ? __ldg(reinterpret_cast<const float4*>(ga.dt_bias + h * K + i * 32 +
+                                                                 lane_col))
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
+
+  for (int t = 0; t < T; ++t) {
+    if (MODE == kTree && t > 0) {
+      const int p = args.parent[(int64_t)r * T + t];
+      if (p != t - 1) {
+        const float* src =
+            p < 0 ? root : args.snapshots + (((size_t)r * T + p) * HV + h) * head_elems;
+#pragma unroll
+        for (int gi = 0; gi < GROUPS; ++gi)
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            S[gi][i] = *reinterpret_cast<const float4*>(src + (size_t)(row0 + gi * 4) * K +
+                                                        i * 32 + lane_col);
+      }
+    }
+    const int64_t row = MODE == kDecode ? r : (int64_t)r * T + t;
+    const kda_bf16* x = args.mixed_qkv + row * args.row_stride;
+    const kda_bf16* qp = x + h * K;
+    const kda_bf16* kp = x + (int64_t)args.H * K + h * K;
+    const kda_bf16* vp = x + 2 * (int64_t)args.H * K + h * V;
+    const kda_bf16* ap = args.a + row * ((int64_t)HV * K) + h * K;
+
+    float4 q[4], k[4], dec[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      q[i] = load_bf16x4(qp + i * 32 + lane_col);
+      k[i] = load_bf16x4(kp + i * 32 + lane_col);
+      dec[i] = load_bf16x4(ap + i * 32 + lane_col);
+    }
+    float vj[GROUPS];
+#pragma unroll
+    for (int gi = 0; gi < GROUPS; ++gi) vj[gi] = bf16_bits_to_float(vp[row0 + gi * 4]);
+    const float beta = fold_beta(ga, bf16_bits_to_float(args.b[row * HV + h]));
+
+    if (ga.use_qk_l2norm) {
+      const float rq = rsqrtf(group_sum8(dot16(q, q)) + kNormEps);
+      const float rk = rsqrtf(group_sum8(dot16(k, k)) + kNormEps);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        q[i].x *= rq; q[i].y *= rq; q[i].z *= rq; q[i].w *= rq;
+        k[i].x *= rk; k[i].y *= rk; k[i].z *= rk; k[i].w *= rk;
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      dec[i].x = expf(gate_log_decay(ga, dec[i].x, exp_alog, bias[i].x));
+      dec[i].y = expf(gate_log_decay(ga, dec[i].y, exp_alog, bias[i].y));
+      dec[i].z = expf(gate_log_decay(ga, dec[i].z, exp_alog, bias[i].z));
+      dec[i].w = expf(gate_log_decay(ga, dec[i].w, exp_alog, bias[i].w));
+    }
+
+    float* snap = MODE == kDecode ? nullptr
+                                  : args.snapshots + (((size_t)r * T + t) * HV + h) * head_elems;
+#pragma unroll
+    for (int gi = 0; gi < GROUPS; ++gi) {
+      // X = Diag(exp g) S;  u = beta (v - X^T k);  S = X + k u^T;  o = scale S^T q
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 lo = mul2(make_float2(S[gi][i].x, S[gi][i].y), make_float2(dec[i].x, dec[i].y));
+        const float2 hi = mul2(make_float2(S[gi][i].z, S[gi][i].w), make_float2(dec[i].z, dec[i].w));
+        S[gi][i] = make_float4(lo.x, lo.y, hi.x, hi.y);
+      }
+      const float u = beta * (vj[gi] - group_sum8(dot16(S[gi], k)));
+      const float2 u2 = make_float2(u, u);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 lo = fma2(make_float2(k[i].x, k[i].y), u2, make_float2(S[gi][i].x, S[gi][i].y));
+        const float2 hi = fma2(make_float2(k[i].z, k[i].w), u2, make_float2(S[gi][i].z, S[gi][i].w));
+        S[gi][i] = make_float4(lo.x, lo.y, hi.x, hi.y);
+      }
+      const float out = ga.scale * group_sum8(dot16(S[gi], q));
+      const int j = row0 + gi * 4;
+      if (sub == 0) args.o[(row * HV + h) * V + j] = float_to_bf16_bits(out);
+      float* dst = MODE == kDecode ? root + (size_t)j * K : snap + (size_t)j * K;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) *reinterpret_cast<float4*>(dst + i * 32 + lane_col) = S[gi][i];
+    }
+  }
+}
+
+__global__ void __launch_bounds__(256) commit_kernel(const float* __restrict__ snapshots, int T,
+                                                     const int32_t* __restrict__ accepted,
+                                                     float* __restrict__ pool, int pool_slots,
+                                                     const int32_t* __restrict__ state_idx,
+                                                     size_t slot_elems, int32_t* err_flag) {
+  const int r = blockIdx.y;
+  const int acc = accepted[r];
+  const int slot = state_idx[r];
+  const bool reporter = threadIdx.x == 0 && blockIdx.x == 0;
+  if (acc < 0) return;
+  if (acc >= T) {
+    if (reporter) set_error(err_flag, KDA_DEVERR_ACCEPTED);
+    return;
+  }
+  if (slot < -1 || slot >= pool_slots) {
+    if (reporter) set_error(err_flag, KDA_DEVERR_SLOT);
+    return;
+  }
+  if (slot < 0) return;
+  const float4* src = reinterpret_cast<const float4*>(snapshots + ((size_t)r * T + acc) * slot_elems);
+  float4* dst = reinterpret_cast<float4*>(pool + (size_t)slot * slot_elems);
+  const size_t n4 = slot_elems / 4;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
+       i += (size_t)gridDim.x * blockDim.x)
+    dst[i] = __ldcs(src + i);
+}
+
+template <int MODE>
+kda_status launch_recurrent(const StepArgs& a, cudaStream_t stream) {
+  // Small batches use 16-row CTAs so that even one request spreads over 128
+  // CTAs; larger batches use 32-row CTAs to halve the per-CTA fold work.
+  const int64_t units = (int64_t)a.B * a.HV;
+  if (units * 8 <= 2 * 152) {
+    dim3 grid(kHeadDim / 16, a.HV, a.B);
+    recurrent_kernel<MODE, 1><<<grid, 128, 0, stream>>>(a);
+  } else {
+    dim3 grid(kHeadDim / 32, a.HV, a.B);
+    recurrent_kernel<MODE, 2><<<grid, 128, 0, stream>>>(a);
+  }
+  return launch_status();
+}
+
+kda_status check_packed(const kda_dims& dims, const kda_gate& gate, const kda_bf16* mixed_qkv,
+                        int64_t row_stride, const kda_bf16* a, const kda_bf16* b, int B,
+                        const void* pool, int pool_slots, const int32_t* state_idx,
+                        const kda_bf16* o, StepArgs* out) {
+  kda_status s = check_dims(dims);
+  if (s != KDA_OK) return s;
+  if (!pool || !state_idx) return KDA_ERR_NULL_ARG;
+  if (B < 0 || pool_slots < 0) return KDA_ERR_SHAPE;
+  if (B > 0 && (!mixed_qkv || !a || !b || !o)) return KDA_ERR_NULL_ARG;
+  if (row_stride < 2 * (int64_t)dims.H * dims.K + (int64_t)dims.HV * dims.V)
+    return KDA_ERR_SHAPE;
+  if (row_stride % 8 != 0 || !aligned16(mixed_qkv) || !aligned16(a) || !aligned16(pool))
+    return KDA_ERR_ALIGNMENT;
+  s = check_gate(gate, &out->gate);
+  if (s != KDA_OK) return s;
+  out->H = dims.H;
+  out->HV = dims.HV;
+  out->mixed_qkv = mixed_qkv;
+  out->row_stride = row_stride;
+  out->a = a;
+  out->b = b;
+  out->B = B;
+  out->pool_slots = pool_slots;
+  out->state_idx = state_idx;
+  return KDA_OK;
+}
+
+}  // namespace
+}  // namespace kda
+
+using namespace kda;
+
+extern "C" kda_status kda_decode_packed(kda_dims dims, kda_gate gate, const kda_bf16* mixed_qkv,
+                                        int64_t row_stride, const kda_bf16* a, const kda_bf16* b,
+                                        int B, float* state_pool, int pool_slots,
+                                        const int32_t* state_idx, kda_bf16* o, int32_t* err_flag,
+                                        void* stream) {
+  StepArgs args{};
+  kda_status s = check_packed(dims, gate, mixed_qkv, row_stride, a, b, B, state_pool, pool_slots,
+                              state_idx, o, &args);
+  if (s != KDA_OK) return s;
+  if (B == 0) return KDA_OK;
+  args.T = 1;
+  args.pool = state_pool;
+  args.o = o;
+  args.err_flag = err_flag;
+  return launch_recurrent<kDecode>(args, static_cast<cudaStream_t>(stream));
+}
+
+static kda_status verify_common(kda_dims dims, kda_gate gate, const kda_bf16* mixed_qkv,
+                                int64_t row_stride, const kda_bf16* a, const kda_bf16* b, int B,
+                                int T, const int32_t* parent_idx, const float* state_pool,
+                                int pool_slots, const int32_t* state_idx, kda_bf16* o,
+                                float* snapshots, int32_t* err_flag, void* stream, bool tree) {
+  StepArgs args{};
+  kda_status s = check_packed(dims, gate, mixed_qkv, row_stride, a, b, B, state_pool, pool_slots,
+                              state_idx, o, &args);
+  if (s != KDA_OK) return s;
+  if (T < 1) return KDA_ERR_SHAPE;
+  if (B == 0) return KDA_OK;
+  if (!snapshots || (tree && !parent_idx)) return KDA_ERR_NULL_ARG;
+  if (!aligned16(snapshots)) return KDA_ERR_ALIGNMENT;
+  args.T = T;
+  args.parent = parent_idx;
+  args.pool = const_cast<float*>(state_pool);  // read only in verify
+  args.o = o;
+  args.snapshots = snapshots;
+  args.err_flag = err_flag;
+  return tree ? launch_recurrent<kTree>(args, static_cast<cudaStream_t>(stream))
+              : launch_recurrent<kChain>(args, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" kda_status kda_verify_chain(kda_dims dims, kda_gate gate, const kda_bf16* mixed_qkv,
+                                       int64_t row_stride, const kda_bf16* a, const kda_bf16* b,
+                                       int B, int T, const float* state_pool, int pool_slots,
+                                       const int32_t* state_idx, kda_bf16* o, float* snapshots,
+                                       int32_t* err_flag, void* stream) {
+  return verify_common(dims, gate, mixed_qkv, row_stride, a, b, B, T, nullptr, state_pool,
+                       pool_slots, state_idx, o, snapshots, err_flag, stream, false);
+}
+
+extern "C" kda_status kda_verify_tree(kda_dims dims, kda_gate gate, const kda_bf16* mixed_qkv,
+                                      int64_t row_stride, const kda_bf16* a, const kda_bf16* b,
+                                      int B, int T, const int32_t* parent_idx,
+                                      const float* state_pool, int pool_slots,
+                                      const int32_t* state_idx, kda_bf16* o, float* snapshots,
+                                      int32_t* err_flag, void* stream) {
+  return verify_common(dims, gate, mixed_qkv, row_stride, a, b, B, T, parent_idx, state_pool,
+                       pool_slots, state_idx, o, snapshots, err_flag, stream, true);
+}
+
+extern "C" kda_status kda_commit(kda_dims dims, const float* snapshots, int B, int T,
+                                 const int32_t* accepted, float* state_pool, int pool_slots,
+                                 const int32_t* state_idx, int32_t* err_flag, void* stream) {
+  kda_status s = check_dims(dims);
+  if (s != KDA_OK) return s;
+  if (!state_pool || !state_idx) return KDA_ERR_NULL_ARG;
+  if (B < 0 || T < 1 || pool_slots < 0) return KDA_ERR_SHAPE;
+  if (B == 0) return KDA_OK;
+  if (!snapshots || !accepted) return KDA_ERR_NULL_ARG;
+  if (!aligned16(snapshots) || !aligned16(state_pool)) return KDA_ERR_ALIGNMENT;
+  const size_t slot_elems = (size_t)dims.HV * dims.V * dims.K;
+  // 16 KiB per CTA: a 1 MiB slot spreads over 64 CTAs per request.
+  const int per_slot = (int)((slot_elems * sizeof(float) + 16383) / 16384);
+  dim3 grid(per_slot, B);
+  commit_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      snapshots, T, accepted, state_pool, pool_slots, state_idx, slot_elems, err_flag);
+  return launch_status();
+}

@@ -1,0 +1,208 @@
+"""ctypes binding of libkda (include/kda.h): the same entry points, taking
+torch tensors on the GPU and marshalling them to device pointers.
+
+Every step of the computation runs in the library's CUDA kernels; this
+module only checks dtypes/devices, passes pointers, sizes and the current
+stream, and raises ``KdaError`` on a non-OK status.  If ``libkda.so`` is
+missing it raises at the first call: there is no other implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libkda.so")
+
+KDA_OK = 0
+KDA_ERR_NULL_ARG = 1
+KDA_ERR_SHAPE = 2
+KDA_ERR_UNSUPPORTED = 3
+KDA_ERR_WORKSPACE = 4
+KDA_ERR_CUDA = 5
+KDA_ERR_ALIGNMENT = 6
+
+KDA_DEVERR_SLOT = 1
+KDA_DEVERR_PARENT = 2
+KDA_DEVERR_SEQLENS = 4
+KDA_DEVERR_ACCEPTED = 8
+
+CHUNK = 64
+
+
+class KdaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} (status {status})")
+
+
+class kda_dims(ctypes.Structure):
+    _fields_ = [("H", ctypes.c_int), ("HV", ctypes.c_int), ("K", ctypes.c_int), ("V", ctypes.c_int)]
+
+
+class kda_gate(ctypes.Structure):
+    _fields_ = [("A_log", ctypes.c_void_p), ("dt_bias", ctypes.c_void_p),
+                ("lower_bound", ctypes.c_float), ("beta_is_raw", ctypes.c_int),
+                ("use_qk_l2norm", ctypes.c_int), ("scale", ctypes.c_float)]
+
+
+EXPORTS = ("kda_status_string", "kda_prefill_workspace_size", "kda_prefill", "kda_decode_packed",
+           "kda_verify_chain", "kda_verify_tree", "kda_commit", "kda_prefill_set_stage_events")
+
+_lib = None
+
+
+def load(path: str = LIB_PATH):
+    """Load libkda.so (built by build.py).  Raises if it is missing."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(path):
+            raise RuntimeError(f"libkda.so not built ({path}); run linear_attention_serving_gated_gb300.build.build()")
+        lib = ctypes.CDLL(path)
+        vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+        lib.kda_status_string.restype = ctypes.c_char_p
+        lib.kda_status_string.argtypes = [i32]
+        lib.kda_prefill_workspace_size.restype = sz
+        lib.kda_prefill_workspace_size.argtypes = [kda_dims, i32, i64]
+        lib.kda_prefill.restype = i32
+        lib.kda_prefill.argtypes = [kda_dims, kda_gate, vp, vp, vp, vp, vp, i64, vp, i32, vp, vp, i32,
+                                    i64, vp, vp, vp, sz, vp, vp]
+        lib.kda_decode_packed.restype = i32
+        lib.kda_decode_packed.argtypes = [kda_dims, kda_gate, vp, i64, vp, vp, i32, vp, i32, vp, vp,
+                                          vp, vp]
+        lib.kda_verify_chain.restype = i32
+        lib.kda_verify_chain.argtypes = [kda_dims, kda_gate, vp, i64, vp, vp, i32, i32, vp, i32, vp,
+                                         vp, vp, vp, vp]
+        lib.kda_verify_tree.restype = i32
+        lib.kda_verify_tree.argtypes = [kda_dims, kda_gate, vp, i64, vp, vp, i32, i32, vp, vp, i32,
+                                        vp, vp, vp, vp, vp]
+        lib.kda_commit.restype = i32
+        lib.kda_commit.argtypes = [kda_dims, vp, i32, i32, vp, vp, i32, vp, vp, vp]
+        lib.kda_prefill_set_stage_events.restype = None
+        lib.kda_prefill_set_stage_events.argtypes = [ctypes.POINTER(ctypes.c_void_p)]
+        _lib = lib
+    return _lib
+
+
+def status_string(status: int) -> str:
+    try:
+        return load().kda_status_string(int(status)).decode()
+    except RuntimeError:
+        return f"status {status}"
+
+
+def _check(status: int, where: str):
+    if status != KDA_OK:
+        raise KdaError(status, where)
+
+
+def _p(t):
+    """Device pointer of a tensor (or None)."""
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("libkda takes device tensors")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _bf16(t, name):
+    if t is not None and t.dtype not in (torch.bfloat16, torch.int16):
+        raise TypeError(f"{name} must be bfloat16 (got {t.dtype})")
+    return _p(t)
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+class Gate:
+    """Fold options of a call (kda_gate): A_log [HV] / dt_bias [HV*K] FP32
+    device tensors or None, lower_bound (None = unbounded, rejected when
+    A_log is given), beta_is_raw, use_qk_l2norm, scale."""
+
+    def __init__(self, A_log=None, dt_bias=None, lower_bound=-5.0, beta_is_raw=True,
+                 use_qk_l2norm=True, scale=128 ** -0.5):
+        self.A_log, self.dt_bias = A_log, dt_bias
+        self.lower_bound = lower_bound
+        self.beta_is_raw, self.use_qk_l2norm, self.scale = beta_is_raw, use_qk_l2norm, scale
+
+    def c(self):
+        for t in (self.A_log, self.dt_bias):
+            if t is not None and t.dtype != torch.float32:
+                raise TypeError("A_log and dt_bias must be float32")
+        lb = float("nan") if self.lower_bound is None else float(self.lower_bound)
+        return kda_gate(_p(self.A_log), _p(self.dt_bias), lb, int(bool(self.beta_is_raw)),
+                        int(bool(self.use_qk_l2norm)), float(self.scale))
+
+
+def dims(H, K=128, V=128, HV=None):
+    return kda_dims(int(H), int(HV if HV is not None else H), int(K), int(V))
+
+
+def kda_prefill_workspace_size(d: kda_dims, num_seqs: int, total_tokens: int) -> int:
+    return int(load().kda_prefill_workspace_size(d, int(num_seqs), int(total_tokens)))
+
+
+def kda_prefill(d, gate: Gate, q, k, v, g, beta, state_pool, state_idx, cu_seqlens, num_seqs,
+                o, intermediate=None, workspace=None, err_flag=None, stream=None):
+    """Chunked varlen prefill (see kda.h).  q,k [T,H,K], v [T,HV,V], g
+    [gb_rows,HV,K], beta [gb_rows,HV] bf16; state_pool [slots,HV,V,K] fp32
+    (in place); o [T,HV,V] bf16 (written)."""
+    T = q.shape[0]
+    gb_rows = g.shape[0]
+    if workspace is None:
+        need = kda_prefill_workspace_size(d, num_seqs, T)
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    st = load().kda_prefill(
+        d, gate.c(), _bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v"), _bf16(g, "g"), _bf16(beta, "beta"),
+        int(gb_rows), _p(state_pool), int(state_pool.shape[0]), _p(state_idx), _p(cu_seqlens),
+        int(num_seqs), int(T), _bf16(o, "o"), _p(intermediate), _p(workspace),
+        int(workspace.numel() * workspace.element_size()), _p(err_flag), _stream(stream))
+    _check(st, "kda_prefill")
+
+
+def kda_decode_packed(d, gate: Gate, mixed_qkv, a, b, state_pool, state_idx, o, err_flag=None,
+                      stream=None):
+    st = load().kda_decode_packed(
+        d, gate.c(), _bf16(mixed_qkv, "mixed_qkv"), int(mixed_qkv.stride(0)), _bf16(a, "a"),
+        _bf16(b, "b"), int(mixed_qkv.shape[0]), _p(state_pool), int(state_pool.shape[0]),
+        _p(state_idx), _bf16(o, "o"), _p(err_flag), _stream(stream))
+    _check(st, "kda_decode_packed")
+
+
+def kda_verify_chain(d, gate: Gate, mixed_qkv, a, b, B, T, state_pool, state_idx, o, snapshots,
+                     err_flag=None, stream=None):
+    st = load().kda_verify_chain(
+        d, gate.c(), _bf16(mixed_qkv, "mixed_qkv"), int(mixed_qkv.stride(0)), _bf16(a, "a"),
+        _bf16(b, "b"), int(B), int(T), _p(state_pool), int(state_pool.shape[0]), _p(state_idx),
+        _bf16(o, "o"), _p(snapshots), _p(err_flag), _stream(stream))
+    _check(st, "kda_verify_chain")
+
+
+def kda_verify_tree(d, gate: Gate, mixed_qkv, a, b, B, T, parent_idx, state_pool, state_idx, o,
+                    snapshots, err_flag=None, stream=None):
+    st = load().kda_verify_tree(
+        d, gate.c(), _bf16(mixed_qkv, "mixed_qkv"), int(mixed_qkv.stride(0)), _bf16(a, "a"),
+        _bf16(b, "b"), int(B), int(T), _p(parent_idx), _p(state_pool), int(state_pool.shape[0]),
+        _p(state_idx), _bf16(o, "o"), _p(snapshots), _p(err_flag), _stream(stream))
+    _check(st, "kda_verify_tree")
+
+
+def kda_commit(d, snapshots, B, T, accepted, state_pool, state_idx, err_flag=None, stream=None):
+    st = load().kda_commit(d, _p(snapshots), int(B), int(T), _p(accepted), _p(state_pool),
+                           int(state_pool.shape[0]), _p(state_idx), _p(err_flag), _stream(stream))
+    _check(st, "kda_commit")
+
+
+def kda_prefill_set_stage_events(events=None):
+    """Profiling aid: torch.cuda.Event triple recorded by every later
+    kda_prefill call (before, between its two kernels, after); None clears."""
+    if events is None:
+        load().kda_prefill_set_stage_events(None)
+        return
+    arr = (ctypes.c_void_p * 3)(*[ctypes.c_void_p(e.cuda_event) for e in events])
+    load().kda_prefill_set_stage_events(arr)

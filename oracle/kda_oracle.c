@@ -118,17 +118,18 @@ static void fold_token(const kdao_params *p, int h, const float *q_in,
 
 /* One step of the gated delta rule on one head.
  * st: S^T in pool layout, st[j*K + c] = S[c][j].
- * work: scratch of V doubles.
+ * work: scratch of V doubles.  g is overwritten with exp(g).
  *   X = Diag(exp(g)) S
  *   S = (I - beta k k^T) X + beta k v^T, applying (I - beta k k^T) to X as
  *       X - beta k (k^T X)
  *   o = scale * S^T q                                                     */
 static void gated_delta_step(int K, int V, double *st, const double *q,
-                             const double *k, const float *v, const double *g,
+                             const double *k, const float *v, double *g,
                              double beta, double scale, double *o,
                              double *work) {
+  for (int c = 0; c < K; ++c) g[c] = exp(g[c]); /* Diag(exp(g)), g consumed */
   for (int j = 0; j < V; ++j)
-    for (int c = 0; c < K; ++c) st[j * K + c] *= exp(g[c]);
+    for (int c = 0; c < K; ++c) st[j * K + c] *= g[c];
   for (int j = 0; j < V; ++j) { /* work = k^T X */
     double s = 0.0;
     for (int c = 0; c < K; ++c) s += k[c] * st[j * K + c];

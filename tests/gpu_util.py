@@ -1,0 +1,64 @@
+"""Helpers for the GPU parity tests: moving seeded inputs to the device and
+the tolerance checks.
+
+Tolerances: BF16 outputs max |err| <= 2e-2 * RMS(o_oracle); FP32 states and
+snapshots max |err| <= 1e-3 * RMS(S_oracle); index handling bit-exact.
+"""
+import numpy as np
+import torch
+
+from linear_attention_serving_gated_gb300 import kda
+from oracle import kda_oracle as ko
+
+O_TOL = 2e-2
+S_TOL = 1e-3
+
+
+def dev_bf16(x):
+    """int16 BF16 bit array -> device bfloat16 tensor."""
+    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.int16)).cuda().view(torch.bfloat16)
+
+
+def dev(x, dtype=None):
+    t = torch.from_numpy(np.ascontiguousarray(x))
+    if dtype is not None:
+        t = t.to(dtype)
+    return t.cuda()
+
+
+def host_f64(t):
+    """Device tensor -> float64 numpy (bf16 widened exactly)."""
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def rms(x):
+    return float(np.sqrt(np.mean(np.square(x)))) if x.size else 0.0
+
+
+def assert_o_close(o_gpu, o_ref, what="o"):
+    got = host_f64(o_gpu) if isinstance(o_gpu, torch.Tensor) else o_gpu
+    err = float(np.max(np.abs(got - o_ref))) if o_ref.size else 0.0
+    bound = O_TOL * rms(o_ref)
+    assert np.isfinite(got).all(), f"{what}: non-finite values"
+    assert err <= bound, f"{what}: max|err| {err:.3e} > {bound:.3e} (2e-2 x RMS)"
+    return err / max(rms(o_ref), 1e-300)
+
+
+def assert_s_close(s_gpu, s_ref, what="state"):
+    got = host_f64(s_gpu) if isinstance(s_gpu, torch.Tensor) else s_gpu
+    err = float(np.max(np.abs(got - s_ref))) if s_ref.size else 0.0
+    bound = S_TOL * rms(s_ref)
+    assert np.isfinite(got).all(), f"{what}: non-finite values"
+    assert err <= bound, f"{what}: max|err| {err:.3e} > {bound:.3e} (1e-3 x RMS)"
+    return err / max(rms(s_ref), 1e-300)
+
+
+def gates(d, lower_bound=-5.0, beta_is_raw=True, use_qk_l2norm=True, scale=None, H=None, K=128):
+    """Matching oracle and device gate descriptions from seeded inputs."""
+    H = H if H is not None else d["A_log"].shape[0]
+    scale = scale if scale is not None else K ** -0.5
+    og = ko.Gate(H, K, K, A_log=d["A_log"], dt_bias=d["dt_bias"], lower_bound=lower_bound,
+                 beta_is_raw=beta_is_raw, use_qk_l2norm=use_qk_l2norm, scale=scale)
+    gg = kda.Gate(A_log=dev(d["A_log"]), dt_bias=dev(d["dt_bias"]), lower_bound=lower_bound,
+                  beta_is_raw=beta_is_raw, use_qk_l2norm=use_qk_l2norm, scale=scale)
+    return og, gg

@@ -1,0 +1,113 @@
+"""C-ABI checks that need no GPU: the library loads, exports every entry
+point include/kda.h declares, and rejects bad host-side arguments with the
+status codes that mirror the pages' ValueErrors ("PR #35197 report:
+fix(kernel) Fix Helion small-token prefill bug", key source snippets of
+kda_prefill.py and kda_decode.py).  Every call here returns before touching
+the device, so dummy non-NULL pointers are safe."""
+import ctypes
+import math
+import os
+import re
+
+import pytest
+
+from linear_attention_serving_gated_gb300 import build, kda
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kda.h")
+DUMMY = ctypes.c_void_p(0x10000)  # 16-byte aligned, never dereferenced
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return kda.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kda_[a-z_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert set(names) == set(kda.EXPORTS), names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    for s in range(7):
+        assert kda.status_string(s)
+    assert "workspace" in kda.status_string(kda.KDA_ERR_WORKSPACE)
+
+
+def test_workspace_size_scales_with_chunks(lib):
+    d = kda.dims(16)
+    one = kda.kda_prefill_workspace_size(d, 1, 64)
+    assert one > 0
+    assert kda.kda_prefill_workspace_size(d, 1, 4096) == one * (4096 // 64 + 1) // 2
+    assert kda.kda_prefill_workspace_size(d, 8, 32768) >= kda.kda_prefill_workspace_size(d, 1, 32768)
+
+
+def _gate(A_log=None, lb=-5.0):
+    return kda.kda_gate(A_log, None, lb, 1, 1, 128 ** -0.5)
+
+
+def _prefill(lib, dims=None, gate=None, pool=DUMMY, idx=DUMMY, gb_rows=64, T=64, num_seqs=1,
+             ws=DUMMY, ws_bytes=1 << 40, q=DUMMY):
+    return lib.kda_prefill(dims or kda.dims(4), gate or _gate(), q, DUMMY, DUMMY, DUMMY, DUMMY,
+                           gb_rows, pool, 4, idx, None, num_seqs, T, DUMMY, None, ws, ws_bytes,
+                           None, None)
+
+
+def test_prefill_host_errors(lib):
+    # no pool or no indices: an indexed initial-state pool is required
+    assert _prefill(lib, pool=None) == kda.KDA_ERR_NULL_ARG
+    assert _prefill(lib, idx=None) == kda.KDA_ERR_NULL_ARG
+    # gate/beta must cover every q token
+    assert _prefill(lib, gb_rows=63) == kda.KDA_ERR_SHAPE
+    # non-power-of-two head dims are rejected; other shapes are not built
+    assert _prefill(lib, dims=kda.dims(4, K=96, V=128)) == kda.KDA_ERR_UNSUPPORTED
+    assert _prefill(lib, dims=kda.dims(4, K=128, V=100)) == kda.KDA_ERR_UNSUPPORTED
+    assert _prefill(lib, dims=kda.dims(4, K=64, V=64)) == kda.KDA_ERR_UNSUPPORTED
+    assert _prefill(lib, dims=kda.dims(4, HV=8)) == kda.KDA_ERR_UNSUPPORTED
+    # bounded gate formula only
+    assert _prefill(lib, gate=_gate(A_log=DUMMY, lb=math.nan)) == kda.KDA_ERR_UNSUPPORTED
+    # fixed layout needs equal lengths
+    assert _prefill(lib, T=65, gb_rows=65, num_seqs=2) == kda.KDA_ERR_SHAPE
+    # workspace
+    assert _prefill(lib, ws=None) == kda.KDA_ERR_WORKSPACE
+    assert _prefill(lib, ws_bytes=16) == kda.KDA_ERR_WORKSPACE
+    assert _prefill(lib, ws=ctypes.c_void_p(0x10010)) == kda.KDA_ERR_ALIGNMENT
+    assert _prefill(lib, q=ctypes.c_void_p(0x10002)) == kda.KDA_ERR_ALIGNMENT
+
+
+def test_decode_host_errors(lib):
+    d, g = kda.dims(16), _gate()
+    row = 2 * 16 * 128 + 16 * 128
+
+    def call(dims=d, stride=row, pool=DUMMY, idx=DUMMY, B=2):
+        return lib.kda_decode_packed(dims, g, DUMMY, stride, DUMMY, DUMMY, B, pool, 240, idx,
+                                     DUMMY, None, None)
+
+    assert call(pool=None) == kda.KDA_ERR_NULL_ARG
+    assert call(idx=None) == kda.KDA_ERR_NULL_ARG
+    assert call(dims=kda.dims(16, K=96)) == kda.KDA_ERR_UNSUPPORTED
+    assert call(stride=row - 8) == kda.KDA_ERR_SHAPE
+    assert call(stride=row + 4) == kda.KDA_ERR_ALIGNMENT
+    assert call(B=0) == kda.KDA_OK  # nothing to do, nothing launched
+
+
+def test_verify_and_commit_host_errors(lib):
+    d, g = kda.dims(16), _gate()
+    row = 3 * 16 * 128
+    assert lib.kda_verify_chain(d, g, DUMMY, row, DUMMY, DUMMY, 2, 0, DUMMY, 240, DUMMY, DUMMY,
+                                DUMMY, None, None) == kda.KDA_ERR_SHAPE
+    assert lib.kda_verify_chain(d, g, DUMMY, row, DUMMY, DUMMY, 2, 6, DUMMY, 240, DUMMY, DUMMY,
+                                None, None, None) == kda.KDA_ERR_NULL_ARG
+    assert lib.kda_verify_tree(d, g, DUMMY, row, DUMMY, DUMMY, 2, 6, None, DUMMY, 240, DUMMY,
+                               DUMMY, DUMMY, None, None) == kda.KDA_ERR_NULL_ARG
+    assert lib.kda_commit(d, DUMMY, 2, 6, DUMMY, None, 240, DUMMY, None, None) == kda.KDA_ERR_NULL_ARG
+    assert lib.kda_commit(d, DUMMY, 2, 0, DUMMY, DUMMY, 240, DUMMY, None, None) == kda.KDA_ERR_SHAPE

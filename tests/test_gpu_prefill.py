@@ -1,0 +1,164 @@
+"""GPU parity of kda_prefill against the FP64 oracle, through the C ABI.
+
+Contract cases follow "PR #35197 report: fix(kernel) Fix Helion small-token
+prefill bug" (implementation steps 1-2 and 4: trimmed gate/beta padding rows,
+T = 1 handled without poisoning later shapes, fixed and varlen layouts) and
+the microbenchmark shapes of "[KDA] Support Helion MTP verification and harden
+prefill, decode" (sglang PR #42857, Speed Tests and Profiling: 1x4096,
+1x8192, 2x4096 at 16 heads x 128).
+"""
+import numpy as np
+import pytest
+import torch
+
+from linear_attention_serving_gated_gb300 import inputs, kda
+from oracle import kda_oracle as ko
+from tests.gpu_util import assert_o_close, assert_s_close, dev, dev_bf16, gates, host_f64
+
+pytestmark = pytest.mark.gpu
+
+K = 128
+
+
+def run_both(d, H, varlen=True, intermediate=False, num_seqs=None, oracle=True):
+    """Runs the CUDA prefill and the oracle on the same inputs.
+    Returns a dict with device results and oracle results."""
+    og, gg = gates(d, H=H)
+    lens = d["lengths"]
+    n = len(lens) if num_seqs is None else num_seqs
+    T = int(lens.sum())
+    x = {name: dev_bf16(d[name]) for name in ("q", "k", "v", "g", "beta")}
+    pool = dev(d["pool"])
+    pool_before = pool.clone()
+    idx = dev(d["state_idx"])
+    cu = dev(d["cu_seqlens"]) if varlen else None
+    o = torch.full((T, H, K), float("nan"), dtype=torch.bfloat16, device="cuda")
+    nch = int(sum((int(L) + 63) // 64 for L in lens))
+    inter = torch.full((nch, H, K, K), float("nan"), device="cuda") if intermediate else None
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kda.kda_prefill(kda.dims(H), gg, x["q"], x["k"], x["v"], x["g"], x["beta"], pool, idx, cu, n, o,
+                    inter, err_flag=err)
+    torch.cuda.synchronize()
+    out = dict(o=o, pool=pool, pool_before=pool_before, inter=inter, err=int(err.item()))
+    if oracle:
+        opool = d["pool"].astype(np.float64)
+        res = ko.prefill(og, d["q"], d["k"], d["v"], d["g"], d["beta"], opool, d["state_idx"],
+                         d["cu_seqlens"] if varlen else None, num_seqs=n, intermediate=intermediate)
+        out["o_ref"], out["inter_ref"] = (res if intermediate else (res, None))
+        out["pool_ref"] = opool
+    return out
+
+
+def check(out, d):
+    assert out["err"] == 0
+    assert_o_close(out["o"], out["o_ref"])
+    idx = [int(s) for s in d["state_idx"] if s >= 0]
+    pool = out["pool"]
+    assert_s_close(pool[idx], out["pool_ref"][idx], "final state")
+    untouched = [s for s in range(pool.shape[0]) if s not in idx]
+    if untouched:
+        assert torch.equal(pool[untouched], out["pool_before"][untouched]), "untouched slots changed"
+    if out["inter"] is not None:
+        assert_s_close(out["inter"], out["inter_ref"], "chunk-start states")
+
+
+def test_prefill_small_config_128_tokens_4_heads():
+    """1 sequence x 128 tokens, 4 heads, slot 0 of a 4-slot pool."""
+    d = inputs.prefill_inputs(seed=0, lengths=[128], H=4, slots=4, state_idx=[0])
+    check(run_both(d, 4, intermediate=True), d)
+
+
+@pytest.mark.parametrize("lengths", [[1], [2], [63], [64], [65], [1, 0, 63, 64, 65, 200, 129]])
+def test_prefill_ragged_varlen_with_garbage_padding(lengths):
+    T = sum(lengths)
+    d = inputs.prefill_inputs(seed=len(lengths) * 7 + T, lengths=lengths, H=2, slots=len(lengths) + 3,
+                              gb_rows=T + 37)
+    check(run_both(d, 2, intermediate=True), d)
+
+
+def test_prefill_fixed_layout_equal_lengths():
+    d = inputs.prefill_inputs(seed=21, lengths=[96, 96, 96], H=2, slots=5, varlen=False)
+    check(run_both(d, 2, varlen=False), d)
+
+
+def test_single_token_prefill_does_not_poison_later_shapes():
+    for seed, lens in ((30, [1]), (31, [130]), (32, [1]), (33, [64, 1, 7])):
+        d = inputs.prefill_inputs(seed=seed, lengths=lens, H=2, slots=4, gb_rows=sum(lens) + 5)
+        check(run_both(d, 2), d)
+
+
+@pytest.mark.parametrize("varlen", [True, False])
+def test_prefill_ignores_padded_gate_rows(varlen):
+    """Same call with NaN/1e4 garbage or zeros in gate/beta padding rows gives
+    bitwise-identical results."""
+    outs = []
+    for garbage in (True, False):
+        d = inputs.prefill_inputs(seed=40, lengths=[70, 70], H=2, slots=3, gb_rows=256,
+                                  garbage=garbage, varlen=varlen)
+        outs.append(run_both(d, 2, varlen=varlen, oracle=garbage))
+    check(outs[0], inputs.prefill_inputs(seed=40, lengths=[70, 70], H=2, slots=3, gb_rows=256,
+                                         varlen=varlen))
+    assert torch.equal(outs[0]["o"], outs[1]["o"])
+    assert torch.equal(outs[0]["pool"], outs[1]["pool"])
+
+
+@pytest.mark.parametrize("T,zero", [(4096, False), (8192, True)])
+def test_prefill_full_size_16_heads(T, zero):
+    """The pages' single-GPU microbenchmark shape: 1 x T, 16 heads x 128."""
+    d = inputs.prefill_inputs(seed=0, lengths=[T], H=16, slots=16, zero_state=zero)
+    check(run_both(d, 16), d)
+
+
+def test_prefill_two_sequences_of_4096():
+    d = inputs.prefill_inputs(seed=3, lengths=[4096, 4096], H=16, slots=16, varlen=False)
+    check(run_both(d, 16, varlen=False), d)
+
+
+def test_prefill_varlen_32k_bucket_240_slot_pool():
+    """8 sequences U[1,8192] (one of length 1), gate/beta padded to a
+    32768-row bucket with garbage, 240-slot pool, random distinct slots."""
+    rng = np.random.default_rng(0)
+    lens = inputs.varlen_lengths(rng)
+    d = inputs.prefill_inputs(seed=0, lengths=lens, H=16, slots=240, gb_rows=32768)
+    out = run_both(d, 16)
+    check(out, d)
+
+
+def test_prefill_padding_sequence_and_device_errors():
+    d = inputs.prefill_inputs(seed=50, lengths=[40, 33], H=2, slots=4, state_idx=[2, -1])
+    out = run_both(d, 2)
+    check(out, d)
+    assert torch.all(out["o"][40:].float() == 0)
+    # out-of-range slot: flagged, sequence skipped, pool untouched
+    d = inputs.prefill_inputs(seed=51, lengths=[40, 33], H=2, slots=4, state_idx=[1, 4])
+    out = run_both(d, 2, oracle=False)
+    assert out["err"] & kda.KDA_DEVERR_SLOT
+    assert torch.equal(out["pool"][[0, 2, 3]], out["pool_before"][[0, 2, 3]])
+    # malformed cu_seqlens: flagged, nothing written to the pool
+    d = inputs.prefill_inputs(seed=52, lengths=[40, 33], H=2, slots=4)
+    d["cu_seqlens"] = np.array([0, 80, 73], np.int32)  # ends at T but not non-decreasing
+    out = run_both(d, 2, oracle=False)
+    assert out["err"] & kda.KDA_DEVERR_SEQLENS
+    assert torch.equal(out["pool"], out["pool_before"])
+
+
+def test_chunked_prefill_across_calls_matches_one_call():
+    """Chunked prefill carries state between calls through the pool."""
+    d = inputs.prefill_inputs(seed=60, lengths=[150], H=2, slots=3)
+    og, gg = gates(d, H=2)
+    pool = dev(d["pool"])
+    idx = dev(d["state_idx"])
+    outs = []
+    for a, b in ((0, 90), (90, 150)):
+        x = {n: dev_bf16(d[n][a:b]) for n in ("q", "k", "v", "g", "beta")}
+        o = torch.empty((b - a, 2, K), dtype=torch.bfloat16, device="cuda")
+        kda.kda_prefill(kda.dims(2), gg, x["q"], x["k"], x["v"], x["g"], x["beta"], pool, idx,
+                        dev(np.array([0, b - a], np.int32)), 1, o)
+        outs.append(o)
+    torch.cuda.synchronize()
+    opool = d["pool"].astype(np.float64)
+    o_ref = ko.prefill(og, d["q"], d["k"], d["v"], d["g"], d["beta"], opool, d["state_idx"],
+                       d["cu_seqlens"])
+    assert_o_close(torch.cat(outs), o_ref)
+    s = int(d["state_idx"][0])
+    assert_s_close(pool[s], opool[s])
