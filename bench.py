@@ -158,6 +158,24 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(mhz)}
 
 
+def max_over_ranks(values, world, device="cpu"):
+    """Element-wise max of a list of floats over all ranks (identity at world 1)."""
+    if world <= 1:
+        return [float(v) for v in values]
+    import torch
+    import torch.distributed as dist
+
+    vec = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(vec, op=dist.ReduceOp.MAX)
+    return [float(x) for x in vec.tolist()]
+
+
+def replica_throughput(units_per_rank_step, steps, world, slowest_seconds):
+    """Whole-job throughput of N independent replicas: every rank's units over
+    the slowest rank's time (weak scaling)."""
+    return units_per_rank_step * steps * world / slowest_seconds
+
+
 def physical_gpu_index(local_rank):
     vis = os.environ.get("CUDA_VISIBLE_DEVICES")
     if vis:
@@ -287,10 +305,7 @@ def run_ours(args, rank, world, local_rank):
         "verify_tree": ph_ms["verify_tree"], "commit": ph_ms["commit"],
     }
     tot = {n: sum(v) for n, v in ph_ms.items()}
-    if world > 1:
-        vec = torch.tensor([tot[n] for n in phases], device=dev, dtype=torch.float64)
-        dist.all_reduce(vec, op=dist.ReduceOp.MAX)
-        tot = {n: float(vec[i]) for i, n in enumerate(phases)}
+    tot = dict(zip(phases, max_over_ranks([tot[n] for n in phases], world, dev)))
 
     # ---- e2e: prefill through the C ABI with host buffers ----
     host = {n: torch.from_numpy(np.ascontiguousarray(pf[n])).pin_memory()
@@ -314,11 +329,7 @@ def run_ours(args, rank, world, local_rank):
         if i >= 3:
             ev_e2e.append((e0, e1))
     torch.cuda.synchronize()
-    e2e_ms = sum(a.elapsed_time(b) for a, b in ev_e2e)
-    if world > 1:
-        x = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(x, op=dist.ReduceOp.MAX)
-        e2e_ms = float(x.item())
+    e2e_ms = max_over_ranks([sum(a.elapsed_time(b) for a, b in ev_e2e)], world, dev)[0]
 
     if rank != 0:
         if world > 1:
@@ -328,7 +339,7 @@ def run_ours(args, rank, world, local_rank):
     hbm, bf16_tf, sm_max, peak_kind = _peaks()
     steps = args.steps
     prefill_s = tot["prefill"] / 1e3
-    value = PREFILL_T * steps * world / prefill_s
+    value = replica_throughput(PREFILL_T, steps, world, prefill_s)
     mean_k = {n: statistics.mean(v) for n, v in k_ms.items()}
     # FP32 CUDA-core peak: 152 SMs x 128 FMA lanes x 2 flops x max SM clock
     alu_peak = 152 * 128 * 2 * sm_max * 1e6 / 1e12
@@ -377,7 +388,8 @@ def run_ours(args, rank, world, local_rank):
         "gpu_launches": steps * len(kernels),
         "phases": phase_out,
         "roofline": roofline,
-        "e2e": {"value": round(PREFILL_T * e2e_steps * world / (e2e_ms / 1e3), 1), "unit": "tokens/s",
+        "e2e": {"value": round(replica_throughput(PREFILL_T, e2e_steps, world, e2e_ms / 1e3), 1),
+                "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "clocks": clocks, "wall_s_timed": round(wall, 3), "source_hash": src,
     }

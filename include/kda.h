@@ -67,6 +67,9 @@ typedef enum {
 #define KDA_DEVERR_PARENT 2   /* tree parent outside [-1, i) */
 #define KDA_DEVERR_SEQLENS 4  /* cu_seqlens not 0 .. total_tokens, non-decreasing */
 #define KDA_DEVERR_ACCEPTED 8 /* accepted index >= T */
+#define KDA_DEVERR_TIMEOUT 16 /* a kernel's bounded wait on its own copies or
+                                 tensor-core work ran out; its unit was not
+                                 written back */
 
 typedef struct {
   int H;  /* q/k heads */

@@ -17,10 +17,16 @@
 //   W      = (I+A)^-1 Diag(beta) Ktil,  Ktil_t = k_t e^{Gam_t}
 //   Util   = (I+A)^-1 Diag(beta) V
 //   U      = Util - W S0
-//   O      = scale (Qtil S0 + P U),     Qtil_t = q_t e^{Gam_t}
+//   O      = scale (Qtil S0 + P U) = scale (Q' S0 + P Util),  Q' = Qtil - P W,
+//            Qtil_t = q_t e^{Gam_t}
 //   S_L    = Diag(e^{Gam_L}) S0 + Khat^T U,  Khat_i = k_i e^{Gam_L - Gam_i}
 // Rows past the end of a sequence are q = k = v = 0, beta = 0, g = 0, which
-// leave every quantity above unchanged.
+// leave every quantity above unchanged.  Writing O through Q' = Qtil - P W
+// moves the cancellation between Qtil S0 and P W S0 into the per-chunk FP32
+// transform, so the state-dependent products need no more than BF16 W and Q'
+// against a BF16 hi/lo split of S; Khat^T U uses hi/lo splits of both
+// operands (three BF16 products), which keeps the state within 1e-4 of its
+// RMS.
 //
 // Decay factors inside A and P are split at a reference token r, the LAST
 // token of each 16-token block of i: e^{Gam_t-Gam_i} = e^{Gam_t-Gam_r} e^{Gam_r-Gam_i}.
@@ -30,17 +36,27 @@
 // lower bound -5 is inside that).  A left factor that underflows can only
 // drop terms that are smaller still.
 //
-// This file holds two kernels, both plain FP32 on the CUDA cores:
-//   chunk_transform_kernel  one CTA per (chunk, head), all chunks in parallel:
-//                           fold, cumulative decay, A, P, (I+A)^-1 by column
-//                           forward substitution, W, Util, Qtil, Khat, gamma,
-//                           written to the workspace.
-//   state_pass_kernel       one CTA per (sequence, head, 16 value columns),
-//                           sequential over the sequence's chunks: gathers S0
-//                           from the pool, applies U, O and the state update,
-//                           writes o, optional chunk-start states and scatters
-//                           the final state back.
+// Two kernels:
+//   chunk_transform_kernel  one CTA per (chunk, head), all chunks in parallel,
+//                           FP32 on the CUDA cores: fold, cumulative decay, A,
+//                           P, (I+A)^-1 by column forward substitution, W,
+//                           Util, Q', P Util, Khat, gamma.  Writes one
+//                           workspace record per (chunk, head) already in the
+//                           tensor-core operand layout.
+//   state_pass_kernel       one CTA per (sequence, head, 32 value columns),
+//                           sequential over the sequence's chunks, on tcgen05:
+//                           per chunk one bulk copy of the record into shared
+//                           memory (double-buffered, mbarrier completion), then
+//                             D1 = [W; Q'] [S_hi | S_lo]      (TMEM, M=128, N=32)
+//                             U  = Util - D1[0:64],  O = scale (D1[64:128] + P Util)
+//                             D2 = Khat^T U  (hi/lo x hi/lo, three products)
+//                             S  = Diag(gamma) S + D2
+//                           with S kept in FP32 registers (one key channel per
+//                           thread) and re-split into BF16 hi/lo operands.
+#include <stdlib.h>
+
 #include "kda_host.h"
+#include "kda_tc.cuh"
 
 namespace kda {
 namespace {
@@ -48,15 +64,20 @@ namespace {
 constexpr int kChunk = 64;
 constexpr int kLd = 132;  // padded row stride (floats) of 64 x 128 tiles in shared memory
 constexpr int kLdT = 65;  // padded row stride of 64 x 64 tiles
+constexpr int kVs = 32;   // value columns per state-pass CTA
+constexpr int kSlices = kHeadDim / kVs;
 
-// Workspace record of one (chunk, head), in floats.
-constexpr int kOffW = 0;
-constexpr int kOffU = kOffW + kChunk * kHeadDim;
-constexpr int kOffQ = kOffU + kChunk * kHeadDim;
-constexpr int kOffKh = kOffQ + kChunk * kHeadDim;
-constexpr int kOffP = kOffKh + kChunk * kHeadDim;
-constexpr int kOffGam = kOffP + kChunk * kChunk;
-constexpr int kRec = kOffGam + kHeadDim;
+// Workspace record of one (chunk, head), bytes.  Tiles are BF16, K-major,
+// 128-byte swizzled (see kda_tc.cuh) so they can be bulk-copied straight into
+// shared memory; Util and P Util are FP32, V-slice-major [slice][64][kVs].
+constexpr uint32_t kRecA1 = 0;                                // [W; Q'] 128 x 128
+constexpr uint32_t kRecKTh = kRecA1 + 128 * 128 * 2;          // Khat^T hi, 128 x 64
+constexpr uint32_t kRecKTl = kRecKTh + 128 * 64 * 2;          // Khat^T lo
+constexpr uint32_t kRecU = kRecKTl + 128 * 64 * 2;            // Util
+constexpr uint32_t kRecOi = kRecU + kChunk * kHeadDim * 4;    // P Util
+constexpr uint32_t kRecGam = kRecOi + kChunk * kHeadDim * 4;  // exp(Gam_L) [128]
+constexpr uint32_t kRecBytes = kRecGam + kHeadDim * 4;
+constexpr uint32_t kSliceBytes = kChunk * kVs * 4;
 
 struct PrefillArgs {
   GateArgs gate;
@@ -70,7 +91,7 @@ struct PrefillArgs {
   int64_t total_tokens;
   kda_bf16* o;
   float* intermediate;
-  float* ws;
+  uint8_t* ws;
   int32_t* err_flag;
 };
 
@@ -120,15 +141,19 @@ __device__ __forceinline__ float dot4(float4 a, float4 b) {
 
 __device__ __forceinline__ float4& f4(float* p) { return *reinterpret_cast<float4*>(p); }
 
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  return (uint32_t)float_to_bf16_bits(lo) | ((uint32_t)float_to_bf16_bits(hi) << 16);
+}
+
 // ---------------------------------------------------------------------------
 // Per-chunk transform (all chunks of all sequences in parallel).
 
 __global__ void __launch_bounds__(256) chunk_transform_kernel(const PrefillArgs a) {
   extern __shared__ __align__(16) float sm[];
-  float* KQ = sm;                    // k-hat      [64][kLd]
-  float* QQ = KQ + kChunk * kLd;     // q-hat      [64][kLd]
-  float* GM = QQ + kChunk * kLd;     // Gam        [64][kLd]
-  float* L1 = GM + kChunk * kLd;     // Lk, later beta*Ktil, beta*V
+  float* KQ = sm;                    // k-hat, later W            [64][kLd]
+  float* QQ = KQ + kChunk * kLd;     // q-hat, later Qtil, Q'     [64][kLd]
+  float* GM = QQ + kChunk * kLd;     // Gam, later Util           [64][kLd]
+  float* L1 = GM + kChunk * kLd;     // Lk, later beta Ktil, beta V
   float* L2 = L1 + kChunk * kLd;     // Lq, later (I+A)^-1 [64][kLdT]
   float* R = L2 + kChunk * kLd;      // right factor [16][kLd]
   float* Am = R + 16 * kLd;          // A [64][kLdT]
@@ -161,14 +186,19 @@ __global__ void __launch_bounds__(256) chunk_transform_kernel(const PrefillArgs 
   const int64_t t0 = loc.t0;
   const GateArgs& ga = a.gate;
   const int H = a.H, HV = a.HV, K = kHeadDim;
+  uint8_t* rec = a.ws + ((size_t)cid * HV + h) * kRecBytes;
 
-  // 1. fold: one warp per token, 4 channels per lane.
+  // 1. fold and cumulative log-decay.  Warp w owns tokens [8w, 8w+8), lane l
+  //    owns channels [4l, 4l+4); each warp keeps a running sum of g over its
+  //    tokens in registers, then adds the totals of the warps before it.
+  float* tot = Am;  // [8][128] warp totals, reused before A is written
   {
     const int c = lane * 4;
     const float exp_alog = ga.A_log ? expf(ga.A_log[h]) : 0.f;
     const float4 bias = ga.dt_bias ? *reinterpret_cast<const float4*>(ga.dt_bias + h * K + c)
                                    : make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int t = warp; t < kChunk; t += 8) {
+    float4 run = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int t = warp * 8; t < warp * 8 + 8; ++t) {
       float4 q4 = make_float4(0.f, 0.f, 0.f, 0.f), k4 = q4, g4 = q4;
       if (t < len) {
         const int64_t tok = t0 + t;
@@ -189,24 +219,27 @@ __global__ void __launch_bounds__(256) chunk_transform_kernel(const PrefillArgs 
       } else if (lane == 0) {
         bt[t] = 0.f;
       }
+      run = make_float4(run.x + g4.x, run.y + g4.y, run.z + g4.z, run.w + g4.w);
       f4(QQ + t * kLd + c) = q4;
       f4(KQ + t * kLd + c) = k4;
-      f4(GM + t * kLd + c) = g4;
+      f4(GM + t * kLd + c) = run;
+    }
+    f4(tot + warp * K + c) = run;
+    __syncthreads();
+    float4 pre = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int w = 0; w < warp; ++w) {
+      const float4 x = f4(tot + w * K + c);
+      pre = make_float4(pre.x + x.x, pre.y + x.y, pre.z + x.z, pre.w + x.w);
+    }
+    for (int t = warp * 8; t < warp * 8 + 8; ++t) {
+      float4& gg = f4(GM + t * kLd + c);
+      gg = make_float4(gg.x + pre.x, gg.y + pre.y, gg.z + pre.z, gg.w + pre.w);
     }
   }
+  __syncthreads();
   for (int i = tid; i < kChunk * kLdT; i += blockDim.x) {
     Am[i] = 0.f;
     Pm[i] = 0.f;
-  }
-  __syncthreads();
-
-  // 2. inclusive cumulative log-decay per channel
-  if (tid < K) {
-    float run = 0.f;
-    for (int t = 0; t < kChunk; ++t) {
-      run += GM[t * kLd + tid];
-      GM[t * kLd + tid] = run;
-    }
   }
   __syncthreads();
 
@@ -232,14 +265,14 @@ __global__ void __launch_bounds__(256) chunk_transform_kernel(const PrefillArgs 
       const int t = b0 + idx / 16, i = b0 + idx % 16;
       if (i > t) continue;
       float sa = 0.f, sp = 0.f;
-      const float* lk = L1 + t * kLd;
-      const float* lq = L2 + t * kLd;
-      const float* rr = R + (i - b0) * kLd;
+      float* lk = L1 + t * kLd;
+      float* lq = L2 + t * kLd;
+      float* rr = R + (i - b0) * kLd;
 #pragma unroll 8
       for (int c = 0; c < K; c += 4) {
-        const float4 rv = f4(const_cast<float*>(rr) + c);
-        sa += dot4(f4(const_cast<float*>(lk) + c), rv);
-        sp += dot4(f4(const_cast<float*>(lq) + c), rv);
+        const float4 rv = f4(rr + c);
+        sa += dot4(f4(lk + c), rv);
+        sp += dot4(f4(lq + c), rv);
       }
       if (i < t) Am[t * kLdT + i] = bt[t] * sa;
       Pm[t * kLdT + i] = sp;
@@ -247,24 +280,73 @@ __global__ void __launch_bounds__(256) chunk_transform_kernel(const PrefillArgs 
     __syncthreads();
   }
 
-  // 4. (I + A)^-1 by forward substitution, one column per thread.
+  // 4. (I + A)^-1, blocked in 16 x 16: the diagonal blocks by forward
+  //    substitution (one column per thread), then the blocks below the
+  //    diagonal one sub-diagonal at a time:
+  //      T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj.
   float* Ti = L2;
+  float* X = R;  // [3][16][16] scratch
+  for (int i = tid; i < kChunk * kLdT; i += blockDim.x) Ti[i] = 0.f;
+  __syncthreads();
   if (tid < kChunk) {
-    const int j = tid;
-    for (int t = 0; t < kChunk; ++t) {
-      float x;
-      if (t < j) {
-        x = 0.f;
-      } else if (t == j) {
-        x = 1.f;
-      } else {
-        x = 0.f;
-        for (int i = j; i < t; ++i) x -= Am[t * kLdT + i] * Ti[i * kLdT + j];
-      }
-      Ti[t * kLdT + j] = x;
+    const int b0 = (tid >> 4) * 16, col = tid & 15;
+    float x[16];
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+      float acc = r == col ? 1.f : 0.f;
+#pragma unroll
+      for (int s2 = 0; s2 < r; ++s2) acc -= Am[(b0 + r) * kLdT + b0 + s2] * x[s2];
+      x[r] = acc;
+      Ti[(b0 + r) * kLdT + b0 + col] = acc;
     }
   }
-  // beta_i Ktil_i = beta_i k_i e^{Gam_i}
+  __syncthreads();
+  for (int d = 1; d < 4; ++d) {
+    const int npairs = 4 - d;
+    for (int idx = tid; idx < npairs * 256; idx += blockDim.x) {
+      const int pr = idx >> 8, r = (idx >> 4) & 15, cc = idx & 15;
+      const int bi = pr + d, bj = pr;
+      float acc = 0.f;
+      for (int bk = bj; bk < bi; ++bk)
+#pragma unroll
+        for (int m = 0; m < 16; ++m)
+          acc += Am[(bi * 16 + r) * kLdT + bk * 16 + m] * Ti[(bk * 16 + m) * kLdT + bj * 16 + cc];
+      X[pr * 256 + r * 16 + cc] = acc;
+    }
+    __syncthreads();
+    for (int idx = tid; idx < npairs * 256; idx += blockDim.x) {
+      const int pr = idx >> 8, r = (idx >> 4) & 15, cc = idx & 15;
+      const int bi = pr + d, bj = pr;
+      float acc = 0.f;
+#pragma unroll
+      for (int m = 0; m < 16; ++m)
+        acc -= Ti[(bi * 16 + r) * kLdT + bi * 16 + m] * X[pr * 256 + m * 16 + cc];
+      Ti[(bi * 16 + r) * kLdT + bj * 16 + cc] = acc;
+    }
+    __syncthreads();
+  }
+  // 5. gamma and Khat^T (hi/lo BF16, swizzled 128 x 64): thread -> (c, 8-token chunk)
+  if (tid < K) reinterpret_cast<float*>(rec + kRecGam)[tid] = expf(GM[(kChunk - 1) * kLd + tid]);
+  for (int idx = tid; idx < K * 8; idx += blockDim.x) {
+    const int c = idx >> 3, j = idx & 7;
+    const float gl = GM[(kChunk - 1) * kLd + c];
+    uint32_t hi[4], lo[4];
+#pragma unroll
+    for (int e = 0; e < 8; e += 2) {
+      uint16_t h0, l0, h1, l1;
+      const int t = j * 8 + e;
+      tc::split_bf16(KQ[t * kLd + c] * expf(gl - GM[t * kLd + c]), h0, l0);
+      tc::split_bf16(KQ[(t + 1) * kLd + c] * expf(gl - GM[(t + 1) * kLd + c]), h1, l1);
+      hi[e / 2] = (uint32_t)h0 | ((uint32_t)h1 << 16);
+      lo[e / 2] = (uint32_t)l0 | ((uint32_t)l1 << 16);
+    }
+    const uint32_t off = tc::sw128_offset(c, j * 8, K);
+    *reinterpret_cast<uint4*>(rec + kRecKTh + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+    *reinterpret_cast<uint4*>(rec + kRecKTl + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+  }
+  __syncthreads();
+
+  // 6. beta Ktil_i = beta_i k_i e^{Gam_i} -> L1 ; then W = Ti (beta Ktil) -> KQ
   for (int idx = tid; idx < kChunk * (K / 4); idx += blockDim.x) {
     const int i = idx / (K / 4), c = (idx % (K / 4)) * 4;
     const float4 kk = f4(KQ + i * kLd + c), gg = f4(GM + i * kLd + c);
@@ -273,88 +355,529 @@ __global__ void __launch_bounds__(256) chunk_transform_kernel(const PrefillArgs 
                                        b * kk.z * expf(gg.z), b * kk.w * expf(gg.w));
   }
   __syncthreads();
-
-  float* rec = a.ws + ((size_t)cid * HV + h) * kRec;
-  // 5. W = Ti (beta Ktil): thread owns column quad c4 = lane, rows warp + 8m.
-  auto tri_gemm_store = [&](float* dst) {
+  // lower-triangular product out[t] = sum_{i<=t} Ti[t][i] X[i]; thread -> column quad, rows warp+8m
+  auto tri_gemm = [&](const float* X, float* out) {
     const int c = lane * 4;
     for (int t = warp; t < kChunk; t += 8) {
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
       for (int i = 0; i <= t; ++i) {
         const float w = Ti[t * kLdT + i];
-        const float4 x = f4(L1 + i * kLd + c);
+        const float4 x = *reinterpret_cast<const float4*>(X + i * kLd + c);
         acc.x += w * x.x;
         acc.y += w * x.y;
         acc.z += w * x.z;
         acc.w += w * x.w;
       }
-      f4(dst + t * K + c) = acc;
+      f4(out + t * kLd + c) = acc;
     }
   };
-  tri_gemm_store(rec + kOffW);
+  tri_gemm(L1, KQ);  // W
   __syncthreads();
-  // 6. Util = Ti (beta V)
+  // 7. Qtil = q e^{Gam} in place; beta V -> L1
   for (int idx = tid; idx < kChunk * (K / 4); idx += blockDim.x) {
     const int i = idx / (K / 4), c = (idx % (K / 4)) * 4;
+    const float4 gg = f4(GM + i * kLd + c);
+    float4& qq = f4(QQ + i * kLd + c);
+    qq = make_float4(qq.x * expf(gg.x), qq.y * expf(gg.y), qq.z * expf(gg.z), qq.w * expf(gg.w));
     float4 vv = make_float4(0.f, 0.f, 0.f, 0.f);
     if (i < len) vv = load_bf16x4(a.v + ((t0 + i) * HV + h) * K + c);
     const float b = bt[i];
     f4(L1 + i * kLd + c) = make_float4(b * vv.x, b * vv.y, b * vv.z, b * vv.w);
   }
   __syncthreads();
-  tri_gemm_store(rec + kOffU);
-
-  // 7. Qtil, Khat, gamma, P
-  for (int idx = tid; idx < kChunk * (K / 4); idx += blockDim.x) {
-    const int t = idx / (K / 4), c = (idx % (K / 4)) * 4;
-    const float4 gg = f4(GM + t * kLd + c), gl = f4(GM + (kChunk - 1) * kLd + c);
-    const float4 qq = f4(QQ + t * kLd + c), kk = f4(KQ + t * kLd + c);
-    f4(rec + kOffQ + t * K + c) =
-        make_float4(qq.x * expf(gg.x), qq.y * expf(gg.y), qq.z * expf(gg.z), qq.w * expf(gg.w));
-    f4(rec + kOffKh + t * K + c) =
-        make_float4(kk.x * expf(gl.x - gg.x), kk.y * expf(gl.y - gg.y), kk.z * expf(gl.z - gg.z),
-                    kk.w * expf(gl.w - gg.w));
+  // 8. Util = Ti (beta V) -> GM
+  tri_gemm(L1, GM);
+  __syncthreads();
+  // 9. Q' = Qtil - P W (in place), P Util and Util -> workspace (FP32, V-slice-major)
+  {
+    const int c = lane * 4;
+    const int slice = c / kVs, cs = c % kVs;
+    float* ut_out = reinterpret_cast<float*>(rec + kRecU) + slice * (kChunk * kVs);
+    float* oi_out = reinterpret_cast<float*>(rec + kRecOi) + slice * (kChunk * kVs);
+    for (int t = warp; t < kChunk; t += 8) {
+      float4 pw = make_float4(0.f, 0.f, 0.f, 0.f), pu = pw;
+      for (int i = 0; i <= t; ++i) {
+        const float p = Pm[t * kLdT + i];
+        const float4 w = f4(KQ + i * kLd + c), u = f4(GM + i * kLd + c);
+        pw.x += p * w.x; pw.y += p * w.y; pw.z += p * w.z; pw.w += p * w.w;
+        pu.x += p * u.x; pu.y += p * u.y; pu.z += p * u.z; pu.w += p * u.w;
+      }
+      float4& qq = f4(QQ + t * kLd + c);
+      qq = make_float4(qq.x - pw.x, qq.y - pw.y, qq.z - pw.z, qq.w - pw.w);
+      *reinterpret_cast<float4*>(oi_out + t * kVs + cs) = pu;
+      *reinterpret_cast<float4*>(ut_out + t * kVs + cs) = f4(GM + t * kLd + c);
+    }
   }
-  for (int idx = tid; idx < kChunk * kChunk; idx += blockDim.x)
-    rec[kOffP + idx] = Pm[(idx / kChunk) * kLdT + idx % kChunk];
-  if (tid < K) rec[kOffGam + tid] = expf(GM[(kChunk - 1) * kLd + tid]);
+  __syncthreads();
+  // 10. [W; Q'] as BF16, swizzled 128 x 128: thread -> (row, 8-column chunk)
+  for (int idx = tid; idx < 128 * 16; idx += blockDim.x) {
+    const int row = idx >> 4, ch = idx & 15;
+    const float* src = (row < kChunk ? KQ + row * kLd : QQ + (row - kChunk) * kLd) + ch * 8;
+    const uint4 pk = make_uint4(pack_bf16x2(src[0], src[1]), pack_bf16x2(src[2], src[3]),
+                                pack_bf16x2(src[4], src[5]), pack_bf16x2(src[6], src[7]));
+    *reinterpret_cast<uint4*>(rec + kRecA1 + tc::sw128_offset(row, ch * 8, 128)) = pk;
+  }
 }
 
 constexpr size_t kTransformSmem =
     sizeof(float) * (5 * kChunk * kLd + 16 * kLd + 2 * kChunk * kLdT + kChunk);
 
 // ---------------------------------------------------------------------------
-// Sequential state pass over the chunks of one sequence, 16 value columns.
+// Per-chunk transform on tcgen05 (all chunks of all sequences in parallel).
+//
+//   M1 (x4 blocks of i):  [Lk; Lq] R^T  -> A (rows 0-63) and P (rows 64-127),
+//        Lk_t = k_t e^{Gam_t - Gam_r}, Lq_t = q_t e^{Gam_t - Gam_r} (t >= block start),
+//        R_i  = k_i e^{Gam_r - Gam_i}, r = last token of the block.  M=128 N=16 K=128.
+//   (I+A)^-1 and P (I+A)^-1 on the CUDA cores (64 x 64, blocked).
+//   M2: [Ti; P Ti] [beta Ktil | beta V]^T -> W | Util (rows 0-63), P W | P Util
+//        (rows 64-127).  M=128 N=256 K=64.
+// Both products use BF16 hi/lo splits of both operands (three MMAs each).
 
-constexpr int kVs = 16;      // value columns per CTA
-constexpr int kLdS = kVs + 1;
+constexpr uint32_t kTxL = 0;                         // L hi, lo: 128 x 128 each
+constexpr uint32_t kTxR = kTxL + 2 * 128 * 128 * 2;  // R hi, lo: 16 x 128 each
+constexpr uint32_t kTxB2 = 0;                        // B2 hi, lo: 256 x 64 each (reuses L)
+constexpr uint32_t kTxA2 = kTxR + 2 * 16 * 128 * 2;  // A2 hi, lo: 128 x 64 each
+constexpr uint32_t kTxQ = kTxA2 + 2 * 128 * 64 * 2;  // raw q BF16 [64][128]
+constexpr uint32_t kTxK = kTxQ + kChunk * kHeadDim * 2;
+constexpr uint32_t kTxG = kTxK + kChunk * kHeadDim * 2;  // Gam FP32 [64][kLd]
+constexpr uint32_t kTxAf = kTxG + kChunk * kLd * 4;      // A FP32 [64][kLdT]
+constexpr uint32_t kTxPf = kTxAf + kChunk * kLdT * 4;    // P FP32
+constexpr uint32_t kTxTf = kTxPf + kChunk * kLdT * 4;    // (I+A)^-1 FP32
+constexpr uint32_t kTxMisc = kTxTf + kChunk * kLdT * 4;  // rq, rk, beta [64] each + scratch [768]
+constexpr uint32_t kTxEnd = kTxMisc + (3 * kChunk + 768) * 4;
+constexpr uint32_t kTransformTcSmem = kTxEnd + 1024;
+constexpr uint32_t kTxTmemCols = 256;
+static_assert(2 * 256 * 64 * 2 <= kTxA2, "B2 fits in the L/R region");
+static_assert(kTxAf + 8 * kHeadDim * 4 <= kTxTf + kChunk * kLdT * 4, "warp totals fit");
 
-__global__ void __launch_bounds__(256) state_pass_kernel(const PrefillArgs a) {
-  extern __shared__ __align__(16) float sm[];
-  float* Wm = sm;                   // [64][kLd]
-  float* Qm = Wm + kChunk * kLd;    // [64][kLd]
-  float* Km = Qm + kChunk * kLd;    // [64][kLd]
-  float* Pm = Km + kChunk * kLd;    // [64][kLdT]
-  float* Sm = Pm + kChunk * kLdT;   // [128][kLdS]
-  float* Um = Sm + kHeadDim * kLdS; // [64][kLdS]
-  float* Ut = Um + kChunk * kLdS;   // [64][kLdS]
-  float* gm = Ut + kChunk * kLdS;   // [128]
+__device__ __forceinline__ void st_split_pair(uint8_t* hi, uint8_t* lo, uint32_t off, const float* x) {
+  // eight consecutive values -> one 16-byte chunk in each of hi and lo
+  uint32_t h[4], l[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    uint16_t h0, l0, h1, l1;
+    tc::split_bf16(x[2 * e], h0, l0);
+    tc::split_bf16(x[2 * e + 1], h1, l1);
+    h[e] = (uint32_t)h0 | ((uint32_t)h1 << 16);
+    l[e] = (uint32_t)l0 | ((uint32_t)l1 << 16);
+  }
+  *reinterpret_cast<uint4*>(hi + off) = make_uint4(h[0], h[1], h[2], h[3]);
+  *reinterpret_cast<uint4*>(lo + off) = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
+__device__ __forceinline__ float bf16_at(const uint8_t* tile, int t, int c) {
+  return bf16_bits_to_float(reinterpret_cast<const uint16_t*>(tile)[t * kHeadDim + c]);
+}
+
+__global__ void __launch_bounds__(256, 1) chunk_transform_tc_kernel(const PrefillArgs a) {
+  extern __shared__ uint8_t smraw[];
+  __shared__ uint64_t mma_bar;
+  __shared__ uint32_t tmem_base;
+  __shared__ ChunkLoc loc;
+  __shared__ int skip, s_abort;
+
+  uint8_t* sb = smraw + ((1024u - (tc::smem_u32(smraw) & 1023u)) & 1023u);
+  uint8_t* Lh = sb + kTxL;
+  uint8_t* Ll = Lh + 128 * 128 * 2;
+  uint8_t* Rh = sb + kTxR;
+  uint8_t* Rl = Rh + 16 * 128 * 2;
+  uint8_t* Bh = sb + kTxB2;
+  uint8_t* Bl = Bh + 256 * 64 * 2;
+  uint8_t* A2h = sb + kTxA2;
+  uint8_t* A2l = A2h + 128 * 64 * 2;
+  uint8_t* Qs = sb + kTxQ;
+  uint8_t* Ks = sb + kTxK;
+  float* GM = reinterpret_cast<float*>(sb + kTxG);
+  float* Af = reinterpret_cast<float*>(sb + kTxAf);
+  float* Pf = reinterpret_cast<float*>(sb + kTxPf);
+  float* Tf = reinterpret_cast<float*>(sb + kTxTf);
+  float* rq = reinterpret_cast<float*>(sb + kTxMisc);
+  float* rk = rq + kChunk;
+  float* bt = rk + kChunk;
+  float* X = bt + kChunk;  // [3][16][16]
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int h = blockIdx.y;
+  const int64_t cid = blockIdx.x;
+  if (tid == 0) {
+    skip = 0;
+    s_abort = 0;
+    if (!seqlens_valid(a)) {
+      skip = 1;
+      if (cid == 0 && h == 0) set_error(a.err_flag, KDA_DEVERR_SEQLENS);
+    } else {
+      loc = locate_chunk(a, cid);
+      if (loc.n < 0) {
+        skip = 1;
+      } else {
+        const int slot = a.state_idx[loc.n];
+        if (slot < 0 || slot >= a.pool_slots) skip = 1;  // padding / rejected sequence
+      }
+    }
+    tc::mbar_init(&mma_bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  if (skip) return;
+  if (warp == 0) tc::tmem_alloc(&tmem_base, kTxTmemCols);
+  const int len = loc.len;
+  const int64_t t0 = loc.t0;
+  const GateArgs& ga = a.gate;
+  const int H = a.H, HV = a.HV, K = kHeadDim;
+  uint8_t* rec = a.ws + ((size_t)cid * HV + h) * kRecBytes;
+
+  // 1. fold: raw q, k kept as BF16 with their norms; Gam by warp-blocked prefix.
+  {
+    float* tot = Af;  // [8][128] warp totals
+    const int c = lane * 4;
+    const float exp_alog = ga.A_log ? expf(ga.A_log[h]) : 0.f;
+    const float4 bias = ga.dt_bias ? *reinterpret_cast<const float4*>(ga.dt_bias + h * K + c)
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 run = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int t = warp * 8; t < warp * 8 + 8; ++t) {
+      uint2 qraw = make_uint2(0u, 0u), kraw = qraw;
+      float4 g4 = make_float4(0.f, 0.f, 0.f, 0.f);
+      float nq = 0.f, nk = 0.f, b = 0.f;
+      if (t < len) {
+        const int64_t tok = t0 + t;
+        qraw = __ldg(reinterpret_cast<const uint2*>(a.q + (tok * H + h) * K + c));
+        kraw = __ldg(reinterpret_cast<const uint2*>(a.k + (tok * H + h) * K + c));
+        const float4 q4 = load_bf16x4(a.q + (tok * H + h) * K + c);
+        const float4 k4 = load_bf16x4(a.k + (tok * H + h) * K + c);
+        const float4 a4 = load_bf16x4(a.g + (tok * HV + h) * K + c);
+        nq = ga.use_qk_l2norm ? rsqrtf(warp_sum(dot4(q4, q4)) + kNormEps) : 1.f;
+        nk = ga.use_qk_l2norm ? rsqrtf(warp_sum(dot4(k4, k4)) + kNormEps) : 1.f;
+        g4 = make_float4(gate_log_decay(ga, a4.x, exp_alog, bias.x),
+                         gate_log_decay(ga, a4.y, exp_alog, bias.y),
+                         gate_log_decay(ga, a4.z, exp_alog, bias.z),
+                         gate_log_decay(ga, a4.w, exp_alog, bias.w));
+        b = fold_beta(ga, bf16_bits_to_float(a.beta[tok * HV + h]));
+      }
+      if (lane == 0) {
+        rq[t] = nq;
+        rk[t] = nk;
+        bt[t] = b;
+      }
+      *reinterpret_cast<uint2*>(Qs + (t * K + c) * 2) = qraw;
+      *reinterpret_cast<uint2*>(Ks + (t * K + c) * 2) = kraw;
+      run = make_float4(run.x + g4.x, run.y + g4.y, run.z + g4.z, run.w + g4.w);
+      f4(GM + t * kLd + c) = run;
+    }
+    f4(tot + warp * K + c) = run;
+    __syncthreads();
+    float4 pre = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int w = 0; w < warp; ++w) {
+      const float4 x = f4(tot + w * K + c);
+      pre = make_float4(pre.x + x.x, pre.y + x.y, pre.z + x.z, pre.w + x.w);
+    }
+    for (int t = warp * 8; t < warp * 8 + 8; ++t) {
+      float4& gg = f4(GM + t * kLd + c);
+      gg = make_float4(gg.x + pre.x, gg.y + pre.y, gg.z + pre.z, gg.w + pre.w);
+    }
+  }
+  __syncthreads();
+
+  // 2. gamma and Khat^T (hi/lo, swizzled 128 x 64) straight to the workspace
+  if (tid < K) reinterpret_cast<float*>(rec + kRecGam)[tid] = expf(GM[(kChunk - 1) * kLd + tid]);
+  for (int idx = tid; idx < K * 8; idx += blockDim.x) {
+    const int c = idx & (K - 1), j = idx >> 7;
+    const float gl = GM[(kChunk - 1) * kLd + c];
+    float x[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const int t = j * 8 + e;
+      x[e] = bf16_at(Ks, t, c) * rk[t] * expf(gl - GM[t * kLd + c]);
+    }
+    st_split_pair(rec + kRecKTh, rec + kRecKTl, tc::sw128_offset(c, j * 8, K), x);
+  }
+
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = tmem_base;
+  const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
+  uint32_t phase = 0;
+
+  // 3. M1: A and P, one 16-token block of i per round.
+  for (int ib = 0; ib < kChunk / 16; ++ib) {
+    const int b0 = ib * 16, r = b0 + 15;
+    // L rows: 0-63 k side, 64-127 q side; thread -> (row, 8-column chunk)
+    for (int idx = tid; idx < 128 * 16; idx += blockDim.x) {
+      const int row = idx >> 4, ch = idx & 15;
+      const int t = row & 63;
+      const uint8_t* src = row < kChunk ? Ks : Qs;
+      const float nrm = row < kChunk ? rk[t] : rq[t];
+      float x[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int c = ch * 8 + e;
+        x[e] = t >= b0 ? bf16_at(src, t, c) * nrm * expf(GM[t * kLd + c] - GM[r * kLd + c]) : 0.f;
+      }
+      st_split_pair(Lh, Ll, tc::sw128_offset(row, ch * 8, 128), x);
+    }
+    for (int idx = tid; idx < 16 * 16; idx += blockDim.x) {
+      const int row = idx >> 4, ch = idx & 15;
+      const int i = b0 + row;
+      float x[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int c = ch * 8 + e;
+        x[e] = bf16_at(Ks, i, c) * rk[i] * expf(GM[r * kLd + c] - GM[i * kLd + c]);
+      }
+      st_split_pair(Rh, Rl, tc::sw128_offset(row, ch * 8, 16), x);
+    }
+    tc::fence_async_smem();
+    tc::tc_fence_before();
+    __syncthreads();
+    if (tid == 0 && !s_abort) {
+      tc::tc_fence_after();
+      constexpr uint32_t idesc = tc::idesc_bf16_f32(128, 16);
+      const uint32_t ah[3] = {tc::smem_u32(Lh), tc::smem_u32(Lh), tc::smem_u32(Ll)};
+      const uint32_t bh[3] = {tc::smem_u32(Rh), tc::smem_u32(Rl), tc::smem_u32(Rh)};
+#pragma unroll
+      for (int p = 0; p < 3; ++p)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t koff = (k & 3) * 32;
+          tc::mma_bf16(tmem + ib * 16, tc::sw128_desc(ah[p] + (k >> 2) * (128 * 128) + koff),
+                       tc::sw128_desc(bh[p] + (k >> 2) * (16 * 128) + koff), idesc, p > 0 || k > 0);
+        }
+      tc::mma_commit(&mma_bar);
+    }
+    if (!tc::mbar_wait(&mma_bar, phase)) s_abort = 1;
+    phase ^= 1;
+    tc::tc_fence_after();
+  }
+
+  // 4. A (beta-scaled, strictly lower) and P (lower) to FP32; warps 0-3 take
+  //    columns 0-31, warps 4-7 columns 32-63.
+  {
+    const int row = (warp & 3) * 32 + lane;
+    const int c0 = (warp >> 2) * 32;
+    float d[32];
+    tc::tmem_ld16(tmem + lane_addr + c0, *reinterpret_cast<float(*)[16]>(d));
+    tc::tmem_ld16(tmem + lane_addr + c0 + 16, *reinterpret_cast<float(*)[16]>(d + 16));
+    if (row < kChunk) {
+      const int t = row;
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        const int i = c0 + e;
+        Af[t * kLdT + i] = i < t ? bt[t] * d[e] : 0.f;
+      }
+    } else {
+      const int t = row - kChunk;
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        const int i = c0 + e;
+        Pf[t * kLdT + i] = i <= t ? d[e] : 0.f;
+      }
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+
+  // 5. (I + A)^-1, blocked in 16 x 16 (see the CUDA-core transform above).
+  for (int i = tid; i < kChunk * kLdT; i += blockDim.x) Tf[i] = 0.f;
+  __syncthreads();
+  if (tid < kChunk) {
+    const int b0 = (tid >> 4) * 16, col = tid & 15;
+    float x[16];
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+      float acc = r == col ? 1.f : 0.f;
+#pragma unroll
+      for (int s2 = 0; s2 < r; ++s2) acc -= Af[(b0 + r) * kLdT + b0 + s2] * x[s2];
+      x[r] = acc;
+      Tf[(b0 + r) * kLdT + b0 + col] = acc;
+    }
+  }
+  __syncthreads();
+  for (int d = 1; d < 4; ++d) {
+    const int npairs = 4 - d;
+    for (int idx = tid; idx < npairs * 256; idx += blockDim.x) {
+      const int pr = idx >> 8, r = (idx >> 4) & 15, cc = idx & 15;
+      const int bi = pr + d, bj = pr;
+      float acc = 0.f;
+      for (int bk = bj; bk < bi; ++bk)
+#pragma unroll
+        for (int m = 0; m < 16; ++m)
+          acc += Af[(bi * 16 + r) * kLdT + bk * 16 + m] * Tf[(bk * 16 + m) * kLdT + bj * 16 + cc];
+      X[pr * 256 + r * 16 + cc] = acc;
+    }
+    __syncthreads();
+    for (int idx = tid; idx < npairs * 256; idx += blockDim.x) {
+      const int pr = idx >> 8, r = (idx >> 4) & 15, cc = idx & 15;
+      const int bi = pr + d, bj = pr;
+      float acc = 0.f;
+#pragma unroll
+      for (int m = 0; m < 16; ++m)
+        acc -= Tf[(bi * 16 + r) * kLdT + bi * 16 + m] * X[pr * 256 + m * 16 + cc];
+      Tf[(bi * 16 + r) * kLdT + bj * 16 + cc] = acc;
+    }
+    __syncthreads();
+  }
+
+  // 6. A2 = [Ti; P Ti] (hi/lo, swizzled 128 x 64); thread -> (row, 8-column chunk)
+  for (int idx = tid; idx < 128 * 8; idx += blockDim.x) {
+    const int row = idx >> 3, ch = idx & 7;
+    float x[8];
+    if (row < kChunk) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) x[e] = Tf[row * kLdT + ch * 8 + e];
+    } else {
+      const int t = row - kChunk;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) x[e] = 0.f;
+      for (int i = ch * 8; i <= t; ++i) {
+        const float p = Pf[t * kLdT + i];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] += p * Tf[i * kLdT + ch * 8 + e];
+      }
+    }
+    st_split_pair(A2h, A2l, tc::sw128_offset(row, ch * 8, 128), x);
+  }
+  // 7. B2 = [(beta Ktil)^T ; (beta V)^T] (hi/lo, swizzled 256 x 64): row -> channel
+  for (int idx = tid; idx < 256 * 8; idx += blockDim.x) {
+    const int row = idx & 255, ch = idx >> 8;
+    float x[8];
+    if (row < K) {
+      const int c = row;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int i = ch * 8 + e;
+        x[e] = bt[i] * bf16_at(Ks, i, c) * rk[i] * expf(GM[i * kLd + c]);
+      }
+    } else {
+      const int c = row - K;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int i = ch * 8 + e;
+        x[e] = i < len ? bt[i] * bf16_bits_to_float(a.v[((t0 + i) * HV + h) * K + c]) : 0.f;
+      }
+    }
+    st_split_pair(Bh, Bl, tc::sw128_offset(row, ch * 8, 256), x);
+  }
+  tc::fence_async_smem();
+  tc::tc_fence_before();
+  __syncthreads();
+
+  // 8. M2: D = A2 B2^T, M=128 N=256 K=64
+  if (tid == 0 && !s_abort) {
+    tc::tc_fence_after();
+    constexpr uint32_t idesc = tc::idesc_bf16_f32(128, 256);
+    const uint32_t ah[3] = {tc::smem_u32(A2h), tc::smem_u32(A2h), tc::smem_u32(A2l)};
+    const uint32_t bh[3] = {tc::smem_u32(Bh), tc::smem_u32(Bl), tc::smem_u32(Bh)};
+#pragma unroll
+    for (int p = 0; p < 3; ++p)
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        tc::mma_bf16(tmem, tc::sw128_desc(ah[p] + k * 32), tc::sw128_desc(bh[p] + k * 32), idesc,
+                     p > 0 || k > 0);
+    tc::mma_commit(&mma_bar);
+  }
+  if (!tc::mbar_wait(&mma_bar, phase)) s_abort = 1;
+  phase ^= 1;
+  tc::tc_fence_after();
+
+  // 9. epilogue: warps 0-3 columns 0-127 (W | P W), warps 4-7 columns 128-255 (Util | P Util)
+  {
+    const int row = (warp & 3) * 32 + lane;
+    const int t = row & 63;
+    const bool upper = row < kChunk;  // rows 0-63: W, Util; rows 64-127: P W, P Util
+    const bool right = warp >= 4;
+    for (int cb = 0; cb < 8; ++cb) {
+      float d[16];
+      const int c0 = cb * 16;  // column within the half
+      tc::tmem_ld16(tmem + lane_addr + (right ? 128 : 0) + c0, d);
+      if (!right) {
+        float x[16];
+        if (upper) {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) x[e] = d[e];
+        } else {  // Q' = Qtil - P W
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int c = c0 + e;
+            x[e] = bf16_at(Qs, t, c) * rq[t] * expf(GM[t * kLd + c]) - d[e];
+          }
+        }
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          const float* xs = x + half * 8;
+          const uint4 pk = make_uint4(pack_bf16x2(xs[0], xs[1]), pack_bf16x2(xs[2], xs[3]),
+                                      pack_bf16x2(xs[4], xs[5]), pack_bf16x2(xs[6], xs[7]));
+          *reinterpret_cast<uint4*>(rec + kRecA1 + tc::sw128_offset(row, c0 + half * 8, 128)) = pk;
+        }
+      } else {
+        const int slice = c0 / kVs, cs = c0 % kVs;
+        float* dst = reinterpret_cast<float*>(rec + (upper ? kRecU : kRecOi)) +
+                     slice * (kChunk * kVs) + t * kVs + cs;
+#pragma unroll
+        for (int e = 0; e < 16; e += 4) f4(dst + e) = make_float4(d[e], d[e + 1], d[e + 2], d[e + 3]);
+      }
+    }
+  }
+  if (s_abort && tid == 0) set_error(a.err_flag, KDA_DEVERR_TIMEOUT);
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tc::tmem_dealloc(tmem, kTxTmemCols);
+}
+
+// ---------------------------------------------------------------------------
+// Sequential state pass on tcgen05.
+
+// Shared-memory layout of the state pass (bytes from a 1024-aligned base).
+constexpr uint32_t kStA1 = 0;
+constexpr uint32_t kStKTh = kStA1 + 128 * 128 * 2;
+constexpr uint32_t kStKTl = kStKTh + 128 * 64 * 2;
+constexpr uint32_t kStU = kStKTl + 128 * 64 * 2;
+constexpr uint32_t kStOi = kStU + kSliceBytes;
+constexpr uint32_t kStGam = kStOi + kSliceBytes;
+constexpr uint32_t kStageBytes = ((kStGam + kHeadDim * 4 + 1023) / 1024) * 1024;
+constexpr uint32_t kSmS = 2 * kStageBytes;       // S^T hi, lo: 32 x 128 each
+constexpr uint32_t kSmSBytes = kVs * kHeadDim * 2;
+constexpr uint32_t kSmU = kSmS + 2 * kSmSBytes;  // U^T hi, lo: 32 x 64 each
+constexpr uint32_t kSmUBytes = kVs * kChunk * 2;
+constexpr uint32_t kPassSmem = kSmU + 2 * kSmUBytes + 1024;  // + alignment slack
+constexpr uint32_t kStageTx = 128 * 128 * 2 + 2 * 128 * 64 * 2 + 2 * kSliceBytes + kHeadDim * 4;
+constexpr uint32_t kTmemCols = 64;  // D1: cols 0-31, D2: cols 32-63
+static_assert(kStKTl == kStKTh + 128 * 64 * 2 && kRecKTl == kRecKTh + 128 * 64 * 2,
+              "Khat^T hi and lo are copied as one block");
+
+__device__ __forceinline__ void issue_stage_loads(uint8_t* stage, const uint8_t* rec, int slice,
+                                                  uint64_t* bar) {
+  tc::mbar_expect_tx(bar, kStageTx);
+  tc::bulk_g2s(stage + kStA1, rec + kRecA1, 128 * 128 * 2, bar);
+  tc::bulk_g2s(stage + kStKTh, rec + kRecKTh, 2 * 128 * 64 * 2, bar);
+  tc::bulk_g2s(stage + kStU, rec + kRecU + slice * kSliceBytes, kSliceBytes, bar);
+  tc::bulk_g2s(stage + kStOi, rec + kRecOi + slice * kSliceBytes, kSliceBytes, bar);
+  tc::bulk_g2s(stage + kStGam, rec + kRecGam, kHeadDim * 4, bar);
+}
+
+__global__ void __launch_bounds__(128, 1) state_pass_kernel(const PrefillArgs a) {
+  extern __shared__ uint8_t smraw[];
+  __shared__ uint64_t full_bar[2];
+  __shared__ uint64_t mma_bar;
+  __shared__ uint32_t tmem_base;
   __shared__ int64_t s_t0, s_t1, s_cbase;
-  __shared__ int s_state;
+  __shared__ int s_state, s_abort;
 
-  const int tid = threadIdx.x;
-  const int n = blockIdx.z, h = blockIdx.y, v0 = blockIdx.x * kVs;
+  uint8_t* smb = smraw + ((1024u - (tc::smem_u32(smraw) & 1023u)) & 1023u);
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int n = blockIdx.z, h = blockIdx.y, slice = blockIdx.x, v0 = slice * kVs;
   const int HV = a.HV, K = kHeadDim, V = kHeadDim;
+
   if (tid == 0) {
     s_state = 0;
+    s_abort = 0;
     if (!seqlens_valid(a)) {
       s_state = 2;
-      if (blockIdx.x == 0 && h == 0 && n == 0) set_error(a.err_flag, KDA_DEVERR_SEQLENS);
+      if (slice == 0 && h == 0 && n == 0) set_error(a.err_flag, KDA_DEVERR_SEQLENS);
     } else {
       const int slot = a.state_idx[n];
       if (slot < -1 || slot >= a.pool_slots) {
         s_state = 2;
-        if (blockIdx.x == 0 && h == 0) set_error(a.err_flag, KDA_DEVERR_SLOT);
+        if (slice == 0 && h == 0) set_error(a.err_flag, KDA_DEVERR_SLOT);
       } else if (slot == -1) {
         s_state = 1;
       }
@@ -365,6 +888,10 @@ __global__ void __launch_bounds__(256) state_pass_kernel(const PrefillArgs a) {
       s_t0 = seq_begin(a, n);
       s_t1 = seq_begin(a, n + 1);
     }
+    tc::mbar_init(&full_bar[0], 1);
+    tc::mbar_init(&full_bar[1], 1);
+    tc::mbar_init(&mma_bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
   if (s_state == 2) return;
@@ -374,101 +901,174 @@ __global__ void __launch_bounds__(256) state_pass_kernel(const PrefillArgs a) {
       a.o[((t0 + idx / kVs) * HV + h) * V + v0 + idx % kVs] = 0;
     return;
   }
+  const int nch = (int)((t1 - t0 + kChunk - 1) / kChunk);
   const int slot = a.state_idx[n];
   float* st = a.pool + ((size_t)slot * HV + h) * V * K;
-  for (int idx = tid; idx < kVs * K; idx += blockDim.x) {
-    const int j = idx / K, c = idx % K;
-    Sm[c * kLdS + j] = st[(size_t)(v0 + j) * K + c];
-  }
-  __syncthreads();
+  const uint8_t* ws_head = a.ws + ((size_t)s_cbase * HV + h) * kRecBytes;
+  const size_t rec_stride = (size_t)HV * kRecBytes;
 
-  const int nch = (int)((t1 - t0 + kChunk - 1) / kChunk);
+  int issued = 0;    // chunks whose loads have been issued (thread 0)
+  int consumed = 0;  // chunks whose loads have landed
+  if (tid == 0) {
+    for (; issued < 2 && issued < nch; ++issued)
+      issue_stage_loads(smb + issued * kStageBytes, ws_head + issued * rec_stride, slice,
+                        &full_bar[issued]);
+  }
+  if (warp == 0) tc::tmem_alloc(&tmem_base, kTmemCols);
+
+  // state: thread c owns S[c][v0 .. v0+32) in FP32 registers
+  const int c = tid;
+  float S[kVs];
+#pragma unroll
+  for (int j = 0; j < kVs; ++j) S[j] = st[(size_t)(v0 + j) * K + c];
+  uint8_t* Sh = smb + kSmS;
+  uint8_t* Sl = Sh + kSmSBytes;
+  uint8_t* Uh = smb + kSmU;
+  uint8_t* Ul = Uh + kSmUBytes;
+  auto write_state_operand = [&]() {
+#pragma unroll
+    for (int j = 0; j < kVs; ++j) {
+      uint16_t hi, lo;
+      tc::split_bf16(S[j], hi, lo);
+      const uint32_t off = tc::sw128_offset(j, c, kVs);
+      *reinterpret_cast<uint16_t*>(Sh + off) = hi;
+      *reinterpret_cast<uint16_t*>(Sl + off) = lo;
+    }
+  };
+  write_state_operand();
+  tc::fence_async_smem();
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = tmem_base;
+  const uint32_t d1 = tmem, d2 = tmem + kVs;
+  const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
+  constexpr uint32_t idesc = tc::idesc_bf16_f32(128, kVs);
+  const float scale = a.gate.scale;
+  uint32_t mma_phase = 0;
+
   for (int ci = 0; ci < nch; ++ci) {
+    const int sidx = ci & 1;
+    uint8_t* stage = smb + sidx * kStageBytes;
     const int64_t cid = s_cbase + ci;
-    const int64_t tc = t0 + (int64_t)ci * kChunk;
-    const int len = (int)(t1 - tc < kChunk ? t1 - tc : kChunk);
-    const float* rec = a.ws + ((size_t)cid * HV + h) * kRec;
+    const int64_t tc0 = t0 + (int64_t)ci * kChunk;
+    const int len = (int)(t1 - tc0 < kChunk ? t1 - tc0 : kChunk);
     if (a.intermediate) {
       float* dst = a.intermediate + ((size_t)cid * HV + h) * V * K;
-      for (int idx = tid; idx < kVs * K; idx += blockDim.x) {
-        const int j = idx / K, c = idx % K;
-        dst[(size_t)(v0 + j) * K + c] = Sm[c * kLdS + j];
+#pragma unroll
+      for (int j = 0; j < kVs; ++j) dst[(size_t)(v0 + j) * K + c] = S[j];
+    }
+    if (tc::mbar_wait(&full_bar[sidx], (ci >> 1) & 1))
+      consumed = ci + 1;
+    else
+      s_abort = 1;
+    // D1 = [W; Q'] (S_hi + S_lo): two passes of eight K=16 steps
+    if (tid == 0 && !s_abort) {
+      tc::tc_fence_after();
+      const uint32_t a1 = tc::smem_u32(stage + kStA1);
+#pragma unroll
+      for (int p = 0; p < 2; ++p) {
+        const uint32_t bbase = tc::smem_u32(p == 0 ? Sh : Sl);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t koff = (k & 3) * 32;
+          const uint64_t ad = tc::sw128_desc(a1 + (k >> 2) * (128 * 128) + koff);
+          const uint64_t bd = tc::sw128_desc(bbase + (k >> 2) * (kVs * 128) + koff);
+          tc::mma_bf16(d1, ad, bd, idesc, p > 0 || k > 0);
+        }
       }
+      tc::mma_commit(&mma_bar);
     }
-    for (int idx = tid; idx < kChunk * (K / 4); idx += blockDim.x) {
-      const int t = idx / (K / 4), c = (idx % (K / 4)) * 4;
-      f4(Wm + t * kLd + c) = *reinterpret_cast<const float4*>(rec + kOffW + t * K + c);
-      f4(Qm + t * kLd + c) = *reinterpret_cast<const float4*>(rec + kOffQ + t * K + c);
-      f4(Km + t * kLd + c) = *reinterpret_cast<const float4*>(rec + kOffKh + t * K + c);
-    }
-    for (int idx = tid; idx < kChunk * kChunk; idx += blockDim.x)
-      Pm[(idx / kChunk) * kLdT + idx % kChunk] = rec[kOffP + idx];
-    for (int idx = tid; idx < kChunk * kVs; idx += blockDim.x)
-      Ut[(idx / kVs) * kLdS + idx % kVs] = rec[kOffU + (idx / kVs) * K + v0 + idx % kVs];
-    if (tid < K) gm[tid] = rec[kOffGam + tid];
-    __syncthreads();
-
-    // U = Util - W S : thread -> (t, 4 columns)
+    if (!tc::mbar_wait(&mma_bar, mma_phase)) s_abort = 1;
+    mma_phase ^= 1;
+    tc::tc_fence_after();
     {
-      const int t = tid >> 2, j0 = (tid & 3) * 4;
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
-      for (int c = 0; c < K; ++c) {
-        const float w = Wm[t * kLd + c];
+      float d[kVs];
+      tc::tmem_ld16(d1 + lane_addr, *reinterpret_cast<float(*)[16]>(d));
+      tc::tmem_ld16(d1 + lane_addr + 16, *reinterpret_cast<float(*)[16]>(d + 16));
+      if (warp < 2) {  // rows 0..63: U = Util - W S  ->  U^T hi/lo operand
+        const int t = tid;
+        const float* ut = reinterpret_cast<const float*>(stage + kStU) + t * kVs;
 #pragma unroll
-        for (int jj = 0; jj < 4; ++jj) acc[jj] += w * Sm[c * kLdS + j0 + jj];
+        for (int j = 0; j < kVs; ++j) {
+          uint16_t hi, lo;
+          tc::split_bf16(ut[j] - d[j], hi, lo);
+          const uint32_t off = tc::sw128_offset(j, t, kVs);
+          *reinterpret_cast<uint16_t*>(Uh + off) = hi;
+          *reinterpret_cast<uint16_t*>(Ul + off) = lo;
+        }
+      } else {  // rows 64..127: O = scale (Q' S + P Util)
+        const int t = tid - kChunk;
+        if (t < len) {
+          const float* oi = reinterpret_cast<const float*>(stage + kStOi) + t * kVs;
+          uint4* dst = reinterpret_cast<uint4*>(a.o + ((tc0 + t) * HV + h) * V + v0);
+#pragma unroll
+          for (int q4 = 0; q4 < kVs / 8; ++q4) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int j = q4 * 8 + e * 2;
+              w[e] = pack_bf16x2(scale * (d[j] + oi[j]), scale * (d[j + 1] + oi[j + 1]));
+            }
+            dst[q4] = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        }
       }
-#pragma unroll
-      for (int jj = 0; jj < 4; ++jj) Um[t * kLdS + j0 + jj] = Ut[t * kLdS + j0 + jj] - acc[jj];
     }
+    tc::fence_async_smem();
+    tc::tc_fence_before();
     __syncthreads();
-    // O = scale (Qtil S + P U)
-    {
-      const int t = tid >> 2, j0 = (tid & 3) * 4;
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
-      for (int c = 0; c < K; ++c) {
-        const float w = Qm[t * kLd + c];
+    // D2 = Khat^T U with hi/lo splits: hi*hi + hi*lo + lo*hi, four K=16 steps each
+    if (tid == 0 && !s_abort) {
+      tc::tc_fence_after();
+      const uint32_t kth = tc::smem_u32(stage + kStKTh), ktl = tc::smem_u32(stage + kStKTl);
+      const uint32_t uh = tc::smem_u32(Uh), ul = tc::smem_u32(Ul);
+      const uint32_t as[3] = {kth, kth, ktl}, bs[3] = {uh, ul, uh};
 #pragma unroll
-        for (int jj = 0; jj < 4; ++jj) acc[jj] += w * Sm[c * kLdS + j0 + jj];
-      }
-      for (int i = 0; i <= t; ++i) {
-        const float p = Pm[t * kLdT + i];
+      for (int p = 0; p < 3; ++p)
 #pragma unroll
-        for (int jj = 0; jj < 4; ++jj) acc[jj] += p * Um[i * kLdS + j0 + jj];
-      }
-      if (t < len) {
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj)
-          a.o[((tc + t) * HV + h) * V + v0 + j0 + jj] = float_to_bf16_bits(a.gate.scale * acc[jj]);
-      }
+        for (int k = 0; k < 4; ++k)
+          tc::mma_bf16(d2, tc::sw128_desc(as[p] + k * 32), tc::sw128_desc(bs[p] + k * 32), idesc,
+                       p > 0 || k > 0);
+      tc::mma_commit(&mma_bar);
     }
-    // S = Diag(gamma) S + Khat^T U : thread -> (c, 8 columns)
-    float snew[8];
+    if (!tc::mbar_wait(&mma_bar, mma_phase)) s_abort = 1;
+    mma_phase ^= 1;
+    tc::tc_fence_after();
     {
-      const int c = tid >> 1, j0 = (tid & 1) * 8;
+      float d[kVs];
+      tc::tmem_ld16(d2 + lane_addr, *reinterpret_cast<float(*)[16]>(d));
+      tc::tmem_ld16(d2 + lane_addr + 16, *reinterpret_cast<float(*)[16]>(d + 16));
+      const float gc = reinterpret_cast<const float*>(stage + kStGam)[c];
 #pragma unroll
-      for (int jj = 0; jj < 8; ++jj) snew[jj] = gm[c] * Sm[c * kLdS + j0 + jj];
-      for (int i = 0; i < kChunk; ++i) {
-        const float kh = Km[i * kLd + c];
-#pragma unroll
-        for (int jj = 0; jj < 8; ++jj) snew[jj] += kh * Um[i * kLdS + j0 + jj];
-      }
+      for (int j = 0; j < kVs; ++j) S[j] = gc * S[j] + d[j];
     }
+    write_state_operand();
+    tc::fence_async_smem();
+    tc::tc_fence_before();
     __syncthreads();
-    {
-      const int c = tid >> 1, j0 = (tid & 1) * 8;
-#pragma unroll
-      for (int jj = 0; jj < 8; ++jj) Sm[c * kLdS + j0 + jj] = snew[jj];
+    if (s_abort) break;
+    if (tid == 0 && ci + 2 < nch) {
+      tc::fence_async_smem();
+      issue_stage_loads(stage, ws_head + (size_t)(ci + 2) * rec_stride, slice, &full_bar[sidx]);
+      issued = ci + 3;
     }
-    __syncthreads();
   }
-  for (int idx = tid; idx < kVs * K; idx += blockDim.x) {
-    const int j = idx / K, c = idx % K;
-    st[(size_t)(v0 + j) * K + c] = Sm[c * kLdS + j];
+  if (s_abort) {
+    if (tid == 0) {
+      set_error(a.err_flag, KDA_DEVERR_TIMEOUT);
+      // let the bulk copies this CTA still has in flight land before it exits
+      for (int cj = consumed; cj < issued; ++cj)
+        tc::mbar_wait(&full_bar[cj & 1], (cj >> 1) & 1, 1u << 20);
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < kVs; ++j) st[(size_t)(v0 + j) * K + c] = S[j];
   }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
 }
-
-constexpr size_t kPassSmem = sizeof(float) * (3 * kChunk * kLd + kChunk * kLdT + kHeadDim * kLdS +
-                                              2 * kChunk * kLdS + kHeadDim);
 
 int64_t max_chunks(int num_seqs, int64_t total_tokens) {
   return total_tokens / kChunk + num_seqs;
@@ -487,7 +1087,7 @@ using namespace kda;
 
 extern "C" size_t kda_prefill_workspace_size(kda_dims dims, int num_seqs, int64_t total_tokens) {
   if (num_seqs < 0 || total_tokens < 0 || dims.HV <= 0) return 0;
-  return (size_t)max_chunks(num_seqs, total_tokens) * dims.HV * kRec * sizeof(float);
+  return (size_t)max_chunks(num_seqs, total_tokens) * dims.HV * kRecBytes;
 }
 
 extern "C" kda_status kda_prefill(kda_dims dims, kda_gate gate, const kda_bf16* q,
@@ -508,7 +1108,7 @@ extern "C" kda_status kda_prefill(kda_dims dims, kda_gate gate, const kda_bf16* 
   s = check_gate(gate, &args.gate);
   if (s != KDA_OK) return s;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(state_pool) ||
-      (intermediate && !aligned16(intermediate)))
+      !aligned16(o) || (intermediate && !aligned16(intermediate)))
     return KDA_ERR_ALIGNMENT;
   const size_t need = kda_prefill_workspace_size(dims, num_seqs, total_tokens);
   if (need > 0 && (!workspace || workspace_bytes < need)) return KDA_ERR_WORKSPACE;
@@ -528,7 +1128,7 @@ extern "C" kda_status kda_prefill(kda_dims dims, kda_gate gate, const kda_bf16* 
   args.total_tokens = total_tokens;
   args.o = o;
   args.intermediate = intermediate;
-  args.ws = static_cast<float*>(workspace);
+  args.ws = static_cast<uint8_t*>(workspace);
   args.err_flag = err_flag;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
@@ -537,14 +1137,19 @@ extern "C" kda_status kda_prefill(kda_dims dims, kda_gate gate, const kda_bf16* 
                        (int)kTransformSmem);
   cudaFuncSetAttribute(state_pass_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        (int)kPassSmem);
+  cudaFuncSetAttribute(chunk_transform_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       (int)kTransformTcSmem);
   const int64_t chunks = max_chunks(num_seqs, total_tokens);
   record_stage(0, st);
   if (chunks > 0) {
-    chunk_transform_kernel<<<dim3((unsigned)chunks, dims.HV), 256, kTransformSmem, st>>>(args);
+    if (getenv("KDA_DEBUG_SIMT_TRANSFORM"))  // TEMPORARY development switch
+      chunk_transform_kernel<<<dim3((unsigned)chunks, dims.HV), 256, kTransformSmem, st>>>(args);
+    else
+      chunk_transform_tc_kernel<<<dim3((unsigned)chunks, dims.HV), 256, kTransformTcSmem, st>>>(args);
     if ((s = launch_status()) != KDA_OK) return s;
   }
   record_stage(1, st);
-  state_pass_kernel<<<dim3(kHeadDim / kVs, dims.HV, num_seqs), 256, kPassSmem, st>>>(args);
+  state_pass_kernel<<<dim3(kSlices, dims.HV, num_seqs), 128, kPassSmem, st>>>(args);
   s = launch_status();
   record_stage(2, st);
   return s;

@@ -29,6 +29,7 @@ KDA_DEVERR_SLOT = 1
 KDA_DEVERR_PARENT = 2
 KDA_DEVERR_SEQLENS = 4
 KDA_DEVERR_ACCEPTED = 8
+KDA_DEVERR_TIMEOUT = 16
 
 CHUNK = 64
 
