@@ -239,8 +239,6 @@ def run_ours(args, rank, world, local_rank):
 
     phases = ["prefill", "decode", "verify_chain", "verify_tree", "commit"]
     kernels = ["prefill_transform", "prefill_pass", "decode", "verify_chain", "verify_tree", "commit"]
-    stage = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
-    kda.kda_prefill_set_stage_events(stage)
 
     def run_phase(name):
         if name == "prefill":
@@ -283,9 +281,17 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     wall0 = time.perf_counter()
     records = []
+    def stage_events():
+        # torch creates the CUDA event on first record(): record once so the
+        # handle exists, then the prefill re-records it around its kernels
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        for e in ev:
+            e.record(stream)
+        return ev
+
     for _ in range(args.steps):
         # fresh stage events per step: the prefill records its two kernels' bounds into them
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        ev = stage_events()
         kda.kda_prefill_set_stage_events(ev)
         rec = one_step(True)
         rec["_stage"] = ev

@@ -18,8 +18,10 @@
 //     128-bit load instruction reads four full 128-byte row segments;
 //   * k^T x and S^T q are 16-term packed-FP32 (f32x2) partial dots finished
 //     with three xor-shuffles inside the 8-lane row group;
-//   * the fold (L2 norm, gate, sigmoid beta) is recomputed per CTA from the
-//     16 channels a lane owns, so no shared memory and no __syncthreads;
+//   * the fold (L2 norm, gate, sigmoid beta) of up to 8 tokens at a time is
+//     computed once per CTA, one key channel per thread, into shared memory;
+//     lanes then read their 16 channels as float4 (broadcast across the
+//     four row groups of a warp);
 //   * verify keeps the state in registers across the T draft tokens and
 //     writes each snapshot straight from registers; a tree node whose parent
 //     is not the previous node reloads the parent's snapshot, which this same
@@ -65,16 +67,28 @@ __device__ __forceinline__ float dot16(const float4 (&x)[4], const float4 (&y)[4
   return acc.x + acc.y;
 }
 
+constexpr int kTokBlock = 8;  // tokens folded per shared-memory pass
+
+struct FoldSmem {
+  float q[kTokBlock][kHeadDim];    // q-hat
+  float k[kTokBlock][kHeadDim];    // k-hat
+  float dec[kTokBlock][kHeadDim];  // exp(g)
+  float v[kTokBlock][kHeadDim];
+  float beta[kTokBlock];
+  float red[kTokBlock][2][4];      // per-warp sums of squares of q and k
+};
+
 template <int MODE, int GROUPS>
 __global__ void __launch_bounds__(128) recurrent_kernel(const StepArgs args) {
   constexpr int K = kHeadDim, V = kHeadDim;
+  __shared__ __align__(16) FoldSmem fs;
   const int r = blockIdx.z, h = blockIdx.y;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int sub = lane & 7;
   const int row0 = blockIdx.x * (16 * GROUPS) + warp * (4 * GROUPS) + (lane >> 3);
   const int T = MODE == kDecode ? 1 : args.T;
   const int HV = args.HV;
-  const bool reporter = threadIdx.x == 0 && blockIdx.x == 0 && h == 0;
+  const bool reporter = tid == 0 && blockIdx.x == 0 && h == 0;
 
   const int slot = args.state_idx[r];
   bool ok = slot >= -1 && slot < args.pool_slots;
@@ -111,89 +125,111 @@ __global__ void __launch_bounds__(128) recurrent_kernel(const StepArgs args) {
 
   const GateArgs& ga = args.gate;
   const float exp_alog = ga.A_log ? expf(ga.A_log[h]) : 0.f;
-  float4 bias[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-    bias[i] = ga.dt_bias ? __ldg(reinterpret_cast<const float4*>(ga.dt_bias + h * K + i * 32 +
-                                                                 lane_col))
-                         : make_float4(0.f, 0.f, 0.f, 0.f);
+  const float bias_c = ga.dt_bias ? ga.dt_bias[h * K + tid] : 0.f;
 
-  for (int t = 0; t < T; ++t) {
-    if (MODE == kTree && t > 0) {
-      const int p = args.parent[(int64_t)r * T + t];
-      if (p != t - 1) {
-        const float* src =
-            p < 0 ? root : args.snapshots + (((size_t)r * T + p) * HV + h) * head_elems;
+  for (int tb = 0; tb < T; tb += kTokBlock) {
+    const int nt = T - tb < kTokBlock ? T - tb : kTokBlock;
+    // fold of tokens [tb, tb+nt): thread tid owns key channel / value column tid
+    float sq[kTokBlock], sk[kTokBlock];
 #pragma unroll
-        for (int gi = 0; gi < GROUPS; ++gi)
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            S[gi][i] = *reinterpret_cast<const float4*>(src + (size_t)(row0 + gi * 4) * K +
-                                                        i * 32 + lane_col);
+    for (int u = 0; u < kTokBlock; ++u) {
+      sq[u] = 0.f;
+      sk[u] = 0.f;
+      if (u < nt) {
+        const int64_t row = MODE == kDecode ? r : (int64_t)r * T + tb + u;
+        const kda_bf16* x = args.mixed_qkv + row * args.row_stride;
+        const float qv = bf16_bits_to_float(x[h * K + tid]);
+        const float kv = bf16_bits_to_float(x[(int64_t)args.H * K + h * K + tid]);
+        const float av = bf16_bits_to_float(args.a[row * ((int64_t)HV * K) + h * K + tid]);
+        fs.q[u][tid] = qv;
+        fs.k[u][tid] = kv;
+        fs.v[u][tid] = bf16_bits_to_float(x[2 * (int64_t)args.H * K + h * V + tid]);
+        fs.dec[u][tid] = expf(gate_log_decay(ga, av, exp_alog, bias_c));
+        if (tid == 0) fs.beta[u] = fold_beta(ga, bf16_bits_to_float(args.b[row * HV + h]));
+        sq[u] = qv * qv;
+        sk[u] = kv * kv;
       }
     }
-    const int64_t row = MODE == kDecode ? r : (int64_t)r * T + t;
-    const kda_bf16* x = args.mixed_qkv + row * args.row_stride;
-    const kda_bf16* qp = x + h * K;
-    const kda_bf16* kp = x + (int64_t)args.H * K + h * K;
-    const kda_bf16* vp = x + 2 * (int64_t)args.H * K + h * V;
-    const kda_bf16* ap = args.a + row * ((int64_t)HV * K) + h * K;
-
-    float4 q[4], k[4], dec[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      q[i] = load_bf16x4(qp + i * 32 + lane_col);
-      k[i] = load_bf16x4(kp + i * 32 + lane_col);
-      dec[i] = load_bf16x4(ap + i * 32 + lane_col);
-    }
-    float vj[GROUPS];
-#pragma unroll
-    for (int gi = 0; gi < GROUPS; ++gi) vj[gi] = bf16_bits_to_float(vp[row0 + gi * 4]);
-    const float beta = fold_beta(ga, bf16_bits_to_float(args.b[row * HV + h]));
-
     if (ga.use_qk_l2norm) {
-      const float rq = rsqrtf(group_sum8(dot16(q, q)) + kNormEps);
-      const float rk = rsqrtf(group_sum8(dot16(k, k)) + kNormEps);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        q[i].x *= rq; q[i].y *= rq; q[i].z *= rq; q[i].w *= rq;
-        k[i].x *= rk; k[i].y *= rk; k[i].z *= rk; k[i].w *= rk;
+      for (int u = 0; u < kTokBlock; ++u) {
+#pragma unroll
+        for (int m = 16; m; m >>= 1) {
+          sq[u] += __shfl_xor_sync(0xffffffffu, sq[u], m);
+          sk[u] += __shfl_xor_sync(0xffffffffu, sk[u], m);
+        }
+        if (lane == 0) {
+          fs.red[u][0][warp] = sq[u];
+          fs.red[u][1][warp] = sk[u];
+        }
+      }
+      __syncthreads();
+#pragma unroll
+      for (int u = 0; u < kTokBlock; ++u) {
+        if (u < nt) {
+          const float rq = rsqrtf(fs.red[u][0][0] + fs.red[u][0][1] + fs.red[u][0][2] +
+                                  fs.red[u][0][3] + kNormEps);
+          const float rk = rsqrtf(fs.red[u][1][0] + fs.red[u][1][1] + fs.red[u][1][2] +
+                                  fs.red[u][1][3] + kNormEps);
+          fs.q[u][tid] *= rq;
+          fs.k[u][tid] *= rk;
+        }
       }
     }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      dec[i].x = expf(gate_log_decay(ga, dec[i].x, exp_alog, bias[i].x));
-      dec[i].y = expf(gate_log_decay(ga, dec[i].y, exp_alog, bias[i].y));
-      dec[i].z = expf(gate_log_decay(ga, dec[i].z, exp_alog, bias[i].z));
-      dec[i].w = expf(gate_log_decay(ga, dec[i].w, exp_alog, bias[i].w));
-    }
+    __syncthreads();
 
-    float* snap = MODE == kDecode ? nullptr
-                                  : args.snapshots + (((size_t)r * T + t) * HV + h) * head_elems;
+    for (int u = 0; u < nt; ++u) {
+      const int t = tb + u;
+      if (MODE == kTree && t > 0) {
+        const int p = args.parent[(int64_t)r * T + t];
+        if (p != t - 1) {
+          const float* src =
+              p < 0 ? root : args.snapshots + (((size_t)r * T + p) * HV + h) * head_elems;
 #pragma unroll
-    for (int gi = 0; gi < GROUPS; ++gi) {
-      // X = Diag(exp g) S;  u = beta (v - X^T k);  S = X + k u^T;  o = scale S^T q
+          for (int gi = 0; gi < GROUPS; ++gi)
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              S[gi][i] = *reinterpret_cast<const float4*>(src + (size_t)(row0 + gi * 4) * K +
+                                                          i * 32 + lane_col);
+        }
+      }
+      const int64_t row = MODE == kDecode ? r : (int64_t)r * T + t;
+      float4 q[4], k[4], dec[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const float2 lo = mul2(make_float2(S[gi][i].x, S[gi][i].y), make_float2(dec[i].x, dec[i].y));
-        const float2 hi = mul2(make_float2(S[gi][i].z, S[gi][i].w), make_float2(dec[i].z, dec[i].w));
-        S[gi][i] = make_float4(lo.x, lo.y, hi.x, hi.y);
+        q[i] = *reinterpret_cast<const float4*>(&fs.q[u][i * 32 + lane_col]);
+        k[i] = *reinterpret_cast<const float4*>(&fs.k[u][i * 32 + lane_col]);
+        dec[i] = *reinterpret_cast<const float4*>(&fs.dec[u][i * 32 + lane_col]);
       }
-      const float u = beta * (vj[gi] - group_sum8(dot16(S[gi], k)));
-      const float2 u2 = make_float2(u, u);
+      const float beta = fs.beta[u];
+      float* snap = MODE == kDecode ? nullptr
+                                    : args.snapshots + (((size_t)r * T + t) * HV + h) * head_elems;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 lo = fma2(make_float2(k[i].x, k[i].y), u2, make_float2(S[gi][i].x, S[gi][i].y));
-        const float2 hi = fma2(make_float2(k[i].z, k[i].w), u2, make_float2(S[gi][i].z, S[gi][i].w));
-        S[gi][i] = make_float4(lo.x, lo.y, hi.x, hi.y);
+      for (int gi = 0; gi < GROUPS; ++gi) {
+        // X = Diag(exp g) S;  u = beta (v - X^T k);  S = X + k u^T;  o = scale S^T q
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 lo = mul2(make_float2(S[gi][i].x, S[gi][i].y), make_float2(dec[i].x, dec[i].y));
+          const float2 hi = mul2(make_float2(S[gi][i].z, S[gi][i].w), make_float2(dec[i].z, dec[i].w));
+          S[gi][i] = make_float4(lo.x, lo.y, hi.x, hi.y);
+        }
+        const int j = row0 + gi * 4;
+        const float uu = beta * (fs.v[u][j] - group_sum8(dot16(S[gi], k)));
+        const float2 u2 = make_float2(uu, uu);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 lo = fma2(make_float2(k[i].x, k[i].y), u2, make_float2(S[gi][i].x, S[gi][i].y));
+          const float2 hi = fma2(make_float2(k[i].z, k[i].w), u2, make_float2(S[gi][i].z, S[gi][i].w));
+          S[gi][i] = make_float4(lo.x, lo.y, hi.x, hi.y);
+        }
+        const float out = ga.scale * group_sum8(dot16(S[gi], q));
+        if (sub == 0) args.o[(row * HV + h) * V + j] = float_to_bf16_bits(out);
+        float* dst = MODE == kDecode ? root + (size_t)j * K : snap + (size_t)j * K;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) *reinterpret_cast<float4*>(dst + i * 32 + lane_col) = S[gi][i];
       }
-      const float out = ga.scale * group_sum8(dot16(S[gi], q));
-      const int j = row0 + gi * 4;
-      if (sub == 0) args.o[(row * HV + h) * V + j] = float_to_bf16_bits(out);
-      float* dst = MODE == kDecode ? root + (size_t)j * K : snap + (size_t)j * K;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) *reinterpret_cast<float4*>(dst + i * 32 + lane_col) = S[gi][i];
     }
+    if (tb + kTokBlock < T) __syncthreads();  // fold buffer reused by the next block
   }
 }
 

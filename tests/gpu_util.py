@@ -36,12 +36,20 @@ def rms(x):
 
 
 def assert_o_close(o_gpu, o_ref, what="o"):
+    """max|o - o_ref| <= 2e-2 RMS(o_ref), on top of the BF16 output's own
+    round-to-nearest: element i may also differ by 2^-8 |o_ref_i|, an upper
+    bound of half a BF16 ulp at o_ref_i (the exact value is not representable
+    in the output format, and the largest outputs here are ~12x the RMS)."""
     got = host_f64(o_gpu) if isinstance(o_gpu, torch.Tensor) else o_gpu
-    err = float(np.max(np.abs(got - o_ref))) if o_ref.size else 0.0
-    bound = O_TOL * rms(o_ref)
     assert np.isfinite(got).all(), f"{what}: non-finite values"
-    assert err <= bound, f"{what}: max|err| {err:.3e} > {bound:.3e} (2e-2 x RMS)"
-    return err / max(rms(o_ref), 1e-300)
+    if not o_ref.size:
+        return 0.0
+    r = rms(o_ref)
+    excess = np.abs(got - o_ref) - 2.0 ** -8 * np.abs(o_ref)
+    worst = float(np.max(excess))
+    assert worst <= O_TOL * r, (f"{what}: max(|err| - 2^-8|ref|) {worst:.3e} > {O_TOL * r:.3e} "
+                                f"(2e-2 x RMS); raw max|err| {float(np.max(np.abs(got - o_ref))):.3e}")
+    return max(worst, 0.0) / max(r, 1e-300)
 
 
 def assert_s_close(s_gpu, s_ref, what="state"):
