@@ -425,32 +425,40 @@ constexpr size_t kTransformSmem =
 // ---------------------------------------------------------------------------
 // Per-chunk transform on tcgen05 (all chunks of all sequences in parallel).
 //
-//   M1 (x4 blocks of i):  [Lk; Lq] R^T  -> A (rows 0-63) and P (rows 64-127),
+//   M1 (x4 blocks of 16 i):  [Lk; Lq] R^T -> A (rows 0-63) and P (rows 64-127),
 //        Lk_t = k_t e^{Gam_t - Gam_r}, Lq_t = q_t e^{Gam_t - Gam_r} (t >= block start),
-//        R_i  = k_i e^{Gam_r - Gam_i}, r = last token of the block.  M=128 N=16 K=128.
+//        R_i  = k_i e^{Gam_r - Gam_i}, r = the block's last token.  M=128 N=16 K=128.
+//        R <= 1, and the left factor is <= e^{15 |g|min} inside the block and
+//        <= 1 past it, so a factor that underflows only drops smaller terms.
+//        Blocks run last to first: round b writes rows t >= 16b only, the rows
+//        above still hold the zeros written once before the first round.
 //   (I+A)^-1 and P (I+A)^-1 on the CUDA cores (64 x 64, blocked).
 //   M2: [Ti; P Ti] [beta Ktil | beta V]^T -> W | Util (rows 0-63), P W | P Util
 //        (rows 64-127).  M=128 N=256 K=64.
 // Both products use BF16 hi/lo splits of both operands (three MMAs each).
 
-constexpr uint32_t kTxL = 0;                         // L hi, lo: 128 x 128 each
-constexpr uint32_t kTxR = kTxL + 2 * 128 * 128 * 2;  // R hi, lo: 16 x 128 each
-constexpr uint32_t kTxB2 = 0;                        // B2 hi, lo: 256 x 64 each (reuses L)
-constexpr uint32_t kTxA2 = kTxR + 2 * 16 * 128 * 2;  // A2 hi, lo: 128 x 64 each
-constexpr uint32_t kTxQ = kTxA2 + 2 * 128 * 64 * 2;  // raw q BF16 [64][128]
-constexpr uint32_t kTxK = kTxQ + kChunk * kHeadDim * 2;
-constexpr uint32_t kTxG = kTxK + kChunk * kHeadDim * 2;  // Gam FP32 [64][kLd]
-constexpr uint32_t kTxAf = kTxG + kChunk * kLd * 4;      // A FP32 [64][kLdT]
-constexpr uint32_t kTxPf = kTxAf + kChunk * kLdT * 4;    // P FP32
-constexpr uint32_t kTxTf = kTxPf + kChunk * kLdT * 4;    // (I+A)^-1 FP32
+constexpr int kLdB = 136;  // padded row stride (BF16 elements) of the raw q, k tiles
+
+constexpr uint32_t kTxL = 0;                          // L hi, lo: 128 x 128 each
+constexpr uint32_t kTxR = kTxL + 2 * 128 * 128 * 2;   // R hi, lo: 16 x 128 each
+constexpr uint32_t kTxB2 = 0;                         // B2 hi, lo: 256 x 64 each (reuses L/R)
+constexpr uint32_t kTxAf = 0;                         // A FP32 [64][kLdT] (reuses L/R)
+constexpr uint32_t kTxPf = kTxAf + kChunk * kLdT * 4;  // P FP32 (reuses L/R)
+constexpr uint32_t kTxA2 = kTxR + 2 * 16 * 128 * 2;   // A2 hi, lo: 128 x 64 each
+constexpr uint32_t kTxQ = kTxA2 + 2 * 128 * 64 * 2;   // raw q BF16 [64][kLdB]
+constexpr uint32_t kTxK = kTxQ + kChunk * kLdB * 2;
+constexpr uint32_t kTxG = kTxK + kChunk * kLdB * 2;   // Gam FP32 [64][kLd]
+constexpr uint32_t kTxTf = kTxG + kChunk * kLd * 4;   // (I+A)^-1 FP32 [64][kLdT]
 constexpr uint32_t kTxMisc = kTxTf + kChunk * kLdT * 4;  // rq, rk, beta [64] each + scratch [768]
 constexpr uint32_t kTxEnd = kTxMisc + (3 * kChunk + 768) * 4;
 constexpr uint32_t kTransformTcSmem = kTxEnd + 1024;
 constexpr uint32_t kTxTmemCols = 256;
 static_assert(2 * 256 * 64 * 2 <= kTxA2, "B2 fits in the L/R region");
-static_assert(kTxAf + 8 * kHeadDim * 4 <= kTxTf + kChunk * kLdT * 4, "warp totals fit");
+static_assert(kTxPf + kChunk * kLdT * 4 <= kTxA2, "A and P fit in the L/R region");
+static_assert(8 * kHeadDim * 4 <= kTxA2, "warp totals fit in the L/R region");
+static_assert(kTxQ % 16 == 0 && kTxK % 16 == 0 && kTxG % 16 == 0 && kTxTf % 16 == 0, "alignment");
 
-__device__ __forceinline__ void st_split_pair(uint8_t* hi, uint8_t* lo, uint32_t off, const float* x) {
+__device__ __forceinline__ void st_split8(uint8_t* hi, uint8_t* lo, uint32_t off, const float* x) {
   // eight consecutive values -> one 16-byte chunk in each of hi and lo
   uint32_t h[4], l[4];
 #pragma unroll
@@ -465,8 +473,25 @@ __device__ __forceinline__ void st_split_pair(uint8_t* hi, uint8_t* lo, uint32_t
   *reinterpret_cast<uint4*>(lo + off) = make_uint4(l[0], l[1], l[2], l[3]);
 }
 
+// Eight consecutive BF16 values of row t, columns [c, c+8), of a raw tile.
+__device__ __forceinline__ void ld_bf16x8(const uint8_t* tile, int t, int c, float* x) {
+  const uint4 u = *reinterpret_cast<const uint4*>(tile + (t * kLdB + c) * 2);
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    x[2 * e] = __uint_as_float(w[e] << 16);
+    x[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
+  }
+}
+
+__device__ __forceinline__ void ld_f32x8(const float* p, float* x) {
+  const float4 a = *reinterpret_cast<const float4*>(p), b = *reinterpret_cast<const float4*>(p + 4);
+  x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+  x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
+
 __device__ __forceinline__ float bf16_at(const uint8_t* tile, int t, int c) {
-  return bf16_bits_to_float(reinterpret_cast<const uint16_t*>(tile)[t * kHeadDim + c]);
+  return bf16_bits_to_float(reinterpret_cast<const uint16_t*>(tile)[t * kLdB + c]);
 }
 
 __global__ void __launch_bounds__(256, 1) chunk_transform_tc_kernel(const PrefillArgs a) {
@@ -528,9 +553,9 @@ __global__ void __launch_bounds__(256, 1) chunk_transform_tc_kernel(const Prefil
 
   // 1. fold: raw q, k kept as BF16 with their norms; Gam by warp-blocked prefix.
   {
-    float* tot = Af;  // [8][128] warp totals
+    float* tot = reinterpret_cast<float*>(sb + kTxL);  // [8][128] warp totals
     const int c = lane * 4;
-    const float exp_alog = ga.A_log ? expf(ga.A_log[h]) : 0.f;
+    const float exp_alog = ga.A_log ? __expf(ga.A_log[h]) : 0.f;
     const float4 bias = ga.dt_bias ? *reinterpret_cast<const float4*>(ga.dt_bias + h * K + c)
                                    : make_float4(0.f, 0.f, 0.f, 0.f);
     float4 run = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -542,8 +567,10 @@ __global__ void __launch_bounds__(256, 1) chunk_transform_tc_kernel(const Prefil
         const int64_t tok = t0 + t;
         qraw = __ldg(reinterpret_cast<const uint2*>(a.q + (tok * H + h) * K + c));
         kraw = __ldg(reinterpret_cast<const uint2*>(a.k + (tok * H + h) * K + c));
-        const float4 q4 = load_bf16x4(a.q + (tok * H + h) * K + c);
-        const float4 k4 = load_bf16x4(a.k + (tok * H + h) * K + c);
+        const float4 q4 = make_float4(__uint_as_float(qraw.x << 16), __uint_as_float(qraw.x & 0xffff0000u),
+                                      __uint_as_float(qraw.y << 16), __uint_as_float(qraw.y & 0xffff0000u));
+        const float4 k4 = make_float4(__uint_as_float(kraw.x << 16), __uint_as_float(kraw.x & 0xffff0000u),
+                                      __uint_as_float(kraw.y << 16), __uint_as_float(kraw.y & 0xffff0000u));
         const float4 a4 = load_bf16x4(a.g + (tok * HV + h) * K + c);
         nq = ga.use_qk_l2norm ? rsqrtf(warp_sum(dot4(q4, q4)) + kNormEps) : 1.f;
         nk = ga.use_qk_l2norm ? rsqrtf(warp_sum(dot4(k4, k4)) + kNormEps) : 1.f;
@@ -558,8 +585,8 @@ __global__ void __launch_bounds__(256, 1) chunk_transform_tc_kernel(const Prefil
         rk[t] = nk;
         bt[t] = b;
       }
-      *reinterpret_cast<uint2*>(Qs + (t * K + c) * 2) = qraw;
-      *reinterpret_cast<uint2*>(Ks + (t * K + c) * 2) = kraw;
+      *reinterpret_cast<uint2*>(Qs + (t * kLdB + c) * 2) = qraw;
+      *reinterpret_cast<uint2*>(Ks + (t * kLdB + c) * 2) = kraw;
       run = make_float4(run.x + g4.x, run.y + g4.y, run.z + g4.z, run.w + g4.w);
       f4(GM + t * kLd + c) = run;
     }
@@ -578,7 +605,7 @@ __global__ void __launch_bounds__(256, 1) chunk_transform_tc_kernel(const Prefil
   __syncthreads();
 
   // 2. gamma and Khat^T (hi/lo, swizzled 128 x 64) straight to the workspace
-  if (tid < K) reinterpret_cast<float*>(rec + kRecGam)[tid] = expf(GM[(kChunk - 1) * kLd + tid]);
+  if (tid < K) reinterpret_cast<float*>(rec + kRecGam)[tid] = __expf(GM[(kChunk - 1) * kLd + tid]);
   for (int idx = tid; idx < K * 8; idx += blockDim.x) {
     const int c = idx & (K - 1), j = idx >> 7;
     const float gl = GM[(kChunk - 1) * kLd + c];
@@ -586,9 +613,9 @@ __global__ void __launch_bounds__(256, 1) chunk_transform_tc_kernel(const Prefil
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
       const int t = j * 8 + e;
-      x[e] = bf16_at(Ks, t, c) * rk[t] * expf(gl - GM[t * kLd + c]);
+      x[e] = bf16_at(Ks, t, c) * rk[t] * __expf(gl - GM[t * kLd + c]);
     }
-    st_split_pair(rec + kRecKTh, rec + kRecKTl, tc::sw128_offset(c, j * 8, K), x);
+    st_split8(rec + kRecKTh, rec + kRecKTl, tc::sw128_offset(c, j * 8, K), x);
   }
 
   tc::tc_fence_before();
@@ -598,33 +625,40 @@ __global__ void __launch_bounds__(256, 1) chunk_transform_tc_kernel(const Prefil
   const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
   uint32_t phase = 0;
 
-  // 3. M1: A and P, one 16-token block of i per round.
-  for (int ib = 0; ib < kChunk / 16; ++ib) {
+  // 3. M1: A and P, one 16-token block of i per round, last block first.
+  for (int idx = tid; idx < 2 * 128 * 128 * 2 / 16; idx += blockDim.x)
+    reinterpret_cast<uint4*>(Lh)[idx] = make_uint4(0u, 0u, 0u, 0u);  // L hi and lo
+  for (int ib = kChunk / 16 - 1; ib >= 0; --ib) {
     const int b0 = ib * 16, r = b0 + 15;
-    // L rows: 0-63 k side, 64-127 q side; thread -> (row, 8-column chunk)
-    for (int idx = tid; idx < 128 * 16; idx += blockDim.x) {
-      const int row = idx >> 4, ch = idx & 15;
-      const int t = row & 63;
-      const uint8_t* src = row < kChunk ? Ks : Qs;
-      const float nrm = row < kChunk ? rk[t] : rq[t];
-      float x[8];
+    // rows t of Lk and Lq share the factor e^{Gam_t - Gam_r}; thread -> (t, 8-column chunk)
+    for (int idx = tid; idx < (kChunk - b0) * 16; idx += blockDim.x) {
+      const int t = b0 + (idx >> 4), c = (idx & 15) * 8;
+      float gt[8], gr[8], xk[8], xq[8];
+      ld_f32x8(GM + t * kLd + c, gt);
+      ld_f32x8(GM + r * kLd + c, gr);
+      ld_bf16x8(Ks, t, c, xk);
+      ld_bf16x8(Qs, t, c, xq);
+      const float nk = rk[t], nq = rq[t];
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        const int c = ch * 8 + e;
-        x[e] = t >= b0 ? bf16_at(src, t, c) * nrm * expf(GM[t * kLd + c] - GM[r * kLd + c]) : 0.f;
+        const float f = __expf(gt[e] - gr[e]);
+        xk[e] *= nk * f;
+        xq[e] *= nq * f;
       }
-      st_split_pair(Lh, Ll, tc::sw128_offset(row, ch * 8, 128), x);
+      st_split8(Lh, Ll, tc::sw128_offset(t, c, 128), xk);
+      st_split8(Lh, Ll, tc::sw128_offset(t + kChunk, c, 128), xq);
     }
     for (int idx = tid; idx < 16 * 16; idx += blockDim.x) {
-      const int row = idx >> 4, ch = idx & 15;
-      const int i = b0 + row;
-      float x[8];
+      const int ii = idx >> 4, c = (idx & 15) * 8;
+      const int i = b0 + ii;
+      float gi[8], gr[8], x[8];
+      ld_f32x8(GM + i * kLd + c, gi);
+      ld_f32x8(GM + r * kLd + c, gr);
+      ld_bf16x8(Ks, i, c, x);
+      const float nk = rk[i];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int c = ch * 8 + e;
-        x[e] = bf16_at(Ks, i, c) * rk[i] * expf(GM[r * kLd + c] - GM[i * kLd + c]);
-      }
-      st_split_pair(Rh, Rl, tc::sw128_offset(row, ch * 8, 16), x);
+      for (int e = 0; e < 8; ++e) x[e] *= nk * __expf(gr[e] - gi[e]);
+      st_split8(Rh, Rl, tc::sw128_offset(ii, c, 16), x);
     }
     tc::fence_async_smem();
     tc::tc_fence_before();
@@ -639,7 +673,7 @@ __global__ void __launch_bounds__(256, 1) chunk_transform_tc_kernel(const Prefil
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const uint32_t koff = (k & 3) * 32;
-          tc::mma_bf16(tmem + ib * 16, tc::sw128_desc(ah[p] + (k >> 2) * (128 * 128) + koff),
+          tc::mma_bf16(tmem + b0, tc::sw128_desc(ah[p] + (k >> 2) * (128 * 128) + koff),
                        tc::sw128_desc(bh[p] + (k >> 2) * (16 * 128) + koff), idesc, p > 0 || k > 0);
         }
       tc::mma_commit(&mma_bar);
@@ -676,7 +710,8 @@ __global__ void __launch_bounds__(256, 1) chunk_transform_tc_kernel(const Prefil
   tc::tc_fence_before();
   __syncthreads();
 
-  // 5. (I + A)^-1, blocked in 16 x 16 (see the CUDA-core transform above).
+  // 5. (I + A)^-1, blocked in 16 x 16: diagonal blocks by forward substitution
+  //    (one column per thread), then T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj.
   for (int i = tid; i < kChunk * kLdT; i += blockDim.x) Tf[i] = 0.f;
   __syncthreads();
   if (tid < kChunk) {
@@ -734,8 +769,9 @@ __global__ void __launch_bounds__(256, 1) chunk_transform_tc_kernel(const Prefil
         for (int e = 0; e < 8; ++e) x[e] += p * Tf[i * kLdT + ch * 8 + e];
       }
     }
-    st_split_pair(A2h, A2l, tc::sw128_offset(row, ch * 8, 128), x);
+    st_split8(A2h, A2l, tc::sw128_offset(row, ch * 8, 128), x);
   }
+  __syncthreads();  // A and P (in the L/R region) are dead before B2 overwrites it
   // 7. B2 = [(beta Ktil)^T ; (beta V)^T] (hi/lo, swizzled 256 x 64): row -> channel
   for (int idx = tid; idx < 256 * 8; idx += blockDim.x) {
     const int row = idx & 255, ch = idx >> 8;
@@ -745,7 +781,7 @@ __global__ void __launch_bounds__(256, 1) chunk_transform_tc_kernel(const Prefil
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         const int i = ch * 8 + e;
-        x[e] = bt[i] * bf16_at(Ks, i, c) * rk[i] * expf(GM[i * kLd + c]);
+        x[e] = bt[i] * bf16_at(Ks, i, c) * rk[i] * __expf(GM[i * kLd + c]);
       }
     } else {
       const int c = row - K;
@@ -755,7 +791,7 @@ __global__ void __launch_bounds__(256, 1) chunk_transform_tc_kernel(const Prefil
         x[e] = i < len ? bt[i] * bf16_bits_to_float(a.v[((t0 + i) * HV + h) * K + c]) : 0.f;
       }
     }
-    st_split_pair(Bh, Bl, tc::sw128_offset(row, ch * 8, 256), x);
+    st_split8(Bh, Bl, tc::sw128_offset(row, ch * 8, 256), x);
   }
   tc::fence_async_smem();
   tc::tc_fence_before();
@@ -790,20 +826,20 @@ __global__ void __launch_bounds__(256, 1) chunk_transform_tc_kernel(const Prefil
       const int c0 = cb * 16;  // column within the half
       tc::tmem_ld16(tmem + lane_addr + (right ? 128 : 0) + c0, d);
       if (!right) {
-        float x[16];
-        if (upper) {
+        if (!upper) {  // Q' = Qtil - P W
+          float q8[8], g8[8];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) x[e] = d[e];
-        } else {  // Q' = Qtil - P W
+          for (int hh = 0; hh < 2; ++hh) {
+            ld_bf16x8(Qs, t, c0 + hh * 8, q8);
+            ld_f32x8(GM + t * kLd + c0 + hh * 8, g8);
+            const float nq = rq[t];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int c = c0 + e;
-            x[e] = bf16_at(Qs, t, c) * rq[t] * expf(GM[t * kLd + c]) - d[e];
+            for (int e = 0; e < 8; ++e) d[hh * 8 + e] = q8[e] * nq * __expf(g8[e]) - d[hh * 8 + e];
           }
         }
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
-          const float* xs = x + half * 8;
+          const float* xs = d + half * 8;
           const uint4 pk = make_uint4(pack_bf16x2(xs[0], xs[1]), pack_bf16x2(xs[2], xs[3]),
                                       pack_bf16x2(xs[4], xs[5]), pack_bf16x2(xs[6], xs[7]));
           *reinterpret_cast<uint4*>(rec + kRecA1 + tc::sw128_offset(row, c0 + half * 8, 128)) = pk;

@@ -97,9 +97,10 @@ def prefill_inputs(seed=0, lengths=(128,), H=4, K=HEAD_DIM, V=HEAD_DIM, slots=4,
     out["g"][:T] = _normal_bf16(rng, (T, H, K))
     out["beta"][:T] = _normal_bf16(rng, (T, H))
     if gb_rows > T:
-        if garbage:
-            out["g"][T:] = _garbage_bf16(rng, (gb_rows - T, H, K))
-            out["beta"][T:] = _garbage_bf16(rng, (gb_rows - T, H))
+        if garbage:  # own stream, so the other inputs do not depend on it
+            grng = np.random.default_rng([seed, 7919])
+            out["g"][T:] = _garbage_bf16(grng, (gb_rows - T, H, K))
+            out["beta"][T:] = _garbage_bf16(grng, (gb_rows - T, H))
         else:
             out["g"][T:] = 0
             out["beta"][T:] = 0
