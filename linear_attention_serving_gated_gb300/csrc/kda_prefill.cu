@@ -425,49 +425,58 @@ constexpr size_t kTransformSmem =
 // ---------------------------------------------------------------------------
 // Per-chunk transform on tcgen05 (all chunks of all sequences in parallel).
 //
-//   M1 (x4 blocks of 16 i):  [Lk; Lq] R^T -> A (rows 0-63) and P (rows 64-127),
-//        Lk_t = k_t e^{Gam_t - Gam_r}, Lq_t = q_t e^{Gam_t - Gam_r} (t >= block start),
-//        R_i  = k_i e^{Gam_r - Gam_i}, r = the block's last token.  M=128 N=16 K=128.
-//        R <= 1, and the left factor is <= e^{15 |g|min} inside the block and
-//        <= 1 past it, so a factor that underflows only drops smaller terms.
-//        Blocks run last to first: round b writes rows t >= 16b only, the rows
-//        above still hold the zeros written once before the first round.
+//   M1, two products, D = L R^T with L rows [k-side; q-side] of
+//        Lk_t = k_t e^{Gam_t - Gam_r},  Lq_t = q_t e^{Gam_t - Gam_r},  R_i = k_i e^{Gam_r - Gam_i}:
+//     round a (M=128 N=64): rows t < 32 against r = 15 (columns 0-31, i < 32) and
+//                           rows t >= 32 against r = 31 (columns 32-63, i < 32);
+//     round b (M=128 N=32): rows t >= 32 against r = 47 (i >= 32).
+//     Within a 32-token window every factor is bounded by e^{16 |g|min}; across
+//     windows (t >= 32 > i, r = 31) both factors are <= 1.  So with per-token
+//     log-decays >= -5.5 no factor leaves FP32/BF16 range; entries with i > t
+//     may overflow and are masked.
 //   (I+A)^-1 and P (I+A)^-1 on the CUDA cores (64 x 64, blocked).
 //   M2: [Ti; P Ti] [beta Ktil | beta V]^T -> W | Util (rows 0-63), P W | P Util
 //        (rows 64-127).  M=128 N=256 K=64.
 // Both products use BF16 hi/lo splits of both operands (three MMAs each).
 
-constexpr int kLdB = 136;  // padded row stride (BF16 elements) of the raw q, k tiles
+constexpr int kLdB = 136;       // padded row stride (BF16 elements) of the raw q, k, v tiles
+constexpr int kTxThreads = 512;
+constexpr int kTxWarps = kTxThreads / 32;
 
 constexpr uint32_t kTxL = 0;                          // L hi, lo: 128 x 128 each
-constexpr uint32_t kTxR = kTxL + 2 * 128 * 128 * 2;   // R hi, lo: 16 x 128 each
+constexpr uint32_t kTxR = kTxL + 2 * 128 * 128 * 2;   // R hi, lo: 64 x 128 each
 constexpr uint32_t kTxB2 = 0;                         // B2 hi, lo: 256 x 64 each (reuses L/R)
 constexpr uint32_t kTxAf = 0;                         // A FP32 [64][kLdT] (reuses L/R)
 constexpr uint32_t kTxPf = kTxAf + kChunk * kLdT * 4;  // P FP32 (reuses L/R)
-constexpr uint32_t kTxA2 = kTxR + 2 * 16 * 128 * 2;   // A2 hi, lo: 128 x 64 each
+constexpr uint32_t kTxA2 = kTxR + 2 * 64 * 128 * 2;   // A2 hi, lo: 128 x 64 each
 constexpr uint32_t kTxQ = kTxA2 + 2 * 128 * 64 * 2;   // raw q BF16 [64][kLdB]
-constexpr uint32_t kTxK = kTxQ + kChunk * kLdB * 2;
-constexpr uint32_t kTxG = kTxK + kChunk * kLdB * 2;   // Gam FP32 [64][kLd]
-constexpr uint32_t kTxTf = kTxG + kChunk * kLd * 4;   // (I+A)^-1 FP32 [64][kLdT]
-constexpr uint32_t kTxMisc = kTxTf + kChunk * kLdT * 4;  // rq, rk, beta [64] each + scratch [768]
+constexpr uint32_t kTxK = kTxQ + kChunk * kLdB * 2;   // raw k
+constexpr uint32_t kTxV = kTxK + kChunk * kLdB * 2;   // raw v
+constexpr uint32_t kTxG = kTxV + kChunk * kLdB * 2;   // Gam FP32 [64][kLd]
+constexpr uint32_t kTxTf = kTxPf + kChunk * kLdT * 4;  // (I+A)^-1 FP32 [64][kLdT] (reuses L/R)
+constexpr uint32_t kTxMisc = kTxG + kChunk * kLd * 4;  // rq, rk, beta [64] each + scratch [768]
 constexpr uint32_t kTxEnd = kTxMisc + (3 * kChunk + 768) * 4;
 constexpr uint32_t kTransformTcSmem = kTxEnd + 1024;
 constexpr uint32_t kTxTmemCols = 256;
 static_assert(2 * 256 * 64 * 2 <= kTxA2, "B2 fits in the L/R region");
-static_assert(kTxPf + kChunk * kLdT * 4 <= kTxA2, "A and P fit in the L/R region");
-static_assert(8 * kHeadDim * 4 <= kTxA2, "warp totals fit in the L/R region");
-static_assert(kTxQ % 16 == 0 && kTxK % 16 == 0 && kTxG % 16 == 0 && kTxTf % 16 == 0, "alignment");
+static_assert(kTxTf + kChunk * kLdT * 4 <= kTxA2, "A, P and (I+A)^-1 fit in the L/R region");
+static_assert(kTxWarps * kHeadDim * 4 <= kTxA2, "warp totals fit in the L/R region");
+static_assert(kTxQ % 16 == 0 && kTxK % 16 == 0 && kTxV % 16 == 0 && kTxG % 16 == 0 &&
+                  kTxTf % 16 == 0 && kTxMisc % 16 == 0 && kTxA2 % 1024 == 0 && kTxR % 1024 == 0,
+              "alignment");
+static_assert(kTransformTcSmem <= 232448, "shared memory");
 
+// Eight consecutive values -> one 16-byte chunk in each of hi and lo
+// (hi = RN(x), lo = RN(x - hi), both BF16).
 __device__ __forceinline__ void st_split8(uint8_t* hi, uint8_t* lo, uint32_t off, const float* x) {
-  // eight consecutive values -> one 16-byte chunk in each of hi and lo
   uint32_t h[4], l[4];
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
-    uint16_t h0, l0, h1, l1;
-    tc::split_bf16(x[2 * e], h0, l0);
-    tc::split_bf16(x[2 * e + 1], h1, l1);
-    h[e] = (uint32_t)h0 | ((uint32_t)h1 << 16);
-    l[e] = (uint32_t)l0 | ((uint32_t)l1 << 16);
+    const __nv_bfloat162 hb = __floats2bfloat162_rn(x[2 * e], x[2 * e + 1]);
+    const float2 hf = __bfloat1622float2(hb);
+    const __nv_bfloat162 lb = __floats2bfloat162_rn(x[2 * e] - hf.x, x[2 * e + 1] - hf.y);
+    h[e] = *reinterpret_cast<const uint32_t*>(&hb);
+    l[e] = *reinterpret_cast<const uint32_t*>(&lb);
   }
   *reinterpret_cast<uint4*>(hi + off) = make_uint4(h[0], h[1], h[2], h[3]);
   *reinterpret_cast<uint4*>(lo + off) = make_uint4(l[0], l[1], l[2], l[3]);
@@ -494,7 +503,12 @@ __device__ __forceinline__ float bf16_at(const uint8_t* tile, int t, int c) {
   return bf16_bits_to_float(reinterpret_cast<const uint16_t*>(tile)[t * kLdB + c]);
 }
 
-__global__ void __launch_bounds__(256, 1) chunk_transform_tc_kernel(const PrefillArgs a) {
+__device__ __forceinline__ float4 bf16x4_to_f4(uint2 u) {
+  return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
+                     __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
+}
+
+__global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const PrefillArgs a) {
   extern __shared__ uint8_t smraw[];
   __shared__ uint64_t mma_bar;
   __shared__ uint32_t tmem_base;
@@ -505,13 +519,14 @@ __global__ void __launch_bounds__(256, 1) chunk_transform_tc_kernel(const Prefil
   uint8_t* Lh = sb + kTxL;
   uint8_t* Ll = Lh + 128 * 128 * 2;
   uint8_t* Rh = sb + kTxR;
-  uint8_t* Rl = Rh + 16 * 128 * 2;
+  uint8_t* Rl = Rh + 64 * 128 * 2;
   uint8_t* Bh = sb + kTxB2;
   uint8_t* Bl = Bh + 256 * 64 * 2;
   uint8_t* A2h = sb + kTxA2;
   uint8_t* A2l = A2h + 128 * 64 * 2;
   uint8_t* Qs = sb + kTxQ;
   uint8_t* Ks = sb + kTxK;
+  uint8_t* Vs = sb + kTxV;
   float* GM = reinterpret_cast<float*>(sb + kTxG);
   float* Af = reinterpret_cast<float*>(sb + kTxAf);
   float* Pf = reinterpret_cast<float*>(sb + kTxPf);
@@ -551,42 +566,53 @@ __global__ void __launch_bounds__(256, 1) chunk_transform_tc_kernel(const Prefil
   const int H = a.H, HV = a.HV, K = kHeadDim;
   uint8_t* rec = a.ws + ((size_t)cid * HV + h) * kRecBytes;
 
-  // 1. fold: raw q, k kept as BF16 with their norms; Gam by warp-blocked prefix.
+  // 1. fold.  Warp w owns tokens [4w, 4w+4), lane l channels [4l, 4l+4); all
+  //    global loads of the warp are issued before any use.  Raw q, k, v stay
+  //    BF16 in shared memory, with the per-token norms; Gam by warp-blocked prefix.
   {
-    float* tot = reinterpret_cast<float*>(sb + kTxL);  // [8][128] warp totals
+    constexpr int kTpw = kChunk / kTxWarps;  // tokens per warp
+    float* tot = reinterpret_cast<float*>(sb + kTxL);  // [kTxWarps][128] warp totals
     const int c = lane * 4;
+    uint2 qr[kTpw], kr[kTpw], vr[kTpw], ar[kTpw];
+    float br[kTpw];
+#pragma unroll
+    for (int u = 0; u < kTpw; ++u) {
+      const int t = warp * kTpw + u;
+      qr[u] = kr[u] = vr[u] = ar[u] = make_uint2(0u, 0u);
+      br[u] = 0.f;
+      if (t < len) {
+        const int64_t tok = t0 + t;
+        qr[u] = __ldg(reinterpret_cast<const uint2*>(a.q + (tok * H + h) * K + c));
+        kr[u] = __ldg(reinterpret_cast<const uint2*>(a.k + (tok * H + h) * K + c));
+        vr[u] = __ldg(reinterpret_cast<const uint2*>(a.v + (tok * HV + h) * K + c));
+        ar[u] = __ldg(reinterpret_cast<const uint2*>(a.g + (tok * HV + h) * K + c));
+        if (lane == 0) br[u] = bf16_bits_to_float(a.beta[tok * HV + h]);
+      }
+    }
     const float exp_alog = ga.A_log ? __expf(ga.A_log[h]) : 0.f;
     const float4 bias = ga.dt_bias ? *reinterpret_cast<const float4*>(ga.dt_bias + h * K + c)
                                    : make_float4(0.f, 0.f, 0.f, 0.f);
     float4 run = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int t = warp * 8; t < warp * 8 + 8; ++t) {
-      uint2 qraw = make_uint2(0u, 0u), kraw = qraw;
+#pragma unroll
+    for (int u = 0; u < kTpw; ++u) {
+      const int t = warp * kTpw + u;
+      const bool live = t < len;
+      const float4 q4 = bf16x4_to_f4(qr[u]), k4 = bf16x4_to_f4(kr[u]), a4 = bf16x4_to_f4(ar[u]);
+      const float sq = warp_sum(dot4(q4, q4)), sk = warp_sum(dot4(k4, k4));
       float4 g4 = make_float4(0.f, 0.f, 0.f, 0.f);
-      float nq = 0.f, nk = 0.f, b = 0.f;
-      if (t < len) {
-        const int64_t tok = t0 + t;
-        qraw = __ldg(reinterpret_cast<const uint2*>(a.q + (tok * H + h) * K + c));
-        kraw = __ldg(reinterpret_cast<const uint2*>(a.k + (tok * H + h) * K + c));
-        const float4 q4 = make_float4(__uint_as_float(qraw.x << 16), __uint_as_float(qraw.x & 0xffff0000u),
-                                      __uint_as_float(qraw.y << 16), __uint_as_float(qraw.y & 0xffff0000u));
-        const float4 k4 = make_float4(__uint_as_float(kraw.x << 16), __uint_as_float(kraw.x & 0xffff0000u),
-                                      __uint_as_float(kraw.y << 16), __uint_as_float(kraw.y & 0xffff0000u));
-        const float4 a4 = load_bf16x4(a.g + (tok * HV + h) * K + c);
-        nq = ga.use_qk_l2norm ? rsqrtf(warp_sum(dot4(q4, q4)) + kNormEps) : 1.f;
-        nk = ga.use_qk_l2norm ? rsqrtf(warp_sum(dot4(k4, k4)) + kNormEps) : 1.f;
+      if (live)
         g4 = make_float4(gate_log_decay(ga, a4.x, exp_alog, bias.x),
                          gate_log_decay(ga, a4.y, exp_alog, bias.y),
                          gate_log_decay(ga, a4.z, exp_alog, bias.z),
                          gate_log_decay(ga, a4.w, exp_alog, bias.w));
-        b = fold_beta(ga, bf16_bits_to_float(a.beta[tok * HV + h]));
-      }
       if (lane == 0) {
-        rq[t] = nq;
-        rk[t] = nk;
-        bt[t] = b;
+        rq[t] = live ? (ga.use_qk_l2norm ? rsqrtf(sq + kNormEps) : 1.f) : 0.f;
+        rk[t] = live ? (ga.use_qk_l2norm ? rsqrtf(sk + kNormEps) : 1.f) : 0.f;
+        bt[t] = live ? fold_beta(ga, br[u]) : 0.f;
       }
-      *reinterpret_cast<uint2*>(Qs + (t * kLdB + c) * 2) = qraw;
-      *reinterpret_cast<uint2*>(Ks + (t * kLdB + c) * 2) = kraw;
+      *reinterpret_cast<uint2*>(Qs + (t * kLdB + c) * 2) = qr[u];
+      *reinterpret_cast<uint2*>(Ks + (t * kLdB + c) * 2) = kr[u];
+      *reinterpret_cast<uint2*>(Vs + (t * kLdB + c) * 2) = vr[u];
       run = make_float4(run.x + g4.x, run.y + g4.y, run.z + g4.z, run.w + g4.w);
       f4(GM + t * kLd + c) = run;
     }
@@ -597,8 +623,9 @@ __global__ void __launch_bounds__(256, 1) chunk_transform_tc_kernel(const Prefil
       const float4 x = f4(tot + w * K + c);
       pre = make_float4(pre.x + x.x, pre.y + x.y, pre.z + x.z, pre.w + x.w);
     }
-    for (int t = warp * 8; t < warp * 8 + 8; ++t) {
-      float4& gg = f4(GM + t * kLd + c);
+#pragma unroll
+    for (int u = 0; u < kTpw; ++u) {
+      float4& gg = f4(GM + (warp * kTpw + u) * kLd + c);
       gg = make_float4(gg.x + pre.x, gg.y + pre.y, gg.z + pre.z, gg.w + pre.w);
     }
   }
@@ -606,7 +633,7 @@ __global__ void __launch_bounds__(256, 1) chunk_transform_tc_kernel(const Prefil
 
   // 2. gamma and Khat^T (hi/lo, swizzled 128 x 64) straight to the workspace
   if (tid < K) reinterpret_cast<float*>(rec + kRecGam)[tid] = __expf(GM[(kChunk - 1) * kLd + tid]);
-  for (int idx = tid; idx < K * 8; idx += blockDim.x) {
+  for (int idx = tid; idx < K * 8; idx += kTxThreads) {
     const int c = idx & (K - 1), j = idx >> 7;
     const float gl = GM[(kChunk - 1) * kLd + c];
     float x[8];
@@ -625,14 +652,22 @@ __global__ void __launch_bounds__(256, 1) chunk_transform_tc_kernel(const Prefil
   const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
   uint32_t phase = 0;
 
-  // 3. M1: A and P, one 16-token block of i per round, last block first.
-  for (int idx = tid; idx < 2 * 128 * 128 * 2 / 16; idx += blockDim.x)
-    reinterpret_cast<uint4*>(Lh)[idx] = make_uint4(0u, 0u, 0u, 0u);  // L hi and lo
-  for (int ib = kChunk / 16 - 1; ib >= 0; --ib) {
-    const int b0 = ib * 16, r = b0 + 15;
-    // rows t of Lk and Lq share the factor e^{Gam_t - Gam_r}; thread -> (t, 8-column chunk)
-    for (int idx = tid; idx < (kChunk - b0) * 16; idx += blockDim.x) {
-      const int t = b0 + (idx >> 4), c = (idx & 15) * 8;
+  // 3. M1 in two rounds (see the header of this kernel).
+  //    L row groups of 32: [Lk, Lq] for the window, R rows [R(window a), R(window b)].
+  for (int round = 0; round < 2; ++round) {
+    // row groups: (t0g, r) for groups 0-1 (rows 0-63) and 2-3 (rows 64-127)
+    const int tA = round == 0 ? 0 : 32, rA = round == 0 ? 15 : 47;
+    const int tB = 32, rB = 31;               // round 0 only
+    for (int idx = tid; idx < 64 * 16; idx += kTxThreads) {
+      const int g = idx >> 9;                  // 0: first window rows, 1: second (round 0 only)
+      const int tt = (idx >> 4) & 31, c = (idx & 15) * 8;
+      if (round == 1 && g == 1) {            // rows 64-127 of round b are zero
+        float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        st_split8(Lh, Ll, tc::sw128_offset(64 + tt, c, 128), z);
+        st_split8(Lh, Ll, tc::sw128_offset(96 + tt, c, 128), z);
+        continue;
+      }
+      const int t = (g == 0 ? tA : tB) + tt, r = g == 0 ? rA : rB;
       float gt[8], gr[8], xk[8], xq[8];
       ld_f32x8(GM + t * kLd + c, gt);
       ld_f32x8(GM + r * kLd + c, gr);
@@ -645,12 +680,14 @@ __global__ void __launch_bounds__(256, 1) chunk_transform_tc_kernel(const Prefil
         xk[e] *= nk * f;
         xq[e] *= nq * f;
       }
-      st_split8(Lh, Ll, tc::sw128_offset(t, c, 128), xk);
-      st_split8(Lh, Ll, tc::sw128_offset(t + kChunk, c, 128), xq);
+      st_split8(Lh, Ll, tc::sw128_offset(g * 64 + tt, c, 128), xk);
+      st_split8(Lh, Ll, tc::sw128_offset(g * 64 + 32 + tt, c, 128), xq);
     }
-    for (int idx = tid; idx < 16 * 16; idx += blockDim.x) {
-      const int ii = idx >> 4, c = (idx & 15) * 8;
-      const int i = b0 + ii;
+    const int nR = round == 0 ? 64 : 32;
+    for (int idx = tid; idx < nR * 16; idx += kTxThreads) {
+      const int row = idx >> 4, c = (idx & 15) * 8;
+      const int i = round == 0 ? (row & 31) : 32 + row;
+      const int r = round == 0 ? (row < 32 ? 15 : 31) : 47;
       float gi[8], gr[8], x[8];
       ld_f32x8(GM + i * kLd + c, gi);
       ld_f32x8(GM + r * kLd + c, gr);
@@ -658,14 +695,14 @@ __global__ void __launch_bounds__(256, 1) chunk_transform_tc_kernel(const Prefil
       const float nk = rk[i];
 #pragma unroll
       for (int e = 0; e < 8; ++e) x[e] *= nk * __expf(gr[e] - gi[e]);
-      st_split8(Rh, Rl, tc::sw128_offset(ii, c, 16), x);
+      st_split8(Rh, Rl, tc::sw128_offset(row, c, nR), x);
     }
     tc::fence_async_smem();
     tc::tc_fence_before();
     __syncthreads();
     if (tid == 0 && !s_abort) {
       tc::tc_fence_after();
-      constexpr uint32_t idesc = tc::idesc_bf16_f32(128, 16);
+      const uint32_t idesc = round == 0 ? tc::idesc_bf16_f32(128, 64) : tc::idesc_bf16_f32(128, 32);
       const uint32_t ah[3] = {tc::smem_u32(Lh), tc::smem_u32(Lh), tc::smem_u32(Ll)};
       const uint32_t bh[3] = {tc::smem_u32(Rh), tc::smem_u32(Rl), tc::smem_u32(Rh)};
 #pragma unroll
@@ -673,8 +710,9 @@ __global__ void __launch_bounds__(256, 1) chunk_transform_tc_kernel(const Prefil
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const uint32_t koff = (k & 3) * 32;
-          tc::mma_bf16(tmem + b0, tc::sw128_desc(ah[p] + (k >> 2) * (128 * 128) + koff),
-                       tc::sw128_desc(bh[p] + (k >> 2) * (16 * 128) + koff), idesc, p > 0 || k > 0);
+          tc::mma_bf16(tmem + round * 64, tc::sw128_desc(ah[p] + (k >> 2) * (128 * 128) + koff),
+                       tc::sw128_desc(bh[p] + (k >> 2) * (nR * 128) + koff), idesc,
+                       p > 0 || k > 0);
         }
       tc::mma_commit(&mma_bar);
     }
@@ -683,27 +721,34 @@ __global__ void __launch_bounds__(256, 1) chunk_transform_tc_kernel(const Prefil
     tc::tc_fence_after();
   }
 
-  // 4. A (beta-scaled, strictly lower) and P (lower) to FP32; warps 0-3 take
-  //    columns 0-31, warps 4-7 columns 32-63.
+  // 4. A (beta-scaled, strictly lower) and P (lower) to FP32.  TMEM columns:
+  //    0-31  rows 0-63   : t = row & 31 (< 32),  i = col        (k rows 0-31, q rows 32-63)
+  //    32-63 rows 64-127 : t = 32 + (row & 31),  i = col - 32
+  //    64-95 rows 0-63   : t = 32 + (row & 31),  i = 32 + col - 64
+  //    warp group 3 writes the zero block t < 32 <= i.
   {
-    const int row = (warp & 3) * 32 + lane;
-    const int c0 = (warp >> 2) * 32;
-    float d[32];
-    tc::tmem_ld16(tmem + lane_addr + c0, *reinterpret_cast<float(*)[16]>(d));
-    tc::tmem_ld16(tmem + lane_addr + c0 + 16, *reinterpret_cast<float(*)[16]>(d + 16));
-    if (row < kChunk) {
-      const int t = row;
+    const int wg = warp >> 2, row = (warp & 3) * 32 + lane;
+    if (wg < 3) {
+      float d[32];
+      tc::tmem_ld16(tmem + lane_addr + wg * 32, *reinterpret_cast<float(*)[16]>(d));
+      tc::tmem_ld16(tmem + lane_addr + wg * 32 + 16, *reinterpret_cast<float(*)[16]>(d + 16));
+      const bool use = wg == 1 ? row >= 64 : row < 64;
+      if (use) {
+        const int t = (wg == 0 ? 0 : 32) + (row & 31);
+        const int i0 = wg == 2 ? 32 : 0;
+        const bool is_q = (row & 63) >= 32;
+        float* dst = (is_q ? Pf : Af) + t * kLdT + i0;
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        const int i = c0 + e;
-        Af[t * kLdT + i] = i < t ? bt[t] * d[e] : 0.f;
+        for (int e = 0; e < 32; ++e) {
+          const int i = i0 + e;
+          dst[e] = is_q ? (i <= t ? d[e] : 0.f) : (i < t ? bt[t] * d[e] : 0.f);
+        }
       }
     } else {
-      const int t = row - kChunk;
-#pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        const int i = c0 + e;
-        Pf[t * kLdT + i] = i <= t ? d[e] : 0.f;
+      for (int idx = tid - 384; idx < 32 * 32; idx += 128) {
+        const int t = idx >> 5, i = 32 + (idx & 31);
+        Af[t * kLdT + i] = 0.f;
+        Pf[t * kLdT + i] = 0.f;
       }
     }
   }
@@ -712,7 +757,7 @@ __global__ void __launch_bounds__(256, 1) chunk_transform_tc_kernel(const Prefil
 
   // 5. (I + A)^-1, blocked in 16 x 16: diagonal blocks by forward substitution
   //    (one column per thread), then T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj.
-  for (int i = tid; i < kChunk * kLdT; i += blockDim.x) Tf[i] = 0.f;
+  for (int i = tid; i < kChunk * kLdT; i += kTxThreads) Tf[i] = 0.f;
   __syncthreads();
   if (tid < kChunk) {
     const int b0 = (tid >> 4) * 16, col = tid & 15;
@@ -729,7 +774,7 @@ __global__ void __launch_bounds__(256, 1) chunk_transform_tc_kernel(const Prefil
   __syncthreads();
   for (int d = 1; d < 4; ++d) {
     const int npairs = 4 - d;
-    for (int idx = tid; idx < npairs * 256; idx += blockDim.x) {
+    for (int idx = tid; idx < npairs * 256; idx += kTxThreads) {
       const int pr = idx >> 8, r = (idx >> 4) & 15, cc = idx & 15;
       const int bi = pr + d, bj = pr;
       float acc = 0.f;
@@ -740,7 +785,7 @@ __global__ void __launch_bounds__(256, 1) chunk_transform_tc_kernel(const Prefil
       X[pr * 256 + r * 16 + cc] = acc;
     }
     __syncthreads();
-    for (int idx = tid; idx < npairs * 256; idx += blockDim.x) {
+    for (int idx = tid; idx < npairs * 256; idx += kTxThreads) {
       const int pr = idx >> 8, r = (idx >> 4) & 15, cc = idx & 15;
       const int bi = pr + d, bj = pr;
       float acc = 0.f;
@@ -753,7 +798,7 @@ __global__ void __launch_bounds__(256, 1) chunk_transform_tc_kernel(const Prefil
   }
 
   // 6. A2 = [Ti; P Ti] (hi/lo, swizzled 128 x 64); thread -> (row, 8-column chunk)
-  for (int idx = tid; idx < 128 * 8; idx += blockDim.x) {
+  for (int idx = tid; idx < 128 * 8; idx += kTxThreads) {
     const int row = idx >> 3, ch = idx & 7;
     float x[8];
     if (row < kChunk) {
@@ -773,23 +818,16 @@ __global__ void __launch_bounds__(256, 1) chunk_transform_tc_kernel(const Prefil
   }
   __syncthreads();  // A and P (in the L/R region) are dead before B2 overwrites it
   // 7. B2 = [(beta Ktil)^T ; (beta V)^T] (hi/lo, swizzled 256 x 64): row -> channel
-  for (int idx = tid; idx < 256 * 8; idx += blockDim.x) {
+  for (int idx = tid; idx < 256 * 8; idx += kTxThreads) {
     const int row = idx & 255, ch = idx >> 8;
+    const bool kside = row < K;
+    const int c = kside ? row : row - K;
     float x[8];
-    if (row < K) {
-      const int c = row;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int i = ch * 8 + e;
-        x[e] = bt[i] * bf16_at(Ks, i, c) * rk[i] * __expf(GM[i * kLd + c]);
-      }
-    } else {
-      const int c = row - K;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int i = ch * 8 + e;
-        x[e] = i < len ? bt[i] * bf16_bits_to_float(a.v[((t0 + i) * HV + h) * K + c]) : 0.f;
-      }
+    for (int e = 0; e < 8; ++e) {
+      const int i = ch * 8 + e;
+      x[e] = kside ? bt[i] * bf16_at(Ks, i, c) * rk[i] * __expf(GM[i * kLd + c])
+                   : bt[i] * bf16_at(Vs, i, c);
     }
     st_split8(Bh, Bl, tc::sw128_offset(row, ch * 8, 256), x);
   }
@@ -815,15 +853,16 @@ __global__ void __launch_bounds__(256, 1) chunk_transform_tc_kernel(const Prefil
   phase ^= 1;
   tc::tc_fence_after();
 
-  // 9. epilogue: warps 0-3 columns 0-127 (W | P W), warps 4-7 columns 128-255 (Util | P Util)
+  // 9. epilogue: warp group wg takes TMEM columns [64 wg, 64 wg + 64):
+  //    columns 0-127 are W (rows 0-63) | P W (rows 64-127), 128-255 Util | P Util.
   {
-    const int row = (warp & 3) * 32 + lane;
+    const int wg = warp >> 2, row = (warp & 3) * 32 + lane;
     const int t = row & 63;
-    const bool upper = row < kChunk;  // rows 0-63: W, Util; rows 64-127: P W, P Util
-    const bool right = warp >= 4;
-    for (int cb = 0; cb < 8; ++cb) {
+    const bool upper = row < kChunk;
+    const bool right = wg >= 2;
+    for (int cb = 0; cb < 4; ++cb) {
       float d[16];
-      const int c0 = cb * 16;  // column within the half
+      const int c0 = (wg & 1) * 64 + cb * 16;  // column within the half
       tc::tmem_ld16(tmem + lane_addr + (right ? 128 : 0) + c0, d);
       if (!right) {
         if (!upper) {  // Q' = Qtil - P W
@@ -1181,7 +1220,7 @@ extern "C" kda_status kda_prefill(kda_dims dims, kda_gate gate, const kda_bf16* 
     if (getenv("KDA_DEBUG_SIMT_TRANSFORM"))  // TEMPORARY development switch
       chunk_transform_kernel<<<dim3((unsigned)chunks, dims.HV), 256, kTransformSmem, st>>>(args);
     else
-      chunk_transform_tc_kernel<<<dim3((unsigned)chunks, dims.HV), 256, kTransformTcSmem, st>>>(args);
+      chunk_transform_tc_kernel<<<dim3((unsigned)chunks, dims.HV), kTxThreads, kTransformTcSmem, st>>>(args);
     if ((s = launch_status()) != KDA_OK) return s;
   }
   record_stage(1, st);
