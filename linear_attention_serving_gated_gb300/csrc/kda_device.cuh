@@ -47,7 +47,7 @@ __device__ __forceinline__ float4 load_bf16x4(const kda_bf16* p) {
   return r;
 }
 
-__device__ __forceinline__ float sigmoidf_(float x) { return 1.0f / (1.0f + expf(-x)); }
+__device__ __forceinline__ float sigmoidf_(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
 
 // Log-decay of one channel from the gate input (bounded gate), or the input
 // itself when A_log is absent.

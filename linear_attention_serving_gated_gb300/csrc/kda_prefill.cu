@@ -575,6 +575,9 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
     const int c = lane * 4;
     uint2 qr[kTpw], kr[kTpw], vr[kTpw], ar[kTpw];
     float br[kTpw];
+    const float alog = ga.A_log ? __ldg(ga.A_log + h) : 0.f;
+    const float4 bias = ga.dt_bias ? __ldg(reinterpret_cast<const float4*>(ga.dt_bias + h * K + c))
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int u = 0; u < kTpw; ++u) {
       const int t = warp * kTpw + u;
@@ -589,9 +592,7 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
         if (lane == 0) br[u] = bf16_bits_to_float(a.beta[tok * HV + h]);
       }
     }
-    const float exp_alog = ga.A_log ? __expf(ga.A_log[h]) : 0.f;
-    const float4 bias = ga.dt_bias ? *reinterpret_cast<const float4*>(ga.dt_bias + h * K + c)
-                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float exp_alog = __expf(alog);
     float4 run = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int u = 0; u < kTpw; ++u) {
@@ -818,18 +819,25 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
   }
   __syncthreads();  // A and P (in the L/R region) are dead before B2 overwrites it
   // 7. B2 = [(beta Ktil)^T ; (beta V)^T] (hi/lo, swizzled 256 x 64): row -> channel
-  for (int idx = tid; idx < 256 * 8; idx += kTxThreads) {
-    const int row = idx & 255, ch = idx >> 8;
-    const bool kside = row < K;
-    const int c = kside ? row : row - K;
+  for (int idx = tid; idx < K * 8; idx += kTxThreads) {  // rows 0-127: beta_i k-hat_i e^{Gam_i}
+    const int c = idx & (K - 1), ch = idx >> 7;
     float x[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
       const int i = ch * 8 + e;
-      x[e] = kside ? bt[i] * bf16_at(Ks, i, c) * rk[i] * __expf(GM[i * kLd + c])
-                   : bt[i] * bf16_at(Vs, i, c);
+      x[e] = bf16_at(Ks, i, c) * (bt[i] * rk[i]) * __expf(GM[i * kLd + c]);
     }
-    st_split8(Bh, Bl, tc::sw128_offset(row, ch * 8, 256), x);
+    st_split8(Bh, Bl, tc::sw128_offset(c, ch * 8, 256), x);
+  }
+  for (int idx = tid; idx < K * 8; idx += kTxThreads) {  // rows 128-255: beta_i v_i
+    const int c = idx & (K - 1), ch = idx >> 7;
+    float x[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const int i = ch * 8 + e;
+      x[e] = bf16_at(Vs, i, c) * bt[i];
+    }
+    st_split8(Bh, Bl, tc::sw128_offset(K + c, ch * 8, 256), x);
   }
   tc::fence_async_smem();
   tc::tc_fence_before();
@@ -929,7 +937,10 @@ __device__ __forceinline__ void issue_stage_loads(uint8_t* stage, const uint8_t*
   tc::bulk_g2s(stage + kStGam, rec + kRecGam, kHeadDim * 4, bar);
 }
 
-__global__ void __launch_bounds__(128, 1) state_pass_kernel(const PrefillArgs a) {
+constexpr int kPassThreads = 512;  // 4 warps per TMEM lane quadrant
+constexpr int kColsPerThread = kVs / 4;
+
+__global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const PrefillArgs a) {
   extern __shared__ uint8_t smraw[];
   __shared__ uint64_t full_bar[2];
   __shared__ uint64_t mma_bar;
@@ -938,7 +949,10 @@ __global__ void __launch_bounds__(128, 1) state_pass_kernel(const PrefillArgs a)
   __shared__ int s_state, s_abort;
 
   uint8_t* smb = smraw + ((1024u - (tc::smem_u32(smraw) & 1023u)) & 1023u);
-  const int tid = threadIdx.x, warp = tid >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int quad = warp & 3, cg = warp >> 2;  // TMEM lane quadrant, column group
+  const int row = quad * 32 + lane;           // key channel c (D2, S) or row of D1
+  const int j0 = cg * kColsPerThread;         // first of this thread's value columns
   const int n = blockIdx.z, h = blockIdx.y, slice = blockIdx.x, v0 = slice * kVs;
   const int HV = a.HV, K = kHeadDim, V = kHeadDim;
 
@@ -972,7 +986,7 @@ __global__ void __launch_bounds__(128, 1) state_pass_kernel(const PrefillArgs a)
   if (s_state == 2) return;
   const int64_t t0 = s_t0, t1 = s_t1;
   if (s_state == 1) {  // padding sequence: zero outputs
-    for (int64_t idx = tid; idx < (t1 - t0) * kVs; idx += blockDim.x)
+    for (int64_t idx = tid; idx < (t1 - t0) * kVs; idx += kPassThreads)
       a.o[((t0 + idx / kVs) * HV + h) * V + v0 + idx % kVs] = 0;
     return;
   }
@@ -991,21 +1005,21 @@ __global__ void __launch_bounds__(128, 1) state_pass_kernel(const PrefillArgs a)
   }
   if (warp == 0) tc::tmem_alloc(&tmem_base, kTmemCols);
 
-  // state: thread c owns S[c][v0 .. v0+32) in FP32 registers
-  const int c = tid;
-  float S[kVs];
+  // state: thread owns S[row][v0 + j0 .. + 8) in FP32 registers
+  const int c = row;
+  float S[kColsPerThread];
 #pragma unroll
-  for (int j = 0; j < kVs; ++j) S[j] = st[(size_t)(v0 + j) * K + c];
+  for (int jj = 0; jj < kColsPerThread; ++jj) S[jj] = st[(size_t)(v0 + j0 + jj) * K + c];
   uint8_t* Sh = smb + kSmS;
   uint8_t* Sl = Sh + kSmSBytes;
   uint8_t* Uh = smb + kSmU;
   uint8_t* Ul = Uh + kSmUBytes;
   auto write_state_operand = [&]() {
 #pragma unroll
-    for (int j = 0; j < kVs; ++j) {
+    for (int jj = 0; jj < kColsPerThread; ++jj) {
       uint16_t hi, lo;
-      tc::split_bf16(S[j], hi, lo);
-      const uint32_t off = tc::sw128_offset(j, c, kVs);
+      tc::split_bf16(S[jj], hi, lo);
+      const uint32_t off = tc::sw128_offset(j0 + jj, c, kVs);
       *reinterpret_cast<uint16_t*>(Sh + off) = hi;
       *reinterpret_cast<uint16_t*>(Sl + off) = lo;
     }
@@ -1017,7 +1031,7 @@ __global__ void __launch_bounds__(128, 1) state_pass_kernel(const PrefillArgs a)
   tc::tc_fence_after();
   const uint32_t tmem = tmem_base;
   const uint32_t d1 = tmem, d2 = tmem + kVs;
-  const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
+  const uint32_t lane_addr = (static_cast<uint32_t>(quad * 32) << 16) + j0;
   constexpr uint32_t idesc = tc::idesc_bf16_f32(128, kVs);
   const float scale = a.gate.scale;
   uint32_t mma_phase = 0;
@@ -1031,7 +1045,7 @@ __global__ void __launch_bounds__(128, 1) state_pass_kernel(const PrefillArgs a)
     if (a.intermediate) {
       float* dst = a.intermediate + ((size_t)cid * HV + h) * V * K;
 #pragma unroll
-      for (int j = 0; j < kVs; ++j) dst[(size_t)(v0 + j) * K + c] = S[j];
+      for (int jj = 0; jj < kColsPerThread; ++jj) dst[(size_t)(v0 + j0 + jj) * K + c] = S[jj];
     }
     if (tc::mbar_wait(&full_bar[sidx], (ci >> 1) & 1))
       consumed = ci + 1;
@@ -1058,35 +1072,31 @@ __global__ void __launch_bounds__(128, 1) state_pass_kernel(const PrefillArgs a)
     mma_phase ^= 1;
     tc::tc_fence_after();
     {
-      float d[kVs];
-      tc::tmem_ld16(d1 + lane_addr, *reinterpret_cast<float(*)[16]>(d));
-      tc::tmem_ld16(d1 + lane_addr + 16, *reinterpret_cast<float(*)[16]>(d + 16));
-      if (warp < 2) {  // rows 0..63: U = Util - W S  ->  U^T hi/lo operand
-        const int t = tid;
-        const float* ut = reinterpret_cast<const float*>(stage + kStU) + t * kVs;
+      float d[kColsPerThread];
+      tc::tmem_ld8(d1 + lane_addr, d);
+      if (quad < 2) {  // rows 0..63: U = Util - W S  ->  U^T hi/lo operand
+        const int t = row;
+        const float4* ut = reinterpret_cast<const float4*>(stage + kStU + (t * kVs + j0) * 4);
+        const float4 u0 = ut[0], u1 = ut[1];
+        const float uu[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
 #pragma unroll
-        for (int j = 0; j < kVs; ++j) {
+        for (int jj = 0; jj < kColsPerThread; ++jj) {
           uint16_t hi, lo;
-          tc::split_bf16(ut[j] - d[j], hi, lo);
-          const uint32_t off = tc::sw128_offset(j, t, kVs);
+          tc::split_bf16(uu[jj] - d[jj], hi, lo);
+          const uint32_t off = tc::sw128_offset(j0 + jj, t, kVs);
           *reinterpret_cast<uint16_t*>(Uh + off) = hi;
           *reinterpret_cast<uint16_t*>(Ul + off) = lo;
         }
       } else {  // rows 64..127: O = scale (Q' S + P Util)
-        const int t = tid - kChunk;
+        const int t = row - kChunk;
         if (t < len) {
-          const float* oi = reinterpret_cast<const float*>(stage + kStOi) + t * kVs;
-          uint4* dst = reinterpret_cast<uint4*>(a.o + ((tc0 + t) * HV + h) * V + v0);
-#pragma unroll
-          for (int q4 = 0; q4 < kVs / 8; ++q4) {
-            uint32_t w[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int j = q4 * 8 + e * 2;
-              w[e] = pack_bf16x2(scale * (d[j] + oi[j]), scale * (d[j + 1] + oi[j + 1]));
-            }
-            dst[q4] = make_uint4(w[0], w[1], w[2], w[3]);
-          }
+          const float4* oi = reinterpret_cast<const float4*>(stage + kStOi + (t * kVs + j0) * 4);
+          const float4 o0 = oi[0], o1 = oi[1];
+          const uint4 w = make_uint4(pack_bf16x2(scale * (d[0] + o0.x), scale * (d[1] + o0.y)),
+                                     pack_bf16x2(scale * (d[2] + o0.z), scale * (d[3] + o0.w)),
+                                     pack_bf16x2(scale * (d[4] + o1.x), scale * (d[5] + o1.y)),
+                                     pack_bf16x2(scale * (d[6] + o1.z), scale * (d[7] + o1.w)));
+          *reinterpret_cast<uint4*>(a.o + ((tc0 + t) * HV + h) * V + v0 + j0) = w;
         }
       }
     }
@@ -1111,12 +1121,11 @@ __global__ void __launch_bounds__(128, 1) state_pass_kernel(const PrefillArgs a)
     mma_phase ^= 1;
     tc::tc_fence_after();
     {
-      float d[kVs];
-      tc::tmem_ld16(d2 + lane_addr, *reinterpret_cast<float(*)[16]>(d));
-      tc::tmem_ld16(d2 + lane_addr + 16, *reinterpret_cast<float(*)[16]>(d + 16));
+      float d[kColsPerThread];
+      tc::tmem_ld8(d2 + lane_addr, d);
       const float gc = reinterpret_cast<const float*>(stage + kStGam)[c];
 #pragma unroll
-      for (int j = 0; j < kVs; ++j) S[j] = gc * S[j] + d[j];
+      for (int jj = 0; jj < kColsPerThread; ++jj) S[jj] = gc * S[jj] + d[jj];
     }
     write_state_operand();
     tc::fence_async_smem();
@@ -1138,7 +1147,7 @@ __global__ void __launch_bounds__(128, 1) state_pass_kernel(const PrefillArgs a)
     }
   } else {
 #pragma unroll
-    for (int j = 0; j < kVs; ++j) st[(size_t)(v0 + j) * K + c] = S[j];
+    for (int jj = 0; jj < kColsPerThread; ++jj) st[(size_t)(v0 + j0 + jj) * K + c] = S[jj];
   }
   tc::tc_fence_before();
   __syncthreads();
@@ -1224,7 +1233,7 @@ extern "C" kda_status kda_prefill(kda_dims dims, kda_gate gate, const kda_bf16* 
     if ((s = launch_status()) != KDA_OK) return s;
   }
   record_stage(1, st);
-  state_pass_kernel<<<dim3(kSlices, dims.HV, num_seqs), 128, kPassSmem, st>>>(args);
+  state_pass_kernel<<<dim3(kSlices, dims.HV, num_seqs), kPassThreads, kPassSmem, st>>>(args);
   s = launch_status();
   record_stage(2, st);
   return s;
