@@ -47,10 +47,12 @@
 //                           sequential over the sequence's chunks, on tcgen05:
 //                           per chunk one bulk copy of the record into shared
 //                           memory (double-buffered, mbarrier completion), then
-//                             D1 = [W; Q'] [S_hi | S_lo]      (TMEM, M=128, N=32)
+//                             D1 = [W; Q'] [S_hi | S_lo]      (TMEM, M=128, N=2x32)
 //                             U  = Util - D1[0:64],  O = scale (D1[64:128] + P Util)
-//                             D2 = Khat^T U  (hi/lo x hi/lo, three products)
+//                             D2 = Khat_hi^T [U_hi | U_lo] + Khat_lo^T U_hi
 //                             S  = Diag(gamma) S + D2
+//                           (the hi and lo halves sit side by side along N and
+//                           are summed in the epilogues)
 //                           with S kept in FP32 registers (one key channel per
 //                           thread) and re-split into BF16 hi/lo operands.
 #include <stdlib.h>
@@ -917,13 +919,13 @@ constexpr uint32_t kStU = kStKTl + 128 * 64 * 2;
 constexpr uint32_t kStOi = kStU + kSliceBytes;
 constexpr uint32_t kStGam = kStOi + kSliceBytes;
 constexpr uint32_t kStageBytes = ((kStGam + kHeadDim * 4 + 1023) / 1024) * 1024;
-constexpr uint32_t kSmS = 2 * kStageBytes;       // S^T hi, lo: 32 x 128 each
-constexpr uint32_t kSmSBytes = kVs * kHeadDim * 2;
-constexpr uint32_t kSmU = kSmS + 2 * kSmSBytes;  // U^T hi, lo: 32 x 64 each
-constexpr uint32_t kSmUBytes = kVs * kChunk * 2;
-constexpr uint32_t kPassSmem = kSmU + 2 * kSmUBytes + 1024;  // + alignment slack
+constexpr uint32_t kSmS = 2 * kStageBytes;         // [S_hi; S_lo]^T: 64 x 128 (rows j, 32 + j)
+constexpr uint32_t kSmSBytes = 2 * kVs * kHeadDim * 2;
+constexpr uint32_t kSmU = kSmS + kSmSBytes;        // [U_hi; U_lo]^T: 64 x 64
+constexpr uint32_t kSmUBytes = 2 * kVs * kChunk * 2;
+constexpr uint32_t kPassSmem = kSmU + kSmUBytes + 1024;  // + alignment slack
 constexpr uint32_t kStageTx = 128 * 128 * 2 + 2 * 128 * 64 * 2 + 2 * kSliceBytes + kHeadDim * 4;
-constexpr uint32_t kTmemCols = 64;  // D1: cols 0-31, D2: cols 32-63
+constexpr uint32_t kTmemCols = 128;  // D1: cols 0-63 (hi | lo), D2: cols 64-127
 static_assert(kStKTl == kStKTh + 128 * 64 * 2 && kRecKTl == kRecKTh + 128 * 64 * 2,
               "Khat^T hi and lo are copied as one block");
 
@@ -1010,18 +1012,15 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
   float S[kColsPerThread];
 #pragma unroll
   for (int jj = 0; jj < kColsPerThread; ++jj) S[jj] = st[(size_t)(v0 + j0 + jj) * K + c];
-  uint8_t* Sh = smb + kSmS;
-  uint8_t* Sl = Sh + kSmSBytes;
-  uint8_t* Uh = smb + kSmU;
-  uint8_t* Ul = Uh + kSmUBytes;
+  uint8_t* S2 = smb + kSmS;
+  uint8_t* U2 = smb + kSmU;
   auto write_state_operand = [&]() {
 #pragma unroll
     for (int jj = 0; jj < kColsPerThread; ++jj) {
       uint16_t hi, lo;
       tc::split_bf16(S[jj], hi, lo);
-      const uint32_t off = tc::sw128_offset(j0 + jj, c, kVs);
-      *reinterpret_cast<uint16_t*>(Sh + off) = hi;
-      *reinterpret_cast<uint16_t*>(Sl + off) = lo;
+      *reinterpret_cast<uint16_t*>(S2 + tc::sw128_offset(j0 + jj, c, 2 * kVs)) = hi;
+      *reinterpret_cast<uint16_t*>(S2 + tc::sw128_offset(kVs + j0 + jj, c, 2 * kVs)) = lo;
     }
   };
   write_state_operand();
@@ -1030,9 +1029,10 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = tmem_base;
-  const uint32_t d1 = tmem, d2 = tmem + kVs;
+  const uint32_t d1 = tmem, d2 = tmem + 2 * kVs;
   const uint32_t lane_addr = (static_cast<uint32_t>(quad * 32) << 16) + j0;
-  constexpr uint32_t idesc = tc::idesc_bf16_f32(128, kVs);
+  constexpr uint32_t idesc2 = tc::idesc_bf16_f32(128, 2 * kVs);
+  constexpr uint32_t idesc1 = tc::idesc_bf16_f32(128, kVs);
   const float scale = a.gate.scale;
   uint32_t mma_phase = 0;
 
@@ -1051,30 +1051,28 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
       consumed = ci + 1;
     else
       s_abort = 1;
-    // D1 = [W; Q'] (S_hi + S_lo): two passes of eight K=16 steps
+    // D1 = [W; Q'] [S_hi | S_lo]: eight K=16 steps, N = 64
     if (tid == 0 && !s_abort) {
       tc::tc_fence_after();
-      const uint32_t a1 = tc::smem_u32(stage + kStA1);
+      const uint32_t a1 = tc::smem_u32(stage + kStA1), sb2 = tc::smem_u32(S2);
 #pragma unroll
-      for (int p = 0; p < 2; ++p) {
-        const uint32_t bbase = tc::smem_u32(p == 0 ? Sh : Sl);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint32_t koff = (k & 3) * 32;
-          const uint64_t ad = tc::sw128_desc(a1 + (k >> 2) * (128 * 128) + koff);
-          const uint64_t bd = tc::sw128_desc(bbase + (k >> 2) * (kVs * 128) + koff);
-          tc::mma_bf16(d1, ad, bd, idesc, p > 0 || k > 0);
-        }
+      for (int k = 0; k < 8; ++k) {
+        const uint32_t koff = (k & 3) * 32;
+        const uint64_t ad = tc::sw128_desc(a1 + (k >> 2) * (128 * 128) + koff);
+        const uint64_t bd = tc::sw128_desc(sb2 + (k >> 2) * (2 * kVs * 128) + koff);
+        tc::mma_bf16(d1, ad, bd, idesc2, k > 0);
       }
       tc::mma_commit(&mma_bar);
     }
     if (!tc::mbar_wait(&mma_bar, mma_phase)) s_abort = 1;
     mma_phase ^= 1;
     tc::tc_fence_after();
+    uint4 o_pack = make_uint4(0u, 0u, 0u, 0u);  // this thread's O, stored after the barrier
     {
-      float d[kColsPerThread];
-      tc::tmem_ld8(d1 + lane_addr, d);
-      if (quad < 2) {  // rows 0..63: U = Util - W S  ->  U^T hi/lo operand
+      float dh[kColsPerThread], dl[kColsPerThread];
+      tc::tmem_ld8(d1 + lane_addr, dh);
+      tc::tmem_ld8(d1 + lane_addr + kVs, dl);
+      if (quad < 2) {  // rows 0..63: U = Util - W S  ->  [U_hi; U_lo]^T operand
         const int t = row;
         const float4* ut = reinterpret_cast<const float4*>(stage + kStU + (t * kVs + j0) * 4);
         const float4 u0 = ut[0], u1 = ut[1];
@@ -1082,50 +1080,50 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
 #pragma unroll
         for (int jj = 0; jj < kColsPerThread; ++jj) {
           uint16_t hi, lo;
-          tc::split_bf16(uu[jj] - d[jj], hi, lo);
-          const uint32_t off = tc::sw128_offset(j0 + jj, t, kVs);
-          *reinterpret_cast<uint16_t*>(Uh + off) = hi;
-          *reinterpret_cast<uint16_t*>(Ul + off) = lo;
+          tc::split_bf16(uu[jj] - (dh[jj] + dl[jj]), hi, lo);
+          *reinterpret_cast<uint16_t*>(U2 + tc::sw128_offset(j0 + jj, t, 2 * kVs)) = hi;
+          *reinterpret_cast<uint16_t*>(U2 + tc::sw128_offset(kVs + j0 + jj, t, 2 * kVs)) = lo;
         }
       } else {  // rows 64..127: O = scale (Q' S + P Util)
         const int t = row - kChunk;
-        if (t < len) {
-          const float4* oi = reinterpret_cast<const float4*>(stage + kStOi + (t * kVs + j0) * 4);
-          const float4 o0 = oi[0], o1 = oi[1];
-          const uint4 w = make_uint4(pack_bf16x2(scale * (d[0] + o0.x), scale * (d[1] + o0.y)),
-                                     pack_bf16x2(scale * (d[2] + o0.z), scale * (d[3] + o0.w)),
-                                     pack_bf16x2(scale * (d[4] + o1.x), scale * (d[5] + o1.y)),
-                                     pack_bf16x2(scale * (d[6] + o1.z), scale * (d[7] + o1.w)));
-          *reinterpret_cast<uint4*>(a.o + ((tc0 + t) * HV + h) * V + v0 + j0) = w;
-        }
+        const float4* oi = reinterpret_cast<const float4*>(stage + kStOi + (t * kVs + j0) * 4);
+        const float4 o0 = oi[0], o1 = oi[1];
+        const float oo[8] = {o0.x, o0.y, o0.z, o0.w, o1.x, o1.y, o1.z, o1.w};
+        float x[8];
+#pragma unroll
+        for (int jj = 0; jj < kColsPerThread; ++jj) x[jj] = scale * (dh[jj] + dl[jj] + oo[jj]);
+        o_pack = make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]),
+                            pack_bf16x2(x[4], x[5]), pack_bf16x2(x[6], x[7]));
       }
     }
     tc::fence_async_smem();
     tc::tc_fence_before();
     __syncthreads();
-    // D2 = Khat^T U with hi/lo splits: hi*hi + hi*lo + lo*hi, four K=16 steps each
+    if (quad >= 2 && row - kChunk < len)
+      *reinterpret_cast<uint4*>(a.o + ((tc0 + row - kChunk) * HV + h) * V + v0 + j0) = o_pack;
+    // D2 = Khat_hi^T [U_hi | U_lo] + Khat_lo^T U_hi (into the U_hi half): 4 + 4 K=16 steps
     if (tid == 0 && !s_abort) {
       tc::tc_fence_after();
       const uint32_t kth = tc::smem_u32(stage + kStKTh), ktl = tc::smem_u32(stage + kStKTl);
-      const uint32_t uh = tc::smem_u32(Uh), ul = tc::smem_u32(Ul);
-      const uint32_t as[3] = {kth, kth, ktl}, bs[3] = {uh, ul, uh};
+      const uint32_t ub = tc::smem_u32(U2);
 #pragma unroll
-      for (int p = 0; p < 3; ++p)
+      for (int k = 0; k < 4; ++k)
+        tc::mma_bf16(d2, tc::sw128_desc(kth + k * 32), tc::sw128_desc(ub + k * 32), idesc2, k > 0);
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          tc::mma_bf16(d2, tc::sw128_desc(as[p] + k * 32), tc::sw128_desc(bs[p] + k * 32), idesc,
-                       p > 0 || k > 0);
+      for (int k = 0; k < 4; ++k)
+        tc::mma_bf16(d2, tc::sw128_desc(ktl + k * 32), tc::sw128_desc(ub + k * 32), idesc1, true);
       tc::mma_commit(&mma_bar);
     }
     if (!tc::mbar_wait(&mma_bar, mma_phase)) s_abort = 1;
     mma_phase ^= 1;
     tc::tc_fence_after();
     {
-      float d[kColsPerThread];
-      tc::tmem_ld8(d2 + lane_addr, d);
+      float dh[kColsPerThread], dl[kColsPerThread];
+      tc::tmem_ld8(d2 + lane_addr, dh);
+      tc::tmem_ld8(d2 + lane_addr + kVs, dl);
       const float gc = reinterpret_cast<const float*>(stage + kStGam)[c];
 #pragma unroll
-      for (int jj = 0; jj < kColsPerThread; ++jj) S[jj] = gc * S[jj] + d[jj];
+      for (int jj = 0; jj < kColsPerThread; ++jj) S[jj] = gc * S[jj] + (dh[jj] + dl[jj]);
     }
     write_state_operand();
     tc::fence_async_smem();
