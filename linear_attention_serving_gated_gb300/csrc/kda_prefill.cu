@@ -71,7 +71,10 @@ constexpr int kSlices = kHeadDim / kVs;
 
 // Workspace record of one (chunk, head), bytes.  Tiles are BF16, K-major,
 // 128-byte swizzled (see kda_tc.cuh) so they can be bulk-copied straight into
-// shared memory; Util and P Util are FP32, V-slice-major [slice][64][kVs].
+// shared memory; Util and P Util are FP32 in [slice][column quad][64][4]
+// order (slice = 32 value columns), so that a thread reading one token's four
+// columns and its neighbours reading the next tokens touch consecutive
+// 16-byte words.
 constexpr uint32_t kRecA1 = 0;                                // [W; Q'] 128 x 128
 constexpr uint32_t kRecKTh = kRecA1 + 128 * 128 * 2;          // Khat^T hi, 128 x 64
 constexpr uint32_t kRecKTl = kRecKTh + 128 * 64 * 2;          // Khat^T lo
@@ -398,6 +401,7 @@ __global__ void __launch_bounds__(256) chunk_transform_kernel(const PrefillArgs 
     float* oi_out = reinterpret_cast<float*>(rec + kRecOi) + slice * (kChunk * kVs);
     for (int t = warp; t < kChunk; t += 8) {
       float4 pw = make_float4(0.f, 0.f, 0.f, 0.f), pu = pw;
+      const int qd = cs / 4;  // column quad inside the slice
       for (int i = 0; i <= t; ++i) {
         const float p = Pm[t * kLdT + i];
         const float4 w = f4(KQ + i * kLd + c), u = f4(GM + i * kLd + c);
@@ -406,8 +410,8 @@ __global__ void __launch_bounds__(256) chunk_transform_kernel(const PrefillArgs 
       }
       float4& qq = f4(QQ + t * kLd + c);
       qq = make_float4(qq.x - pw.x, qq.y - pw.y, qq.z - pw.z, qq.w - pw.w);
-      *reinterpret_cast<float4*>(oi_out + t * kVs + cs) = pu;
-      *reinterpret_cast<float4*>(ut_out + t * kVs + cs) = f4(GM + t * kLd + c);
+      *reinterpret_cast<float4*>(oi_out + qd * (kChunk * 4) + t * 4) = pu;
+      *reinterpret_cast<float4*>(ut_out + qd * (kChunk * 4) + t * 4) = f4(GM + t * kLd + c);
     }
   }
   __syncthreads();
@@ -442,7 +446,7 @@ constexpr size_t kTransformSmem =
 // Both products use BF16 hi/lo splits of both operands (three MMAs each).
 
 constexpr int kLdB = 136;       // padded row stride (BF16 elements) of the raw q, k, v tiles
-constexpr int kTxThreads = 512;
+constexpr int kTxThreads = 1024;
 constexpr int kTxWarps = kTxThreads / 32;
 
 constexpr uint32_t kTxL = 0;                          // L hi, lo: 128 x 128 each
@@ -748,7 +752,7 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
         }
       }
     } else {
-      for (int idx = tid - 384; idx < 32 * 32; idx += 128) {
+      for (int idx = tid - 384; idx < 32 * 32; idx += kTxThreads - 384) {
         const int t = idx >> 5, i = 32 + (idx & 31);
         Af[t * kLdT + i] = 0.f;
         Pf[t * kLdT + i] = 0.f;
@@ -863,16 +867,18 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
   phase ^= 1;
   tc::tc_fence_after();
 
-  // 9. epilogue: warp group wg takes TMEM columns [64 wg, 64 wg + 64):
-  //    columns 0-127 are W (rows 0-63) | P W (rows 64-127), 128-255 Util | P Util.
+  // 9. epilogue: warp group wg (four warps, one per TMEM lane quadrant) takes
+  //    256 / kGroups consecutive TMEM columns: columns 0-127 are W (rows 0-63) |
+  //    P W (rows 64-127), 128-255 Util | P Util.
   {
+    constexpr int kGroups = kTxWarps / 4, kCols = 256 / kGroups;
     const int wg = warp >> 2, row = (warp & 3) * 32 + lane;
     const int t = row & 63;
     const bool upper = row < kChunk;
-    const bool right = wg >= 2;
-    for (int cb = 0; cb < 4; ++cb) {
+    const bool right = wg >= kGroups / 2;
+    for (int cb = 0; cb < kCols / 16; ++cb) {
       float d[16];
-      const int c0 = (wg & 1) * 64 + cb * 16;  // column within the half
+      const int c0 = (wg % (kGroups / 2)) * kCols + cb * 16;  // column within the half
       tc::tmem_ld16(tmem + lane_addr + (right ? 128 : 0) + c0, d);
       if (!right) {
         if (!upper) {  // Q' = Qtil - P W
@@ -894,11 +900,13 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
           *reinterpret_cast<uint4*>(rec + kRecA1 + tc::sw128_offset(row, c0 + half * 8, 128)) = pk;
         }
       } else {
-        const int slice = c0 / kVs, cs = c0 % kVs;
-        float* dst = reinterpret_cast<float*>(rec + (upper ? kRecU : kRecOi)) +
-                     slice * (kChunk * kVs) + t * kVs + cs;
+        float* base = reinterpret_cast<float*>(rec + (upper ? kRecU : kRecOi));
 #pragma unroll
-        for (int e = 0; e < 16; e += 4) f4(dst + e) = make_float4(d[e], d[e + 1], d[e + 2], d[e + 3]);
+        for (int e = 0; e < 16; e += 4) {  // column quad (c0 + e) / 4
+          const int col = c0 + e;
+          f4(base + (col / kVs) * (kChunk * kVs) + ((col % kVs) / 4) * (kChunk * 4) + t * 4) =
+              make_float4(d[e], d[e + 1], d[e + 2], d[e + 3]);
+        }
       }
     }
   }
@@ -998,9 +1006,9 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
   const uint8_t* ws_head = a.ws + ((size_t)s_cbase * HV + h) * kRecBytes;
   const size_t rec_stride = (size_t)HV * kRecBytes;
 
-  int issued = 0;    // chunks whose loads have been issued (thread 0)
+  int issued = 0;    // chunks whose loads have been issued (thread 32)
   int consumed = 0;  // chunks whose loads have landed
-  if (tid == 0) {
+  if (tid == 32) {
     for (; issued < 2 && issued < nch; ++issued)
       issue_stage_loads(smb + issued * kStageBytes, ws_head + issued * rec_stride, slice,
                         &full_bar[issued]);
@@ -1074,8 +1082,8 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
       tc::tmem_ld8(d1 + lane_addr + kVs, dl);
       if (quad < 2) {  // rows 0..63: U = Util - W S  ->  [U_hi; U_lo]^T operand
         const int t = row;
-        const float4* ut = reinterpret_cast<const float4*>(stage + kStU + (t * kVs + j0) * 4);
-        const float4 u0 = ut[0], u1 = ut[1];
+        const float4* ut = reinterpret_cast<const float4*>(stage + kStU) + (j0 / 4) * kChunk + t;
+        const float4 u0 = ut[0], u1 = ut[kChunk];
         const float uu[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
 #pragma unroll
         for (int jj = 0; jj < kColsPerThread; ++jj) {
@@ -1086,8 +1094,8 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
         }
       } else {  // rows 64..127: O = scale (Q' S + P Util)
         const int t = row - kChunk;
-        const float4* oi = reinterpret_cast<const float4*>(stage + kStOi + (t * kVs + j0) * 4);
-        const float4 o0 = oi[0], o1 = oi[1];
+        const float4* oi = reinterpret_cast<const float4*>(stage + kStOi) + (j0 / 4) * kChunk + t;
+        const float4 o0 = oi[0], o1 = oi[kChunk];
         const float oo[8] = {o0.x, o0.y, o0.z, o0.w, o1.x, o1.y, o1.z, o1.w};
         float x[8];
 #pragma unroll
@@ -1130,15 +1138,15 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
     tc::tc_fence_before();
     __syncthreads();
     if (s_abort) break;
-    if (tid == 0 && ci + 2 < nch) {
+    if (tid == 32 && ci + 2 < nch) {  // not the MMA-issuing thread
       tc::fence_async_smem();
       issue_stage_loads(stage, ws_head + (size_t)(ci + 2) * rec_stride, slice, &full_bar[sidx]);
       issued = ci + 3;
     }
   }
   if (s_abort) {
-    if (tid == 0) {
-      set_error(a.err_flag, KDA_DEVERR_TIMEOUT);
+    if (tid == 0) set_error(a.err_flag, KDA_DEVERR_TIMEOUT);
+    if (tid == 32) {
       // let the bulk copies this CTA still has in flight land before it exits
       for (int cj = consumed; cj < issued; ++cj)
         tc::mbar_wait(&full_bar[cj & 1], (cj >> 1) & 1, 1u << 20);
