@@ -49,6 +49,11 @@ __device__ __forceinline__ float4 load_bf16x4(const kda_bf16* p) {
 
 __device__ __forceinline__ float sigmoidf_(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
 
+// exp(x) for decay factors.  Results below the smallest normal FP32 value
+// (x < -87) are flushed to zero instead of being produced as denormals: such
+// factors multiply O(1) terms into nothing, and the denormal results are slow.
+__device__ __forceinline__ float decay_exp(float x) { return x < -87.0f ? 0.0f : __expf(x); }
+
 // Log-decay of one channel from the gate input (bounded gate), or the input
 // itself when A_log is absent.
 __device__ __forceinline__ float gate_log_decay(const GateArgs& ga, float a_in, float exp_alog,

@@ -639,7 +639,7 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
   __syncthreads();
 
   // 2. gamma and Khat^T (hi/lo, swizzled 128 x 64) straight to the workspace
-  if (tid < K) reinterpret_cast<float*>(rec + kRecGam)[tid] = __expf(GM[(kChunk - 1) * kLd + tid]);
+  if (tid < K) reinterpret_cast<float*>(rec + kRecGam)[tid] = decay_exp(GM[(kChunk - 1) * kLd + tid]);
   for (int idx = tid; idx < K * 8; idx += kTxThreads) {
     const int c = idx & (K - 1), j = idx >> 7;
     const float gl = GM[(kChunk - 1) * kLd + c];
@@ -647,7 +647,7 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
       const int t = j * 8 + e;
-      x[e] = bf16_at(Ks, t, c) * rk[t] * __expf(gl - GM[t * kLd + c]);
+      x[e] = bf16_at(Ks, t, c) * rk[t] * decay_exp(gl - GM[t * kLd + c]);
     }
     st_split8(rec + kRecKTh, rec + kRecKTl, tc::sw128_offset(c, j * 8, K), x);
   }
@@ -683,7 +683,7 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
       const float nk = rk[t], nq = rq[t];
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        const float f = __expf(gt[e] - gr[e]);
+        const float f = decay_exp(gt[e] - gr[e]);
         xk[e] *= nk * f;
         xq[e] *= nq * f;
       }
@@ -701,7 +701,7 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
       ld_bf16x8(Ks, i, c, x);
       const float nk = rk[i];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) x[e] *= nk * __expf(gr[e] - gi[e]);
+      for (int e = 0; e < 8; ++e) x[e] *= nk * decay_exp(gr[e] - gi[e]);
       st_split8(Rh, Rl, tc::sw128_offset(row, c, nR), x);
     }
     tc::fence_async_smem();
@@ -831,7 +831,7 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
       const int i = ch * 8 + e;
-      x[e] = bf16_at(Ks, i, c) * (bt[i] * rk[i]) * __expf(GM[i * kLd + c]);
+      x[e] = bf16_at(Ks, i, c) * (bt[i] * rk[i]) * decay_exp(GM[i * kLd + c]);
     }
     st_split8(Bh, Bl, tc::sw128_offset(c, ch * 8, 256), x);
   }
@@ -889,7 +889,7 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
             ld_f32x8(GM + t * kLd + c0 + hh * 8, g8);
             const float nq = rq[t];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) d[hh * 8 + e] = q8[e] * nq * __expf(g8[e]) - d[hh * 8 + e];
+            for (int e = 0; e < 8; ++e) d[hh * 8 + e] = q8[e] * nq * decay_exp(g8[e]) - d[hh * 8 + e];
           }
         }
 #pragma unroll
