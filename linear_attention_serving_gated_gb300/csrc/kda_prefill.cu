@@ -804,26 +804,61 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
     __syncthreads();
   }
 
-  // 6. A2 = [Ti; P Ti] (hi/lo, swizzled 128 x 64); thread -> (row, 8-column chunk)
-  for (int idx = tid; idx < 128 * 8; idx += kTxThreads) {
-    const int row = idx >> 3, ch = idx & 7;
-    float x[8];
-    if (row < kChunk) {
+  // 6. A2 = [Ti; P Ti] on the tensor core: D = [I; P] Ti, M=128 N=64 K=64.
+  //    Operands: X = [I; P] (128 x 64, K = i) in the R region, Ti^T (64 x 64,
+  //    rows j, K = i) over the dead A block; both hi/lo.  The result lands in
+  //    TMEM columns 128-191 and is split into A2 (hi/lo) by all warps.
+  {
+    uint8_t* Xh = Rh;                     // 128 x 64, 16 KB each half
+    uint8_t* Xl = Xh + 128 * 64 * 2;
+    uint8_t* Th = sb + kTxAf;             // 64 x 64, 8 KB each half
+    uint8_t* Tl = Th + 64 * 64 * 2;
+    for (int idx = tid; idx < 128 * 8 + 64 * 8; idx += kTxThreads) {
+      float x[8];
+      if (idx < 128 * 8) {                // X rows: identity (0-63) or P (64-127)
+        const int row = idx >> 3, ch = idx & 7;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) x[e] = Tf[row * kLdT + ch * 8 + e];
-    } else {
-      const int t = row - kChunk;
+        for (int e = 0; e < 8; ++e)
+          x[e] = row < kChunk ? (ch * 8 + e == row ? 1.f : 0.f) : Pf[(row - kChunk) * kLdT + ch * 8 + e];
+        st_split8(Xh, Xl, tc::sw128_offset(row, ch * 8, 128), x);
+      } else {                            // Ti^T rows j
+        const int j = (idx - 128 * 8) >> 3, ch = (idx - 128 * 8) & 7;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) x[e] = 0.f;
-      for (int i = ch * 8; i <= t; ++i) {
-        const float p = Pf[t * kLdT + i];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) x[e] += p * Tf[i * kLdT + ch * 8 + e];
+        for (int e = 0; e < 8; ++e) x[e] = Tf[(ch * 8 + e) * kLdT + j];
+        st_split8(Th, Tl, tc::sw128_offset(j, ch * 8, 64), x);
       }
     }
-    st_split8(A2h, A2l, tc::sw128_offset(row, ch * 8, 128), x);
+    tc::fence_async_smem();
+    tc::tc_fence_before();
+    __syncthreads();
+    if (tid == 0 && !s_abort) {
+      tc::tc_fence_after();
+      constexpr uint32_t idesc = tc::idesc_bf16_f32(128, 64);
+      const uint32_t ah[3] = {tc::smem_u32(Xh), tc::smem_u32(Xh), tc::smem_u32(Xl)};
+      const uint32_t bh[3] = {tc::smem_u32(Th), tc::smem_u32(Tl), tc::smem_u32(Th)};
+#pragma unroll
+      for (int p = 0; p < 3; ++p)
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          tc::mma_bf16(tmem + 128, tc::sw128_desc(ah[p] + k * 32), tc::sw128_desc(bh[p] + k * 32),
+                       idesc, p > 0 || k > 0);
+      tc::mma_commit(&mma_bar);
+    }
+    if (!tc::mbar_wait(&mma_bar, phase)) s_abort = 1;
+    phase ^= 1;
+    tc::tc_fence_after();
+    // TMEM -> A2: warp group g takes 8 of the 64 columns
+    {
+      const int row = (warp & 3) * 32 + lane, c0 = (warp >> 2) * (64 / (kTxWarps / 4));
+      for (int cc = 0; cc < 64 / (kTxWarps / 4); cc += 8) {
+        float d[8];
+        tc::tmem_ld8(tmem + lane_addr + 128 + c0 + cc, d);
+        st_split8(A2h, A2l, tc::sw128_offset(row, c0 + cc, 128), d);
+      }
+    }
   }
-  __syncthreads();  // A and P (in the L/R region) are dead before B2 overwrites it
+  tc::tc_fence_before();
+  __syncthreads();  // X, Ti^T (L/R region) are dead before B2 overwrites it
   // 7. B2 = [(beta Ktil)^T ; (beta V)^T] (hi/lo, swizzled 256 x 64): row -> channel
   for (int idx = tid; idx < K * 8; idx += kTxThreads) {  // rows 0-127: beta_i k-hat_i e^{Gam_i}
     const int c = idx & (K - 1), ch = idx >> 7;
