@@ -178,6 +178,37 @@ kda_status kda_commit(kda_dims dims, const float *snapshots, int B, int T,
                       const int32_t *state_idx, int32_t *err_flag, void *stream);
 
 /*
+ * kda_prefill without a caller-provided workspace.  The pages have no
+ * counterpart to this entry point; it exists for callers that cannot
+ * allocate device memory: a host whose whole device memory already belongs
+ * to its own pools, code issuing the call while a CUDA graph is being
+ * captured (cudaMalloc is not allowed there), or a plugin that only receives
+ * tensors through this ABI and has no allocator.  It allocates nothing
+ * (no cudaMalloc, no cudaFree, no allocating library call).
+ *
+ * Its scratch is a file-scope static device array of
+ * KDA_PREFILL_STATIC_SCRATCH_BYTES that every GPU loading the library keeps
+ * until the process exits.  Calls whose workspace need
+ * (kda_prefill_workspace_size) exceeds it return KDA_ERR_WORKSPACE and
+ * launch nothing; at 16 heads that is about 4000 tokens per call.
+ *
+ * The first call on each device looks up the array's device address with
+ * that device current; make that first call before any stream capture.
+ * All calls in the process share the one array (per device): calls whose
+ * work overlaps on the GPU race on it, so serialise them (one stream, or
+ * events).  Each call writes every scratch byte it reads, so nothing needs
+ * clearing between calls.  Arguments and results are exactly those of
+ * kda_prefill.
+ */
+#define KDA_PREFILL_STATIC_SCRATCH_BYTES ((size_t)128 << 20)
+kda_status kda_prefill_noalloc(kda_dims dims, kda_gate gate, const kda_bf16 *q,
+                               const kda_bf16 *k, const kda_bf16 *v, const kda_bf16 *g,
+                               const kda_bf16 *beta, int64_t gb_rows, float *state_pool,
+                               int pool_slots, const int32_t *state_idx,
+                               const int32_t *cu_seqlens, int num_seqs, int64_t total_tokens,
+                               kda_bf16 *o, float *intermediate, int32_t *err_flag, void *stream);
+
+/*
  * Profiling aid (not part of the pages' contract): per-stage timing of
  * kda_prefill.  After kda_prefill_set_stage_events(ev) with three cudaEvent_t
  * handles passed as void*, every kda_prefill call records ev[0] on its stream

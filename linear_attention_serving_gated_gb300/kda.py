@@ -51,7 +51,10 @@ class kda_gate(ctypes.Structure):
 
 
 EXPORTS = ("kda_status_string", "kda_prefill_workspace_size", "kda_prefill", "kda_decode_packed",
-           "kda_verify_chain", "kda_verify_tree", "kda_commit", "kda_prefill_set_stage_events")
+           "kda_verify_chain", "kda_verify_tree", "kda_commit", "kda_prefill_set_stage_events",
+           "kda_prefill_noalloc")
+
+PREFILL_STATIC_SCRATCH_BYTES = 128 << 20
 
 _lib = None
 
@@ -82,6 +85,9 @@ def load(path: str = LIB_PATH):
                                         vp, vp, vp, vp, vp]
         lib.kda_commit.restype = i32
         lib.kda_commit.argtypes = [kda_dims, vp, i32, i32, vp, vp, i32, vp, vp, vp]
+        lib.kda_prefill_noalloc.restype = i32
+        lib.kda_prefill_noalloc.argtypes = [kda_dims, kda_gate, vp, vp, vp, vp, vp, i64, vp, i32, vp,
+                                            vp, i32, i64, vp, vp, vp, vp]
         lib.kda_prefill_set_stage_events.restype = None
         lib.kda_prefill_set_stage_events.argtypes = [ctypes.POINTER(ctypes.c_void_p)]
         _lib = lib
@@ -164,6 +170,18 @@ def kda_prefill(d, gate: Gate, q, k, v, g, beta, state_pool, state_idx, cu_seqle
         int(num_seqs), int(T), _bf16(o, "o"), _p(intermediate), _p(workspace),
         int(workspace.numel() * workspace.element_size()), _p(err_flag), _stream(stream))
     _check(st, "kda_prefill")
+
+
+def kda_prefill_noalloc(d, gate: Gate, q, k, v, g, beta, state_pool, state_idx, cu_seqlens,
+                        num_seqs, o, intermediate=None, err_flag=None, stream=None):
+    """kda_prefill with the library's built-in static scratch (see kda.h): for
+    callers that cannot allocate device memory."""
+    st = load().kda_prefill_noalloc(
+        d, gate.c(), _bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v"), _bf16(g, "g"), _bf16(beta, "beta"),
+        int(g.shape[0]), _p(state_pool), int(state_pool.shape[0]), _p(state_idx), _p(cu_seqlens),
+        int(num_seqs), int(q.shape[0]), _bf16(o, "o"), _p(intermediate), _p(err_flag),
+        _stream(stream))
+    _check(st, "kda_prefill_noalloc")
 
 
 def kda_decode_packed(d, gate: Gate, mixed_qkv, a, b, state_pool, state_idx, o, err_flag=None,
