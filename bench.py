@@ -255,22 +255,58 @@ def run_ours(args, rank, world, local_rank):
         elif name == "commit":
             kda.kda_commit(D, v_snap, COMMIT_B, VERIFY_T, accepted, v_pool, v_idx)
 
-    def one_step(record):
+    def stage_events():
+        # torch creates the CUDA event on first record(): record once so the
+        # handle exists, then the prefill re-records it around its kernels
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        for e in ev:
+            e.record(stream)
+        return ev
+
+    # Each phase is captured once in a CUDA graph and timed as graph replays
+    # (the pages' microbenchmark method), so host-side launch latency stays out
+    # of the measured intervals.  The prefill gets one graph per timed step, each
+    # with its own stage events around its two kernels.
+    for _ in range(max(args.warmup, 3)):
+        for name in phases:
+            flush.zero_()
+            run_phase(name)
+    torch.cuda.synchronize()
+
+    def capture(name, ev=None):
+        g = torch.cuda.CUDAGraph()
+        kda.kda_prefill_set_stage_events(ev)
+        with torch.cuda.graph(g):
+            run_phase(name)
+        kda.kda_prefill_set_stage_events(None)
+        return g
+
+    graphs = {n: capture(n) for n in phases if n != "prefill"}
+    prefill_graphs = []
+    for _ in range(args.steps):
+        ev = stage_events()
+        prefill_graphs.append((capture("prefill", ev), ev))
+    torch.cuda.synchronize()
+    for _ in range(2):  # warm the replays
+        for n in phases:
+            flush.zero_()
+            (prefill_graphs[0][0] if n == "prefill" else graphs[n]).replay()
+    torch.cuda.synchronize()
+
+    def one_step(step):
         times = {}
         for name in phases:
             flush.zero_()
-            if record:
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record(stream)
-            run_phase(name)
-            if record:
-                e1.record(stream)
-                times[name] = (e0, e1)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            if name == "prefill":
+                prefill_graphs[step][0].replay()
+            else:
+                graphs[name].replay()
+            e1.record(stream)
+            times[name] = (e0, e1)
+        times["_stage"] = prefill_graphs[step][1]
         return times
-
-    for _ in range(max(args.warmup, 3)):
-        one_step(False)
-    torch.cuda.synchronize()
 
     sampler = ClockSampler(physical_gpu_index(local_rank)) if rank == 0 else None
     if sampler:
@@ -280,28 +316,12 @@ def run_ours(args, rank, world, local_rank):
         dist.barrier()
     torch.cuda.synchronize()
     wall0 = time.perf_counter()
-    records = []
-    def stage_events():
-        # torch creates the CUDA event on first record(): record once so the
-        # handle exists, then the prefill re-records it around its kernels
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
-        for e in ev:
-            e.record(stream)
-        return ev
-
-    for _ in range(args.steps):
-        # fresh stage events per step: the prefill records its two kernels' bounds into them
-        ev = stage_events()
-        kda.kda_prefill_set_stage_events(ev)
-        rec = one_step(True)
-        rec["_stage"] = ev
-        records.append(rec)
+    records = [one_step(step) for step in range(args.steps)]
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     wall = time.perf_counter() - wall0
     clocks = sampler.stop() if sampler else None
-    kda.kda_prefill_set_stage_events(None)
 
     ph_ms = {n: [r[n][0].elapsed_time(r[n][1]) for r in records] for n in phases}
     k_ms = {
@@ -347,11 +367,12 @@ def run_ours(args, rank, world, local_rank):
     prefill_s = tot["prefill"] / 1e3
     value = replica_throughput(PREFILL_T, steps, world, prefill_s)
     mean_k = {n: statistics.mean(v) for n, v in k_ms.items()}
-    # FP32 CUDA-core peak: 152 SMs x 128 FMA lanes x 2 flops x max SM clock
-    alu_peak = 152 * 128 * 2 * sm_max * 1e6 / 1e12
+    # Both prefill kernels run their contractions on tcgen05 (BF16 operands,
+    # FP32 accumulation): judged against the measured dense BF16 peak, with
+    # algorithmic flops only (the hi/lo split passes are not counted).
     work = {
-        "prefill_transform": ("alu", transform_flops(PREFILL_T) / 1e12, alu_peak, "TFLOP/s"),
-        "prefill_pass": ("alu", pass_flops(PREFILL_T) / 1e12, alu_peak, "TFLOP/s"),
+        "prefill_transform": ("tensor", transform_flops(PREFILL_T) / 1e12, bf16_tf, "TFLOP/s"),
+        "prefill_pass": ("tensor", pass_flops(PREFILL_T) / 1e12, bf16_tf, "TFLOP/s"),
         "decode": ("hbm", decode_bytes(DECODE_B) / 1e9, hbm, "GB/s"),
         "verify_chain": ("hbm", verify_bytes(VERIFY_B, VERIFY_T) / 1e9, hbm, "GB/s"),
         "verify_tree": ("hbm", verify_bytes(VERIFY_B, VERIFY_T) / 1e9, hbm, "GB/s"),
@@ -365,7 +386,7 @@ def run_ours(args, rank, world, local_rank):
     traffic = tr["bytes"] if tr and tr.get("src") == src else None
     roofline = {"kernel": dom, "bound": bound, "achieved": round(achieved, 3), "peak": peak,
                 "unit": unit, "frac": round(achieved / peak, 4), "traffic": traffic,
-                "peak_source": peak_kind if bound != "alu" else "derived: 152 SM x 128 FP32 lanes x 2 x max SM clock"}
+                "peak_source": f"{peak_kind} ({'dense BF16 burst' if bound == 'tensor' else 'HBM copy'})"}
     kern = {}
     for n in kernels:
         b_, w_, p_, u_ = work[n]
@@ -389,6 +410,7 @@ def run_ours(args, rank, world, local_rank):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16 in / fp32 state",
         "data": "synthetic (seeded; q,k,v,a,beta ~N(0,1) BF16, A_log~U(-1,1), dt_bias~N(0,0.1), state~N(0,0.02))",
         "config": {"workload": "KDA prefill 1x4096 tokens, 16 heads x 128 (+ decode B=48, verify 16x6 chain/tree, commit 16)",
+                   "timing": "CUDA-graph replay per phase, CUDA events on the replay stream",
                    "global_batch": world, "seq_len": PREFILL_T, "heads": H, "head_dim": K,
                    "parallelism": f"replicas x{world}", "l2": "flushed (512 MiB write) before every phase"},
         "gpu_launches": steps * len(kernels),

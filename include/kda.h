@@ -116,7 +116,9 @@ size_t kda_prefill_workspace_size(kda_dims dims, int num_seqs, int64_t total_tok
  *                 the start of every 64-token chunk of every sequence,
  *                 sequence-major.
  *   workspace     >= kda_prefill_workspace_size(...) bytes, 256-byte aligned.
- * T = 1 takes the same kernels as any other length.
+ * T = 1 takes the same kernels as any other length.  The first call on each
+ * device sets the kernels' shared-memory limits (cudaFuncSetAttribute); make
+ * it before capturing calls into a CUDA graph.
  */
 kda_status kda_prefill(kda_dims dims, kda_gate gate, const kda_bf16 *q, const kda_bf16 *k,
                        const kda_bf16 *v, const kda_bf16 *g, const kda_bf16 *beta,

@@ -1199,6 +1199,24 @@ int64_t max_chunks(int num_seqs, int64_t total_tokens) {
   return total_tokens / kChunk + num_seqs;
 }
 
+constexpr int kMaxDevices = 64;
+bool g_attributes_set[kMaxDevices] = {};
+
+kda_status ensure_kernel_attributes() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KDA_ERR_CUDA;
+  if (g_attributes_set[dev]) return KDA_OK;
+  if (cudaFuncSetAttribute(chunk_transform_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)kTransformSmem) != cudaSuccess ||
+      cudaFuncSetAttribute(chunk_transform_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)kTransformTcSmem) != cudaSuccess ||
+      cudaFuncSetAttribute(state_pass_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)kPassSmem) != cudaSuccess)
+    return KDA_ERR_CUDA;
+  g_attributes_set[dev] = true;
+  return KDA_OK;
+}
+
 cudaEvent_t g_stage_events[3] = {nullptr, nullptr, nullptr};
 
 void record_stage(int i, cudaStream_t st) {
@@ -1257,13 +1275,10 @@ extern "C" kda_status kda_prefill(kda_dims dims, kda_gate gate, const kda_bf16* 
   args.err_flag = err_flag;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
-  // Per device and cheap; not a stream operation, so also fine under capture.
-  cudaFuncSetAttribute(chunk_transform_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                       (int)kTransformSmem);
-  cudaFuncSetAttribute(state_pass_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                       (int)kPassSmem);
-  cudaFuncSetAttribute(chunk_transform_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                       (int)kTransformTcSmem);
+  // Kernel shared-memory limits are set once per device, on the first call
+  // made with that device current (so that first call should precede any
+  // stream capture).
+  if ((s = ensure_kernel_attributes()) != KDA_OK) return s;
   const int64_t chunks = max_chunks(num_seqs, total_tokens);
   record_stage(0, st);
   if (chunks > 0) {
