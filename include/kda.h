@@ -215,8 +215,10 @@ kda_status kda_prefill_noalloc(kda_dims dims, kda_gate gate, const kda_bf16 *q,
  * kda_prefill.  After kda_prefill_set_stage_events(ev) with three cudaEvent_t
  * handles passed as void*, every kda_prefill call records ev[0] on its stream
  * before its first kernel, ev[1] between the chunk-transform and the
- * state-pass kernels, and ev[2] after the state pass.  NULL clears it.  The
- * setting is process-wide and not meant for concurrent callers.
+ * state-pass kernels, and ev[2] after the state pass (as external event
+ * nodes when the call is captured in a CUDA graph, so replays record them).
+ * NULL clears it.  The setting is process-wide and not meant for concurrent
+ * callers.
  */
 void kda_prefill_set_stage_events(void *const *events);
 

@@ -1219,8 +1219,10 @@ kda_status ensure_kernel_attributes() {
 
 cudaEvent_t g_stage_events[3] = {nullptr, nullptr, nullptr};
 
+// Recorded as an external event node when the stream is being captured, so
+// the event fires on every replay of the graph.
 void record_stage(int i, cudaStream_t st) {
-  if (g_stage_events[i]) cudaEventRecord(g_stage_events[i], st);
+  if (g_stage_events[i]) cudaEventRecordWithFlags(g_stage_events[i], st, cudaEventRecordExternal);
 }
 
 }  // namespace
