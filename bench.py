@@ -10,11 +10,13 @@ PR #42857, Speed Tests and Profiling):
   verify    16 requests x 6 draft tokens, chain and tree, with snapshots
   commit    16 requests, accepted prefix copied into the pool
 `value` is prefill tokens/s (the metric's first term) over the prefill phase
-time; every phase is timed with CUDA events on the launching stream, and L2
-is flushed (a 512 MiB write) before each phase.  `phases` carries the
-per-layer-call microseconds of every phase.  `e2e` repeats the prefill with
-its inputs copied from pinned host memory and its output copied back inside
-the timed region.
+time.  Every phase is a CUDA-graph replay timed with CUDA events recorded as
+graph nodes around its kernels, after an L2 flush (a 512 MiB write, then a
+read of the same buffer).  Decode, verify and commit replay 8 layer calls back
+to back, each on its own state pool and buffers, and report the span / 8.
+`phases` carries the per-layer-call microseconds of every phase.  `e2e`
+repeats the prefill with its inputs copied from pinned host memory and its
+output copied back inside the timed region.
 
 Multi-GPU: the path has no exchange step, so N ranks run N independent
 replicas (weak scaling); `value` is the tokens of all ranks over the slowest
@@ -45,6 +47,7 @@ DECODE_B = 48
 VERIFY_B, VERIFY_T = 16, 6
 COMMIT_B = VERIFY_B
 FLUSH_BYTES = 512 << 20
+LAYERS = 8  # decode/verify/commit calls per timed replay
 
 # DRAM traffic per launch from ncu (dram__bytes_read.sum + dram__bytes_write.sum),
 # keyed by kernel; valid only while the kernel sources hash to the recorded value.
@@ -220,92 +223,116 @@ def run_ours(args, rank, world, local_rank):
     p_o = torch.empty((PREFILL_T, H, K), dtype=torch.bfloat16, device=dev)
     ws = torch.empty(kda.kda_prefill_workspace_size(D, 1, PREFILL_T), dtype=torch.uint8, device=dev)
 
+    # Decode, verify and commit run LAYERS calls back to back, each on its own
+    # copy of the state pool, inputs and outputs (as consecutive KDA layers of
+    # one model do), so every call starts from data no earlier call touched.
     dd = inputs.decode_inputs(seed=100 + rank, B=DECODE_B, H=H, slots=240)
-    DX = {n: bf(dd[n]) for n in ("mixed_qkv", "a", "b")}
-    d_pool = t(dd["pool"])
-    d_idx = t(dd["state_idx"])
-    d_o = torch.empty((DECODE_B, H, K), dtype=torch.bfloat16, device=dev)
-
     vd = inputs.verify_inputs(seed=200 + rank, B=VERIFY_B, T=VERIFY_T, H=H, slots=240)
-    VX = {n: bf(vd[n]) for n in ("mixed_qkv", "a", "b")}
-    v_pool = t(vd["pool"])
-    v_idx = t(vd["state_idx"])
-    v_par = t(vd["parent"])
-    v_o = torch.empty((VERIFY_B, VERIFY_T, H, K), dtype=torch.bfloat16, device=dev)
-    v_snap = torch.empty((VERIFY_B, VERIFY_T, H, K, K), device=dev)
-    v_snap2 = torch.empty_like(v_snap)
-    accepted = t(np.random.default_rng(rank).integers(-1, VERIFY_T, size=COMMIT_B).astype(np.int32))
+    d_pool0, v_pool0 = t(dd["pool"]), t(vd["pool"])
+    L = []
+    for _ in range(LAYERS):
+        L.append({
+            "DX": {n: bf(dd[n]) for n in ("mixed_qkv", "a", "b")},
+            "d_pool": d_pool0.clone(), "d_idx": t(dd["state_idx"]),
+            "d_o": torch.empty((DECODE_B, H, K), dtype=torch.bfloat16, device=dev),
+            "VX": {n: bf(vd[n]) for n in ("mixed_qkv", "a", "b")},
+            "v_pool": v_pool0.clone(), "v_idx": t(vd["state_idx"]), "v_par": t(vd["parent"]),
+            "v_o": torch.empty((VERIFY_B, VERIFY_T, H, K), dtype=torch.bfloat16, device=dev),
+            "v_snap": torch.empty((VERIFY_B, VERIFY_T, H, K, K), device=dev),
+            "v_snap2": torch.empty((VERIFY_B, VERIFY_T, H, K, K), device=dev),
+            # every request accepts some prefix, so every commit copies one state
+            "accepted": t(np.random.default_rng(rank).integers(0, VERIFY_T, size=COMMIT_B).astype(np.int32)),
+        })
+    del d_pool0, v_pool0
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def flush_l2():
+        # A write larger than L2 evicts every line the previous phase left;
+        # reading the buffer back then writes the flush's own dirty lines out,
+        # so the next phase starts from a cold L2 with nothing left to write back.
+        flush.zero_()
+        flush.view(torch.int64).sum()
 
     phases = ["prefill", "decode", "verify_chain", "verify_tree", "commit"]
     kernels = ["prefill_transform", "prefill_pass", "decode", "verify_chain", "verify_tree", "commit"]
 
-    def run_phase(name):
+    def run_call(name, x):
         if name == "prefill":
             kda.kda_prefill(D, gate, P["q"], P["k"], P["v"], P["g"], P["beta"], p_pool, p_idx, p_cu, 1,
                             p_o, workspace=ws)
         elif name == "decode":
-            kda.kda_decode_packed(D, gate, DX["mixed_qkv"], DX["a"], DX["b"], d_pool, d_idx, d_o)
+            kda.kda_decode_packed(D, gate, x["DX"]["mixed_qkv"], x["DX"]["a"], x["DX"]["b"], x["d_pool"],
+                                  x["d_idx"], x["d_o"])
         elif name == "verify_chain":
-            kda.kda_verify_chain(D, gate, VX["mixed_qkv"], VX["a"], VX["b"], VERIFY_B, VERIFY_T, v_pool,
-                                 v_idx, v_o, v_snap)
+            kda.kda_verify_chain(D, gate, x["VX"]["mixed_qkv"], x["VX"]["a"], x["VX"]["b"], VERIFY_B,
+                                 VERIFY_T, x["v_pool"], x["v_idx"], x["v_o"], x["v_snap"])
         elif name == "verify_tree":
-            kda.kda_verify_tree(D, gate, VX["mixed_qkv"], VX["a"], VX["b"], VERIFY_B, VERIFY_T, v_par,
-                                v_pool, v_idx, v_o, v_snap2)
+            kda.kda_verify_tree(D, gate, x["VX"]["mixed_qkv"], x["VX"]["a"], x["VX"]["b"], VERIFY_B,
+                                VERIFY_T, x["v_par"], x["v_pool"], x["v_idx"], x["v_o"], x["v_snap2"])
         elif name == "commit":
-            kda.kda_commit(D, v_snap, COMMIT_B, VERIFY_T, accepted, v_pool, v_idx)
+            kda.kda_commit(D, x["v_snap"], COMMIT_B, VERIFY_T, x["accepted"], x["v_pool"], x["v_idx"])
+
+    def calls(name):
+        return [None] if name == "prefill" else L
+
+    def run_phase(name, ev=None):
+        """One phase; with events, ev[0] is recorded right before the first
+        kernel and ev[2] right after the last (ev[1] between the two prefill
+        kernels), as graph nodes when captured."""
+        cs = calls(name)
+        for i, x in enumerate(cs):
+            if ev is not None:
+                first, last = i == 0, i == len(cs) - 1
+                kda.kda_set_stage_events([ev[0] if first else None, ev[1] if first and last else None,
+                                          ev[2] if last else None])
+            run_call(name, x)
+        kda.kda_set_stage_events(None)
 
     def stage_events():
         # torch creates the CUDA event on first record(): record once so the
-        # handle exists, then the prefill re-records it around its kernels
+        # handle exists, then the library re-records it around its kernels
         ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
         for e in ev:
             e.record(stream)
         return ev
 
-    # Each phase is captured once in a CUDA graph and timed as graph replays
-    # (the pages' microbenchmark method), so host-side launch latency stays out
-    # of the measured intervals.  The prefill gets one graph per timed step, each
-    # with its own stage events around its two kernels.
+    # Each phase is captured in a CUDA graph and timed as graph replays (the
+    # pages' microbenchmark method), so host-side launch latency stays out of
+    # the measured intervals.  Every (step, phase) has its own graph and its
+    # own events.
     for _ in range(max(args.warmup, 3)):
         for name in phases:
-            flush.zero_()
+            flush_l2()
             run_phase(name)
     torch.cuda.synchronize()
 
-    def capture(name, ev=None):
+    def capture(name, ev):
         g = torch.cuda.CUDAGraph()
-        kda.kda_prefill_set_stage_events(ev)
         with torch.cuda.graph(g):
-            run_phase(name)
-        kda.kda_prefill_set_stage_events(None)
+            run_phase(name, ev)
         return g
 
-    graphs = {n: capture(n) for n in phases if n != "prefill"}
-    prefill_graphs = []
+    step_graphs = []
     for _ in range(args.steps):
-        ev = stage_events()
-        prefill_graphs.append((capture("prefill", ev), ev))
+        row = {}
+        for n in phases:
+            ev = stage_events()
+            row[n] = (capture(n, ev), ev)
+        step_graphs.append(row)
     torch.cuda.synchronize()
     for _ in range(2):  # warm the replays
         for n in phases:
-            flush.zero_()
-            (prefill_graphs[0][0] if n == "prefill" else graphs[n]).replay()
+            flush_l2()
+            step_graphs[0][n][0].replay()
     torch.cuda.synchronize()
 
     def one_step(step):
         times = {}
         for name in phases:
-            flush.zero_()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            if name == "prefill":
-                prefill_graphs[step][0].replay()
-            else:
-                graphs[name].replay()
-            e1.record(stream)
-            times[name] = (e0, e1)
-        times["_stage"] = prefill_graphs[step][1]
+            flush_l2()
+            g, ev = step_graphs[step][name]
+            g.replay()
+            times[name] = ev
         return times
 
     sampler = ClockSampler(physical_gpu_index(local_rank)) if rank == 0 else None
@@ -323,10 +350,11 @@ def run_ours(args, rank, world, local_rank):
     wall = time.perf_counter() - wall0
     clocks = sampler.stop() if sampler else None
 
-    ph_ms = {n: [r[n][0].elapsed_time(r[n][1]) for r in records] for n in phases}
+    # per-call milliseconds of every phase (a layer phase's span / LAYERS)
+    ph_ms = {n: [r[n][0].elapsed_time(r[n][2]) / len(calls(n)) for r in records] for n in phases}
     k_ms = {
-        "prefill_transform": [r["_stage"][0].elapsed_time(r["_stage"][1]) for r in records],
-        "prefill_pass": [r["_stage"][1].elapsed_time(r["_stage"][2]) for r in records],
+        "prefill_transform": [r["prefill"][0].elapsed_time(r["prefill"][1]) for r in records],
+        "prefill_pass": [r["prefill"][1].elapsed_time(r["prefill"][2]) for r in records],
         "decode": ph_ms["decode"], "verify_chain": ph_ms["verify_chain"],
         "verify_tree": ph_ms["verify_tree"], "commit": ph_ms["commit"],
     }
@@ -343,7 +371,7 @@ def run_ours(args, rank, world, local_rank):
     e2e_steps = max(3, min(args.steps, 50))
     ev_e2e = []
     for i in range(e2e_steps + 3):
-        flush.zero_()
+        flush_l2()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for n in host:
@@ -397,6 +425,7 @@ def run_ours(args, rank, world, local_rank):
         "prefill_1x4096": {"us": round(statistics.mean(ph_ms["prefill"]) * 1e3, 2),
                            "tok_s": round(value / world, 1),
                            "hbm_frac_of_call": round(prefill_bytes(PREFILL_T) / (statistics.mean(ph_ms["prefill"]) / 1e3) / 1e9 / hbm, 4)},
+        "layers_per_replay": LAYERS,
         "decode_b48": {"us": round(statistics.mean(ph_ms["decode"]) * 1e3, 2)},
         "verify_chain_b16x6": {"us": round(statistics.mean(ph_ms["verify_chain"]) * 1e3, 2)},
         "verify_tree_b16x6": {"us": round(statistics.mean(ph_ms["verify_tree"]) * 1e3, 2)},
@@ -410,10 +439,12 @@ def run_ours(args, rank, world, local_rank):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16 in / fp32 state",
         "data": "synthetic (seeded; q,k,v,a,beta ~N(0,1) BF16, A_log~U(-1,1), dt_bias~N(0,0.1), state~N(0,0.02))",
         "config": {"workload": "KDA prefill 1x4096 tokens, 16 heads x 128 (+ decode B=48, verify 16x6 chain/tree, commit 16)",
-                   "timing": "CUDA-graph replay per phase, CUDA events on the replay stream",
+                   "timing": (f"CUDA-graph replay per phase; CUDA events recorded as graph nodes around the phase's kernels; "
+                              f"decode/verify/commit: {LAYERS} layer calls back to back, each on its own state pool and "
+                              f"buffers, time per call = span / {LAYERS}"),
                    "global_batch": world, "seq_len": PREFILL_T, "heads": H, "head_dim": K,
-                   "parallelism": f"replicas x{world}", "l2": "flushed (512 MiB write) before every phase"},
-        "gpu_launches": steps * len(kernels),
+                   "parallelism": f"replicas x{world}", "l2": "flushed before every phase (512 MiB write, then the same buffer read back); layer calls touch disjoint buffers larger than L2"},
+        "gpu_launches": steps * (2 + (len(phases) - 1) * LAYERS),
         "phases": phase_out,
         "roofline": roofline,
         "e2e": {"value": round(replica_throughput(PREFILL_T, e2e_steps, world, e2e_ms / 1e3), 1),

@@ -211,16 +211,17 @@ kda_status kda_prefill_noalloc(kda_dims dims, kda_gate gate, const kda_bf16 *q,
                                kda_bf16 *o, float *intermediate, int32_t *err_flag, void *stream);
 
 /*
- * Profiling aid (not part of the pages' contract): per-stage timing of
- * kda_prefill.  After kda_prefill_set_stage_events(ev) with three cudaEvent_t
- * handles passed as void*, every kda_prefill call records ev[0] on its stream
- * before its first kernel, ev[1] between the chunk-transform and the
- * state-pass kernels, and ev[2] after the state pass (as external event
- * nodes when the call is captured in a CUDA graph, so replays record them).
- * NULL clears it.  The setting is process-wide and not meant for concurrent
- * callers.
+ * Profiling aid (not part of the pages' contract): per-kernel timing of every
+ * entry point.  After kda_set_stage_events(ev) with three cudaEvent_t
+ * handles passed as void*, each later call records ev[0] on its stream before
+ * its first kernel and ev[2] after its last; kda_prefill records ev[1]
+ * between its chunk-transform and state-pass kernels, the single-kernel entry
+ * points record ev[1] together with ev[2].  Under stream capture they become
+ * external event nodes, so every replay of the graph records them.  A NULL
+ * entry is not recorded; a NULL array clears the setting, which is
+ * process-wide and not meant for concurrent callers.
  */
-void kda_prefill_set_stage_events(void *const *events);
+void kda_set_stage_events(void *const *events);
 
 #ifdef __cplusplus
 }

@@ -44,4 +44,8 @@ inline kda_status launch_status() {
   return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
+// Profiling aid: records stage event i (see kda_set_stage_events) on the
+// stream if one is set.
+void record_stage(int i, cudaStream_t st);
+
 }  // namespace kda

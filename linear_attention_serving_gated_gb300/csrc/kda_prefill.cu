@@ -37,12 +37,14 @@
 // drop terms that are smaller still.
 //
 // Two kernels:
-//   chunk_transform_kernel  one CTA per (chunk, head), all chunks in parallel,
-//                           FP32 on the CUDA cores: fold, cumulative decay, A,
-//                           P, (I+A)^-1 by column forward substitution, W,
-//                           Util, Q', P Util, Khat, gamma.  Writes one
-//                           workspace record per (chunk, head) already in the
-//                           tensor-core operand layout.
+//   chunk_transform_tc_kernel  one CTA per (chunk, head), all chunks in
+//                           parallel: fold and cumulative decay on the CUDA
+//                           cores, A and P as tcgen05 products of decay-split
+//                           factors, (I+A)^-1 blocked on the CUDA cores, then
+//                           W, Util, P W, P Util as one more tcgen05 product;
+//                           Q' = Qtil - P W, Khat and gamma in the epilogue.
+//                           Writes one workspace record per (chunk, head)
+//                           already in the tensor-core operand layout.
 //   state_pass_kernel       one CTA per (sequence, head, 32 value columns),
 //                           sequential over the sequence's chunks, on tcgen05:
 //                           per chunk one bulk copy of the record into shared
@@ -55,8 +57,6 @@
 //                           are summed in the epilogues)
 //                           with S kept in FP32 registers (one key channel per
 //                           thread) and re-split into BF16 hi/lo operands.
-#include <stdlib.h>
-
 #include "kda_host.h"
 #include "kda_tc.cuh"
 
@@ -149,284 +149,6 @@ __device__ __forceinline__ float4& f4(float* p) { return *reinterpret_cast<float
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return (uint32_t)float_to_bf16_bits(lo) | ((uint32_t)float_to_bf16_bits(hi) << 16);
 }
-
-// ---------------------------------------------------------------------------
-// Per-chunk transform (all chunks of all sequences in parallel).
-
-__global__ void __launch_bounds__(256) chunk_transform_kernel(const PrefillArgs a) {
-  extern __shared__ __align__(16) float sm[];
-  float* KQ = sm;                    // k-hat, later W            [64][kLd]
-  float* QQ = KQ + kChunk * kLd;     // q-hat, later Qtil, Q'     [64][kLd]
-  float* GM = QQ + kChunk * kLd;     // Gam, later Util           [64][kLd]
-  float* L1 = GM + kChunk * kLd;     // Lk, later beta Ktil, beta V
-  float* L2 = L1 + kChunk * kLd;     // Lq, later (I+A)^-1 [64][kLdT]
-  float* R = L2 + kChunk * kLd;      // right factor [16][kLd]
-  float* Am = R + 16 * kLd;          // A [64][kLdT]
-  float* Pm = Am + kChunk * kLdT;    // P [64][kLdT]
-  float* bt = Pm + kChunk * kLdT;    // beta [64]
-  __shared__ ChunkLoc loc;
-  __shared__ int skip;
-
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int h = blockIdx.y;
-  const int64_t cid = blockIdx.x;
-  if (tid == 0) {
-    skip = 0;
-    if (!seqlens_valid(a)) {
-      skip = 1;
-      if (cid == 0 && h == 0) set_error(a.err_flag, KDA_DEVERR_SEQLENS);
-    } else {
-      loc = locate_chunk(a, cid);
-      if (loc.n < 0) {
-        skip = 1;
-      } else {
-        const int slot = a.state_idx[loc.n];
-        if (slot < 0 || slot >= a.pool_slots) skip = 1;  // padding / rejected sequence
-      }
-    }
-  }
-  __syncthreads();
-  if (skip) return;
-  const int len = loc.len;
-  const int64_t t0 = loc.t0;
-  const GateArgs& ga = a.gate;
-  const int H = a.H, HV = a.HV, K = kHeadDim;
-  uint8_t* rec = a.ws + ((size_t)cid * HV + h) * kRecBytes;
-
-  // 1. fold and cumulative log-decay.  Warp w owns tokens [8w, 8w+8), lane l
-  //    owns channels [4l, 4l+4); each warp keeps a running sum of g over its
-  //    tokens in registers, then adds the totals of the warps before it.
-  float* tot = Am;  // [8][128] warp totals, reused before A is written
-  {
-    const int c = lane * 4;
-    const float exp_alog = ga.A_log ? expf(ga.A_log[h]) : 0.f;
-    const float4 bias = ga.dt_bias ? *reinterpret_cast<const float4*>(ga.dt_bias + h * K + c)
-                                   : make_float4(0.f, 0.f, 0.f, 0.f);
-    float4 run = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int t = warp * 8; t < warp * 8 + 8; ++t) {
-      float4 q4 = make_float4(0.f, 0.f, 0.f, 0.f), k4 = q4, g4 = q4;
-      if (t < len) {
-        const int64_t tok = t0 + t;
-        q4 = load_bf16x4(a.q + (tok * H + h) * K + c);
-        k4 = load_bf16x4(a.k + (tok * H + h) * K + c);
-        const float4 a4 = load_bf16x4(a.g + (tok * HV + h) * K + c);
-        if (ga.use_qk_l2norm) {
-          const float rq = rsqrtf(warp_sum(dot4(q4, q4)) + kNormEps);
-          const float rk = rsqrtf(warp_sum(dot4(k4, k4)) + kNormEps);
-          q4 = make_float4(q4.x * rq, q4.y * rq, q4.z * rq, q4.w * rq);
-          k4 = make_float4(k4.x * rk, k4.y * rk, k4.z * rk, k4.w * rk);
-        }
-        g4 = make_float4(gate_log_decay(ga, a4.x, exp_alog, bias.x),
-                         gate_log_decay(ga, a4.y, exp_alog, bias.y),
-                         gate_log_decay(ga, a4.z, exp_alog, bias.z),
-                         gate_log_decay(ga, a4.w, exp_alog, bias.w));
-        if (lane == 0) bt[t] = fold_beta(ga, bf16_bits_to_float(a.beta[tok * HV + h]));
-      } else if (lane == 0) {
-        bt[t] = 0.f;
-      }
-      run = make_float4(run.x + g4.x, run.y + g4.y, run.z + g4.z, run.w + g4.w);
-      f4(QQ + t * kLd + c) = q4;
-      f4(KQ + t * kLd + c) = k4;
-      f4(GM + t * kLd + c) = run;
-    }
-    f4(tot + warp * K + c) = run;
-    __syncthreads();
-    float4 pre = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int w = 0; w < warp; ++w) {
-      const float4 x = f4(tot + w * K + c);
-      pre = make_float4(pre.x + x.x, pre.y + x.y, pre.z + x.z, pre.w + x.w);
-    }
-    for (int t = warp * 8; t < warp * 8 + 8; ++t) {
-      float4& gg = f4(GM + t * kLd + c);
-      gg = make_float4(gg.x + pre.x, gg.y + pre.y, gg.z + pre.z, gg.w + pre.w);
-    }
-  }
-  __syncthreads();
-  for (int i = tid; i < kChunk * kLdT; i += blockDim.x) {
-    Am[i] = 0.f;
-    Pm[i] = 0.f;
-  }
-  __syncthreads();
-
-  // 3. A and P, one 16-token block of i at a time, reference r = block end.
-  for (int ib = 0; ib < kChunk / 16; ++ib) {
-    const int b0 = ib * 16, r = b0 + 15;
-    for (int idx = tid; idx < (kChunk - b0) * (K / 4); idx += blockDim.x) {
-      const int t = b0 + idx / (K / 4), c = (idx % (K / 4)) * 4;
-      const float4 gt = f4(GM + t * kLd + c), gr = f4(GM + r * kLd + c);
-      const float4 kk = f4(KQ + t * kLd + c), qq = f4(QQ + t * kLd + c);
-      const float4 e = make_float4(expf(gt.x - gr.x), expf(gt.y - gr.y), expf(gt.z - gr.z),
-                                   expf(gt.w - gr.w));
-      f4(L1 + t * kLd + c) = make_float4(kk.x * e.x, kk.y * e.y, kk.z * e.z, kk.w * e.w);
-      f4(L2 + t * kLd + c) = make_float4(qq.x * e.x, qq.y * e.y, qq.z * e.z, qq.w * e.w);
-      if (t <= r) {  // right factor of token t as i: k_i e^{Gam_r - Gam_i}
-        const float4 f = make_float4(expf(gr.x - gt.x), expf(gr.y - gt.y), expf(gr.z - gt.z),
-                                     expf(gr.w - gt.w));
-        f4(R + (t - b0) * kLd + c) = make_float4(kk.x * f.x, kk.y * f.y, kk.z * f.z, kk.w * f.w);
-      }
-    }
-    __syncthreads();
-    for (int idx = tid; idx < (kChunk - b0) * 16; idx += blockDim.x) {
-      const int t = b0 + idx / 16, i = b0 + idx % 16;
-      if (i > t) continue;
-      float sa = 0.f, sp = 0.f;
-      float* lk = L1 + t * kLd;
-      float* lq = L2 + t * kLd;
-      float* rr = R + (i - b0) * kLd;
-#pragma unroll 8
-      for (int c = 0; c < K; c += 4) {
-        const float4 rv = f4(rr + c);
-        sa += dot4(f4(lk + c), rv);
-        sp += dot4(f4(lq + c), rv);
-      }
-      if (i < t) Am[t * kLdT + i] = bt[t] * sa;
-      Pm[t * kLdT + i] = sp;
-    }
-    __syncthreads();
-  }
-
-  // 4. (I + A)^-1, blocked in 16 x 16: the diagonal blocks by forward
-  //    substitution (one column per thread), then the blocks below the
-  //    diagonal one sub-diagonal at a time:
-  //      T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj.
-  float* Ti = L2;
-  float* X = R;  // [3][16][16] scratch
-  for (int i = tid; i < kChunk * kLdT; i += blockDim.x) Ti[i] = 0.f;
-  __syncthreads();
-  if (tid < kChunk) {
-    const int b0 = (tid >> 4) * 16, col = tid & 15;
-    float x[16];
-#pragma unroll
-    for (int r = 0; r < 16; ++r) {
-      float acc = r == col ? 1.f : 0.f;
-#pragma unroll
-      for (int s2 = 0; s2 < r; ++s2) acc -= Am[(b0 + r) * kLdT + b0 + s2] * x[s2];
-      x[r] = acc;
-      Ti[(b0 + r) * kLdT + b0 + col] = acc;
-    }
-  }
-  __syncthreads();
-  for (int d = 1; d < 4; ++d) {
-    const int npairs = 4 - d;
-    for (int idx = tid; idx < npairs * 256; idx += blockDim.x) {
-      const int pr = idx >> 8, r = (idx >> 4) & 15, cc = idx & 15;
-      const int bi = pr + d, bj = pr;
-      float acc = 0.f;
-      for (int bk = bj; bk < bi; ++bk)
-#pragma unroll
-        for (int m = 0; m < 16; ++m)
-          acc += Am[(bi * 16 + r) * kLdT + bk * 16 + m] * Ti[(bk * 16 + m) * kLdT + bj * 16 + cc];
-      X[pr * 256 + r * 16 + cc] = acc;
-    }
-    __syncthreads();
-    for (int idx = tid; idx < npairs * 256; idx += blockDim.x) {
-      const int pr = idx >> 8, r = (idx >> 4) & 15, cc = idx & 15;
-      const int bi = pr + d, bj = pr;
-      float acc = 0.f;
-#pragma unroll
-      for (int m = 0; m < 16; ++m)
-        acc -= Ti[(bi * 16 + r) * kLdT + bi * 16 + m] * X[pr * 256 + m * 16 + cc];
-      Ti[(bi * 16 + r) * kLdT + bj * 16 + cc] = acc;
-    }
-    __syncthreads();
-  }
-  // 5. gamma and Khat^T (hi/lo BF16, swizzled 128 x 64): thread -> (c, 8-token chunk)
-  if (tid < K) reinterpret_cast<float*>(rec + kRecGam)[tid] = expf(GM[(kChunk - 1) * kLd + tid]);
-  for (int idx = tid; idx < K * 8; idx += blockDim.x) {
-    const int c = idx >> 3, j = idx & 7;
-    const float gl = GM[(kChunk - 1) * kLd + c];
-    uint32_t hi[4], lo[4];
-#pragma unroll
-    for (int e = 0; e < 8; e += 2) {
-      uint16_t h0, l0, h1, l1;
-      const int t = j * 8 + e;
-      tc::split_bf16(KQ[t * kLd + c] * expf(gl - GM[t * kLd + c]), h0, l0);
-      tc::split_bf16(KQ[(t + 1) * kLd + c] * expf(gl - GM[(t + 1) * kLd + c]), h1, l1);
-      hi[e / 2] = (uint32_t)h0 | ((uint32_t)h1 << 16);
-      lo[e / 2] = (uint32_t)l0 | ((uint32_t)l1 << 16);
-    }
-    const uint32_t off = tc::sw128_offset(c, j * 8, K);
-    *reinterpret_cast<uint4*>(rec + kRecKTh + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-    *reinterpret_cast<uint4*>(rec + kRecKTl + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-  }
-  __syncthreads();
-
-  // 6. beta Ktil_i = beta_i k_i e^{Gam_i} -> L1 ; then W = Ti (beta Ktil) -> KQ
-  for (int idx = tid; idx < kChunk * (K / 4); idx += blockDim.x) {
-    const int i = idx / (K / 4), c = (idx % (K / 4)) * 4;
-    const float4 kk = f4(KQ + i * kLd + c), gg = f4(GM + i * kLd + c);
-    const float b = bt[i];
-    f4(L1 + i * kLd + c) = make_float4(b * kk.x * expf(gg.x), b * kk.y * expf(gg.y),
-                                       b * kk.z * expf(gg.z), b * kk.w * expf(gg.w));
-  }
-  __syncthreads();
-  // lower-triangular product out[t] = sum_{i<=t} Ti[t][i] X[i]; thread -> column quad, rows warp+8m
-  auto tri_gemm = [&](const float* X, float* out) {
-    const int c = lane * 4;
-    for (int t = warp; t < kChunk; t += 8) {
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int i = 0; i <= t; ++i) {
-        const float w = Ti[t * kLdT + i];
-        const float4 x = *reinterpret_cast<const float4*>(X + i * kLd + c);
-        acc.x += w * x.x;
-        acc.y += w * x.y;
-        acc.z += w * x.z;
-        acc.w += w * x.w;
-      }
-      f4(out + t * kLd + c) = acc;
-    }
-  };
-  tri_gemm(L1, KQ);  // W
-  __syncthreads();
-  // 7. Qtil = q e^{Gam} in place; beta V -> L1
-  for (int idx = tid; idx < kChunk * (K / 4); idx += blockDim.x) {
-    const int i = idx / (K / 4), c = (idx % (K / 4)) * 4;
-    const float4 gg = f4(GM + i * kLd + c);
-    float4& qq = f4(QQ + i * kLd + c);
-    qq = make_float4(qq.x * expf(gg.x), qq.y * expf(gg.y), qq.z * expf(gg.z), qq.w * expf(gg.w));
-    float4 vv = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (i < len) vv = load_bf16x4(a.v + ((t0 + i) * HV + h) * K + c);
-    const float b = bt[i];
-    f4(L1 + i * kLd + c) = make_float4(b * vv.x, b * vv.y, b * vv.z, b * vv.w);
-  }
-  __syncthreads();
-  // 8. Util = Ti (beta V) -> GM
-  tri_gemm(L1, GM);
-  __syncthreads();
-  // 9. Q' = Qtil - P W (in place), P Util and Util -> workspace (FP32, V-slice-major)
-  {
-    const int c = lane * 4;
-    const int slice = c / kVs, cs = c % kVs;
-    float* ut_out = reinterpret_cast<float*>(rec + kRecU) + slice * (kChunk * kVs);
-    float* oi_out = reinterpret_cast<float*>(rec + kRecOi) + slice * (kChunk * kVs);
-    for (int t = warp; t < kChunk; t += 8) {
-      float4 pw = make_float4(0.f, 0.f, 0.f, 0.f), pu = pw;
-      const int qd = cs / 4;  // column quad inside the slice
-      for (int i = 0; i <= t; ++i) {
-        const float p = Pm[t * kLdT + i];
-        const float4 w = f4(KQ + i * kLd + c), u = f4(GM + i * kLd + c);
-        pw.x += p * w.x; pw.y += p * w.y; pw.z += p * w.z; pw.w += p * w.w;
-        pu.x += p * u.x; pu.y += p * u.y; pu.z += p * u.z; pu.w += p * u.w;
-      }
-      float4& qq = f4(QQ + t * kLd + c);
-      qq = make_float4(qq.x - pw.x, qq.y - pw.y, qq.z - pw.z, qq.w - pw.w);
-      *reinterpret_cast<float4*>(oi_out + qd * (kChunk * 4) + t * 4) = pu;
-      *reinterpret_cast<float4*>(ut_out + qd * (kChunk * 4) + t * 4) = f4(GM + t * kLd + c);
-    }
-  }
-  __syncthreads();
-  // 10. [W; Q'] as BF16, swizzled 128 x 128: thread -> (row, 8-column chunk)
-  for (int idx = tid; idx < 128 * 16; idx += blockDim.x) {
-    const int row = idx >> 4, ch = idx & 15;
-    const float* src = (row < kChunk ? KQ + row * kLd : QQ + (row - kChunk) * kLd) + ch * 8;
-    const uint4 pk = make_uint4(pack_bf16x2(src[0], src[1]), pack_bf16x2(src[2], src[3]),
-                                pack_bf16x2(src[4], src[5]), pack_bf16x2(src[6], src[7]));
-    *reinterpret_cast<uint4*>(rec + kRecA1 + tc::sw128_offset(row, ch * 8, 128)) = pk;
-  }
-}
-
-constexpr size_t kTransformSmem =
-    sizeof(float) * (5 * kChunk * kLd + 16 * kLd + 2 * kChunk * kLdT + kChunk);
 
 // ---------------------------------------------------------------------------
 // Per-chunk transform on tcgen05 (all chunks of all sequences in parallel).
@@ -1206,9 +928,7 @@ kda_status ensure_kernel_attributes() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KDA_ERR_CUDA;
   if (g_attributes_set[dev]) return KDA_OK;
-  if (cudaFuncSetAttribute(chunk_transform_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)kTransformSmem) != cudaSuccess ||
-      cudaFuncSetAttribute(chunk_transform_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(chunk_transform_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)kTransformTcSmem) != cudaSuccess ||
       cudaFuncSetAttribute(state_pass_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)kPassSmem) != cudaSuccess)
@@ -1219,13 +939,14 @@ kda_status ensure_kernel_attributes() {
 
 cudaEvent_t g_stage_events[3] = {nullptr, nullptr, nullptr};
 
+}  // namespace
+
 // Recorded as an external event node when the stream is being captured, so
 // the event fires on every replay of the graph.
 void record_stage(int i, cudaStream_t st) {
   if (g_stage_events[i]) cudaEventRecordWithFlags(g_stage_events[i], st, cudaEventRecordExternal);
 }
 
-}  // namespace
 }  // namespace kda
 
 using namespace kda;
@@ -1284,10 +1005,7 @@ extern "C" kda_status kda_prefill(kda_dims dims, kda_gate gate, const kda_bf16* 
   const int64_t chunks = max_chunks(num_seqs, total_tokens);
   record_stage(0, st);
   if (chunks > 0) {
-    if (getenv("KDA_DEBUG_SIMT_TRANSFORM"))  // TEMPORARY development switch
-      chunk_transform_kernel<<<dim3((unsigned)chunks, dims.HV), 256, kTransformSmem, st>>>(args);
-    else
-      chunk_transform_tc_kernel<<<dim3((unsigned)chunks, dims.HV), kTxThreads, kTransformTcSmem, st>>>(args);
+    chunk_transform_tc_kernel<<<dim3((unsigned)chunks, dims.HV), kTxThreads, kTransformTcSmem, st>>>(args);
     if ((s = launch_status()) != KDA_OK) return s;
   }
   record_stage(1, st);
@@ -1297,7 +1015,7 @@ extern "C" kda_status kda_prefill(kda_dims dims, kda_gate gate, const kda_bf16* 
   return s;
 }
 
-extern "C" void kda_prefill_set_stage_events(void* const* events) {
+extern "C" void kda_set_stage_events(void* const* events) {
   for (int i = 0; i < 3; ++i)
     g_stage_events[i] = events ? static_cast<cudaEvent_t>(events[i]) : nullptr;
 }

@@ -265,6 +265,7 @@ kda_status launch_recurrent(const StepArgs& a, cudaStream_t stream) {
   // Small batches use 16-row CTAs so that even one request spreads over 128
   // CTAs; larger batches use 32-row CTAs to halve the per-CTA fold work.
   const int64_t units = (int64_t)a.B * a.HV;
+  record_stage(0, stream);
   if (units * 8 <= 2 * 152) {
     dim3 grid(kHeadDim / 16, a.HV, a.B);
     recurrent_kernel<MODE, 1><<<grid, 128, 0, stream>>>(a);
@@ -272,7 +273,10 @@ kda_status launch_recurrent(const StepArgs& a, cudaStream_t stream) {
     dim3 grid(kHeadDim / 32, a.HV, a.B);
     recurrent_kernel<MODE, 2><<<grid, 128, 0, stream>>>(a);
   }
-  return launch_status();
+  const kda_status s = launch_status();
+  record_stage(1, stream);
+  record_stage(2, stream);
+  return s;
 }
 
 kda_status check_packed(const kda_dims& dims, const kda_gate& gate, const kda_bf16* mixed_qkv,
@@ -380,7 +384,12 @@ extern "C" kda_status kda_commit(kda_dims dims, const float* snapshots, int B, i
   // 16 KiB per CTA: a 1 MiB slot spreads over 64 CTAs per request.
   const int per_slot = (int)((slot_elems * sizeof(float) + 16383) / 16384);
   dim3 grid(per_slot, B);
-  commit_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
-      snapshots, T, accepted, state_pool, pool_slots, state_idx, slot_elems, err_flag);
-  return launch_status();
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  record_stage(0, st);
+  commit_kernel<<<grid, 256, 0, st>>>(snapshots, T, accepted, state_pool, pool_slots, state_idx,
+                                      slot_elems, err_flag);
+  s = launch_status();
+  record_stage(1, st);
+  record_stage(2, st);
+  return s;
 }

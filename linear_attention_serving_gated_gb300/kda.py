@@ -51,7 +51,7 @@ class kda_gate(ctypes.Structure):
 
 
 EXPORTS = ("kda_status_string", "kda_prefill_workspace_size", "kda_prefill", "kda_decode_packed",
-           "kda_verify_chain", "kda_verify_tree", "kda_commit", "kda_prefill_set_stage_events",
+           "kda_verify_chain", "kda_verify_tree", "kda_commit", "kda_set_stage_events",
            "kda_prefill_noalloc")
 
 PREFILL_STATIC_SCRATCH_BYTES = 128 << 20
@@ -88,8 +88,8 @@ def load(path: str = LIB_PATH):
         lib.kda_prefill_noalloc.restype = i32
         lib.kda_prefill_noalloc.argtypes = [kda_dims, kda_gate, vp, vp, vp, vp, vp, i64, vp, i32, vp,
                                             vp, i32, i64, vp, vp, vp, vp]
-        lib.kda_prefill_set_stage_events.restype = None
-        lib.kda_prefill_set_stage_events.argtypes = [ctypes.POINTER(ctypes.c_void_p)]
+        lib.kda_set_stage_events.restype = None
+        lib.kda_set_stage_events.argtypes = [ctypes.POINTER(ctypes.c_void_p)]
         _lib = lib
     return _lib
 
@@ -217,11 +217,13 @@ def kda_commit(d, snapshots, B, T, accepted, state_pool, state_idx, err_flag=Non
     _check(st, "kda_commit")
 
 
-def kda_prefill_set_stage_events(events=None):
-    """Profiling aid: torch.cuda.Event triple recorded by every later
-    kda_prefill call (before, between its two kernels, after); None clears."""
+def kda_set_stage_events(events=None):
+    """Profiling aid: torch.cuda.Event triple recorded by every later call
+    (before its first kernel, between the prefill's two kernels, after its
+    last kernel); a None entry is not recorded; None clears all three."""
     if events is None:
-        load().kda_prefill_set_stage_events(None)
+        load().kda_set_stage_events(None)
         return
-    arr = (ctypes.c_void_p * 3)(*[ctypes.c_void_p(e.cuda_event) for e in events])
-    load().kda_prefill_set_stage_events(arr)
+    arr = (ctypes.c_void_p * 3)(*[ctypes.c_void_p(e.cuda_event if e is not None else None)
+                                  for e in events])
+    load().kda_set_stage_events(arr)
