@@ -47,7 +47,7 @@ DECODE_B = 48
 VERIFY_B, VERIFY_T = 16, 6
 COMMIT_B = VERIFY_B
 FLUSH_BYTES = 512 << 20
-LAYERS = 8  # decode/verify/commit calls per timed replay
+LAYERS = 8  # default decode/verify/commit calls per timed replay (--layers)
 
 # DRAM traffic per launch from ncu (dram__bytes_read.sum + dram__bytes_write.sum),
 # keyed by kernel; valid only while the kernel sources hash to the recorded value.
@@ -223,14 +223,14 @@ def run_ours(args, rank, world, local_rank):
     p_o = torch.empty((PREFILL_T, H, K), dtype=torch.bfloat16, device=dev)
     ws = torch.empty(kda.kda_prefill_workspace_size(D, 1, PREFILL_T), dtype=torch.uint8, device=dev)
 
-    # Decode, verify and commit run LAYERS calls back to back, each on its own
+    # Decode, verify and commit run args.layers calls back to back, each on its own
     # copy of the state pool, inputs and outputs (as consecutive KDA layers of
     # one model do), so every call starts from data no earlier call touched.
     dd = inputs.decode_inputs(seed=100 + rank, B=DECODE_B, H=H, slots=240)
     vd = inputs.verify_inputs(seed=200 + rank, B=VERIFY_B, T=VERIFY_T, H=H, slots=240)
     d_pool0, v_pool0 = t(dd["pool"]), t(vd["pool"])
     L = []
-    for _ in range(LAYERS):
+    for _ in range(args.layers):
         L.append({
             "DX": {n: bf(dd[n]) for n in ("mixed_qkv", "a", "b")},
             "d_pool": d_pool0.clone(), "d_idx": t(dd["state_idx"]),
@@ -350,7 +350,7 @@ def run_ours(args, rank, world, local_rank):
     wall = time.perf_counter() - wall0
     clocks = sampler.stop() if sampler else None
 
-    # per-call milliseconds of every phase (a layer phase's span / LAYERS)
+    # per-call milliseconds of every phase (a layer phase's span / args.layers)
     ph_ms = {n: [r[n][0].elapsed_time(r[n][2]) / len(calls(n)) for r in records] for n in phases}
     k_ms = {
         "prefill_transform": [r["prefill"][0].elapsed_time(r["prefill"][1]) for r in records],
@@ -425,7 +425,7 @@ def run_ours(args, rank, world, local_rank):
         "prefill_1x4096": {"us": round(statistics.mean(ph_ms["prefill"]) * 1e3, 2),
                            "tok_s": round(value / world, 1),
                            "hbm_frac_of_call": round(prefill_bytes(PREFILL_T) / (statistics.mean(ph_ms["prefill"]) / 1e3) / 1e9 / hbm, 4)},
-        "layers_per_replay": LAYERS,
+        "layers_per_replay": args.layers,
         "decode_b48": {"us": round(statistics.mean(ph_ms["decode"]) * 1e3, 2)},
         "verify_chain_b16x6": {"us": round(statistics.mean(ph_ms["verify_chain"]) * 1e3, 2)},
         "verify_tree_b16x6": {"us": round(statistics.mean(ph_ms["verify_tree"]) * 1e3, 2)},
@@ -440,11 +440,11 @@ def run_ours(args, rank, world, local_rank):
         "data": "synthetic (seeded; q,k,v,a,beta ~N(0,1) BF16, A_log~U(-1,1), dt_bias~N(0,0.1), state~N(0,0.02))",
         "config": {"workload": "KDA prefill 1x4096 tokens, 16 heads x 128 (+ decode B=48, verify 16x6 chain/tree, commit 16)",
                    "timing": (f"CUDA-graph replay per phase; CUDA events recorded as graph nodes around the phase's kernels; "
-                              f"decode/verify/commit: {LAYERS} layer calls back to back, each on its own state pool and "
-                              f"buffers, time per call = span / {LAYERS}"),
+                              f"decode/verify/commit: {args.layers} layer calls back to back, each on its own state pool and "
+                              f"buffers, time per call = span / {args.layers}"),
                    "global_batch": world, "seq_len": PREFILL_T, "heads": H, "head_dim": K,
                    "parallelism": f"replicas x{world}", "l2": "flushed before every phase (512 MiB write, then the same buffer read back); layer calls touch disjoint buffers larger than L2"},
-        "gpu_launches": steps * (2 + (len(phases) - 1) * LAYERS),
+        "gpu_launches": steps * (2 + (len(phases) - 1) * args.layers),
         "phases": phase_out,
         "roofline": roofline,
         "e2e": {"value": round(replica_throughput(PREFILL_T, e2e_steps, world, e2e_ms / 1e3), 1),
@@ -526,6 +526,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=LAYERS,
+                    help="decode/verify/commit calls per timed replay, each on its own buffers")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", args.gpus if "RANK" in os.environ else 1))

@@ -233,6 +233,8 @@ __global__ void __launch_bounds__(128) recurrent_kernel(const StepArgs args) {
   }
 }
 
+constexpr int kCommitVec = 4;  // float4 per thread
+
 __global__ void __launch_bounds__(256) commit_kernel(const float* __restrict__ snapshots, int T,
                                                      const int32_t* __restrict__ accepted,
                                                      float* __restrict__ pool, int pool_slots,
@@ -255,9 +257,20 @@ __global__ void __launch_bounds__(256) commit_kernel(const float* __restrict__ s
   const float4* src = reinterpret_cast<const float4*>(snapshots + ((size_t)r * T + acc) * slot_elems);
   float4* dst = reinterpret_cast<float4*>(pool + (size_t)slot * slot_elems);
   const size_t n4 = slot_elems / 4;
-  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
-       i += (size_t)gridDim.x * blockDim.x)
-    dst[i] = __ldcs(src + i);
+  // each thread moves kCommitVec float4 spaced blockDim.x apart, with all its
+  // loads in flight before the first store
+  const size_t base = (size_t)blockIdx.x * blockDim.x * kCommitVec + threadIdx.x;
+  float4 v[kCommitVec];
+#pragma unroll
+  for (int e = 0; e < kCommitVec; ++e) {
+    const size_t i = base + (size_t)e * blockDim.x;
+    if (i < n4) v[e] = __ldcs(src + i);
+  }
+#pragma unroll
+  for (int e = 0; e < kCommitVec; ++e) {
+    const size_t i = base + (size_t)e * blockDim.x;
+    if (i < n4) dst[i] = v[e];
+  }
 }
 
 template <int MODE>
@@ -381,8 +394,9 @@ extern "C" kda_status kda_commit(kda_dims dims, const float* snapshots, int B, i
   if (!snapshots || !accepted) return KDA_ERR_NULL_ARG;
   if (!aligned16(snapshots) || !aligned16(state_pool)) return KDA_ERR_ALIGNMENT;
   const size_t slot_elems = (size_t)dims.HV * dims.V * dims.K;
-  // 16 KiB per CTA: a 1 MiB slot spreads over 64 CTAs per request.
-  const int per_slot = (int)((slot_elems * sizeof(float) + 16383) / 16384);
+  // 16 KiB per CTA (256 threads x kCommitVec float4): a 1 MiB slot spreads
+  // over 64 CTAs per request.
+  const int per_slot = (int)((slot_elems / 4 + 256 * kCommitVec - 1) / (256 * kCommitVec));
   dim3 grid(per_slot, B);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   record_stage(0, st);

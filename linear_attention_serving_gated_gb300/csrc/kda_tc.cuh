@@ -30,6 +30,15 @@ __device__ __forceinline__ uint32_t sw128_offset(int row, int col, int rows) {
          static_cast<uint32_t>((cc & 7) << 1);
 }
 
+// As sw128_offset for a 32-bit (TF32) tile: 32 elements per 128-byte line,
+// atom column a holds columns [32a, 32a+32).
+__device__ __forceinline__ uint32_t sw128_offset_f32(int row, int col, int rows) {
+  const int atom = col >> 5, cc = col & 31;
+  const uint32_t chunk = static_cast<uint32_t>((cc >> 2) ^ (row & 7));
+  return static_cast<uint32_t>(atom * rows * 128 + row * 128) + (chunk << 4) +
+         static_cast<uint32_t>((cc & 3) << 2);
+}
+
 // Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
 // 1024 bytes apart (stride byte offset), leading byte offset unused for this
 // layout (encoded as 1), descriptor version 1, base offset 0.
@@ -49,6 +58,16 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
   return (1u << 4)                                   // D format F32
          | (1u << 7)                                 // A format BF16
          | (1u << 10)                                // B format BF16
+         | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
+         | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
+}
+
+// Instruction descriptor of kind::tf32: TF32 A/B, FP32 accumulator, both
+// operands K-major, M x N.
+__host__ __device__ constexpr uint32_t idesc_tf32_f32(int M, int N) {
+  return (1u << 4)                                   // D format F32
+         | (2u << 7)                                 // A format TF32
+         | (2u << 10)                                // B format TF32
          | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
          | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
 }
@@ -97,6 +116,22 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// Bulk copy shared -> global (no tensor map), tracked by this thread's bulk
+// groups.  src, dst 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_s2g(void* dst, const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
+               "r"(smem_u32(src)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// Waits until every committed bulk store of this thread has finished reading
+// shared memory (the source may then be overwritten).
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
 // ---------------------------------------------------------------------------
 // Fences
 
@@ -138,6 +173,17 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint6
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(static_cast<uint32_t>(accumulate))
+      : "memory");
+}
+
+// As mma_bf16 for TF32 operands (K = 8 per instruction, 32 bytes of each row).
+__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, bool accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(static_cast<uint32_t>(accumulate))
       : "memory");
 }
@@ -184,6 +230,23 @@ __device__ __forceinline__ void split_bf16(float x, uint16_t& hi, uint16_t& lo) 
   const __nv_bfloat16 h = __float2bfloat16_rn(x);
   hi = __bfloat16_as_ushort(h);
   lo = __bfloat16_as_ushort(__float2bfloat16_rn(x - __bfloat162float(h)));
+}
+
+// FP32 -> TF32 rounded to nearest (ties away from zero), low 13 bits zero, so
+// that the tensor core's use of the top 19 bits is exact.
+__device__ __forceinline__ uint32_t tf32_rna(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return r;
+}
+
+// Eight consecutive values of row `row`, columns [col, col+8) (col a multiple
+// of 8), rounded to TF32 into a swizzled K-major 32-bit tile of `rows` rows.
+__device__ __forceinline__ void st_tf32x8(uint8_t* tile, int row, int col, int rows, const float* x) {
+  *reinterpret_cast<uint4*>(tile + sw128_offset_f32(row, col, rows)) =
+      make_uint4(tf32_rna(x[0]), tf32_rna(x[1]), tf32_rna(x[2]), tf32_rna(x[3]));
+  *reinterpret_cast<uint4*>(tile + sw128_offset_f32(row, col + 4, rows)) =
+      make_uint4(tf32_rna(x[4]), tf32_rna(x[5]), tf32_rna(x[6]), tf32_rna(x[7]));
 }
 
 }  // namespace tc
