@@ -119,6 +119,19 @@ size_t kda_prefill_workspace_size(kda_dims dims, int num_seqs, int64_t total_tok
  * T = 1 takes the same kernels as any other length.  The first call on each
  * device sets the kernels' shared-memory limits (cudaFuncSetAttribute); make
  * it before capturing calls into a CUDA graph.
+ *
+ * Schedule: when every sequence has the same length known on the host (one
+ * sequence, or the fixed layout) and spans at least 32 chunks, and
+ * 4 * HV * num_seqs does not exceed the SM count, the chunk positions are cut
+ * into up to four segments.  Each segment's state pass runs on a second,
+ * highest-priority stream owned by the library while the next segment's
+ * transform runs on `stream`.  The state is carried in its pool slot.  That
+ * stream and its events are created on the first such call made by each host
+ * thread on each device; make that call before any capture too.  They are
+ * forked from and joined back to `stream` with events, so ordering relative
+ * to `stream` is unchanged: the call completes when `stream` passes it, and
+ * under capture the fork and join become graph edges.  Results are bit-for-bit
+ * those of the one-segment schedule.
  */
 kda_status kda_prefill(kda_dims dims, kda_gate gate, const kda_bf16 *q, const kda_bf16 *k,
                        const kda_bf16 *v, const kda_bf16 *g, const kda_bf16 *beta,

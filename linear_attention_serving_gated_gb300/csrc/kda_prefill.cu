@@ -98,6 +98,10 @@ struct PrefillArgs {
   float* intermediate;
   uint8_t* ws;
   int32_t* err_flag;
+  // Position segment (seg_len > 0): this launch handles chunk positions
+  // [seg_pos0, seg_pos0 + seg_len) of every sequence, each of which has
+  // seq_nch chunks.  seg_len == 0: every chunk.
+  int seg_pos0, seg_len, seq_nch;
 };
 
 __device__ __forceinline__ int64_t seq_begin(const PrefillArgs& a, int n) {
@@ -245,6 +249,7 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
   __shared__ uint64_t mma_bar;
   __shared__ uint32_t tmem_base;
   __shared__ ChunkLoc loc;
+  __shared__ int64_t s_cid;
   __shared__ int skip, s_abort;
 
   uint8_t* sb = smraw + ((1024u - (tc::smem_u32(smraw) & 1023u)) & 1023u);
@@ -270,15 +275,22 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int h = blockIdx.y;
-  const int64_t cid = blockIdx.x;
   if (tid == 0) {
     skip = 0;
     s_abort = 0;
     if (!seqlens_valid(a)) {
       skip = 1;
-      if (cid == 0 && h == 0) set_error(a.err_flag, KDA_DEVERR_SEQLENS);
+      if (blockIdx.x == 0 && h == 0) set_error(a.err_flag, KDA_DEVERR_SEQLENS);
     } else {
-      loc = locate_chunk(a, cid);
+      if (a.seg_len > 0) {  // (sequence, position) of this CTA in the segment
+        const int n = blockIdx.x / a.seg_len, pos = a.seg_pos0 + blockIdx.x % a.seg_len;
+        const int64_t b = seq_begin(a, n) + (int64_t)pos * kChunk, e = seq_begin(a, n + 1);
+        loc = b < e ? ChunkLoc{n, b, (int)(e - b < kChunk ? e - b : kChunk)} : ChunkLoc{-1, 0, 0};
+        s_cid = (int64_t)n * a.seq_nch + pos;
+      } else {
+        loc = locate_chunk(a, blockIdx.x);
+        s_cid = blockIdx.x;
+      }
       if (loc.n < 0) {
         skip = 1;
       } else {
@@ -291,6 +303,7 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
   }
   __syncthreads();
   if (skip) return;
+  const int64_t cid = s_cid;
   if (warp == 0) tc::tmem_alloc(&tmem_base, kTxTmemCols);
   const int len = loc.len;
   const int64_t t0 = loc.t0;
@@ -795,15 +808,22 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
   __syncthreads();
   if (s_state == 2) return;
   const int64_t t0 = s_t0, t1 = s_t1;
+  // chunk positions [p0, p1) of this sequence in this launch
+  const int nch_seq = (int)((t1 - t0 + kChunk - 1) / kChunk);
+  const int p0 = a.seg_len > 0 ? (a.seg_pos0 < nch_seq ? a.seg_pos0 : nch_seq) : 0;
+  const int p1 = a.seg_len > 0 ? (p0 + a.seg_len < nch_seq ? p0 + a.seg_len : nch_seq) : nch_seq;
   if (s_state == 1) {  // padding sequence: zero outputs
-    for (int64_t idx = tid; idx < (t1 - t0) * kVs; idx += kPassThreads)
-      a.o[((t0 + idx / kVs) * HV + h) * V + v0 + idx % kVs] = 0;
+    const int64_t ta = t0 + (int64_t)p0 * kChunk;
+    const int64_t tb = t0 + (int64_t)p1 * kChunk < t1 ? t0 + (int64_t)p1 * kChunk : t1;
+    for (int64_t idx = tid; idx < (tb - ta) * kVs; idx += kPassThreads)
+      a.o[((ta + idx / kVs) * HV + h) * V + v0 + idx % kVs] = 0;
     return;
   }
-  const int nch = (int)((t1 - t0 + kChunk - 1) / kChunk);
+  if (p0 >= p1) return;  // no chunk of this sequence in this segment
+  const int nch = p1 - p0;  // chunks handled here; chunk i of them is position p0 + i
   const int slot = a.state_idx[n];
   float* st = a.pool + ((size_t)slot * HV + h) * V * K;
-  const uint8_t* ws_head = a.ws + ((size_t)s_cbase * HV + h) * kRecBytes;
+  const uint8_t* ws_head = a.ws + ((size_t)(s_cbase + p0) * HV + h) * kRecBytes;
   const size_t rec_stride = (size_t)HV * kRecBytes;
 
   int issued = 0;    // chunks whose loads have been issued (thread 32)
@@ -847,8 +867,8 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
   for (int ci = 0; ci < nch; ++ci) {
     const int sidx = ci & 1;
     uint8_t* stage = smb + sidx * kStageBytes;
-    const int64_t cid = s_cbase + ci;
-    const int64_t tc0 = t0 + (int64_t)ci * kChunk;
+    const int64_t cid = s_cbase + p0 + ci;
+    const int64_t tc0 = t0 + (int64_t)(p0 + ci) * kChunk;
     const int len = (int)(t1 - tc0 < kChunk ? t1 - tc0 : kChunk);
     if (a.intermediate) {
       float* dst = a.intermediate + ((size_t)cid * HV + h) * V * K;
@@ -966,17 +986,59 @@ int64_t max_chunks(int num_seqs, int64_t total_tokens) {
 
 constexpr int kMaxDevices = 64;
 bool g_attributes_set[kMaxDevices] = {};
+int g_num_sms[kMaxDevices] = {};
 
-kda_status ensure_kernel_attributes() {
+// Sets the kernels' shared-memory limits and reads the SM count, once per
+// device; returns the current device.
+kda_status ensure_kernel_attributes(int* dev_out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KDA_ERR_CUDA;
+  *dev_out = dev;
   if (g_attributes_set[dev]) return KDA_OK;
   if (cudaFuncSetAttribute(chunk_transform_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)kTransformTcSmem) != cudaSuccess ||
       cudaFuncSetAttribute(state_pass_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)kPassSmem) != cudaSuccess)
+                           (int)kPassSmem) != cudaSuccess ||
+      cudaDeviceGetAttribute(&g_num_sms[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return KDA_ERR_CUDA;
   g_attributes_set[dev] = true;
+  return KDA_OK;
+}
+
+// Segmented schedule.  When every sequence has the same number of chunks and
+// the state pass occupies at most one wave of SMs, the chunk positions are cut
+// into up to kMaxSegments segments of at least kSegmentMinChunks: the pass of
+// segment s runs on a second stream while the transform of segment s+1 runs on
+// the caller's, so the pass (latency-bound, a few SMs) hides under the
+// transform (throughput-bound, all SMs).  The state is carried between pass
+// segments in its pool slot.
+constexpr int kMaxSegments = 4;
+constexpr int kSegmentMinChunks = 16;
+
+// The second stream (highest priority, so the pass's CTAs are placed before
+// the transform's waiting ones) and its events: one set per host thread and
+// device, created on the first segmented call and kept for the process.
+struct PassStream {
+  cudaStream_t stream = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr, seg[kMaxSegments] = {};
+  bool ready = false;
+};
+thread_local PassStream t_pass[kMaxDevices];
+
+kda_status pass_stream(int dev, PassStream** out) {
+  PassStream& p = t_pass[dev];
+  if (!p.ready) {
+    int least = 0, greatest = 0;
+    if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess ||
+        cudaStreamCreateWithPriority(&p.stream, cudaStreamNonBlocking, greatest) != cudaSuccess ||
+        cudaEventCreateWithFlags(&p.fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&p.join, cudaEventDisableTiming) != cudaSuccess)
+      return KDA_ERR_CUDA;
+    for (int i = 0; i < kMaxSegments; ++i)
+      if (cudaEventCreateWithFlags(&p.seg[i], cudaEventDisableTiming) != cudaSuccess) return KDA_ERR_CUDA;
+    p.ready = true;
+  }
+  *out = &p;
   return KDA_OK;
 }
 
@@ -1041,19 +1103,59 @@ extern "C" kda_status kda_prefill(kda_dims dims, kda_gate gate, const kda_bf16* 
   args.err_flag = err_flag;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
-  // Kernel shared-memory limits are set once per device, on the first call
-  // made with that device current (so that first call should precede any
-  // stream capture).
-  if ((s = ensure_kernel_attributes()) != KDA_OK) return s;
+  // Kernel shared-memory limits are set once per device, and the second
+  // stream of the segmented schedule is created once per host thread and
+  // device, on the first call made with that device current (so that first
+  // call should precede any stream capture).
+  int dev = 0;
+  if ((s = ensure_kernel_attributes(&dev)) != KDA_OK) return s;
   const int64_t chunks = max_chunks(num_seqs, total_tokens);
-  record_stage(0, st);
-  if (chunks > 0) {
-    chunk_transform_tc_kernel<<<dim3((unsigned)chunks, dims.HV), kTxThreads, kTransformTcSmem, st>>>(args);
-    if ((s = launch_status()) != KDA_OK) return s;
+  const dim3 pass_grid(kSlices, dims.HV, num_seqs);
+  int nseg = 1, seq_nch = 0;
+  if (total_tokens > 0 && (num_seqs == 1 || !cu_seqlens) &&
+      (int64_t)kSlices * dims.HV * num_seqs <= g_num_sms[dev]) {
+    seq_nch = (int)((total_tokens / num_seqs + kChunk - 1) / kChunk);
+    nseg = seq_nch / kSegmentMinChunks < kMaxSegments ? seq_nch / kSegmentMinChunks : kMaxSegments;
   }
-  record_stage(1, st);
-  state_pass_kernel<<<dim3(kSlices, dims.HV, num_seqs), kPassThreads, kPassSmem, st>>>(args);
-  s = launch_status();
+  record_stage(0, st);
+  if (nseg <= 1) {
+    if (chunks > 0) {
+      chunk_transform_tc_kernel<<<dim3((unsigned)chunks, dims.HV), kTxThreads, kTransformTcSmem, st>>>(args);
+      if ((s = launch_status()) != KDA_OK) return s;
+    }
+    record_stage(1, st);
+    state_pass_kernel<<<pass_grid, kPassThreads, kPassSmem, st>>>(args);
+    s = launch_status();
+  } else {
+    PassStream* ps = nullptr;
+    if ((s = pass_stream(dev, &ps)) != KDA_OK) return s;
+    if (cudaEventRecord(ps->fork, st) != cudaSuccess ||
+        cudaStreamWaitEvent(ps->stream, ps->fork, 0) != cudaSuccess)
+      return KDA_ERR_CUDA;
+    const int seg = (seq_nch + nseg - 1) / nseg;
+    for (int i = 0; i < nseg && s == KDA_OK; ++i) {
+      PrefillArgs sa = args;
+      sa.seg_pos0 = i * seg;
+      sa.seg_len = seq_nch - i * seg < seg ? seq_nch - i * seg : seg;
+      sa.seq_nch = seq_nch;
+      if (sa.seg_len <= 0) break;
+      chunk_transform_tc_kernel<<<dim3((unsigned)(num_seqs * sa.seg_len), dims.HV), kTxThreads,
+                                  kTransformTcSmem, st>>>(sa);
+      if ((s = launch_status()) != KDA_OK) break;
+      if (cudaEventRecord(ps->seg[i], st) != cudaSuccess ||
+          cudaStreamWaitEvent(ps->stream, ps->seg[i], 0) != cudaSuccess) {
+        s = KDA_ERR_CUDA;
+        break;
+      }
+      state_pass_kernel<<<pass_grid, kPassThreads, kPassSmem, ps->stream>>>(sa);
+      s = launch_status();
+    }
+    record_stage(1, st);
+    // always join, so that a capture of `st` stays well formed
+    if (cudaEventRecord(ps->join, ps->stream) != cudaSuccess ||
+        cudaStreamWaitEvent(st, ps->join, 0) != cudaSuccess)
+      s = KDA_ERR_CUDA;
+  }
   record_stage(2, st);
   return s;
 }

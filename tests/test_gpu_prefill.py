@@ -162,3 +162,78 @@ def test_chunked_prefill_across_calls_matches_one_call():
     assert_o_close(torch.cat(outs), o_ref)
     s = int(d["state_idx"][0])
     assert_s_close(pool[s], opool[s])
+
+
+# --- segmented schedule -----------------------------------------------------
+# A long single sequence (or equal-length fixed layout) whose state pass fits
+# in one wave runs in position segments, the pass of segment s on a second
+# stream alongside the transform of segment s+1, the state carried in the
+# pool slot.  These cases pin the segment edges and the carry.
+
+@pytest.mark.parametrize("T", [2048 + 452, 4097])
+def test_segmented_prefill_ragged_tail_with_chunk_states(T):
+    """1 x T at 2 heads: 40 or 65 chunk positions cut into 2 or 4 segments,
+    the last chunk ragged (4 tokens, 1 token); chunk-start states too."""
+    d = inputs.prefill_inputs(seed=T, lengths=[T], H=2, slots=3, state_idx=[2])
+    check(run_both(d, 2, intermediate=True), d)
+
+
+def test_segmented_prefill_fixed_layout_with_padding_sequence():
+    d = inputs.prefill_inputs(seed=70, lengths=[2100, 2100], H=2, slots=4, state_idx=[3, -1],
+                              varlen=False)
+    out = run_both(d, 2, varlen=False)
+    check(out, d)
+    assert torch.all(out["o"][2100:].float() == 0)
+
+
+def test_segmented_prefill_bitwise_equals_unsegmented_batch():
+    """Sequence A alone (one sequence: segmented) and the same tokens as the
+    first sequence of a varlen batch of two (not segmented) give identical
+    bits: the schedule does not change the arithmetic."""
+    H, TA, TB = 4, 2500, 100
+    d = inputs.prefill_inputs(seed=80, lengths=[TA, TB], H=H, slots=4, state_idx=[1, 3])
+    og, gg = gates(d, H=H)
+    x = {name: dev_bf16(d[name]) for name in ("q", "k", "v", "g", "beta")}
+    pool0 = dev(d["pool"])
+
+    pool_a = pool0.clone()
+    o_a = torch.zeros((TA, H, K), dtype=torch.bfloat16, device="cuda")
+    kda.kda_prefill(kda.dims(H), gg, *(x[n][:TA].contiguous() for n in ("q", "k", "v", "g", "beta")),
+                    pool_a, dev(np.array([1], np.int32)), dev(np.array([0, TA], np.int32)), 1, o_a)
+    pool_b = pool0.clone()
+    o_b = torch.zeros((TA + TB, H, K), dtype=torch.bfloat16, device="cuda")
+    kda.kda_prefill(kda.dims(H), gg, x["q"], x["k"], x["v"], x["g"], x["beta"], pool_b,
+                    dev(d["state_idx"]), dev(d["cu_seqlens"]), 2, o_b)
+    torch.cuda.synchronize()
+    assert torch.equal(o_a, o_b[:TA])
+    assert torch.equal(pool_a[1], pool_b[1])
+
+
+def test_segmented_prefill_under_graph_capture_matches_eager():
+    """The fork to the pass stream and the join back are captured as graph
+    edges: a replay gives the eager result bit for bit."""
+    H, T = 16, 4096
+    d = inputs.prefill_inputs(seed=90, lengths=[T], H=H, slots=2, state_idx=[1])
+    og, gg = gates(d, H=H)
+    x = {name: dev_bf16(d[name]) for name in ("q", "k", "v", "g", "beta")}
+    idx, cu = dev(d["state_idx"]), dev(d["cu_seqlens"])
+    pool0 = dev(d["pool"])
+    ws = torch.empty(kda.kda_prefill_workspace_size(kda.dims(H), 1, T), dtype=torch.uint8, device="cuda")
+
+    pool_e = pool0.clone()
+    o_e = torch.empty((T, H, K), dtype=torch.bfloat16, device="cuda")
+    kda.kda_prefill(kda.dims(H), gg, x["q"], x["k"], x["v"], x["g"], x["beta"], pool_e, idx, cu, 1, o_e,
+                    workspace=ws)
+    torch.cuda.synchronize()
+
+    pool_g = pool0.clone()
+    o_g = torch.empty_like(o_e)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        kda.kda_prefill(kda.dims(H), gg, x["q"], x["k"], x["v"], x["g"], x["beta"], pool_g, idx, cu, 1,
+                        o_g, workspace=ws)
+    pool_g.copy_(pool0)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(o_g, o_e)
+    assert torch.equal(pool_g, pool_e)
