@@ -51,7 +51,11 @@ LAYERS = 8  # default decode/verify/commit calls per timed replay (--layers)
 
 # DRAM traffic per launch from ncu (dram__bytes_read.sum + dram__bytes_write.sum),
 # keyed by kernel; valid only while the kernel sources hash to the recorded value.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    # the four segment launches of one 1x4096 prefill call, 16 heads: read
+    # 67,593,728 B + write 10,240 B (profiles/chunk_transform_1x4096_h16.md)
+    "prefill_transform": {"bytes": 67603968, "src": "252242181ca7a494"},
+}
 
 
 def _peaks():

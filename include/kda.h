@@ -100,7 +100,11 @@ size_t kda_prefill_workspace_size(kda_dims dims, int num_seqs, int64_t total_tok
  * Chunked varlen prefill from an indexed initial-state pool (chunk_kda).
  *   q, k          [total_tokens, H, K]    BF16
  *   v             [total_tokens, HV, V]   BF16
- *   g             [gb_rows, HV, K] BF16: gate input a (A_log given) or log-decay
+ *   g             [gb_rows, HV, K] BF16: gate input a (A_log given) or log-decay.
+ *                 The chunk form needs per-token log-decays >= -5.5: a bounded
+ *                 gate with lower_bound < -5.5 returns KDA_ERR_UNSUPPORTED, and
+ *                 given log-decays must respect the same bound (the pages' gate
+ *                 uses -5).
  *   beta          [gb_rows, HV]    BF16: raw beta (beta_is_raw) or beta
  *   gb_rows       >= total_tokens (else KDA_ERR_SHAPE).  Rows past
  *                 total_tokens are CUDA-graph bucket padding and never read.

@@ -175,6 +175,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 //        (rows 64-127).  M=128 N=256 K=64.
 // A2 and M2 use BF16 hi/lo splits of both operands (three MMAs each).
 
+constexpr float kMinLogDecay = -5.5f;  // smallest per-token log-decay the windows allow
 constexpr int kLdB = 136;       // padded row stride (BF16 elements) of the raw q, k, v tiles
 constexpr int kTxThreads = 1024;
 constexpr int kTxWarps = kTxThreads / 32;
@@ -1078,6 +1079,9 @@ extern "C" kda_status kda_prefill(kda_dims dims, kda_gate gate, const kda_bf16* 
   PrefillArgs args{};
   s = check_gate(gate, &args.gate);
   if (s != KDA_OK) return s;
+  // The chunk transform's decay-factor windows stay inside FP32 range for
+  // per-token log-decays >= kMinLogDecay; a bounded gate below it is refused.
+  if (gate.A_log && gate.lower_bound < kMinLogDecay) return KDA_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(state_pool) ||
       !aligned16(o) || (intermediate && !aligned16(intermediate)))
     return KDA_ERR_ALIGNMENT;
