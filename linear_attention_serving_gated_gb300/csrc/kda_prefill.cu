@@ -102,6 +102,7 @@ struct PrefillArgs {
   // [seg_pos0, seg_pos0 + seg_len) of every sequence, each of which has
   // seq_nch chunks.  seg_len == 0: every chunk.
   int seg_pos0, seg_len, seq_nch;
+  int64_t tx_units;  // (chunk, head) units of this transform launch
 };
 
 __device__ __forceinline__ int64_t seq_begin(const PrefillArgs& a, int n) {
@@ -245,13 +246,50 @@ __device__ __forceinline__ float4 bf16x4_to_f4(uint2 u) {
                      __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
 }
 
+// Four consecutive BF16 values of row t, columns [c, c+4), of a raw tile.
+__device__ __forceinline__ float4 ld_bf16x4(const uint8_t* tile, int t, int c) {
+  return bf16x4_to_f4(*reinterpret_cast<const uint2*>(tile + (t * kLdB + c) * 2));
+}
+
+__device__ __forceinline__ float4 scale4(float4 a, float s) {
+  return make_float4(a.x * s, a.y * s, a.z * s, a.w * s);
+}
+
+__device__ __forceinline__ float4 mul4(float4 a, float4 b) {
+  return make_float4(a.x * b.x, a.y * b.y, a.z * b.z, a.w * b.w);
+}
+
+// e^{a - b} element-wise, for decay factors.
+__device__ __forceinline__ float4 exp_diff4(float4 a, float4 b) {
+  return make_float4(decay_exp(a.x - b.x), decay_exp(a.y - b.y), decay_exp(a.z - b.z),
+                     decay_exp(a.w - b.w));
+}
+
+// Chunk of transform unit u (chunk-major: u = chunk slot * HV + head): its
+// sequence, first token and length (n = -1 if the slot holds no chunk), its
+// global chunk id and its head.
+__device__ ChunkLoc unit_loc(const PrefillArgs& a, int64_t u, int64_t* cid, int* h) {
+  const int64_t cx = u / a.HV;
+  *h = (int)(u % a.HV);
+  if (a.seg_len > 0) {  // (sequence, position) within the segment
+    const int n = (int)(cx / a.seg_len), pos = a.seg_pos0 + (int)(cx % a.seg_len);
+    const int64_t b = seq_begin(a, n) + (int64_t)pos * kChunk, e = seq_begin(a, n + 1);
+    *cid = (int64_t)n * a.seq_nch + pos;
+    return b < e ? ChunkLoc{n, b, (int)(e - b < kChunk ? e - b : kChunk)} : ChunkLoc{-1, 0, 0};
+  }
+  *cid = cx;
+  return locate_chunk(a, cx);
+}
+
+// Persistent: CTA b takes units b, b + gridDim.x, ...  While it works on one
+// unit, the next unit's q, k, v and gate rows are prefetched into L2.
 __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const PrefillArgs a) {
   extern __shared__ uint8_t smraw[];
   __shared__ uint64_t mma_bar;
   __shared__ uint32_t tmem_base;
-  __shared__ ChunkLoc loc;
+  __shared__ ChunkLoc loc, s_pf;
   __shared__ int64_t s_cid;
-  __shared__ int skip, s_abort;
+  __shared__ int skip, s_abort, s_ok, s_h, s_pf_h;
 
   uint8_t* sb = smraw + ((1024u - (tc::smem_u32(smraw) & 1023u)) & 1023u);
   uint8_t* Lt = sb + kTxL;  // M1 left operand, TF32 128 x 128
@@ -275,459 +313,476 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
   float* X = bt + kChunk;  // [6][16][16]
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int h = blockIdx.y;
   if (tid == 0) {
-    skip = 0;
     s_abort = 0;
-    if (!seqlens_valid(a)) {
-      skip = 1;
-      if (blockIdx.x == 0 && h == 0) set_error(a.err_flag, KDA_DEVERR_SEQLENS);
-    } else {
-      if (a.seg_len > 0) {  // (sequence, position) of this CTA in the segment
-        const int n = blockIdx.x / a.seg_len, pos = a.seg_pos0 + blockIdx.x % a.seg_len;
-        const int64_t b = seq_begin(a, n) + (int64_t)pos * kChunk, e = seq_begin(a, n + 1);
-        loc = b < e ? ChunkLoc{n, b, (int)(e - b < kChunk ? e - b : kChunk)} : ChunkLoc{-1, 0, 0};
-        s_cid = (int64_t)n * a.seq_nch + pos;
-      } else {
-        loc = locate_chunk(a, blockIdx.x);
-        s_cid = blockIdx.x;
-      }
-      if (loc.n < 0) {
-        skip = 1;
-      } else {
-        const int slot = a.state_idx[loc.n];
-        if (slot < 0 || slot >= a.pool_slots) skip = 1;  // padding / rejected sequence
-      }
-    }
+    s_ok = seqlens_valid(a);
+    if (!s_ok && blockIdx.x == 0) set_error(a.err_flag, KDA_DEVERR_SEQLENS);
     tc::mbar_init(&mma_bar, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  __syncthreads();
-  if (skip) return;
-  const int64_t cid = s_cid;
   if (warp == 0) tc::tmem_alloc(&tmem_base, kTxTmemCols);
-  const int len = loc.len;
-  const int64_t t0 = loc.t0;
-  const GateArgs& ga = a.gate;
-  const int H = a.H, HV = a.HV, K = kHeadDim;
-  uint8_t* rec = a.ws + ((size_t)cid * HV + h) * kRecBytes;
-
-  // 1. fold.  Warp w owns tokens [4w, 4w+4), lane l channels [4l, 4l+4); all
-  //    global loads of the warp are issued before any use.  Raw q, k, v stay
-  //    BF16 in shared memory, with the per-token norms; Gam by warp-blocked prefix.
-  {
-    constexpr int kTpw = kChunk / kTxWarps;  // tokens per warp
-    float* tot = reinterpret_cast<float*>(sb + kTxL);  // [kTxWarps][128] warp totals
-    const int c = lane * 4;
-    uint2 qr[kTpw], kr[kTpw], vr[kTpw], ar[kTpw];
-    float br[kTpw];
-    const float alog = ga.A_log ? __ldg(ga.A_log + h) : 0.f;
-    const float4 bias = ga.dt_bias ? __ldg(reinterpret_cast<const float4*>(ga.dt_bias + h * K + c))
-                                   : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int u = 0; u < kTpw; ++u) {
-      const int t = warp * kTpw + u;
-      qr[u] = kr[u] = vr[u] = ar[u] = make_uint2(0u, 0u);
-      br[u] = 0.f;
-      if (t < len) {
-        const int64_t tok = t0 + t;
-        qr[u] = __ldg(reinterpret_cast<const uint2*>(a.q + (tok * H + h) * K + c));
-        kr[u] = __ldg(reinterpret_cast<const uint2*>(a.k + (tok * H + h) * K + c));
-        vr[u] = __ldg(reinterpret_cast<const uint2*>(a.v + (tok * HV + h) * K + c));
-        ar[u] = __ldg(reinterpret_cast<const uint2*>(a.g + (tok * HV + h) * K + c));
-        if (lane == 0) br[u] = bf16_bits_to_float(a.beta[tok * HV + h]);
-      }
-    }
-    const float exp_alog = __expf(alog);
-    float4 run = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int u = 0; u < kTpw; ++u) {
-      const int t = warp * kTpw + u;
-      const bool live = t < len;
-      const float4 q4 = bf16x4_to_f4(qr[u]), k4 = bf16x4_to_f4(kr[u]), a4 = bf16x4_to_f4(ar[u]);
-      const float sq = warp_sum(dot4(q4, q4)), sk = warp_sum(dot4(k4, k4));
-      float4 g4 = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (live)
-        g4 = make_float4(gate_log_decay(ga, a4.x, exp_alog, bias.x),
-                         gate_log_decay(ga, a4.y, exp_alog, bias.y),
-                         gate_log_decay(ga, a4.z, exp_alog, bias.z),
-                         gate_log_decay(ga, a4.w, exp_alog, bias.w));
-      if (lane == 0) {
-        rq[t] = live ? (ga.use_qk_l2norm ? rsqrtf(sq + kNormEps) : 1.f) : 0.f;
-        rk[t] = live ? (ga.use_qk_l2norm ? rsqrtf(sk + kNormEps) : 1.f) : 0.f;
-        bt[t] = live ? fold_beta(ga, br[u]) : 0.f;
-      }
-      *reinterpret_cast<uint2*>(Qs + (t * kLdB + c) * 2) = qr[u];
-      *reinterpret_cast<uint2*>(Ks + (t * kLdB + c) * 2) = kr[u];
-      *reinterpret_cast<uint2*>(Vs + (t * kLdB + c) * 2) = vr[u];
-      run = make_float4(run.x + g4.x, run.y + g4.y, run.z + g4.z, run.w + g4.w);
-      f4(GM + t * kLd + c) = run;
-    }
-    f4(tot + warp * K + c) = run;
-    __syncthreads();
-    float4 pre = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int w = 0; w < warp; ++w) {
-      const float4 x = f4(tot + w * K + c);
-      pre = make_float4(pre.x + x.x, pre.y + x.y, pre.z + x.z, pre.w + x.w);
-    }
-#pragma unroll
-    for (int u = 0; u < kTpw; ++u) {
-      float4& gg = f4(GM + (warp * kTpw + u) * kLd + c);
-      gg = make_float4(gg.x + pre.x, gg.y + pre.y, gg.z + pre.z, gg.w + pre.w);
-    }
-  }
-  __syncthreads();
-
-  // 2. gamma to the workspace; Khat^T (hi/lo, swizzled 128 x 64) built in the
-  //    A2 region (free until step 6) and sent to the workspace as one bulk copy.
-  if (tid < K) reinterpret_cast<float*>(rec + kRecGam)[tid] = decay_exp(GM[(kChunk - 1) * kLd + tid]);
-  for (int idx = tid; idx < K * 8; idx += kTxThreads) {
-    const int c = idx & (K - 1), j = idx >> 7;
-    const float gl = GM[(kChunk - 1) * kLd + c];
-    float x[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const int t = j * 8 + e;
-      x[e] = bf16_at(Ks, t, c) * rk[t] * decay_exp(gl - GM[t * kLd + c]);
-    }
-    st_split8(A2h, A2h + 128 * 64 * 2, tc::sw128_offset(c, j * 8, K), x);
-  }
-  tc::fence_async_smem();
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
-  if (tid == 0) {
-    static_assert(kRecKTl == kRecKTh + 128 * 64 * 2, "Khat^T hi and lo are contiguous");
-    tc::bulk_s2g(rec + kRecKTh, A2h, 2 * 128 * 64 * 2);
-    tc::bulk_commit();
-  }
   const uint32_t tmem = tmem_base;
-  const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
   uint32_t phase = 0;
-
-  // 3. M1 in two rounds (see the header of this kernel).
-  //    L row groups of 32: [Lk, Lq] for the window, R rows [R(window a), R(window b)].
-  for (int round = 0; round < 2; ++round) {
-    // row groups: (t0g, r) for groups 0-1 (rows 0-63) and 2-3 (rows 64-127)
-    const int tA = round == 0 ? 0 : 32, rA = round == 0 ? 15 : 47;
-    const int tB = 32, rB = 31;               // round 0 only
-    for (int idx = tid; idx < 64 * 16; idx += kTxThreads) {
-      const int g = idx >> 9;                  // 0: first window rows, 1: second (round 0 only)
-      const int tt = (idx >> 4) & 31, c = (idx & 15) * 8;
-      if (round == 1 && g == 1) {            // rows 64-127 of round b are zero
-        const float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        tc::st_tf32x8(Lt, 64 + tt, c, 128, z);
-        tc::st_tf32x8(Lt, 96 + tt, c, 128, z);
-        continue;
+  for (int64_t u = blockIdx.x; s_ok && u < a.tx_units; u += gridDim.x) {
+    __syncthreads();  // every thread is done with the previous unit's shared values
+    if (tid == 0) {
+      int64_t cid;
+      int hh;
+      loc = unit_loc(a, u, &cid, &hh);
+      s_cid = cid;
+      s_h = hh;
+      skip = loc.n < 0;
+      if (!skip) {
+        const int slot = a.state_idx[loc.n];
+        if (slot < 0 || slot >= a.pool_slots) skip = 1;  // padding / rejected sequence
       }
-      const int t = (g == 0 ? tA : tB) + tt, r = g == 0 ? rA : rB;
-      float gt[8], gr[8], xk[8], xq[8];
-      ld_f32x8(GM + t * kLd + c, gt);
-      ld_f32x8(GM + r * kLd + c, gr);
-      ld_bf16x8(Ks, t, c, xk);
-      ld_bf16x8(Qs, t, c, xq);
-      const float nk = rk[t], nq = rq[t];
+      s_pf = u + gridDim.x < a.tx_units ? unit_loc(a, u + gridDim.x, &cid, &hh) : ChunkLoc{-1, 0, 0};
+      s_pf_h = hh;
+    }
+    __syncthreads();
+    if (tid < 512 && s_pf.n >= 0) {  // next unit's rows -> L2: 4 tensors x 64 tokens x 2 lines
+      const int tensor = tid >> 7, tok = (tid >> 1) & 63, part = tid & 1;
+      if (tok < s_pf.len) {
+        const int64_t row = s_pf.t0 + tok;
+        const kda_bf16* base = tensor == 0 ? a.q + (row * a.H + s_pf_h) * kHeadDim
+                             : tensor == 1 ? a.k + (row * a.H + s_pf_h) * kHeadDim
+                             : tensor == 2 ? a.v + (row * a.HV + s_pf_h) * kHeadDim
+                                           : a.g + (row * a.HV + s_pf_h) * kHeadDim;
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const uint8_t*>(base) + part * 128));
+      }
+    }
+    if (skip) continue;
+    const int h = s_h;
+    const int64_t cid = s_cid;
+    const int len = loc.len;
+    const int64_t t0 = loc.t0;
+    const GateArgs& ga = a.gate;
+    const int H = a.H, HV = a.HV, K = kHeadDim;
+    uint8_t* rec = a.ws + ((size_t)cid * HV + h) * kRecBytes;
+
+    // 1. fold.  Warp w owns tokens [4w, 4w+4), lane l channels [4l, 4l+4); all
+    //    global loads of the warp are issued before any use.  Raw q, k, v stay
+    //    BF16 in shared memory, with the per-token norms; Gam by warp-blocked prefix.
+    {
+      constexpr int kTpw = kChunk / kTxWarps;  // tokens per warp
+      float* tot = reinterpret_cast<float*>(sb + kTxL);  // [kTxWarps][128] warp totals
+      const int c = lane * 4;
+      uint2 qr[kTpw], kr[kTpw], vr[kTpw], ar[kTpw];
+      float br[kTpw];
+      const float alog = ga.A_log ? __ldg(ga.A_log + h) : 0.f;
+      const float4 bias = ga.dt_bias ? __ldg(reinterpret_cast<const float4*>(ga.dt_bias + h * K + c))
+                                     : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int u = 0; u < kTpw; ++u) {
+        const int t = warp * kTpw + u;
+        qr[u] = kr[u] = vr[u] = ar[u] = make_uint2(0u, 0u);
+        br[u] = 0.f;
+        if (t < len) {
+          const int64_t tok = t0 + t;
+          qr[u] = __ldg(reinterpret_cast<const uint2*>(a.q + (tok * H + h) * K + c));
+          kr[u] = __ldg(reinterpret_cast<const uint2*>(a.k + (tok * H + h) * K + c));
+          vr[u] = __ldg(reinterpret_cast<const uint2*>(a.v + (tok * HV + h) * K + c));
+          ar[u] = __ldg(reinterpret_cast<const uint2*>(a.g + (tok * HV + h) * K + c));
+          if (lane == 0) br[u] = bf16_bits_to_float(a.beta[tok * HV + h]);
+        }
+      }
+      const float exp_alog = __expf(alog);
+      float4 run = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int u = 0; u < kTpw; ++u) {
+        const int t = warp * kTpw + u;
+        const bool live = t < len;
+        const float4 q4 = bf16x4_to_f4(qr[u]), k4 = bf16x4_to_f4(kr[u]), a4 = bf16x4_to_f4(ar[u]);
+        const float sq = warp_sum(dot4(q4, q4)), sk = warp_sum(dot4(k4, k4));
+        float4 g4 = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (live)
+          g4 = make_float4(gate_log_decay(ga, a4.x, exp_alog, bias.x),
+                           gate_log_decay(ga, a4.y, exp_alog, bias.y),
+                           gate_log_decay(ga, a4.z, exp_alog, bias.z),
+                           gate_log_decay(ga, a4.w, exp_alog, bias.w));
+        if (lane == 0) {
+          rq[t] = live ? (ga.use_qk_l2norm ? rsqrtf(sq + kNormEps) : 1.f) : 0.f;
+          rk[t] = live ? (ga.use_qk_l2norm ? rsqrtf(sk + kNormEps) : 1.f) : 0.f;
+          bt[t] = live ? fold_beta(ga, br[u]) : 0.f;
+        }
+        *reinterpret_cast<uint2*>(Qs + (t * kLdB + c) * 2) = qr[u];
+        *reinterpret_cast<uint2*>(Ks + (t * kLdB + c) * 2) = kr[u];
+        *reinterpret_cast<uint2*>(Vs + (t * kLdB + c) * 2) = vr[u];
+        run = make_float4(run.x + g4.x, run.y + g4.y, run.z + g4.z, run.w + g4.w);
+        f4(GM + t * kLd + c) = run;
+      }
+      f4(tot + warp * K + c) = run;
+      __syncthreads();
+      float4 pre = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int w = 0; w < warp; ++w) {
+        const float4 x = f4(tot + w * K + c);
+        pre = make_float4(pre.x + x.x, pre.y + x.y, pre.z + x.z, pre.w + x.w);
+      }
+#pragma unroll
+      for (int u = 0; u < kTpw; ++u) {
+        float4& gg = f4(GM + (warp * kTpw + u) * kLd + c);
+        gg = make_float4(gg.x + pre.x, gg.y + pre.y, gg.z + pre.z, gg.w + pre.w);
+      }
+    }
+    __syncthreads();
+
+    // 2. gamma to the workspace; Khat^T (hi/lo, swizzled 128 x 64) built in the
+    //    A2 region (free until step 6) and sent to the workspace as one bulk copy.
+    if (tid < K) reinterpret_cast<float*>(rec + kRecGam)[tid] = decay_exp(GM[(kChunk - 1) * kLd + tid]);
+    for (int idx = tid; idx < K * 8; idx += kTxThreads) {
+      const int c = idx & (K - 1), j = idx >> 7;
+      const float gl = GM[(kChunk - 1) * kLd + c];
+      float x[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        const float f = decay_exp(gt[e] - gr[e]);
-        xk[e] *= nk * f;
-        xq[e] *= nq * f;
+        const int t = j * 8 + e;
+        x[e] = bf16_at(Ks, t, c) * rk[t] * decay_exp(gl - GM[t * kLd + c]);
       }
-      tc::st_tf32x8(Lt, g * 64 + tt, c, 128, xk);
-      tc::st_tf32x8(Lt, g * 64 + 32 + tt, c, 128, xq);
-    }
-    const int nR = round == 0 ? 64 : 32;
-    for (int idx = tid; idx < nR * 16; idx += kTxThreads) {
-      const int row = idx >> 4, c = (idx & 15) * 8;
-      const int i = round == 0 ? (row & 31) : 32 + row;
-      const int r = round == 0 ? (row < 32 ? 15 : 31) : 47;
-      float gi[8], gr[8], x[8];
-      ld_f32x8(GM + i * kLd + c, gi);
-      ld_f32x8(GM + r * kLd + c, gr);
-      ld_bf16x8(Ks, i, c, x);
-      const float nk = rk[i];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) x[e] *= nk * decay_exp(gr[e] - gi[e]);
-      tc::st_tf32x8(Rt, row, c, nR, x);
+      st_split8(A2h, A2h + 128 * 64 * 2, tc::sw128_offset(c, j * 8, K), x);
     }
     tc::fence_async_smem();
     tc::tc_fence_before();
     __syncthreads();
-    if (tid == 0 && !s_abort) {
-      tc::tc_fence_after();
-      const uint32_t idesc = round == 0 ? tc::idesc_tf32_f32(128, 64) : tc::idesc_tf32_f32(128, 32);
-      const uint32_t la = tc::smem_u32(Lt), ra = tc::smem_u32(Rt);
-#pragma unroll
-      for (int k = 0; k < 16; ++k) {  // K = 128 in steps of 8 (32 bytes of each row)
-        const uint32_t koff = (k & 3) * 32;
-        tc::mma_tf32(tmem + round * 64, tc::sw128_desc(la + (k >> 2) * (128 * 128) + koff),
-                     tc::sw128_desc(ra + (k >> 2) * (nR * 128) + koff), idesc, k > 0);
-      }
-      tc::mma_commit(&mma_bar);
-    }
-    if (!tc::mbar_wait(&mma_bar, phase)) s_abort = 1;
-    phase ^= 1;
     tc::tc_fence_after();
-  }
+    if (tid == 0) {
+      static_assert(kRecKTl == kRecKTh + 128 * 64 * 2, "Khat^T hi and lo are contiguous");
+      tc::bulk_s2g(rec + kRecKTh, A2h, 2 * 128 * 64 * 2);
+      tc::bulk_commit();
+    }
+    const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
 
-  // 4. A (beta-scaled, strictly lower) and P (lower) to FP32.  TMEM columns:
-  //    0-31  rows 0-63   : t = row & 31 (< 32),  i = col        (k rows 0-31, q rows 32-63)
-  //    32-63 rows 64-127 : t = 32 + (row & 31),  i = col - 32
-  //    64-95 rows 0-63   : t = 32 + (row & 31),  i = 32 + col - 64
-  //    warp group 3 writes the zero block t < 32 <= i.
-  {
-    const int wg = warp >> 2, row = (warp & 3) * 32 + lane;
-    if (wg < 3) {
-      float d[32];
-      tc::tmem_ld16(tmem + lane_addr + wg * 32, *reinterpret_cast<float(*)[16]>(d));
-      tc::tmem_ld16(tmem + lane_addr + wg * 32 + 16, *reinterpret_cast<float(*)[16]>(d + 16));
-      const bool use = wg == 1 ? row >= 64 : row < 64;
-      if (use) {
-        const int t = (wg == 0 ? 0 : 32) + (row & 31);
-        const int i0 = wg == 2 ? 32 : 0;
-        const bool is_q = (row & 63) >= 32;
-        float* dst = (is_q ? Pf : Af) + t * kLdT + i0;
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int i = i0 + e;
-          dst[e] = is_q ? (i <= t ? d[e] : 0.f) : (i < t ? bt[t] * d[e] : 0.f);
+    // 3. M1 in two rounds (see the header of this kernel).  Warp w builds the
+    //    rows of token w (round 1) or 32 + w (round 2), lane l channels
+    //    [4l, 4l+4): every shared-memory access of a warp is one whole row.
+    //    Round 1: L rows [Lk(t<32, r=15); Lq(t<32, r=15); Lk(t>=32, r=31);
+    //             Lq(t>=32, r=31)], R rows [R(i<32, r=15); R(i<32, r=31)].
+    //    Round 2: L rows [Lk(t>=32, r=47); Lq(t>=32, r=47)], R rows R(i>=32, r=47);
+    //             L rows 64-127 keep round 1's values and their products are
+    //             never read.
+    static_assert(kTxWarps == 32, "M1 operands: one warp per token row");
+    for (int round = 0; round < 2; ++round) {
+      {
+        const int tt = warp, c = lane * 4;
+        if (round == 0) {
+          const float4 g15 = f4(GM + 15 * kLd + c), g31 = f4(GM + 31 * kLd + c);
+          const float4 ga = f4(GM + tt * kLd + c), gb = f4(GM + (32 + tt) * kLd + c);
+          const float4 ka = scale4(ld_bf16x4(Ks, tt, c), rk[tt]), qa = scale4(ld_bf16x4(Qs, tt, c), rq[tt]);
+          const float4 kb = scale4(ld_bf16x4(Ks, 32 + tt, c), rk[32 + tt]);
+          const float4 qb = scale4(ld_bf16x4(Qs, 32 + tt, c), rq[32 + tt]);
+          const float4 fa = exp_diff4(ga, g15), fb = exp_diff4(gb, g31);
+          tc::st_tf32x4(Lt, tt, c, 128, mul4(ka, fa));
+          tc::st_tf32x4(Lt, 32 + tt, c, 128, mul4(qa, fa));
+          tc::st_tf32x4(Lt, 64 + tt, c, 128, mul4(kb, fb));
+          tc::st_tf32x4(Lt, 96 + tt, c, 128, mul4(qb, fb));
+          tc::st_tf32x4(Rt, tt, c, 64, mul4(ka, exp_diff4(g15, ga)));
+          tc::st_tf32x4(Rt, 32 + tt, c, 64, mul4(ka, exp_diff4(g31, ga)));
+        } else {
+          const int t = 32 + tt;
+          const float4 g47 = f4(GM + 47 * kLd + c), gt = f4(GM + t * kLd + c);
+          const float4 kt = scale4(ld_bf16x4(Ks, t, c), rk[t]), qt = scale4(ld_bf16x4(Qs, t, c), rq[t]);
+          const float4 f = exp_diff4(gt, g47);
+          tc::st_tf32x4(Lt, tt, c, 128, mul4(kt, f));
+          tc::st_tf32x4(Lt, 32 + tt, c, 128, mul4(qt, f));
+          tc::st_tf32x4(Rt, tt, c, 32, mul4(kt, exp_diff4(g47, gt)));
         }
+      }
+      const int nR = round == 0 ? 64 : 32;
+      tc::fence_async_smem();
+      tc::tc_fence_before();
+      __syncthreads();
+      if (tid == 0 && !s_abort) {
+        tc::tc_fence_after();
+        const uint32_t idesc = round == 0 ? tc::idesc_tf32_f32(128, 64) : tc::idesc_tf32_f32(128, 32);
+        const uint32_t la = tc::smem_u32(Lt), ra = tc::smem_u32(Rt);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {  // K = 128 in steps of 8 (32 bytes of each row)
+          const uint32_t koff = (k & 3) * 32;
+          tc::mma_tf32(tmem + round * 64, tc::sw128_desc(la + (k >> 2) * (128 * 128) + koff),
+                       tc::sw128_desc(ra + (k >> 2) * (nR * 128) + koff), idesc, k > 0);
+        }
+        tc::mma_commit(&mma_bar);
+      }
+      if (!tc::mbar_wait(&mma_bar, phase)) s_abort = 1;
+      phase ^= 1;
+      tc::tc_fence_after();
+    }
+
+    // 4. A (beta-scaled, strictly lower) and P (lower) to FP32.  TMEM columns:
+    //    0-31  rows 0-63   : t = row & 31 (< 32),  i = col        (k rows 0-31, q rows 32-63)
+    //    32-63 rows 64-127 : t = 32 + (row & 31),  i = col - 32
+    //    64-95 rows 0-63   : t = 32 + (row & 31),  i = 32 + col - 64
+    //    warp group 3 writes the zero block t < 32 <= i.
+    {
+      const int wg = warp >> 2, row = (warp & 3) * 32 + lane;
+      if (wg < 3) {
+        float d[32];
+        tc::tmem_ld16(tmem + lane_addr + wg * 32, *reinterpret_cast<float(*)[16]>(d));
+        tc::tmem_ld16(tmem + lane_addr + wg * 32 + 16, *reinterpret_cast<float(*)[16]>(d + 16));
+        const bool use = wg == 1 ? row >= 64 : row < 64;
+        if (use) {
+          const int t = (wg == 0 ? 0 : 32) + (row & 31);
+          const int i0 = wg == 2 ? 32 : 0;
+          const bool is_q = (row & 63) >= 32;
+          float* dst = (is_q ? Pf : Af) + t * kLdT + i0;
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int i = i0 + e;
+            dst[e] = is_q ? (i <= t ? d[e] : 0.f) : (i < t ? bt[t] * d[e] : 0.f);
+          }
+        }
+      } else {
+        for (int idx = tid - 384; idx < 32 * 32; idx += kTxThreads - 384) {
+          const int t = idx >> 5, i = 32 + (idx & 31);
+          Af[t * kLdT + i] = 0.f;
+          Pf[t * kLdT + i] = 0.f;
+        }
+      }
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+
+    // 5. (I + A)^-1 = Ti, blocked in 16 x 16.  With T_ii the inverses of the
+    //    diagonal blocks I + A_ii and M_ik = T_ii A_ik (k < i), block forward
+    //    substitution gives T_ij = -sum_{k=j}^{i-1} M_ik T_kj, one block
+    //    diagonal d = i - j at a time.
+    //    5a. T_ii by forward substitution (one column per thread, threads 0-63);
+    //        the other threads zero the strictly upper blocks.
+    if (tid < kChunk) {
+      const int b0 = (tid >> 4) * 16, col = tid & 15;
+      float x[16];
+#pragma unroll
+      for (int r = 0; r < 16; ++r) {
+        float acc = r == col ? 1.f : 0.f;
+#pragma unroll
+        for (int s2 = 0; s2 < r; ++s2) acc -= Af[(b0 + r) * kLdT + b0 + s2] * x[s2];
+        x[r] = acc;
+        Tf[(b0 + r) * kLdT + b0 + col] = acc;
       }
     } else {
-      for (int idx = tid - 384; idx < 32 * 32; idx += kTxThreads - 384) {
-        const int t = idx >> 5, i = 32 + (idx & 31);
-        Af[t * kLdT + i] = 0.f;
-        Pf[t * kLdT + i] = 0.f;
+      for (int idx = tid - kChunk; idx < 6 * 256; idx += kTxThreads - kChunk) {
+        const int blk = idx >> 8, r = (idx >> 4) & 15, cc = idx & 15;
+        const int bi = blk < 3 ? 0 : (blk < 5 ? 1 : 2);               // (0,1) (0,2) (0,3) (1,2) (1,3) (2,3)
+        const int bj = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
+        Tf[(bi * 16 + r) * kLdT + bj * 16 + cc] = 0.f;
       }
-    }
-  }
-  tc::tc_fence_before();
-  __syncthreads();
-
-  // 5. (I + A)^-1 = Ti, blocked in 16 x 16.  With T_ii the inverses of the
-  //    diagonal blocks I + A_ii and M_ik = T_ii A_ik (k < i), block forward
-  //    substitution gives T_ij = -sum_{k=j}^{i-1} M_ik T_kj, one block
-  //    diagonal d = i - j at a time.
-  //    5a. T_ii by forward substitution (one column per thread, threads 0-63);
-  //        the other threads zero the strictly upper blocks.
-  if (tid < kChunk) {
-    const int b0 = (tid >> 4) * 16, col = tid & 15;
-    float x[16];
-#pragma unroll
-    for (int r = 0; r < 16; ++r) {
-      float acc = r == col ? 1.f : 0.f;
-#pragma unroll
-      for (int s2 = 0; s2 < r; ++s2) acc -= Af[(b0 + r) * kLdT + b0 + s2] * x[s2];
-      x[r] = acc;
-      Tf[(b0 + r) * kLdT + b0 + col] = acc;
-    }
-  } else {
-    for (int idx = tid - kChunk; idx < 6 * 256; idx += kTxThreads - kChunk) {
-      const int blk = idx >> 8, r = (idx >> 4) & 15, cc = idx & 15;
-      const int bi = blk < 3 ? 0 : (blk < 5 ? 1 : 2);               // (0,1) (0,2) (0,3) (1,2) (1,3) (2,3)
-      const int bj = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
-      Tf[(bi * 16 + r) * kLdT + bj * 16 + cc] = 0.f;
-    }
-  }
-  __syncthreads();
-  //    5b. M_ik for the six blocks k < i, stored transposed (X[blk][m][r] =
-  //        M_ik[r][m], blk = i(i-1)/2 + k).  64 threads per block, each a
-  //        2 x 2 patch (rows r0, r0+1; columns c0, c0+1).
-  if (tid < 6 * 64) {
-    const int blk = tid >> 6, r0 = ((tid & 63) >> 3) * 2, c0 = (tid & 7) * 2;
-    const int bi = blk < 1 ? 1 : (blk < 3 ? 2 : 3);
-    const int bk = blk - bi * (bi - 1) / 2;
-    const float* Ti0 = Tf + (bi * 16 + r0) * kLdT + bi * 16;
-    const float* Ab = Af + (bi * 16) * kLdT + bk * 16 + c0;
-    float a00 = 0.f, a01 = 0.f, a10 = 0.f, a11 = 0.f;
-#pragma unroll
-    for (int m = 0; m < 16; ++m) {
-      const float t0 = Ti0[m], t1 = Ti0[kLdT + m];
-      const float b0 = Ab[m * kLdT], b1 = Ab[m * kLdT + 1];
-      a00 += t0 * b0; a01 += t0 * b1; a10 += t1 * b0; a11 += t1 * b1;
-    }
-    float* Mt = X + blk * 256;
-    *reinterpret_cast<float2*>(Mt + c0 * 16 + r0) = make_float2(a00, a10);
-    *reinterpret_cast<float2*>(Mt + (c0 + 1) * 16 + r0) = make_float2(a01, a11);
-  }
-  __syncthreads();
-  //    5c. block diagonals d = 1, 2, 3, same patches
-  for (int d = 1; d < 4; ++d) {
-    if (tid < (4 - d) * 64) {
-      const int bj = tid >> 6, r0 = ((tid & 63) >> 3) * 2, c0 = (tid & 7) * 2;
-      const int bi = bj + d;
-      float a00 = 0.f, a01 = 0.f, a10 = 0.f, a11 = 0.f;
-      for (int bk = bj; bk < bi; ++bk) {
-        const float* Mt = X + (bi * (bi - 1) / 2 + bk) * 256 + r0;
-        const float* Tk = Tf + (bk * 16) * kLdT + bj * 16 + c0;
-#pragma unroll
-        for (int m = 0; m < 16; ++m) {
-          const float2 mm = *reinterpret_cast<const float2*>(Mt + m * 16);
-          const float b0 = Tk[m * kLdT], b1 = Tk[m * kLdT + 1];
-          a00 += mm.x * b0; a01 += mm.x * b1; a10 += mm.y * b0; a11 += mm.y * b1;
-        }
-      }
-      float* dst = Tf + (bi * 16 + r0) * kLdT + bj * 16 + c0;
-      dst[0] = -a00; dst[1] = -a01; dst[kLdT] = -a10; dst[kLdT + 1] = -a11;
     }
     __syncthreads();
-  }
+    //    5b. M_ik for the six blocks k < i, stored transposed (X[blk][m][r] =
+    //        M_ik[r][m], blk = i(i-1)/2 + k).  64 threads per block, each a
+    //        2 x 2 patch (rows r0, r0+1; columns c0, c0+1).
+    if (tid < 6 * 64) {
+      const int blk = tid >> 6, r0 = ((tid & 63) >> 3) * 2, c0 = (tid & 7) * 2;
+      const int bi = blk < 1 ? 1 : (blk < 3 ? 2 : 3);
+      const int bk = blk - bi * (bi - 1) / 2;
+      const float* Ti0 = Tf + (bi * 16 + r0) * kLdT + bi * 16;
+      const float* Ab = Af + (bi * 16) * kLdT + bk * 16 + c0;
+      float a00 = 0.f, a01 = 0.f, a10 = 0.f, a11 = 0.f;
+#pragma unroll
+      for (int m = 0; m < 16; ++m) {
+        const float t0 = Ti0[m], t1 = Ti0[kLdT + m];
+        const float b0 = Ab[m * kLdT], b1 = Ab[m * kLdT + 1];
+        a00 += t0 * b0; a01 += t0 * b1; a10 += t1 * b0; a11 += t1 * b1;
+      }
+      float* Mt = X + blk * 256;
+      *reinterpret_cast<float2*>(Mt + c0 * 16 + r0) = make_float2(a00, a10);
+      *reinterpret_cast<float2*>(Mt + (c0 + 1) * 16 + r0) = make_float2(a01, a11);
+    }
+    __syncthreads();
+    //    5c. block diagonals d = 1, 2, 3, same patches
+    for (int d = 1; d < 4; ++d) {
+      if (tid < (4 - d) * 64) {
+        const int bj = tid >> 6, r0 = ((tid & 63) >> 3) * 2, c0 = (tid & 7) * 2;
+        const int bi = bj + d;
+        float a00 = 0.f, a01 = 0.f, a10 = 0.f, a11 = 0.f;
+        for (int bk = bj; bk < bi; ++bk) {
+          const float* Mt = X + (bi * (bi - 1) / 2 + bk) * 256 + r0;
+          const float* Tk = Tf + (bk * 16) * kLdT + bj * 16 + c0;
+#pragma unroll
+          for (int m = 0; m < 16; ++m) {
+            const float2 mm = *reinterpret_cast<const float2*>(Mt + m * 16);
+            const float b0 = Tk[m * kLdT], b1 = Tk[m * kLdT + 1];
+            a00 += mm.x * b0; a01 += mm.x * b1; a10 += mm.y * b0; a11 += mm.y * b1;
+          }
+        }
+        float* dst = Tf + (bi * 16 + r0) * kLdT + bj * 16 + c0;
+        dst[0] = -a00; dst[1] = -a01; dst[kLdT] = -a10; dst[kLdT + 1] = -a11;
+      }
+      __syncthreads();
+    }
 
-  // 6. A2 = [Ti; P Ti] on the tensor core: D = [I; P] Ti, M=128 N=64 K=64.
-  //    Operands: X = [I; P] (128 x 64, K = i) in the R region, Ti^T (64 x 64,
-  //    rows j, K = i) over the dead A block; both hi/lo.  The result lands in
-  //    TMEM columns 128-191 and is split into A2 (hi/lo) by all warps.
-  {
-    uint8_t* Xh = Rh;                     // 128 x 64, 16 KB each half
-    uint8_t* Xl = Xh + 128 * 64 * 2;
-    uint8_t* Th = sb + kTxAf;             // 64 x 64, 8 KB each half
-    uint8_t* Tl = Th + 64 * 64 * 2;
-    for (int idx = tid; idx < 128 * 8 + 64 * 8; idx += kTxThreads) {
-      float x[8];
-      if (idx < 128 * 8) {                // X rows: identity (0-63) or P (64-127)
-        const int row = idx >> 3, ch = idx & 7;
+    // 6. A2 = [Ti; P Ti] on the tensor core: D = [I; P] Ti, M=128 N=64 K=64.
+    //    Operands: X = [I; P] (128 x 64, K = i) in the R region, Ti^T (64 x 64,
+    //    rows j, K = i) over the dead A block; both hi/lo.  The result lands in
+    //    TMEM columns 128-191 and is split into A2 (hi/lo) by all warps.
+    {
+      uint8_t* Xh = Rh;                     // 128 x 64, 16 KB each half
+      uint8_t* Xl = Xh + 128 * 64 * 2;
+      uint8_t* Th = sb + kTxAf;             // 64 x 64, 8 KB each half
+      uint8_t* Tl = Th + 64 * 64 * 2;
+      for (int idx = tid; idx < 128 * 8 + 64 * 8; idx += kTxThreads) {
+        float x[8];
+        if (idx < 128 * 8) {                // X rows: identity (0-63) or P (64-127)
+          const int row = idx >> 3, ch = idx & 7;
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
-          x[e] = row < kChunk ? (ch * 8 + e == row ? 1.f : 0.f) : Pf[(row - kChunk) * kLdT + ch * 8 + e];
-        st_split8(Xh, Xl, tc::sw128_offset(row, ch * 8, 128), x);
-      } else {                            // Ti^T rows j
-        const int j = (idx - 128 * 8) >> 3, ch = (idx - 128 * 8) & 7;
+          for (int e = 0; e < 8; ++e)
+            x[e] = row < kChunk ? (ch * 8 + e == row ? 1.f : 0.f) : Pf[(row - kChunk) * kLdT + ch * 8 + e];
+          st_split8(Xh, Xl, tc::sw128_offset(row, ch * 8, 128), x);
+        } else {                            // Ti^T rows j
+          const int j = (idx - 128 * 8) >> 3, ch = (idx - 128 * 8) & 7;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) x[e] = Tf[(ch * 8 + e) * kLdT + j];
-        st_split8(Th, Tl, tc::sw128_offset(j, ch * 8, 64), x);
+          for (int e = 0; e < 8; ++e) x[e] = Tf[(ch * 8 + e) * kLdT + j];
+          st_split8(Th, Tl, tc::sw128_offset(j, ch * 8, 64), x);
+        }
+      }
+      if (tid == 0) tc::bulk_wait_read();  // Khat^T staging (A2 region) reused below
+      tc::fence_async_smem();
+      tc::tc_fence_before();
+      __syncthreads();
+      if (tid == 0 && !s_abort) {
+        tc::tc_fence_after();
+        constexpr uint32_t idesc = tc::idesc_bf16_f32(128, 64);
+        const uint32_t ah[3] = {tc::smem_u32(Xh), tc::smem_u32(Xh), tc::smem_u32(Xl)};
+        const uint32_t bh[3] = {tc::smem_u32(Th), tc::smem_u32(Tl), tc::smem_u32(Th)};
+#pragma unroll
+        for (int p = 0; p < 3; ++p)
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            tc::mma_bf16(tmem + 128, tc::sw128_desc(ah[p] + k * 32), tc::sw128_desc(bh[p] + k * 32),
+                         idesc, p > 0 || k > 0);
+        tc::mma_commit(&mma_bar);
+      }
+      if (!tc::mbar_wait(&mma_bar, phase)) s_abort = 1;
+      phase ^= 1;
+      tc::tc_fence_after();
+      // TMEM -> A2: warp group g takes 8 of the 64 columns
+      {
+        const int row = (warp & 3) * 32 + lane, c0 = (warp >> 2) * (64 / (kTxWarps / 4));
+        for (int cc = 0; cc < 64 / (kTxWarps / 4); cc += 8) {
+          float d[8];
+          tc::tmem_ld8(tmem + lane_addr + 128 + c0 + cc, d);
+          st_split8(A2h, A2l, tc::sw128_offset(row, c0 + cc, 128), d);
+        }
       }
     }
-    if (tid == 0) tc::bulk_wait_read();  // Khat^T staging (A2 region) reused below
+    tc::tc_fence_before();
+    __syncthreads();  // X, Ti^T (L/R region) are dead before B2 overwrites it
+    // 7. B2 = [(beta Ktil)^T ; (beta V)^T] (hi/lo, swizzled 256 x 64): row -> channel
+    for (int idx = tid; idx < K * 8; idx += kTxThreads) {  // rows 0-127: beta_i k-hat_i e^{Gam_i}
+      const int c = idx & (K - 1), ch = idx >> 7;
+      float x[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int i = ch * 8 + e;
+        x[e] = bf16_at(Ks, i, c) * (bt[i] * rk[i]) * decay_exp(GM[i * kLd + c]);
+      }
+      st_split8(Bh, Bl, tc::sw128_offset(c, ch * 8, 256), x);
+    }
+    for (int idx = tid; idx < K * 8; idx += kTxThreads) {  // rows 128-255: beta_i v_i
+      const int c = idx & (K - 1), ch = idx >> 7;
+      float x[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int i = ch * 8 + e;
+        x[e] = bf16_at(Vs, i, c) * bt[i];
+      }
+      st_split8(Bh, Bl, tc::sw128_offset(K + c, ch * 8, 256), x);
+    }
     tc::fence_async_smem();
     tc::tc_fence_before();
     __syncthreads();
+
+    // 8. M2: D = A2 B2^T, M=128 N=256 K=64
     if (tid == 0 && !s_abort) {
       tc::tc_fence_after();
-      constexpr uint32_t idesc = tc::idesc_bf16_f32(128, 64);
-      const uint32_t ah[3] = {tc::smem_u32(Xh), tc::smem_u32(Xh), tc::smem_u32(Xl)};
-      const uint32_t bh[3] = {tc::smem_u32(Th), tc::smem_u32(Tl), tc::smem_u32(Th)};
+      constexpr uint32_t idesc = tc::idesc_bf16_f32(128, 256);
+      const uint32_t ah[3] = {tc::smem_u32(A2h), tc::smem_u32(A2h), tc::smem_u32(A2l)};
+      const uint32_t bh[3] = {tc::smem_u32(Bh), tc::smem_u32(Bl), tc::smem_u32(Bh)};
 #pragma unroll
       for (int p = 0; p < 3; ++p)
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          tc::mma_bf16(tmem + 128, tc::sw128_desc(ah[p] + k * 32), tc::sw128_desc(bh[p] + k * 32),
-                       idesc, p > 0 || k > 0);
+          tc::mma_bf16(tmem, tc::sw128_desc(ah[p] + k * 32), tc::sw128_desc(bh[p] + k * 32), idesc,
+                       p > 0 || k > 0);
       tc::mma_commit(&mma_bar);
     }
     if (!tc::mbar_wait(&mma_bar, phase)) s_abort = 1;
     phase ^= 1;
     tc::tc_fence_after();
-    // TMEM -> A2: warp group g takes 8 of the 64 columns
+
+    // 9. epilogue: warp group wg (four warps, one per TMEM lane quadrant) takes
+    //    256 / kGroups consecutive TMEM columns: columns 0-127 are W (rows 0-63) |
+    //    P W (rows 64-127), 128-255 Util | P Util.  M2 has finished reading its
+    //    operands, so [W; Q'] is staged in the A2 region and Util | P Util in the
+    //    L/R region, laid out as in the workspace record, and each goes out as
+    //    one bulk copy.
     {
-      const int row = (warp & 3) * 32 + lane, c0 = (warp >> 2) * (64 / (kTxWarps / 4));
-      for (int cc = 0; cc < 64 / (kTxWarps / 4); cc += 8) {
-        float d[8];
-        tc::tmem_ld8(tmem + lane_addr + 128 + c0 + cc, d);
-        st_split8(A2h, A2l, tc::sw128_offset(row, c0 + cc, 128), d);
-      }
-    }
-  }
-  tc::tc_fence_before();
-  __syncthreads();  // X, Ti^T (L/R region) are dead before B2 overwrites it
-  // 7. B2 = [(beta Ktil)^T ; (beta V)^T] (hi/lo, swizzled 256 x 64): row -> channel
-  for (int idx = tid; idx < K * 8; idx += kTxThreads) {  // rows 0-127: beta_i k-hat_i e^{Gam_i}
-    const int c = idx & (K - 1), ch = idx >> 7;
-    float x[8];
+      constexpr int kGroups = kTxWarps / 4, kCols = 256 / kGroups;
+      static_assert(kCols == 32, "two 16-column TMEM loads per thread");
+      const int wg = warp >> 2, row = (warp & 3) * 32 + lane;
+      const int t = row & 63;
+      const bool upper = row < kChunk;
+      const bool right = wg >= kGroups / 2;
+      const int cbase = (wg % (kGroups / 2)) * kCols;  // first column within the half
+      uint32_t raw[2][16];
+      tc::tmem_ld16_async(tmem + lane_addr + (right ? 128 : 0) + cbase, raw[0]);
+      tc::tmem_ld16_async(tmem + lane_addr + (right ? 128 : 0) + cbase + 16, raw[1]);
+      tc::tmem_wait_ld();
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const int i = ch * 8 + e;
-      x[e] = bf16_at(Ks, i, c) * (bt[i] * rk[i]) * decay_exp(GM[i * kLd + c]);
-    }
-    st_split8(Bh, Bl, tc::sw128_offset(c, ch * 8, 256), x);
-  }
-  for (int idx = tid; idx < K * 8; idx += kTxThreads) {  // rows 128-255: beta_i v_i
-    const int c = idx & (K - 1), ch = idx >> 7;
-    float x[8];
+      for (int cb = 0; cb < 2; ++cb) {
+        float d[16];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const int i = ch * 8 + e;
-      x[e] = bf16_at(Vs, i, c) * bt[i];
-    }
-    st_split8(Bh, Bl, tc::sw128_offset(K + c, ch * 8, 256), x);
-  }
-  tc::fence_async_smem();
-  tc::tc_fence_before();
-  __syncthreads();
-
-  // 8. M2: D = A2 B2^T, M=128 N=256 K=64
-  if (tid == 0 && !s_abort) {
-    tc::tc_fence_after();
-    constexpr uint32_t idesc = tc::idesc_bf16_f32(128, 256);
-    const uint32_t ah[3] = {tc::smem_u32(A2h), tc::smem_u32(A2h), tc::smem_u32(A2l)};
-    const uint32_t bh[3] = {tc::smem_u32(Bh), tc::smem_u32(Bl), tc::smem_u32(Bh)};
-#pragma unroll
-    for (int p = 0; p < 3; ++p)
-#pragma unroll
-      for (int k = 0; k < 4; ++k)
-        tc::mma_bf16(tmem, tc::sw128_desc(ah[p] + k * 32), tc::sw128_desc(bh[p] + k * 32), idesc,
-                     p > 0 || k > 0);
-    tc::mma_commit(&mma_bar);
-  }
-  if (!tc::mbar_wait(&mma_bar, phase)) s_abort = 1;
-  phase ^= 1;
-  tc::tc_fence_after();
-
-  // 9. epilogue: warp group wg (four warps, one per TMEM lane quadrant) takes
-  //    256 / kGroups consecutive TMEM columns: columns 0-127 are W (rows 0-63) |
-  //    P W (rows 64-127), 128-255 Util | P Util.  [W; Q'] is staged in the A2
-  //    region (M2 has finished reading it) and stored as one bulk copy; Util and
-  //    P Util go straight to the workspace (consecutive threads, consecutive
-  //    16-byte words).
-  {
-    constexpr int kGroups = kTxWarps / 4, kCols = 256 / kGroups;
-    const int wg = warp >> 2, row = (warp & 3) * 32 + lane;
-    const int t = row & 63;
-    const bool upper = row < kChunk;
-    const bool right = wg >= kGroups / 2;
-    for (int cb = 0; cb < kCols / 16; ++cb) {
-      float d[16];
-      const int c0 = (wg % (kGroups / 2)) * kCols + cb * 16;  // column within the half
-      tc::tmem_ld16(tmem + lane_addr + (right ? 128 : 0) + c0, d);
-      if (!right) {
-        if (!upper) {  // Q' = Qtil - P W
-          float q8[8], g8[8];
-#pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            ld_bf16x8(Qs, t, c0 + hh * 8, q8);
-            ld_f32x8(GM + t * kLd + c0 + hh * 8, g8);
+        for (int e = 0; e < 16; ++e) d[e] = __uint_as_float(raw[cb][e]);
+        const int c0 = cbase + cb * 16;
+        if (!right) {
+          if (!upper) {  // Q' = Qtil - P W
             const float nq = rq[t];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) d[hh * 8 + e] = q8[e] * nq * decay_exp(g8[e]) - d[hh * 8 + e];
+            for (int e = 0; e < 16; e += 4) {
+              const float4 qq = scale4(ld_bf16x4(Qs, t, c0 + e), nq);
+              const float4 gg = f4(GM + t * kLd + c0 + e);
+              d[e] = qq.x * decay_exp(gg.x) - d[e];
+              d[e + 1] = qq.y * decay_exp(gg.y) - d[e + 1];
+              d[e + 2] = qq.z * decay_exp(gg.z) - d[e + 2];
+              d[e + 3] = qq.w * decay_exp(gg.w) - d[e + 3];
+            }
           }
-        }
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          const float* xs = d + half * 8;
-          const uint4 pk = make_uint4(pack_bf16x2(xs[0], xs[1]), pack_bf16x2(xs[2], xs[3]),
-                                      pack_bf16x2(xs[4], xs[5]), pack_bf16x2(xs[6], xs[7]));
-          *reinterpret_cast<uint4*>(A2h + tc::sw128_offset(row, c0 + half * 8, 128)) = pk;
-        }
-      } else {
-        float* base = reinterpret_cast<float*>(rec + (upper ? kRecU : kRecOi));
+          for (int half = 0; half < 2; ++half) {
+            const float* xs = d + half * 8;
+            const uint4 pk = make_uint4(pack_bf16x2(xs[0], xs[1]), pack_bf16x2(xs[2], xs[3]),
+                                        pack_bf16x2(xs[4], xs[5]), pack_bf16x2(xs[6], xs[7]));
+            *reinterpret_cast<uint4*>(A2h + tc::sw128_offset(row, c0 + half * 8, 128)) = pk;
+          }
+        } else {
+          float* base = reinterpret_cast<float*>(sb + kTxL + (upper ? 0u : kRecOi - kRecU));
 #pragma unroll
-        for (int e = 0; e < 16; e += 4) {  // column quad (c0 + e) / 4
-          const int col = c0 + e;
-          f4(base + (col / kVs) * (kChunk * kVs) + ((col % kVs) / 4) * (kChunk * 4) + t * 4) =
-              make_float4(d[e], d[e + 1], d[e + 2], d[e + 3]);
+          for (int e = 0; e < 16; e += 4) {  // column quad (c0 + e) / 4
+            const int col = c0 + e;
+            f4(base + (col / kVs) * (kChunk * kVs) + ((col % kVs) / 4) * (kChunk * 4) + t * 4) =
+                make_float4(d[e], d[e + 1], d[e + 2], d[e + 3]);
+          }
         }
       }
     }
-  }
-  if (s_abort && tid == 0) set_error(a.err_flag, KDA_DEVERR_TIMEOUT);
-  tc::fence_async_smem();
+    if (s_abort && tid == 0) set_error(a.err_flag, KDA_DEVERR_TIMEOUT);
+    tc::fence_async_smem();
+    tc::tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {
+      static_assert(kRecOi == kRecU + kChunk * kHeadDim * 4, "Util and P Util are contiguous");
+      static_assert(2 * kChunk * kHeadDim * 4 <= kTxA2 - kTxL, "Util | P Util staging fits the L/R region");
+      tc::bulk_s2g(rec + kRecA1, A2h, 128 * 128 * 2);
+      tc::bulk_s2g(rec + kRecU, sb + kTxL, 2 * kChunk * kHeadDim * 4);
+      tc::bulk_commit();
+      tc::bulk_wait_read();  // the staging is reused by the next unit
+    }
+  }  // units
   tc::tc_fence_before();
   __syncthreads();
-  if (tid == 0) {  // [W; Q'] staged in the A2 region (free after M2) -> workspace
-    tc::bulk_s2g(rec + kRecA1, A2h, 128 * 128 * 2);
-    tc::bulk_commit();
-  }
   if (warp == 0) tc::tmem_dealloc(tmem, kTxTmemCols);
-  if (tid == 0) tc::bulk_wait_read();  // shared memory stays valid until read
 }
 
 // ---------------------------------------------------------------------------
@@ -1006,6 +1061,12 @@ kda_status ensure_kernel_attributes(int* dev_out) {
   return KDA_OK;
 }
 
+// Persistent transform: one CTA per SM (each holds a whole SM's shared
+// memory), or one per unit when there are fewer units.
+unsigned transform_grid(int64_t units, int dev) {
+  return (unsigned)(units < g_num_sms[dev] ? units : g_num_sms[dev]);
+}
+
 // Segmented schedule.  When every sequence has the same number of chunks and
 // the state pass occupies at most one wave of SMs, the chunk positions are cut
 // into up to kMaxSegments segments of at least kSegmentMinChunks: the pass of
@@ -1124,7 +1185,8 @@ extern "C" kda_status kda_prefill(kda_dims dims, kda_gate gate, const kda_bf16* 
   record_stage(0, st);
   if (nseg <= 1) {
     if (chunks > 0) {
-      chunk_transform_tc_kernel<<<dim3((unsigned)chunks, dims.HV), kTxThreads, kTransformTcSmem, st>>>(args);
+      args.tx_units = chunks * dims.HV;
+      chunk_transform_tc_kernel<<<transform_grid(args.tx_units, dev), kTxThreads, kTransformTcSmem, st>>>(args);
       if ((s = launch_status()) != KDA_OK) return s;
     }
     record_stage(1, st);
@@ -1143,8 +1205,8 @@ extern "C" kda_status kda_prefill(kda_dims dims, kda_gate gate, const kda_bf16* 
       sa.seg_len = seq_nch - i * seg < seg ? seq_nch - i * seg : seg;
       sa.seq_nch = seq_nch;
       if (sa.seg_len <= 0) break;
-      chunk_transform_tc_kernel<<<dim3((unsigned)(num_seqs * sa.seg_len), dims.HV), kTxThreads,
-                                  kTransformTcSmem, st>>>(sa);
+      sa.tx_units = (int64_t)num_seqs * sa.seg_len * dims.HV;
+      chunk_transform_tc_kernel<<<transform_grid(sa.tx_units, dev), kTxThreads, kTransformTcSmem, st>>>(sa);
       if ((s = launch_status()) != KDA_OK) break;
       if (cudaEventRecord(ps->seg[i], st) != cudaSuccess ||
           cudaStreamWaitEvent(ps->stream, ps->seg[i], 0) != cudaSuccess) {

@@ -213,6 +213,21 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// As tmem_ld16 without the wait: the registers are valid after tmem_wait_ld().
+__device__ __forceinline__ void tmem_ld16_async(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
 // As tmem_ld16, 8 columns.
 __device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
   uint32_t r[8];
@@ -232,12 +247,20 @@ __device__ __forceinline__ void split_bf16(float x, uint16_t& hi, uint16_t& lo) 
   lo = __bfloat16_as_ushort(__float2bfloat16_rn(x - __bfloat162float(h)));
 }
 
-// FP32 -> TF32 rounded to nearest (ties away from zero), low 13 bits zero, so
-// that the tensor core's use of the top 19 bits is exact.
+// FP32 -> TF32 rounded to nearest, ties away from zero, low 13 bits zero, so
+// that the tensor core's use of the top 19 bits is exact.  Done on the bit
+// pattern (sign-magnitude: adding half a TF32 unit to the magnitude and
+// dropping the low bits rounds half away from zero; a carry into the exponent
+// gives the next binade) with two integer operations; finite inputs only.
 __device__ __forceinline__ uint32_t tf32_rna(float x) {
-  uint32_t r;
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-  return r;
+  return (__float_as_uint(x) + 0x1000u) & 0xFFFFE000u;
+}
+
+// Four consecutive values of row `row`, columns [col, col+4) (col a multiple
+// of 4), rounded to TF32 into a swizzled K-major 32-bit tile of `rows` rows.
+__device__ __forceinline__ void st_tf32x4(uint8_t* tile, int row, int col, int rows, float4 x) {
+  *reinterpret_cast<uint4*>(tile + sw128_offset_f32(row, col, rows)) =
+      make_uint4(tf32_rna(x.x), tf32_rna(x.y), tf32_rna(x.z), tf32_rna(x.w));
 }
 
 // Eight consecutive values of row `row`, columns [col, col+8) (col a multiple
