@@ -184,6 +184,7 @@ constexpr int kTxWarps = kTxThreads / 32;
 constexpr uint32_t kTxL = 0;                          // L: TF32 128 x 128
 constexpr uint32_t kTxR = kTxL + 128 * 128 * 4;       // R: TF32 64 x 128
 constexpr uint32_t kTxB2 = 0;                         // B2 hi, lo: 256 x 64 each (reuses L/R)
+constexpr uint32_t kTxUst = 32 * 1024;                // Util | P Util output staging (upper L/R)
 constexpr uint32_t kTxAf = 0;                         // A FP32 [64][kLdT] (reuses L/R)
 constexpr uint32_t kTxPf = kTxAf + kChunk * kLdT * 4;  // P FP32 (reuses L/R)
 constexpr uint32_t kTxA2 = kTxR + 2 * 64 * 128 * 2;   // A2 hi, lo: 128 x 64 each
@@ -198,7 +199,8 @@ constexpr uint32_t kTransformTcSmem = kTxEnd + 1024;
 constexpr uint32_t kTxTmemCols = 256;
 static_assert(2 * 256 * 64 * 2 <= kTxA2, "B2 fits in the L/R region");
 static_assert(kTxTf + kChunk * kLdT * 4 <= kTxA2, "A, P and (I+A)^-1 fit in the L/R region");
-static_assert(kTxWarps * kHeadDim * 4 <= kTxA2, "warp totals fit in the L/R region");
+static_assert(kTxWarps * kHeadDim * 4 <= kTxUst, "fold warp totals stay below the output staging");
+static_assert(kTxUst + 2 * kChunk * kHeadDim * 4 <= kTxA2, "output staging fits the L/R region");
 static_assert(kTxQ % 16 == 0 && kTxK % 16 == 0 && kTxV % 16 == 0 && kTxG % 16 == 0 &&
                   kTxTf % 16 == 0 && kTxMisc % 16 == 0 && kTxA2 % 1024 == 0 && kTxR % 1024 == 0,
               "alignment");
@@ -218,23 +220,6 @@ __device__ __forceinline__ void st_split8(uint8_t* hi, uint8_t* lo, uint32_t off
   }
   *reinterpret_cast<uint4*>(hi + off) = make_uint4(h[0], h[1], h[2], h[3]);
   *reinterpret_cast<uint4*>(lo + off) = make_uint4(l[0], l[1], l[2], l[3]);
-}
-
-// Eight consecutive BF16 values of row t, columns [c, c+8), of a raw tile.
-__device__ __forceinline__ void ld_bf16x8(const uint8_t* tile, int t, int c, float* x) {
-  const uint4 u = *reinterpret_cast<const uint4*>(tile + (t * kLdB + c) * 2);
-  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    x[2 * e] = __uint_as_float(w[e] << 16);
-    x[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
-  }
-}
-
-__device__ __forceinline__ void ld_f32x8(const float* p, float* x) {
-  const float4 a = *reinterpret_cast<const float4*>(p), b = *reinterpret_cast<const float4*>(p + 4);
-  x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
-  x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
 }
 
 __device__ __forceinline__ float bf16_at(const uint8_t* tile, int t, int c) {
@@ -294,8 +279,7 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
   uint8_t* sb = smraw + ((1024u - (tc::smem_u32(smraw) & 1023u)) & 1023u);
   uint8_t* Lt = sb + kTxL;  // M1 left operand, TF32 128 x 128
   uint8_t* Rt = sb + kTxR;  // M1 right operand, TF32 64 x 128
-  uint8_t* Rh = Rt;         // the R region reused as BF16 hi/lo halves
-  uint8_t* Rl = Rh + 64 * 128 * 2;
+  uint8_t* Rh = Rt;         // the R region, later reused for BF16 hi/lo operands
   uint8_t* Bh = sb + kTxB2;
   uint8_t* Bl = Bh + 256 * 64 * 2;
   uint8_t* A2h = sb + kTxA2;
@@ -427,6 +411,9 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
         gg = make_float4(gg.x + pre.x, gg.y + pre.y, gg.z + pre.z, gg.w + pre.w);
       }
     }
+    // the previous unit's output staging (A2 region, upper L/R region) is
+    // rewritten from step 2 on: its bulk stores must have read it by now
+    if (tid == 0) tc::bulk_wait_read();
     __syncthreads();
 
     // 2. gamma to the workspace; Khat^T (hi/lo, swizzled 128 x 64) built in the
@@ -757,7 +744,7 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
             *reinterpret_cast<uint4*>(A2h + tc::sw128_offset(row, c0 + half * 8, 128)) = pk;
           }
         } else {
-          float* base = reinterpret_cast<float*>(sb + kTxL + (upper ? 0u : kRecOi - kRecU));
+          float* base = reinterpret_cast<float*>(sb + kTxUst + (upper ? 0u : kRecOi - kRecU));
 #pragma unroll
           for (int e = 0; e < 16; e += 4) {  // column quad (c0 + e) / 4
             const int col = c0 + e;
@@ -773,13 +760,12 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
     __syncthreads();
     if (tid == 0) {
       static_assert(kRecOi == kRecU + kChunk * kHeadDim * 4, "Util and P Util are contiguous");
-      static_assert(2 * kChunk * kHeadDim * 4 <= kTxA2 - kTxL, "Util | P Util staging fits the L/R region");
       tc::bulk_s2g(rec + kRecA1, A2h, 128 * 128 * 2);
-      tc::bulk_s2g(rec + kRecU, sb + kTxL, 2 * kChunk * kHeadDim * 4);
-      tc::bulk_commit();
-      tc::bulk_wait_read();  // the staging is reused by the next unit
+      tc::bulk_s2g(rec + kRecU, sb + kTxUst, 2 * kChunk * kHeadDim * 4);
+      tc::bulk_commit();  // awaited at the end of the next unit's fold, or on exit
     }
   }  // units
+  if (tid == 0) tc::bulk_wait_read();  // shared memory stays valid until read
   tc::tc_fence_before();
   __syncthreads();
   if (warp == 0) tc::tmem_dealloc(tmem, kTxTmemCols);
