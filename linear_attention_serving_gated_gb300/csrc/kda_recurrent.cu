@@ -91,16 +91,20 @@ __global__ void __launch_bounds__(128) recurrent_kernel(const StepArgs args) {
   const bool reporter = tid == 0 && blockIdx.x == 0 && h == 0;
 
   const int slot = args.state_idx[r];
-  bool ok = slot >= -1 && slot < args.pool_slots;
+  const bool ok = slot >= -1 && slot < args.pool_slots;
   if (!ok && reporter) set_error(args.err_flag, KDA_DEVERR_SLOT);
-  if (MODE == kTree && ok) {
-    for (int i = 0; i < T; ++i) {
+  // Tree: a request with a parent outside [-1, i) is rejected.  It runs down
+  // the chain path (no parent reloads), writes no snapshot and zero outputs,
+  // so the rejection adds no branch around the main loop.
+  bool parents_ok = true;
+  if (MODE == kTree && ok && slot >= 0) {
+    bool bad = false;
+    for (int i = tid; i < T; i += 128) {
       const int p = args.parent[(int64_t)r * T + i];
-      if (p < -1 || p >= i) {
-        ok = false;
-        if (reporter) set_error(args.err_flag, KDA_DEVERR_PARENT);
-      }
+      bad |= p < -1 || p >= i;
     }
+    parents_ok = !__syncthreads_or(bad);
+    if (!parents_ok && reporter) set_error(args.err_flag, KDA_DEVERR_PARENT);
   }
   if (!ok || slot < 0) {  // padding or rejected request: zero outputs, touch no state
     if (sub == 0)
@@ -180,7 +184,7 @@ __global__ void __launch_bounds__(128) recurrent_kernel(const StepArgs args) {
 
     for (int u = 0; u < nt; ++u) {
       const int t = tb + u;
-      if (MODE == kTree && t > 0) {
+      if (MODE == kTree && t > 0 && parents_ok) {
         const int p = args.parent[(int64_t)r * T + t];
         if (p != t - 1) {
           const float* src =
@@ -223,10 +227,12 @@ __global__ void __launch_bounds__(128) recurrent_kernel(const StepArgs args) {
           S[gi][i] = make_float4(lo.x, lo.y, hi.x, hi.y);
         }
         const float out = ga.scale * group_sum8(dot16(S[gi], q));
-        if (sub == 0) args.o[(row * HV + h) * V + j] = float_to_bf16_bits(out);
-        float* dst = MODE == kDecode ? root + (size_t)j * K : snap + (size_t)j * K;
+        if (sub == 0) args.o[(row * HV + h) * V + j] = parents_ok ? float_to_bf16_bits(out) : 0;
+        if (MODE != kTree || parents_ok) {
+          float* dst = MODE == kDecode ? root + (size_t)j * K : snap + (size_t)j * K;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) *reinterpret_cast<float4*>(dst + i * 32 + lane_col) = S[gi][i];
+          for (int i = 0; i < 4; ++i) *reinterpret_cast<float4*>(dst + i * 32 + lane_col) = S[gi][i];
+        }
       }
     }
     if (tb + kTokBlock < T) __syncthreads();  // fold buffer reused by the next block
