@@ -1054,7 +1054,7 @@ unsigned transform_grid(int64_t units, int dev) {
 }
 
 // Segmented schedule.  When every sequence has the same number of chunks and
-// the state pass occupies at most one wave of SMs, the chunk positions are cut
+// the state pass occupies at most half of the SMs, the chunk positions are cut
 // into up to kMaxSegments segments of at least kSegmentMinChunks: the pass of
 // segment s runs on a second stream while the transform of segment s+1 runs on
 // the caller's, so the pass (latency-bound, a few SMs) hides under the
@@ -1164,7 +1164,7 @@ extern "C" kda_status kda_prefill(kda_dims dims, kda_gate gate, const kda_bf16* 
   const dim3 pass_grid(kSlices, dims.HV, num_seqs);
   int nseg = 1, seq_nch = 0;
   if (total_tokens > 0 && (num_seqs == 1 || !cu_seqlens) &&
-      (int64_t)kSlices * dims.HV * num_seqs <= g_num_sms[dev]) {
+      2 * (int64_t)kSlices * dims.HV * num_seqs <= g_num_sms[dev]) {
     seq_nch = (int)((total_tokens / num_seqs + kChunk - 1) / kChunk);
     nseg = seq_nch / kSegmentMinChunks < kMaxSegments ? seq_nch / kSegmentMinChunks : kMaxSegments;
   }

@@ -82,6 +82,7 @@ template <int MODE, int GROUPS>
 __global__ void __launch_bounds__(128) recurrent_kernel(const StepArgs args) {
   constexpr int K = kHeadDim, V = kHeadDim;
   __shared__ __align__(16) FoldSmem fs;
+  __shared__ int tree_par[kTokBlock];  // tree: the parents of the first kTokBlock nodes
   const int r = blockIdx.z, h = blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int sub = lane & 7;
@@ -103,6 +104,7 @@ __global__ void __launch_bounds__(128) recurrent_kernel(const StepArgs args) {
       const int p = args.parent[(int64_t)r * T + i];
       bad |= p < -1 || p >= i;
     }
+    if (tid < kTokBlock && tid < T) tree_par[tid] = args.parent[(int64_t)r * T + tid];
     parents_ok = !__syncthreads_or(bad);
     if (!parents_ok && reporter) set_error(args.err_flag, KDA_DEVERR_PARENT);
   }
@@ -185,7 +187,7 @@ __global__ void __launch_bounds__(128) recurrent_kernel(const StepArgs args) {
     for (int u = 0; u < nt; ++u) {
       const int t = tb + u;
       if (MODE == kTree && t > 0 && parents_ok) {
-        const int p = args.parent[(int64_t)r * T + t];
+        const int p = t < kTokBlock ? tree_par[t] : args.parent[(int64_t)r * T + t];
         if (p != t - 1) {
           const float* src =
               p < 0 ? root : args.snapshots + (((size_t)r * T + p) * HV + h) * head_elems;
