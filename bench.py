@@ -8,7 +8,11 @@ PR #42857, Speed Tests and Profiling):
   prefill   1 sequence x 4096 tokens, 16-slot FP32 pool      (the headline)
   decode    48 requests x 1 token, 240-slot pool
   verify    16 requests x 6 draft tokens, chain and tree, with snapshots
-  commit    16 requests, accepted prefix copied into the pool
+  commit    16 requests, accepted snapshot copied into the pool
+  replay    the same verify keeping a ring of folded token inputs instead of
+            snapshots, and its commit replaying the accepted prefix ("[KDA]
+            Default GLM-5-Next spec verify to the CuTe DSL KDA kernel #42905",
+            Results: ReplaySSM rings)
 `value` is prefill tokens/s (the metric's first term) over the prefill phase
 time.  Every phase is a CUDA-graph replay timed with CUDA events recorded as
 graph nodes around its kernels, after an L2 flush (a 512 MiB write, then a
@@ -102,6 +106,19 @@ def decode_bytes(B):
 
 def verify_bytes(B, T):
     return B * (H * K * K * 4 + T * H * K * K * 4 + T * token_io_bytes())
+
+
+RING_FLOATS = 3 * K + 4  # replay ring record per (request, token, head)
+
+
+def verify_replay_bytes(B, T):
+    # state read once, token rows, ring records written (no snapshots)
+    return B * (H * K * K * 4 + T * token_io_bytes() + T * H * RING_FLOATS * 4)
+
+
+def commit_replay_bytes(accepted, T):
+    # per committing request: state read + write, ring records of the replayed prefix
+    return sum(2 * H * K * K * 4 + (int(a) + 1) * H * RING_FLOATS * 4 for a in accepted if a >= 0)
 
 
 def commit_bytes(B):
@@ -227,6 +244,8 @@ def run_ours(args, rank, world, local_rank):
     dd = inputs.decode_inputs(seed=100 + rank, B=DECODE_B, H=H, slots=240)
     vd = inputs.verify_inputs(seed=200 + rank, B=VERIFY_B, T=VERIFY_T, H=H, slots=240)
     d_pool0, v_pool0 = t(dd["pool"]), t(vd["pool"])
+    # every request accepts some prefix, so every commit moves one state
+    acc_host = np.random.default_rng(rank).integers(0, VERIFY_T, size=COMMIT_B).astype(np.int32)
     L = []
     for _ in range(args.layers):
         L.append({
@@ -238,8 +257,9 @@ def run_ours(args, rank, world, local_rank):
             "v_o": torch.empty((VERIFY_B, VERIFY_T, H, K), dtype=torch.bfloat16, device=dev),
             "v_snap": torch.empty((VERIFY_B, VERIFY_T, H, K, K), device=dev),
             "v_snap2": torch.empty((VERIFY_B, VERIFY_T, H, K, K), device=dev),
-            # every request accepts some prefix, so every commit copies one state
-            "accepted": t(np.random.default_rng(rank).integers(0, VERIFY_T, size=COMMIT_B).astype(np.int32)),
+            "v_pool_r": v_pool0.clone(),
+            "ring": torch.empty((kda.kda_replay_ring_bytes(D, VERIFY_B, VERIFY_T) // 4,), device=dev),
+            "accepted": t(acc_host),
         })
     del d_pool0, v_pool0
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -251,12 +271,13 @@ def run_ours(args, rank, world, local_rank):
         flush.zero_()
         flush.view(torch.int64).sum()
 
-    phases = ["prefill", "decode", "verify_chain", "verify_tree", "commit"]
+    phases = ["prefill", "decode", "verify_chain", "verify_tree", "commit", "verify_replay", "commit_replay"]
     # The prefill's state pass of segment s overlaps the transform of segment
     # s+1, so its stage events give the span of the transform launches (ev0 ->
     # ev1, earlier segments' passes running alongside) and the exposed tail of
     # the last pass segment (ev1 -> ev2).
-    kernels = ["prefill_transform", "prefill_pass_tail", "decode", "verify_chain", "verify_tree", "commit"]
+    kernels = ["prefill_transform", "prefill_pass_tail", "decode", "verify_chain", "verify_tree", "commit",
+               "verify_replay", "commit_replay"]
 
     def run_call(name, x):
         if name == "prefill":
@@ -271,6 +292,11 @@ def run_ours(args, rank, world, local_rank):
         elif name == "verify_tree":
             kda.kda_verify_tree(D, gate, x["VX"]["mixed_qkv"], x["VX"]["a"], x["VX"]["b"], VERIFY_B,
                                 VERIFY_T, x["v_par"], x["v_pool"], x["v_idx"], x["v_o"], x["v_snap2"])
+        elif name == "verify_replay":
+            kda.kda_verify_chain_replay(D, gate, x["VX"]["mixed_qkv"], x["VX"]["a"], x["VX"]["b"], VERIFY_B,
+                                        VERIFY_T, x["v_pool_r"], x["v_idx"], x["v_o"], x["ring"])
+        elif name == "commit_replay":
+            kda.kda_commit_replay(D, x["ring"], COMMIT_B, VERIFY_T, x["accepted"], x["v_pool_r"], x["v_idx"])
         elif name == "commit":
             kda.kda_commit(D, x["v_snap"], COMMIT_B, VERIFY_T, x["accepted"], x["v_pool"], x["v_idx"])
 
@@ -359,6 +385,7 @@ def run_ours(args, rank, world, local_rank):
         "prefill_pass_tail": [r["prefill"][1].elapsed_time(r["prefill"][2]) for r in records],
         "decode": ph_ms["decode"], "verify_chain": ph_ms["verify_chain"],
         "verify_tree": ph_ms["verify_tree"], "commit": ph_ms["commit"],
+        "verify_replay": ph_ms["verify_replay"], "commit_replay": ph_ms["commit_replay"],
     }
     tot = {n: sum(v) for n, v in ph_ms.items()}
     tot = dict(zip(phases, max_over_ranks([tot[n] for n in phases], world, dev)))
@@ -393,6 +420,13 @@ def run_ours(args, rank, world, local_rank):
         return
 
     hbm, bf16_tf, sm_max, peak_kind = _peaks()
+    # The library splits a single long prefill into up to four segments (a
+    # transform and a state-pass launch each) when 8 * heads fits in the SM
+    # count; same rule here, to count the launches.
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    seq_nch = (PREFILL_T + CHUNK - 1) // CHUNK
+    nseg = min(4, seq_nch // 16) if seq_nch >= 32 and 8 * H <= sms else 1
+    prefill_launches = 2 * max(nseg, 1)
     steps = args.steps
     prefill_s = tot["prefill"] / 1e3
     value = replica_throughput(PREFILL_T, steps, world, prefill_s)
@@ -409,6 +443,8 @@ def run_ours(args, rank, world, local_rank):
         "verify_chain": ("hbm", verify_bytes(VERIFY_B, VERIFY_T) / 1e9, hbm, "GB/s"),
         "verify_tree": ("hbm", verify_bytes(VERIFY_B, VERIFY_T) / 1e9, hbm, "GB/s"),
         "commit": ("hbm", commit_bytes(COMMIT_B) / 1e9, hbm, "GB/s"),
+        "verify_replay": ("hbm", verify_replay_bytes(VERIFY_B, VERIFY_T) / 1e9, hbm, "GB/s"),
+        "commit_replay": ("hbm", commit_replay_bytes(acc_host, VERIFY_T) / 1e9, hbm, "GB/s"),
     }
     dom = max((n for n in mean_k if work[n] is not None), key=mean_k.get)
     bound, per_launch, peak, unit = work[dom]
@@ -437,6 +473,8 @@ def run_ours(args, rank, world, local_rank):
         "verify_chain_b16x6": {"us": round(statistics.mean(ph_ms["verify_chain"]) * 1e3, 2)},
         "verify_tree_b16x6": {"us": round(statistics.mean(ph_ms["verify_tree"]) * 1e3, 2)},
         "commit_b16": {"us": round(statistics.mean(ph_ms["commit"]) * 1e3, 2)},
+        "verify_replay_b16x6": {"us": round(statistics.mean(ph_ms["verify_replay"]) * 1e3, 2)},
+        "commit_replay_b16": {"us": round(statistics.mean(ph_ms["commit_replay"]) * 1e3, 2)},
         "kernels": kern,
     }
     out = {
@@ -445,13 +483,13 @@ def run_ours(args, rank, world, local_rank):
         "ms_per_step": round(sum(tot.values()) / steps, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16 in / fp32 state",
         "data": "synthetic (seeded; q,k,v,a,beta ~N(0,1) BF16, A_log~U(-1,1), dt_bias~N(0,0.1), state~N(0,0.02))",
-        "config": {"workload": "KDA prefill 1x4096 tokens, 16 heads x 128 (+ decode B=48, verify 16x6 chain/tree, commit 16)",
+        "config": {"workload": "KDA prefill 1x4096 tokens, 16 heads x 128 (+ decode B=48, verify 16x6 chain/tree/replay, commit 16 snapshot/replay)",
                    "timing": (f"CUDA-graph replay per phase; CUDA events recorded as graph nodes around the phase's kernels; "
                               f"decode/verify/commit: {args.layers} layer calls back to back, each on its own state pool and "
                               f"buffers, time per call = span / {args.layers}"),
                    "global_batch": world, "seq_len": PREFILL_T, "heads": H, "head_dim": K,
                    "parallelism": f"replicas x{world}", "l2": "flushed before every phase (512 MiB write, then the same buffer read back); layer calls touch disjoint buffers larger than L2"},
-        "gpu_launches": steps * (2 + (len(phases) - 1) * args.layers),
+        "gpu_launches": steps * (prefill_launches + (len(phases) - 1) * args.layers),
         "phases": phase_out,
         "roofline": roofline,
         "e2e": {"value": round(replica_throughput(PREFILL_T, e2e_steps, world, e2e_ms / 1e3), 1),

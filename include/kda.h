@@ -228,6 +228,44 @@ kda_status kda_prefill_noalloc(kda_dims dims, kda_gate gate, const kda_bf16 *q,
                                kda_bf16 *o, float *intermediate, int32_t *err_flag, void *stream);
 
 /*
+ * ReplaySSM verify ("[KDA] Default GLM-5-Next spec verify to the CuTe DSL KDA
+ * kernel #42905", Results: the "ReplaySSM rings" columns beside the
+ * "intermediate-state snapshots" ones; left out of scope in "[KDA] Support
+ * Helion MTP verification and harden prefill, decode", Motivation): chain
+ * verify that keeps no per-token state snapshots.  Outputs o
+ * are those of kda_verify_chain, bit for bit; instead of snapshots, each draft
+ * token's folded inputs (k-hat, exp(g), v, beta) are recorded in `ring`, and
+ * kda_commit_replay replays the accepted prefix onto the pool.  The state is
+ * read once and nothing state-sized is written, so the call moves about
+ * 1/7 of the bytes of the snapshot verify at T = 6.
+ *   ring          device, kda_replay_ring_bytes(dims, B, T) bytes, 16-byte
+ *                 aligned; layout [B, T, HV, 388] FP32 (k-hat [128], exp(g)
+ *                 [128], v [128], beta, 3 unused), owned by the caller and
+ *                 read by the next kda_commit_replay.
+ * Other arguments and errors as kda_verify_chain.  The pool is not written.
+ */
+size_t kda_replay_ring_bytes(kda_dims dims, int B, int T);
+kda_status kda_verify_chain_replay(kda_dims dims, kda_gate gate, const kda_bf16 *mixed_qkv,
+                                   int64_t row_stride, const kda_bf16 *a, const kda_bf16 *b,
+                                   int B, int T, const float *state_pool, int pool_slots,
+                                   const int32_t *state_idx, kda_bf16 *o, float *ring,
+                                   int32_t *err_flag, void *stream);
+
+/*
+ * Commit for ReplaySSM verify: for each request r with accepted[r] >= 0, the
+ * pool state is advanced through draft tokens 0..accepted[r] from `ring`,
+ * with the verify's own arithmetic, so the new pool state equals, bit for
+ * bit, the snapshot kda_verify_chain would have written after that token.
+ * accepted[r] = -1 keeps the pool state; accepted[r] >= T sets
+ * KDA_DEVERR_ACCEPTED and skips the request; slot -1 is skipped.
+ *   ring          as written by kda_verify_chain_replay with the same B, T
+ *   accepted      [B] int32 (device)
+ */
+kda_status kda_commit_replay(kda_dims dims, const float *ring, int B, int T,
+                             const int32_t *accepted, float *state_pool, int pool_slots,
+                             const int32_t *state_idx, int32_t *err_flag, void *stream);
+
+/*
  * Profiling aid (not part of the pages' contract): per-kernel timing of every
  * entry point.  After kda_set_stage_events(ev) with three cudaEvent_t
  * handles passed as void*, each later call records ev[0] on its stream before

@@ -31,7 +31,14 @@
 namespace kda {
 namespace {
 
-enum Mode { kDecode = 0, kChain = 1, kTree = 2 };
+// kChainReplay: chain verify that keeps no snapshots; instead each draft
+// token's folded inputs go to a per-request ring.  kCommitReplay: replays the
+// accepted prefix from that ring onto the pool state.
+enum Mode { kDecode = 0, kChain = 1, kTree = 2, kChainReplay = 3, kCommitReplay = 4 };
+
+// Ring record of one (request, token, head): k-hat [128], exp(g) [128],
+// v [128], beta, padding -- FP32, 16-byte aligned.
+constexpr int kRingFloats = 3 * kHeadDim + 4;
 
 struct StepArgs {
   GateArgs gate;
@@ -47,6 +54,8 @@ struct StepArgs {
   const int32_t* state_idx;
   kda_bf16* o;
   float* snapshots;
+  float* ring;                // replay modes
+  const int32_t* accepted;    // kCommitReplay
   int32_t* err_flag;
 };
 
@@ -87,9 +96,18 @@ __global__ void __launch_bounds__(128) recurrent_kernel(const StepArgs args) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int sub = lane & 7;
   const int row0 = blockIdx.x * (16 * GROUPS) + warp * (4 * GROUPS) + (lane >> 3);
-  const int T = MODE == kDecode ? 1 : args.T;
   const int HV = args.HV;
   const bool reporter = tid == 0 && blockIdx.x == 0 && h == 0;
+  // commit replay: tokens 0..accepted[r] of the verify's T are replayed
+  const int acc = MODE == kCommitReplay ? args.accepted[r] : 0;
+  if (MODE == kCommitReplay) {
+    if (acc < 0) return;  // nothing accepted: the pool keeps its state
+    if (acc >= args.T) {
+      if (reporter) set_error(args.err_flag, KDA_DEVERR_ACCEPTED);
+      return;
+    }
+  }
+  const int T = MODE == kDecode ? 1 : MODE == kCommitReplay ? acc + 1 : args.T;
 
   const int slot = args.state_idx[r];
   const bool ok = slot >= -1 && slot < args.pool_slots;
@@ -109,7 +127,7 @@ __global__ void __launch_bounds__(128) recurrent_kernel(const StepArgs args) {
     if (!parents_ok && reporter) set_error(args.err_flag, KDA_DEVERR_PARENT);
   }
   if (!ok || slot < 0) {  // padding or rejected request: zero outputs, touch no state
-    if (sub == 0)
+    if (MODE != kCommitReplay && sub == 0)
       for (int i = 0; i < T; ++i)
 #pragma unroll
         for (int gi = 0; gi < GROUPS; ++gi)
@@ -141,7 +159,15 @@ __global__ void __launch_bounds__(128) recurrent_kernel(const StepArgs args) {
     for (int u = 0; u < kTokBlock; ++u) {
       sq[u] = 0.f;
       sk[u] = 0.f;
-      if (u < nt) {
+      if (MODE == kCommitReplay) {  // folded values recorded by the verify
+        if (u < nt) {
+          const float* rec = args.ring + (((int64_t)r * args.T + tb + u) * HV + h) * kRingFloats;
+          fs.k[u][tid] = rec[tid];
+          fs.dec[u][tid] = rec[kHeadDim + tid];
+          fs.v[u][tid] = rec[2 * kHeadDim + tid];
+          if (tid == 0) fs.beta[u] = rec[3 * kHeadDim];
+        }
+      } else if (u < nt) {
         const int64_t row = MODE == kDecode ? r : (int64_t)r * T + tb + u;
         const kda_bf16* x = args.mixed_qkv + row * args.row_stride;
         const float qv = bf16_bits_to_float(x[h * K + tid]);
@@ -156,7 +182,7 @@ __global__ void __launch_bounds__(128) recurrent_kernel(const StepArgs args) {
         sk[u] = kv * kv;
       }
     }
-    if (ga.use_qk_l2norm) {
+    if (MODE != kCommitReplay && ga.use_qk_l2norm) {
 #pragma unroll
       for (int u = 0; u < kTokBlock; ++u) {
 #pragma unroll
@@ -183,9 +209,15 @@ __global__ void __launch_bounds__(128) recurrent_kernel(const StepArgs args) {
       }
     }
     __syncthreads();
-
     for (int u = 0; u < nt; ++u) {
       const int t = tb + u;
+      if (MODE == kChainReplay && blockIdx.x == 0) {  // one row block per head records the fold
+        float* rec = args.ring + (((int64_t)r * T + t) * HV + h) * kRingFloats;
+        rec[tid] = fs.k[u][tid];
+        rec[kHeadDim + tid] = fs.dec[u][tid];
+        rec[2 * kHeadDim + tid] = fs.v[u][tid];
+        if (tid == 0) rec[3 * kHeadDim] = fs.beta[u];
+      }
       if (MODE == kTree && t > 0 && parents_ok) {
         const int p = t < kTokBlock ? tree_par[t] : args.parent[(int64_t)r * T + t];
         if (p != t - 1) {
@@ -208,8 +240,9 @@ __global__ void __launch_bounds__(128) recurrent_kernel(const StepArgs args) {
         dec[i] = *reinterpret_cast<const float4*>(&fs.dec[u][i * 32 + lane_col]);
       }
       const float beta = fs.beta[u];
-      float* snap = MODE == kDecode ? nullptr
-                                    : args.snapshots + (((size_t)r * T + t) * HV + h) * head_elems;
+      float* snap = MODE == kChain || MODE == kTree
+                        ? args.snapshots + (((size_t)r * T + t) * HV + h) * head_elems
+                        : nullptr;
 #pragma unroll
       for (int gi = 0; gi < GROUPS; ++gi) {
         // X = Diag(exp g) S;  u = beta (v - X^T k);  S = X + k u^T;  o = scale S^T q
@@ -228,8 +261,10 @@ __global__ void __launch_bounds__(128) recurrent_kernel(const StepArgs args) {
           const float2 hi = fma2(make_float2(k[i].z, k[i].w), u2, make_float2(S[gi][i].z, S[gi][i].w));
           S[gi][i] = make_float4(lo.x, lo.y, hi.x, hi.y);
         }
+        if (MODE == kCommitReplay) continue;  // the state is written once, after the last token
         const float out = ga.scale * group_sum8(dot16(S[gi], q));
         if (sub == 0) args.o[(row * HV + h) * V + j] = parents_ok ? float_to_bf16_bits(out) : 0;
+        if (MODE == kChainReplay) continue;  // no snapshots
         if (MODE != kTree || parents_ok) {
           float* dst = MODE == kDecode ? root + (size_t)j * K : snap + (size_t)j * K;
 #pragma unroll
@@ -238,6 +273,13 @@ __global__ void __launch_bounds__(128) recurrent_kernel(const StepArgs args) {
       }
     }
     if (tb + kTokBlock < T) __syncthreads();  // fold buffer reused by the next block
+  }
+  if (MODE == kCommitReplay) {
+#pragma unroll
+    for (int gi = 0; gi < GROUPS; ++gi)
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        *reinterpret_cast<float4*>(root + (size_t)(row0 + gi * 4) * K + i * 32 + lane_col) = S[gi][i];
   }
 }
 
@@ -414,4 +456,56 @@ extern "C" kda_status kda_commit(kda_dims dims, const float* snapshots, int B, i
   record_stage(1, st);
   record_stage(2, st);
   return s;
+}
+
+extern "C" size_t kda_replay_ring_bytes(kda_dims dims, int B, int T) {
+  if (B < 0 || T < 1 || dims.HV <= 0) return 0;
+  return (size_t)B * T * dims.HV * kRingFloats * sizeof(float);
+}
+
+extern "C" kda_status kda_verify_chain_replay(kda_dims dims, kda_gate gate,
+                                              const kda_bf16* mixed_qkv, int64_t row_stride,
+                                              const kda_bf16* a, const kda_bf16* b, int B, int T,
+                                              const float* state_pool, int pool_slots,
+                                              const int32_t* state_idx, kda_bf16* o, float* ring,
+                                              int32_t* err_flag, void* stream) {
+  StepArgs args{};
+  kda_status s = check_packed(dims, gate, mixed_qkv, row_stride, a, b, B, state_pool, pool_slots,
+                              state_idx, o, &args);
+  if (s != KDA_OK) return s;
+  if (T < 1) return KDA_ERR_SHAPE;
+  if (B == 0) return KDA_OK;
+  if (!ring) return KDA_ERR_NULL_ARG;
+  if (!aligned16(ring)) return KDA_ERR_ALIGNMENT;
+  args.T = T;
+  args.pool = const_cast<float*>(state_pool);  // read only in verify
+  args.o = o;
+  args.ring = ring;
+  args.err_flag = err_flag;
+  return launch_recurrent<kChainReplay>(args, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" kda_status kda_commit_replay(kda_dims dims, const float* ring, int B, int T,
+                                        const int32_t* accepted, float* state_pool, int pool_slots,
+                                        const int32_t* state_idx, int32_t* err_flag,
+                                        void* stream) {
+  kda_status s = check_dims(dims);
+  if (s != KDA_OK) return s;
+  if (!state_pool || !state_idx) return KDA_ERR_NULL_ARG;
+  if (B < 0 || T < 1 || pool_slots < 0) return KDA_ERR_SHAPE;
+  if (B == 0) return KDA_OK;
+  if (!ring || !accepted) return KDA_ERR_NULL_ARG;
+  if (!aligned16(ring) || !aligned16(state_pool)) return KDA_ERR_ALIGNMENT;
+  StepArgs args{};
+  args.H = dims.H;
+  args.HV = dims.HV;
+  args.B = B;
+  args.T = T;
+  args.pool = state_pool;
+  args.pool_slots = pool_slots;
+  args.state_idx = state_idx;
+  args.ring = const_cast<float*>(ring);
+  args.accepted = accepted;
+  args.err_flag = err_flag;
+  return launch_recurrent<kCommitReplay>(args, static_cast<cudaStream_t>(stream));
 }

@@ -52,7 +52,8 @@ class kda_gate(ctypes.Structure):
 
 EXPORTS = ("kda_status_string", "kda_prefill_workspace_size", "kda_prefill", "kda_decode_packed",
            "kda_verify_chain", "kda_verify_tree", "kda_commit", "kda_set_stage_events",
-           "kda_prefill_noalloc")
+           "kda_prefill_noalloc", "kda_replay_ring_bytes", "kda_verify_chain_replay",
+           "kda_commit_replay")
 
 PREFILL_STATIC_SCRATCH_BYTES = 128 << 20
 
@@ -88,6 +89,13 @@ def load(path: str = LIB_PATH):
         lib.kda_prefill_noalloc.restype = i32
         lib.kda_prefill_noalloc.argtypes = [kda_dims, kda_gate, vp, vp, vp, vp, vp, i64, vp, i32, vp,
                                             vp, i32, i64, vp, vp, vp, vp]
+        lib.kda_replay_ring_bytes.restype = sz
+        lib.kda_replay_ring_bytes.argtypes = [kda_dims, i32, i32]
+        lib.kda_verify_chain_replay.restype = i32
+        lib.kda_verify_chain_replay.argtypes = [kda_dims, kda_gate, vp, i64, vp, vp, i32, i32, vp, i32,
+                                                vp, vp, vp, vp, vp]
+        lib.kda_commit_replay.restype = i32
+        lib.kda_commit_replay.argtypes = [kda_dims, vp, i32, i32, vp, vp, i32, vp, vp, vp]
         lib.kda_set_stage_events.restype = None
         lib.kda_set_stage_events.argtypes = [ctypes.POINTER(ctypes.c_void_p)]
         _lib = lib
@@ -215,6 +223,30 @@ def kda_commit(d, snapshots, B, T, accepted, state_pool, state_idx, err_flag=Non
     st = load().kda_commit(d, _p(snapshots), int(B), int(T), _p(accepted), _p(state_pool),
                            int(state_pool.shape[0]), _p(state_idx), _p(err_flag), _stream(stream))
     _check(st, "kda_commit")
+
+
+def kda_replay_ring_bytes(d, B, T) -> int:
+    return int(load().kda_replay_ring_bytes(d, int(B), int(T)))
+
+
+def kda_verify_chain_replay(d, gate: Gate, mixed_qkv, a, b, B, T, state_pool, state_idx, o, ring,
+                            err_flag=None, stream=None):
+    """Chain verify without snapshots: o as kda_verify_chain, each token's
+    folded inputs recorded in `ring` (kda_replay_ring_bytes bytes, FP32)."""
+    st = load().kda_verify_chain_replay(
+        d, gate.c(), _bf16(mixed_qkv, "mixed_qkv"), int(mixed_qkv.stride(0)), _bf16(a, "a"),
+        _bf16(b, "b"), int(B), int(T), _p(state_pool), int(state_pool.shape[0]), _p(state_idx),
+        _bf16(o, "o"), _p(ring), _p(err_flag), _stream(stream))
+    _check(st, "kda_verify_chain_replay")
+
+
+def kda_commit_replay(d, ring, B, T, accepted, state_pool, state_idx, err_flag=None, stream=None):
+    """Advances each request's pool state through its accepted draft tokens
+    from the ring written by kda_verify_chain_replay."""
+    st = load().kda_commit_replay(d, _p(ring), int(B), int(T), _p(accepted), _p(state_pool),
+                                  int(state_pool.shape[0]), _p(state_idx), _p(err_flag),
+                                  _stream(stream))
+    _check(st, "kda_commit_replay")
 
 
 def kda_set_stage_events(events=None):

@@ -113,3 +113,19 @@ def test_verify_and_commit_host_errors(lib):
                                DUMMY, DUMMY, None, None) == kda.KDA_ERR_NULL_ARG
     assert lib.kda_commit(d, DUMMY, 2, 6, DUMMY, None, 240, DUMMY, None, None) == kda.KDA_ERR_NULL_ARG
     assert lib.kda_commit(d, DUMMY, 2, 0, DUMMY, DUMMY, 240, DUMMY, None, None) == kda.KDA_ERR_SHAPE
+
+
+def test_replay_host_errors(lib):
+    d, g = kda.dims(16), _gate()
+    row = 3 * 16 * 128
+    # ring bytes: [B, T, HV, 388] FP32
+    assert lib.kda_replay_ring_bytes(d, 16, 6) == 16 * 6 * 16 * 388 * 4
+    assert lib.kda_verify_chain_replay(d, g, DUMMY, row, DUMMY, DUMMY, 2, 0, DUMMY, 240, DUMMY, DUMMY,
+                                       DUMMY, None, None) == kda.KDA_ERR_SHAPE
+    assert lib.kda_verify_chain_replay(d, g, DUMMY, row, DUMMY, DUMMY, 2, 6, DUMMY, 240, DUMMY, DUMMY,
+                                       None, None, None) == kda.KDA_ERR_NULL_ARG
+    assert lib.kda_commit_replay(d, None, 2, 6, DUMMY, DUMMY, 240, DUMMY, None, None) == kda.KDA_ERR_NULL_ARG
+    assert lib.kda_commit_replay(d, DUMMY, 2, 6, DUMMY, None, 240, DUMMY, None, None) == kda.KDA_ERR_NULL_ARG
+    assert lib.kda_commit_replay(d, DUMMY, 2, 0, DUMMY, DUMMY, 240, DUMMY, None, None) == kda.KDA_ERR_SHAPE
+    # nothing to do for B = 0
+    assert lib.kda_commit_replay(d, None, 0, 6, None, DUMMY, 240, DUMMY, None, None) == kda.KDA_OK
