@@ -87,27 +87,84 @@ struct FoldSmem {
   float red[kTokBlock][2][4];      // per-warp sums of squares of q and k
 };
 
+// 16-byte global -> shared copy (not through registers); the issuing thread
+// waits for its own copies with cp_async_wait_all.
+__device__ __forceinline__ void cp_async16(void* dst_smem, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                   static_cast<uint32_t>(__cvta_generic_to_shared(dst_smem))),
+               "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async4(void* dst_smem, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(
+                   static_cast<uint32_t>(__cvta_generic_to_shared(dst_smem))),
+               "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
 template <int MODE, int GROUPS>
 __global__ void __launch_bounds__(128) recurrent_kernel(const StepArgs args) {
   constexpr int K = kHeadDim, V = kHeadDim;
   __shared__ __align__(16) FoldSmem fs;
   __shared__ int tree_par[kTokBlock];  // tree: the parents of the first kTokBlock nodes
+  // raw BF16 token rows of this head: q, k, v, gate input, per token of the block
+  __shared__ __align__(16) uint16_t raw_s[kTokBlock][4][kHeadDim];
+  __shared__ uint16_t raw_b[kTokBlock];
   const int r = blockIdx.z, h = blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int sub = lane & 7;
   const int row0 = blockIdx.x * (16 * GROUPS) + warp * (4 * GROUPS) + (lane >> 3);
   const int HV = args.HV;
   const bool reporter = tid == 0 && blockIdx.x == 0 && h == 0;
-  // commit replay: tokens 0..accepted[r] of the verify's T are replayed
+  // commit replay: the ring records of the first block are copied into the
+  // fold buffers before the accepted index is known (4-byte and 16-byte
+  // asynchronous copies), then tokens 0..accepted[r] are replayed
+  if (MODE == kCommitReplay) {
+    const int n0 = args.T < kTokBlock ? args.T : kTokBlock;
+    for (int idx = tid; idx < n0 * 3 * 32; idx += 128) {
+      const int u = idx / 96, part = idx % 96, m = part >> 5, piece = (part & 31) * 4;
+      const float* rec = args.ring + (((int64_t)r * args.T + u) * args.HV + h) * kRingFloats;
+      float* dst = m == 0 ? &fs.k[u][piece] : m == 1 ? &fs.dec[u][piece] : &fs.v[u][piece];
+      cp_async16(dst, rec + m * kHeadDim + piece);
+    }
+    if (tid < n0)
+      cp_async4(&fs.beta[tid], args.ring + (((int64_t)r * args.T + tid) * args.HV + h) * kRingFloats +
+                                   3 * kHeadDim);
+    cp_async_commit();
+  }
   const int acc = MODE == kCommitReplay ? args.accepted[r] : 0;
   if (MODE == kCommitReplay) {
-    if (acc < 0) return;  // nothing accepted: the pool keeps its state
-    if (acc >= args.T) {
-      if (reporter) set_error(args.err_flag, KDA_DEVERR_ACCEPTED);
-      return;
+    if (acc < 0 || acc >= args.T) {
+      if (acc >= args.T && reporter) set_error(args.err_flag, KDA_DEVERR_ACCEPTED);
+      cp_async_wait_all();  // no copy into shared memory outlives the CTA
+      return;  // acc < 0: nothing accepted, the pool keeps its state
     }
   }
   const int T = MODE == kDecode ? 1 : MODE == kCommitReplay ? acc + 1 : args.T;
+
+  // Raw token rows of a block, copied 16 bytes at a time into raw_s.  The
+  // first block's copies are issued before anything that waits on memory,
+  // so their latency overlaps the slot lookup and the state load.
+  auto request_raw = [&](int tb, int nt) {
+    for (int idx = tid; idx < nt * 64; idx += 128) {
+      const int u = idx >> 6, m = (idx >> 4) & 3, piece = (idx & 15) * 8;
+      const int64_t row = MODE == kDecode ? r : (int64_t)r * T + tb + u;
+      const kda_bf16* x = args.mixed_qkv + row * args.row_stride;
+      const kda_bf16* src = m == 0 ? x + h * kHeadDim
+                          : m == 1 ? x + (int64_t)args.H * kHeadDim + h * kHeadDim
+                          : m == 2 ? x + 2 * (int64_t)args.H * kHeadDim + h * kHeadDim
+                                   : args.a + row * ((int64_t)args.HV * kHeadDim) + h * kHeadDim;
+      cp_async16(&raw_s[u][m][piece], src + piece);
+    }
+    cp_async_commit();
+    if (tid < nt) {
+      const int64_t row = MODE == kDecode ? r : (int64_t)r * T + tb + tid;
+      raw_b[tid] = args.b[row * args.HV + h];
+    }
+  };
+  if (MODE != kCommitReplay) request_raw(0, T < kTokBlock ? T : kTokBlock);
 
   const int slot = args.state_idx[r];
   const bool ok = slot >= -1 && slot < args.pool_slots;
@@ -127,6 +184,7 @@ __global__ void __launch_bounds__(128) recurrent_kernel(const StepArgs args) {
     if (!parents_ok && reporter) set_error(args.err_flag, KDA_DEVERR_PARENT);
   }
   if (!ok || slot < 0) {  // padding or rejected request: zero outputs, touch no state
+    cp_async_wait_all();  // no copy into shared memory outlives the CTA
     if (MODE != kCommitReplay && sub == 0)
       for (int i = 0; i < T; ++i)
 #pragma unroll
@@ -154,13 +212,18 @@ __global__ void __launch_bounds__(128) recurrent_kernel(const StepArgs args) {
   for (int tb = 0; tb < T; tb += kTokBlock) {
     const int nt = T - tb < kTokBlock ? T - tb : kTokBlock;
     // fold of tokens [tb, tb+nt): thread tid owns key channel / value column tid
+    if (MODE != kCommitReplay && tb > 0) request_raw(tb, nt);
+    if (tb == 0 || MODE != kCommitReplay) {
+      cp_async_wait_all();
+      __syncthreads();
+    }
     float sq[kTokBlock], sk[kTokBlock];
 #pragma unroll
     for (int u = 0; u < kTokBlock; ++u) {
       sq[u] = 0.f;
       sk[u] = 0.f;
       if (MODE == kCommitReplay) {  // folded values recorded by the verify
-        if (u < nt) {
+        if (u < nt && tb > 0) {  // the first block arrived by asynchronous copies
           const float* rec = args.ring + (((int64_t)r * args.T + tb + u) * HV + h) * kRingFloats;
           fs.k[u][tid] = rec[tid];
           fs.dec[u][tid] = rec[kHeadDim + tid];
@@ -168,16 +231,14 @@ __global__ void __launch_bounds__(128) recurrent_kernel(const StepArgs args) {
           if (tid == 0) fs.beta[u] = rec[3 * kHeadDim];
         }
       } else if (u < nt) {
-        const int64_t row = MODE == kDecode ? r : (int64_t)r * T + tb + u;
-        const kda_bf16* x = args.mixed_qkv + row * args.row_stride;
-        const float qv = bf16_bits_to_float(x[h * K + tid]);
-        const float kv = bf16_bits_to_float(x[(int64_t)args.H * K + h * K + tid]);
-        const float av = bf16_bits_to_float(args.a[row * ((int64_t)HV * K) + h * K + tid]);
+        const float qv = bf16_bits_to_float(raw_s[u][0][tid]);
+        const float kv = bf16_bits_to_float(raw_s[u][1][tid]);
+        const float av = bf16_bits_to_float(raw_s[u][3][tid]);
         fs.q[u][tid] = qv;
         fs.k[u][tid] = kv;
-        fs.v[u][tid] = bf16_bits_to_float(x[2 * (int64_t)args.H * K + h * V + tid]);
+        fs.v[u][tid] = bf16_bits_to_float(raw_s[u][2][tid]);
         fs.dec[u][tid] = expf(gate_log_decay(ga, av, exp_alog, bias_c));
-        if (tid == 0) fs.beta[u] = fold_beta(ga, bf16_bits_to_float(args.b[row * HV + h]));
+        if (tid == 0) fs.beta[u] = fold_beta(ga, bf16_bits_to_float(raw_b[u]));
         sq[u] = qv * qv;
         sk[u] = kv * kv;
       }
