@@ -416,29 +416,9 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
     if (tid == 0) tc::bulk_wait_read();
     __syncthreads();
 
-    // 2. gamma to the workspace; Khat^T (hi/lo, swizzled 128 x 64) built in the
-    //    A2 region (free until step 6) and sent to the workspace as one bulk copy.
+    // 2. gamma to the workspace (Khat^T follows in step 3, while the first
+    //    M1 product runs).
     if (tid < K) reinterpret_cast<float*>(rec + kRecGam)[tid] = decay_exp(GM[(kChunk - 1) * kLd + tid]);
-    for (int idx = tid; idx < K * 8; idx += kTxThreads) {
-      const int c = idx & (K - 1), j = idx >> 7;
-      const float gl = GM[(kChunk - 1) * kLd + c];
-      float x[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int t = j * 8 + e;
-        x[e] = bf16_at(Ks, t, c) * rk[t] * decay_exp(gl - GM[t * kLd + c]);
-      }
-      st_split8(A2h, A2h + 128 * 64 * 2, tc::sw128_offset(c, j * 8, K), x);
-    }
-    tc::fence_async_smem();
-    tc::tc_fence_before();
-    __syncthreads();
-    tc::tc_fence_after();
-    if (tid == 0) {
-      static_assert(kRecKTl == kRecKTh + 128 * 64 * 2, "Khat^T hi and lo are contiguous");
-      tc::bulk_s2g(rec + kRecKTh, A2h, 2 * 128 * 64 * 2);
-      tc::bulk_commit();
-    }
     const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
 
     // 3. M1 in two rounds (see the header of this kernel).  Warp w builds the
@@ -492,6 +472,28 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
         }
         tc::mma_commit(&mma_bar);
       }
+      if (round == 0) {
+        // Khat^T (hi/lo, swizzled 128 x 64), built in the A2 region (free until
+        // step 6) while the tensor core works, and sent out as one bulk copy.
+        for (int idx = tid; idx < K * 8; idx += kTxThreads) {
+          const int c = idx & (K - 1), j = idx >> 7;
+          const float gl = GM[(kChunk - 1) * kLd + c];
+          float x[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int t = j * 8 + e;
+            x[e] = bf16_at(Ks, t, c) * rk[t] * decay_exp(gl - GM[t * kLd + c]);
+          }
+          st_split8(A2h, A2h + 128 * 64 * 2, tc::sw128_offset(c, j * 8, K), x);
+        }
+        tc::fence_async_smem();
+        __syncthreads();
+        if (tid == 0) {
+          static_assert(kRecKTl == kRecKTh + 128 * 64 * 2, "Khat^T hi and lo are contiguous");
+          tc::bulk_s2g(rec + kRecKTh, A2h, 2 * 128 * 64 * 2);
+          tc::bulk_commit();
+        }
+      }
       if (!tc::mbar_wait(&mma_bar, phase)) s_abort = 1;
       phase ^= 1;
       tc::tc_fence_after();
@@ -528,6 +530,7 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
         }
       }
     }
+    if (tid == 0) tc::bulk_wait_read();  // Khat^T staging: the A2 region is reused in step 6
     tc::tc_fence_before();
     __syncthreads();
 
@@ -602,13 +605,15 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
 
     // 6. A2 = [Ti; P Ti] on the tensor core: D = [I; P] Ti, M=128 N=64 K=64.
     //    Operands: X = [I; P] (128 x 64, K = i) in the R region, Ti^T (64 x 64,
-    //    rows j, K = i) over the dead A block; both hi/lo.  The result lands in
-    //    TMEM columns 128-191 and is split into A2 (hi/lo) by all warps.
+    //    rows j, K = i) in the A2 region; both hi/lo.  While the product runs,
+    //    B2 (step 7) is built in the lower L/R region, dead by then; the result
+    //    lands in TMEM columns 128-191 and is split into A2 (hi/lo) by all warps.
     {
       uint8_t* Xh = Rh;                     // 128 x 64, 16 KB each half
       uint8_t* Xl = Xh + 128 * 64 * 2;
-      uint8_t* Th = sb + kTxAf;             // 64 x 64, 8 KB each half
+      uint8_t* Th = A2h;                    // 64 x 64, 8 KB each half
       uint8_t* Tl = Th + 64 * 64 * 2;
+      static_assert(kTxB2 + 2 * 256 * 64 * 2 <= kTxR, "B2 stays clear of X");
       for (int idx = tid; idx < 128 * 8 + 64 * 8; idx += kTxThreads) {
         float x[8];
         if (idx < 128 * 8) {                // X rows: identity (0-63) or P (64-127)
@@ -624,7 +629,6 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
           st_split8(Th, Tl, tc::sw128_offset(j, ch * 8, 64), x);
         }
       }
-      if (tid == 0) tc::bulk_wait_read();  // Khat^T staging (A2 region) reused below
       tc::fence_async_smem();
       tc::tc_fence_before();
       __syncthreads();
@@ -641,10 +645,31 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
                          idesc, p > 0 || k > 0);
         tc::mma_commit(&mma_bar);
       }
+      // 7. B2 = [(beta Ktil)^T ; (beta V)^T] (hi/lo, swizzled 256 x 64): row -> channel
+      for (int idx = tid; idx < K * 8; idx += kTxThreads) {  // rows 0-127: beta_i k-hat_i e^{Gam_i}
+        const int c = idx & (K - 1), ch = idx >> 7;
+        float x[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int i = ch * 8 + e;
+          x[e] = bf16_at(Ks, i, c) * (bt[i] * rk[i]) * decay_exp(GM[i * kLd + c]);
+        }
+        st_split8(Bh, Bl, tc::sw128_offset(c, ch * 8, 256), x);
+      }
+      for (int idx = tid; idx < K * 8; idx += kTxThreads) {  // rows 128-255: beta_i v_i
+        const int c = idx & (K - 1), ch = idx >> 7;
+        float x[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int i = ch * 8 + e;
+          x[e] = bf16_at(Vs, i, c) * bt[i];
+        }
+        st_split8(Bh, Bl, tc::sw128_offset(K + c, ch * 8, 256), x);
+      }
       if (!tc::mbar_wait(&mma_bar, phase)) s_abort = 1;
       phase ^= 1;
       tc::tc_fence_after();
-      // TMEM -> A2: warp group g takes 8 of the 64 columns
+      // TMEM -> A2 (Ti^T is dead now): warp group g takes 8 of the 64 columns
       {
         const int row = (warp & 3) * 32 + lane, c0 = (warp >> 2) * (64 / (kTxWarps / 4));
         for (int cc = 0; cc < 64 / (kTxWarps / 4); cc += 8) {
@@ -653,29 +678,6 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
           st_split8(A2h, A2l, tc::sw128_offset(row, c0 + cc, 128), d);
         }
       }
-    }
-    tc::tc_fence_before();
-    __syncthreads();  // X, Ti^T (L/R region) are dead before B2 overwrites it
-    // 7. B2 = [(beta Ktil)^T ; (beta V)^T] (hi/lo, swizzled 256 x 64): row -> channel
-    for (int idx = tid; idx < K * 8; idx += kTxThreads) {  // rows 0-127: beta_i k-hat_i e^{Gam_i}
-      const int c = idx & (K - 1), ch = idx >> 7;
-      float x[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int i = ch * 8 + e;
-        x[e] = bf16_at(Ks, i, c) * (bt[i] * rk[i]) * decay_exp(GM[i * kLd + c]);
-      }
-      st_split8(Bh, Bl, tc::sw128_offset(c, ch * 8, 256), x);
-    }
-    for (int idx = tid; idx < K * 8; idx += kTxThreads) {  // rows 128-255: beta_i v_i
-      const int c = idx & (K - 1), ch = idx >> 7;
-      float x[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int i = ch * 8 + e;
-        x[e] = bf16_at(Vs, i, c) * bt[i];
-      }
-      st_split8(Bh, Bl, tc::sw128_offset(K + c, ch * 8, 256), x);
     }
     tc::fence_async_smem();
     tc::tc_fence_before();
