@@ -57,8 +57,8 @@ LAYERS = 8  # default decode/verify/commit calls per timed replay (--layers)
 # keyed by kernel; valid only while the kernel sources hash to the recorded value.
 NCU_TRAFFIC = {
     # the four segment launches of one 1x4096 prefill call, 16 heads: read
-    # 67,593,728 B + write 10,240 B (profiles/chunk_transform_1x4096_h16.md)
-    "prefill_transform": {"bytes": 67603968, "src": "252242181ca7a494"},
+    # 67,632,896 B + write 22,272 B (profiles/chunk_transform_1x4096_h16.md)
+    "prefill_transform": {"bytes": 67655168, "src": "8b1b19b50a3cd8f6"},
 }
 
 
