@@ -104,8 +104,14 @@ __device__ __forceinline__ void cp_async4(void* dst_smem, const void* src) {
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
+// CTAs per SM the register allocation must allow: 7 (72 registers) lets the
+// 1024 CTAs of a 16-request chain verify run as one wave; tree verify would
+// spill there and gets 5.
+template <int MODE>
+constexpr int kMinCtasPerSm = MODE == kTree ? 5 : 7;
+
 template <int MODE, int GROUPS>
-__global__ void __launch_bounds__(128) recurrent_kernel(const StepArgs args) {
+__global__ void __launch_bounds__(128, kMinCtasPerSm<MODE>) recurrent_kernel(const StepArgs args) {
   constexpr int K = kHeadDim, V = kHeadDim;
   __shared__ __align__(16) FoldSmem fs;
   __shared__ int tree_par[kTokBlock];  // tree: the parents of the first kTokBlock nodes
@@ -246,14 +252,16 @@ __global__ void __launch_bounds__(128) recurrent_kernel(const StepArgs args) {
     if (MODE != kCommitReplay && ga.use_qk_l2norm) {
 #pragma unroll
       for (int u = 0; u < kTokBlock; ++u) {
+        if (u < nt) {  // nt is the same in every thread
 #pragma unroll
-        for (int m = 16; m; m >>= 1) {
-          sq[u] += __shfl_xor_sync(0xffffffffu, sq[u], m);
-          sk[u] += __shfl_xor_sync(0xffffffffu, sk[u], m);
-        }
-        if (lane == 0) {
-          fs.red[u][0][warp] = sq[u];
-          fs.red[u][1][warp] = sk[u];
+          for (int m = 16; m; m >>= 1) {
+            sq[u] += __shfl_xor_sync(0xffffffffu, sq[u], m);
+            sk[u] += __shfl_xor_sync(0xffffffffu, sk[u], m);
+          }
+          if (lane == 0) {
+            fs.red[u][0][warp] = sq[u];
+            fs.red[u][1][warp] = sk[u];
+          }
         }
       }
       __syncthreads();
