@@ -10,8 +10,8 @@ Speed Tests and Profiling: 16 heads x 128, BF16 inputs, FP32 state, bounded
 gate -5) with the concrete draws chosen for this library:
 
   q, k, v, gate input a, raw beta  ~ N(0, 1), rounded to BF16 (nearest-even)
-  A_log [H] ~ U(-1, 1),  dt_bias [H, K] ~ N(0, 0.1)   (FP32)
-  state pool [slots, H, V, K] ~ N(0, 0.02) in FP32 (or zero)
+  A_log [HV] ~ U(-1, 1),  dt_bias [HV, K] ~ N(0, 0.1)   (FP32)
+  state pool [slots, HV, V, K] ~ N(0, 0.02) in FP32 (or zero)
   varlen lengths U[1, 8192] with one length forced to 1, redrawn from the same
   stream until the total fits the padded bucket
   gate/beta padding rows: +-1e4 and NaN garbage (must never be read)
@@ -74,37 +74,39 @@ def varlen_lengths(rng, n=8, max_len=8192, bucket=32768):
 
 
 def prefill_inputs(seed=0, lengths=(128,), H=4, K=HEAD_DIM, V=HEAD_DIM, slots=4, gb_rows=None,
-                   state_idx=None, zero_state=False, varlen=True, garbage=True):
+                   state_idx=None, zero_state=False, varlen=True, garbage=True, HV=None):
     """Inputs of one prefill call.
 
     lengths: per-sequence token counts; varlen=False means the fixed layout
     (cu_seqlens absent, all lengths equal).  gb_rows >= sum(lengths) is the
-    padded gate/beta row count."""
+    padded gate/beta row count.  HV (default H) value heads: q and k have H
+    heads, everything else HV."""
+    HV = H if HV is None else HV
     rng = np.random.default_rng(seed)
     lengths = np.asarray(lengths, dtype=np.int64)
     T = int(lengths.sum())
     gb_rows = T if gb_rows is None else int(gb_rows)
     assert gb_rows >= T
-    A_log, dt_bias = gate_params(rng, H, K)
+    A_log, dt_bias = gate_params(rng, HV, K)
     out = dict(
         q=_normal_bf16(rng, (T, H, K)),
         k=_normal_bf16(rng, (T, H, K)),
-        v=_normal_bf16(rng, (T, H, V)),
-        g=np.empty((gb_rows, H, K), dtype=np.int16),
-        beta=np.empty((gb_rows, H), dtype=np.int16),
+        v=_normal_bf16(rng, (T, HV, V)),
+        g=np.empty((gb_rows, HV, K), dtype=np.int16),
+        beta=np.empty((gb_rows, HV), dtype=np.int16),
         A_log=A_log, dt_bias=dt_bias,
     )
-    out["g"][:T] = _normal_bf16(rng, (T, H, K))
-    out["beta"][:T] = _normal_bf16(rng, (T, H))
+    out["g"][:T] = _normal_bf16(rng, (T, HV, K))
+    out["beta"][:T] = _normal_bf16(rng, (T, HV))
     if gb_rows > T:
         if garbage:  # own stream, so the other inputs do not depend on it
             grng = np.random.default_rng([seed, 7919])
-            out["g"][T:] = _garbage_bf16(grng, (gb_rows - T, H, K))
-            out["beta"][T:] = _garbage_bf16(grng, (gb_rows - T, H))
+            out["g"][T:] = _garbage_bf16(grng, (gb_rows - T, HV, K))
+            out["beta"][T:] = _garbage_bf16(grng, (gb_rows - T, HV))
         else:
             out["g"][T:] = 0
             out["beta"][T:] = 0
-    out["pool"] = state_pool(rng, slots, H, K, V, zero=zero_state)
+    out["pool"] = state_pool(rng, slots, HV, K, V, zero=zero_state)
     n = len(lengths)
     if state_idx is None:
         state_idx = rng.permutation(slots)[:n]
@@ -115,24 +117,26 @@ def prefill_inputs(seed=0, lengths=(128,), H=4, K=HEAD_DIM, V=HEAD_DIM, slots=4,
     return out
 
 
-def packed_rows(rng, rows, H, K=HEAD_DIM, V=HEAD_DIM):
-    """rows of mixed_qkv [rows, 2*H*K + H*V], gate input a [rows, H*K], raw
-    beta b [rows, H], all BF16 bits."""
+def packed_rows(rng, rows, H, K=HEAD_DIM, V=HEAD_DIM, HV=None):
+    """rows of mixed_qkv [rows, 2*H*K + HV*V], gate input a [rows, HV*K], raw
+    beta b [rows, HV], all BF16 bits (HV defaults to H)."""
+    HV = H if HV is None else HV
     return dict(
-        mixed_qkv=_normal_bf16(rng, (rows, 2 * H * K + H * V)),
-        a=_normal_bf16(rng, (rows, H * K)),
-        b=_normal_bf16(rng, (rows, H)),
+        mixed_qkv=_normal_bf16(rng, (rows, 2 * H * K + HV * V)),
+        a=_normal_bf16(rng, (rows, HV * K)),
+        b=_normal_bf16(rng, (rows, HV)),
     )
 
 
-def decode_inputs(seed=0, B=16, H=16, K=HEAD_DIM, V=HEAD_DIM, slots=240, zero_state=False):
+def decode_inputs(seed=0, B=16, H=16, K=HEAD_DIM, V=HEAD_DIM, slots=240, zero_state=False, HV=None):
     """One packed decode call: B requests gathered from a slots-deep pool by a
     random permutation prefix."""
+    HV = H if HV is None else HV
     rng = np.random.default_rng(seed)
-    A_log, dt_bias = gate_params(rng, H, K)
-    out = packed_rows(rng, B, H, K, V)
+    A_log, dt_bias = gate_params(rng, HV, K)
+    out = packed_rows(rng, B, H, K, V, HV)
     out.update(A_log=A_log, dt_bias=dt_bias,
-               pool=state_pool(rng, slots, H, K, V, zero=zero_state),
+               pool=state_pool(rng, slots, HV, K, V, zero=zero_state),
                state_idx=rng.permutation(slots)[:B].astype(np.int32))
     return out
 
@@ -151,13 +155,15 @@ def tree_parents(rng, B, T):
     return par
 
 
-def verify_inputs(seed=0, B=16, T=6, H=16, K=HEAD_DIM, V=HEAD_DIM, slots=240, zero_state=False):
+def verify_inputs(seed=0, B=16, T=6, H=16, K=HEAD_DIM, V=HEAD_DIM, slots=240, zero_state=False,
+                  HV=None):
     """One verify call: B requests x T draft tokens, request-major rows."""
+    HV = H if HV is None else HV
     rng = np.random.default_rng(seed)
-    A_log, dt_bias = gate_params(rng, H, K)
-    out = packed_rows(rng, B * T, H, K, V)
+    A_log, dt_bias = gate_params(rng, HV, K)
+    out = packed_rows(rng, B * T, H, K, V, HV)
     out.update(A_log=A_log, dt_bias=dt_bias,
-               pool=state_pool(rng, slots, H, K, V, zero=zero_state),
+               pool=state_pool(rng, slots, HV, K, V, zero=zero_state),
                state_idx=rng.permutation(slots)[:B].astype(np.int32),
                parent=tree_parents(rng, B, T))
     return out

@@ -53,7 +53,13 @@
  *     sequence, [sum_n ceil(T_n/chunk), HV, V, K], sequence-major.
  *   - snapshot[b][i] is the state after consuming draft token i; a tree node's
  *     state is one step from its parent's state (parent -1 = pool state).
- *   - only H == HV (no grouped value heads).
+ *   - grouped value heads: HV may be a multiple of H, and value head h then
+ *     takes its q and k from q/k head h / (HV / H) (all other per-head
+ *     inputs, the gate parameters and the state are per value head).  The
+ *     pages' packed-decode validator reads HV from the state shape and checks
+ *     the gate input against HV*K, while the q and k widths of a packed row
+ *     follow H; the grouping itself is not printed there, and this is the
+ *     plainest reading.
  *
  * Build: gcc -O2 -std=c11 -Wall -Werror -ffp-contract=off -fPIC -shared -o libkda_oracle.so
  *        kda_oracle.c -lm -lpthread
@@ -209,6 +215,11 @@ static size_t step_scratch(const kdao_params *p) {
   return (size_t)3 * p->K + (size_t)p->V + (size_t)p->K * p->V;
 }
 
+/* head counts: HV value heads in groups over H q/k heads */
+static int heads_ok(const kdao_params *p) {
+  return p->H >= 1 && p->HV >= p->H && p->HV % p->H == 0;
+}
+
 static int slots_distinct_and_valid(const int *idx, int n, int pool_slots) {
   for (int i = 0; i < n; ++i) {
     if (idx[i] < -1 || idx[i] >= pool_slots) return KDAO_ERR_SLOT;
@@ -257,7 +268,8 @@ static void prefill_unit(void *vctx, long unit, double *scratch) {
              sizeof(double) * (size_t)K * V);
     }
     double beta;
-    fold_token(p, h, cx->q + (t * H + h) * K, cx->k + (t * H + h) * K,
+    const int hk = h / (HV / H); /* q/k head of value head h */
+    fold_token(p, h, cx->q + (t * H + hk) * K, cx->k + (t * H + hk) * K,
                cx->g + (t * HV + h) * K, cx->beta[t * HV + h], q, k, g, &beta);
     gated_delta_step(K, V, st, q, k, cx->v + (t * HV + h) * V, g, beta, p->scale,
                      cx->o + (t * HV + h) * V, work);
@@ -275,7 +287,7 @@ int kdao_prefill(const kdao_params *p, const float *q, const float *k,
                  long total_tokens, int chunk, double *o, double *intermediate,
                  int nthreads) {
   if (!p || !pool || !state_idx || num_seqs < 1 || total_tokens < 0 ||
-      chunk < 1 || p->H != p->HV)
+      chunk < 1 || !heads_ok(p))
     return KDAO_ERR_ARG;
   if (gb_rows < total_tokens) return KDAO_ERR_ARG; /* g/beta must cover q */
   int rc = slots_distinct_and_valid(state_idx, num_seqs, pool_slots);
@@ -345,7 +357,8 @@ static void decode_unit(void *vctx, long unit, double *scratch) {
   }
   const float *row = cx->mixed_qkv + r * cx->row_stride;
   double beta;
-  fold_token(p, h, row + h * K, row + (long)H * K + h * K,
+  const int hk = h / (HV / H); /* q/k head of value head h */
+  fold_token(p, h, row + hk * K, row + (long)H * K + hk * K,
              cx->a + (r * HV + h) * K, cx->b[r * HV + h], q, k, g, &beta);
   gated_delta_step(K, V, cx->pool + ((long)slot * HV + h) * (long)V * K, q, k,
                    row + 2L * H * K + (long)h * V, g, beta, p->scale, o, work);
@@ -354,7 +367,7 @@ static void decode_unit(void *vctx, long unit, double *scratch) {
 int kdao_decode(const kdao_params *p, const float *mixed_qkv, long row_stride,
                 const float *a, const float *b, int B, double *pool,
                 int pool_slots, const int *state_idx, double *o, int nthreads) {
-  if (!p || !pool || !state_idx || B < 0 || p->H != p->HV ||
+  if (!p || !pool || !state_idx || B < 0 || !heads_ok(p) ||
       row_stride < 2L * p->H * p->K + (long)p->HV * p->V)
     return KDAO_ERR_ARG;
   int rc = slots_distinct_and_valid(state_idx, B, pool_slots);
@@ -402,7 +415,8 @@ static void verify_unit(void *vctx, long unit, double *scratch) {
     const long row = r * T + i;
     const float *x = cx->mixed_qkv + row * cx->row_stride;
     double beta;
-    fold_token(p, h, x + h * K, x + (long)H * K + h * K,
+    const int hk = h / (HV / H); /* q/k head of value head h */
+    fold_token(p, h, x + hk * K, x + (long)H * K + hk * K,
                cx->a + (row * HV + h) * K, cx->b[row * HV + h], q, k, g, &beta);
     gated_delta_step(K, V, st, q, k, x + 2L * H * K + (long)h * V, g, beta,
                      p->scale, cx->o + (row * HV + h) * V, work);
@@ -419,7 +433,7 @@ int kdao_verify(const kdao_params *p, const float *mixed_qkv, long row_stride,
                 const int *state_idx, double *o, double *snapshots,
                 int nthreads) {
   if (!p || !pool || !state_idx || !snapshots || B < 0 || T < 1 ||
-      p->H != p->HV || row_stride < 2L * p->H * p->K + (long)p->HV * p->V)
+      !heads_ok(p) || row_stride < 2L * p->H * p->K + (long)p->HV * p->V)
     return KDAO_ERR_ARG;
   int rc = slots_distinct_and_valid(state_idx, B, pool_slots);
   if (rc) return rc;

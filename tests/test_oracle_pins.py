@@ -448,3 +448,66 @@ def test_invalid_inputs_are_rejected():
         ko.verify(gate, d["mixed_qkv"], d["a"], d["b"], 2, 3, pool, d["state_idx"], parent=bad)
     with pytest.raises(ko.OracleError):
         ko.verify(gate, d["mixed_qkv"], d["a"], d["b"], 2, 3, pool, np.array([0, 4], np.int32))
+
+
+# --------------------------------------------------------------------------- #
+# Grouped value heads: HV = G * H, value head h reading q/k head h // G.  The
+# same call with every q/k head repeated G times (H' = HV) takes the plain
+# one-q/k-head-per-value-head path and must give the same bits.
+
+G_GROUP = 2
+
+
+def _group_gate(Hq, HV, A_log, dt_bias):
+    return ko.Gate(Hq, K, V, HV=HV, A_log=A_log, dt_bias=dt_bias, lower_bound=-5.0)
+
+
+def _repeat_packed_qk(x, Hq):
+    """Packed rows [q (Hq*K) | k (Hq*K) | v] -> [q repeated | k repeated | v]."""
+    rows = x.shape[0]
+    q = np.repeat(x[:, :Hq * K].reshape(rows, Hq, K), G_GROUP, axis=1).reshape(rows, -1)
+    k = np.repeat(x[:, Hq * K:2 * Hq * K].reshape(rows, Hq, K), G_GROUP, axis=1).reshape(rows, -1)
+    return np.ascontiguousarray(np.concatenate([q, k, x[:, 2 * Hq * K:]], axis=1))
+
+
+def test_grouped_value_heads_prefill_equals_repeated_qk():
+    Hq, HV = 2, 2 * G_GROUP
+    d = inputs.prefill_inputs(seed=21, lengths=[70, 33], H=Hq, HV=HV, K=K, V=V, slots=4)
+    pool_g = d["pool"].astype(np.float64)
+    pool_p = pool_g.copy()
+    o_g, st_g = ko.prefill(_group_gate(Hq, HV, d["A_log"], d["dt_bias"]), d["q"], d["k"], d["v"], d["g"],
+                           d["beta"], pool_g, d["state_idx"], d["cu_seqlens"], intermediate=True)
+    o_p, st_p = ko.prefill(_group_gate(HV, HV, d["A_log"], d["dt_bias"]), np.repeat(d["q"], G_GROUP, axis=1),
+                           np.repeat(d["k"], G_GROUP, axis=1), d["v"], d["g"], d["beta"], pool_p,
+                           d["state_idx"], d["cu_seqlens"], intermediate=True)
+    assert np.array_equal(o_g, o_p) and np.array_equal(st_g, st_p) and np.array_equal(pool_g, pool_p)
+    # value heads of one group read the same q/k but their own v, gate and state
+    assert not np.array_equal(o_g[:, 0], o_g[:, 1])
+
+
+def test_grouped_value_heads_decode_and_verify_equal_repeated_qk():
+    Hq, HV = 2, 2 * G_GROUP
+    d = inputs.decode_inputs(seed=22, B=3, H=Hq, HV=HV, K=K, V=V, slots=5)
+    pool_g = d["pool"].astype(np.float64)
+    pool_p = pool_g.copy()
+    o_g = ko.decode(_group_gate(Hq, HV, d["A_log"], d["dt_bias"]), d["mixed_qkv"], d["a"], d["b"], pool_g,
+                    d["state_idx"])
+    o_p = ko.decode(_group_gate(HV, HV, d["A_log"], d["dt_bias"]), _repeat_packed_qk(d["mixed_qkv"], Hq),
+                    d["a"], d["b"], pool_p, d["state_idx"])
+    assert np.array_equal(o_g, o_p) and np.array_equal(pool_g, pool_p)
+
+    v = inputs.verify_inputs(seed=23, B=2, T=4, H=Hq, HV=HV, K=K, V=V, slots=5)
+    pool = v["pool"].astype(np.float64)
+    for parent in (None, v["parent"]):
+        og, sg = ko.verify(_group_gate(Hq, HV, v["A_log"], v["dt_bias"]), v["mixed_qkv"], v["a"], v["b"], 2, 4,
+                           pool, v["state_idx"], parent=parent)
+        op, sp = ko.verify(_group_gate(HV, HV, v["A_log"], v["dt_bias"]), _repeat_packed_qk(v["mixed_qkv"], Hq),
+                           v["a"], v["b"], 2, 4, pool, v["state_idx"], parent=parent)
+        assert np.array_equal(og, op) and np.array_equal(sg, sp)
+
+
+def test_head_counts_must_group():
+    d = inputs.prefill_inputs(seed=24, lengths=[8], H=2, HV=3, K=K, V=V, slots=2)
+    with pytest.raises(ko.OracleError):
+        ko.prefill(_group_gate(2, 3, d["A_log"], d["dt_bias"]), d["q"], d["k"], d["v"], d["g"], d["beta"],
+                   d["pool"].astype(np.float64), d["state_idx"], d["cu_seqlens"])
