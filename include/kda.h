@@ -36,7 +36,9 @@
  *   - A state slot of -1 marks a padding sequence/request: it is skipped,
  *     its output rows are written as zero and its pool slot is not touched.
  *   - Slots within one call must be distinct (a caller error otherwise).
- *   - This build supports H == HV and K == V == 128; other shapes return
+ *   - This build supports K == V == 128 and HV a multiple of H (grouped
+ *     value heads; the pages' packed-decode validator takes HV from the
+ *     state shape and the q/k widths from H); other shapes return
  *     KDA_ERR_UNSUPPORTED (non-power-of-two K or V are always rejected, as
  *     the packed-decode validator does).
  */
@@ -73,7 +75,9 @@ typedef enum {
 
 typedef struct {
   int H;  /* q/k heads */
-  int HV; /* value heads (== H in this build) */
+  int HV; /* value heads, a multiple of H: value head h reads q/k head
+             h / (HV / H) (grouped value heads); everything else is per
+             value head */
   int K;  /* key head dim (128) */
   int V;  /* value head dim (128) */
 } kda_dims;

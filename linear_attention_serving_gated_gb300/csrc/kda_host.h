@@ -24,7 +24,8 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 inline kda_status check_dims(const kda_dims& d) {
   if (d.H <= 0 || d.HV <= 0 || d.K <= 0 || d.V <= 0) return KDA_ERR_SHAPE;
   if (!is_pow2(d.K) || !is_pow2(d.V)) return KDA_ERR_UNSUPPORTED;
-  if (d.H != d.HV || d.K != kHeadDim || d.V != kHeadDim) return KDA_ERR_UNSUPPORTED;
+  // grouped value heads: HV a multiple of H, value head h reading q/k head h / (HV / H)
+  if (d.HV % d.H != 0 || d.K != kHeadDim || d.V != kHeadDim) return KDA_ERR_UNSUPPORTED;
   return KDA_OK;
 }
 

@@ -331,8 +331,9 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
       const int tensor = tid >> 7, tok = (tid >> 1) & 63, part = tid & 1;
       if (tok < s_pf.len) {
         const int64_t row = s_pf.t0 + tok;
-        const kda_bf16* base = tensor == 0 ? a.q + (row * a.H + s_pf_h) * kHeadDim
-                             : tensor == 1 ? a.k + (row * a.H + s_pf_h) * kHeadDim
+        const int hk = s_pf_h / (a.HV / a.H);  // q/k head of the value head
+        const kda_bf16* base = tensor == 0 ? a.q + (row * a.H + hk) * kHeadDim
+                             : tensor == 1 ? a.k + (row * a.H + hk) * kHeadDim
                              : tensor == 2 ? a.v + (row * a.HV + s_pf_h) * kHeadDim
                                            : a.g + (row * a.HV + s_pf_h) * kHeadDim;
         asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const uint8_t*>(base) + part * 128));
@@ -345,6 +346,7 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
     const int64_t t0 = loc.t0;
     const GateArgs& ga = a.gate;
     const int H = a.H, HV = a.HV, K = kHeadDim;
+    const int hk = h / (HV / H);  // q/k head of value head h
     uint8_t* rec = a.ws + ((size_t)cid * HV + h) * kRecBytes;
 
     // 1. fold.  Warp w owns tokens [4w, 4w+4), lane l channels [4l, 4l+4); all
@@ -366,8 +368,8 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
         br[u] = 0.f;
         if (t < len) {
           const int64_t tok = t0 + t;
-          qr[u] = __ldg(reinterpret_cast<const uint2*>(a.q + (tok * H + h) * K + c));
-          kr[u] = __ldg(reinterpret_cast<const uint2*>(a.k + (tok * H + h) * K + c));
+          qr[u] = __ldg(reinterpret_cast<const uint2*>(a.q + (tok * H + hk) * K + c));
+          kr[u] = __ldg(reinterpret_cast<const uint2*>(a.k + (tok * H + hk) * K + c));
           vr[u] = __ldg(reinterpret_cast<const uint2*>(a.v + (tok * HV + h) * K + c));
           ar[u] = __ldg(reinterpret_cast<const uint2*>(a.g + (tok * HV + h) * K + c));
           if (lane == 0) br[u] = bf16_bits_to_float(a.beta[tok * HV + h]);

@@ -43,6 +43,7 @@ constexpr int kRingFloats = 3 * kHeadDim + 4;
 struct StepArgs {
   GateArgs gate;
   int H, HV;
+  int G;  // value heads per q/k head (HV / H)
   const kda_bf16* mixed_qkv;
   int64_t row_stride;
   const kda_bf16* a;
@@ -153,16 +154,21 @@ __global__ void __launch_bounds__(128, kMinCtasPerSm<MODE>) recurrent_kernel(con
   // Raw token rows of a block, copied 16 bytes at a time into raw_s.  The
   // first block's copies are issued before anything that waits on memory,
   // so their latency overlaps the slot lookup and the state load.
+  // Thread tid copies 16-byte piece tid % 16 of tensor (tid / 16) % 4 (q, k,
+  // v of a packed row, or the gate input row) of tokens tid / 64, +2, ...:
+  // its element offset within the row is fixed.  Value head h reads q/k head
+  // h / G.
+  const int raw_m = (tid >> 4) & 3, raw_piece = (tid & 15) * 8;
+  const int raw_off = raw_piece + (raw_m == 0 ? (h / args.G) * kHeadDim
+                                 : raw_m == 1 ? (args.H + h / args.G) * kHeadDim
+                                 : raw_m == 2 ? (2 * args.H + h) * kHeadDim
+                                              : h * kHeadDim);
   auto request_raw = [&](int tb, int nt) {
-    for (int idx = tid; idx < nt * 64; idx += 128) {
-      const int u = idx >> 6, m = (idx >> 4) & 3, piece = (idx & 15) * 8;
+    for (int u = tid >> 6; u < nt; u += 2) {
       const int64_t row = MODE == kDecode ? r : (int64_t)r * T + tb + u;
-      const kda_bf16* x = args.mixed_qkv + row * args.row_stride;
-      const kda_bf16* src = m == 0 ? x + h * kHeadDim
-                          : m == 1 ? x + (int64_t)args.H * kHeadDim + h * kHeadDim
-                          : m == 2 ? x + 2 * (int64_t)args.H * kHeadDim + h * kHeadDim
-                                   : args.a + row * ((int64_t)args.HV * kHeadDim) + h * kHeadDim;
-      cp_async16(&raw_s[u][m][piece], src + piece);
+      const kda_bf16* x = raw_m < 3 ? args.mixed_qkv + row * args.row_stride
+                                    : args.a + row * ((int64_t)args.HV * kHeadDim);
+      cp_async16(&raw_s[u][raw_m][raw_piece], x + raw_off);
     }
     cp_async_commit();
     if (tid < nt) {
@@ -428,6 +434,7 @@ kda_status check_packed(const kda_dims& dims, const kda_gate& gate, const kda_bf
   if (s != KDA_OK) return s;
   out->H = dims.H;
   out->HV = dims.HV;
+  out->G = dims.HV / dims.H;
   out->mixed_qkv = mixed_qkv;
   out->row_stride = row_stride;
   out->a = a;

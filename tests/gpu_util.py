@@ -61,11 +61,14 @@ def assert_s_close(s_gpu, s_ref, what="state"):
     return err / max(rms(s_ref), 1e-300)
 
 
-def gates(d, lower_bound=-5.0, beta_is_raw=True, use_qk_l2norm=True, scale=None, H=None, K=128):
-    """Matching oracle and device gate descriptions from seeded inputs."""
-    H = H if H is not None else d["A_log"].shape[0]
+def gates(d, lower_bound=-5.0, beta_is_raw=True, use_qk_l2norm=True, scale=None, H=None, K=128, HV=None):
+    """Matching oracle and device gate descriptions from seeded inputs.  HV
+    value heads (default: the gate parameters' head count), H q/k heads
+    (default HV)."""
+    HV = HV if HV is not None else d["A_log"].shape[0]
+    H = H if H is not None else HV
     scale = scale if scale is not None else K ** -0.5
-    og = ko.Gate(H, K, K, A_log=d["A_log"], dt_bias=d["dt_bias"], lower_bound=lower_bound,
+    og = ko.Gate(H, K, K, HV=HV, A_log=d["A_log"], dt_bias=d["dt_bias"], lower_bound=lower_bound,
                  beta_is_raw=beta_is_raw, use_qk_l2norm=use_qk_l2norm, scale=scale)
     gg = kda.Gate(A_log=dev(d["A_log"]), dt_bias=dev(d["dt_bias"]), lower_bound=lower_bound,
                   beta_is_raw=beta_is_raw, use_qk_l2norm=use_qk_l2norm, scale=scale)

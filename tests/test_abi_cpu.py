@@ -72,7 +72,9 @@ def test_prefill_host_errors(lib):
     assert _prefill(lib, dims=kda.dims(4, K=96, V=128)) == kda.KDA_ERR_UNSUPPORTED
     assert _prefill(lib, dims=kda.dims(4, K=128, V=100)) == kda.KDA_ERR_UNSUPPORTED
     assert _prefill(lib, dims=kda.dims(4, K=64, V=64)) == kda.KDA_ERR_UNSUPPORTED
-    assert _prefill(lib, dims=kda.dims(4, HV=8)) == kda.KDA_ERR_UNSUPPORTED
+    # value heads come in whole groups per q/k head (HV a multiple of H)
+    assert _prefill(lib, dims=kda.dims(4, HV=6)) == kda.KDA_ERR_UNSUPPORTED
+    assert _prefill(lib, dims=kda.dims(4, HV=2)) == kda.KDA_ERR_UNSUPPORTED
     # bounded gate formula only
     assert _prefill(lib, gate=_gate(A_log=DUMMY, lb=math.nan)) == kda.KDA_ERR_UNSUPPORTED
     # the chunk form's decay windows need per-token log-decays >= -5.5
@@ -97,6 +99,7 @@ def test_decode_host_errors(lib):
     assert call(pool=None) == kda.KDA_ERR_NULL_ARG
     assert call(idx=None) == kda.KDA_ERR_NULL_ARG
     assert call(dims=kda.dims(16, K=96)) == kda.KDA_ERR_UNSUPPORTED
+    assert call(dims=kda.dims(16, HV=24)) == kda.KDA_ERR_UNSUPPORTED
     assert call(stride=row - 8) == kda.KDA_ERR_SHAPE
     assert call(stride=row + 4) == kda.KDA_ERR_ALIGNMENT
     assert call(B=0) == kda.KDA_OK  # nothing to do, nothing launched
