@@ -25,7 +25,9 @@
  *     library allocates nothing, never synchronises and never reads device
  *     memory from the host, so each call can be captured in a CUDA graph and
  *     replayed with new device-resident indices.
- *   - BF16 tensors are passed as raw 16-bit patterns (kda_bf16).
+ *   - 16-bit token tensors (q, k, v, g, beta, mixed_qkv, a, b, o) are passed
+ *     as raw bit patterns (kda_bf16): BF16, or FP16 when kda_dims.dtype is
+ *     KDA_DTYPE_F16.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy stream).
  *   - Host-checkable errors return a status and launch nothing.
  *   - Device-resident index errors (a state slot outside [-1, pool_slots), a
@@ -52,7 +54,7 @@
 extern "C" {
 #endif
 
-typedef uint16_t kda_bf16; /* raw BF16 bits */
+typedef uint16_t kda_bf16; /* raw 16-bit element bits: BF16, or FP16 per kda_dims.dtype */
 
 typedef enum {
   KDA_OK = 0,
@@ -73,6 +75,14 @@ typedef enum {
                                  tensor-core work ran out; its unit was not
                                  written back */
 
+/* element type of the token tensors (q, k, v, g, beta, mixed_qkv, a, b) and
+ * of the output o: the "two precisions" of the pages' prefill sweep
+ * ("PR #35197 report: fix(kernel) Fix Helion small-token prefill bug",
+ * implementation step 4).  States, snapshots, rings and the gate parameters
+ * are FP32 either way. */
+#define KDA_DTYPE_BF16 0
+#define KDA_DTYPE_F16 1
+
 typedef struct {
   int H;  /* q/k heads */
   int HV; /* value heads, a multiple of H: value head h reads q/k head
@@ -80,6 +90,7 @@ typedef struct {
              value head */
   int K;  /* key head dim (128) */
   int V;  /* value head dim (128) */
+  int dtype; /* KDA_DTYPE_BF16 (0, so a zeroed struct means BF16) or KDA_DTYPE_F16 */
 } kda_dims;
 
 typedef struct {

@@ -10,6 +10,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 #include "../../include/kda.h"
@@ -36,15 +37,42 @@ __device__ __forceinline__ uint16_t float_to_bf16_bits(float x) {
   return __bfloat16_as_ushort(__float2bfloat16_rn(x));
 }
 
-// Four consecutive BF16 values (8-byte aligned) widened to float.
-__device__ __forceinline__ float4 load_bf16x4(const kda_bf16* p) {
-  const uint2 u = __ldg(reinterpret_cast<const uint2*>(p));
-  float4 r;
-  r.x = __uint_as_float(u.x << 16);
-  r.y = __uint_as_float(u.x & 0xffff0000u);
-  r.z = __uint_as_float(u.y << 16);
-  r.w = __uint_as_float(u.y & 0xffff0000u);
-  return r;
+// Token tensors (q, k, v, gate input, beta, packed rows) and the output o
+// hold 16-bit elements: BF16 (F16 = false) or FP16 (F16 = true), per
+// kda_dims.dtype.  Widening is exact; narrowing rounds to nearest even.
+template <bool F16>
+__device__ __forceinline__ float in16_to_float(uint16_t x) {
+  if constexpr (F16)
+    return __half2float(__ushort_as_half(x));
+  else
+    return bf16_bits_to_float(x);
+}
+
+template <bool F16>
+__device__ __forceinline__ uint16_t float_to_out16(float x) {
+  if constexpr (F16)
+    return __half_as_ushort(__float2half_rn(x));
+  else
+    return float_to_bf16_bits(x);
+}
+
+// Four consecutive 16-bit elements (one 8-byte word) widened to float.
+template <bool F16>
+__device__ __forceinline__ float4 in16x4_to_f4(uint2 u) {
+  if constexpr (F16) {
+    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+    const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+    return make_float4(a.x, a.y, b.x, b.y);
+  } else {
+    return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
+                       __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
+  }
+}
+
+// Two floats narrowed to one 32-bit word of 16-bit output elements (lo first).
+template <bool F16>
+__device__ __forceinline__ uint32_t pack_out16x2(float lo, float hi) {
+  return (uint32_t)float_to_out16<F16>(lo) | ((uint32_t)float_to_out16<F16>(hi) << 16);
 }
 
 __device__ __forceinline__ float sigmoidf_(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }

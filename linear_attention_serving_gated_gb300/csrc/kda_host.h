@@ -26,6 +26,7 @@ inline kda_status check_dims(const kda_dims& d) {
   if (!is_pow2(d.K) || !is_pow2(d.V)) return KDA_ERR_UNSUPPORTED;
   // grouped value heads: HV a multiple of H, value head h reading q/k head h / (HV / H)
   if (d.HV % d.H != 0 || d.K != kHeadDim || d.V != kHeadDim) return KDA_ERR_UNSUPPORTED;
+  if (d.dtype != KDA_DTYPE_BF16 && d.dtype != KDA_DTYPE_F16) return KDA_ERR_UNSUPPORTED;
   return KDA_OK;
 }
 

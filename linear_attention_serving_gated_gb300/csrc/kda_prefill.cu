@@ -222,18 +222,16 @@ __device__ __forceinline__ void st_split8(uint8_t* hi, uint8_t* lo, uint32_t off
   *reinterpret_cast<uint4*>(lo + off) = make_uint4(l[0], l[1], l[2], l[3]);
 }
 
-__device__ __forceinline__ float bf16_at(const uint8_t* tile, int t, int c) {
-  return bf16_bits_to_float(reinterpret_cast<const uint16_t*>(tile)[t * kLdB + c]);
+// Element (t, c) of a raw 16-bit input tile (BF16 or FP16 bits), widened.
+template <bool F16>
+__device__ __forceinline__ float in_at(const uint8_t* tile, int t, int c) {
+  return in16_to_float<F16>(reinterpret_cast<const uint16_t*>(tile)[t * kLdB + c]);
 }
 
-__device__ __forceinline__ float4 bf16x4_to_f4(uint2 u) {
-  return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
-                     __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
-}
-
-// Four consecutive BF16 values of row t, columns [c, c+4), of a raw tile.
-__device__ __forceinline__ float4 ld_bf16x4(const uint8_t* tile, int t, int c) {
-  return bf16x4_to_f4(*reinterpret_cast<const uint2*>(tile + (t * kLdB + c) * 2));
+// Four consecutive values of row t, columns [c, c+4), of a raw input tile.
+template <bool F16>
+__device__ __forceinline__ float4 ld_in4(const uint8_t* tile, int t, int c) {
+  return in16x4_to_f4<F16>(*reinterpret_cast<const uint2*>(tile + (t * kLdB + c) * 2));
 }
 
 __device__ __forceinline__ float4 scale4(float4 a, float s) {
@@ -268,6 +266,7 @@ __device__ ChunkLoc unit_loc(const PrefillArgs& a, int64_t u, int64_t* cid, int*
 
 // Persistent: CTA b takes units b, b + gridDim.x, ...  While it works on one
 // unit, the next unit's q, k, v and gate rows are prefetched into L2.
+template <bool F16>
 __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const PrefillArgs a) {
   extern __shared__ uint8_t smraw[];
   __shared__ uint64_t mma_bar;
@@ -372,7 +371,7 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
           kr[u] = __ldg(reinterpret_cast<const uint2*>(a.k + (tok * H + hk) * K + c));
           vr[u] = __ldg(reinterpret_cast<const uint2*>(a.v + (tok * HV + h) * K + c));
           ar[u] = __ldg(reinterpret_cast<const uint2*>(a.g + (tok * HV + h) * K + c));
-          if (lane == 0) br[u] = bf16_bits_to_float(a.beta[tok * HV + h]);
+          if (lane == 0) br[u] = in16_to_float<F16>(a.beta[tok * HV + h]);
         }
       }
       const float exp_alog = __expf(alog);
@@ -381,7 +380,7 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
       for (int u = 0; u < kTpw; ++u) {
         const int t = warp * kTpw + u;
         const bool live = t < len;
-        const float4 q4 = bf16x4_to_f4(qr[u]), k4 = bf16x4_to_f4(kr[u]), a4 = bf16x4_to_f4(ar[u]);
+        const float4 q4 = in16x4_to_f4<F16>(qr[u]), k4 = in16x4_to_f4<F16>(kr[u]), a4 = in16x4_to_f4<F16>(ar[u]);
         const float sq = warp_sum(dot4(q4, q4)), sk = warp_sum(dot4(k4, k4));
         float4 g4 = make_float4(0.f, 0.f, 0.f, 0.f);
         if (live)
@@ -438,9 +437,9 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
         if (round == 0) {
           const float4 g15 = f4(GM + 15 * kLd + c), g31 = f4(GM + 31 * kLd + c);
           const float4 ga = f4(GM + tt * kLd + c), gb = f4(GM + (32 + tt) * kLd + c);
-          const float4 ka = scale4(ld_bf16x4(Ks, tt, c), rk[tt]), qa = scale4(ld_bf16x4(Qs, tt, c), rq[tt]);
-          const float4 kb = scale4(ld_bf16x4(Ks, 32 + tt, c), rk[32 + tt]);
-          const float4 qb = scale4(ld_bf16x4(Qs, 32 + tt, c), rq[32 + tt]);
+          const float4 ka = scale4(ld_in4<F16>(Ks, tt, c), rk[tt]), qa = scale4(ld_in4<F16>(Qs, tt, c), rq[tt]);
+          const float4 kb = scale4(ld_in4<F16>(Ks, 32 + tt, c), rk[32 + tt]);
+          const float4 qb = scale4(ld_in4<F16>(Qs, 32 + tt, c), rq[32 + tt]);
           const float4 fa = exp_diff4(ga, g15), fb = exp_diff4(gb, g31);
           tc::st_tf32x4(Lt, tt, c, 128, mul4(ka, fa));
           tc::st_tf32x4(Lt, 32 + tt, c, 128, mul4(qa, fa));
@@ -451,7 +450,7 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
         } else {
           const int t = 32 + tt;
           const float4 g47 = f4(GM + 47 * kLd + c), gt = f4(GM + t * kLd + c);
-          const float4 kt = scale4(ld_bf16x4(Ks, t, c), rk[t]), qt = scale4(ld_bf16x4(Qs, t, c), rq[t]);
+          const float4 kt = scale4(ld_in4<F16>(Ks, t, c), rk[t]), qt = scale4(ld_in4<F16>(Qs, t, c), rq[t]);
           const float4 f = exp_diff4(gt, g47);
           tc::st_tf32x4(Lt, tt, c, 128, mul4(kt, f));
           tc::st_tf32x4(Lt, 32 + tt, c, 128, mul4(qt, f));
@@ -484,7 +483,7 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
             const int t = j * 8 + e;
-            x[e] = bf16_at(Ks, t, c) * rk[t] * decay_exp(gl - GM[t * kLd + c]);
+            x[e] = in_at<F16>(Ks, t, c) * rk[t] * decay_exp(gl - GM[t * kLd + c]);
           }
           st_split8(A2h, A2h + 128 * 64 * 2, tc::sw128_offset(c, j * 8, K), x);
         }
@@ -654,7 +653,7 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const int i = ch * 8 + e;
-          x[e] = bf16_at(Ks, i, c) * (bt[i] * rk[i]) * decay_exp(GM[i * kLd + c]);
+          x[e] = in_at<F16>(Ks, i, c) * (bt[i] * rk[i]) * decay_exp(GM[i * kLd + c]);
         }
         st_split8(Bh, Bl, tc::sw128_offset(c, ch * 8, 256), x);
       }
@@ -664,7 +663,7 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const int i = ch * 8 + e;
-          x[e] = bf16_at(Vs, i, c) * bt[i];
+          x[e] = in_at<F16>(Vs, i, c) * bt[i];
         }
         st_split8(Bh, Bl, tc::sw128_offset(K + c, ch * 8, 256), x);
       }
@@ -732,7 +731,7 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
             const float nq = rq[t];
 #pragma unroll
             for (int e = 0; e < 16; e += 4) {
-              const float4 qq = scale4(ld_bf16x4(Qs, t, c0 + e), nq);
+              const float4 qq = scale4(ld_in4<F16>(Qs, t, c0 + e), nq);
               const float4 gg = f4(GM + t * kLd + c0 + e);
               d[e] = qq.x * decay_exp(gg.x) - d[e];
               d[e + 1] = qq.y * decay_exp(gg.y) - d[e + 1];
@@ -809,6 +808,7 @@ __device__ __forceinline__ void issue_stage_loads(uint8_t* stage, const uint8_t*
 constexpr int kPassThreads = 512;  // 4 warps per TMEM lane quadrant
 constexpr int kColsPerThread = kVs / 4;
 
+template <bool F16>
 __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const PrefillArgs a) {
   extern __shared__ uint8_t smraw[];
   __shared__ uint64_t full_bar[2];
@@ -966,8 +966,8 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
         float x[8];
 #pragma unroll
         for (int jj = 0; jj < kColsPerThread; ++jj) x[jj] = scale * (dh[jj] + dl[jj] + oo[jj]);
-        o_pack = make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]),
-                            pack_bf16x2(x[4], x[5]), pack_bf16x2(x[6], x[7]));
+        o_pack = make_uint4(pack_out16x2<F16>(x[0], x[1]), pack_out16x2<F16>(x[2], x[3]),
+                            pack_out16x2<F16>(x[4], x[5]), pack_out16x2<F16>(x[6], x[7]));
       }
     }
     tc::fence_async_smem();
@@ -1041,9 +1041,13 @@ kda_status ensure_kernel_attributes(int* dev_out) {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KDA_ERR_CUDA;
   *dev_out = dev;
   if (g_attributes_set[dev]) return KDA_OK;
-  if (cudaFuncSetAttribute(chunk_transform_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(chunk_transform_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)kTransformTcSmem) != cudaSuccess ||
-      cudaFuncSetAttribute(state_pass_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      cudaFuncSetAttribute(chunk_transform_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)kTransformTcSmem) != cudaSuccess ||
+      cudaFuncSetAttribute(state_pass_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)kPassSmem) != cudaSuccess ||
+      cudaFuncSetAttribute(state_pass_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)kPassSmem) != cudaSuccess ||
       cudaDeviceGetAttribute(&g_num_sms[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return KDA_ERR_CUDA;
@@ -1166,6 +1170,11 @@ extern "C" kda_status kda_prefill(kda_dims dims, kda_gate gate, const kda_bf16* 
   if ((s = ensure_kernel_attributes(&dev)) != KDA_OK) return s;
   const int64_t chunks = max_chunks(num_seqs, total_tokens);
   const dim3 pass_grid(kSlices, dims.HV, num_seqs);
+  // the kernels for this call's 16-bit element type
+  void (*const transform_kernel)(PrefillArgs) =
+      dims.dtype == KDA_DTYPE_F16 ? chunk_transform_tc_kernel<true> : chunk_transform_tc_kernel<false>;
+  void (*const pass_kernel)(PrefillArgs) =
+      dims.dtype == KDA_DTYPE_F16 ? state_pass_kernel<true> : state_pass_kernel<false>;
   int nseg = 1, seq_nch = 0;
   if (total_tokens > 0 && (num_seqs == 1 || !cu_seqlens) &&
       2 * (int64_t)kSlices * dims.HV * num_seqs <= g_num_sms[dev]) {
@@ -1176,11 +1185,11 @@ extern "C" kda_status kda_prefill(kda_dims dims, kda_gate gate, const kda_bf16* 
   if (nseg <= 1) {
     if (chunks > 0) {
       args.tx_units = chunks * dims.HV;
-      chunk_transform_tc_kernel<<<transform_grid(args.tx_units, dev), kTxThreads, kTransformTcSmem, st>>>(args);
+      transform_kernel<<<transform_grid(args.tx_units, dev), kTxThreads, kTransformTcSmem, st>>>(args);
       if ((s = launch_status()) != KDA_OK) return s;
     }
     record_stage(1, st);
-    state_pass_kernel<<<pass_grid, kPassThreads, kPassSmem, st>>>(args);
+    pass_kernel<<<pass_grid, kPassThreads, kPassSmem, st>>>(args);
     s = launch_status();
   } else {
     PassStream* ps = nullptr;
@@ -1203,14 +1212,14 @@ extern "C" kda_status kda_prefill(kda_dims dims, kda_gate gate, const kda_bf16* 
       pos += want;
       sa.seq_nch = seq_nch;
       sa.tx_units = (int64_t)num_seqs * sa.seg_len * dims.HV;
-      chunk_transform_tc_kernel<<<transform_grid(sa.tx_units, dev), kTxThreads, kTransformTcSmem, st>>>(sa);
+      transform_kernel<<<transform_grid(sa.tx_units, dev), kTxThreads, kTransformTcSmem, st>>>(sa);
       if ((s = launch_status()) != KDA_OK) break;
       if (cudaEventRecord(ps->seg[i], st) != cudaSuccess ||
           cudaStreamWaitEvent(ps->stream, ps->seg[i], 0) != cudaSuccess) {
         s = KDA_ERR_CUDA;
         break;
       }
-      state_pass_kernel<<<pass_grid, kPassThreads, kPassSmem, ps->stream>>>(sa);
+      pass_kernel<<<pass_grid, kPassThreads, kPassSmem, ps->stream>>>(sa);
       s = launch_status();
     }
     record_stage(1, st);

@@ -43,7 +43,8 @@ constexpr int kRingFloats = 3 * kHeadDim + 4;
 struct StepArgs {
   GateArgs gate;
   int H, HV;
-  int G;  // value heads per q/k head (HV / H)
+  int G;      // value heads per q/k head (HV / H)
+  int dtype;  // KDA_DTYPE_BF16 or KDA_DTYPE_F16: token rows and o
   const kda_bf16* mixed_qkv;
   int64_t row_stride;
   const kda_bf16* a;
@@ -111,7 +112,7 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 template <int MODE>
 constexpr int kMinCtasPerSm = MODE == kTree ? 5 : 7;
 
-template <int MODE, int GROUPS>
+template <int MODE, int GROUPS, bool F16>
 __global__ void __launch_bounds__(128, kMinCtasPerSm<MODE>) recurrent_kernel(const StepArgs args) {
   constexpr int K = kHeadDim, V = kHeadDim;
   __shared__ __align__(16) FoldSmem fs;
@@ -243,14 +244,14 @@ __global__ void __launch_bounds__(128, kMinCtasPerSm<MODE>) recurrent_kernel(con
           if (tid == 0) fs.beta[u] = rec[3 * kHeadDim];
         }
       } else if (u < nt) {
-        const float qv = bf16_bits_to_float(raw_s[u][0][tid]);
-        const float kv = bf16_bits_to_float(raw_s[u][1][tid]);
-        const float av = bf16_bits_to_float(raw_s[u][3][tid]);
+        const float qv = in16_to_float<F16>(raw_s[u][0][tid]);
+        const float kv = in16_to_float<F16>(raw_s[u][1][tid]);
+        const float av = in16_to_float<F16>(raw_s[u][3][tid]);
         fs.q[u][tid] = qv;
         fs.k[u][tid] = kv;
-        fs.v[u][tid] = bf16_bits_to_float(raw_s[u][2][tid]);
+        fs.v[u][tid] = in16_to_float<F16>(raw_s[u][2][tid]);
         fs.dec[u][tid] = expf(gate_log_decay(ga, av, exp_alog, bias_c));
-        if (tid == 0) fs.beta[u] = fold_beta(ga, bf16_bits_to_float(raw_b[u]));
+        if (tid == 0) fs.beta[u] = fold_beta(ga, in16_to_float<F16>(raw_b[u]));
         sq[u] = qv * qv;
         sk[u] = kv * kv;
       }
@@ -338,7 +339,7 @@ __global__ void __launch_bounds__(128, kMinCtasPerSm<MODE>) recurrent_kernel(con
         }
         if (MODE == kCommitReplay) continue;  // the state is written once, after the last token
         const float out = ga.scale * group_sum8(dot16(S[gi], q));
-        if (sub == 0) args.o[(row * HV + h) * V + j] = parents_ok ? float_to_bf16_bits(out) : 0;
+        if (sub == 0) args.o[(row * HV + h) * V + j] = parents_ok ? float_to_out16<F16>(out) : 0;
         if (MODE == kChainReplay) continue;  // no snapshots
         if (MODE != kTree || parents_ok) {
           float* dst = MODE == kDecode ? root + (size_t)j * K : snap + (size_t)j * K;
@@ -404,12 +405,13 @@ kda_status launch_recurrent(const StepArgs& a, cudaStream_t stream) {
   // CTAs; larger batches use 32-row CTAs to halve the per-CTA fold work.
   const int64_t units = (int64_t)a.B * a.HV;
   record_stage(0, stream);
+  const bool f16 = a.dtype == KDA_DTYPE_F16;
   if (units * 8 <= 2 * 152) {
     dim3 grid(kHeadDim / 16, a.HV, a.B);
-    recurrent_kernel<MODE, 1><<<grid, 128, 0, stream>>>(a);
+    (f16 ? recurrent_kernel<MODE, 1, true> : recurrent_kernel<MODE, 1, false>)<<<grid, 128, 0, stream>>>(a);
   } else {
     dim3 grid(kHeadDim / 32, a.HV, a.B);
-    recurrent_kernel<MODE, 2><<<grid, 128, 0, stream>>>(a);
+    (f16 ? recurrent_kernel<MODE, 2, true> : recurrent_kernel<MODE, 2, false>)<<<grid, 128, 0, stream>>>(a);
   }
   const kda_status s = launch_status();
   record_stage(1, stream);
@@ -435,6 +437,7 @@ kda_status check_packed(const kda_dims& dims, const kda_gate& gate, const kda_bf
   out->H = dims.H;
   out->HV = dims.HV;
   out->G = dims.HV / dims.H;
+  out->dtype = dims.dtype;
   out->mixed_qkv = mixed_qkv;
   out->row_stride = row_stride;
   out->a = a;

@@ -40,8 +40,12 @@ class KdaError(RuntimeError):
         super().__init__(f"{where}: {status_string(status)} (status {status})")
 
 
+KDA_DTYPE_BF16, KDA_DTYPE_F16 = 0, 1
+
+
 class kda_dims(ctypes.Structure):
-    _fields_ = [("H", ctypes.c_int), ("HV", ctypes.c_int), ("K", ctypes.c_int), ("V", ctypes.c_int)]
+    _fields_ = [("H", ctypes.c_int), ("HV", ctypes.c_int), ("K", ctypes.c_int), ("V", ctypes.c_int),
+                ("dtype", ctypes.c_int)]
 
 
 class kda_gate(ctypes.Structure):
@@ -123,9 +127,12 @@ def _p(t):
     return ctypes.c_void_p(t.data_ptr())
 
 
-def _bf16(t, name):
-    if t is not None and t.dtype not in (torch.bfloat16, torch.int16):
-        raise TypeError(f"{name} must be bfloat16 (got {t.dtype})")
+def _in16(d, t, name):
+    """A 16-bit token tensor: bfloat16 (or float16 when d.dtype is F16); int16
+    raw bits are accepted either way."""
+    want = torch.float16 if d.dtype == KDA_DTYPE_F16 else torch.bfloat16
+    if t is not None and t.dtype not in (want, torch.int16):
+        raise TypeError(f"{name} must be {want} (got {t.dtype})")
     return _p(t)
 
 
@@ -154,8 +161,10 @@ class Gate:
                         int(bool(self.use_qk_l2norm)), float(self.scale))
 
 
-def dims(H, K=128, V=128, HV=None):
-    return kda_dims(int(H), int(HV if HV is not None else H), int(K), int(V))
+def dims(H, K=128, V=128, HV=None, dtype=KDA_DTYPE_BF16):
+    """Head counts and sizes of a call; dtype: element type of the 16-bit
+    token tensors and of o (KDA_DTYPE_BF16 or KDA_DTYPE_F16)."""
+    return kda_dims(int(H), int(HV if HV is not None else H), int(K), int(V), int(dtype))
 
 
 def kda_prefill_workspace_size(d: kda_dims, num_seqs: int, total_tokens: int) -> int:
@@ -173,9 +182,9 @@ def kda_prefill(d, gate: Gate, q, k, v, g, beta, state_pool, state_idx, cu_seqle
         need = kda_prefill_workspace_size(d, num_seqs, T)
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
     st = load().kda_prefill(
-        d, gate.c(), _bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v"), _bf16(g, "g"), _bf16(beta, "beta"),
+        d, gate.c(), _in16(d, q, "q"), _in16(d, k, "k"), _in16(d, v, "v"), _in16(d, g, "g"), _in16(d, beta, "beta"),
         int(gb_rows), _p(state_pool), int(state_pool.shape[0]), _p(state_idx), _p(cu_seqlens),
-        int(num_seqs), int(T), _bf16(o, "o"), _p(intermediate), _p(workspace),
+        int(num_seqs), int(T), _in16(d, o, "o"), _p(intermediate), _p(workspace),
         int(workspace.numel() * workspace.element_size()), _p(err_flag), _stream(stream))
     _check(st, "kda_prefill")
 
@@ -185,9 +194,9 @@ def kda_prefill_noalloc(d, gate: Gate, q, k, v, g, beta, state_pool, state_idx, 
     """kda_prefill with the library's built-in static scratch (see kda.h): for
     callers that cannot allocate device memory."""
     st = load().kda_prefill_noalloc(
-        d, gate.c(), _bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v"), _bf16(g, "g"), _bf16(beta, "beta"),
+        d, gate.c(), _in16(d, q, "q"), _in16(d, k, "k"), _in16(d, v, "v"), _in16(d, g, "g"), _in16(d, beta, "beta"),
         int(g.shape[0]), _p(state_pool), int(state_pool.shape[0]), _p(state_idx), _p(cu_seqlens),
-        int(num_seqs), int(q.shape[0]), _bf16(o, "o"), _p(intermediate), _p(err_flag),
+        int(num_seqs), int(q.shape[0]), _in16(d, o, "o"), _p(intermediate), _p(err_flag),
         _stream(stream))
     _check(st, "kda_prefill_noalloc")
 
@@ -195,27 +204,27 @@ def kda_prefill_noalloc(d, gate: Gate, q, k, v, g, beta, state_pool, state_idx, 
 def kda_decode_packed(d, gate: Gate, mixed_qkv, a, b, state_pool, state_idx, o, err_flag=None,
                       stream=None):
     st = load().kda_decode_packed(
-        d, gate.c(), _bf16(mixed_qkv, "mixed_qkv"), int(mixed_qkv.stride(0)), _bf16(a, "a"),
-        _bf16(b, "b"), int(mixed_qkv.shape[0]), _p(state_pool), int(state_pool.shape[0]),
-        _p(state_idx), _bf16(o, "o"), _p(err_flag), _stream(stream))
+        d, gate.c(), _in16(d, mixed_qkv, "mixed_qkv"), int(mixed_qkv.stride(0)), _in16(d, a, "a"),
+        _in16(d, b, "b"), int(mixed_qkv.shape[0]), _p(state_pool), int(state_pool.shape[0]),
+        _p(state_idx), _in16(d, o, "o"), _p(err_flag), _stream(stream))
     _check(st, "kda_decode_packed")
 
 
 def kda_verify_chain(d, gate: Gate, mixed_qkv, a, b, B, T, state_pool, state_idx, o, snapshots,
                      err_flag=None, stream=None):
     st = load().kda_verify_chain(
-        d, gate.c(), _bf16(mixed_qkv, "mixed_qkv"), int(mixed_qkv.stride(0)), _bf16(a, "a"),
-        _bf16(b, "b"), int(B), int(T), _p(state_pool), int(state_pool.shape[0]), _p(state_idx),
-        _bf16(o, "o"), _p(snapshots), _p(err_flag), _stream(stream))
+        d, gate.c(), _in16(d, mixed_qkv, "mixed_qkv"), int(mixed_qkv.stride(0)), _in16(d, a, "a"),
+        _in16(d, b, "b"), int(B), int(T), _p(state_pool), int(state_pool.shape[0]), _p(state_idx),
+        _in16(d, o, "o"), _p(snapshots), _p(err_flag), _stream(stream))
     _check(st, "kda_verify_chain")
 
 
 def kda_verify_tree(d, gate: Gate, mixed_qkv, a, b, B, T, parent_idx, state_pool, state_idx, o,
                     snapshots, err_flag=None, stream=None):
     st = load().kda_verify_tree(
-        d, gate.c(), _bf16(mixed_qkv, "mixed_qkv"), int(mixed_qkv.stride(0)), _bf16(a, "a"),
-        _bf16(b, "b"), int(B), int(T), _p(parent_idx), _p(state_pool), int(state_pool.shape[0]),
-        _p(state_idx), _bf16(o, "o"), _p(snapshots), _p(err_flag), _stream(stream))
+        d, gate.c(), _in16(d, mixed_qkv, "mixed_qkv"), int(mixed_qkv.stride(0)), _in16(d, a, "a"),
+        _in16(d, b, "b"), int(B), int(T), _p(parent_idx), _p(state_pool), int(state_pool.shape[0]),
+        _p(state_idx), _in16(d, o, "o"), _p(snapshots), _p(err_flag), _stream(stream))
     _check(st, "kda_verify_tree")
 
 
@@ -234,9 +243,9 @@ def kda_verify_chain_replay(d, gate: Gate, mixed_qkv, a, b, B, T, state_pool, st
     """Chain verify without snapshots: o as kda_verify_chain, each token's
     folded inputs recorded in `ring` (kda_replay_ring_bytes bytes, FP32)."""
     st = load().kda_verify_chain_replay(
-        d, gate.c(), _bf16(mixed_qkv, "mixed_qkv"), int(mixed_qkv.stride(0)), _bf16(a, "a"),
-        _bf16(b, "b"), int(B), int(T), _p(state_pool), int(state_pool.shape[0]), _p(state_idx),
-        _bf16(o, "o"), _p(ring), _p(err_flag), _stream(stream))
+        d, gate.c(), _in16(d, mixed_qkv, "mixed_qkv"), int(mixed_qkv.stride(0)), _in16(d, a, "a"),
+        _in16(d, b, "b"), int(B), int(T), _p(state_pool), int(state_pool.shape[0]), _p(state_idx),
+        _in16(d, o, "o"), _p(ring), _p(err_flag), _stream(stream))
     _check(st, "kda_verify_chain_replay")
 
 

@@ -19,6 +19,14 @@ def dev_bf16(x):
     return torch.from_numpy(np.ascontiguousarray(x, dtype=np.int16)).cuda().view(torch.bfloat16)
 
 
+def dev_in(x):
+    """16-bit token array -> device tensor: int16 BF16 bits as bfloat16,
+    float16 as float16."""
+    x = np.ascontiguousarray(x)
+    t = torch.from_numpy(x).cuda()
+    return t.view(torch.bfloat16) if x.dtype == np.int16 else t
+
+
 def dev(x, dtype=None):
     t = torch.from_numpy(np.ascontiguousarray(x))
     if dtype is not None:

@@ -75,6 +75,8 @@ def test_prefill_host_errors(lib):
     # value heads come in whole groups per q/k head (HV a multiple of H)
     assert _prefill(lib, dims=kda.dims(4, HV=6)) == kda.KDA_ERR_UNSUPPORTED
     assert _prefill(lib, dims=kda.dims(4, HV=2)) == kda.KDA_ERR_UNSUPPORTED
+    # token tensors are BF16 or FP16
+    assert _prefill(lib, dims=kda.dims(4, dtype=2)) == kda.KDA_ERR_UNSUPPORTED
     # bounded gate formula only
     assert _prefill(lib, gate=_gate(A_log=DUMMY, lb=math.nan)) == kda.KDA_ERR_UNSUPPORTED
     # the chunk form's decay windows need per-token log-decays >= -5.5

@@ -511,3 +511,17 @@ def test_head_counts_must_group():
     with pytest.raises(ko.OracleError):
         ko.prefill(_group_gate(2, 3, d["A_log"], d["dt_bias"]), d["q"], d["k"], d["v"], d["g"], d["beta"],
                    d["pool"].astype(np.float64), d["state_idx"], d["cu_seqlens"])
+
+
+def test_fp16_token_inputs_widen_exactly():
+    """The second token precision, FP16: values that FP16 holds exactly come
+    back unchanged from the seeded encoder and the oracle's widening, and
+    others round to nearest even (IEEE binary16: 10 fraction bits)."""
+    exact = np.array([0.0, 1.0, -2.5, 1.0 + 2.0 ** -10, 65504.0, 2.0 ** -14, 6.103515625e-05,
+                      -3.0517578125e-05], np.float32)
+    f16 = inputs.encode16(exact, "f16")
+    assert f16.dtype == np.float16
+    assert np.array_equal(ko.bf16_to_f32(f16), exact)
+    # halfway between 1 and 1 + 2^-10 rounds to the even neighbour 1; just above it rounds up
+    assert ko.bf16_to_f32(inputs.encode16(np.float32([1.0 + 2.0 ** -11]), "f16"))[0] == 1.0
+    assert ko.bf16_to_f32(inputs.encode16(np.float32([1.0 + 3 * 2.0 ** -12]), "f16"))[0] == 1.0 + 2.0 ** -10
