@@ -47,6 +47,7 @@ H, K = 16, 128
 CHUNK = 64
 METRIC = "KDA prefill tok/s @16h×128; decode/verify µs/layer; % HBM/TC roofline"
 PREFILL_T = 4096
+LONG_T, LONG_CALLS = 32768, 8  # one long sequence, in one call or continued over 8 calls
 DECODE_B = 48
 VERIFY_B, VERIFY_T = 16, 6
 COMMIT_B = VERIFY_B
@@ -238,6 +239,18 @@ def run_ours(args, rank, world, local_rank):
     p_o = torch.empty((PREFILL_T, H, K), dtype=torch.bfloat16, device=dev)
     ws = torch.empty(kda.kda_prefill_workspace_size(D, 1, PREFILL_T), dtype=torch.uint8, device=dev)
 
+    # The 1 x 4096 call again with the state at the start of every chunk
+    # written out, and one 32768-token sequence prefilled by one call or by 8
+    # calls of 4096 tokens that continue its state through the pool slot.
+    p_inter = torch.empty((PREFILL_T // CHUNK, H, K, K), device=dev)
+    lg = inputs.prefill_inputs(seed=50 + rank, lengths=[LONG_T], H=H, slots=2, state_idx=[1])
+    LG = {n: bf(lg[n]) for n in ("q", "k", "v", "g", "beta")}
+    lg_pool, lg_idx = t(lg["pool"]), t(lg["state_idx"])
+    lg_cu = {T_: t(np.array([0, T_], np.int32)) for T_ in (LONG_T, LONG_T // LONG_CALLS)}
+    lg_o = torch.empty((LONG_T, H, K), dtype=torch.bfloat16, device=dev)
+    lg_ws = torch.empty(kda.kda_prefill_workspace_size(D, 1, LONG_T), dtype=torch.uint8, device=dev)
+    del lg
+
     # Decode, verify and commit run args.layers calls back to back, each on its own
     # copy of the state pool, inputs and outputs (as consecutive KDA layers of
     # one model do), so every call starts from data no earlier call touched.
@@ -271,7 +284,8 @@ def run_ours(args, rank, world, local_rank):
         flush.zero_()
         flush.view(torch.int64).sum()
 
-    phases = ["prefill", "decode", "verify_chain", "verify_tree", "commit", "verify_replay", "commit_replay"]
+    phases = ["prefill", "decode", "verify_chain", "verify_tree", "commit", "verify_replay", "commit_replay",
+              "prefill_states", "prefill_long", "prefill_long_calls"]
     # The prefill's state pass of segment s overlaps the transform of segment
     # s+1, so its stage events give the span of the transform launches (ev0 ->
     # ev1, earlier segments' passes running alongside) and the exposed tail of
@@ -297,11 +311,24 @@ def run_ours(args, rank, world, local_rank):
                                         VERIFY_T, x["v_pool_r"], x["v_idx"], x["v_o"], x["ring"])
         elif name == "commit_replay":
             kda.kda_commit_replay(D, x["ring"], COMMIT_B, VERIFY_T, x["accepted"], x["v_pool_r"], x["v_idx"])
+        elif name == "prefill_states":
+            kda.kda_prefill(D, gate, P["q"], P["k"], P["v"], P["g"], P["beta"], p_pool, p_idx, p_cu, 1,
+                            p_o, p_inter, workspace=ws)
+        elif name == "prefill_long":
+            kda.kda_prefill(D, gate, *(LG[n] for n in ("q", "k", "v", "g", "beta")), lg_pool, lg_idx,
+                            lg_cu[LONG_T], 1, lg_o, workspace=lg_ws)
+        elif name == "prefill_long_calls":  # call x of 8, continuing the state
+            n_ = LONG_T // LONG_CALLS
+            part = slice(x * n_, (x + 1) * n_)
+            kda.kda_prefill(D, gate, *(LG[n][part] for n in ("q", "k", "v", "g", "beta")), lg_pool, lg_idx,
+                            lg_cu[n_], 1, lg_o[part], workspace=lg_ws)
         elif name == "commit":
             kda.kda_commit(D, x["v_snap"], COMMIT_B, VERIFY_T, x["accepted"], x["v_pool"], x["v_idx"])
 
     def calls(name):
-        return [None] if name == "prefill" else L
+        if name == "prefill_long_calls":
+            return list(range(LONG_CALLS))
+        return [None] if name.startswith("prefill") else L
 
     def run_phase(name, ev=None):
         """One phase; with events, ev[0] is recorded right before the first
@@ -378,8 +405,10 @@ def run_ours(args, rank, world, local_rank):
     wall = time.perf_counter() - wall0
     clocks = sampler.stop() if sampler else None
 
-    # per-call milliseconds of every phase (a layer phase's span / args.layers)
-    ph_ms = {n: [r[n][0].elapsed_time(r[n][2]) / len(calls(n)) for r in records] for n in phases}
+    # per-call milliseconds of every phase (a layer phase's span / args.layers;
+    # a prefill phase's whole span, however many calls it makes)
+    ph_ms = {n: [r[n][0].elapsed_time(r[n][2]) / (1 if n.startswith("prefill") else len(calls(n)))
+                 for r in records] for n in phases}
     k_ms = {
         "prefill_transform": [r["prefill"][0].elapsed_time(r["prefill"][1]) for r in records],
         "prefill_pass_tail": [r["prefill"][1].elapsed_time(r["prefill"][2]) for r in records],
@@ -389,6 +418,9 @@ def run_ours(args, rank, world, local_rank):
     }
     tot = {n: sum(v) for n, v in ph_ms.items()}
     tot = dict(zip(phases, max_over_ranks([tot[n] for n in phases], world, dev)))
+    # a step is one pass over the hot path's phases; the chunk-state and long
+    # prefills are reported on their own and kept out of ms_per_step
+    core = [n for n in phases if n not in ("prefill_states", "prefill_long", "prefill_long_calls")]
 
     # ---- e2e: prefill through the C ABI with host buffers ----
     host = {n: torch.from_numpy(np.ascontiguousarray(pf[n])).pin_memory()
@@ -424,9 +456,14 @@ def run_ours(args, rank, world, local_rank):
     # transform and a state-pass launch each) when 8 * heads fits in the SM
     # count; same rule here, to count the launches.
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    seq_nch = (PREFILL_T + CHUNK - 1) // CHUNK
-    nseg = min(4, seq_nch // 16) if seq_nch >= 32 and 8 * H <= sms else 1
-    prefill_launches = 2 * max(nseg, 1)
+    def launches_of(T_):
+        seq_nch = (T_ + CHUNK - 1) // CHUNK
+        nseg = min(4, seq_nch // 16) if seq_nch >= 32 and 8 * H <= sms else 1
+        return 2 * max(nseg, 1)
+
+    prefill_launches = launches_of(PREFILL_T)
+    extra_launches = (prefill_launches + launches_of(LONG_T) +
+                      LONG_CALLS * launches_of(LONG_T // LONG_CALLS))
     steps = args.steps
     prefill_s = tot["prefill"] / 1e3
     value = replica_throughput(PREFILL_T, steps, world, prefill_s)
@@ -476,11 +513,21 @@ def run_ours(args, rank, world, local_rank):
         "verify_replay_b16x6": {"us": round(statistics.mean(ph_ms["verify_replay"]) * 1e3, 2)},
         "commit_replay_b16": {"us": round(statistics.mean(ph_ms["commit_replay"]) * 1e3, 2)},
         "kernels": kern,
+        # chunk-start states out, and a long sequence in one call or continued
+        # over several calls through its pool slot
+        "prefill_1x4096_chunk_states": {
+            "us": round(statistics.mean(ph_ms["prefill_states"]) * 1e3, 2),
+            "states_bytes": PREFILL_T // CHUNK * H * K * K * 4},
+        "prefill_1x32768": {"us": round(statistics.mean(ph_ms["prefill_long"]) * 1e3, 2),
+                            "tok_s": round(LONG_T / statistics.mean(ph_ms["prefill_long"]) * 1e3, 1)},
+        "prefill_32768_as_8x4096": {
+            "us": round(statistics.mean(ph_ms["prefill_long_calls"]) * 1e3, 2),
+            "tok_s": round(LONG_T / statistics.mean(ph_ms["prefill_long_calls"]) * 1e3, 1)},
     }
     out = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
         "steps": steps, "warmup": args.warmup,
-        "ms_per_step": round(sum(tot.values()) / steps, 4), "higher_is_better": True,
+        "ms_per_step": round(sum(tot[n] for n in core) / steps, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16 in / fp32 state",
         "data": "synthetic (seeded; q,k,v,a,beta ~N(0,1) BF16, A_log~U(-1,1), dt_bias~N(0,0.1), state~N(0,0.02))",
         "config": {"workload": "KDA prefill 1x4096 tokens, 16 heads x 128 (+ decode B=48, verify 16x6 chain/tree/replay, commit 16 snapshot/replay)",
@@ -489,7 +536,7 @@ def run_ours(args, rank, world, local_rank):
                               f"buffers, time per call = span / {args.layers}"),
                    "global_batch": world, "seq_len": PREFILL_T, "heads": H, "head_dim": K,
                    "parallelism": f"replicas x{world}", "l2": "flushed before every phase (512 MiB write, then the same buffer read back); layer calls touch disjoint buffers larger than L2"},
-        "gpu_launches": steps * (prefill_launches + (len(phases) - 1) * args.layers),
+        "gpu_launches": steps * (prefill_launches + (len(core) - 1) * args.layers + extra_launches),
         "phases": phase_out,
         "roofline": roofline,
         "e2e": {"value": round(replica_throughput(PREFILL_T, e2e_steps, world, e2e_ms / 1e3), 1),
