@@ -58,7 +58,8 @@ LAYERS = 8  # default decode/verify/commit calls per timed replay (--layers)
 # keyed by kernel; valid only while the kernel sources hash to the recorded value.
 NCU_TRAFFIC = {
     # the four segment launches of one 1x4096 prefill call, 16 heads: read
-    # 67,632,896 B + write 22,272 B (profiles/chunk_transform_1x4096_h16.md)
+    # 67,632,896 B + write 22,272 B (profiles/chunk_transform_1x4096_h16.md);
+    # refreshed whenever the kernel sources change
     "prefill_transform": {"bytes": 67655168, "src": "8b1b19b50a3cd8f6"},
 }
 
@@ -94,6 +95,11 @@ def transform_flops(T):
     # A, P, W, Util (C^2 K each, triangular) and the inverse (C^3 / 3) per chunk-head
     n = (T + CHUNK - 1) // CHUNK * H
     return n * (4 * CHUNK * CHUNK * K + CHUNK ** 3 / 3)
+
+
+def transform_bytes(T):
+    # the chunk transform's inputs: q, k, v, gate input a (BF16, T x H x 128 each) and beta
+    return 4 * T * H * K * 2 + T * H * 2
 
 
 def token_io_bytes():
@@ -243,13 +249,14 @@ def run_ours(args, rank, world, local_rank):
     # written out, and one 32768-token sequence prefilled by one call or by 8
     # calls of 4096 tokens that continue its state through the pool slot.
     p_inter = torch.empty((PREFILL_T // CHUNK, H, K, K), device=dev)
-    lg = inputs.prefill_inputs(seed=50 + rank, lengths=[LONG_T], H=H, slots=2, state_idx=[1])
-    LG = {n: bf(lg[n]) for n in ("q", "k", "v", "g", "beta")}
-    lg_pool, lg_idx = t(lg["pool"]), t(lg["state_idx"])
-    lg_cu = {T_: t(np.array([0, T_], np.int32)) for T_ in (LONG_T, LONG_T // LONG_CALLS)}
-    lg_o = torch.empty((LONG_T, H, K), dtype=torch.bfloat16, device=dev)
-    lg_ws = torch.empty(kda.kda_prefill_workspace_size(D, 1, LONG_T), dtype=torch.uint8, device=dev)
-    del lg
+    if not args.no_long:
+        lg = inputs.prefill_inputs(seed=50 + rank, lengths=[LONG_T], H=H, slots=2, state_idx=[1])
+        LG = {n: bf(lg[n]) for n in ("q", "k", "v", "g", "beta")}
+        lg_pool, lg_idx = t(lg["pool"]), t(lg["state_idx"])
+        lg_cu = {T_: t(np.array([0, T_], np.int32)) for T_ in (LONG_T, LONG_T // LONG_CALLS)}
+        lg_o = torch.empty((LONG_T, H, K), dtype=torch.bfloat16, device=dev)
+        lg_ws = torch.empty(kda.kda_prefill_workspace_size(D, 1, LONG_T), dtype=torch.uint8, device=dev)
+        del lg
 
     # Decode, verify and commit run args.layers calls back to back, each on its own
     # copy of the state pool, inputs and outputs (as consecutive KDA layers of
@@ -285,7 +292,7 @@ def run_ours(args, rank, world, local_rank):
         flush.view(torch.int64).sum()
 
     phases = ["prefill", "decode", "verify_chain", "verify_tree", "commit", "verify_replay", "commit_replay",
-              "prefill_states", "prefill_long", "prefill_long_calls"]
+              "prefill_states"] + ([] if args.no_long else ["prefill_long", "prefill_long_calls"])
     # The prefill's state pass of segment s overlaps the transform of segment
     # s+1, so its stage events give the span of the transform launches (ev0 ->
     # ev1, earlier segments' passes running alongside) and the exposed tail of
@@ -462,19 +469,20 @@ def run_ours(args, rank, world, local_rank):
         return 2 * max(nseg, 1)
 
     prefill_launches = launches_of(PREFILL_T)
-    extra_launches = (prefill_launches + launches_of(LONG_T) +
-                      LONG_CALLS * launches_of(LONG_T // LONG_CALLS))
+    extra_launches = prefill_launches + (0 if args.no_long else
+                                         launches_of(LONG_T) + LONG_CALLS * launches_of(LONG_T // LONG_CALLS))
     steps = args.steps
     prefill_s = tot["prefill"] / 1e3
     value = replica_throughput(PREFILL_T, steps, world, prefill_s)
     mean_k = {n: statistics.mean(v) for n, v in k_ms.items()}
-    # The chunk transform runs its contractions on tcgen05 (TF32 and BF16
-    # operands, FP32 accumulation): judged against the measured dense BF16
-    # peak (the higher one), with algorithmic flops only (hi/lo split passes
-    # not counted), over the span of its launches.  The exposed pass tail has
-    # no roofline of its own.
+    # The chunk transform's slower roofline is HBM: its input bytes at the
+    # measured copy bandwidth (9.9 us at 1 x 4096) take far longer than its
+    # algorithmic flops (2.2 GFLOP, hi/lo split passes not counted) at the
+    # dense BF16 peak (1.2 us).  It is judged on those bytes over the span of
+    # its launches; its flop rate is reported beside.  The exposed pass tail
+    # has no roofline of its own.
     work = {
-        "prefill_transform": ("tensor", transform_flops(PREFILL_T) / 1e12, bf16_tf, "TFLOP/s"),
+        "prefill_transform": ("hbm", transform_bytes(PREFILL_T) / 1e9, hbm, "GB/s"),
         "prefill_pass_tail": None,
         "decode": ("hbm", decode_bytes(DECODE_B) / 1e9, hbm, "GB/s"),
         "verify_chain": ("hbm", verify_bytes(VERIFY_B, VERIFY_T) / 1e9, hbm, "GB/s"),
@@ -490,6 +498,8 @@ def run_ours(args, rank, world, local_rank):
     tr = NCU_TRAFFIC.get(dom)
     traffic = tr["bytes"] if tr and tr.get("src") == src else None
     roofline = {"kernel": dom, "bound": bound, "achieved": round(achieved, 3), "peak": peak,
+                "tensor_tflops": round(transform_flops(PREFILL_T) / 1e12 / (mean_k["prefill_transform"] / 1e3), 3),
+                "tensor_frac": round(transform_flops(PREFILL_T) / 1e12 / (mean_k["prefill_transform"] / 1e3) / bf16_tf, 5),
                 "unit": unit, "frac": round(achieved / peak, 4), "traffic": traffic,
                 "peak_source": f"{peak_kind} ({'dense BF16 burst' if bound == 'tensor' else 'HBM copy'})"}
     kern = {}
@@ -518,12 +528,13 @@ def run_ours(args, rank, world, local_rank):
         "prefill_1x4096_chunk_states": {
             "us": round(statistics.mean(ph_ms["prefill_states"]) * 1e3, 2),
             "states_bytes": PREFILL_T // CHUNK * H * K * K * 4},
-        "prefill_1x32768": {"us": round(statistics.mean(ph_ms["prefill_long"]) * 1e3, 2),
-                            "tok_s": round(LONG_T / statistics.mean(ph_ms["prefill_long"]) * 1e3, 1)},
-        "prefill_32768_as_8x4096": {
-            "us": round(statistics.mean(ph_ms["prefill_long_calls"]) * 1e3, 2),
-            "tok_s": round(LONG_T / statistics.mean(ph_ms["prefill_long_calls"]) * 1e3, 1)},
     }
+    if not args.no_long:
+        phase_out["prefill_1x32768"] = {"us": round(statistics.mean(ph_ms["prefill_long"]) * 1e3, 2),
+                                        "tok_s": round(LONG_T / statistics.mean(ph_ms["prefill_long"]) * 1e3, 1)}
+        phase_out["prefill_32768_as_8x4096"] = {
+            "us": round(statistics.mean(ph_ms["prefill_long_calls"]) * 1e3, 2),
+            "tok_s": round(LONG_T / statistics.mean(ph_ms["prefill_long_calls"]) * 1e3, 1)}
     out = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
         "steps": steps, "warmup": args.warmup,
@@ -620,6 +631,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=LAYERS,
                     help="decode/verify/commit calls per timed replay, each on its own buffers")
+    ap.add_argument("--no-long", action="store_true",
+                    help="skip the 32768-token prefill phases (about 1.4 GB less device memory, e.g. under ncu)")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", args.gpus if "RANK" in os.environ else 1))
