@@ -58,9 +58,9 @@ LAYERS = 8  # default decode/verify/commit calls per timed replay (--layers)
 # keyed by kernel; valid only while the kernel sources hash to the recorded value.
 NCU_TRAFFIC = {
     # the four segment launches of one 1x4096 prefill call, 16 heads: read
-    # 67,639,808 B + write 11,264 B (profiles/chunk_transform_1x4096_h16.md);
+    # 67,638,016 B + write 12,800 B (profiles/chunk_transform_1x4096_h16.md);
     # refreshed whenever the kernel sources change
-    "prefill_transform": {"bytes": 67651072, "src": "c0f34f49e508e456"},
+    "prefill_transform": {"bytes": 67650816, "src": "30cbda600e28f256"},
 }
 
 

@@ -119,7 +119,6 @@ __global__ void __launch_bounds__(128, kMinCtasPerSm<MODE>) recurrent_kernel(con
   __shared__ int tree_par[kTokBlock];  // tree: the parents of the first kTokBlock nodes
   // raw BF16 token rows of this head: q, k, v, gate input, per token of the block
   __shared__ __align__(16) uint16_t raw_s[kTokBlock][4][kHeadDim];
-  __shared__ uint16_t raw_b[kTokBlock];
   const int r = blockIdx.z, h = blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int sub = lane & 7;
@@ -164,6 +163,7 @@ __global__ void __launch_bounds__(128, kMinCtasPerSm<MODE>) recurrent_kernel(con
                                  : raw_m == 1 ? (args.H + h / args.G) * kHeadDim
                                  : raw_m == 2 ? (2 * args.H + h) * kHeadDim
                                               : h * kHeadDim);
+  uint16_t b_raw = 0;  // thread u < nt: raw beta of token u of the block
   auto request_raw = [&](int tb, int nt) {
     for (int u = tid >> 6; u < nt; u += 2) {
       const int64_t row = MODE == kDecode ? r : (int64_t)r * T + tb + u;
@@ -172,12 +172,22 @@ __global__ void __launch_bounds__(128, kMinCtasPerSm<MODE>) recurrent_kernel(con
       cp_async16(&raw_s[u][raw_m][raw_piece], x + raw_off);
     }
     cp_async_commit();
-    if (tid < nt) {
+    if (tid < nt) {  // kept in a register: its latency overlaps the slot lookup and state load
       const int64_t row = MODE == kDecode ? r : (int64_t)r * T + tb + tid;
-      raw_b[tid] = args.b[row * args.HV + h];
+      b_raw = args.b[row * args.HV + h];
     }
   };
   if (MODE != kCommitReplay) request_raw(0, T < kTokBlock ? T : kTokBlock);
+  // Gate parameters: loaded before the slot lookup so that their latency
+  // overlaps it, except in ReplaySSM verify, where the longer live range
+  // spills at its register budget.  exp(A_log) is taken after the state load.
+  constexpr bool kEarlyGate = MODE != kChainReplay;
+  const GateArgs& ga = args.gate;
+  float alog_early = 0.f, bias_early = 0.f;
+  if constexpr (kEarlyGate) {
+    alog_early = ga.A_log ? ga.A_log[h] : 0.f;
+    bias_early = ga.dt_bias ? ga.dt_bias[h * K + tid] : 0.f;
+  }
 
   const int slot = args.state_idx[r];
   const bool ok = slot >= -1 && slot < args.pool_slots;
@@ -218,9 +228,8 @@ __global__ void __launch_bounds__(128, kMinCtasPerSm<MODE>) recurrent_kernel(con
       S[gi][i] = *reinterpret_cast<const float4*>(root + (size_t)(row0 + gi * 4) * K + i * 32 +
                                                   lane_col);
 
-  const GateArgs& ga = args.gate;
-  const float exp_alog = ga.A_log ? expf(ga.A_log[h]) : 0.f;
-  const float bias_c = ga.dt_bias ? ga.dt_bias[h * K + tid] : 0.f;
+  const float exp_alog = ga.A_log ? __expf(kEarlyGate ? alog_early : ga.A_log[h]) : 0.f;
+  const float bias_c = kEarlyGate ? bias_early : (ga.dt_bias ? ga.dt_bias[h * K + tid] : 0.f);
 
   for (int tb = 0; tb < T; tb += kTokBlock) {
     const int nt = T - tb < kTokBlock ? T - tb : kTokBlock;
@@ -250,12 +259,12 @@ __global__ void __launch_bounds__(128, kMinCtasPerSm<MODE>) recurrent_kernel(con
         fs.q[u][tid] = qv;
         fs.k[u][tid] = kv;
         fs.v[u][tid] = in16_to_float<F16>(raw_s[u][2][tid]);
-        fs.dec[u][tid] = expf(gate_log_decay(ga, av, exp_alog, bias_c));
-        if (tid == 0) fs.beta[u] = fold_beta(ga, in16_to_float<F16>(raw_b[u]));
+        fs.dec[u][tid] = decay_exp(gate_log_decay(ga, av, exp_alog, bias_c));
         sq[u] = qv * qv;
         sk[u] = kv * kv;
       }
     }
+    if (MODE != kCommitReplay && tid < nt) fs.beta[tid] = fold_beta(ga, in16_to_float<F16>(b_raw));
     if (MODE != kCommitReplay && ga.use_qk_l2norm) {
 #pragma unroll
       for (int u = 0; u < kTokBlock; ++u) {
