@@ -68,6 +68,18 @@ def test_replay_verify_and_commit_equal_the_snapshot_path(B):
             assert torch.equal(pool_r[slot], dev(d["pool"])[slot])
 
 
+def test_replay_longer_than_one_token_block():
+    """T = 11 spans two 8-token blocks in the verify and, for the accepted
+    indices 8 and 10, in the commit's replay."""
+    B, T = 5, 11
+    d = inputs.verify_inputs(seed=330, B=B, T=T, H=H, slots=12)
+    og, gg = gates(d, H=H)
+    o_s, o_r, _, pool_s, pool_r, err = _both_paths(d, B, T, gg, [10, 8, 3, -1, 7])
+    assert err == [0, 0]
+    assert torch.equal(o_s, o_r)
+    assert torch.equal(pool_s, pool_r)
+
+
 def test_replay_commit_flags_bad_accepted_and_skips_padding():
     B, T = 3, 6
     d = inputs.verify_inputs(seed=310, B=B, T=T, H=H, slots=8)
