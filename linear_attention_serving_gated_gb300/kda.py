@@ -136,6 +136,36 @@ def _in16(d, t, name):
     return _p(t)
 
 
+def _at_least(t, n, name, shape):
+    """t must hold n elements (the rows the kernels touch), t None allowed."""
+    if t is not None and t.numel() < n:
+        raise ValueError(f"{name} must hold {shape} = {n} elements (got shape {tuple(t.shape)})")
+
+
+def _packed_shapes(d, mixed_qkv, a, b, state_pool, state_idx, rows, reqs):
+    """Shape rules of a packed-row call, checked on the host because the
+    library sees only pointers.  As the pages' packed-decode validator does
+    ("PR #35197 report: fix(kernel) Fix Helion small-token prefill bug",
+    kda_decode.py snippet), HV, V and K come from the state's trailing
+    dimensions and the gate input `a` must be [rows, HV*K]; every row the
+    kernels read (rows = requests x tokens) must exist."""
+    if state_pool.dim() < 3 or tuple(state_pool.shape[-3:]) != (d.HV, d.V, d.K):
+        raise ValueError(f"state_pool must end in [HV, V, K] = [{d.HV}, {d.V}, {d.K}] "
+                         f"(got {tuple(state_pool.shape)})")
+    width = 2 * d.H * d.K + d.HV * d.V
+    if mixed_qkv.dim() != 2 or mixed_qkv.shape[0] < rows or mixed_qkv.shape[1] < width \
+            or mixed_qkv.stride(1) != 1:
+        raise ValueError(f"mixed_qkv must be [>= {rows}, >= {width}] with unit column stride "
+                         f"(got {tuple(mixed_qkv.shape)})")
+    if a.shape[-1] != d.HV * d.K or a.numel() < rows * d.HV * d.K or not a.is_contiguous():
+        raise ValueError(f"`a` must have shape [B, HV*K] = [{rows}, {d.HV * d.K}], contiguous "
+                         f"(got {tuple(a.shape)})")
+    if b.numel() < rows * d.HV or not b.is_contiguous():
+        raise ValueError(f"`b` must have shape [B, HV] = [{rows}, {d.HV}], contiguous "
+                         f"(got {tuple(b.shape)})")
+    _at_least(state_idx, reqs, "state_idx", f"[{reqs}]")
+
+
 def _stream(stream):
     s = stream if stream is not None else torch.cuda.current_stream()
     return ctypes.c_void_p(s.cuda_stream)
@@ -171,6 +201,23 @@ def kda_prefill_workspace_size(d: kda_dims, num_seqs: int, total_tokens: int) ->
     return int(load().kda_prefill_workspace_size(d, int(num_seqs), int(total_tokens)))
 
 
+def _prefill_shapes(d, q, k, v, g, beta, state_pool, state_idx, cu_seqlens, num_seqs, o):
+    """Every element the prefill kernels touch for T = q.shape[0] tokens and
+    gb_rows = g.shape[0] gate rows must exist (the library sees pointers)."""
+    T, gb_rows, n = q.shape[0], g.shape[0], int(num_seqs)
+    if state_pool.dim() < 3 or tuple(state_pool.shape[-3:]) != (d.HV, d.V, d.K):
+        raise ValueError(f"state_pool must end in [HV, V, K] = [{d.HV}, {d.V}, {d.K}] "
+                         f"(got {tuple(state_pool.shape)})")
+    _at_least(q, T * d.H * d.K, "q", f"[{T}, H, K]")
+    _at_least(k, T * d.H * d.K, "k", f"[{T}, H, K]")
+    _at_least(v, T * d.HV * d.V, "v", f"[{T}, HV, V]")
+    _at_least(g, gb_rows * d.HV * d.K, "g", f"[{gb_rows}, HV, K]")
+    _at_least(beta, gb_rows * d.HV, "beta", f"[{gb_rows}, HV]")
+    _at_least(o, T * d.HV * d.V, "o", f"[{T}, HV, V]")
+    _at_least(state_idx, n, "state_idx", f"[{n}]")
+    _at_least(cu_seqlens, n + 1, "cu_seqlens", f"[{n + 1}]")
+
+
 def kda_prefill(d, gate: Gate, q, k, v, g, beta, state_pool, state_idx, cu_seqlens, num_seqs,
                 o, intermediate=None, workspace=None, err_flag=None, stream=None):
     """Chunked varlen prefill (see kda.h).  q,k [T,H,K], v [T,HV,V], g
@@ -178,6 +225,7 @@ def kda_prefill(d, gate: Gate, q, k, v, g, beta, state_pool, state_idx, cu_seqle
     (in place); o [T,HV,V] bf16 (written)."""
     T = q.shape[0]
     gb_rows = g.shape[0]
+    _prefill_shapes(d, q, k, v, g, beta, state_pool, state_idx, cu_seqlens, num_seqs, o)
     if workspace is None:
         need = kda_prefill_workspace_size(d, num_seqs, T)
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
@@ -193,6 +241,7 @@ def kda_prefill_noalloc(d, gate: Gate, q, k, v, g, beta, state_pool, state_idx, 
                         num_seqs, o, intermediate=None, err_flag=None, stream=None):
     """kda_prefill with the library's built-in static scratch (see kda.h): for
     callers that cannot allocate device memory."""
+    _prefill_shapes(d, q, k, v, g, beta, state_pool, state_idx, cu_seqlens, num_seqs, o)
     st = load().kda_prefill_noalloc(
         d, gate.c(), _in16(d, q, "q"), _in16(d, k, "k"), _in16(d, v, "v"), _in16(d, g, "g"), _in16(d, beta, "beta"),
         int(g.shape[0]), _p(state_pool), int(state_pool.shape[0]), _p(state_idx), _p(cu_seqlens),
@@ -203,6 +252,9 @@ def kda_prefill_noalloc(d, gate: Gate, q, k, v, g, beta, state_pool, state_idx, 
 
 def kda_decode_packed(d, gate: Gate, mixed_qkv, a, b, state_pool, state_idx, o, err_flag=None,
                       stream=None):
+    B = mixed_qkv.shape[0]
+    _packed_shapes(d, mixed_qkv, a, b, state_pool, state_idx, B, B)
+    _at_least(o, B * d.HV * d.V, "o", f"[{B}, HV, V]")
     st = load().kda_decode_packed(
         d, gate.c(), _in16(d, mixed_qkv, "mixed_qkv"), int(mixed_qkv.stride(0)), _in16(d, a, "a"),
         _in16(d, b, "b"), int(mixed_qkv.shape[0]), _p(state_pool), int(state_pool.shape[0]),
@@ -210,8 +262,16 @@ def kda_decode_packed(d, gate: Gate, mixed_qkv, a, b, state_pool, state_idx, o, 
     _check(st, "kda_decode_packed")
 
 
+def _verify_shapes(d, mixed_qkv, a, b, B, T, state_pool, state_idx, o):
+    rows = int(B) * int(T)
+    _packed_shapes(d, mixed_qkv, a, b, state_pool, state_idx, rows, int(B))
+    _at_least(o, rows * d.HV * d.V, "o", f"[{B}, {T}, HV, V]")
+
+
 def kda_verify_chain(d, gate: Gate, mixed_qkv, a, b, B, T, state_pool, state_idx, o, snapshots,
                      err_flag=None, stream=None):
+    _verify_shapes(d, mixed_qkv, a, b, B, T, state_pool, state_idx, o)
+    _at_least(snapshots, B * T * d.HV * d.V * d.K, "snapshots", f"[{B}, {T}, HV, V, K]")
     st = load().kda_verify_chain(
         d, gate.c(), _in16(d, mixed_qkv, "mixed_qkv"), int(mixed_qkv.stride(0)), _in16(d, a, "a"),
         _in16(d, b, "b"), int(B), int(T), _p(state_pool), int(state_pool.shape[0]), _p(state_idx),
@@ -221,6 +281,9 @@ def kda_verify_chain(d, gate: Gate, mixed_qkv, a, b, B, T, state_pool, state_idx
 
 def kda_verify_tree(d, gate: Gate, mixed_qkv, a, b, B, T, parent_idx, state_pool, state_idx, o,
                     snapshots, err_flag=None, stream=None):
+    _verify_shapes(d, mixed_qkv, a, b, B, T, state_pool, state_idx, o)
+    _at_least(snapshots, B * T * d.HV * d.V * d.K, "snapshots", f"[{B}, {T}, HV, V, K]")
+    _at_least(parent_idx, B * T, "parent_idx", f"[{B}, {T}]")
     st = load().kda_verify_tree(
         d, gate.c(), _in16(d, mixed_qkv, "mixed_qkv"), int(mixed_qkv.stride(0)), _in16(d, a, "a"),
         _in16(d, b, "b"), int(B), int(T), _p(parent_idx), _p(state_pool), int(state_pool.shape[0]),
@@ -229,6 +292,9 @@ def kda_verify_tree(d, gate: Gate, mixed_qkv, a, b, B, T, parent_idx, state_pool
 
 
 def kda_commit(d, snapshots, B, T, accepted, state_pool, state_idx, err_flag=None, stream=None):
+    _at_least(snapshots, B * T * d.HV * d.V * d.K, "snapshots", f"[{B}, {T}, HV, V, K]")
+    _at_least(accepted, B, "accepted", f"[{B}]")
+    _at_least(state_idx, B, "state_idx", f"[{B}]")
     st = load().kda_commit(d, _p(snapshots), int(B), int(T), _p(accepted), _p(state_pool),
                            int(state_pool.shape[0]), _p(state_idx), _p(err_flag), _stream(stream))
     _check(st, "kda_commit")
@@ -242,6 +308,8 @@ def kda_verify_chain_replay(d, gate: Gate, mixed_qkv, a, b, B, T, state_pool, st
                             err_flag=None, stream=None):
     """Chain verify without snapshots: o as kda_verify_chain, each token's
     folded inputs recorded in `ring` (kda_replay_ring_bytes bytes, FP32)."""
+    _verify_shapes(d, mixed_qkv, a, b, B, T, state_pool, state_idx, o)
+    _at_least(ring, kda_replay_ring_bytes(d, B, T) // 4, "ring", "kda_replay_ring_bytes / 4 FP32")
     st = load().kda_verify_chain_replay(
         d, gate.c(), _in16(d, mixed_qkv, "mixed_qkv"), int(mixed_qkv.stride(0)), _in16(d, a, "a"),
         _in16(d, b, "b"), int(B), int(T), _p(state_pool), int(state_pool.shape[0]), _p(state_idx),
@@ -252,6 +320,9 @@ def kda_verify_chain_replay(d, gate: Gate, mixed_qkv, a, b, B, T, state_pool, st
 def kda_commit_replay(d, ring, B, T, accepted, state_pool, state_idx, err_flag=None, stream=None):
     """Advances each request's pool state through its accepted draft tokens
     from the ring written by kda_verify_chain_replay."""
+    _at_least(ring, kda_replay_ring_bytes(d, B, T) // 4, "ring", "kda_replay_ring_bytes / 4 FP32")
+    _at_least(accepted, B, "accepted", f"[{B}]")
+    _at_least(state_idx, B, "state_idx", f"[{B}]")
     st = load().kda_commit_replay(d, _p(ring), int(B), int(T), _p(accepted), _p(state_pool),
                                   int(state_pool.shape[0]), _p(state_idx), _p(err_flag),
                                   _stream(stream))
