@@ -48,3 +48,52 @@ def chunk_prefill(q, k, v, g, beta, S0, scale, chunk=64):
         khat = kk * np.exp(gam[-1] - gam)
         S = np.exp(gam[-1])[:, None] * S + khat.T @ U
     return o, S, starts
+
+
+# --- chunk-parallel state passing -------------------------------------------
+# The end state of a chunk is affine in its start state:
+#   S_L = Diag(e^{Gam_L}) S0 + Khat^T (Util - W S0) = M S0 + B,
+#   M = Diag(e^{Gam_L}) - Khat^T W  (K x K),   B = Khat^T Util  (K x V).
+# Every chunk-start state is therefore a prefix composition of these maps,
+# (M2, B2) o (M1, B1) = (M2 M1, M2 B1 + B2), which a scan finds in log2(n)
+# levels instead of n sequential steps.
+
+
+def chunk_maps(q, k, v, g, beta, chunk=64, dtype=np.float64):
+    """The per-chunk maps (M_c, B_c) of a sequence, in `dtype`."""
+    q, k, v, g, beta = (np.asarray(x, dtype=np.float64) for x in (q, k, v, g, beta))
+    maps = []
+    for s in range(0, q.shape[0], chunk):
+        e = min(s + chunk, q.shape[0])
+        L = e - s
+        gam = np.cumsum(g[s:e], axis=0)
+        kk, vv, bb = k[s:e], v[s:e], beta[s:e]
+        diff = gam[:, None, :] - gam[None, :, :]
+        lower = np.tril(np.ones((L, L), dtype=bool))
+        dec = np.where(lower[:, :, None], np.exp(np.minimum(diff, 0.0)), 0.0)
+        A = bb[:, None] * np.einsum("tc,ic,tic->ti", kk, kk, dec) * np.tril(np.ones((L, L)), -1)
+        Tinv = np.linalg.inv(np.eye(L) + A)
+        W = Tinv @ (bb[:, None] * kk * np.exp(gam))
+        Util = Tinv @ (bb[:, None] * vv)
+        khat = kk * np.exp(gam[-1] - gam)
+        maps.append(((np.diag(np.exp(gam[-1])) - khat.T @ W).astype(dtype),
+                     (khat.T @ Util).astype(dtype)))
+    return maps
+
+
+def scan_chunk_states(maps, S0):
+    """Chunk-start states and the final state from an inclusive
+    Hillis-Steele scan of the maps (level d composes each prefix with the one
+    d chunks before it), in the maps' precision."""
+    Mp = [m for m, _ in maps]
+    Bp = [b for _, b in maps]
+    n, d = len(maps), 1
+    while d < n:
+        Mn, Bn = list(Mp), list(Bp)
+        for c in range(d, n):
+            Mn[c] = Mp[c] @ Mp[c - d]
+            Bn[c] = Mp[c] @ Bp[c - d] + Bp[c]
+        Mp, Bp, d = Mn, Bn, 2 * d
+    S0 = np.asarray(S0, dtype=Mp[0].dtype)
+    starts = [S0] + [Mp[c] @ S0 + Bp[c] for c in range(n - 1)]
+    return starts, Mp[-1] @ S0 + Bp[-1]
