@@ -29,7 +29,11 @@
  *     as raw bit patterns (kda_bf16): BF16, or FP16 when kda_dims.dtype is
  *     KDA_DTYPE_F16.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy stream).
- *   - Host-checkable errors return a status and launch nothing.
+ *   - Host-checkable errors return a status and launch nothing.  Buffer
+ *     sizes are implied by the sizes passed (B, T, num_seqs, total_tokens,
+ *     gb_rows, pool_slots) and cannot be checked through bare pointers: a
+ *     buffer shorter than its documented shape is a caller error.  (The
+ *     Python binding checks tensor shapes before it calls.)
  *   - Device-resident index errors (a state slot outside [-1, pool_slots), a
  *     tree parent outside [-1, i), a malformed cu_seqlens, an accepted index
  *     >= T) set bits in *err_flag when err_flag is non-NULL and the affected
