@@ -76,6 +76,19 @@ def test_prefill_ragged_varlen_with_garbage_padding(lengths):
     check(run_both(d, 2, intermediate=True), d)
 
 
+def test_prefill_with_no_tokens_leaves_the_pool_unchanged():
+    """The empty call: every sequence has length 0 (one of them a padding
+    slot).  No transform runs, the state pass returns before it reads any
+    workspace, the pool is untouched and nothing is flagged, as in the
+    oracle, where a length-0 sequence passes its state through."""
+    d = inputs.prefill_inputs(seed=90, lengths=[0, 0], H=2, slots=4, state_idx=[1, -1])
+    out = run_both(d, 2)
+    assert out["err"] == 0
+    assert out["o"].numel() == 0
+    assert torch.equal(out["pool"], out["pool_before"])
+    assert np.array_equal(out["pool"].cpu().numpy().astype(np.float64), out["pool_ref"])
+
+
 def test_prefill_fixed_layout_equal_lengths():
     d = inputs.prefill_inputs(seed=21, lengths=[96, 96, 96], H=2, slots=5, varlen=False)
     check(run_both(d, 2, varlen=False), d)
