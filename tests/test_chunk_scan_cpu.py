@@ -12,7 +12,9 @@ pass would rely on:
     ||k|| = 1 and 0 <= beta <= 1; so a window of h chunks started from zero
     misses the true state by at most the product of h such bounds times the
     state at the window's start;
-  * the scan run in FP32 stays far inside the state tolerance (1e-3 x RMS).
+  * the scan run in FP32 stays far inside the state tolerance (1e-3 x RMS);
+  * on tensor cores its products need split operands: TF32 alone misses the
+    tolerance when the decay is slow, three TF32 products (hi/lo) do not.
 """
 import numpy as np
 
@@ -88,3 +90,49 @@ def test_fp32_scan_within_state_tolerance():
     ref = np.array(starts)
     rms = np.sqrt(np.mean(np.square(ref)))
     assert np.max(np.abs(np.array(st32, np.float64) - ref)) <= 1e-5 * rms
+
+
+def _tf32(x):
+    """FP32 rounded to TF32 (10 mantissa bits), to nearest even."""
+    u = np.asarray(x, np.float32).view(np.uint32).astype(np.uint64)
+    u = (u + 0xFFF + ((u >> 13) & 1)) & ~np.uint64(0x1FFF)
+    return u.astype(np.uint32).view(np.float32)
+
+
+def _scan_with(maps, S0, mm):
+    """scan_chunk_states with every product done by mm (FP32 results)."""
+    Mp, Bp = [m for m, _ in maps], [b for _, b in maps]
+    n, d = len(maps), 1
+    while d < n:
+        Mn, Bn = list(Mp), list(Bp)
+        for c in range(d, n):
+            Mn[c] = mm(Mp[c], Mp[c - d])
+            Bn[c] = (mm(Mp[c], Bp[c - d]).astype(np.float64) + Bp[c]).astype(np.float32)
+        Mp, Bp, d = Mn, Bn, 2 * d
+    S0 = np.asarray(S0, np.float32)
+    return [S0] + [(mm(Mp[c], S0).astype(np.float64) + Bp[c]).astype(np.float32) for c in range(n - 1)]
+
+
+def test_tensor_core_scan_needs_split_operands():
+    """The scan's products on tensor cores: with TF32 operands (FP32
+    accumulation) the chunk-start states miss the state tolerance when the
+    decay is slow; with each operand split into TF32 hi + lo and three
+    products (dropping lo x lo) they stay far inside it."""
+    f64 = lambda x: x.astype(np.float64)
+
+    def tf32_mm(a, b):
+        return (f64(_tf32(a)) @ f64(_tf32(b))).astype(np.float32)
+
+    def split_mm(a, b):
+        ah, bh = _tf32(a), _tf32(b)
+        al, bl = _tf32(np.float32(a) - ah), _tf32(np.float32(b) - bh)
+        return (f64(ah) @ f64(bh) + f64(ah) @ f64(bl) + f64(al) @ f64(bh)).astype(np.float32)
+
+    q, k, v, g, beta, S0 = _inputs(4096, 128, -0.005, seed=4)
+    _, _, starts = chunk_prefill(q, k, v, g, beta, S0, 128 ** -0.5)
+    maps = [(m.astype(np.float32), b.astype(np.float32)) for m, b in chunk_maps(q, k, v, g, beta)]
+    ref = np.array(starts)
+    rms = np.sqrt(np.mean(np.square(ref)))
+    err = lambda st: np.max(np.abs(np.array(st, np.float64) - ref)) / rms
+    assert err(_scan_with(maps, S0, tf32_mm)) > 1e-3
+    assert err(_scan_with(maps, S0, split_mm)) < 1e-5
