@@ -137,8 +137,13 @@ def _in16(d, t, name):
 
 
 def _at_least(t, n, name, shape):
-    """t must hold n elements (the rows the kernels touch), t None allowed."""
-    if t is not None and t.numel() < n:
+    """t must be dense (the library indexes it by its documented layout) and
+    hold n elements (the rows the kernels touch); t None allowed."""
+    if t is None:
+        return
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.numel() < n:
         raise ValueError(f"{name} must hold {shape} = {n} elements (got shape {tuple(t.shape)})")
 
 
@@ -152,6 +157,7 @@ def _packed_shapes(d, mixed_qkv, a, b, state_pool, state_idx, rows, reqs):
     if state_pool.dim() < 3 or tuple(state_pool.shape[-3:]) != (d.HV, d.V, d.K):
         raise ValueError(f"state_pool must end in [HV, V, K] = [{d.HV}, {d.V}, {d.K}] "
                          f"(got {tuple(state_pool.shape)})")
+    _at_least(state_pool, 0, "state_pool", "[slots, HV, V, K]")
     width = 2 * d.H * d.K + d.HV * d.V
     if mixed_qkv.dim() != 2 or mixed_qkv.shape[0] < rows or mixed_qkv.shape[1] < width \
             or mixed_qkv.stride(1) != 1:
@@ -208,6 +214,7 @@ def _prefill_shapes(d, q, k, v, g, beta, state_pool, state_idx, cu_seqlens, num_
     if state_pool.dim() < 3 or tuple(state_pool.shape[-3:]) != (d.HV, d.V, d.K):
         raise ValueError(f"state_pool must end in [HV, V, K] = [{d.HV}, {d.V}, {d.K}] "
                          f"(got {tuple(state_pool.shape)})")
+    _at_least(state_pool, 0, "state_pool", "[slots, HV, V, K]")
     _at_least(q, T * d.H * d.K, "q", f"[{T}, H, K]")
     _at_least(k, T * d.H * d.K, "k", f"[{T}, H, K]")
     _at_least(v, T * d.HV * d.V, "v", f"[{T}, HV, V]")
@@ -226,6 +233,7 @@ def kda_prefill(d, gate: Gate, q, k, v, g, beta, state_pool, state_idx, cu_seqle
     T = q.shape[0]
     gb_rows = g.shape[0]
     _prefill_shapes(d, q, k, v, g, beta, state_pool, state_idx, cu_seqlens, num_seqs, o)
+    _at_least(intermediate, 0, "intermediate", "[chunks, HV, V, K]")  # size set by cu_seqlens on the device
     if workspace is None:
         need = kda_prefill_workspace_size(d, num_seqs, T)
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
@@ -242,6 +250,7 @@ def kda_prefill_noalloc(d, gate: Gate, q, k, v, g, beta, state_pool, state_idx, 
     """kda_prefill with the library's built-in static scratch (see kda.h): for
     callers that cannot allocate device memory."""
     _prefill_shapes(d, q, k, v, g, beta, state_pool, state_idx, cu_seqlens, num_seqs, o)
+    _at_least(intermediate, 0, "intermediate", "[chunks, HV, V, K]")  # size set by cu_seqlens on the device
     st = load().kda_prefill_noalloc(
         d, gate.c(), _in16(d, q, "q"), _in16(d, k, "k"), _in16(d, v, "v"), _in16(d, g, "g"), _in16(d, beta, "beta"),
         int(g.shape[0]), _p(state_pool), int(state_pool.shape[0]), _p(state_idx), _p(cu_seqlens),

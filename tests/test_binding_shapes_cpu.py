@@ -80,6 +80,19 @@ def test_decode_output_must_hold_every_row():
         decode(rows(2), o=torch.zeros((1, H, K), dtype=BF))
 
 
+def test_buffers_must_be_dense():
+    """The library indexes every buffer by its documented dense layout (only
+    mixed_qkv carries a row stride)."""
+    with pytest.raises(ValueError, match="o must be contiguous"):
+        decode(rows(2), o=torch.zeros((H, 2, K), dtype=BF).transpose(0, 1))
+    with pytest.raises(ValueError, match="state_pool must be contiguous"):
+        decode(rows(2), p=torch.zeros((4, K, K, H)).permute(0, 3, 1, 2))
+    x = rows(2)
+    x["mixed_qkv"] = torch.zeros((2, 2 * (2 * H * K + H * K)), dtype=BF)[:, :2 * H * K + H * K]
+    with pytest.raises(ValueError, match="device tensors"):  # a row stride is fine for mixed_qkv
+        decode(x)
+
+
 def verify(B, T, x, snaps=None, o=None, parent=None, tree=False):
     o = torch.zeros((B, T, H, K), dtype=BF) if o is None else o
     snaps = torch.zeros((B, T, H, K, K)) if snaps is None else snaps
