@@ -97,3 +97,53 @@ def scan_chunk_states(maps, S0):
     S0 = np.asarray(S0, dtype=Mp[0].dtype)
     starts = [S0] + [Mp[c] @ S0 + Bp[c] for c in range(n - 1)]
     return starts, Mp[-1] @ S0 + Bp[-1]
+
+
+def grouped_prefill(q, k, v, g, beta, S0, scale, group=4, chunk=64):
+    """The chunk form with the chain over chunks cut into groups of `group`
+    chunks, in three stages and without storing anything per chunk:
+      1. every group, independently, runs the chunk recurrence from a zero
+         state with the identity carried beside it ([S | P], P <- M_c P), and
+         keeps only its end: (S_end, P_end), so that true end = S_end + P_end C;
+      2. the true group-start states C_g follow in one short chain:
+         C_{g+1} = S_end_g + P_end_g C_g, C_0 = S0;
+      3. every group reruns the chunk form from its C_g.
+    Returns what chunk_prefill returns (o, final state, chunk-start states)."""
+    q, k, v, g, beta = (np.asarray(x, dtype=np.float64) for x in (q, k, v, g, beta))
+    T, K = q.shape
+    bounds = [(s, min(s + chunk, T)) for s in range(0, T, chunk)]
+    groups = [bounds[i:i + group] for i in range(0, len(bounds), group)]
+
+    def run(grp, S, P=None):
+        """The chunk form over the group's chunks from S (and P when given)."""
+        o_parts, starts = [], []
+        for s, e in grp:
+            L = e - s
+            gam = np.cumsum(g[s:e], axis=0)
+            kk, qq, vv, bb = k[s:e], q[s:e], v[s:e], beta[s:e]
+            diff = gam[:, None, :] - gam[None, :, :]
+            lower = np.tril(np.ones((L, L), dtype=bool))
+            dec = np.where(lower[:, :, None], np.exp(np.minimum(diff, 0.0)), 0.0)
+            A = bb[:, None] * np.einsum("tc,ic,tic->ti", kk, kk, dec) * np.tril(np.ones((L, L)), -1)
+            Pm = np.einsum("tc,ic,tic->ti", qq, kk, dec)
+            Tinv = np.linalg.inv(np.eye(L) + A)
+            W = Tinv @ (bb[:, None] * kk * np.exp(gam))
+            U = Tinv @ (bb[:, None] * vv) - W @ S
+            starts.append(S.copy())
+            o_parts.append(scale * ((qq * np.exp(gam)) @ S + Pm @ U))
+            khat = kk * np.exp(gam[-1] - gam)
+            S = np.exp(gam[-1])[:, None] * S + khat.T @ U
+            if P is not None:
+                P = np.exp(gam[-1])[:, None] * P - khat.T @ (W @ P)
+        return o_parts, starts, S, P
+
+    ends = [run(grp, np.zeros((K, v.shape[1])), np.eye(K))[2:] for grp in groups]   # stage 1
+    C = [np.array(S0, dtype=np.float64)]                                             # stage 2
+    for S_end, P_end in ends[:-1]:
+        C.append(S_end + P_end @ C[-1])
+    o, starts, S = [], [], None                                                      # stage 3
+    for grp, Cg in zip(groups, C):
+        o_parts, st, S, _ = run(grp, Cg)
+        o += o_parts
+        starts += st
+    return np.concatenate(o), S, starts

@@ -14,11 +14,13 @@ pass would rely on:
     state at the window's start;
   * the scan run in FP32 stays far inside the state tolerance (1e-3 x RMS);
   * on tensor cores its products need split operands: TF32 alone misses the
-    tolerance when the decay is slow, three TF32 products (hi/lo) do not.
+    tolerance when the decay is slow, three TF32 products (hi/lo) do not;
+  * the grouped three-stage pass (tests/chunk_form.py, grouped_prefill), which
+    needs no per-chunk storage, gives the sequential outputs and states.
 """
 import numpy as np
 
-from tests.chunk_form import chunk_maps, chunk_prefill, scan_chunk_states
+from tests.chunk_form import chunk_maps, chunk_prefill, grouped_prefill, scan_chunk_states
 
 
 def _inputs(T, K, lower_bound, seed):
@@ -136,3 +138,18 @@ def test_tensor_core_scan_needs_split_operands():
     err = lambda st: np.max(np.abs(np.array(st, np.float64) - ref)) / rms
     assert err(_scan_with(maps, S0, tf32_mm)) > 1e-3
     assert err(_scan_with(maps, S0, split_mm)) < 1e-5
+
+
+def test_grouped_pass_equals_sequential_chunk_form():
+    """The three-stage grouped pass (groups from zero with the identity
+    carried, a short chain over group starts, groups rerun from their true
+    starts) gives the sequential chunk form's outputs and states, for group
+    sizes that divide the chunk count and ones that do not."""
+    q, k, v, g, beta, S0 = _inputs(64 * 11 + 9, 32, -0.05, seed=5)
+    o, S_T, starts = chunk_prefill(q, k, v, g, beta, S0, 32 ** -0.5)
+    orms, srms = np.sqrt(np.mean(np.square(o))), np.sqrt(np.mean(np.square(starts)))
+    for group in (1, 3, 4, 12, 20):
+        og, Sg, stg = grouped_prefill(q, k, v, g, beta, S0, 32 ** -0.5, group=group)
+        np.testing.assert_allclose(og, o, rtol=0, atol=1e-12 * orms)
+        np.testing.assert_allclose(np.array(stg), np.array(starts), rtol=0, atol=1e-12 * srms)
+        np.testing.assert_allclose(Sg, S_T, rtol=0, atol=1e-12 * srms)
