@@ -134,3 +134,28 @@ def test_replay_host_errors(lib):
     assert lib.kda_commit_replay(d, DUMMY, 2, 0, DUMMY, DUMMY, 240, DUMMY, None, None) == kda.KDA_ERR_SHAPE
     # nothing to do for B = 0
     assert lib.kda_commit_replay(d, None, 0, 6, None, DUMMY, 240, DUMMY, None, None) == kda.KDA_OK
+
+
+def test_packed_alignment_and_gate_errors(lib):
+    """Every 128-bit load of the recurrent kernels needs 16-byte aligned rows,
+    pools and rings; the unbounded gate is refused on every path."""
+    d, row = kda.dims(16), 3 * 16 * 128
+    odd = ctypes.c_void_p(0x10004)
+
+    def decode(gate=None, qkv=DUMMY, a=DUMMY, pool=DUMMY):
+        return lib.kda_decode_packed(d, gate or _gate(), qkv, row, a, DUMMY, 2, pool, 240, DUMMY, DUMMY,
+                                     None, None)
+
+    assert decode(qkv=odd) == kda.KDA_ERR_ALIGNMENT
+    assert decode(a=odd) == kda.KDA_ERR_ALIGNMENT
+    assert decode(pool=odd) == kda.KDA_ERR_ALIGNMENT
+    assert decode(gate=_gate(A_log=DUMMY, lb=math.nan)) == kda.KDA_ERR_UNSUPPORTED
+    assert decode(gate=kda.kda_gate(DUMMY, odd, -5.0, 1, 1, 128 ** -0.5)) == kda.KDA_ERR_ALIGNMENT
+    assert lib.kda_verify_chain(d, _gate(), DUMMY, row, DUMMY, DUMMY, 2, 6, odd, 240, DUMMY, DUMMY,
+                                DUMMY, None, None) == kda.KDA_ERR_ALIGNMENT
+    assert lib.kda_verify_tree(d, _gate(A_log=DUMMY, lb=math.nan), DUMMY, row, DUMMY, DUMMY, 2, 6, DUMMY,
+                               DUMMY, 240, DUMMY, DUMMY, DUMMY, None, None) == kda.KDA_ERR_UNSUPPORTED
+    assert lib.kda_verify_chain_replay(d, _gate(), DUMMY, row, DUMMY, DUMMY, 2, 6, DUMMY, 240, DUMMY,
+                                       DUMMY, odd, None, None) == kda.KDA_ERR_ALIGNMENT
+    assert lib.kda_commit_replay(d, odd, 2, 6, DUMMY, DUMMY, 240, DUMMY, None, None) == kda.KDA_ERR_ALIGNMENT
+    assert lib.kda_commit_replay(d, DUMMY, 2, 6, DUMMY, odd, 240, DUMMY, None, None) == kda.KDA_ERR_ALIGNMENT
