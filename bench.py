@@ -55,13 +55,15 @@ FLUSH_BYTES = 512 << 20
 LAYERS = 8  # default decode/verify/commit calls per timed replay (--layers)
 
 # DRAM traffic per launch from ncu (dram__bytes_read.sum + dram__bytes_write.sum),
-# keyed by kernel; valid only while the kernel sources hash to the recorded value.
+# keyed by kernel; valid only while the kernel sources hash to the recorded
+# value (the figure is re-taken whenever they change; see the transform's ncu
+# traffic summary under profiles/).
 NCU_TRAFFIC = {
-    # the four segment launches of one 1x4096 prefill call, 16 heads: read
-    # 67,638,016 B + write 12,800 B (profiles/chunk_transform_1x4096_h16.md);
-    # refreshed whenever the kernel sources change
+    # the segment launches of one 1x4096 prefill call, 16 heads
     "prefill_transform": {"bytes": 67650816, "src": "30cbda600e28f256"},
 }
+VERIFY_SWEEP = (1, 2, 4, 8, 12, 16, 24, 32, 48)  # requests x 6 draft tokens, chain and tree
+DECODE_SWEEP = (1, 16)  # besides the core step's 48
 
 
 def _peaks():
@@ -130,6 +132,13 @@ def commit_replay_bytes(accepted, T):
 
 def commit_bytes(B):
     return B * 2 * H * K * K * 4
+
+
+def varlen_prefill_bytes(lengths, heads=H):
+    # token tensors (q, k, v, gate input, o) and beta over the real tokens, the
+    # gathered and scattered states
+    T = int(sum(lengths))
+    return 5 * T * heads * K * 2 + T * heads * 2 + len(lengths) * 2 * heads * K * K * 4
 
 
 # --------------------------------------------------------------------------- #
@@ -453,10 +462,45 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks([sum(a.elapsed_time(b) for a, b in ev_e2e)], world, dev)[0]
 
+    # ---- e2e of the layer phases: decode B=48 and chain verify 16x6 with their
+    # inputs copied from pinned host memory and o read back every call ----
+    e2e_layers = {}
+    for name, rows_host, B_, T_ in (("decode_b48", dd, DECODE_B, 1), ("verify_chain_b16x6", vd, VERIFY_B, VERIFY_T)):
+        hx = {n: torch.from_numpy(np.ascontiguousarray(rows_host[n])).pin_memory() for n in ("mixed_qkv", "a", "b")}
+        dx = {n: torch.empty(hx[n].shape, dtype=torch.int16, device=dev) for n in hx}
+        x0 = L[0]
+        o_dev = x0["d_o"] if T_ == 1 else x0["v_o"]
+        o_h = torch.empty(o_dev.shape, dtype=torch.int16).pin_memory()
+        ev_l = []
+        for i in range(e2e_steps + 3):
+            flush_l2()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for n in hx:
+                dx[n].copy_(hx[n], non_blocking=True)
+            if T_ == 1:
+                kda.kda_decode_packed(D, gate, *(dx[n].view(torch.bfloat16) for n in ("mixed_qkv", "a", "b")),
+                                      x0["d_pool"], x0["d_idx"], o_dev)
+            else:
+                kda.kda_verify_chain(D, gate, *(dx[n].view(torch.bfloat16) for n in ("mixed_qkv", "a", "b")),
+                                     B_, T_, x0["v_pool"], x0["v_idx"], o_dev, x0["v_snap"])
+            o_h.copy_(o_dev.view(torch.int16), non_blocking=True)
+            e1.record(stream)
+            if i >= 3:
+                ev_l.append((e0, e1))
+        torch.cuda.synchronize()
+        us = statistics.mean(a.elapsed_time(b) for a, b in ev_l) * 1e3
+        e2e_layers[name] = {"us_per_call": round(us, 2),
+                            "h2d_bytes": sum(x.numel() * x.element_size() for x in hx.values()),
+                            "d2h_bytes": o_h.numel() * o_h.element_size()}
+
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
         return
+    del L, step_graphs, records
+    torch.cuda.empty_cache()
+    extras = {} if args.no_extras else run_extras(args, dev, stream, flush_l2, gate_seed=rank)
 
     hbm, bf16_tf, sm_max, peak_kind = _peaks()
     # The library splits a single long prefill into up to four segments (a
@@ -555,20 +599,24 @@ def run_ours(args, rank, world, local_rank):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "clocks": clocks, "wall_s_timed": round(wall, 3), "source_hash": src,
     }
+    phase_out["e2e_layers"] = e2e_layers
+    phase_out.update(extras)
     if world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(pf, budget_s=10.0)
+        out["cpu_baseline"]["single_thread"] = cpu_baseline(pf, budget_s=5.0, tokens=256, threads=1)
     print(json.dumps(out), flush=True)
     if world > 1:
         dist.destroy_process_group()
 
 
-def cpu_baseline(pf, budget_s=10.0, tokens=None):
-    """The oracle, as it stands, on this host's cores."""
+def cpu_baseline(pf, budget_s=10.0, tokens=None, threads=None):
+    """The oracle, as it stands, on this host's cores (all of them, or
+    `threads`)."""
     from oracle import kda_oracle as ko
 
     T = PREFILL_T if tokens is None else tokens
     gate = ko.Gate(H, K, K, A_log=pf["A_log"], dt_bias=pf["dt_bias"], lower_bound=-5.0)
-    cores = os.cpu_count() or 1
+    cores = threads or os.cpu_count() or 1
     sl = {n: np.ascontiguousarray(pf[n][:T]) for n in ("q", "k", "v", "g", "beta")}
     runs, t0 = 0, time.perf_counter()
     while True:
@@ -580,7 +628,137 @@ def cpu_baseline(pf, budget_s=10.0, tokens=None):
         if el >= budget_s or runs >= 50:
             break
     return {"value": round(T * runs / el, 1), "unit": "tokens/s", "cores": cores, "kind": "oracle",
-            "sample": f"prefill 1x{T} tokens x 16 heads, full call, {runs} run(s) in {el:.1f} s"}
+            "sample": f"prefill 1x{T} tokens x 16 heads ({'full call' if T == PREFILL_T else 'first tokens of the 1x4096 call'}), "
+                      f"{runs} run(s) in {el:.1f} s"}
+
+
+def run_extras(args, dev, stream, flush_l2, gate_seed=0):
+    """Every other configuration of the workload, each timed on its own and
+    reported beside the step (not in ms_per_step): the 1x128 prefill at 4
+    heads, 1x8192 and 2x4096 at 16 heads, 8 varlen sequences in a 32768-row
+    bucket with garbage padding rows and a 240-slot pool, decode at 1 and 16
+    requests, and chain and tree verify over the request sweep at 6 draft
+    tokens.  Each is one CUDA graph (8 layer calls on disjoint buffers for the
+    layer phases) replayed after an L2 flush, its kernels bracketed by events
+    recorded as graph nodes."""
+    import torch
+
+    from linear_attention_serving_gated_gb300 import inputs, kda
+
+    hbm = _peaks()[0]
+    reps = max(3, min(args.steps, 20))
+
+    def bf(x):
+        return torch.from_numpy(np.ascontiguousarray(x)).to(dev).view(torch.bfloat16)
+
+    def t(x):
+        return torch.from_numpy(np.ascontiguousarray(x)).to(dev)
+
+    def timed(fn):
+        for _ in range(3):
+            flush_l2()
+            fn(None)
+        torch.cuda.synchronize()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        for e in ev:
+            e.record(stream)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn(ev)
+        ms = []
+        for _ in range(reps):
+            flush_l2()
+            g.replay()
+            torch.cuda.synchronize()
+            ms.append(ev[0].elapsed_time(ev[2]))
+        del g
+        return statistics.mean(ms)
+
+    def with_events(ev, calls):
+        for i, c in enumerate(calls):
+            if ev is not None:
+                first, last = i == 0, i == len(calls) - 1
+                kda.kda_set_stage_events([ev[0] if first else None, ev[1] if first and last else None,
+                                          ev[2] if last else None])
+            c()
+        kda.kda_set_stage_events(None)
+
+    out = {}
+
+    # ---- prefills ----
+    rng0 = np.random.default_rng(0)
+    prefills = [
+        ("prefill_1x128_h4", dict(seed=0, lengths=[128], H=4, slots=4, state_idx=[0]), True),
+        ("prefill_1x8192", dict(seed=1, lengths=[8192], H=H, slots=16), True),
+        ("prefill_2x4096_fixed", dict(seed=3, lengths=[4096, 4096], H=H, slots=16, varlen=False), False),
+        ("prefill_varlen_8seq_32k_bucket", dict(seed=0, lengths=inputs.varlen_lengths(rng0), H=H, slots=240,
+                                                gb_rows=32768), True),
+    ]
+    for name, kw, varlen in prefills:
+        d = inputs.prefill_inputs(**kw)
+        heads = kw["H"]
+        Dh = kda.dims(heads)
+        gate = kda.Gate(A_log=t(d["A_log"]), dt_bias=t(d["dt_bias"]), lower_bound=-5.0)
+        x = {n: bf(d[n]) for n in ("q", "k", "v", "g", "beta")}
+        pool, idx = t(d["pool"]), t(d["state_idx"])
+        cu = t(d["cu_seqlens"]) if varlen else None
+        lens = [int(v) for v in d["lengths"]]
+        T_ = sum(lens)
+        o = torch.empty((T_, heads, K), dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(kda.kda_prefill_workspace_size(Dh, len(lens), T_), dtype=torch.uint8, device=dev)
+        del d
+        ms = timed(lambda ev: with_events(ev, [lambda: kda.kda_prefill(
+            Dh, gate, x["q"], x["k"], x["v"], x["g"], x["beta"], pool, idx, cu, len(lens), o, workspace=ws)]))
+        byts = varlen_prefill_bytes(lens, heads)
+        out[name] = {"us": round(ms * 1e3, 2), "tok_s": round(T_ / (ms / 1e3), 1), "tokens": T_,
+                     "sequences": len(lens), "heads": heads,
+                     "hbm_frac_of_call": round(byts / (ms / 1e3) / 1e9 / hbm, 4)}
+        del x, pool, idx, cu, o, ws
+        torch.cuda.empty_cache()
+
+    # ---- decode and verify sweeps, 8 layer calls on disjoint buffers ----
+    layers = args.layers
+    D = kda.dims(H)
+    for B in DECODE_SWEEP:
+        d = inputs.decode_inputs(seed=100 + B + gate_seed, B=B, H=H, slots=240)
+        gate = kda.Gate(A_log=t(d["A_log"]), dt_bias=t(d["dt_bias"]), lower_bound=-5.0)
+        Lx = [{"x": {n: bf(d[n]) for n in ("mixed_qkv", "a", "b")}, "pool": t(d["pool"]),
+               "idx": t(d["state_idx"]), "o": torch.empty((B, H, K), dtype=torch.bfloat16, device=dev)}
+              for _ in range(layers)]
+        ms = timed(lambda ev: with_events(ev, [
+            (lambda y=y: kda.kda_decode_packed(D, gate, y["x"]["mixed_qkv"], y["x"]["a"], y["x"]["b"], y["pool"],
+                                               y["idx"], y["o"])) for y in Lx]))
+        us = ms * 1e3 / layers
+        out[f"decode_b{B}"] = {"us": round(us, 2), "hbm_frac": round(decode_bytes(B) / (us / 1e6) / 1e9 / hbm, 4)}
+        del Lx
+        torch.cuda.empty_cache()
+    sweep = {}
+    for B in VERIFY_SWEEP:
+        d = inputs.verify_inputs(seed=200 + B + gate_seed, B=B, T=VERIFY_T, H=H, slots=240)
+        gate = kda.Gate(A_log=t(d["A_log"]), dt_bias=t(d["dt_bias"]), lower_bound=-5.0)
+        Lx = [{"x": {n: bf(d[n]) for n in ("mixed_qkv", "a", "b")}, "pool": t(d["pool"]),
+               "idx": t(d["state_idx"]), "par": t(d["parent"]),
+               "o": torch.empty((B, VERIFY_T, H, K), dtype=torch.bfloat16, device=dev),
+               "snap": torch.empty((B, VERIFY_T, H, K, K), device=dev)} for _ in range(layers)]
+        row = {}
+        for mode in ("chain", "tree"):
+            def call(y, mode=mode):
+                if mode == "chain":
+                    kda.kda_verify_chain(D, gate, y["x"]["mixed_qkv"], y["x"]["a"], y["x"]["b"], B, VERIFY_T,
+                                         y["pool"], y["idx"], y["o"], y["snap"])
+                else:
+                    kda.kda_verify_tree(D, gate, y["x"]["mixed_qkv"], y["x"]["a"], y["x"]["b"], B, VERIFY_T,
+                                        y["par"], y["pool"], y["idx"], y["o"], y["snap"])
+            ms = timed(lambda ev: with_events(ev, [(lambda y=y: call(y)) for y in Lx]))
+            us = ms * 1e3 / layers
+            row[mode] = {"us": round(us, 2),
+                         "hbm_frac": round(verify_bytes(B, VERIFY_T) / (us / 1e6) / 1e9 / hbm, 4)}
+        sweep[str(B)] = row
+        del Lx
+        torch.cuda.empty_cache()
+    out["verify_sweep_x6"] = sweep
+    out["extras_timing"] = f"one CUDA graph per configuration, {reps} replays after an L2 flush, mean"
+    return out
 
 
 def run_reference(args, rank, world):
@@ -633,6 +811,9 @@ def main():
                     help="decode/verify/commit calls per timed replay, each on its own buffers")
     ap.add_argument("--no-long", action="store_true",
                     help="skip the 32768-token prefill phases (about 1.4 GB less device memory, e.g. under ncu)")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the other configurations (1x128 at 4 heads, 1x8192, 2x4096, varlen 32K bucket, "
+                         "decode 1/16, verify sweep)")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", args.gpus if "RANK" in os.environ else 1))

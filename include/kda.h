@@ -78,6 +78,13 @@ typedef enum {
 #define KDA_DEVERR_TIMEOUT 16 /* a kernel's bounded wait on its own copies or
                                  tensor-core work ran out; its unit was not
                                  written back */
+#define KDA_DEVERR_INTERMEDIATE 32 /* the chunk-start state buffer holds fewer
+                                      records than the call's sequences have
+                                      chunks; the states past its end were not
+                                      written */
+#define KDA_DEVERR_DECAY 64   /* prefill with given log-decays (A_log NULL): a
+                                 value outside [-5.5, 0] or NaN; its sequence
+                                 was skipped (pool slot and o rows untouched) */
 
 /* element type of the token tensors (q, k, v, g, beta, mixed_qkv, a, b) and
  * of the output o: the "two precisions" of the pages' prefill sweep
@@ -112,7 +119,9 @@ typedef struct {
 const char *kda_status_string(kda_status s);
 
 /* Bytes of device workspace kda_prefill needs for this call shape (an upper
- * bound over every cu_seqlens with this many sequences and tokens). */
+ * bound over every cu_seqlens with this many sequences and tokens):
+ *   align256(4 * num_seqs) + (total_tokens / 64 + num_seqs) * HV * 164352.
+ * total_tokens above INT32_MAX (cu_seqlens are int32) gives SIZE_MAX. */
 size_t kda_prefill_workspace_size(kda_dims dims, int num_seqs, int64_t total_tokens);
 
 /*
@@ -120,10 +129,13 @@ size_t kda_prefill_workspace_size(kda_dims dims, int num_seqs, int64_t total_tok
  *   q, k          [total_tokens, H, K]    BF16
  *   v             [total_tokens, HV, V]   BF16
  *   g             [gb_rows, HV, K] BF16: gate input a (A_log given) or log-decay.
- *                 The chunk form needs per-token log-decays >= -5.5: a bounded
- *                 gate with lower_bound < -5.5 returns KDA_ERR_UNSUPPORTED, and
- *                 given log-decays must respect the same bound (the pages' gate
- *                 uses -5).
+ *                 The chunk form needs per-token log-decays in [-5.5, 0]: a
+ *                 bounded gate with lower_bound < -5.5 returns
+ *                 KDA_ERR_UNSUPPORTED (the pages' gate uses -5).  Given
+ *                 log-decays (A_log NULL) are checked on the device: a sequence
+ *                 with any value outside [-5.5, 0] (or NaN) sets
+ *                 KDA_DEVERR_DECAY and is skipped, its pool slot and o rows
+ *                 left untouched.  Decode and verify take any log-decay.
  *   beta          [gb_rows, HV]    BF16: raw beta (beta_is_raw) or beta
  *   gb_rows       >= total_tokens (else KDA_ERR_SHAPE).  Rows past
  *                 total_tokens are CUDA-graph bucket padding and never read.
@@ -138,6 +150,11 @@ size_t kda_prefill_workspace_size(kda_dims dims, int num_seqs, int64_t total_tok
  *   intermediate  NULL, or [sum_n ceil(T_n/64), HV, V, K] FP32: the state at
  *                 the start of every 64-token chunk of every sequence,
  *                 sequence-major.
+ *   intermediate_chunks
+ *                 the number of [HV, V, K] records `intermediate` holds
+ *                 (ignored when it is NULL).  The chunk count depends on
+ *                 cu_seqlens, which only the device reads: records past this
+ *                 capacity are not written and KDA_DEVERR_INTERMEDIATE is set.
  *   workspace     >= kda_prefill_workspace_size(...) bytes, 256-byte aligned.
  * T = 1 takes the same kernels as any other length.  The first call on each
  * device sets the kernels' shared-memory limits (cudaFuncSetAttribute); make
@@ -161,8 +178,8 @@ kda_status kda_prefill(kda_dims dims, kda_gate gate, const kda_bf16 *q, const kd
                        int64_t gb_rows, float *state_pool, int pool_slots,
                        const int32_t *state_idx, const int32_t *cu_seqlens, int num_seqs,
                        int64_t total_tokens, kda_bf16 *o, float *intermediate,
-                       void *workspace, size_t workspace_bytes, int32_t *err_flag,
-                       void *stream);
+                       int64_t intermediate_chunks, void *workspace, size_t workspace_bytes,
+                       int32_t *err_flag, void *stream);
 
 /*
  * Packed single-token decode (one token per request), state updated in place.
@@ -228,15 +245,20 @@ kda_status kda_commit(kda_dims dims, const float *snapshots, int B, int T,
  * KDA_PREFILL_STATIC_SCRATCH_BYTES that every GPU loading the library keeps
  * until the process exits.  Calls whose workspace need
  * (kda_prefill_workspace_size) exceeds it return KDA_ERR_WORKSPACE and
- * launch nothing; at 16 heads that is about 4000 tokens per call.
+ * launch nothing.  The rule is
+ *   align256(4 * num_seqs) + (total_tokens / 64 + num_seqs) * HV * 164352
+ *       <= KDA_PREFILL_STATIC_SCRATCH_BYTES,
+ * so one sequence at 16 heads takes at most 3263 tokens (51 records per
+ * head); the 1 x 4096 shape at 16 heads needs 65 and is refused.
  *
  * The first call on each device looks up the array's device address with
  * that device current; make that first call before any stream capture.
  * All calls in the process share the one array (per device): calls whose
  * work overlaps on the GPU race on it, so serialise them (one stream, or
- * events).  Each call writes every scratch byte it reads, so nothing needs
- * clearing between calls.  Arguments and results are exactly those of
- * kda_prefill.
+ * events).  The per-sequence flags at the start of the scratch are cleared
+ * by each call that uses them, and every other scratch byte a call reads it
+ * has written itself, so nothing is left to clear between calls.  Arguments
+ * and results are exactly those of kda_prefill.
  */
 #define KDA_PREFILL_STATIC_SCRATCH_BYTES ((size_t)128 << 20)
 kda_status kda_prefill_noalloc(kda_dims dims, kda_gate gate, const kda_bf16 *q,
@@ -244,7 +266,8 @@ kda_status kda_prefill_noalloc(kda_dims dims, kda_gate gate, const kda_bf16 *q,
                                const kda_bf16 *beta, int64_t gb_rows, float *state_pool,
                                int pool_slots, const int32_t *state_idx,
                                const int32_t *cu_seqlens, int num_seqs, int64_t total_tokens,
-                               kda_bf16 *o, float *intermediate, int32_t *err_flag, void *stream);
+                               kda_bf16 *o, float *intermediate, int64_t intermediate_chunks,
+                               int32_t *err_flag, void *stream);
 
 /*
  * ReplaySSM verify ("[KDA] Default GLM-5-Next spec verify to the CuTe DSL KDA

@@ -23,10 +23,12 @@
 // Rows past the end of a sequence are q = k = v = 0, beta = 0, g = 0, which
 // leave every quantity above unchanged.  Writing O through Q' = Qtil - P W
 // moves the cancellation between Qtil S0 and P W S0 into the per-chunk FP32
-// transform, so the state-dependent products need no more than BF16 W and Q'
-// against a BF16 hi/lo split of S; Khat^T U uses hi/lo splits of both
-// operands (three BF16 products), which keeps the state within 1e-4 of its
-// RMS.
+// transform.  Every state-dependent product splits both operands into BF16
+// hi + lo and sums three BF16 products (hi hi, hi lo, lo hi): [W; Q'] against
+// S and Khat^T against U.  With slow decay the state carries its errors over
+// many chunks, and a single BF16 rounding of W (2^-9 relative) already moves
+// the state by several 1e-3 of its RMS over 64 chunks; split, the state error
+// is set by the TF32 A and P products, a few 1e-4 of its RMS at g = 0.
 //
 // Decay factors inside A and P are split at a reference token r, the LAST
 // token of each 16-token block of i: e^{Gam_t-Gam_i} = e^{Gam_t-Gam_r} e^{Gam_r-Gam_i}.
@@ -47,9 +49,12 @@
 //                           already in the tensor-core operand layout.
 //   state_pass_kernel       one CTA per (sequence, head, 32 value columns),
 //                           sequential over the sequence's chunks, on tcgen05:
-//                           per chunk one bulk copy of the record into shared
-//                           memory (double-buffered, mbarrier completion), then
-//                             D1 = [W; Q'] [S_hi | S_lo]      (TMEM, M=128, N=2x32)
+//                           per chunk one bulk copy of the record's operand
+//                           tiles into shared memory (double-buffered, mbarrier
+//                           completion; Util and P Util are read straight into
+//                           registers), then
+//                             D1 = [W; Q']_hi [S_hi | S_lo] + [W; Q']_lo S_hi
+//                                                              (TMEM, M=128, N=2x32)
 //                             U  = Util - D1[0:64],  O = scale (D1[64:128] + P Util)
 //                             D2 = Khat_hi^T [U_hi | U_lo] + Khat_lo^T U_hi
 //                             S  = Diag(gamma) S + D2
@@ -75,8 +80,9 @@ constexpr int kSlices = kHeadDim / kVs;
 // order (slice = 32 value columns), so that a thread reading one token's four
 // columns and its neighbours reading the next tokens touch consecutive
 // 16-byte words.
-constexpr uint32_t kRecA1 = 0;                                // [W; Q'] 128 x 128
-constexpr uint32_t kRecKTh = kRecA1 + 128 * 128 * 2;          // Khat^T hi, 128 x 64
+constexpr uint32_t kRecA1 = 0;                                // [W; Q'] hi, 128 x 128
+constexpr uint32_t kRecA1L = kRecA1 + 128 * 128 * 2;          // [W; Q'] lo
+constexpr uint32_t kRecKTh = kRecA1L + 128 * 128 * 2;         // Khat^T hi, 128 x 64
 constexpr uint32_t kRecKTl = kRecKTh + 128 * 64 * 2;          // Khat^T lo
 constexpr uint32_t kRecU = kRecKTl + 128 * 64 * 2;            // Util
 constexpr uint32_t kRecOi = kRecU + kChunk * kHeadDim * 4;    // P Util
@@ -96,7 +102,10 @@ struct PrefillArgs {
   int64_t total_tokens;
   kda_bf16* o;
   float* intermediate;
-  uint8_t* ws;
+  int64_t inter_chunks;       // chunk records `intermediate` holds
+  uint8_t* ws;                // the (chunk, head) records
+  const int32_t* seq_flags;   // [num_seqs] nonzero: sequence rejected (given decay
+                              // out of range); nullptr when nothing is checked
   int32_t* err_flag;
   // Position segment (seg_len > 0): this launch handles chunk positions
   // [seg_pos0, seg_pos0 + seg_len) of every sequence, each of which has
@@ -151,10 +160,6 @@ __device__ __forceinline__ float dot4(float4 a, float4 b) {
 
 __device__ __forceinline__ float4& f4(float* p) { return *reinterpret_cast<float4*>(p); }
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  return (uint32_t)float_to_bf16_bits(lo) | ((uint32_t)float_to_bf16_bits(hi) << 16);
-}
-
 // ---------------------------------------------------------------------------
 // Per-chunk transform on tcgen05 (all chunks of all sequences in parallel).
 //
@@ -184,6 +189,7 @@ constexpr int kTxWarps = kTxThreads / 32;
 constexpr uint32_t kTxL = 0;                          // L: TF32 128 x 128
 constexpr uint32_t kTxR = kTxL + 128 * 128 * 4;       // R: TF32 64 x 128
 constexpr uint32_t kTxB2 = 0;                         // B2 hi, lo: 256 x 64 each (reuses L/R)
+constexpr uint32_t kTxA1L = 0;                         // [W; Q'] lo output staging (lower L/R)
 constexpr uint32_t kTxUst = 32 * 1024;                // Util | P Util output staging (upper L/R)
 constexpr uint32_t kTxAf = 0;                         // A FP32 [64][kLdT] (reuses L/R)
 constexpr uint32_t kTxPf = kTxAf + kChunk * kLdT * 4;  // P FP32 (reuses L/R)
@@ -199,7 +205,7 @@ constexpr uint32_t kTransformTcSmem = kTxEnd + 1024;
 constexpr uint32_t kTxTmemCols = 256;
 static_assert(2 * 256 * 64 * 2 <= kTxA2, "B2 fits in the L/R region");
 static_assert(kTxTf + kChunk * kLdT * 4 <= kTxA2, "A, P and (I+A)^-1 fit in the L/R region");
-static_assert(kTxWarps * kHeadDim * 4 <= kTxUst, "fold warp totals stay below the output staging");
+static_assert(kTxA1L + 128 * 128 * 2 <= kTxUst, "[W; Q'] lo staging stays below Util | P Util");
 static_assert(kTxUst + 2 * kChunk * kHeadDim * 4 <= kTxA2, "output staging fits the L/R region");
 static_assert(kTxQ % 16 == 0 && kTxK % 16 == 0 && kTxV % 16 == 0 && kTxG % 16 == 0 &&
                   kTxTf % 16 == 0 && kTxMisc % 16 == 0 && kTxA2 % 1024 == 0 && kTxR % 1024 == 0,
@@ -321,6 +327,7 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
       if (!skip) {
         const int slot = a.state_idx[loc.n];
         if (slot < 0 || slot >= a.pool_slots) skip = 1;  // padding / rejected sequence
+        if (a.seq_flags && a.seq_flags[loc.n]) skip = 1;  // given decay out of range
       }
       s_pf = u + gridDim.x < a.tx_units ? unit_loc(a, u + gridDim.x, &cid, &hh) : ChunkLoc{-1, 0, 0};
       s_pf_h = hh;
@@ -348,12 +355,14 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
     const int hk = h / (HV / H);  // q/k head of value head h
     uint8_t* rec = a.ws + ((size_t)cid * HV + h) * kRecBytes;
 
-    // 1. fold.  Warp w owns tokens [4w, 4w+4), lane l channels [4l, 4l+4); all
+    // 1. fold.  Warp w owns tokens [2w, 2w+2), lane l channels [4l, 4l+4); all
     //    global loads of the warp are issued before any use.  Raw q, k, v stay
-    //    BF16 in shared memory, with the per-token norms; Gam by warp-blocked prefix.
+    //    BF16 in shared memory, with the per-token norms; Gam by warp-blocked
+    //    prefix (the running sum of a warp's last token is its total).  The
+    //    previous unit's output staging (L/R and A2 regions) may still be read
+    //    by its bulk stores: the fold writes none of it.
     {
       constexpr int kTpw = kChunk / kTxWarps;  // tokens per warp
-      float* tot = reinterpret_cast<float*>(sb + kTxL);  // [kTxWarps][128] warp totals
       const int c = lane * 4;
       uint2 qr[kTpw], kr[kTpw], vr[kTpw], ar[kTpw];
       float br[kTpw];
@@ -399,13 +408,13 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
         run = make_float4(run.x + g4.x, run.y + g4.y, run.z + g4.z, run.w + g4.w);
         f4(GM + t * kLd + c) = run;
       }
-      f4(tot + warp * K + c) = run;
       __syncthreads();
       float4 pre = make_float4(0.f, 0.f, 0.f, 0.f);
       for (int w = 0; w < warp; ++w) {
-        const float4 x = f4(tot + w * K + c);
+        const float4 x = f4(GM + (w * kTpw + kTpw - 1) * kLd + c);
         pre = make_float4(pre.x + x.x, pre.y + x.y, pre.z + x.z, pre.w + x.w);
       }
+      __syncthreads();  // every warp has read the totals it needs before any row changes
 #pragma unroll
       for (int u = 0; u < kTpw; ++u) {
         float4& gg = f4(GM + (warp * kTpw + u) * kLd + c);
@@ -707,7 +716,8 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
     //    P W (rows 64-127), 128-255 Util | P Util.  M2 has finished reading its
     //    operands, so [W; Q'] is staged in the A2 region and Util | P Util in the
     //    L/R region, laid out as in the workspace record, and each goes out as
-    //    one bulk copy.
+    //    one bulk copy.  [W; Q'] is split into BF16 hi (A2 region) and lo
+    //    (lower L/R region).
     {
       constexpr int kGroups = kTxWarps / 4, kCols = 256 / kGroups;
       static_assert(kCols == 32, "two 16-column TMEM loads per thread");
@@ -740,12 +750,8 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
             }
           }
 #pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            const float* xs = d + half * 8;
-            const uint4 pk = make_uint4(pack_bf16x2(xs[0], xs[1]), pack_bf16x2(xs[2], xs[3]),
-                                        pack_bf16x2(xs[4], xs[5]), pack_bf16x2(xs[6], xs[7]));
-            *reinterpret_cast<uint4*>(A2h + tc::sw128_offset(row, c0 + half * 8, 128)) = pk;
-          }
+          for (int half = 0; half < 2; ++half)
+            st_split8(A2h, sb + kTxA1L, tc::sw128_offset(row, c0 + half * 8, 128), d + half * 8);
         } else {
           float* base = reinterpret_cast<float*>(sb + kTxUst + (upper ? 0u : kRecOi - kRecU));
 #pragma unroll
@@ -764,6 +770,7 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
     if (tid == 0) {
       static_assert(kRecOi == kRecU + kChunk * kHeadDim * 4, "Util and P Util are contiguous");
       tc::bulk_s2g(rec + kRecA1, A2h, 128 * 128 * 2);
+      tc::bulk_s2g(rec + kRecA1L, sb + kTxA1L, 128 * 128 * 2);
       tc::bulk_s2g(rec + kRecU, sb + kTxUst, 2 * kChunk * kHeadDim * 4);
       tc::bulk_commit();  // awaited at the end of the next unit's fold, or on exit
     }
@@ -778,30 +785,30 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
 // Sequential state pass on tcgen05.
 
 // Shared-memory layout of the state pass (bytes from a 1024-aligned base).
-constexpr uint32_t kStA1 = 0;
-constexpr uint32_t kStKTh = kStA1 + 128 * 128 * 2;
+// One stage holds a chunk's operand tiles; Util and P Util go straight from
+// the record into registers.
+constexpr uint32_t kStA1 = 0;                         // [W; Q'] hi
+constexpr uint32_t kStA1L = kStA1 + 128 * 128 * 2;    // [W; Q'] lo
+constexpr uint32_t kStKTh = kStA1L + 128 * 128 * 2;
 constexpr uint32_t kStKTl = kStKTh + 128 * 64 * 2;
-constexpr uint32_t kStU = kStKTl + 128 * 64 * 2;
-constexpr uint32_t kStOi = kStU + kSliceBytes;
-constexpr uint32_t kStGam = kStOi + kSliceBytes;
+constexpr uint32_t kStGam = kStKTl + 128 * 64 * 2;
 constexpr uint32_t kStageBytes = ((kStGam + kHeadDim * 4 + 1023) / 1024) * 1024;
 constexpr uint32_t kSmS = 2 * kStageBytes;         // [S_hi; S_lo]^T: 64 x 128 (rows j, 32 + j)
 constexpr uint32_t kSmSBytes = 2 * kVs * kHeadDim * 2;
 constexpr uint32_t kSmU = kSmS + kSmSBytes;        // [U_hi; U_lo]^T: 64 x 64
 constexpr uint32_t kSmUBytes = 2 * kVs * kChunk * 2;
 constexpr uint32_t kPassSmem = kSmU + kSmUBytes + 1024;  // + alignment slack
-constexpr uint32_t kStageTx = 128 * 128 * 2 + 2 * 128 * 64 * 2 + 2 * kSliceBytes + kHeadDim * 4;
+constexpr uint32_t kStageTx = 2 * 128 * 128 * 2 + 2 * 128 * 64 * 2 + kHeadDim * 4;
 constexpr uint32_t kTmemCols = 128;  // D1: cols 0-63 (hi | lo), D2: cols 64-127
-static_assert(kStKTl == kStKTh + 128 * 64 * 2 && kRecKTl == kRecKTh + 128 * 64 * 2,
-              "Khat^T hi and lo are copied as one block");
+static_assert(kStA1L == kStA1 + 128 * 128 * 2 && kRecA1L == kRecA1 + 128 * 128 * 2 &&
+                  kStKTh == kStA1L + 128 * 128 * 2 && kRecKTh == kRecA1L + 128 * 128 * 2 &&
+                  kStKTl == kStKTh + 128 * 64 * 2 && kRecKTl == kRecKTh + 128 * 64 * 2,
+              "[W; Q'] hi, lo and Khat^T hi, lo are copied as one block");
+static_assert(kPassSmem <= 232448, "shared memory");
 
-__device__ __forceinline__ void issue_stage_loads(uint8_t* stage, const uint8_t* rec, int slice,
-                                                  uint64_t* bar) {
+__device__ __forceinline__ void issue_stage_loads(uint8_t* stage, const uint8_t* rec, uint64_t* bar) {
   tc::mbar_expect_tx(bar, kStageTx);
-  tc::bulk_g2s(stage + kStA1, rec + kRecA1, 128 * 128 * 2, bar);
-  tc::bulk_g2s(stage + kStKTh, rec + kRecKTh, 2 * 128 * 64 * 2, bar);
-  tc::bulk_g2s(stage + kStU, rec + kRecU + slice * kSliceBytes, kSliceBytes, bar);
-  tc::bulk_g2s(stage + kStOi, rec + kRecOi + slice * kSliceBytes, kSliceBytes, bar);
+  tc::bulk_g2s(stage + kStA1, rec + kRecA1, 2 * 128 * 128 * 2 + 2 * 128 * 64 * 2, bar);
   tc::bulk_g2s(stage + kStGam, rec + kRecGam, kHeadDim * 4, bar);
 }
 
@@ -838,6 +845,8 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
         if (slice == 0 && h == 0) set_error(a.err_flag, KDA_DEVERR_SLOT);
       } else if (slot == -1) {
         s_state = 1;
+      } else if (a.seq_flags && a.seq_flags[n]) {
+        s_state = 2;  // given log-decay out of range: flagged by decay_check_kernel
       }
       int64_t base = 0;
       for (int m = 0; m < n; ++m)
@@ -876,8 +885,7 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
   int consumed = 0;  // chunks whose loads have landed
   if (tid == 32) {
     for (; issued < 2 && issued < nch; ++issued)
-      issue_stage_loads(smb + issued * kStageBytes, ws_head + issued * rec_stride, slice,
-                        &full_bar[issued]);
+      issue_stage_loads(smb + issued * kStageBytes, ws_head + issued * rec_stride, &full_bar[issued]);
   }
   if (warp == 0) tc::tmem_alloc(&tmem_base, kTmemCols);
 
@@ -916,25 +924,49 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
     const int64_t cid = s_cbase + p0 + ci;
     const int64_t tc0 = t0 + (int64_t)(p0 + ci) * kChunk;
     const int len = (int)(t1 - tc0 < kChunk ? t1 - tc0 : kChunk);
+    // this thread's Util (rows 0-63) or P Util (rows 64-127) values: read
+    // from the record into registers while the stage lands and D1 runs
+    float4 xu0, xu1;
+    {
+      const float4* src = reinterpret_cast<const float4*>(ws_head + (size_t)ci * rec_stride +
+                                                          (quad < 2 ? kRecU : kRecOi) +
+                                                          slice * kSliceBytes) +
+                          (j0 / 4) * kChunk + (row & (kChunk - 1));
+      xu0 = __ldcg(src);
+      xu1 = __ldcg(src + kChunk);
+    }
     if (a.intermediate) {
-      float* dst = a.intermediate + ((size_t)cid * HV + h) * V * K;
+      if (cid < a.inter_chunks) {
+        float* dst = a.intermediate + ((size_t)cid * HV + h) * V * K;
 #pragma unroll
-      for (int jj = 0; jj < kColsPerThread; ++jj) dst[(size_t)(v0 + j0 + jj) * K + c] = S[jj];
+        for (int jj = 0; jj < kColsPerThread; ++jj) dst[(size_t)(v0 + j0 + jj) * K + c] = S[jj];
+      } else if (tid == 0 && slice == 0) {
+        set_error(a.err_flag, KDA_DEVERR_INTERMEDIATE);
+      }
     }
     if (tc::mbar_wait(&full_bar[sidx], (ci >> 1) & 1))
       consumed = ci + 1;
     else
       s_abort = 1;
-    // D1 = [W; Q'] [S_hi | S_lo]: eight K=16 steps, N = 64
+    // D1 = [W; Q']_hi [S_hi | S_lo] + [W; Q']_lo S_hi: eight K=16 steps at
+    // N = 64, then eight at N = 32 into the S_lo half
     if (tid == 0 && !s_abort) {
       tc::tc_fence_after();
-      const uint32_t a1 = tc::smem_u32(stage + kStA1), sb2 = tc::smem_u32(S2);
+      const uint32_t a1 = tc::smem_u32(stage + kStA1), a1l = tc::smem_u32(stage + kStA1L);
+      const uint32_t sb2 = tc::smem_u32(S2);
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
         const uint32_t koff = (k & 3) * 32;
         const uint64_t ad = tc::sw128_desc(a1 + (k >> 2) * (128 * 128) + koff);
         const uint64_t bd = tc::sw128_desc(sb2 + (k >> 2) * (2 * kVs * 128) + koff);
         tc::mma_bf16(d1, ad, bd, idesc2, k > 0);
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const uint32_t koff = (k & 3) * 32;
+        const uint64_t ad = tc::sw128_desc(a1l + (k >> 2) * (128 * 128) + koff);
+        const uint64_t bd = tc::sw128_desc(sb2 + (k >> 2) * (2 * kVs * 128) + koff);
+        tc::mma_bf16(d1 + kVs, ad, bd, idesc1, true);
       }
       tc::mma_commit(&mma_bar);
     }
@@ -948,9 +980,7 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
       tc::tmem_ld8(d1 + lane_addr + kVs, dl);
       if (quad < 2) {  // rows 0..63: U = Util - W S  ->  [U_hi; U_lo]^T operand
         const int t = row;
-        const float4* ut = reinterpret_cast<const float4*>(stage + kStU) + (j0 / 4) * kChunk + t;
-        const float4 u0 = ut[0], u1 = ut[kChunk];
-        const float uu[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+        const float uu[8] = {xu0.x, xu0.y, xu0.z, xu0.w, xu1.x, xu1.y, xu1.z, xu1.w};
 #pragma unroll
         for (int jj = 0; jj < kColsPerThread; ++jj) {
           uint16_t hi, lo;
@@ -959,10 +989,7 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
           *reinterpret_cast<uint16_t*>(U2 + tc::sw128_offset(kVs + j0 + jj, t, 2 * kVs)) = lo;
         }
       } else {  // rows 64..127: O = scale (Q' S + P Util)
-        const int t = row - kChunk;
-        const float4* oi = reinterpret_cast<const float4*>(stage + kStOi) + (j0 / 4) * kChunk + t;
-        const float4 o0 = oi[0], o1 = oi[kChunk];
-        const float oo[8] = {o0.x, o0.y, o0.z, o0.w, o1.x, o1.y, o1.z, o1.w};
+        const float oo[8] = {xu0.x, xu0.y, xu0.z, xu0.w, xu1.x, xu1.y, xu1.z, xu1.w};
         float x[8];
 #pragma unroll
         for (int jj = 0; jj < kColsPerThread; ++jj) x[jj] = scale * (dh[jj] + dl[jj] + oo[jj]);
@@ -1006,7 +1033,7 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
     if (s_abort) break;
     if (tid == 32 && ci + 2 < nch) {  // not the MMA-issuing thread
       tc::fence_async_smem();
-      issue_stage_loads(stage, ws_head + (size_t)(ci + 2) * rec_stride, slice, &full_bar[sidx]);
+      issue_stage_loads(stage, ws_head + (size_t)(ci + 2) * rec_stride, &full_bar[sidx]);
       issued = ci + 3;
     }
   }
@@ -1026,9 +1053,53 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
   if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
 }
 
+// Given log-decays (A_log absent): the chunk transform's decay windows need
+// every per-token log-decay in [kMinLogDecay, 0].  Each thread checks eight
+// consecutive values of the real token rows (padding rows are never read); a
+// value outside the range, or NaN, flags its sequence, which the transform and
+// the state pass then skip, so that its pool slot is left as it was.
+template <bool F16>
+__global__ void __launch_bounds__(256) decay_check_kernel(const PrefillArgs a, int32_t* flags) {
+  const int64_t words_per_row = (int64_t)a.HV * kHeadDim / 8;
+  const int64_t words = a.total_tokens * words_per_row;
+  const uint4* g = reinterpret_cast<const uint4*>(a.g);
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < words;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const uint4 w = __ldg(g + i);
+    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+    bool bad = false;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float lo = in16_to_float<F16>((uint16_t)(u[e] & 0xffffu));
+      const float hi = in16_to_float<F16>((uint16_t)(u[e] >> 16));
+      bad |= !(lo >= kMinLogDecay && lo <= 0.f) || !(hi >= kMinLogDecay && hi <= 0.f);
+    }
+    if (bad) {
+      const int64_t row = i / words_per_row;
+      int n = 0;
+      if (a.cu_seqlens) {  // last sequence whose start is <= row (binary search)
+        int lo_n = 0, hi_n = a.num_seqs - 1;
+        while (lo_n < hi_n) {
+          const int mid = (lo_n + hi_n + 1) / 2;
+          if ((int64_t)a.cu_seqlens[mid] <= row) lo_n = mid; else hi_n = mid - 1;
+        }
+        n = lo_n;
+      } else {
+        n = (int)(row / (a.total_tokens / a.num_seqs));
+      }
+      flags[n] = 1;
+      set_error(a.err_flag, KDA_DEVERR_DECAY);
+    }
+  }
+}
+
 int64_t max_chunks(int num_seqs, int64_t total_tokens) {
   return total_tokens / kChunk + num_seqs;
 }
+
+// Workspace: the per-sequence flags of the given-decay check, then the
+// (chunk, head) records, 256-byte aligned.
+size_t flags_bytes(int num_seqs) { return ((size_t)num_seqs * 4 + 255) & ~(size_t)255; }
 
 constexpr int kMaxDevices = 64;
 bool g_attributes_set[kMaxDevices] = {};
@@ -1114,7 +1185,10 @@ using namespace kda;
 
 extern "C" size_t kda_prefill_workspace_size(kda_dims dims, int num_seqs, int64_t total_tokens) {
   if (num_seqs < 0 || total_tokens < 0 || dims.HV <= 0) return 0;
-  return (size_t)max_chunks(num_seqs, total_tokens) * dims.HV * kRecBytes;
+  // cu_seqlens are int32: larger calls are refused, and SIZE_MAX makes every
+  // capacity check fail instead of wrapping
+  if (total_tokens > INT32_MAX || dims.HV > (1 << 16)) return SIZE_MAX;
+  return flags_bytes(num_seqs) + (size_t)max_chunks(num_seqs, total_tokens) * dims.HV * kRecBytes;
 }
 
 extern "C" kda_status kda_prefill(kda_dims dims, kda_gate gate, const kda_bf16* q,
@@ -1122,12 +1196,14 @@ extern "C" kda_status kda_prefill(kda_dims dims, kda_gate gate, const kda_bf16* 
                                   const kda_bf16* beta, int64_t gb_rows, float* state_pool,
                                   int pool_slots, const int32_t* state_idx,
                                   const int32_t* cu_seqlens, int num_seqs, int64_t total_tokens,
-                                  kda_bf16* o, float* intermediate, void* workspace,
-                                  size_t workspace_bytes, int32_t* err_flag, void* stream) {
+                                  kda_bf16* o, float* intermediate, int64_t intermediate_chunks,
+                                  void* workspace, size_t workspace_bytes, int32_t* err_flag,
+                                  void* stream) {
   kda_status s = check_dims(dims);
   if (s != KDA_OK) return s;
   if (!state_pool || !state_idx) return KDA_ERR_NULL_ARG;  // indexed pool required
   if (num_seqs < 1 || total_tokens < 0 || pool_slots < 0) return KDA_ERR_SHAPE;
+  if (total_tokens > INT32_MAX || (intermediate && intermediate_chunks < 0)) return KDA_ERR_SHAPE;
   if (gb_rows < total_tokens) return KDA_ERR_SHAPE;  // g/beta must cover every q token
   if (!cu_seqlens && total_tokens % num_seqs != 0) return KDA_ERR_SHAPE;
   if (total_tokens > 0 && (!q || !k || !v || !g || !beta || !o)) return KDA_ERR_NULL_ARG;
@@ -1158,7 +1234,8 @@ extern "C" kda_status kda_prefill(kda_dims dims, kda_gate gate, const kda_bf16* 
   args.total_tokens = total_tokens;
   args.o = o;
   args.intermediate = intermediate;
-  args.ws = static_cast<uint8_t*>(workspace);
+  args.inter_chunks = intermediate ? intermediate_chunks : 0;
+  args.ws = static_cast<uint8_t*>(workspace) + flags_bytes(num_seqs);
   args.err_flag = err_flag;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
@@ -1182,6 +1259,18 @@ extern "C" kda_status kda_prefill(kda_dims dims, kda_gate gate, const kda_bf16* 
     nseg = seq_nch / kSegmentMinChunks < kMaxSegments ? seq_nch / kSegmentMinChunks : kMaxSegments;
   }
   record_stage(0, st);
+  if (!gate.A_log && total_tokens > 0) {
+    // given log-decays: flag the sequences the chunk form cannot take
+    int32_t* flags = static_cast<int32_t*>(workspace);
+    if (cudaMemsetAsync(flags, 0, (size_t)num_seqs * 4, st) != cudaSuccess) return KDA_ERR_CUDA;
+    const int64_t words = total_tokens * dims.HV * kHeadDim / 8;
+    const int64_t want = (words + 255) / 256;
+    const unsigned blocks = (unsigned)(want < 8LL * g_num_sms[dev] ? want : 8LL * g_num_sms[dev]);
+    (dims.dtype == KDA_DTYPE_F16 ? decay_check_kernel<true> : decay_check_kernel<false>)
+        <<<blocks, 256, 0, st>>>(args, flags);
+    if ((s = launch_status()) != KDA_OK) return s;
+    args.seq_flags = flags;
+  }
   if (nseg <= 1) {
     if (chunks > 0) {
       args.tx_units = chunks * dims.HV;

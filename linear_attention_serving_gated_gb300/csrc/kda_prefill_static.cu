@@ -10,6 +10,8 @@
 // GPU that loads the library holds until the process exits.
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "../../include/kda.h"
 
 namespace {
@@ -22,17 +24,19 @@ static __device__ __align__(256) unsigned char g_prefill_scratch[kStaticScratchB
 // Device address of g_prefill_scratch on each device, looked up on the first
 // call made with that device current.  In host code the array's name is only
 // a host-side stand-in, so its device address must come from the runtime.
-void* g_scratch_ptr[kMaxDevices] = {};
+// Host threads making their first calls at once may each look it up; they
+// store the same address, and the atomics keep that well defined.
+std::atomic<void*> g_scratch_ptr[kMaxDevices] = {};
 
 kda_status scratch_for_current_device(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KDA_ERR_CUDA;
-  if (!g_scratch_ptr[dev]) {
-    void* p = nullptr;
+  void* p = g_scratch_ptr[dev].load(std::memory_order_relaxed);
+  if (!p) {
     if (cudaGetSymbolAddress(&p, g_prefill_scratch) != cudaSuccess || !p) return KDA_ERR_CUDA;
-    g_scratch_ptr[dev] = p;
+    g_scratch_ptr[dev].store(p, std::memory_order_relaxed);
   }
-  *out = g_scratch_ptr[dev];
+  *out = p;
   return KDA_OK;
 }
 
@@ -44,16 +48,18 @@ extern "C" kda_status kda_prefill_noalloc(kda_dims dims, kda_gate gate, const kd
                                           int pool_slots, const int32_t* state_idx,
                                           const int32_t* cu_seqlens, int num_seqs,
                                           int64_t total_tokens, kda_bf16* o, float* intermediate,
-                                          int32_t* err_flag, void* stream) {
+                                          int64_t intermediate_chunks, int32_t* err_flag,
+                                          void* stream) {
   // Reject work that does not fit the static scratch before touching anything.
   if (kda_prefill_workspace_size(dims, num_seqs, total_tokens) > kStaticScratchBytes)
     return KDA_ERR_WORKSPACE;
   void* scratch = nullptr;
   const kda_status s = scratch_for_current_device(&scratch);
   if (s != KDA_OK) return s;
-  // The prefill writes every workspace byte it reads within the same call, so
-  // nothing left in the array by an earlier call needs clearing.
+  // The prefill clears the flags it uses and writes every other workspace
+  // byte it reads within the same call, so nothing left in the array by an
+  // earlier call needs clearing here.
   return kda_prefill(dims, gate, q, k, v, g, beta, gb_rows, state_pool, pool_slots, state_idx,
-                     cu_seqlens, num_seqs, total_tokens, o, intermediate, scratch,
-                     kStaticScratchBytes, err_flag, stream);
+                     cu_seqlens, num_seqs, total_tokens, o, intermediate, intermediate_chunks,
+                     scratch, kStaticScratchBytes, err_flag, stream);
 }

@@ -159,7 +159,8 @@ __global__ void __launch_bounds__(128, kMinCtasPerSm<MODE>) recurrent_kernel(con
   // its element offset within the row is fixed.  Value head h reads q/k head
   // h / G.
   const int raw_m = (tid >> 4) & 3, raw_piece = (tid & 15) * 8;
-  const int raw_off = raw_piece + (raw_m == 0 ? (h / args.G) * kHeadDim
+  const int raw_off = MODE == kCommitReplay ? 0  // reads no token rows
+                    : raw_piece + (raw_m == 0 ? (h / args.G) * kHeadDim
                                  : raw_m == 1 ? (args.H + h / args.G) * kHeadDim
                                  : raw_m == 2 ? (2 * args.H + h) * kHeadDim
                                               : h * kHeadDim);
@@ -587,6 +588,8 @@ extern "C" kda_status kda_commit_replay(kda_dims dims, const float* ring, int B,
   StepArgs args{};
   args.H = dims.H;
   args.HV = dims.HV;
+  args.G = dims.HV / dims.H;  // check_dims: HV is a positive multiple of H
+  args.dtype = dims.dtype;
   args.B = B;
   args.T = T;
   args.pool = state_pool;

@@ -30,6 +30,8 @@ KDA_DEVERR_PARENT = 2
 KDA_DEVERR_SEQLENS = 4
 KDA_DEVERR_ACCEPTED = 8
 KDA_DEVERR_TIMEOUT = 16
+KDA_DEVERR_INTERMEDIATE = 32
+KDA_DEVERR_DECAY = 64
 
 CHUNK = 64
 
@@ -59,7 +61,7 @@ EXPORTS = ("kda_status_string", "kda_prefill_workspace_size", "kda_prefill", "kd
            "kda_prefill_noalloc", "kda_replay_ring_bytes", "kda_verify_chain_replay",
            "kda_commit_replay")
 
-PREFILL_STATIC_SCRATCH_BYTES = 128 << 20
+PREFILL_STATIC_SCRATCH_BYTES = 128 << 20  # KDA_PREFILL_STATIC_SCRATCH_BYTES in include/kda.h
 
 _lib = None
 
@@ -78,7 +80,7 @@ def load(path: str = LIB_PATH):
         lib.kda_prefill_workspace_size.argtypes = [kda_dims, i32, i64]
         lib.kda_prefill.restype = i32
         lib.kda_prefill.argtypes = [kda_dims, kda_gate, vp, vp, vp, vp, vp, i64, vp, i32, vp, vp, i32,
-                                    i64, vp, vp, vp, sz, vp, vp]
+                                    i64, vp, vp, i64, vp, sz, vp, vp]
         lib.kda_decode_packed.restype = i32
         lib.kda_decode_packed.argtypes = [kda_dims, kda_gate, vp, i64, vp, vp, i32, vp, i32, vp, vp,
                                           vp, vp]
@@ -92,7 +94,7 @@ def load(path: str = LIB_PATH):
         lib.kda_commit.argtypes = [kda_dims, vp, i32, i32, vp, vp, i32, vp, vp, vp]
         lib.kda_prefill_noalloc.restype = i32
         lib.kda_prefill_noalloc.argtypes = [kda_dims, kda_gate, vp, vp, vp, vp, vp, i64, vp, i32, vp,
-                                            vp, i32, i64, vp, vp, vp, vp]
+                                            vp, i32, i64, vp, vp, i64, vp, vp]
         lib.kda_replay_ring_bytes.restype = sz
         lib.kda_replay_ring_bytes.argtypes = [kda_dims, i32, i32]
         lib.kda_verify_chain_replay.restype = i32
@@ -207,6 +209,21 @@ def kda_prefill_workspace_size(d: kda_dims, num_seqs: int, total_tokens: int) ->
     return int(load().kda_prefill_workspace_size(d, int(num_seqs), int(total_tokens)))
 
 
+def _intermediate_chunks(d, intermediate):
+    """Chunk records an intermediate-state buffer holds: it must be a dense
+    [chunks, HV, V, K] FP32 tensor.  The library writes only that many (the
+    chunk count follows cu_seqlens, which is on the device) and flags the
+    rest."""
+    if intermediate is None:
+        return 0
+    if intermediate.dtype != torch.float32 or intermediate.dim() != 4 or \
+            tuple(intermediate.shape[1:]) != (d.HV, d.V, d.K):
+        raise ValueError(f"intermediate must be float32 [chunks, HV, V, K] = [*, {d.HV}, {d.V}, {d.K}] "
+                         f"(got {intermediate.dtype} {tuple(intermediate.shape)})")
+    _at_least(intermediate, 0, "intermediate", "[chunks, HV, V, K]")
+    return int(intermediate.shape[0])
+
+
 def _prefill_shapes(d, q, k, v, g, beta, state_pool, state_idx, cu_seqlens, num_seqs, o):
     """Every element the prefill kernels touch for T = q.shape[0] tokens and
     gb_rows = g.shape[0] gate rows must exist (the library sees pointers)."""
@@ -233,14 +250,14 @@ def kda_prefill(d, gate: Gate, q, k, v, g, beta, state_pool, state_idx, cu_seqle
     T = q.shape[0]
     gb_rows = g.shape[0]
     _prefill_shapes(d, q, k, v, g, beta, state_pool, state_idx, cu_seqlens, num_seqs, o)
-    _at_least(intermediate, 0, "intermediate", "[chunks, HV, V, K]")  # size set by cu_seqlens on the device
+    inter_chunks = _intermediate_chunks(d, intermediate)
     if workspace is None:
         need = kda_prefill_workspace_size(d, num_seqs, T)
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
     st = load().kda_prefill(
         d, gate.c(), _in16(d, q, "q"), _in16(d, k, "k"), _in16(d, v, "v"), _in16(d, g, "g"), _in16(d, beta, "beta"),
         int(gb_rows), _p(state_pool), int(state_pool.shape[0]), _p(state_idx), _p(cu_seqlens),
-        int(num_seqs), int(T), _in16(d, o, "o"), _p(intermediate), _p(workspace),
+        int(num_seqs), int(T), _in16(d, o, "o"), _p(intermediate), inter_chunks, _p(workspace),
         int(workspace.numel() * workspace.element_size()), _p(err_flag), _stream(stream))
     _check(st, "kda_prefill")
 
@@ -250,12 +267,12 @@ def kda_prefill_noalloc(d, gate: Gate, q, k, v, g, beta, state_pool, state_idx, 
     """kda_prefill with the library's built-in static scratch (see kda.h): for
     callers that cannot allocate device memory."""
     _prefill_shapes(d, q, k, v, g, beta, state_pool, state_idx, cu_seqlens, num_seqs, o)
-    _at_least(intermediate, 0, "intermediate", "[chunks, HV, V, K]")  # size set by cu_seqlens on the device
+    inter_chunks = _intermediate_chunks(d, intermediate)
     st = load().kda_prefill_noalloc(
         d, gate.c(), _in16(d, q, "q"), _in16(d, k, "k"), _in16(d, v, "v"), _in16(d, g, "g"), _in16(d, beta, "beta"),
         int(g.shape[0]), _p(state_pool), int(state_pool.shape[0]), _p(state_idx), _p(cu_seqlens),
-        int(num_seqs), int(q.shape[0]), _in16(d, o, "o"), _p(intermediate), _p(err_flag),
-        _stream(stream))
+        int(num_seqs), int(q.shape[0]), _in16(d, o, "o"), _p(intermediate), inter_chunks,
+        _p(err_flag), _stream(stream))
     _check(st, "kda_prefill_noalloc")
 
 

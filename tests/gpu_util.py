@@ -69,15 +69,19 @@ def assert_s_close(s_gpu, s_ref, what="state"):
     return err / max(rms(s_ref), 1e-300)
 
 
-def gates(d, lower_bound=-5.0, beta_is_raw=True, use_qk_l2norm=True, scale=None, H=None, K=128, HV=None):
+def gates(d, lower_bound=-5.0, beta_is_raw=True, use_qk_l2norm=True, scale=None, H=None, K=128, HV=None,
+          given_decay=False):
     """Matching oracle and device gate descriptions from seeded inputs.  HV
     value heads (default: the gate parameters' head count), H q/k heads
-    (default HV)."""
+    (default HV).  given_decay: no A_log / dt_bias, the gate input is the
+    log-decay itself."""
     HV = HV if HV is not None else d["A_log"].shape[0]
     H = H if H is not None else HV
     scale = scale if scale is not None else K ** -0.5
-    og = ko.Gate(H, K, K, HV=HV, A_log=d["A_log"], dt_bias=d["dt_bias"], lower_bound=lower_bound,
+    A_log, dt_bias = (None, None) if given_decay else (d["A_log"], d["dt_bias"])
+    og = ko.Gate(H, K, K, HV=HV, A_log=A_log, dt_bias=dt_bias, lower_bound=lower_bound,
                  beta_is_raw=beta_is_raw, use_qk_l2norm=use_qk_l2norm, scale=scale)
-    gg = kda.Gate(A_log=dev(d["A_log"]), dt_bias=dev(d["dt_bias"]), lower_bound=lower_bound,
-                  beta_is_raw=beta_is_raw, use_qk_l2norm=use_qk_l2norm, scale=scale)
+    gg = kda.Gate(A_log=None if given_decay else dev(A_log), dt_bias=None if given_decay else dev(dt_bias),
+                  lower_bound=lower_bound, beta_is_raw=beta_is_raw, use_qk_l2norm=use_qk_l2norm,
+                  scale=scale)
     return og, gg

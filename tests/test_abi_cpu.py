@@ -43,12 +43,17 @@ def test_status_strings(lib):
     assert "workspace" in kda.status_string(kda.KDA_ERR_WORKSPACE)
 
 
-def test_workspace_size_scales_with_chunks(lib):
-    d = kda.dims(16)
-    one = kda.kda_prefill_workspace_size(d, 1, 64)
-    assert one > 0
-    assert kda.kda_prefill_workspace_size(d, 1, 4096) == one * (4096 // 64 + 1) // 2
-    assert kda.kda_prefill_workspace_size(d, 8, 32768) >= kda.kda_prefill_workspace_size(d, 1, 32768)
+REC_BYTES = 164352  # one (chunk, head) record, as include/kda.h states
+
+
+def test_workspace_size_formula(lib):
+    """align256(4 num_seqs) + (T / 64 + num_seqs) HV 164352 bytes, as kda.h
+    states; sizes past int32 tokens give SIZE_MAX so that no check passes."""
+    for HV, n, T in ((16, 1, 64), (16, 1, 4096), (16, 8, 32768), (4, 3, 100), (2, 70, 0)):
+        want = ((4 * n + 255) // 256) * 256 + (T // 64 + n) * HV * REC_BYTES
+        assert kda.kda_prefill_workspace_size(kda.dims(HV), n, T) == want
+    assert kda.kda_prefill_workspace_size(kda.dims(16), 1, 2 ** 31) == 2 ** 64 - 1
+    assert kda.kda_prefill_workspace_size(kda.dims(16), 1, 2 ** 31 - 1) < 2 ** 63
 
 
 def _gate(A_log=None, lb=-5.0):
@@ -56,10 +61,10 @@ def _gate(A_log=None, lb=-5.0):
 
 
 def _prefill(lib, dims=None, gate=None, pool=DUMMY, idx=DUMMY, gb_rows=64, T=64, num_seqs=1,
-             ws=DUMMY, ws_bytes=1 << 40, q=DUMMY):
+             ws=DUMMY, ws_bytes=1 << 40, q=DUMMY, inter=None, inter_chunks=0):
     return lib.kda_prefill(dims or kda.dims(4), gate or _gate(), q, DUMMY, DUMMY, DUMMY, DUMMY,
-                           gb_rows, pool, 4, idx, None, num_seqs, T, DUMMY, None, ws, ws_bytes,
-                           None, None)
+                           gb_rows, pool, 4, idx, None, num_seqs, T, DUMMY, inter, inter_chunks, ws,
+                           ws_bytes, None, None)
 
 
 def test_prefill_host_errors(lib):
@@ -88,6 +93,10 @@ def test_prefill_host_errors(lib):
     assert _prefill(lib, ws_bytes=16) == kda.KDA_ERR_WORKSPACE
     assert _prefill(lib, ws=ctypes.c_void_p(0x10010)) == kda.KDA_ERR_ALIGNMENT
     assert _prefill(lib, q=ctypes.c_void_p(0x10002)) == kda.KDA_ERR_ALIGNMENT
+    # cu_seqlens are int32: more tokens than that is a shape error
+    assert _prefill(lib, T=2 ** 31, gb_rows=2 ** 31) == kda.KDA_ERR_SHAPE
+    # a chunk-start state buffer with a negative capacity
+    assert _prefill(lib, inter=DUMMY, inter_chunks=-1) == kda.KDA_ERR_SHAPE
 
 
 def test_decode_host_errors(lib):

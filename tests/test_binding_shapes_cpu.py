@@ -137,13 +137,23 @@ def test_replay_ring_and_commits():
         kda.kda_commit(d, torch.zeros((B, T, H, K, K)), B, T, idx(B), pool(), idx(B - 1))
 
 
-def prefill(T=100, o=None, n=1, cu_len=None, idx_len=None):
+def prefill(T=100, o=None, n=1, cu_len=None, idx_len=None, inter=None):
     q = torch.zeros((T, H, K), dtype=BF)
     kda.kda_prefill(kda.dims(H), kda.Gate(), q, q.clone(), q.clone(), torch.zeros((T, H, K), dtype=BF),
                     torch.zeros((T, H), dtype=BF), pool(), idx(n if idx_len is None else idx_len),
                     torch.zeros(n + 1 if cu_len is None else cu_len, dtype=torch.int32), n,
-                    torch.zeros((T, H, K), dtype=BF) if o is None else o,
+                    torch.zeros((T, H, K), dtype=BF) if o is None else o, inter,
                     workspace=torch.zeros(16, dtype=torch.uint8))
+
+
+def test_prefill_intermediate_is_a_stack_of_state_records():
+    """The chunk-start state buffer's record count is passed to the library
+    (which writes no more than that many), so it must be a dense float32
+    [chunks, HV, V, K] tensor."""
+    for bad in (torch.zeros((2, H, K, K - 1)), torch.zeros((2, H, K, K), dtype=torch.float64),
+                torch.zeros((2 * H * K * K,)), torch.zeros((2, K, K, H)).permute(0, 3, 1, 2)):
+        with pytest.raises(ValueError, match="intermediate must be"):
+            prefill(inter=bad)
 
 
 def test_prefill_shapes():
