@@ -192,19 +192,18 @@ constexpr uint32_t kTxB2 = 0;                         // B2 hi, lo: 256 x 64 eac
 constexpr uint32_t kTxA1L = 0;                         // [W; Q'] lo output staging (lower L/R)
 constexpr uint32_t kTxUst = 32 * 1024;                // Util | P Util output staging (upper L/R)
 constexpr uint32_t kTxAf = 0;                         // A FP32 [64][kLdT] (reuses L/R)
-constexpr uint32_t kTxPf = kTxAf + kChunk * kLdT * 4;  // P FP32 (reuses L/R)
 constexpr uint32_t kTxA2 = kTxR + 2 * 64 * 128 * 2;   // A2 hi, lo: 128 x 64 each
 constexpr uint32_t kTxQ = kTxA2 + 2 * 128 * 64 * 2;   // raw q BF16 [64][kLdB]
 constexpr uint32_t kTxK = kTxQ + kChunk * kLdB * 2;   // raw k
 constexpr uint32_t kTxV = kTxK + kChunk * kLdB * 2;   // raw v
 constexpr uint32_t kTxG = kTxV + kChunk * kLdB * 2;   // Gam FP32 [64][kLd]
-constexpr uint32_t kTxTf = kTxPf + kChunk * kLdT * 4;  // (I+A)^-1 FP32 [64][kLdT] (reuses L/R)
+constexpr uint32_t kTxTf = kTxAf + kChunk * kLdT * 4;  // (I+A)^-1 FP32 [64][kLdT] (reuses L/R)
 constexpr uint32_t kTxMisc = kTxG + kChunk * kLd * 4;  // rq, rk, beta [64] each + scratch [1536]
 constexpr uint32_t kTxEnd = kTxMisc + (3 * kChunk + 1536) * 4;
 constexpr uint32_t kTransformTcSmem = kTxEnd + 1024;
 constexpr uint32_t kTxTmemCols = 256;
 static_assert(2 * 256 * 64 * 2 <= kTxA2, "B2 fits in the L/R region");
-static_assert(kTxTf + kChunk * kLdT * 4 <= kTxA2, "A, P and (I+A)^-1 fit in the L/R region");
+static_assert(kTxTf + kChunk * kLdT * 4 <= kTxR, "A and (I+A)^-1 stay below X in the R region");
 static_assert(kTxA1L + 128 * 128 * 2 <= kTxUst, "[W; Q'] lo staging stays below Util | P Util");
 static_assert(kTxUst + 2 * kChunk * kHeadDim * 4 <= kTxA2, "output staging fits the L/R region");
 static_assert(kTxQ % 16 == 0 && kTxK % 16 == 0 && kTxV % 16 == 0 && kTxG % 16 == 0 &&
@@ -277,9 +276,9 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
   extern __shared__ uint8_t smraw[];
   __shared__ uint64_t mma_bar;
   __shared__ uint32_t tmem_base;
-  __shared__ ChunkLoc loc, s_pf;
-  __shared__ int64_t s_cid;
-  __shared__ int skip, s_abort, s_ok, s_h, s_pf_h;
+  __shared__ ChunkLoc loc, s_nloc;
+  __shared__ int64_t s_cid, s_ncid;
+  __shared__ int skip, s_abort, s_ok, s_h, s_nh, s_nskip, s_nvalid;
 
   uint8_t* sb = smraw + ((1024u - (tc::smem_u32(smraw) & 1023u)) & 1023u);
   uint8_t* Lt = sb + kTxL;  // M1 left operand, TF32 128 x 128
@@ -294,7 +293,6 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
   uint8_t* Vs = sb + kTxV;
   float* GM = reinterpret_cast<float*>(sb + kTxG);
   float* Af = reinterpret_cast<float*>(sb + kTxAf);
-  float* Pf = reinterpret_cast<float*>(sb + kTxPf);
   float* Tf = reinterpret_cast<float*>(sb + kTxTf);
   float* rq = reinterpret_cast<float*>(sb + kTxMisc);
   float* rk = rq + kChunk;
@@ -304,6 +302,7 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) {
     s_abort = 0;
+    s_nvalid = 0;
     s_ok = seqlens_valid(a);
     if (!s_ok && blockIdx.x == 0) set_error(a.err_flag, KDA_DEVERR_SEQLENS);
     tc::mbar_init(&mma_bar, 1);
@@ -315,36 +314,37 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
   tc::tc_fence_after();
   const uint32_t tmem = tmem_base;
   uint32_t phase = 0;
+  // Unit descriptor (chunk location, head, whether it is skipped).  The next
+  // unit's is worked out by warp 1 while the tensor core runs this unit's M2
+  // product, together with an L2 prefetch of its rows, so that the slot lookup
+  // and the row loads are off the per-unit path; a unit whose predecessor was
+  // skipped (or the first) looks itself up.
+  auto describe = [&](int64_t uu, ChunkLoc* l, int64_t* cid, int* hh) -> int {
+    *l = unit_loc(a, uu, cid, hh);
+    if (l->n < 0) return 1;
+    const int slot = a.state_idx[l->n];
+    if (slot < 0 || slot >= a.pool_slots) return 1;    // padding / rejected sequence
+    if (a.seq_flags && a.seq_flags[l->n]) return 1;    // given decay out of range
+    return 0;
+  };
   for (int64_t u = blockIdx.x; s_ok && u < a.tx_units; u += gridDim.x) {
     __syncthreads();  // every thread is done with the previous unit's shared values
     if (tid == 0) {
-      int64_t cid;
-      int hh;
-      loc = unit_loc(a, u, &cid, &hh);
-      s_cid = cid;
-      s_h = hh;
-      skip = loc.n < 0;
-      if (!skip) {
-        const int slot = a.state_idx[loc.n];
-        if (slot < 0 || slot >= a.pool_slots) skip = 1;  // padding / rejected sequence
-        if (a.seq_flags && a.seq_flags[loc.n]) skip = 1;  // given decay out of range
+      if (s_nvalid) {
+        loc = s_nloc;
+        s_cid = s_ncid;
+        s_h = s_nh;
+        skip = s_nskip;
+      } else {
+        int64_t cid;
+        int hh;
+        skip = describe(u, &loc, &cid, &hh);
+        s_cid = cid;
+        s_h = hh;
       }
-      s_pf = u + gridDim.x < a.tx_units ? unit_loc(a, u + gridDim.x, &cid, &hh) : ChunkLoc{-1, 0, 0};
-      s_pf_h = hh;
+      s_nvalid = 0;
     }
     __syncthreads();
-    if (tid < 512 && s_pf.n >= 0) {  // next unit's rows -> L2: 4 tensors x 64 tokens x 2 lines
-      const int tensor = tid >> 7, tok = (tid >> 1) & 63, part = tid & 1;
-      if (tok < s_pf.len) {
-        const int64_t row = s_pf.t0 + tok;
-        const int hk = s_pf_h / (a.HV / a.H);  // q/k head of the value head
-        const kda_bf16* base = tensor == 0 ? a.q + (row * a.H + hk) * kHeadDim
-                             : tensor == 1 ? a.k + (row * a.H + hk) * kHeadDim
-                             : tensor == 2 ? a.v + (row * a.HV + s_pf_h) * kHeadDim
-                                           : a.g + (row * a.HV + s_pf_h) * kHeadDim;
-        asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const uint8_t*>(base) + part * 128));
-      }
-    }
     if (skip) continue;
     const int h = s_h;
     const int64_t cid = s_cid;
@@ -509,11 +509,17 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
       tc::tc_fence_after();
     }
 
-    // 4. A (beta-scaled, strictly lower) and P (lower) to FP32.  TMEM columns:
+    // 4. A (beta-scaled, strictly lower) to FP32 for the inverse, and P (lower)
+    //    straight into the A2 product's left operand X = [I; P] (128 x 64, BF16
+    //    hi/lo, in the R region, dead since M1 completed).  TMEM columns:
     //    0-31  rows 0-63   : t = row & 31 (< 32),  i = col        (k rows 0-31, q rows 32-63)
     //    32-63 rows 64-127 : t = 32 + (row & 31),  i = col - 32
     //    64-95 rows 0-63   : t = 32 + (row & 31),  i = 32 + col - 64
-    //    warp group 3 writes the zero block t < 32 <= i.
+    //    The inverse reads only A's lower blocks.  Warp groups 3-7 (640 threads)
+    //    write X's identity rows (64 rows x 8 chunks) and P's zero block
+    //    t < 32 <= i (32 rows x 4 chunks), one 8-column chunk each.
+    uint8_t* Xh = Rh;  // X = [I; P]: 128 x 64, 16 KB each half
+    uint8_t* Xl = Xh + 128 * 64 * 2;
     {
       const int wg = warp >> 2, row = (warp & 3) * 32 + lane;
       if (wg < 3) {
@@ -524,21 +530,33 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
         if (use) {
           const int t = (wg == 0 ? 0 : 32) + (row & 31);
           const int i0 = wg == 2 ? 32 : 0;
-          const bool is_q = (row & 63) >= 32;
-          float* dst = (is_q ? Pf : Af) + t * kLdT + i0;
+          if ((row & 63) >= 32) {  // P row t
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int i = i0 + e;
-            dst[e] = is_q ? (i <= t ? d[e] : 0.f) : (i < t ? bt[t] * d[e] : 0.f);
+            for (int e = 0; e < 32; ++e) d[e] = i0 + e <= t ? d[e] : 0.f;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) st_split8(Xh, Xl, tc::sw128_offset(kChunk + t, i0 + 8 * j, 128), d + 8 * j);
+          } else {  // A row t
+            float* dst = Af + t * kLdT + i0;
+#pragma unroll
+            for (int e = 0; e < 32; ++e) dst[e] = i0 + e < t ? bt[t] * d[e] : 0.f;
           }
         }
       } else {
-        for (int idx = tid - 384; idx < 32 * 32; idx += kTxThreads - 384) {
-          const int t = idx >> 5, i = 32 + (idx & 31);
-          Af[t * kLdT + i] = 0.f;
-          Pf[t * kLdT + i] = 0.f;
+        const int idx = tid - 384;  // 0 .. 639
+        float x[8];
+        if (idx < kChunk * 8) {  // identity row r, chunk ch
+          const int r = idx >> 3, ch = idx & 7;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) x[e] = ch * 8 + e == r ? 1.f : 0.f;
+          st_split8(Xh, Xl, tc::sw128_offset(r, ch * 8, 128), x);
+        } else {  // P row t < 32, chunk 4 + ch: columns i >= 32
+          const int t = (idx - kChunk * 8) >> 2, ch = 4 + ((idx - kChunk * 8) & 3);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) x[e] = 0.f;
+          st_split8(Xh, Xl, tc::sw128_offset(kChunk + t, ch * 8, 128), x);
         }
       }
+      static_assert(kTxThreads - 384 == kChunk * 8 + 32 * 4, "one X chunk per thread of warp groups 3-7");
     }
     if (tid == 0) tc::bulk_wait_read();  // Khat^T staging: the A2 region is reused in step 6
     tc::tc_fence_before();
@@ -614,30 +632,21 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
     }
 
     // 6. A2 = [Ti; P Ti] on the tensor core: D = [I; P] Ti, M=128 N=64 K=64.
-    //    Operands: X = [I; P] (128 x 64, K = i) in the R region, Ti^T (64 x 64,
-    //    rows j, K = i) in the A2 region; both hi/lo.  While the product runs,
-    //    B2 (step 7) is built in the lower L/R region, dead by then; the result
-    //    lands in TMEM columns 128-191 and is split into A2 (hi/lo) by all warps.
+    //    Operands: X = [I; P] (128 x 64, K = i, written in step 4) in the R
+    //    region, Ti^T (64 x 64, rows j, K = i) in the A2 region; both hi/lo.
+    //    While the product runs, B2 (step 7) is built in the lower L/R region,
+    //    dead by then; the result lands in TMEM columns 128-191 and is split
+    //    into A2 (hi/lo) by all warps.
     {
-      uint8_t* Xh = Rh;                     // 128 x 64, 16 KB each half
-      uint8_t* Xl = Xh + 128 * 64 * 2;
       uint8_t* Th = A2h;                    // 64 x 64, 8 KB each half
       uint8_t* Tl = Th + 64 * 64 * 2;
       static_assert(kTxB2 + 2 * 256 * 64 * 2 <= kTxR, "B2 stays clear of X");
-      for (int idx = tid; idx < 128 * 8 + 64 * 8; idx += kTxThreads) {
+      if (tid < 64 * 8) {                   // Ti^T rows j
+        const int j = tid >> 3, ch = tid & 7;
         float x[8];
-        if (idx < 128 * 8) {                // X rows: identity (0-63) or P (64-127)
-          const int row = idx >> 3, ch = idx & 7;
 #pragma unroll
-          for (int e = 0; e < 8; ++e)
-            x[e] = row < kChunk ? (ch * 8 + e == row ? 1.f : 0.f) : Pf[(row - kChunk) * kLdT + ch * 8 + e];
-          st_split8(Xh, Xl, tc::sw128_offset(row, ch * 8, 128), x);
-        } else {                            // Ti^T rows j
-          const int j = (idx - 128 * 8) >> 3, ch = (idx - 128 * 8) & 7;
-#pragma unroll
-          for (int e = 0; e < 8; ++e) x[e] = Tf[(ch * 8 + e) * kLdT + j];
-          st_split8(Th, Tl, tc::sw128_offset(j, ch * 8, 64), x);
-        }
+        for (int e = 0; e < 8; ++e) x[e] = Tf[(ch * 8 + e) * kLdT + j];
+        st_split8(Th, Tl, tc::sw128_offset(j, ch * 8, 64), x);
       }
       tc::fence_async_smem();
       tc::tc_fence_before();
@@ -706,6 +715,39 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
           tc::mma_bf16(tmem, tc::sw128_desc(ah[p] + k * 32), tc::sw128_desc(bh[p] + k * 32), idesc,
                        p > 0 || k > 0);
       tc::mma_commit(&mma_bar);
+    }
+    if (warp == 1) {  // the next unit: descriptor, and its rows -> L2 (4 tensors x 64 tokens x 2 lines)
+      ChunkLoc nl{-1, 0, 0};
+      int nh = 0;
+      const int64_t un = u + gridDim.x;
+      if (un < a.tx_units) {
+        if (lane == 0) {
+          int64_t ncid;
+          s_nskip = describe(un, &nl, &ncid, &nh);
+          s_nloc = nl;
+          s_ncid = ncid;
+          s_nh = nh;
+          s_nvalid = 1;
+        }
+        nl.n = __shfl_sync(0xffffffffu, nl.n, 0);
+        nl.len = __shfl_sync(0xffffffffu, nl.len, 0);
+        nl.t0 = __shfl_sync(0xffffffffu, nl.t0, 0);
+        nh = __shfl_sync(0xffffffffu, nh, 0);
+        if (nl.n >= 0) {
+          const int hkn = nh / (a.HV / a.H);  // q/k head of the value head
+          for (int i = lane; i < 512; i += 32) {
+            const int tensor = i >> 7, tok = (i >> 1) & 63, part = i & 1;
+            if (tok < nl.len) {
+              const int64_t row = nl.t0 + tok;
+              const kda_bf16* base = tensor == 0 ? a.q + (row * a.H + hkn) * kHeadDim
+                                   : tensor == 1 ? a.k + (row * a.H + hkn) * kHeadDim
+                                   : tensor == 2 ? a.v + (row * a.HV + nh) * kHeadDim
+                                                 : a.g + (row * a.HV + nh) * kHeadDim;
+              asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const uint8_t*>(base) + part * 128));
+            }
+          }
+        }
+      }
     }
     if (!tc::mbar_wait(&mma_bar, phase)) s_abort = 1;
     phase ^= 1;
