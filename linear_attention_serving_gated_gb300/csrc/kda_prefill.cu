@@ -80,15 +80,12 @@ constexpr int kSlices = kHeadDim / kVs;
 // order (slice = 32 value columns), so that a thread reading one token's four
 // columns and its neighbours reading the next tokens touch consecutive
 // 16-byte words.
-constexpr uint32_t kRecA1 = 0;                                // [W; Q'] hi, 128 x 128
-constexpr uint32_t kRecA1L = kRecA1 + 128 * 128 * 2;          // [W; Q'] lo
-constexpr uint32_t kRecKTh = kRecA1L + 128 * 128 * 2;         // Khat^T hi, 128 x 64
-constexpr uint32_t kRecKTl = kRecKTh + 128 * 64 * 2;          // Khat^T lo
-constexpr uint32_t kRecU = kRecKTl + 128 * 64 * 2;            // Util
-constexpr uint32_t kRecOi = kRecU + kChunk * kHeadDim * 4;    // P Util
-constexpr uint32_t kRecGam = kRecOi + kChunk * kHeadDim * 4;  // exp(Gam_L) [128]
-constexpr uint32_t kRecBytes = kRecGam + kHeadDim * 4;
-constexpr uint32_t kSliceBytes = kChunk * kVs * 4;
+constexpr uint32_t kRecM = 0;                                  // M_c hi, 128 x 128 (rows c', K = c)
+constexpr uint32_t kRecML = kRecM + 128 * 128 * 2;             // M_c lo
+constexpr uint32_t kRecQ = kRecML + 128 * 128 * 2;             // Q' (BF16), 64 x 128
+constexpr uint32_t kRecB = kRecQ + 64 * 128 * 2;               // B_c, FP32 [slice][quad][128][4]
+constexpr uint32_t kRecOi = kRecB + kHeadDim * kHeadDim * 4;   // P Util, FP32 [slice][quad][64][4]
+constexpr uint32_t kRecBytes = kRecOi + kChunk * kHeadDim * 4;
 
 struct PrefillArgs {
   GateArgs gate;
@@ -189,8 +186,8 @@ constexpr int kTxWarps = kTxThreads / 32;
 constexpr uint32_t kTxL = 0;                          // L: TF32 128 x 128
 constexpr uint32_t kTxR = kTxL + 128 * 128 * 4;       // R: TF32 64 x 128
 constexpr uint32_t kTxB2 = 0;                         // B2 hi, lo: 256 x 64 each (reuses L/R)
-constexpr uint32_t kTxA1L = 0;                         // [W; Q'] lo output staging (lower L/R)
-constexpr uint32_t kTxUst = 32 * 1024;                // Util | P Util output staging (upper L/R)
+constexpr uint32_t kTxB3 = 0;                          // [W^T; Util^T] hi, lo: 256 x 64 each (reuses B2)
+constexpr uint32_t kTxMs = 0;                          // M_c hi, lo output staging (reuses B3)
 constexpr uint32_t kTxAf = 0;                         // A FP32 [64][kLdT] (reuses L/R)
 constexpr uint32_t kTxA2 = kTxR + 2 * 64 * 128 * 2;   // A2 hi, lo: 128 x 64 each
 constexpr uint32_t kTxQ = kTxA2 + 2 * 128 * 64 * 2;   // raw q BF16 [64][kLdB]
@@ -201,11 +198,11 @@ constexpr uint32_t kTxTf = kTxAf + kChunk * kLdT * 4;  // (I+A)^-1 FP32 [64][kLd
 constexpr uint32_t kTxMisc = kTxG + kChunk * kLd * 4;  // rq, rk, beta [64] each + scratch [1536]
 constexpr uint32_t kTxEnd = kTxMisc + (3 * kChunk + 1536) * 4;
 constexpr uint32_t kTransformTcSmem = kTxEnd + 1024;
-constexpr uint32_t kTxTmemCols = 256;
+constexpr uint32_t kTxTmemCols = 512;  // M1, A2, M2: 0-255; the map product: 256-511
 static_assert(2 * 256 * 64 * 2 <= kTxA2, "B2 fits in the L/R region");
 static_assert(kTxTf + kChunk * kLdT * 4 <= kTxR, "A and (I+A)^-1 stay below X in the R region");
-static_assert(kTxA1L + 128 * 128 * 2 <= kTxUst, "[W; Q'] lo staging stays below Util | P Util");
-static_assert(kTxUst + 2 * kChunk * kHeadDim * 4 <= kTxA2, "output staging fits the L/R region");
+static_assert(kTxB3 + 2 * 256 * 64 * 2 <= kTxR && kTxMs + 2 * 128 * 128 * 2 <= kTxR,
+              "B3 and the M_c staging stay below Khat^T in the R region");
 static_assert(kTxQ % 16 == 0 && kTxK % 16 == 0 && kTxV % 16 == 0 && kTxG % 16 == 0 &&
                   kTxTf % 16 == 0 && kTxMisc % 16 == 0 && kTxA2 % 1024 == 0 && kTxR % 1024 == 0,
               "alignment");
@@ -213,18 +210,31 @@ static_assert(kTransformTcSmem <= 232448, "shared memory");
 
 // Eight consecutive values -> one 16-byte chunk in each of hi and lo
 // (hi = RN(x), lo = RN(x - hi), both BF16).
+__device__ __forceinline__ void split8(const float* x, uint4& h, uint4& l);
 __device__ __forceinline__ void st_split8(uint8_t* hi, uint8_t* lo, uint32_t off, const float* x) {
-  uint32_t h[4], l[4];
+  uint4 h, l;
+  split8(x, h, l);
+  *reinterpret_cast<uint4*>(hi + off) = h;
+  *reinterpret_cast<uint4*>(lo + off) = l;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  return (uint32_t)float_to_bf16_bits(lo) | ((uint32_t)float_to_bf16_bits(hi) << 16);
+}
+
+// Eight consecutive values -> their BF16 hi and lo parts as two 16-byte words.
+__device__ __forceinline__ void split8(const float* x, uint4& h, uint4& l) {
+  uint32_t hh[4], ll[4];
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
     const __nv_bfloat162 hb = __floats2bfloat162_rn(x[2 * e], x[2 * e + 1]);
     const float2 hf = __bfloat1622float2(hb);
     const __nv_bfloat162 lb = __floats2bfloat162_rn(x[2 * e] - hf.x, x[2 * e + 1] - hf.y);
-    h[e] = *reinterpret_cast<const uint32_t*>(&hb);
-    l[e] = *reinterpret_cast<const uint32_t*>(&lb);
+    hh[e] = *reinterpret_cast<const uint32_t*>(&hb);
+    ll[e] = *reinterpret_cast<const uint32_t*>(&lb);
   }
-  *reinterpret_cast<uint4*>(hi + off) = make_uint4(h[0], h[1], h[2], h[3]);
-  *reinterpret_cast<uint4*>(lo + off) = make_uint4(l[0], l[1], l[2], l[3]);
+  h = make_uint4(hh[0], hh[1], hh[2], hh[3]);
+  l = make_uint4(ll[0], ll[1], ll[2], ll[3]);
 }
 
 // Element (t, c) of a raw 16-bit input tile (BF16 or FP16 bits), widened.
@@ -426,9 +436,6 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
     if (tid == 0) tc::bulk_wait_read();
     __syncthreads();
 
-    // 2. gamma to the workspace (Khat^T follows in step 3, while the first
-    //    M1 product runs).
-    if (tid < K) reinterpret_cast<float*>(rec + kRecGam)[tid] = decay_exp(GM[(kChunk - 1) * kLd + tid]);
     const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
 
     // 3. M1 in two rounds (see the header of this kernel).  Warp w builds the
@@ -481,28 +488,6 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
                        tc::sw128_desc(ra + (k >> 2) * (nR * 128) + koff), idesc, k > 0);
         }
         tc::mma_commit(&mma_bar);
-      }
-      if (round == 0) {
-        // Khat^T (hi/lo, swizzled 128 x 64), built in the A2 region (free until
-        // step 6) while the tensor core works, and sent out as one bulk copy.
-        for (int idx = tid; idx < K * 8; idx += kTxThreads) {
-          const int c = idx & (K - 1), j = idx >> 7;
-          const float gl = GM[(kChunk - 1) * kLd + c];
-          float x[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int t = j * 8 + e;
-            x[e] = in_at<F16>(Ks, t, c) * rk[t] * decay_exp(gl - GM[t * kLd + c]);
-          }
-          st_split8(A2h, A2h + 128 * 64 * 2, tc::sw128_offset(c, j * 8, K), x);
-        }
-        tc::fence_async_smem();
-        __syncthreads();
-        if (tid == 0) {
-          static_assert(kRecKTl == kRecKTh + 128 * 64 * 2, "Khat^T hi and lo are contiguous");
-          tc::bulk_s2g(rec + kRecKTh, A2h, 2 * 128 * 64 * 2);
-          tc::bulk_commit();
-        }
       }
       if (!tc::mbar_wait(&mma_bar, phase)) s_abort = 1;
       phase ^= 1;
@@ -558,7 +543,6 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
       }
       static_assert(kTxThreads - 384 == kChunk * 8 + 32 * 4, "one X chunk per thread of warp groups 3-7");
     }
-    if (tid == 0) tc::bulk_wait_read();  // Khat^T staging: the A2 region is reused in step 6
     tc::tc_fence_before();
     __syncthreads();
 
@@ -716,6 +700,23 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
                        p > 0 || k > 0);
       tc::mma_commit(&mma_bar);
     }
+    // Khat^T (hi/lo, swizzled 128 x 64: rows c, K = token i) for the map
+    // product of step 9, built in the R region (X is dead since the A2
+    // product) while the tensor core runs M2.
+    uint8_t* KTh = sb + kTxR;
+    uint8_t* KTl = KTh + 128 * 64 * 2;
+    {
+      const int c = tid & (K - 1), j = tid >> 7;  // channel c, tokens [8j, 8j+8)
+      static_assert(kTxThreads == kHeadDim * 8, "one Khat^T chunk per thread");
+      const float gl = GM[(kChunk - 1) * kLd + c];
+      float x[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int t = j * 8 + e;
+        x[e] = in_at<F16>(Ks, t, c) * rk[t] * decay_exp(gl - GM[t * kLd + c]);
+      }
+      st_split8(KTh, KTl, tc::sw128_offset(c, j * 8, K), x);
+    }
     if (warp == 1) {  // the next unit: descriptor, and its rows -> L2 (4 tensors x 64 tokens x 2 lines)
       ChunkLoc nl{-1, 0, 0};
       int nh = 0;
@@ -753,56 +754,121 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
     phase ^= 1;
     tc::tc_fence_after();
 
-    // 9. epilogue: warp group wg (four warps, one per TMEM lane quadrant) takes
-    //    256 / kGroups consecutive TMEM columns: columns 0-127 are W (rows 0-63) |
-    //    P W (rows 64-127), 128-255 Util | P Util.  M2 has finished reading its
-    //    operands, so [W; Q'] is staged in the A2 region and Util | P Util in the
-    //    L/R region, laid out as in the workspace record, and each goes out as
-    //    one bulk copy.  [W; Q'] is split into BF16 hi (A2 region) and lo
-    //    (lower L/R region).
+    // 9. epilogue.  Thread (TMEM lane quadrant warp & 3, column group warp >> 2)
+    //    takes lane 32 (warp & 3) + lane and 32 consecutive columns.  After M2,
+    //    columns 0-127 hold W (lanes 0-63, token t = lane) | P W (lanes 64-127,
+    //    t = lane - 64) and columns 128-255 Util | P Util.  M2 has finished
+    //    reading its operands.
+    //    9a. Q' = Qtil - P W in BF16 (a 64 x 128 tile) staged in the A2 region
+    //        and bulk-stored; P Util straight to the record;
+    //        W and Util written transposed (rows = channel / value column, K =
+    //        token) and split into B3 = [W^T; Util^T] in the B2 region.
+    //    9b. The chunk's affine map S_end = M_c S0 + B_c as one product
+    //        Khat^T [W | Util] (M=128 N=256 K=64, BF16 x3) into TMEM columns
+    //        256-511: M_c = Diag(gamma) - Khat^T W, B_c = Khat^T Util.
+    //    9c. M_c split hi/lo, staged in the (now dead) B3 region and
+    //        bulk-stored; B_c FP32 straight to the record.
+    uint8_t* B3h = sb + kTxB3;
+    uint8_t* B3l = B3h + 256 * 64 * 2;
+    uint8_t* QQ = A2h;  // Q': 64 x 128 BF16, 16 KB
     {
-      constexpr int kGroups = kTxWarps / 4, kCols = 256 / kGroups;
-      static_assert(kCols == 32, "two 16-column TMEM loads per thread");
-      const int wg = warp >> 2, row = (warp & 3) * 32 + lane;
-      const int t = row & 63;
-      const bool upper = row < kChunk;
-      const bool right = wg >= kGroups / 2;
-      const int cbase = (wg % (kGroups / 2)) * kCols;  // first column within the half
+      const int row = (warp & 3) * 32 + lane, cg = warp >> 2;
       uint32_t raw[2][16];
-      tc::tmem_ld16_async(tmem + lane_addr + (right ? 128 : 0) + cbase, raw[0]);
-      tc::tmem_ld16_async(tmem + lane_addr + (right ? 128 : 0) + cbase + 16, raw[1]);
+      tc::tmem_ld16_async(tmem + lane_addr + cg * 32, raw[0]);
+      tc::tmem_ld16_async(tmem + lane_addr + cg * 32 + 16, raw[1]);
       tc::tmem_wait_ld();
+      float d[32];
 #pragma unroll
-      for (int cb = 0; cb < 2; ++cb) {
-        float d[16];
+      for (int e = 0; e < 16; ++e) {
+        d[e] = __uint_as_float(raw[0][e]);
+        d[16 + e] = __uint_as_float(raw[1][e]);
+      }
+      if (row < kChunk) {  // W / Util of token t: row n = 32 cg + e of B3, column t
+        const int t = row;
 #pragma unroll
-        for (int e = 0; e < 16; ++e) d[e] = __uint_as_float(raw[cb][e]);
-        const int c0 = cbase + cb * 16;
-        if (!right) {
-          if (!upper) {  // Q' = Qtil - P W
-            const float nq = rq[t];
-#pragma unroll
-            for (int e = 0; e < 16; e += 4) {
-              const float4 qq = scale4(ld_in4<F16>(Qs, t, c0 + e), nq);
-              const float4 gg = f4(GM + t * kLd + c0 + e);
-              d[e] = qq.x * decay_exp(gg.x) - d[e];
-              d[e + 1] = qq.y * decay_exp(gg.y) - d[e + 1];
-              d[e + 2] = qq.z * decay_exp(gg.z) - d[e + 2];
-              d[e + 3] = qq.w * decay_exp(gg.w) - d[e + 3];
-            }
-          }
-#pragma unroll
-          for (int half = 0; half < 2; ++half)
-            st_split8(A2h, sb + kTxA1L, tc::sw128_offset(row, c0 + half * 8, 128), d + half * 8);
-        } else {
-          float* base = reinterpret_cast<float*>(sb + kTxUst + (upper ? 0u : kRecOi - kRecU));
-#pragma unroll
-          for (int e = 0; e < 16; e += 4) {  // column quad (c0 + e) / 4
-            const int col = c0 + e;
-            f4(base + (col / kVs) * (kChunk * kVs) + ((col % kVs) / 4) * (kChunk * 4) + t * 4) =
-                make_float4(d[e], d[e + 1], d[e + 2], d[e + 3]);
-          }
+        for (int e = 0; e < 32; ++e) {
+          uint16_t hi, lo;
+          tc::split_bf16(d[e], hi, lo);
+          const uint32_t off = tc::sw128_offset(cg * 32 + e, t, 256);
+          *reinterpret_cast<uint16_t*>(B3h + off) = hi;
+          *reinterpret_cast<uint16_t*>(B3l + off) = lo;
         }
+      } else if (cg < 4) {  // Q' = Qtil - P W, channels [32 cg, 32 cg + 32) of token t
+        const int t = row - kChunk, c0 = cg * 32;
+        const float nq = rq[t];
+#pragma unroll
+        for (int e = 0; e < 32; e += 4) {
+          const float4 qq = scale4(ld_in4<F16>(Qs, t, c0 + e), nq);
+          const float4 gg = f4(GM + t * kLd + c0 + e);
+          d[e] = qq.x * decay_exp(gg.x) - d[e];
+          d[e + 1] = qq.y * decay_exp(gg.y) - d[e + 1];
+          d[e + 2] = qq.z * decay_exp(gg.z) - d[e + 2];
+          d[e + 3] = qq.w * decay_exp(gg.w) - d[e + 3];
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float* xs = d + 8 * j;
+          *reinterpret_cast<uint4*>(QQ + tc::sw128_offset(t, c0 + 8 * j, kChunk)) =
+              make_uint4(pack_bf16x2(xs[0], xs[1]), pack_bf16x2(xs[2], xs[3]), pack_bf16x2(xs[4], xs[5]),
+                         pack_bf16x2(xs[6], xs[7]));
+        }
+      } else {  // P Util, value slice cg - 4 of token t -> [slice][quad][64][4]
+        const int t = row - kChunk;
+        float4* dst = reinterpret_cast<float4*>(rec + kRecOi) + (cg - 4) * (kVs / 4) * kChunk + t;
+#pragma unroll
+        for (int qd = 0; qd < kVs / 4; ++qd)
+          dst[qd * kChunk] = make_float4(d[4 * qd], d[4 * qd + 1], d[4 * qd + 2], d[4 * qd + 3]);
+      }
+    }
+    tc::fence_async_smem();
+    tc::tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {
+      tc::bulk_s2g(rec + kRecQ, QQ, kChunk * 128 * 2);
+      tc::bulk_commit();  // awaited at the end of the next unit's fold, or on exit
+      if (!s_abort) {
+        tc::tc_fence_after();
+        constexpr uint32_t idesc = tc::idesc_bf16_f32(128, 256);
+        const uint32_t ah[3] = {tc::smem_u32(KTh), tc::smem_u32(KTh), tc::smem_u32(KTl)};
+        const uint32_t bh[3] = {tc::smem_u32(B3h), tc::smem_u32(B3l), tc::smem_u32(B3h)};
+#pragma unroll
+        for (int p = 0; p < 3; ++p)
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            tc::mma_bf16(tmem + 256, tc::sw128_desc(ah[p] + k * 32), tc::sw128_desc(bh[p] + k * 32),
+                         idesc, p > 0 || k > 0);
+        tc::mma_commit(&mma_bar);
+      }
+    }
+    if (!tc::mbar_wait(&mma_bar, phase)) s_abort = 1;
+    phase ^= 1;
+    tc::tc_fence_after();
+    {  // 9c: lane = output row c'
+      const int row = (warp & 3) * 32 + lane, cg = warp >> 2;
+      uint32_t raw[2][16];
+      tc::tmem_ld16_async(tmem + lane_addr + 256 + cg * 32, raw[0]);
+      tc::tmem_ld16_async(tmem + lane_addr + 256 + cg * 32 + 16, raw[1]);
+      tc::tmem_wait_ld();
+      float d[32];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        d[e] = __uint_as_float(raw[0][e]);
+        d[16 + e] = __uint_as_float(raw[1][e]);
+      }
+      if (cg < 4) {  // M_c[c'][c] = gamma_c' [c == c'] - (Khat^T W)[c'][c]
+        const int c0 = cg * 32;
+        const float gam = decay_exp(GM[(kChunk - 1) * kLd + row]);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) d[e] = (c0 + e == row ? gam : 0.f) - d[e];
+        uint8_t* Mh = sb + kTxMs;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          st_split8(Mh, Mh + 128 * 128 * 2, tc::sw128_offset(row, c0 + 8 * j, 128), d + 8 * j);
+      } else {  // B_c, value slice cg - 4 of row c' -> [slice][quad][128][4]
+        float4* dst = reinterpret_cast<float4*>(rec + kRecB) + (cg - 4) * (kVs / 4) * kHeadDim + row;
+#pragma unroll
+        for (int qd = 0; qd < kVs / 4; ++qd)
+          dst[qd * kHeadDim] = make_float4(d[4 * qd], d[4 * qd + 1], d[4 * qd + 2], d[4 * qd + 3]);
       }
     }
     if (s_abort && tid == 0) set_error(a.err_flag, KDA_DEVERR_TIMEOUT);
@@ -810,10 +876,8 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
     tc::tc_fence_before();
     __syncthreads();
     if (tid == 0) {
-      static_assert(kRecOi == kRecU + kChunk * kHeadDim * 4, "Util and P Util are contiguous");
-      tc::bulk_s2g(rec + kRecA1, A2h, 128 * 128 * 2);
-      tc::bulk_s2g(rec + kRecA1L, sb + kTxA1L, 128 * 128 * 2);
-      tc::bulk_s2g(rec + kRecU, sb + kTxUst, 2 * kChunk * kHeadDim * 4);
+      static_assert(kRecML == kRecM + 128 * 128 * 2, "M_c hi and lo are contiguous");
+      tc::bulk_s2g(rec + kRecM, sb + kTxMs, 2 * 128 * 128 * 2);
       tc::bulk_commit();  // awaited at the end of the next unit's fold, or on exit
     }
   }  // units
@@ -827,50 +891,80 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
 // Sequential state pass on tcgen05.
 
 // Shared-memory layout of the state pass (bytes from a 1024-aligned base).
-// One stage holds a chunk's operand tiles; Util and P Util go straight from
-// the record into registers.
-constexpr uint32_t kStA1 = 0;                         // [W; Q'] hi
-constexpr uint32_t kStA1L = kStA1 + 128 * 128 * 2;    // [W; Q'] lo
-constexpr uint32_t kStKTh = kStA1L + 128 * 128 * 2;
-constexpr uint32_t kStKTl = kStKTh + 128 * 64 * 2;
-constexpr uint32_t kStGam = kStKTl + 128 * 64 * 2;
-constexpr uint32_t kStageBytes = ((kStGam + kHeadDim * 4 + 1023) / 1024) * 1024;
-constexpr uint32_t kSmS = 2 * kStageBytes;         // [S_hi; S_lo]^T: 64 x 128 (rows j, 32 + j)
+// A stage holds one chunk's operand tiles, bulk-copied from its record in two
+// parts: M_c (hi, lo), read by the chain product, and Q', read by the output
+// product, each reloaded as soon as its own reader is done.  B_c and P Util go
+// straight from the record into registers.
+constexpr uint32_t kStM = 0;                           // M_c hi, lo: 128 x 128 each
+constexpr uint32_t kStMBytes = 2 * 128 * 128 * 2;
+constexpr uint32_t kStQ = kStM + kStMBytes;            // Q': 64 x 128 (two 8 KB atom columns)
+constexpr uint32_t kStQBytes = kChunk * 128 * 2;
+constexpr uint32_t kStageBytes = kStQ + kStQBytes;
+constexpr int kSBufs = 3;                              // state operand buffers
+constexpr uint32_t kSmS = 2 * kStageBytes;             // [S_hi; S_lo]^T: 64 x 128, kSBufs buffers
 constexpr uint32_t kSmSBytes = 2 * kVs * kHeadDim * 2;
-constexpr uint32_t kSmU = kSmS + kSmSBytes;        // [U_hi; U_lo]^T: 64 x 64
-constexpr uint32_t kSmUBytes = 2 * kVs * kChunk * 2;
-constexpr uint32_t kPassSmem = kSmU + kSmUBytes + 1024;  // + alignment slack
-constexpr uint32_t kStageTx = 2 * 128 * 128 * 2 + 2 * 128 * 64 * 2 + kHeadDim * 4;
-constexpr uint32_t kTmemCols = 128;  // D1: cols 0-63 (hi | lo), D2: cols 64-127
-static_assert(kStA1L == kStA1 + 128 * 128 * 2 && kRecA1L == kRecA1 + 128 * 128 * 2 &&
-                  kStKTh == kStA1L + 128 * 128 * 2 && kRecKTh == kRecA1L + 128 * 128 * 2 &&
-                  kStKTl == kStKTh + 128 * 64 * 2 && kRecKTl == kRecKTh + 128 * 64 * 2,
-              "[W; Q'] hi, lo and Khat^T hi, lo are copied as one block");
+constexpr uint32_t kPassSmem = kSmS + kSBufs * kSmSBytes + 1024;  // + alignment slack
+// TMEM: the chain product in columns 0-63 (S_hi | S_lo halves), the output
+// product in 64-127 or 128-191 (two buffers)
+constexpr uint32_t kTmemCols = 256;
+static_assert(kStQ == kStM + kStMBytes && kRecQ == kRecM + kStMBytes, "the record's tiles in stage order");
 static_assert(kPassSmem <= 232448, "shared memory");
+// The output product is M = 128 over the 64-row Q' tile: its rows 64-127
+// read the 8 KB after each of the tile's two atom columns (the second atom
+// column, then the next stage or the state operands), all inside the
+// allocation, and feed TMEM lanes 64-127, which are never read.
+static_assert(kStQ + kStQBytes + 8 * 1024 <= kSmS, "rows past the Q' tile stay in shared memory");
 
-__device__ __forceinline__ void issue_stage_loads(uint8_t* stage, const uint8_t* rec, uint64_t* bar) {
-  tc::mbar_expect_tx(bar, kStageTx);
-  tc::bulk_g2s(stage + kStA1, rec + kRecA1, 2 * 128 * 128 * 2 + 2 * 128 * 64 * 2, bar);
-  tc::bulk_g2s(stage + kStGam, rec + kRecGam, kHeadDim * 4, bar);
+// Copies as 16 KB pieces, which the copy engine keeps in flight together.
+constexpr uint32_t kCopyPiece = 16 * 1024;
+static_assert(kStMBytes % kCopyPiece == 0 && kStQBytes % kCopyPiece == 0, "whole pieces");
+__device__ __forceinline__ void issue_copy(uint8_t* dst, const uint8_t* src, uint32_t bytes, uint64_t* bar) {
+  tc::mbar_expect_tx(bar, bytes);
+  for (uint32_t off = 0; off < bytes; off += kCopyPiece) tc::bulk_g2s(dst + off, src + off, kCopyPiece, bar);
 }
 
-constexpr int kPassThreads = 512;  // 4 warps per TMEM lane quadrant
+// Chunks ahead of the copies whose records are prefetched into L2.
+constexpr int kPassL2Ahead = 3;
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(tc::smem_u32(bar)) : "memory");
+}
+
+constexpr int kPassEpiThreads = 512;                // 4 warps per TMEM lane quadrant
+constexpr int kPassThreads = kPassEpiThreads + 64;  // + the MMA warp and the copy warp
 constexpr int kColsPerThread = kVs / 4;
 
+// Per (sequence, head, 32 value columns), sequential over the sequence's
+// chunks.  Epilogue thread (lane quadrant, column group) owns S[c][v0 + j0 ..
+// + 8) for key channel c = its TMEM lane.  Per chunk i, with S_i its start
+// state:
+//   chain   D_ch = M_hi [S_hi | S_lo] + M_lo S_hi      (M=128 N=64, then N=32)
+//           S_{i+1} = D_ch[S_hi half] + D_ch[S_lo half] + B_c
+//   output  D_O  = Q' [S_hi | S_lo]                     (M=128 N=64, lanes 0-63 = tokens)
+//           O    = scale (D_O[S_hi half] + D_O[S_lo half] + P Util)
+// Warp 16 issues the products: chunk i's chain product, then chunk i - 1's
+// output product, which thus runs while the epilogue warps turn chunk i's
+// chain product into S_{i+1}, and never delays a chain product.  Warp 17
+// issues the stage copies and L2 prefetches.  Neither blocks the epilogue
+// warps, which own the state; the state operand has three buffers (chunk
+// i - 1's output product may still read S_{i-1} while S_{i+1} is written).
 template <bool F16>
 __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const PrefillArgs a) {
   extern __shared__ uint8_t smraw[];
-  __shared__ uint64_t full_bar[2];
-  __shared__ uint64_t mma_bar;
+  __shared__ uint64_t m_full[2], q_full[2];  // stage i & 1 holds chunk i's M_c / Q'
+  __shared__ uint64_t m_free[2];             // chunk i's chain product is done (its M_c is free)
+  __shared__ uint64_t ch_bar, o_bar[2];      // chain product done; chunk i's output product done
+  __shared__ uint64_t s_ready;               // the next state operand is written (per-warp arrivals)
   __shared__ uint32_t tmem_base;
   __shared__ int64_t s_t0, s_t1, s_cbase;
   __shared__ int s_state, s_abort;
 
   uint8_t* smb = smraw + ((1024u - (tc::smem_u32(smraw) & 1023u)) & 1023u);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int quad = warp & 3, cg = warp >> 2;  // TMEM lane quadrant, column group
-  const int row = quad * 32 + lane;           // key channel c (D2, S) or row of D1
-  const int j0 = cg * kColsPerThread;         // first of this thread's value columns
+  const bool mma_warp = warp == kPassEpiThreads / 32, copy_warp = warp == kPassEpiThreads / 32 + 1;
+  const int quad = warp & 3, cg = (warp >> 2) & 3;  // TMEM lane quadrant, column group
+  const int row = quad * 32 + lane;                 // key channel c (chain) or output row
+  const int j0 = cg * kColsPerThread;               // first of this thread's value columns
   const int n = blockIdx.z, h = blockIdx.y, slice = blockIdx.x, v0 = slice * kVs;
   const int HV = a.HV, K = kHeadDim, V = kHeadDim;
 
@@ -897,9 +991,14 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
       s_t0 = seq_begin(a, n);
       s_t1 = seq_begin(a, n + 1);
     }
-    tc::mbar_init(&full_bar[0], 1);
-    tc::mbar_init(&full_bar[1], 1);
-    tc::mbar_init(&mma_bar, 1);
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(&m_full[i], 1);
+      tc::mbar_init(&q_full[i], 1);
+      tc::mbar_init(&m_free[i], 1);
+      tc::mbar_init(&o_bar[i], 1);
+    }
+    tc::mbar_init(&ch_bar, 1);
+    tc::mbar_init(&s_ready, kPassEpiThreads / 32);  // one arrival per epilogue warp
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
@@ -922,62 +1021,154 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
   float* st = a.pool + ((size_t)slot * HV + h) * V * K;
   const uint8_t* ws_head = a.ws + ((size_t)(s_cbase + p0) * HV + h) * kRecBytes;
   const size_t rec_stride = (size_t)HV * kRecBytes;
-
-  int issued = 0;    // chunks whose loads have been issued (thread 32)
-  int consumed = 0;  // chunks whose loads have landed
-  if (tid == 32) {
-    for (; issued < 2 && issued < nch; ++issued)
-      issue_stage_loads(smb + issued * kStageBytes, ws_head + issued * rec_stride, &full_bar[issued]);
-  }
-  if (warp == 0) tc::tmem_alloc(&tmem_base, kTmemCols);
-
-  // state: thread owns S[row][v0 + j0 .. + 8) in FP32 registers
   const int c = row;
-  float S[kColsPerThread];
-#pragma unroll
-  for (int jj = 0; jj < kColsPerThread; ++jj) S[jj] = st[(size_t)(v0 + j0 + jj) * K + c];
-  uint8_t* S2 = smb + kSmS;
-  uint8_t* U2 = smb + kSmU;
-  auto write_state_operand = [&]() {
-#pragma unroll
-    for (int jj = 0; jj < kColsPerThread; ++jj) {
-      uint16_t hi, lo;
-      tc::split_bf16(S[jj], hi, lo);
-      *reinterpret_cast<uint16_t*>(S2 + tc::sw128_offset(j0 + jj, c, 2 * kVs)) = hi;
-      *reinterpret_cast<uint16_t*>(S2 + tc::sw128_offset(kVs + j0 + jj, c, 2 * kVs)) = lo;
-    }
-  };
-  write_state_operand();
-  tc::fence_async_smem();
+  float S[kColsPerThread];  // epilogue threads: S[c][v0 + j0 .. + 8)
+
+  if (warp == 0) tc::tmem_alloc(&tmem_base, kTmemCols);
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = tmem_base;
-  const uint32_t d1 = tmem, d2 = tmem + 2 * kVs;
-  const uint32_t lane_addr = (static_cast<uint32_t>(quad * 32) << 16) + j0;
+  const uint32_t dch = tmem;
   constexpr uint32_t idesc2 = tc::idesc_bf16_f32(128, 2 * kVs);
   constexpr uint32_t idesc1 = tc::idesc_bf16_f32(128, kVs);
-  const float scale = a.gate.scale;
-  uint32_t mma_phase = 0;
 
-  for (int ci = 0; ci < nch; ++ci) {
-    const int sidx = ci & 1;
-    uint8_t* stage = smb + sidx * kStageBytes;
-    const int64_t cid = s_cbase + p0 + ci;
-    const int64_t tc0 = t0 + (int64_t)(p0 + ci) * kChunk;
-    const int len = (int)(t1 - tc0 < kChunk ? t1 - tc0 : kChunk);
-    // this thread's Util (rows 0-63) or P Util (rows 64-127) values: read
-    // from the record into registers while the stage lands and D1 runs
-    float4 xu0, xu1;
-    {
-      const float4* src = reinterpret_cast<const float4*>(ws_head + (size_t)ci * rec_stride +
-                                                          (quad < 2 ? kRecU : kRecOi) +
-                                                          slice * kSliceBytes) +
-                          (j0 / 4) * kChunk + (row & (kChunk - 1));
-      xu0 = __ldcg(src);
-      xu1 = __ldcg(src + kChunk);
+  if (copy_warp) {
+    // ---- copy warp (one lane) ----
+    if (lane == 0) {
+      auto prefetch_record = [&](int cj) {  // the operand tiles, this slice of B_c and P Util
+        const uint8_t* rec = ws_head + (size_t)cj * rec_stride;
+        tc::bulk_prefetch_l2(rec + kRecM, kStageBytes);
+        tc::bulk_prefetch_l2(rec + kRecB + slice * (kVs * kHeadDim * 4), kVs * kHeadDim * 4);
+        tc::bulk_prefetch_l2(rec + kRecOi + slice * (kVs * kChunk * 4), kVs * kChunk * 4);
+      };
+      auto copy_m = [&](int cj) {
+        issue_copy(smb + (cj & 1) * kStageBytes + kStM, ws_head + (size_t)cj * rec_stride + kRecM, kStMBytes,
+                   &m_full[cj & 1]);
+      };
+      auto copy_q = [&](int cj) {
+        issue_copy(smb + (cj & 1) * kStageBytes + kStQ, ws_head + (size_t)cj * rec_stride + kRecQ, kStQBytes,
+                   &q_full[cj & 1]);
+      };
+      int issued = 0;  // chunks whose two copies were issued
+      for (; issued < 2 && issued < nch; ++issued) {
+        copy_m(issued);
+        copy_q(issued);
+      }
+      for (int cj = 2; cj < 2 + kPassL2Ahead && cj < nch; ++cj) prefetch_record(cj);
+      bool abort = false;
+      for (int cj = 2; cj < nch && !abort; ++cj) {
+        // stage cj & 1 held chunk cj - 2: its M_c is free once that chunk's
+        // chain product is done, its Q' once its output product is
+        if (!tc::mbar_wait(&m_free[cj & 1], ((cj - 2) >> 1) & 1)) abort = true;
+        if (!abort) {
+          tc::fence_async_smem();
+          copy_m(cj);
+          if (cj + kPassL2Ahead < nch) prefetch_record(cj + kPassL2Ahead);
+        }
+        if (!abort && !tc::mbar_wait(&o_bar[cj & 1], ((cj - 2) >> 1) & 1)) abort = true;
+        if (!abort) {
+          tc::fence_async_smem();
+          copy_q(cj);
+          issued = cj + 1;
+        }
+      }
+      if (abort) {
+        s_abort = 1;
+        set_error(a.err_flag, KDA_DEVERR_TIMEOUT);
+      }
+      // no copy may outlive the CTA; the last ones issued are the latest
+      // phases of their barriers (an M_c copy issued without its Q' copy
+      // has landed or times out here as well)
+      for (int cj = issued - 2 > 0 ? issued - 2 : 0; cj < issued + (abort ? 1 : 0) && cj < nch; ++cj) {
+        tc::mbar_wait(&m_full[cj & 1], (cj >> 1) & 1, 1u << 20);
+        if (cj < issued) tc::mbar_wait(&q_full[cj & 1], (cj >> 1) & 1, 1u << 20);
+      }
     }
-    if (a.intermediate) {
+  } else if (mma_warp) {
+    // ---- MMA warp (one lane) ----
+    if (lane == 0) {
+      auto issue_output = [&](int cj) {  // chunk cj's output product (stage cj & 1, state buffer cj % 3)
+        const uint32_t qq = tc::smem_u32(smb + (cj & 1) * kStageBytes + kStQ);
+        const uint32_t sb2 = tc::smem_u32(smb + kSmS + (cj % kSBufs) * kSmSBytes);
+        const uint32_t dO = tmem + 64 + 64 * (cj & 1);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {  // Q' [S_hi | S_lo]; Q' atom columns are 64 rows (8 KB) apart
+          const uint32_t koff = (k & 3) * 32;
+          tc::mma_bf16(dO, tc::sw128_desc(qq + (k >> 2) * (kChunk * 128) + koff),
+                       tc::sw128_desc(sb2 + (k >> 2) * (2 * kVs * 128) + koff), idesc2, k > 0);
+        }
+        tc::mma_commit(&o_bar[cj & 1]);
+      };
+      bool abort = false;
+      for (int ci = 0; ci <= nch && !abort; ++ci) {
+        if (ci < nch) {
+          // state operand of chunk ci written (chunk 0's by the prologue), its M_c landed
+          if (!tc::mbar_wait(&s_ready, ci & 1) || !tc::mbar_wait(&m_full[ci & 1], (ci >> 1) & 1)) {
+            abort = true;
+            break;
+          }
+          tc::tc_fence_after();
+          const uint32_t mh = tc::smem_u32(smb + (ci & 1) * kStageBytes + kStM), ml = mh + 128 * 128 * 2;
+          const uint32_t sb2 = tc::smem_u32(smb + kSmS + (ci % kSBufs) * kSmSBytes);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {  // M_hi [S_hi | S_lo]
+            const uint32_t koff = (k & 3) * 32;
+            tc::mma_bf16(dch, tc::sw128_desc(mh + (k >> 2) * (128 * 128) + koff),
+                         tc::sw128_desc(sb2 + (k >> 2) * (2 * kVs * 128) + koff), idesc2, k > 0);
+          }
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {  // + M_lo S_hi, into the S_lo half
+            const uint32_t koff = (k & 3) * 32;
+            tc::mma_bf16(dch + kVs, tc::sw128_desc(ml + (k >> 2) * (128 * 128) + koff),
+                         tc::sw128_desc(sb2 + (k >> 2) * (2 * kVs * 128) + koff), idesc1, true);
+          }
+          tc::mma_commit(&ch_bar);
+          tc::mma_commit(&m_free[ci & 1]);
+        }
+        if (ci >= 1) {  // chunk ci - 1's output product, behind chunk ci's chain product
+          if (!tc::mbar_wait(&q_full[(ci - 1) & 1], ((ci - 1) >> 1) & 1)) {
+            abort = true;
+            break;
+          }
+          tc::tc_fence_after();
+          issue_output(ci - 1);
+        }
+      }
+      if (abort) {
+        s_abort = 1;
+        set_error(a.err_flag, KDA_DEVERR_TIMEOUT);
+      }
+    }
+  } else {
+    // ---- epilogue warps ----
+    auto load_bc = [&](int ci, float4& b0, float4& b1) {  // B_c rows c, [slice][quad][128][4]
+      const float4* src = reinterpret_cast<const float4*>(ws_head + (size_t)ci * rec_stride + kRecB) +
+                          (slice * (kVs / 4) + j0 / 4) * kHeadDim + row;
+      b0 = __ldcg(src);
+      b1 = __ldcg(src + kHeadDim);
+    };
+    auto load_pu = [&](int ci, float4& u0, float4& u1) {  // P Util rows t, [slice][quad][64][4]
+      const float4* src = reinterpret_cast<const float4*>(ws_head + (size_t)ci * rec_stride + kRecOi) +
+                          (slice * (kVs / 4) + j0 / 4) * kChunk + (row & (kChunk - 1));
+      u0 = __ldcg(src);
+      u1 = __ldcg(src + kChunk);
+    };
+#pragma unroll
+    for (int jj = 0; jj < kColsPerThread; ++jj) S[jj] = st[(size_t)(v0 + j0 + jj) * K + c];
+    auto write_state_operand = [&](int buf) {
+      uint8_t* S2 = smb + kSmS + buf * kSmSBytes;
+#pragma unroll
+      for (int jj = 0; jj < kColsPerThread; ++jj) {
+        uint16_t hi, lo;
+        tc::split_bf16(S[jj], hi, lo);
+        *reinterpret_cast<uint16_t*>(S2 + tc::sw128_offset(j0 + jj, c, 2 * kVs)) = hi;
+        *reinterpret_cast<uint16_t*>(S2 + tc::sw128_offset(kVs + j0 + jj, c, 2 * kVs)) = lo;
+      }
+    };
+    auto write_intermediate = [&](int ci) {  // S is the start state of chunk ci
+      if (!a.intermediate) return;
+      const int64_t cid = s_cbase + p0 + ci;
       if (cid < a.inter_chunks) {
         float* dst = a.intermediate + ((size_t)cid * HV + h) * V * K;
 #pragma unroll
@@ -985,108 +1176,81 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
       } else if (tid == 0 && slice == 0) {
         set_error(a.err_flag, KDA_DEVERR_INTERMEDIATE);
       }
+    };
+    const uint32_t lane_addr = (static_cast<uint32_t>(quad * 32) << 16) + j0;
+    const float scale = a.gate.scale;
+    // chunk cj's output: TMEM lanes 0-63 are its tokens (quadrants 0-1)
+    auto output = [&](int cj, const float4& u0, const float4& u1) -> bool {
+      if (quad >= 2) return true;
+      const bool ok = tc::mbar_wait(&o_bar[cj & 1], (cj >> 1) & 1);
+      tc::tc_fence_after();
+      float dh[kColsPerThread], dl[kColsPerThread];
+      const uint32_t dO = tmem + 64 + 64 * (cj & 1);
+      tc::tmem_ld8(dO + lane_addr, dh);
+      tc::tmem_ld8(dO + lane_addr + kVs, dl);
+      const float oo[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+      float x[8];
+#pragma unroll
+      for (int jj = 0; jj < kColsPerThread; ++jj) x[jj] = a.gate.scale * (dh[jj] + dl[jj] + oo[jj]);
+      const int64_t tcj = t0 + (int64_t)(p0 + cj) * kChunk;
+      const int len = (int)(t1 - tcj < kChunk ? t1 - tcj : kChunk);
+      if (row < len)
+        *reinterpret_cast<uint4*>(a.o + ((tcj + row) * HV + h) * V + v0 + j0) =
+            make_uint4(pack_out16x2<F16>(x[0], x[1]), pack_out16x2<F16>(x[2], x[3]),
+                       pack_out16x2<F16>(x[4], x[5]), pack_out16x2<F16>(x[6], x[7]));
+      tc::tc_fence_before();
+      return ok;
+    };
+    (void)scale;
+    float4 bc0, bc1, pu0, pu1, pp0 = make_float4(0.f, 0.f, 0.f, 0.f), pp1 = pp0;  // pp: previous chunk's P Util
+    load_bc(0, bc0, bc1);
+    load_pu(0, pu0, pu1);
+    write_state_operand(0);
+    write_intermediate(0);
+    tc::fence_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&s_ready);
+    bool ok = true;
+    for (int ci = 0; ci < nch && ok; ++ci) {
+      const bool more = ci + 1 < nch;
+      float4 nb0 = bc0, nb1 = bc1, nu0 = pu0, nu1 = pu1;
+      if (more) {  // next chunk's B_c and P Util, landing while this one finishes
+        load_bc(ci + 1, nb0, nb1);
+        load_pu(ci + 1, nu0, nu1);
+      }
+      // chain: S_{ci+1} = M_c S_ci + B_c
+      if (!tc::mbar_wait(&ch_bar, ci & 1)) ok = false;
+      tc::tc_fence_after();
+      {
+        float dh[kColsPerThread], dl[kColsPerThread];
+        tc::tmem_ld8(dch + lane_addr, dh);
+        tc::tmem_ld8(dch + lane_addr + kVs, dl);
+        const float bb[8] = {bc0.x, bc0.y, bc0.z, bc0.w, bc1.x, bc1.y, bc1.z, bc1.w};
+#pragma unroll
+        for (int jj = 0; jj < kColsPerThread; ++jj) S[jj] = dh[jj] + dl[jj] + bb[jj];
+      }
+      if (more) {
+        // its buffer's last readers, chunk ci - 2's products, finished before
+        // chunk ci's chain product did
+        write_state_operand((ci + 1) % kSBufs);
+        tc::fence_async_smem();
+        tc::tc_fence_before();
+        __syncwarp();  // the warp's operand writes (and TMEM reads) precede its arrival
+        if (lane == 0) mbar_arrive(&s_ready);  // the MMA warp may issue chunk ci + 1
+        write_intermediate(ci + 1);
+      }
+      if (ci >= 1 && !output(ci - 1, pp0, pp1)) ok = false;  // issued behind chunk ci's chain product
+      pp0 = pu0; pp1 = pu1;
+      bc0 = nb0; bc1 = nb1; pu0 = nu0; pu1 = nu1;
     }
-    if (tc::mbar_wait(&full_bar[sidx], (ci >> 1) & 1))
-      consumed = ci + 1;
-    else
+    if (ok && !output(nch - 1, pp0, pp1)) ok = false;
+    if (!ok) {
       s_abort = 1;
-    // D1 = [W; Q']_hi [S_hi | S_lo] + [W; Q']_lo S_hi: eight K=16 steps at
-    // N = 64, then eight at N = 32 into the S_lo half
-    if (tid == 0 && !s_abort) {
-      tc::tc_fence_after();
-      const uint32_t a1 = tc::smem_u32(stage + kStA1), a1l = tc::smem_u32(stage + kStA1L);
-      const uint32_t sb2 = tc::smem_u32(S2);
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const uint32_t koff = (k & 3) * 32;
-        const uint64_t ad = tc::sw128_desc(a1 + (k >> 2) * (128 * 128) + koff);
-        const uint64_t bd = tc::sw128_desc(sb2 + (k >> 2) * (2 * kVs * 128) + koff);
-        tc::mma_bf16(d1, ad, bd, idesc2, k > 0);
-      }
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const uint32_t koff = (k & 3) * 32;
-        const uint64_t ad = tc::sw128_desc(a1l + (k >> 2) * (128 * 128) + koff);
-        const uint64_t bd = tc::sw128_desc(sb2 + (k >> 2) * (2 * kVs * 128) + koff);
-        tc::mma_bf16(d1 + kVs, ad, bd, idesc1, true);
-      }
-      tc::mma_commit(&mma_bar);
-    }
-    if (!tc::mbar_wait(&mma_bar, mma_phase)) s_abort = 1;
-    mma_phase ^= 1;
-    tc::tc_fence_after();
-    uint4 o_pack = make_uint4(0u, 0u, 0u, 0u);  // this thread's O, stored after the barrier
-    {
-      float dh[kColsPerThread], dl[kColsPerThread];
-      tc::tmem_ld8(d1 + lane_addr, dh);
-      tc::tmem_ld8(d1 + lane_addr + kVs, dl);
-      if (quad < 2) {  // rows 0..63: U = Util - W S  ->  [U_hi; U_lo]^T operand
-        const int t = row;
-        const float uu[8] = {xu0.x, xu0.y, xu0.z, xu0.w, xu1.x, xu1.y, xu1.z, xu1.w};
-#pragma unroll
-        for (int jj = 0; jj < kColsPerThread; ++jj) {
-          uint16_t hi, lo;
-          tc::split_bf16(uu[jj] - (dh[jj] + dl[jj]), hi, lo);
-          *reinterpret_cast<uint16_t*>(U2 + tc::sw128_offset(j0 + jj, t, 2 * kVs)) = hi;
-          *reinterpret_cast<uint16_t*>(U2 + tc::sw128_offset(kVs + j0 + jj, t, 2 * kVs)) = lo;
-        }
-      } else {  // rows 64..127: O = scale (Q' S + P Util)
-        const float oo[8] = {xu0.x, xu0.y, xu0.z, xu0.w, xu1.x, xu1.y, xu1.z, xu1.w};
-        float x[8];
-#pragma unroll
-        for (int jj = 0; jj < kColsPerThread; ++jj) x[jj] = scale * (dh[jj] + dl[jj] + oo[jj]);
-        o_pack = make_uint4(pack_out16x2<F16>(x[0], x[1]), pack_out16x2<F16>(x[2], x[3]),
-                            pack_out16x2<F16>(x[4], x[5]), pack_out16x2<F16>(x[6], x[7]));
-      }
-    }
-    tc::fence_async_smem();
-    tc::tc_fence_before();
-    __syncthreads();
-    if (quad >= 2 && row - kChunk < len)
-      *reinterpret_cast<uint4*>(a.o + ((tc0 + row - kChunk) * HV + h) * V + v0 + j0) = o_pack;
-    // D2 = Khat_hi^T [U_hi | U_lo] + Khat_lo^T U_hi (into the U_hi half): 4 + 4 K=16 steps
-    if (tid == 0 && !s_abort) {
-      tc::tc_fence_after();
-      const uint32_t kth = tc::smem_u32(stage + kStKTh), ktl = tc::smem_u32(stage + kStKTl);
-      const uint32_t ub = tc::smem_u32(U2);
-#pragma unroll
-      for (int k = 0; k < 4; ++k)
-        tc::mma_bf16(d2, tc::sw128_desc(kth + k * 32), tc::sw128_desc(ub + k * 32), idesc2, k > 0);
-#pragma unroll
-      for (int k = 0; k < 4; ++k)
-        tc::mma_bf16(d2, tc::sw128_desc(ktl + k * 32), tc::sw128_desc(ub + k * 32), idesc1, true);
-      tc::mma_commit(&mma_bar);
-    }
-    if (!tc::mbar_wait(&mma_bar, mma_phase)) s_abort = 1;
-    mma_phase ^= 1;
-    tc::tc_fence_after();
-    {
-      float dh[kColsPerThread], dl[kColsPerThread];
-      tc::tmem_ld8(d2 + lane_addr, dh);
-      tc::tmem_ld8(d2 + lane_addr + kVs, dl);
-      const float gc = reinterpret_cast<const float*>(stage + kStGam)[c];
-#pragma unroll
-      for (int jj = 0; jj < kColsPerThread; ++jj) S[jj] = gc * S[jj] + (dh[jj] + dl[jj]);
-    }
-    write_state_operand();
-    tc::fence_async_smem();
-    tc::tc_fence_before();
-    __syncthreads();
-    if (s_abort) break;
-    if (tid == 32 && ci + 2 < nch) {  // not the MMA-issuing thread
-      tc::fence_async_smem();
-      issue_stage_loads(stage, ws_head + (size_t)(ci + 2) * rec_stride, &full_bar[sidx]);
-      issued = ci + 3;
+      set_error(a.err_flag, KDA_DEVERR_TIMEOUT);
     }
   }
-  if (s_abort) {
-    if (tid == 0) set_error(a.err_flag, KDA_DEVERR_TIMEOUT);
-    if (tid == 32) {
-      // let the bulk copies this CTA still has in flight land before it exits
-      for (int cj = consumed; cj < issued; ++cj)
-        tc::mbar_wait(&full_bar[cj & 1], (cj >> 1) & 1, 1u << 20);
-    }
-  } else {
+  __syncthreads();
+  if (!s_abort && !mma_warp && !copy_warp) {
 #pragma unroll
     for (int jj = 0; jj < kColsPerThread; ++jj) st[(size_t)(v0 + j0 + jj) * K + c] = S[jj];
   }

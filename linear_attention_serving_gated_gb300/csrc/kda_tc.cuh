@@ -126,6 +126,12 @@ __device__ __forceinline__ void bulk_s2g(void* dst, const void* src, uint32_t by
 
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
+// Bulk prefetch of global memory into L2 (no shared memory involved).  src
+// 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // Waits until every committed bulk store of this thread has finished reading
 // shared memory (the source may then be overwritten).
 __device__ __forceinline__ void bulk_wait_read() {

@@ -43,7 +43,7 @@ def test_status_strings(lib):
     assert "workspace" in kda.status_string(kda.KDA_ERR_WORKSPACE)
 
 
-REC_BYTES = 164352  # one (chunk, head) record, as include/kda.h states
+REC_BYTES = 180224  # one (chunk, head) record, as include/kda.h states
 
 
 def test_workspace_size_formula(lib):

@@ -68,7 +68,7 @@ def _largest_fitting_tokens(lib):
 def test_size_limit_is_the_documented_rule():
     lib = _lib()
     t_max = _largest_fitting_tokens(lib)
-    assert t_max == 3263  # 51 records per head at 16 heads, as kda.h states
+    assert t_max == 2943  # 46 records per head at 16 heads, as kda.h states
     assert _noalloc_status(lib, t_max, None) != kda.KDA_ERR_WORKSPACE
     assert _noalloc_status(lib, t_max + 1, None) == kda.KDA_ERR_WORKSPACE
     # the pages' 1 x 4096 shape at 16 heads does not fit
