@@ -503,14 +503,14 @@ def run_ours(args, rank, world, local_rank):
     extras = {} if args.no_extras else run_extras(args, dev, stream, flush_l2, gate_seed=rank)
 
     hbm, bf16_tf, sm_max, peak_kind = _peaks()
-    # The library splits a single long prefill into up to four segments (a
-    # transform and a state-pass launch each) when 8 * heads fits in the SM
-    # count; same rule here, to count the launches.
+    # The library splits a single prefill of 256 chunks or more into four
+    # segments (a transform and a state-pass launch each) when 8 * heads fits
+    # in the SM count; same rule here, to count the launches.
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     def launches_of(T_):
         seq_nch = (T_ + CHUNK - 1) // CHUNK
-        nseg = min(4, seq_nch // 16) if seq_nch >= 32 and 8 * H <= sms else 1
-        return 2 * max(nseg, 1)
+        nseg = 4 if seq_nch >= 256 and 8 * H <= sms else 1
+        return 2 * nseg
 
     prefill_launches = launches_of(PREFILL_T)
     extra_launches = prefill_launches + (0 if args.no_long else

@@ -161,9 +161,9 @@ size_t kda_prefill_workspace_size(kda_dims dims, int num_seqs, int64_t total_tok
  * it before capturing calls into a CUDA graph.
  *
  * Schedule: when every sequence has the same length known on the host (one
- * sequence, or the fixed layout) and spans at least 32 chunks, and
- * 8 * HV * num_seqs does not exceed the SM count, the chunk positions are cut
- * into up to four segments.  Each segment's state pass runs on a second,
+ * sequence, or the fixed layout) and spans at least 256 chunks (16384
+ * tokens), and 8 * HV * num_seqs does not exceed the SM count, the chunk
+ * positions are cut into four segments.  Each segment's state pass runs on a second,
  * highest-priority stream owned by the library while the next segment's
  * transform runs on `stream`.  The state is carried in its pool slot.  That
  * stream and its events are created on the first such call made by each host

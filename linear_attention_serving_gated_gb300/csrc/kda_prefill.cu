@@ -1338,15 +1338,21 @@ unsigned transform_grid(int64_t units, int dev) {
   return (unsigned)(units < g_num_sms[dev] ? units : g_num_sms[dev]);
 }
 
-// Segmented schedule.  When every sequence has the same number of chunks and
-// the state pass occupies at most half of the SMs, the chunk positions are cut
-// into up to kMaxSegments segments of at least kSegmentMinChunks: the pass of
-// segment s runs on a second stream while the transform of segment s+1 runs on
-// the caller's, so the pass (latency-bound, a few SMs) hides under the
-// transform (throughput-bound, all SMs).  The state is carried between pass
-// segments in its pool slot.
+// Segmented schedule.  When every sequence has the same number of chunks, at
+// least kSegmentMinChunks of them, and the state pass occupies at most half
+// of the SMs, the chunk positions are cut into kMaxSegments segments in the
+// ratio 12:10:7:3: the pass of segment s runs on a second stream while the
+// transform of segment s+1 runs on the caller's, so the pass (latency-bound,
+// a few SMs) hides under the transform (throughput-bound, all SMs), and the
+// last, unhidden pass segment is short.  The state is carried between pass
+// segments in its pool slot.  Shorter sequences run unsegmented: their pass
+// is short, and the segments' partial waves and the pass's SMs cost the
+// transform more than the overlap saves (1 x 4096 at 16 heads: 268 against
+// 280 us; 1 x 32768: 1731 unsegmented against 1916 us segmented).
 constexpr int kMaxSegments = 4;
-constexpr int kSegmentMinChunks = 16;
+constexpr int kSegmentMinChunks = 256;
+constexpr int kSegmentWeights[kMaxSegments] = {12, 10, 7, 3};
+constexpr int kSegmentWeightSum = 32;
 
 // The second stream (highest priority, so the pass's CTAs are placed before
 // the transform's waiting ones) and its events: one set per host thread and
@@ -1462,7 +1468,7 @@ extern "C" kda_status kda_prefill(kda_dims dims, kda_gate gate, const kda_bf16* 
   if (total_tokens > 0 && (num_seqs == 1 || !cu_seqlens) &&
       2 * (int64_t)kSlices * dims.HV * num_seqs <= g_num_sms[dev]) {
     seq_nch = (int)((total_tokens / num_seqs + kChunk - 1) / kChunk);
-    nseg = seq_nch / kSegmentMinChunks < kMaxSegments ? seq_nch / kSegmentMinChunks : kMaxSegments;
+    nseg = seq_nch >= kSegmentMinChunks ? kMaxSegments : 1;
   }
   record_stage(0, st);
   if (!gate.A_log && total_tokens > 0) {
@@ -1492,15 +1498,10 @@ extern "C" kda_status kda_prefill(kda_dims dims, kda_gate gate, const kda_bf16* 
     if (cudaEventRecord(ps->fork, st) != cudaSuccess ||
         cudaStreamWaitEvent(ps->stream, ps->fork, 0) != cudaSuccess)
       return KDA_ERR_CUDA;
-    // Equal segments up to 96 chunks; longer sequences get segments in the
-    // ratio 7:5:3:1, so that the last pass segment (the only one not hidden
-    // under a transform) is short (1x8192: 450 against 482 us).
-    static const int kLongWeights[kMaxSegments] = {7, 5, 3, 1};
-    const bool shrink = nseg == kMaxSegments && seq_nch >= 96;
     int pos = 0;
     for (int i = 0; i < nseg && pos < seq_nch && s == KDA_OK; ++i) {
       PrefillArgs sa = args;
-      int want = shrink ? (kLongWeights[i] * seq_nch + 15) / 16 : (seq_nch + nseg - 1) / nseg;
+      int want = (kSegmentWeights[i] * seq_nch + kSegmentWeightSum - 1) / kSegmentWeightSum;
       if (i == nseg - 1 || pos + want > seq_nch) want = seq_nch - pos;
       sa.seg_pos0 = pos;
       sa.seg_len = want;

@@ -54,8 +54,8 @@ def test_fp16_prefill_varlen_with_garbage_padding_and_chunk_states():
     _prefill(d, 2, 2, intermediate=True)
 
 
-def test_fp16_prefill_single_sequence_segmented_16_heads():
-    """1 x 4096 at 16 heads: the benchmark shape, segmented schedule."""
+def test_fp16_prefill_single_sequence_16_heads():
+    """1 x 4096 at 16 heads: the benchmark shape."""
     d = inputs.prefill_inputs(seed=602, lengths=[4096], H=16, slots=16, dtype="f16")
     _prefill(d, 16, 16)
 

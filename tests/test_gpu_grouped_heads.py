@@ -54,8 +54,8 @@ def test_grouped_prefill_varlen_with_chunk_states():
 
 
 def test_grouped_prefill_single_sequence_segmented():
-    """2500 tokens (40 chunk positions) at 4 value heads: the segmented schedule."""
-    d = inputs.prefill_inputs(seed=502, lengths=[2500], H=1, HV=4, slots=3, state_idx=[2])
+    """16450 tokens (258 chunk positions) at 4 value heads: the segmented schedule."""
+    d = inputs.prefill_inputs(seed=502, lengths=[16450], H=1, HV=4, slots=3, state_idx=[2])
     _prefill(d, 1, 4)
 
 

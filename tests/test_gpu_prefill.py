@@ -178,32 +178,34 @@ def test_chunked_prefill_across_calls_matches_one_call():
 
 
 # --- segmented schedule -----------------------------------------------------
-# A long single sequence (or equal-length fixed layout) whose state pass fits
-# in one wave runs in position segments, the pass of segment s on a second
-# stream alongside the transform of segment s+1, the state carried in the
-# pool slot.  These cases pin the segment edges and the carry.
+# A long single sequence (or equal-length fixed layout, 256 chunks or more)
+# whose state pass fits in half the SMs runs in four position segments, the
+# pass of segment s on a second stream alongside the transform of segment
+# s+1, the state carried in the pool slot.  These cases pin the segment edges
+# and the carry.
 
-@pytest.mark.parametrize("T", [2048 + 452, 4097])
+@pytest.mark.parametrize("T", [16384 + 452, 16385])
 def test_segmented_prefill_ragged_tail_with_chunk_states(T):
-    """1 x T at 2 heads: 40 or 65 chunk positions cut into 2 or 4 segments,
-    the last chunk ragged (4 tokens, 1 token); chunk-start states too."""
+    """1 x T at 2 heads: 264 or 257 chunk positions cut into four
+    segments, the last chunk ragged (4 tokens, 1 token); chunk-start states
+    too."""
     d = inputs.prefill_inputs(seed=T, lengths=[T], H=2, slots=3, state_idx=[2])
     check(run_both(d, 2, intermediate=True), d)
 
 
 def test_segmented_prefill_fixed_layout_with_padding_sequence():
-    d = inputs.prefill_inputs(seed=70, lengths=[2100, 2100], H=2, slots=4, state_idx=[3, -1],
+    d = inputs.prefill_inputs(seed=70, lengths=[16400, 16400], H=2, slots=4, state_idx=[3, -1],
                               varlen=False)
     out = run_both(d, 2, varlen=False)
     check(out, d)
-    assert torch.all(out["o"][2100:].float() == 0)
+    assert torch.all(out["o"][16400:].float() == 0)
 
 
 def test_segmented_prefill_bitwise_equals_unsegmented_batch():
     """Sequence A alone (one sequence: segmented) and the same tokens as the
     first sequence of a varlen batch of two (not segmented) give identical
     bits: the schedule does not change the arithmetic."""
-    H, TA, TB = 4, 2500, 100
+    H, TA, TB = 4, 16500, 100
     d = inputs.prefill_inputs(seed=80, lengths=[TA, TB], H=H, slots=4, state_idx=[1, 3])
     og, gg = gates(d, H=H)
     x = {name: dev_bf16(d[name]) for name in ("q", "k", "v", "g", "beta")}
@@ -225,7 +227,7 @@ def test_segmented_prefill_bitwise_equals_unsegmented_batch():
 def test_segmented_prefill_under_graph_capture_matches_eager():
     """The fork to the pass stream and the join back are captured as graph
     edges: a replay gives the eager result bit for bit."""
-    H, T = 16, 4096
+    H, T = 4, 16448
     d = inputs.prefill_inputs(seed=90, lengths=[T], H=H, slots=2, state_idx=[1])
     og, gg = gates(d, H=H)
     x = {name: dev_bf16(d[name]) for name in ("q", "k", "v", "g", "beta")}
