@@ -909,11 +909,8 @@ constexpr uint32_t kPassSmem = kSmS + kSBufs * kSmSBytes + 1024;  // + alignment
 constexpr uint32_t kTmemCols = 256;
 static_assert(kStQ == kStM + kStMBytes && kRecQ == kRecM + kStMBytes, "the record's tiles in stage order");
 static_assert(kPassSmem <= 232448, "shared memory");
-// The output product is M = 128 over the 64-row Q' tile: its rows 64-127
-// read the 8 KB after each of the tile's two atom columns (the second atom
-// column, then the next stage or the state operands), all inside the
-// allocation, and feed TMEM lanes 64-127, which are never read.
-static_assert(kStQ + kStQBytes + 8 * 1024 <= kSmS, "rows past the Q' tile stay in shared memory");
+// The output product is M = 64: its accumulator rows 16 q + l sit in TMEM
+// lanes 32 q + l (l < 16) of the four lane quadrants.
 
 // Copies as 16 KB pieces, which the copy engine keeps in flight together.
 constexpr uint32_t kCopyPiece = 16 * 1024;
@@ -940,7 +937,7 @@ constexpr int kColsPerThread = kVs / 4;
 // state:
 //   chain   D_ch = M_hi [S_hi | S_lo] + M_lo S_hi      (M=128 N=64, then N=32)
 //           S_{i+1} = D_ch[S_hi half] + D_ch[S_lo half] + B_c
-//   output  D_O  = Q' [S_hi | S_lo]                     (M=128 N=64, lanes 0-63 = tokens)
+//   output  D_O  = Q' [S_hi | S_lo]                     (M=64 N=64)
 //           O    = scale (D_O[S_hi half] + D_O[S_lo half] + P Util)
 // Warp 16 issues the products: chunk i's chain product, then chunk i - 1's
 // output product, which thus runs while the epilogue warps turn chunk i's
@@ -1032,6 +1029,7 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
   const uint32_t dch = tmem;
   constexpr uint32_t idesc2 = tc::idesc_bf16_f32(128, 2 * kVs);
   constexpr uint32_t idesc1 = tc::idesc_bf16_f32(128, kVs);
+  constexpr uint32_t idescO = tc::idesc_bf16_f32(kChunk, 2 * kVs);
 
   if (copy_warp) {
     // ---- copy warp (one lane) ----
@@ -1096,7 +1094,7 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
         for (int k = 0; k < 8; ++k) {  // Q' [S_hi | S_lo]; Q' atom columns are 64 rows (8 KB) apart
           const uint32_t koff = (k & 3) * 32;
           tc::mma_bf16(dO, tc::sw128_desc(qq + (k >> 2) * (kChunk * 128) + koff),
-                       tc::sw128_desc(sb2 + (k >> 2) * (2 * kVs * 128) + koff), idesc2, k > 0);
+                       tc::sw128_desc(sb2 + (k >> 2) * (2 * kVs * 128) + koff), idescO, k > 0);
         }
         tc::mma_commit(&o_bar[cj & 1]);
       };
@@ -1150,7 +1148,7 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
     };
     auto load_pu = [&](int ci, float4& u0, float4& u1) {  // P Util rows t, [slice][quad][64][4]
       const float4* src = reinterpret_cast<const float4*>(ws_head + (size_t)ci * rec_stride + kRecOi) +
-                          (slice * (kVs / 4) + j0 / 4) * kChunk + (row & (kChunk - 1));
+                          (slice * (kVs / 4) + j0 / 4) * kChunk + (quad * 16 + (lane & 15));
       u0 = __ldcg(src);
       u1 = __ldcg(src + kChunk);
     };
@@ -1179,9 +1177,9 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
     };
     const uint32_t lane_addr = (static_cast<uint32_t>(quad * 32) << 16) + j0;
     const float scale = a.gate.scale;
-    // chunk cj's output: TMEM lanes 0-63 are its tokens (quadrants 0-1)
+    // chunk cj's output: token 16 q + l is in TMEM lane 32 q + l (l < 16)
+    const int orow = quad * 16 + (lane & 15);
     auto output = [&](int cj, const float4& u0, const float4& u1) -> bool {
-      if (quad >= 2) return true;
       const bool ok = tc::mbar_wait(&o_bar[cj & 1], (cj >> 1) & 1);
       tc::tc_fence_after();
       float dh[kColsPerThread], dl[kColsPerThread];
@@ -1194,8 +1192,8 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
       for (int jj = 0; jj < kColsPerThread; ++jj) x[jj] = a.gate.scale * (dh[jj] + dl[jj] + oo[jj]);
       const int64_t tcj = t0 + (int64_t)(p0 + cj) * kChunk;
       const int len = (int)(t1 - tcj < kChunk ? t1 - tcj : kChunk);
-      if (row < len)
-        *reinterpret_cast<uint4*>(a.o + ((tcj + row) * HV + h) * V + v0 + j0) =
+      if (lane < 16 && orow < len)
+        *reinterpret_cast<uint4*>(a.o + ((tcj + orow) * HV + h) * V + v0 + j0) =
             make_uint4(pack_out16x2<F16>(x[0], x[1]), pack_out16x2<F16>(x[2], x[3]),
                        pack_out16x2<F16>(x[4], x[5]), pack_out16x2<F16>(x[6], x[7]));
       tc::tc_fence_before();
