@@ -85,7 +85,18 @@ constexpr uint32_t kRecML = kRecM + 128 * 128 * 2;             // M_c lo
 constexpr uint32_t kRecQ = kRecML + 128 * 128 * 2;             // Q' (BF16), 64 x 128
 constexpr uint32_t kRecB = kRecQ + 64 * 128 * 2;               // B_c, FP32 [slice][quad][128][4]
 constexpr uint32_t kRecOi = kRecB + kHeadDim * kHeadDim * 4;   // P Util, FP32 [slice][quad][64][4]
-constexpr uint32_t kRecBytes = kRecOi + kChunk * kHeadDim * 4;
+constexpr uint32_t kRecMeta = kRecOi + kChunk * kHeadDim * 4;   // skip thresholds, FP32 [slice]
+constexpr uint32_t kRecBytes = kRecMeta + 128;
+// Skipping a chain product.  With r = 128 max|M_c| >= every row sum of |M_c|,
+// each element of the chain product M_c S is at most about r max|S| in
+// magnitude (the split operands add a factor below 1 + 2^-7).  When that is
+// below half an ulp of every element of B_c -- below 2^-25 min|B_c| -- the
+// FP32 sum S_end = M_c S + B_c rounds to B_c whatever the product is, so the
+// product can be left out without changing a bit of the state.  The record
+// keeps tau = 2^-27 min|B_c| / r per value slice (a factor 4 of margin); the
+// pass skips the product iff max|S| <= tau, the max taken over the slice's
+// start state.  tau = +inf marks an all-zero M_c, which is not stored.
+constexpr float kSkipMargin = 7.450580596923828125e-09f;  // 2^-27
 
 struct PrefillArgs {
   GateArgs gate;
@@ -196,7 +207,10 @@ constexpr uint32_t kTxV = kTxK + kChunk * kLdB * 2;   // raw v
 constexpr uint32_t kTxG = kTxV + kChunk * kLdB * 2;   // Gam FP32 [64][kLd]
 constexpr uint32_t kTxTf = kTxAf + kChunk * kLdT * 4;  // (I+A)^-1 FP32 [64][kLdT] (reuses L/R)
 constexpr uint32_t kTxMisc = kTxG + kChunk * kLd * 4;  // rq, rk, beta [64] each + scratch [1536]
-constexpr uint32_t kTxEnd = kTxMisc + (3 * kChunk + 1536) * 4;
+                                                       // + dt_bias [128], A_log [1] (+3),
+                                                       // raw beta [64] (16-bit)
+constexpr uint32_t kTxEnd = kTxMisc + (3 * kChunk + 1536 + kHeadDim + 4 + kChunk / 2) * 4;
+constexpr int kDescBatch = 64;  // unit descriptors looked up together
 constexpr uint32_t kTransformTcSmem = kTxEnd + 1024;
 constexpr uint32_t kTxTmemCols = 512;  // M1, A2, M2: 0-255; the map product: 256-511
 static_assert(2 * 256 * 64 * 2 <= kTxA2, "B2 fits in the L/R region");
@@ -206,7 +220,7 @@ static_assert(kTxB3 + 2 * 256 * 64 * 2 <= kTxR && kTxMs + 2 * 128 * 128 * 2 <= k
 static_assert(kTxQ % 16 == 0 && kTxK % 16 == 0 && kTxV % 16 == 0 && kTxG % 16 == 0 &&
                   kTxTf % 16 == 0 && kTxMisc % 16 == 0 && kTxA2 % 1024 == 0 && kTxR % 1024 == 0,
               "alignment");
-static_assert(kTransformTcSmem <= 232448, "shared memory");
+static_assert(kTransformTcSmem + kDescBatch * 16 + 256 <= 232448, "shared memory");
 
 // Eight consecutive values -> one 16-byte chunk in each of hi and lo
 // (hi = RN(x), lo = RN(x - hi), both BF16).
@@ -279,16 +293,29 @@ __device__ ChunkLoc unit_loc(const PrefillArgs& a, int64_t u, int64_t* cid, int*
   return locate_chunk(a, cx);
 }
 
-// Persistent: CTA b takes units b, b + gridDim.x, ...  While it works on one
-// unit, the next unit's q, k, v and gate rows are prefetched into L2.
+// Global chunk id of transform unit u (arithmetic only; see unit_loc).
+__device__ __forceinline__ int64_t unit_cid(const PrefillArgs& a, int64_t u) {
+  const int64_t cx = u / a.HV;
+  if (a.seg_len > 0) return (cx / a.seg_len) * a.seq_nch + a.seg_pos0 + cx % a.seg_len;
+  return cx;
+}
+
+// Persistent: CTA b takes units b, b + gridDim.x, ...  The next unit's q, k, v
+// and gate rows are copied into shared memory while this unit finishes.
 template <bool F16>
 __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const PrefillArgs a) {
   extern __shared__ uint8_t smraw[];
+  // Unit descriptor: first token and length of the unit's chunk; n < 0 marks
+  // a unit that is skipped (no chunk, padding or rejected sequence).
+  struct UnitDesc {
+    int64_t t0;
+    int n, len;
+  };
   __shared__ uint64_t mma_bar;
   __shared__ uint32_t tmem_base;
-  __shared__ ChunkLoc loc, s_nloc;
-  __shared__ int64_t s_cid, s_ncid;
-  __shared__ int skip, s_abort, s_ok, s_h, s_nh, s_nskip, s_nvalid;
+  __shared__ UnitDesc s_desc[kDescBatch];
+  __shared__ int s_abort, s_ok;
+  __shared__ uint32_t s_mmax, s_bmin[kSlices];  // max|M_c|, min|B_c| per slice (FP32 bits, >= 0)
 
   uint8_t* sb = smraw + ((1024u - (tc::smem_u32(smraw) & 1023u)) & 1023u);
   uint8_t* Lt = sb + kTxL;  // M1 left operand, TF32 128 x 128
@@ -298,6 +325,7 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
   uint8_t* Bl = Bh + 256 * 64 * 2;
   uint8_t* A2h = sb + kTxA2;
   uint8_t* A2l = A2h + 128 * 64 * 2;
+  uint8_t* Gs = A2l;  // raw gate input [64][128] (16-bit), dead from M2 to the next A2 product
   uint8_t* Qs = sb + kTxQ;
   uint8_t* Ks = sb + kTxK;
   uint8_t* Vs = sb + kTxV;
@@ -308,11 +336,13 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
   float* rk = rq + kChunk;
   float* bt = rk + kChunk;
   float* X = bt + kChunk;  // [6][16][16]
+  float* gbias = X + 1536;    // dt_bias of the unit's head [128]
+  float* galog = gbias + kHeadDim;  // A_log of the unit's head
+  uint16_t* braw = reinterpret_cast<uint16_t*>(galog + 4);  // raw beta of the unit's tokens
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) {
     s_abort = 0;
-    s_nvalid = 0;
     s_ok = seqlens_valid(a);
     if (!s_ok && blockIdx.x == 0) set_error(a.err_flag, KDA_DEVERR_SEQLENS);
     tc::mbar_init(&mma_bar, 1);
@@ -324,82 +354,92 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
   tc::tc_fence_after();
   const uint32_t tmem = tmem_base;
   uint32_t phase = 0;
-  // Unit descriptor (chunk location, head, whether it is skipped).  The next
-  // unit's is worked out by warp 1 while the tensor core runs this unit's M2
-  // product, together with an L2 prefetch of its rows, so that the slot lookup
-  // and the row loads are off the per-unit path; a unit whose predecessor was
-  // skipped (or the first) looks itself up.
-  auto describe = [&](int64_t uu, ChunkLoc* l, int64_t* cid, int* hh) -> int {
-    *l = unit_loc(a, uu, cid, hh);
-    if (l->n < 0) return 1;
-    const int slot = a.state_idx[l->n];
-    if (slot < 0 || slot >= a.pool_slots) return 1;    // padding / rejected sequence
-    if (a.seq_flags && a.seq_flags[l->n]) return 1;    // given decay out of range
-    return 0;
+  // Descriptors of this CTA's next kDescBatch units, one thread each, so that
+  // the slot lookups (dependent global reads) of a batch overlap.
+  auto describe = [&](int64_t uu) -> UnitDesc {
+    int64_t cid;
+    int hh;
+    const ChunkLoc l = unit_loc(a, uu, &cid, &hh);
+    if (l.n < 0) return UnitDesc{0, -1, 0};
+    const int slot = a.state_idx[l.n];
+    if (slot < 0 || slot >= a.pool_slots) return UnitDesc{0, -1, 0};  // padding / rejected
+    if (a.seq_flags && a.seq_flags[l.n]) return UnitDesc{0, -1, 0};    // given decay out of range
+    return UnitDesc{l.t0, l.n, l.len};
   };
-  for (int64_t u = blockIdx.x; s_ok && u < a.tx_units; u += gridDim.x) {
-    __syncthreads();  // every thread is done with the previous unit's shared values
-    if (tid == 0) {
-      if (s_nvalid) {
-        loc = s_nloc;
-        s_cid = s_ncid;
-        s_h = s_nh;
-        skip = s_nskip;
-      } else {
-        int64_t cid;
-        int hh;
-        skip = describe(u, &loc, &cid, &hh);
-        s_cid = cid;
-        s_h = hh;
-      }
-      s_nvalid = 0;
+  // A unit's raw q, k, v rows into Qs, Ks, Vs and its gate input rows into Gs
+  // (16-byte asynchronous copies, one row piece per thread and tensor; rows
+  // past the chunk's end are zero-filled), dt_bias and A_log of its head into
+  // gbias and galog, and the raw beta of its tokens into braw (plain loads by
+  // threads 64-127, which have nothing else to do until the next barrier).
+  auto issue_rows = [&](const UnitDesc& ud, int hh) {
+    static_assert(kTxThreads == kChunk * 16, "one 16-byte piece of each row per thread");
+    const int hkk = hh / (a.HV / a.H), row = tid >> 4, piece = (tid & 15) * 8;
+    const bool live = row < ud.len;
+    const int64_t tok = ud.t0 + (live ? row : 0);
+    const uint32_t nb = live ? 16u : 0u;
+    cp_async16_zfill(Qs + (row * kLdB + piece) * 2, a.q + (tok * a.H + hkk) * kHeadDim + piece, nb);
+    cp_async16_zfill(Ks + (row * kLdB + piece) * 2, a.k + (tok * a.H + hkk) * kHeadDim + piece, nb);
+    cp_async16_zfill(Vs + (row * kLdB + piece) * 2, a.v + (tok * a.HV + hh) * kHeadDim + piece, nb);
+    cp_async16_zfill(Gs + (row * kHeadDim + piece) * 2, a.g + (tok * a.HV + hh) * kHeadDim + piece, nb);
+    if (tid < kHeadDim / 4 && a.gate.dt_bias) cp_async16(gbias + tid * 4, a.gate.dt_bias + hh * kHeadDim + tid * 4);
+    if (tid == kHeadDim / 4 && a.gate.A_log) cp_async4(galog, a.gate.A_log + hh);
+    cp_async_commit();
+    if (tid >= kChunk && tid < 2 * kChunk) {
+      const int t = tid - kChunk;
+      braw[t] = t < ud.len ? a.beta[(ud.t0 + t) * a.HV + hh] : 0;
     }
-    __syncthreads();
-    if (skip) continue;
-    const int h = s_h;
-    const int64_t cid = s_cid;
-    const int len = loc.len;
-    const int64_t t0 = loc.t0;
+  };
+  bool rows_ready = false;  // this unit's rows were copied during the previous unit
+  int it = 0;               // units of this CTA so far
+  for (int64_t u = blockIdx.x; s_ok && u < a.tx_units; u += gridDim.x, ++it) {
+    const int bi = it % kDescBatch;
+    if (bi == 0) {
+      __syncthreads();  // nobody reads the previous batch any more
+      if (tid < kDescBatch) {
+        const int64_t uu = u + (int64_t)tid * gridDim.x;
+        s_desc[tid] = uu < a.tx_units ? describe(uu) : UnitDesc{0, -1, 0};
+      }
+    }
+    __syncthreads();  // every thread is done with the previous unit's shared values
+    if (tid == 0) {  // read by 9c, after several barriers
+      s_mmax = 0u;
+      for (int sl = 0; sl < kSlices; ++sl) s_bmin[sl] = 0x7f800000u;  // +inf
+    }
+    const UnitDesc ud = s_desc[bi];
+    if (ud.n < 0) {
+      rows_ready = false;
+      continue;
+    }
+    const int h = (int)(u % a.HV);
+    const int64_t cid = unit_cid(a, u);
+    const int len = ud.len;
     const GateArgs& ga = a.gate;
-    const int H = a.H, HV = a.HV, K = kHeadDim;
-    const int hk = h / (HV / H);  // q/k head of value head h
-    uint8_t* rec = a.ws + ((size_t)cid * HV + h) * kRecBytes;
+    const int K = kHeadDim;
+    uint8_t* rec = a.ws + ((size_t)cid * a.HV + h) * kRecBytes;
 
-    // 1. fold.  Warp w owns tokens [2w, 2w+2), lane l channels [4l, 4l+4); all
-    //    global loads of the warp are issued before any use.  Raw q, k, v stay
-    //    BF16 in shared memory, with the per-token norms; Gam by warp-blocked
-    //    prefix (the running sum of a warp's last token is its total).  The
-    //    previous unit's output staging (L/R and A2 regions) may still be read
-    //    by its bulk stores: the fold writes none of it.
+    // 1. fold.  The unit's rows are in shared memory (copied during the
+    //    previous unit, or now).  Warp w owns tokens [2w, 2w+2), lane l
+    //    channels [4l, 4l+4): every shared-memory access of a warp is one
+    //    whole row.  Per-token norms and beta, and Gam by warp-blocked prefix
+    //    (the running sum of a warp's last token is its total).  The previous
+    //    unit's output staging (L/R and A2h regions) may still be read by its
+    //    bulk stores: the fold writes none of it.
+    if (!rows_ready) issue_rows(ud, h);
+    cp_async_wait_all();
+    __syncthreads();
     {
       constexpr int kTpw = kChunk / kTxWarps;  // tokens per warp
       const int c = lane * 4;
-      uint2 qr[kTpw], kr[kTpw], vr[kTpw], ar[kTpw];
-      float br[kTpw];
-      const float alog = ga.A_log ? __ldg(ga.A_log + h) : 0.f;
-      const float4 bias = ga.dt_bias ? __ldg(reinterpret_cast<const float4*>(ga.dt_bias + h * K + c))
-                                     : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int u = 0; u < kTpw; ++u) {
-        const int t = warp * kTpw + u;
-        qr[u] = kr[u] = vr[u] = ar[u] = make_uint2(0u, 0u);
-        br[u] = 0.f;
-        if (t < len) {
-          const int64_t tok = t0 + t;
-          qr[u] = __ldg(reinterpret_cast<const uint2*>(a.q + (tok * H + hk) * K + c));
-          kr[u] = __ldg(reinterpret_cast<const uint2*>(a.k + (tok * H + hk) * K + c));
-          vr[u] = __ldg(reinterpret_cast<const uint2*>(a.v + (tok * HV + h) * K + c));
-          ar[u] = __ldg(reinterpret_cast<const uint2*>(a.g + (tok * HV + h) * K + c));
-          if (lane == 0) br[u] = in16_to_float<F16>(a.beta[tok * HV + h]);
-        }
-      }
-      const float exp_alog = __expf(alog);
+      const float exp_alog = ga.A_log ? __expf(*galog) : 0.f;
+      const float4 bias = ga.dt_bias ? f4(gbias + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+      if (tid < kChunk) bt[tid] = tid < len ? fold_beta(ga, in16_to_float<F16>(braw[tid])) : 0.f;
       float4 run = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-      for (int u = 0; u < kTpw; ++u) {
-        const int t = warp * kTpw + u;
+      for (int u2 = 0; u2 < kTpw; ++u2) {
+        const int t = warp * kTpw + u2;
         const bool live = t < len;
-        const float4 q4 = in16x4_to_f4<F16>(qr[u]), k4 = in16x4_to_f4<F16>(kr[u]), a4 = in16x4_to_f4<F16>(ar[u]);
+        const float4 q4 = ld_in4<F16>(Qs, t, c), k4 = ld_in4<F16>(Ks, t, c);
+        const float4 a4 = in16x4_to_f4<F16>(*reinterpret_cast<const uint2*>(Gs + (t * K + c) * 2));
         const float sq = warp_sum(dot4(q4, q4)), sk = warp_sum(dot4(k4, k4));
         float4 g4 = make_float4(0.f, 0.f, 0.f, 0.f);
         if (live)
@@ -410,11 +450,7 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
         if (lane == 0) {
           rq[t] = live ? (ga.use_qk_l2norm ? rsqrtf(sq + kNormEps) : 1.f) : 0.f;
           rk[t] = live ? (ga.use_qk_l2norm ? rsqrtf(sk + kNormEps) : 1.f) : 0.f;
-          bt[t] = live ? fold_beta(ga, br[u]) : 0.f;
         }
-        *reinterpret_cast<uint2*>(Qs + (t * kLdB + c) * 2) = qr[u];
-        *reinterpret_cast<uint2*>(Ks + (t * kLdB + c) * 2) = kr[u];
-        *reinterpret_cast<uint2*>(Vs + (t * kLdB + c) * 2) = vr[u];
         run = make_float4(run.x + g4.x, run.y + g4.y, run.z + g4.z, run.w + g4.w);
         f4(GM + t * kLd + c) = run;
       }
@@ -426,8 +462,8 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
       }
       __syncthreads();  // every warp has read the totals it needs before any row changes
 #pragma unroll
-      for (int u = 0; u < kTpw; ++u) {
-        float4& gg = f4(GM + (warp * kTpw + u) * kLd + c);
+      for (int u2 = 0; u2 < kTpw; ++u2) {
+        float4& gg = f4(GM + (warp * kTpw + u2) * kLd + c);
         gg = make_float4(gg.x + pre.x, gg.y + pre.y, gg.z + pre.z, gg.w + pre.w);
       }
     }
@@ -717,39 +753,6 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
       }
       st_split8(KTh, KTl, tc::sw128_offset(c, j * 8, K), x);
     }
-    if (warp == 1) {  // the next unit: descriptor, and its rows -> L2 (4 tensors x 64 tokens x 2 lines)
-      ChunkLoc nl{-1, 0, 0};
-      int nh = 0;
-      const int64_t un = u + gridDim.x;
-      if (un < a.tx_units) {
-        if (lane == 0) {
-          int64_t ncid;
-          s_nskip = describe(un, &nl, &ncid, &nh);
-          s_nloc = nl;
-          s_ncid = ncid;
-          s_nh = nh;
-          s_nvalid = 1;
-        }
-        nl.n = __shfl_sync(0xffffffffu, nl.n, 0);
-        nl.len = __shfl_sync(0xffffffffu, nl.len, 0);
-        nl.t0 = __shfl_sync(0xffffffffu, nl.t0, 0);
-        nh = __shfl_sync(0xffffffffu, nh, 0);
-        if (nl.n >= 0) {
-          const int hkn = nh / (a.HV / a.H);  // q/k head of the value head
-          for (int i = lane; i < 512; i += 32) {
-            const int tensor = i >> 7, tok = (i >> 1) & 63, part = i & 1;
-            if (tok < nl.len) {
-              const int64_t row = nl.t0 + tok;
-              const kda_bf16* base = tensor == 0 ? a.q + (row * a.H + hkn) * kHeadDim
-                                   : tensor == 1 ? a.k + (row * a.H + hkn) * kHeadDim
-                                   : tensor == 2 ? a.v + (row * a.HV + nh) * kHeadDim
-                                                 : a.g + (row * a.HV + nh) * kHeadDim;
-              asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const uint8_t*>(base) + part * 128));
-            }
-          }
-        }
-      }
-    }
     if (!tc::mbar_wait(&mma_bar, phase)) s_abort = 1;
     phase ^= 1;
     tc::tc_fence_after();
@@ -840,6 +843,18 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
         tc::mma_commit(&mma_bar);
       }
     }
+    // The next unit's rows: this unit reads Qs, Ks, Vs and Gs no more, so they
+    // are copied now, behind the map product's issue, and land while it and
+    // 9c run.  A next unit in the next descriptor batch, or skipped, is not
+    // prefetched.
+    rows_ready = false;
+    if (bi + 1 < kDescBatch) {
+      const UnitDesc nd = s_desc[bi + 1];
+      if (nd.n >= 0) {
+        issue_rows(nd, (int)((u + gridDim.x) % a.HV));
+        rows_ready = true;
+      }
+    }
     if (!tc::mbar_wait(&mma_bar, phase)) s_abort = 1;
     phase ^= 1;
     tc::tc_fence_after();
@@ -860,6 +875,12 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
         const float gam = decay_exp(GM[(kChunk - 1) * kLd + row]);
 #pragma unroll
         for (int e = 0; e < 32; ++e) d[e] = (c0 + e == row ? gam : 0.f) - d[e];
+        uint32_t mx = 0u;  // max |d| as FP32 bits (monotone for non-negative values; NaN is largest)
+#pragma unroll
+        for (int e = 0; e < 32; ++e) mx = max(mx, __float_as_uint(d[e]) & 0x7fffffffu);
+#pragma unroll
+        for (int m = 16; m; m >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, m));
+        if (lane == 0) atomicMax(&s_mmax, mx);
         uint8_t* Mh = sb + kTxMs;
 #pragma unroll
         for (int j = 0; j < 4; ++j)
@@ -869,6 +890,12 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
 #pragma unroll
         for (int qd = 0; qd < kVs / 4; ++qd)
           dst[qd * kHeadDim] = make_float4(d[4 * qd], d[4 * qd + 1], d[4 * qd + 2], d[4 * qd + 3]);
+        uint32_t mn = 0xffffffffu;  // min |B_c| of the slice as FP32 bits
+#pragma unroll
+        for (int e = 0; e < 32; ++e) mn = min(mn, __float_as_uint(d[e]) & 0x7fffffffu);
+#pragma unroll
+        for (int m = 16; m; m >>= 1) mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, m));
+        if (lane == 0) atomicMin(&s_bmin[cg - 4], mn);
       }
     }
     if (s_abort && tid == 0) set_error(a.err_flag, KDA_DEVERR_TIMEOUT);
@@ -876,11 +903,23 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
     tc::tc_fence_before();
     __syncthreads();
     if (tid == 0) {
-      static_assert(kRecML == kRecM + 128 * 128 * 2, "M_c hi and lo are contiguous");
-      tc::bulk_s2g(rec + kRecM, sb + kTxMs, 2 * 128 * 128 * 2);
-      tc::bulk_commit();  // awaited at the end of the next unit's fold, or on exit
+      const float mmax = __uint_as_float(s_mmax);
+      const float r = 128.f * mmax;  // NaN stays NaN: never skipped
+      float* meta = reinterpret_cast<float*>(rec + kRecMeta);
+      // an infinite or NaN bound never skips; a finite one stays below +inf,
+      // which marks the all-zero map alone
+      for (int sl = 0; sl < kSlices; ++sl)
+        meta[sl] = s_mmax == 0u ? __int_as_float(0x7f800000)
+                 : r < __int_as_float(0x7f800000) ? fminf(kSkipMargin * __uint_as_float(s_bmin[sl]) / r, 3.402823466e38f)
+                                                  : -1.f;
+      if (s_mmax != 0u) {  // an all-zero M_c is never read
+        static_assert(kRecML == kRecM + 128 * 128 * 2, "M_c hi and lo are contiguous");
+        tc::bulk_s2g(rec + kRecM, sb + kTxMs, 2 * 128 * 128 * 2);
+        tc::bulk_commit();  // awaited at the end of the next unit's fold, or on exit
+      }
     }
   }  // units
+  cp_async_wait_all();  // no copy into shared memory outlives the CTA
   if (tid == 0) tc::bulk_wait_read();  // shared memory stays valid until read
   tc::tc_fence_before();
   __syncthreads();
@@ -907,6 +946,7 @@ constexpr uint32_t kPassSmem = kSmS + kSBufs * kSmSBytes + 1024;  // + alignment
 // TMEM: the chain product in columns 0-63 (S_hi | S_lo halves), the output
 // product in 64-127 or 128-191 (two buffers)
 constexpr uint32_t kTmemCols = 256;
+constexpr int kOBufs = 2;  // output product buffers (TMEM columns, o_bar barriers)
 static_assert(kStQ == kStM + kStMBytes && kRecQ == kRecM + kStMBytes, "the record's tiles in stage order");
 static_assert(kPassSmem <= 232448, "shared memory");
 // The output product is M = 64: its accumulator rows 16 q + l sit in TMEM
@@ -948,10 +988,13 @@ constexpr int kColsPerThread = kVs / 4;
 template <bool F16>
 __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const PrefillArgs a) {
   extern __shared__ uint8_t smraw[];
-  __shared__ uint64_t m_full[2], q_full[2];  // stage i & 1 holds chunk i's M_c / Q'
-  __shared__ uint64_t m_free[2];             // chunk i's chain product is done (its M_c is free)
-  __shared__ uint64_t ch_bar, o_bar[2];      // chain product done; chunk i's output product done
-  __shared__ uint64_t s_ready;               // the next state operand is written (per-warp arrivals)
+  // M_c stage j & 1 holds the j-th M_c copied (maps that are all zero are not
+  // copied); Q' stage i & 1 holds chunk i's Q'.
+  __shared__ uint64_t m_full[2], q_full[2];
+  __shared__ uint64_t m_free[2];             // the M_c stage is free again
+  __shared__ uint64_t ch_bar, o_bar[kOBufs];  // chain product done; chunk i's output product done (i % 2)
+  __shared__ uint64_t s_ready[kSBufs];       // state operand buffer b written (per-warp arrivals)
+  __shared__ uint32_t s_pmax[kSBufs][kPassEpiThreads / 32];  // per-warp max|S| (FP32 bits) of buffer b's state
   __shared__ uint32_t tmem_base;
   __shared__ int64_t s_t0, s_t1, s_cbase;
   __shared__ int s_state, s_abort;
@@ -992,10 +1035,10 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
       tc::mbar_init(&m_full[i], 1);
       tc::mbar_init(&q_full[i], 1);
       tc::mbar_init(&m_free[i], 1);
-      tc::mbar_init(&o_bar[i], 1);
     }
     tc::mbar_init(&ch_bar, 1);
-    tc::mbar_init(&s_ready, kPassEpiThreads / 32);  // one arrival per epilogue warp
+    for (int b = 0; b < kOBufs; ++b) tc::mbar_init(&o_bar[b], 1);
+    for (int b = 0; b < kSBufs; ++b) tc::mbar_init(&s_ready[b], kPassEpiThreads / 32);  // one arrival per epilogue warp
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
@@ -1031,98 +1074,129 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
   constexpr uint32_t idesc1 = tc::idesc_bf16_f32(128, kVs);
   constexpr uint32_t idescO = tc::idesc_bf16_f32(kChunk, 2 * kVs);
 
+  // Chunk ci's skip threshold for this slice (+inf: M_c is all zero and not
+  // stored), and the decision every role takes the same way from it and from
+  // the per-warp maxima of the chunk's start state.
+  auto tau_of = [&](int ci) -> float {
+    return __ldcg(reinterpret_cast<const float*>(ws_head + (size_t)ci * rec_stride + kRecMeta) + slice);
+  };
+  auto map_stored = [](float tau) { return __float_as_uint(tau) != 0x7f800000u; };
+  auto state_max = [&](int b) -> float {  // max|S| of the state in buffer b (NaN is largest)
+    uint32_t m = 0u;
+#pragma unroll
+    for (int w = 0; w < kPassEpiThreads / 32; ++w) m = max(m, s_pmax[b][w]);
+    return __uint_as_float(m);
+  };
+  auto skip_chain = [&](float tau, float smax) { return !map_stored(tau) || smax <= tau; };
+
   if (copy_warp) {
     // ---- copy warp (one lane) ----
     if (lane == 0) {
-      auto prefetch_record = [&](int cj) {  // the operand tiles, this slice of B_c and P Util
-        const uint8_t* rec = ws_head + (size_t)cj * rec_stride;
-        tc::bulk_prefetch_l2(rec + kRecM, kStageBytes);
+      auto rec_of = [&](int cj) { return ws_head + (size_t)cj * rec_stride; };
+      auto prefetch_record = [&](int cj, bool with_m) {  // the operand tiles, this slice of B_c and P Util
+        const uint8_t* rec = rec_of(cj);
+        if (with_m) tc::bulk_prefetch_l2(rec + kRecM, kStMBytes);
+        tc::bulk_prefetch_l2(rec + kRecQ, kStQBytes);
         tc::bulk_prefetch_l2(rec + kRecB + slice * (kVs * kHeadDim * 4), kVs * kHeadDim * 4);
         tc::bulk_prefetch_l2(rec + kRecOi + slice * (kVs * kChunk * 4), kVs * kChunk * 4);
       };
-      auto copy_m = [&](int cj) {
-        issue_copy(smb + (cj & 1) * kStageBytes + kStM, ws_head + (size_t)cj * rec_stride + kRecM, kStMBytes,
-                   &m_full[cj & 1]);
-      };
-      auto copy_q = [&](int cj) {
-        issue_copy(smb + (cj & 1) * kStageBytes + kStQ, ws_head + (size_t)cj * rec_stride + kRecQ, kStQBytes,
-                   &q_full[cj & 1]);
-      };
-      int issued = 0;  // chunks whose two copies were issued
-      for (; issued < 2 && issued < nch; ++issued) {
-        copy_m(issued);
-        copy_q(issued);
-      }
-      for (int cj = 2; cj < 2 + kPassL2Ahead && cj < nch; ++cj) prefetch_record(cj);
+      auto tau_ahead = [&](int cj) { return cj < nch ? tau_of(cj) : 0.f; };
+      float ta0 = tau_ahead(0), ta1 = tau_ahead(1), ta2 = tau_ahead(2), ta3 = tau_ahead(3);  // chunks cj .. cj + 3
+      for (int cj = 1; cj < kPassL2Ahead && cj < nch; ++cj) prefetch_record(cj, map_stored(cj == 1 ? ta1 : ta2));
+      int m_issued = 0, q_issued = 0;  // M_c and Q' copies issued
       bool abort = false;
-      for (int cj = 2; cj < nch && !abort; ++cj) {
-        // stage cj & 1 held chunk cj - 2: its M_c is free once that chunk's
-        // chain product is done, its Q' once its output product is
-        if (!tc::mbar_wait(&m_free[cj & 1], ((cj - 2) >> 1) & 1)) abort = true;
-        if (!abort) {
+      for (int cj = 0; cj < nch && !abort; ++cj) {
+        if (map_stored(ta0)) {  // the M_c stage m_issued & 1 last held copy m_issued - 2
+          if (m_issued >= 2 && !tc::mbar_wait(&m_free[m_issued & 1], ((m_issued - 2) >> 1) & 1)) {
+            abort = true;
+            break;
+          }
           tc::fence_async_smem();
-          copy_m(cj);
-          if (cj + kPassL2Ahead < nch) prefetch_record(cj + kPassL2Ahead);
+          issue_copy(smb + (m_issued & 1) * kStageBytes + kStM, rec_of(cj) + kRecM, kStMBytes, &m_full[m_issued & 1]);
+          ++m_issued;
         }
-        if (!abort && !tc::mbar_wait(&o_bar[cj & 1], ((cj - 2) >> 1) & 1)) abort = true;
-        if (!abort) {
-          tc::fence_async_smem();
-          copy_q(cj);
-          issued = cj + 1;
+        // the Q' stage cj & 1 held chunk cj - 2's Q': free once its output product is done
+        if (cj >= 2 && !tc::mbar_wait(&o_bar[(cj - 2) % kOBufs], ((cj - 2) / kOBufs) & 1)) {
+          abort = true;
+          break;
         }
+        tc::fence_async_smem();
+        issue_copy(smb + (cj & 1) * kStageBytes + kStQ, rec_of(cj) + kRecQ, kStQBytes, &q_full[cj & 1]);
+        ++q_issued;
+        if (cj + kPassL2Ahead < nch) prefetch_record(cj + kPassL2Ahead, map_stored(ta3));
+        ta0 = ta1;
+        ta1 = ta2;
+        ta2 = ta3;
+        ta3 = tau_ahead(cj + 4);
       }
       if (abort) {
         s_abort = 1;
         set_error(a.err_flag, KDA_DEVERR_TIMEOUT);
       }
-      // no copy may outlive the CTA; the last ones issued are the latest
-      // phases of their barriers (an M_c copy issued without its Q' copy
-      // has landed or times out here as well)
-      for (int cj = issued - 2 > 0 ? issued - 2 : 0; cj < issued + (abort ? 1 : 0) && cj < nch; ++cj) {
-        tc::mbar_wait(&m_full[cj & 1], (cj >> 1) & 1, 1u << 20);
-        if (cj < issued) tc::mbar_wait(&q_full[cj & 1], (cj >> 1) & 1, 1u << 20);
-      }
+      // no copy may outlive the CTA: the last two of each kind are the
+      // latest phases of their barriers
+      for (int j = m_issued - 2 > 0 ? m_issued - 2 : 0; j < m_issued; ++j)
+        tc::mbar_wait(&m_full[j & 1], (j >> 1) & 1, 1u << 20);
+      for (int j = q_issued - 2 > 0 ? q_issued - 2 : 0; j < q_issued; ++j)
+        tc::mbar_wait(&q_full[j & 1], (j >> 1) & 1, 1u << 20);
     }
   } else if (mma_warp) {
     // ---- MMA warp (one lane) ----
     if (lane == 0) {
-      auto issue_output = [&](int cj) {  // chunk cj's output product (stage cj & 1, state buffer cj % 3)
+      auto issue_output = [&](int cj) {  // chunk cj's output product (Q' stage cj & 1, state buffer cj % 3)
         const uint32_t qq = tc::smem_u32(smb + (cj & 1) * kStageBytes + kStQ);
         const uint32_t sb2 = tc::smem_u32(smb + kSmS + (cj % kSBufs) * kSmSBytes);
-        const uint32_t dO = tmem + 64 + 64 * (cj & 1);
+        const uint32_t dO = tmem + 64 + 64 * (cj % kOBufs);
 #pragma unroll
         for (int k = 0; k < 8; ++k) {  // Q' [S_hi | S_lo]; Q' atom columns are 64 rows (8 KB) apart
           const uint32_t koff = (k & 3) * 32;
           tc::mma_bf16(dO, tc::sw128_desc(qq + (k >> 2) * (kChunk * 128) + koff),
                        tc::sw128_desc(sb2 + (k >> 2) * (2 * kVs * 128) + koff), idescO, k > 0);
         }
-        tc::mma_commit(&o_bar[cj & 1]);
+        tc::mma_commit(&o_bar[cj % kOBufs]);
       };
+      float tau = tau_of(0);
+      int m_used = 0;  // M_c stages taken
       bool abort = false;
       for (int ci = 0; ci <= nch && !abort; ++ci) {
         if (ci < nch) {
-          // state operand of chunk ci written (chunk 0's by the prologue), its M_c landed
-          if (!tc::mbar_wait(&s_ready, ci & 1) || !tc::mbar_wait(&m_full[ci & 1], (ci >> 1) & 1)) {
+          const float tau_next = ci + 1 < nch ? tau_of(ci + 1) : 0.f;
+          const int b = ci % kSBufs;
+          // state operand of chunk ci written (chunk 0's by the prologue)
+          if (!tc::mbar_wait(&s_ready[b], (ci / kSBufs) & 1)) {
             abort = true;
             break;
           }
-          tc::tc_fence_after();
-          const uint32_t mh = tc::smem_u32(smb + (ci & 1) * kStageBytes + kStM), ml = mh + 128 * 128 * 2;
-          const uint32_t sb2 = tc::smem_u32(smb + kSmS + (ci % kSBufs) * kSmSBytes);
+          const bool skip = skip_chain(tau, state_max(b));
+          if (map_stored(tau)) {
+            if (!tc::mbar_wait(&m_full[m_used & 1], (m_used >> 1) & 1)) {
+              abort = true;
+              break;
+            }
+            if (!skip) {
+              tc::tc_fence_after();
+              const uint32_t mh = tc::smem_u32(smb + (m_used & 1) * kStageBytes + kStM), ml = mh + 128 * 128 * 2;
+              const uint32_t sb2 = tc::smem_u32(smb + kSmS + b * kSmSBytes);
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {  // M_hi [S_hi | S_lo]
-            const uint32_t koff = (k & 3) * 32;
-            tc::mma_bf16(dch, tc::sw128_desc(mh + (k >> 2) * (128 * 128) + koff),
-                         tc::sw128_desc(sb2 + (k >> 2) * (2 * kVs * 128) + koff), idesc2, k > 0);
-          }
+              for (int k = 0; k < 8; ++k) {  // M_hi [S_hi | S_lo]
+                const uint32_t koff = (k & 3) * 32;
+                tc::mma_bf16(dch, tc::sw128_desc(mh + (k >> 2) * (128 * 128) + koff),
+                             tc::sw128_desc(sb2 + (k >> 2) * (2 * kVs * 128) + koff), idesc2, k > 0);
+              }
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {  // + M_lo S_hi, into the S_lo half
-            const uint32_t koff = (k & 3) * 32;
-            tc::mma_bf16(dch + kVs, tc::sw128_desc(ml + (k >> 2) * (128 * 128) + koff),
-                         tc::sw128_desc(sb2 + (k >> 2) * (2 * kVs * 128) + koff), idesc1, true);
+              for (int k = 0; k < 8; ++k) {  // + M_lo S_hi, into the S_lo half
+                const uint32_t koff = (k & 3) * 32;
+                tc::mma_bf16(dch + kVs, tc::sw128_desc(ml + (k >> 2) * (128 * 128) + koff),
+                             tc::sw128_desc(sb2 + (k >> 2) * (2 * kVs * 128) + koff), idesc1, true);
+              }
+              tc::mma_commit(&ch_bar);
+              tc::mma_commit(&m_free[m_used & 1]);
+            } else {
+              mbar_arrive(&m_free[m_used & 1]);  // landed and not read
+            }
+            ++m_used;
           }
-          tc::mma_commit(&ch_bar);
-          tc::mma_commit(&m_free[ci & 1]);
+          tau = tau_next;
         }
         if (ci >= 1) {  // chunk ci - 1's output product, behind chunk ci's chain product
           if (!tc::mbar_wait(&q_full[(ci - 1) & 1], ((ci - 1) >> 1) & 1)) {
@@ -1154,6 +1228,14 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
     };
 #pragma unroll
     for (int jj = 0; jj < kColsPerThread; ++jj) S[jj] = st[(size_t)(v0 + j0 + jj) * K + c];
+    auto publish_max = [&](int buf) {  // this warp's max|S| for buffer buf's state
+      uint32_t m = 0u;
+#pragma unroll
+      for (int jj = 0; jj < kColsPerThread; ++jj) m = max(m, __float_as_uint(S[jj]) & 0x7fffffffu);
+#pragma unroll
+      for (int o = 16; o; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+      if (lane == 0) s_pmax[buf][warp] = m;
+    };
     auto write_state_operand = [&](int buf) {
       uint8_t* S2 = smb + kSmS + buf * kSmSBytes;
 #pragma unroll
@@ -1176,14 +1258,13 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
       }
     };
     const uint32_t lane_addr = (static_cast<uint32_t>(quad * 32) << 16) + j0;
-    const float scale = a.gate.scale;
     // chunk cj's output: token 16 q + l is in TMEM lane 32 q + l (l < 16)
     const int orow = quad * 16 + (lane & 15);
     auto output = [&](int cj, const float4& u0, const float4& u1) -> bool {
-      const bool ok = tc::mbar_wait(&o_bar[cj & 1], (cj >> 1) & 1);
+      const bool ok = tc::mbar_wait(&o_bar[cj % kOBufs], (cj / kOBufs) & 1);
       tc::tc_fence_after();
       float dh[kColsPerThread], dl[kColsPerThread];
-      const uint32_t dO = tmem + 64 + 64 * (cj & 1);
+      const uint32_t dO = tmem + 64 + 64 * (cj % kOBufs);
       tc::tmem_ld8(dO + lane_addr, dh);
       tc::tmem_ld8(dO + lane_addr + kVs, dl);
       const float oo[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
@@ -1199,47 +1280,63 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
       tc::tc_fence_before();
       return ok;
     };
-    (void)scale;
     float4 bc0, bc1, pu0, pu1, pp0 = make_float4(0.f, 0.f, 0.f, 0.f), pp1 = pp0;  // pp: previous chunk's P Util
     load_bc(0, bc0, bc1);
     load_pu(0, pu0, pu1);
+    float tau = tau_of(0);
+    publish_max(0);
     write_state_operand(0);
     write_intermediate(0);
     tc::fence_async_smem();
     __syncwarp();
-    if (lane == 0) mbar_arrive(&s_ready);
-    bool ok = true;
+    if (lane == 0) mbar_arrive(&s_ready[0]);
+    bool ok = tc::mbar_wait(&s_ready[0], 0);
+    float smax = state_max(0);  // max|S| of the current chunk's start state
+    int nchain = 0;             // chain products so far
     for (int ci = 0; ci < nch && ok; ++ci) {
       const bool more = ci + 1 < nch;
       float4 nb0 = bc0, nb1 = bc1, nu0 = pu0, nu1 = pu1;
-      if (more) {  // next chunk's B_c and P Util, landing while this one finishes
+      float ntau = tau;
+      if (more) {  // next chunk's B_c, P Util and threshold, landing while this one finishes
         load_bc(ci + 1, nb0, nb1);
         load_pu(ci + 1, nu0, nu1);
+        ntau = tau_of(ci + 1);
       }
-      // chain: S_{ci+1} = M_c S_ci + B_c
-      if (!tc::mbar_wait(&ch_bar, ci & 1)) ok = false;
-      tc::tc_fence_after();
-      {
+      // S_{ci+1} = M_c S_ci + B_c, or B_c where the product cannot change it
+      const float bb[8] = {bc0.x, bc0.y, bc0.z, bc0.w, bc1.x, bc1.y, bc1.z, bc1.w};
+      if (!skip_chain(tau, smax)) {
+        if (!tc::mbar_wait(&ch_bar, nchain & 1)) ok = false;
+        ++nchain;
+        tc::tc_fence_after();
         float dh[kColsPerThread], dl[kColsPerThread];
         tc::tmem_ld8(dch + lane_addr, dh);
         tc::tmem_ld8(dch + lane_addr + kVs, dl);
-        const float bb[8] = {bc0.x, bc0.y, bc0.z, bc0.w, bc1.x, bc1.y, bc1.z, bc1.w};
 #pragma unroll
         for (int jj = 0; jj < kColsPerThread; ++jj) S[jj] = dh[jj] + dl[jj] + bb[jj];
+      } else {
+#pragma unroll
+        for (int jj = 0; jj < kColsPerThread; ++jj) S[jj] = bb[jj];
       }
+      const int nb = (ci + 1) % kSBufs;
       if (more) {
         // its buffer's last readers, chunk ci - 2's products, finished before
-        // chunk ci's chain product did
-        write_state_operand((ci + 1) % kSBufs);
+        // chunk ci - 2's output product did, which this warp has waited for
+        publish_max(nb);
+        write_state_operand(nb);
         tc::fence_async_smem();
         tc::tc_fence_before();
         __syncwarp();  // the warp's operand writes (and TMEM reads) precede its arrival
-        if (lane == 0) mbar_arrive(&s_ready);  // the MMA warp may issue chunk ci + 1
+        if (lane == 0) mbar_arrive(&s_ready[nb]);  // the MMA warp may issue chunk ci + 1
         write_intermediate(ci + 1);
       }
       if (ci >= 1 && !output(ci - 1, pp0, pp1)) ok = false;  // issued behind chunk ci's chain product
+      if (more) {  // every epilogue warp's maximum of S_{ci+1}
+        if (!tc::mbar_wait(&s_ready[nb], ((ci + 1) / kSBufs) & 1)) ok = false;
+        smax = state_max(nb);
+      }
       pp0 = pu0; pp1 = pu1;
       bc0 = nb0; bc1 = nb1; pu0 = nu0; pu1 = nu1;
+      tau = ntau;
     }
     if (ok && !output(nch - 1, pp0, pp1)) ok = false;
     if (!ok) {

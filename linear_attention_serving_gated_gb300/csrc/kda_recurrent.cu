@@ -89,23 +89,6 @@ struct FoldSmem {
   float red[kTokBlock][2][4];      // per-warp sums of squares of q and k
 };
 
-// 16-byte global -> shared copy (not through registers); the issuing thread
-// waits for its own copies with cp_async_wait_all.
-__device__ __forceinline__ void cp_async16(void* dst_smem, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
-                   static_cast<uint32_t>(__cvta_generic_to_shared(dst_smem))),
-               "l"(src)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async4(void* dst_smem, const void* src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(
-                   static_cast<uint32_t>(__cvta_generic_to_shared(dst_smem))),
-               "l"(src)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
-
 // CTAs per SM the register allocation must allow: 7 (72 registers) lets the
 // 1024 CTAs of a 16-request chain verify run as one wave; tree verify would
 // spill there and gets 5.

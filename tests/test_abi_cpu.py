@@ -43,11 +43,11 @@ def test_status_strings(lib):
     assert "workspace" in kda.status_string(kda.KDA_ERR_WORKSPACE)
 
 
-REC_BYTES = 180224  # one (chunk, head) record, as include/kda.h states
+REC_BYTES = 180352  # one (chunk, head) record, as include/kda.h states
 
 
 def test_workspace_size_formula(lib):
-    """align256(4 num_seqs) + (T / 64 + num_seqs) HV 164352 bytes, as kda.h
+    """align256(4 num_seqs) + (T / 64 + num_seqs) HV 180352 bytes, as kda.h
     states; sizes past int32 tokens give SIZE_MAX so that no check passes."""
     for HV, n, T in ((16, 1, 64), (16, 1, 4096), (16, 8, 32768), (4, 3, 100), (2, 70, 0)):
         want = ((4 * n + 255) // 256) * 256 + (T // 64 + n) * HV * REC_BYTES
