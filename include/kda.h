@@ -120,8 +120,11 @@ const char *kda_status_string(kda_status s);
 
 /* Bytes of device workspace kda_prefill needs for this call shape (an upper
  * bound over every cu_seqlens with this many sequences and tokens):
- *   align256(4 * num_seqs) + (total_tokens / 64 + num_seqs) * HV * 180352.
- * total_tokens above INT32_MAX (cu_seqlens are int32) gives SIZE_MAX. */
+ *   align256(4 * num_seqs) + (total_tokens / 64 + num_seqs) * HV * 180352
+ *     + num_seqs * HV * 65536
+ * (per-sequence flags, one record per (chunk, head), one staged start state
+ * per (sequence, head)).  total_tokens above INT32_MAX (cu_seqlens are int32)
+ * gives SIZE_MAX. */
 size_t kda_prefill_workspace_size(kda_dims dims, int num_seqs, int64_t total_tokens);
 
 /*
@@ -247,7 +250,7 @@ kda_status kda_commit(kda_dims dims, const float *snapshots, int B, int T,
  * (kda_prefill_workspace_size) exceeds it return KDA_ERR_WORKSPACE and
  * launch nothing.  The rule is
  *   align256(4 * num_seqs) + (total_tokens / 64 + num_seqs) * HV * 180352
- *       <= KDA_PREFILL_STATIC_SCRATCH_BYTES,
+ *       + num_seqs * HV * 65536 <= KDA_PREFILL_STATIC_SCRATCH_BYTES,
  * so one sequence at 16 heads takes at most 2943 tokens (46 records per
  * head); the 1 x 4096 shape at 16 heads needs 65 and is refused.
  *

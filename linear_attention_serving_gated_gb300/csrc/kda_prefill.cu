@@ -120,6 +120,10 @@ struct PrefillArgs {
   // seq_nch chunks.  seg_len == 0: every chunk.
   int seg_pos0, seg_len, seq_nch;
   int64_t tx_units;  // (chunk, head) units of this transform launch
+  // Start states [num_seqs][HV][V][K] staged by the transform for a pass that
+  // runs each chain in parts (nullptr: the pass reads the pool).  A later
+  // part writes the pool's final state, so no part may read the slot itself.
+  float* init_states;
 };
 
 __device__ __forceinline__ int64_t seq_begin(const PrefillArgs& a, int n) {
@@ -167,6 +171,13 @@ __device__ __forceinline__ float dot4(float4 a, float4 b) {
 }
 
 __device__ __forceinline__ float4& f4(float* p) { return *reinterpret_cast<float4*>(p); }
+
+// Programmatic dependent launch: the chunk transform lets the state pass be
+// scheduled before it ends (its CTAs then take SMs as transform CTAs leave),
+// and the pass waits here for the transform's completion and memory before
+// it reads a record.  Without a dependent launch both are no-ops.
+__device__ __forceinline__ void grid_dependency_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // ---------------------------------------------------------------------------
 // Per-chunk transform on tcgen05 (all chunks of all sequences in parallel).
@@ -305,12 +316,15 @@ __device__ __forceinline__ int64_t unit_cid(const PrefillArgs& a, int64_t u) {
 template <bool F16>
 __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const PrefillArgs a) {
   extern __shared__ uint8_t smraw[];
-  // Unit descriptor: first token and length of the unit's chunk; n < 0 marks
-  // a unit that is skipped (no chunk, padding or rejected sequence).
+  // Unit descriptor: first token and length of the unit's chunk, and whether
+  // it is its sequence's first chunk; n < 0 marks a unit that is skipped (no
+  // chunk, padding or rejected sequence).
   struct UnitDesc {
     int64_t t0;
-    int n, len;
+    int n;
+    int16_t len, first;
   };
+  static_assert(sizeof(UnitDesc) == 16, "descriptor size");
   __shared__ uint64_t mma_bar;
   __shared__ uint32_t tmem_base;
   __shared__ UnitDesc s_desc[kDescBatch];
@@ -341,6 +355,7 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
   uint16_t* braw = reinterpret_cast<uint16_t*>(galog + 4);  // raw beta of the unit's tokens
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  grid_dependency_launch();
   if (tid == 0) {
     s_abort = 0;
     s_ok = seqlens_valid(a);
@@ -360,11 +375,11 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
     int64_t cid;
     int hh;
     const ChunkLoc l = unit_loc(a, uu, &cid, &hh);
-    if (l.n < 0) return UnitDesc{0, -1, 0};
+    if (l.n < 0) return UnitDesc{0, -1, 0, 0};
     const int slot = a.state_idx[l.n];
-    if (slot < 0 || slot >= a.pool_slots) return UnitDesc{0, -1, 0};  // padding / rejected
-    if (a.seq_flags && a.seq_flags[l.n]) return UnitDesc{0, -1, 0};    // given decay out of range
-    return UnitDesc{l.t0, l.n, l.len};
+    if (slot < 0 || slot >= a.pool_slots) return UnitDesc{0, -1, 0, 0};  // padding / rejected
+    if (a.seq_flags && a.seq_flags[l.n]) return UnitDesc{0, -1, 0, 0};    // given decay out of range
+    return UnitDesc{l.t0, l.n, (int16_t)l.len, (int16_t)(l.t0 == seq_begin(a, l.n))};
   };
   // A unit's raw q, k, v rows into Qs, Ks, Vs and its gate input rows into Gs
   // (16-byte asynchronous copies, one row piece per thread and tensor; rows
@@ -397,7 +412,7 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
       __syncthreads();  // nobody reads the previous batch any more
       if (tid < kDescBatch) {
         const int64_t uu = u + (int64_t)tid * gridDim.x;
-        s_desc[tid] = uu < a.tx_units ? describe(uu) : UnitDesc{0, -1, 0};
+        s_desc[tid] = uu < a.tx_units ? describe(uu) : UnitDesc{0, -1, 0, 0};
       }
     }
     __syncthreads();  // every thread is done with the previous unit's shared values
@@ -424,6 +439,12 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
     //    (the running sum of a warp's last token is its total).  The previous
     //    unit's output staging (L/R and A2h regions) may still be read by its
     //    bulk stores: the fold writes none of it.
+    if (a.init_states && ud.first) {  // the sequence's first chunk: stage its start state
+      const float4* src = reinterpret_cast<const float4*>(
+          a.pool + ((size_t)a.state_idx[ud.n] * a.HV + h) * kHeadDim * kHeadDim);
+      float4* dst = reinterpret_cast<float4*>(a.init_states + ((size_t)ud.n * a.HV + h) * kHeadDim * kHeadDim);
+      for (int i = tid; i < kHeadDim * kHeadDim / 4; i += kTxThreads) __stcg(dst + i, __ldcg(src + i));
+    }
     if (!rows_ready) issue_rows(ud, h);
     cp_async_wait_all();
     __syncthreads();
@@ -997,7 +1018,7 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
   __shared__ uint32_t s_pmax[kSBufs][kPassEpiThreads / 32];  // per-warp max|S| (FP32 bits) of buffer b's state
   __shared__ uint32_t tmem_base;
   __shared__ int64_t s_t0, s_t1, s_cbase;
-  __shared__ int s_state, s_abort;
+  __shared__ int s_state, s_abort, s_cs;
 
   uint8_t* smb = smraw + ((1024u - (tc::smem_u32(smraw) & 1023u)) & 1023u);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1005,20 +1026,22 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
   const int quad = warp & 3, cg = (warp >> 2) & 3;  // TMEM lane quadrant, column group
   const int row = quad * 32 + lane;                 // key channel c (chain) or output row
   const int j0 = cg * kColsPerThread;               // first of this thread's value columns
-  const int n = blockIdx.z, h = blockIdx.y, slice = blockIdx.x, v0 = slice * kVs;
+  const int n = blockIdx.z, h = blockIdx.y, slice = blockIdx.x % kSlices, v0 = slice * kVs;
+  const int part = blockIdx.x / kSlices, parts = gridDim.x / kSlices;  // share of the chain
   const int HV = a.HV, K = kHeadDim, V = kHeadDim;
+  const bool reporter = slice == 0 && part == 0;
 
   if (tid == 0) {
     s_state = 0;
     s_abort = 0;
     if (!seqlens_valid(a)) {
       s_state = 2;
-      if (slice == 0 && h == 0 && n == 0) set_error(a.err_flag, KDA_DEVERR_SEQLENS);
+      if (reporter && h == 0 && n == 0) set_error(a.err_flag, KDA_DEVERR_SEQLENS);
     } else {
       const int slot = a.state_idx[n];
       if (slot < -1 || slot >= a.pool_slots) {
         s_state = 2;
-        if (slice == 0 && h == 0) set_error(a.err_flag, KDA_DEVERR_SLOT);
+        if (reporter && h == 0) set_error(a.err_flag, KDA_DEVERR_SLOT);
       } else if (slot == -1) {
         s_state = 1;
       } else if (a.seq_flags && a.seq_flags[n]) {
@@ -1048,18 +1071,20 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
   const int nch_seq = (int)((t1 - t0 + kChunk - 1) / kChunk);
   const int p0 = a.seg_len > 0 ? (a.seg_pos0 < nch_seq ? a.seg_pos0 : nch_seq) : 0;
   const int p1 = a.seg_len > 0 ? (p0 + a.seg_len < nch_seq ? p0 + a.seg_len : nch_seq) : nch_seq;
+  const int nch = p1 > p0 ? p1 - p0 : 0;  // chunks of this launch; chunk i of them is position p0 + i
+  // this CTA's share of them: its outputs and chunk-start states, and the
+  // final state for the last part
+  const int own0 = (int)((int64_t)part * nch / parts), own1 = (int)((int64_t)(part + 1) * nch / parts);
   if (s_state == 1) {  // padding sequence: zero outputs
-    const int64_t ta = t0 + (int64_t)p0 * kChunk;
-    const int64_t tb = t0 + (int64_t)p1 * kChunk < t1 ? t0 + (int64_t)p1 * kChunk : t1;
+    const int64_t ta = t0 + (int64_t)(p0 + own0) * kChunk;
+    const int64_t tb = t0 + (int64_t)(p0 + own1) * kChunk < t1 ? t0 + (int64_t)(p0 + own1) * kChunk : t1;
     for (int64_t idx = tid; idx < (tb - ta) * kVs; idx += kPassThreads)
       a.o[((ta + idx / kVs) * HV + h) * V + v0 + idx % kVs] = 0;
     return;
   }
-  if (p0 >= p1) return;  // no chunk of this sequence in this segment
-  const int nch = p1 - p0;  // chunks handled here; chunk i of them is position p0 + i
+  if (own0 >= own1) return;  // no chunk of this sequence in this segment, or none in this part
   const int slot = a.state_idx[n];
   float* st = a.pool + ((size_t)slot * HV + h) * V * K;
-  const uint8_t* ws_head = a.ws + ((size_t)(s_cbase + p0) * HV + h) * kRecBytes;
   const size_t rec_stride = (size_t)HV * kRecBytes;
   const int c = row;
   float S[kColsPerThread];  // epilogue threads: S[c][v0 + j0 .. + 8)
@@ -1068,6 +1093,30 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
+  // Everything below reads the chunk transform's records: with a dependent
+  // launch, this is where the transform's completion is awaited.
+  grid_dependency_wait();
+  // Part k > 0 starts at the latest chunk j + 1 <= own0 (j >= own0 - 32)
+  // whose predecessor j has an all-zero map, so that S_{j+1} = B_j bit for bit,
+  // else at the launch's first chunk; it runs the chunks before own0 again
+  // without writing their outputs.  Part 0 starts at own0 = 0.
+  if (warp == 0) {
+    int cs = 0;
+    if (own0 > 0) {
+      const int j = own0 - 1 - lane;
+      const bool zero =
+          j >= 0 && __float_as_uint(__ldcg(reinterpret_cast<const float*>(
+                        a.ws + ((size_t)(s_cbase + p0 + j) * HV + h) * kRecBytes + kRecMeta) + slice)) == 0x7f800000u;
+      const uint32_t m = __ballot_sync(0xffffffffu, zero);
+      cs = m ? own0 - (__ffs(m) - 1) : 0;
+    }
+    if (lane == 0) s_cs = cs;
+  }
+  __syncthreads();
+  const int cs = s_cs;
+  const int nrun = own1 - cs;   // chunks run here, from position p0 + cs
+  const int emit0 = own0 - cs;  // the first of them whose outputs are written
+  const uint8_t* ws_head = a.ws + ((size_t)(s_cbase + p0 + cs) * HV + h) * kRecBytes;
   const uint32_t tmem = tmem_base;
   const uint32_t dch = tmem;
   constexpr uint32_t idesc2 = tc::idesc_bf16_f32(128, 2 * kVs);
@@ -1100,12 +1149,12 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
         tc::bulk_prefetch_l2(rec + kRecB + slice * (kVs * kHeadDim * 4), kVs * kHeadDim * 4);
         tc::bulk_prefetch_l2(rec + kRecOi + slice * (kVs * kChunk * 4), kVs * kChunk * 4);
       };
-      auto tau_ahead = [&](int cj) { return cj < nch ? tau_of(cj) : 0.f; };
+      auto tau_ahead = [&](int cj) { return cj < nrun ? tau_of(cj) : 0.f; };
       float ta0 = tau_ahead(0), ta1 = tau_ahead(1), ta2 = tau_ahead(2), ta3 = tau_ahead(3);  // chunks cj .. cj + 3
-      for (int cj = 1; cj < kPassL2Ahead && cj < nch; ++cj) prefetch_record(cj, map_stored(cj == 1 ? ta1 : ta2));
+      for (int cj = 1; cj < kPassL2Ahead && cj < nrun; ++cj) prefetch_record(cj, map_stored(cj == 1 ? ta1 : ta2));
       int m_issued = 0, q_issued = 0;  // M_c and Q' copies issued
       bool abort = false;
-      for (int cj = 0; cj < nch && !abort; ++cj) {
+      for (int cj = 0; cj < nrun && !abort; ++cj) {
         if (map_stored(ta0)) {  // the M_c stage m_issued & 1 last held copy m_issued - 2
           if (m_issued >= 2 && !tc::mbar_wait(&m_free[m_issued & 1], ((m_issued - 2) >> 1) & 1)) {
             abort = true;
@@ -1123,7 +1172,7 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
         tc::fence_async_smem();
         issue_copy(smb + (cj & 1) * kStageBytes + kStQ, rec_of(cj) + kRecQ, kStQBytes, &q_full[cj & 1]);
         ++q_issued;
-        if (cj + kPassL2Ahead < nch) prefetch_record(cj + kPassL2Ahead, map_stored(ta3));
+        if (cj + kPassL2Ahead < nrun) prefetch_record(cj + kPassL2Ahead, map_stored(ta3));
         ta0 = ta1;
         ta1 = ta2;
         ta2 = ta3;
@@ -1158,9 +1207,9 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
       float tau = tau_of(0);
       int m_used = 0;  // M_c stages taken
       bool abort = false;
-      for (int ci = 0; ci <= nch && !abort; ++ci) {
-        if (ci < nch) {
-          const float tau_next = ci + 1 < nch ? tau_of(ci + 1) : 0.f;
+      for (int ci = 0; ci <= nrun && !abort; ++ci) {
+        if (ci < nrun) {
+          const float tau_next = ci + 1 < nrun ? tau_of(ci + 1) : 0.f;
           const int b = ci % kSBufs;
           // state operand of chunk ci written (chunk 0's by the prologue)
           if (!tc::mbar_wait(&s_ready[b], (ci / kSBufs) & 1)) {
@@ -1215,7 +1264,7 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
   } else {
     // ---- epilogue warps ----
     auto load_bc = [&](int ci, float4& b0, float4& b1) {  // B_c rows c, [slice][quad][128][4]
-      const float4* src = reinterpret_cast<const float4*>(ws_head + (size_t)ci * rec_stride + kRecB) +
+      const float4* src = reinterpret_cast<const float4*>(ws_head + (int64_t)ci * (int64_t)rec_stride + kRecB) +
                           (slice * (kVs / 4) + j0 / 4) * kHeadDim + row;
       b0 = __ldcg(src);
       b1 = __ldcg(src + kHeadDim);
@@ -1226,8 +1275,16 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
       u0 = __ldcg(src);
       u1 = __ldcg(src + kChunk);
     };
+    if (cs == 0) {  // the launch's start state (staged by the transform when run in parts)
+      const float* s0 = a.init_states ? a.init_states + ((size_t)n * HV + h) * V * K : st;
 #pragma unroll
-    for (int jj = 0; jj < kColsPerThread; ++jj) S[jj] = st[(size_t)(v0 + j0 + jj) * K + c];
+      for (int jj = 0; jj < kColsPerThread; ++jj) S[jj] = s0[(size_t)(v0 + j0 + jj) * K + c];
+    } else {  // S_cs = B_{cs-1}: its map is all zero
+      float4 b0, b1;
+      load_bc(-1, b0, b1);
+      S[0] = b0.x; S[1] = b0.y; S[2] = b0.z; S[3] = b0.w;
+      S[4] = b1.x; S[5] = b1.y; S[6] = b1.z; S[7] = b1.w;
+    }
     auto publish_max = [&](int buf) {  // this warp's max|S| for buffer buf's state
       uint32_t m = 0u;
 #pragma unroll
@@ -1247,8 +1304,8 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
       }
     };
     auto write_intermediate = [&](int ci) {  // S is the start state of chunk ci
-      if (!a.intermediate) return;
-      const int64_t cid = s_cbase + p0 + ci;
+      if (!a.intermediate || ci < emit0) return;
+      const int64_t cid = s_cbase + p0 + cs + ci;
       if (cid < a.inter_chunks) {
         float* dst = a.intermediate + ((size_t)cid * HV + h) * V * K;
 #pragma unroll
@@ -1271,9 +1328,9 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
       float x[8];
 #pragma unroll
       for (int jj = 0; jj < kColsPerThread; ++jj) x[jj] = a.gate.scale * (dh[jj] + dl[jj] + oo[jj]);
-      const int64_t tcj = t0 + (int64_t)(p0 + cj) * kChunk;
+      const int64_t tcj = t0 + (int64_t)(p0 + cs + cj) * kChunk;
       const int len = (int)(t1 - tcj < kChunk ? t1 - tcj : kChunk);
-      if (lane < 16 && orow < len)
+      if (lane < 16 && orow < len && cj >= emit0)
         *reinterpret_cast<uint4*>(a.o + ((tcj + orow) * HV + h) * V + v0 + j0) =
             make_uint4(pack_out16x2<F16>(x[0], x[1]), pack_out16x2<F16>(x[2], x[3]),
                        pack_out16x2<F16>(x[4], x[5]), pack_out16x2<F16>(x[6], x[7]));
@@ -1293,8 +1350,8 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
     bool ok = tc::mbar_wait(&s_ready[0], 0);
     float smax = state_max(0);  // max|S| of the current chunk's start state
     int nchain = 0;             // chain products so far
-    for (int ci = 0; ci < nch && ok; ++ci) {
-      const bool more = ci + 1 < nch;
+    for (int ci = 0; ci < nrun && ok; ++ci) {
+      const bool more = ci + 1 < nrun;
       float4 nb0 = bc0, nb1 = bc1, nu0 = pu0, nu1 = pu1;
       float ntau = tau;
       if (more) {  // next chunk's B_c, P Util and threshold, landing while this one finishes
@@ -1338,14 +1395,14 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
       bc0 = nb0; bc1 = nb1; pu0 = nu0; pu1 = nu1;
       tau = ntau;
     }
-    if (ok && !output(nch - 1, pp0, pp1)) ok = false;
+    if (ok && !output(nrun - 1, pp0, pp1)) ok = false;
     if (!ok) {
       s_abort = 1;
       set_error(a.err_flag, KDA_DEVERR_TIMEOUT);
     }
   }
   __syncthreads();
-  if (!s_abort && !mma_warp && !copy_warp) {
+  if (!s_abort && !mma_warp && !copy_warp && part == parts - 1) {
 #pragma unroll
     for (int jj = 0; jj < kColsPerThread; ++jj) st[(size_t)(v0 + j0 + jj) * K + c] = S[jj];
   }
@@ -1399,8 +1456,10 @@ int64_t max_chunks(int num_seqs, int64_t total_tokens) {
 }
 
 // Workspace: the per-sequence flags of the given-decay check, then the
-// (chunk, head) records, 256-byte aligned.
+// (chunk, head) records, 256-byte aligned, then one start state per
+// (sequence, head).
 size_t flags_bytes(int num_seqs) { return ((size_t)num_seqs * 4 + 255) & ~(size_t)255; }
+constexpr size_t kStateBytes = (size_t)kHeadDim * kHeadDim * 4;
 
 constexpr int kMaxDevices = 64;
 bool g_attributes_set[kMaxDevices] = {};
@@ -1495,7 +1554,8 @@ extern "C" size_t kda_prefill_workspace_size(kda_dims dims, int num_seqs, int64_
   // cu_seqlens are int32: larger calls are refused, and SIZE_MAX makes every
   // capacity check fail instead of wrapping
   if (total_tokens > INT32_MAX || dims.HV > (1 << 16)) return SIZE_MAX;
-  return flags_bytes(num_seqs) + (size_t)max_chunks(num_seqs, total_tokens) * dims.HV * kRecBytes;
+  return flags_bytes(num_seqs) + (size_t)max_chunks(num_seqs, total_tokens) * dims.HV * kRecBytes +
+         (size_t)num_seqs * dims.HV * kStateBytes;
 }
 
 extern "C" kda_status kda_prefill(kda_dims dims, kda_gate gate, const kda_bf16* q,
@@ -1554,6 +1614,7 @@ extern "C" kda_status kda_prefill(kda_dims dims, kda_gate gate, const kda_bf16* 
   if ((s = ensure_kernel_attributes(&dev)) != KDA_OK) return s;
   const int64_t chunks = max_chunks(num_seqs, total_tokens);
   const dim3 pass_grid(kSlices, dims.HV, num_seqs);
+  uint8_t* const ws_states = args.ws + (size_t)chunks * dims.HV * kRecBytes;
   // the kernels for this call's 16-bit element type
   void (*const transform_kernel)(PrefillArgs) =
       dims.dtype == KDA_DTYPE_F16 ? chunk_transform_tc_kernel<true> : chunk_transform_tc_kernel<false>;
@@ -1579,14 +1640,35 @@ extern "C" kda_status kda_prefill(kda_dims dims, kda_gate gate, const kda_bf16* 
     args.seq_flags = flags;
   }
   if (nseg <= 1) {
+    // Each (sequence, head, slice) chain in two parts where the grid still
+    // fits the SMs: the second part restarts behind an all-zero map (see the
+    // pass), which halves the chain wherever the decay is strong.  The start
+    // states are then staged by the transform.
+    const int parts = total_tokens > 0 && 2 * (int64_t)kSlices * dims.HV * num_seqs <= g_num_sms[dev] ? 2 : 1;
+    if (parts > 1) args.init_states = reinterpret_cast<float*>(ws_states);
     if (chunks > 0) {
       args.tx_units = chunks * dims.HV;
       transform_kernel<<<transform_grid(args.tx_units, dev), kTxThreads, kTransformTcSmem, st>>>(args);
       if ((s = launch_status()) != KDA_OK) return s;
     }
-    record_stage(1, st);
-    pass_kernel<<<pass_grid, kPassThreads, kPassSmem, st>>>(args);
-    s = launch_status();
+    const dim3 grid(kSlices * parts, dims.HV, num_seqs);
+    if (g_stage_events[1]) {  // a stage event between the kernels: an ordinary launch
+      record_stage(1, st);
+      pass_kernel<<<grid, kPassThreads, kPassSmem, st>>>(args);
+      s = launch_status();
+    } else {  // dependent launch: the pass's CTAs start as the transform's leave
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[0].val.programmaticStreamSerializationAllowed = 1;
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = grid;
+      cfg.blockDim = dim3(kPassThreads);
+      cfg.dynamicSmemBytes = kPassSmem;
+      cfg.stream = st;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      s = cudaLaunchKernelEx(&cfg, pass_kernel, args) == cudaSuccess ? launch_status() : KDA_ERR_CUDA;
+    }
   } else {
     PassStream* ps = nullptr;
     if ((s = pass_stream(dev, &ps)) != KDA_OK) return s;
