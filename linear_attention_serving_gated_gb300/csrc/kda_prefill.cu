@@ -85,7 +85,7 @@ constexpr uint32_t kRecML = kRecM + 128 * 128 * 2;             // M_c lo
 constexpr uint32_t kRecQ = kRecML + 128 * 128 * 2;             // Q' (BF16), 64 x 128
 constexpr uint32_t kRecB = kRecQ + 64 * 128 * 2;               // B_c, FP32 [slice][quad][128][4]
 constexpr uint32_t kRecOi = kRecB + kHeadDim * kHeadDim * 4;   // P Util, FP32 [slice][quad][64][4]
-constexpr uint32_t kRecMeta = kRecOi + kChunk * kHeadDim * 4;   // skip thresholds, FP32 [slice]
+constexpr uint32_t kRecMeta = kRecOi + kChunk * kHeadDim * 4;   // FP32 [slice] {tau, ||B_c||}
 constexpr uint32_t kRecBytes = kRecMeta + 128;
 // Skipping a chain product.  With r = 128 max|M_c| >= every row sum of |M_c|,
 // each element of the chain product M_c S is at most about r max|S| in
@@ -96,7 +96,13 @@ constexpr uint32_t kRecBytes = kRecMeta + 128;
 // keeps tau = 2^-27 min|B_c| / r per value slice (a factor 4 of margin); the
 // pass skips the product iff max|S| <= tau, the max taken over the slice's
 // start state.  tau = +inf marks an all-zero M_c, which is not stored.
+// Next to tau the record keeps ||B_c||_F of the slice, rounded up by 2^-10:
+// with L2-normalised keys, beta <= 1 and g <= 0 every token's factor
+// (I - beta k k^T) Diag(e^g) has norm <= 1, so M_c has too, and
+// ||S_{c+1}|| <= ||S_c|| + ||B_c|| bounds every element of a later state
+// before it is computed (see the pass).
 constexpr float kSkipMargin = 7.450580596923828125e-09f;  // 2^-27
+constexpr float kNormRoundUp = 1.0009765625f;              // 1 + 2^-10
 
 struct PrefillArgs {
   GateArgs gate;
@@ -330,6 +336,7 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
   __shared__ UnitDesc s_desc[kDescBatch];
   __shared__ int s_abort, s_ok;
   __shared__ uint32_t s_mmax, s_bmin[kSlices];  // max|M_c|, min|B_c| per slice (FP32 bits, >= 0)
+  __shared__ float s_bsq[kSlices];                // sum of B_c^2 per slice
 
   uint8_t* sb = smraw + ((1024u - (tc::smem_u32(smraw) & 1023u)) & 1023u);
   uint8_t* Lt = sb + kTxL;  // M1 left operand, TF32 128 x 128
@@ -418,7 +425,10 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
     __syncthreads();  // every thread is done with the previous unit's shared values
     if (tid == 0) {  // read by 9c, after several barriers
       s_mmax = 0u;
-      for (int sl = 0; sl < kSlices; ++sl) s_bmin[sl] = 0x7f800000u;  // +inf
+      for (int sl = 0; sl < kSlices; ++sl) {
+        s_bmin[sl] = 0x7f800000u;  // +inf
+        s_bsq[sl] = 0.f;
+      }
     }
     const UnitDesc ud = s_desc[bi];
     if (ud.n < 0) {
@@ -916,7 +926,14 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
         for (int e = 0; e < 32; ++e) mn = min(mn, __float_as_uint(d[e]) & 0x7fffffffu);
 #pragma unroll
         for (int m = 16; m; m >>= 1) mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, m));
-        if (lane == 0) atomicMin(&s_bmin[cg - 4], mn);
+        float sq = 0.f;
+#pragma unroll
+        for (int e = 0; e < 32; ++e) sq += d[e] * d[e];
+        sq = warp_sum(sq);
+        if (lane == 0) {
+          atomicMin(&s_bmin[cg - 4], mn);
+          atomicAdd(&s_bsq[cg - 4], sq);
+        }
       }
     }
     if (s_abort && tid == 0) set_error(a.err_flag, KDA_DEVERR_TIMEOUT);
@@ -929,10 +946,12 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
       float* meta = reinterpret_cast<float*>(rec + kRecMeta);
       // an infinite or NaN bound never skips; a finite one stays below +inf,
       // which marks the all-zero map alone
-      for (int sl = 0; sl < kSlices; ++sl)
-        meta[sl] = s_mmax == 0u ? __int_as_float(0x7f800000)
-                 : r < __int_as_float(0x7f800000) ? fminf(kSkipMargin * __uint_as_float(s_bmin[sl]) / r, 3.402823466e38f)
-                                                  : -1.f;
+      for (int sl = 0; sl < kSlices; ++sl) {
+        meta[2 * sl] = s_mmax == 0u ? __int_as_float(0x7f800000)
+                     : r < __int_as_float(0x7f800000) ? fminf(kSkipMargin * __uint_as_float(s_bmin[sl]) / r, 3.402823466e38f)
+                                                      : -1.f;
+        meta[2 * sl + 1] = sqrtf(s_bsq[sl]) * kNormRoundUp;
+      }
       if (s_mmax != 0u) {  // an all-zero M_c is never read
         static_assert(kRecML == kRecM + 128 * 128 * 2, "M_c hi and lo are contiguous");
         tc::bulk_s2g(rec + kRecM, sb + kTxMs, 2 * 128 * 128 * 2);
@@ -1019,6 +1038,7 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
   __shared__ uint32_t tmem_base;
   __shared__ int64_t s_t0, s_t1, s_cbase;
   __shared__ int s_state, s_abort, s_cs;
+  __shared__ float s_bnd0, s_pn[kPassEpiThreads / 32];  // run start bound; per-warp sums
 
   uint8_t* smb = smraw + ((1024u - (tc::smem_u32(smraw) & 1023u)) & 1023u);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1096,21 +1116,61 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
   // Everything below reads the chunk transform's records: with a dependent
   // launch, this is where the transform's completion is awaited.
   grid_dependency_wait();
-  // Part k > 0 starts at the latest chunk j + 1 <= own0 (j >= own0 - 32)
-  // whose predecessor j has an all-zero map, so that S_{j+1} = B_j bit for bit,
-  // else at the launch's first chunk; it runs the chunks before own0 again
-  // without writing their outputs.  Part 0 starts at own0 = 0.
-  if (warp == 0) {
-    int cs = 0;
-    if (own0 > 0) {
-      const int j = own0 - 1 - lane;
-      const bool zero =
-          j >= 0 && __float_as_uint(__ldcg(reinterpret_cast<const float*>(
-                        a.ws + ((size_t)(s_cbase + p0 + j) * HV + h) * kRecBytes + kRecMeta) + slice)) == 0x7f800000u;
-      const uint32_t m = __ballot_sync(0xffffffffu, zero);
-      cs = m ? own0 - (__ffs(m) - 1) : 0;
+  // A bound on the slice's states before they are computed: with
+  // L2-normalised keys, beta = sigmoid(raw) < 1 and g <= 0, every map has norm
+  // <= 1, so ||S_{c+1}|| <= ||S_c|| + ||B_c|| (the records keep ||B_c||).
+  const bool bounded = a.gate.use_qk_l2norm && a.gate.beta_is_raw && (!a.gate.A_log || a.gate.lower_bound <= 0.f);
+  const float* s_start = a.init_states ? a.init_states + ((size_t)n * HV + h) * V * K : st;  // the launch's
+  auto meta_of = [&](int j) -> float2 {  // {tau, ||B_c||} of chunk j of this launch, this slice
+    return __ldcg(reinterpret_cast<const float2*>(a.ws + ((size_t)(s_cbase + p0 + j) * HV + h) * kRecBytes +
+                                                  kRecMeta) + slice);
+  };
+  if (bounded && warp < kPassEpiThreads / 32) {  // ||S_start[:, slice]||^2 by warp
+    float sq = 0.f;
+#pragma unroll
+    for (int jj = 0; jj < kColsPerThread; ++jj) {
+      const float x = s_start[(size_t)(v0 + j0 + jj) * K + row];
+      sq += x * x;
     }
-    if (lane == 0) s_cs = cs;
+    sq = warp_sum(sq);
+    if (lane == 0) s_pn[warp] = sq;
+  }
+  __syncthreads();
+  // Part k > 0 starts at the latest chunk j + 1 <= own0 (j >= own0 - 32)
+  // whose chain product is left out whatever S_j is -- an all-zero map, or
+  // tau_j at least twice the bound on S_j -- so that S_{j+1} = B_j bit for
+  // bit; else at the launch's first chunk.  It runs the chunks before own0
+  // again without writing their outputs.  Part 0 starts at own0 = 0.
+  if (warp == 0) {
+    float s0n = 0.f;
+    if (bounded) {
+      float t = 0.f;
+      for (int w = 0; w < kPassEpiThreads / 32; ++w) t += s_pn[w];
+      s0n = sqrtf(t) * kNormRoundUp;
+    }
+    int cs = 0;
+    float bnd0 = s0n;  // bound on the run's start state
+    if (own0 > 0) {
+      float pre = 0.f;  // sum of ||B_c|| over c < own0: with s0n, a bound on every S_j, j <= own0
+      if (bounded) {
+        for (int j = lane; j < own0; j += 32) pre += meta_of(j).y;
+        pre = warp_sum(pre);
+      }
+      const float bnd = (s0n + pre) * kNormRoundUp;
+      const int j = own0 - 1 - lane;
+      const float2 mj = j >= 0 ? meta_of(j) : make_float2(0.f, 0.f);
+      const bool cut = j >= 0 && (__float_as_uint(mj.x) == 0x7f800000u || (bounded && 2.f * bnd <= mj.x));
+      const uint32_t m = __ballot_sync(0xffffffffu, cut);
+      if (m) {
+        const int l = __ffs(m) - 1;
+        cs = own0 - l;
+        bnd0 = __shfl_sync(0xffffffffu, mj.y, l);  // S_cs = B_{cs-1}
+      }
+    }
+    if (lane == 0) {
+      s_cs = cs;
+      s_bnd0 = bnd0;
+    }
   }
   __syncthreads();
   const int cs = s_cs;
@@ -1123,20 +1183,28 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
   constexpr uint32_t idesc1 = tc::idesc_bf16_f32(128, kVs);
   constexpr uint32_t idescO = tc::idesc_bf16_f32(kChunk, 2 * kVs);
 
-  // Chunk ci's skip threshold for this slice (+inf: M_c is all zero and not
-  // stored), and the decision every role takes the same way from it and from
-  // the per-warp maxima of the chunk's start state.
-  auto tau_of = [&](int ci) -> float {
-    return __ldcg(reinterpret_cast<const float*>(ws_head + (size_t)ci * rec_stride + kRecMeta) + slice);
+  // Chunk ci's {tau, ||B_c||} for this slice (tau = +inf: M_c is all zero and
+  // not stored), and the decisions every role takes the same way from them,
+  // from the running bound on the chunk's start state (s_bnd0 plus the
+  // ||B_c|| of the chunks before, added in order) and from the per-warp
+  // maxima of that state.
+  auto meta_at = [&](int ci) -> float2 {
+    return __ldcg(reinterpret_cast<const float2*>(ws_head + (size_t)ci * rec_stride + kRecMeta) + slice);
   };
   auto map_stored = [](float tau) { return __float_as_uint(tau) != 0x7f800000u; };
+  // left out whatever the state: the bound (doubled) is within tau
+  auto certain_skip = [&](float tau, float bnd) { return bounded && 2.f * bnd <= tau; };
+  // the M_c stage is copied and taken only for a product that may run
+  auto m_needed = [&](float2 m, float bnd) { return map_stored(m.x) && !certain_skip(m.x, bnd); };
   auto state_max = [&](int b) -> float {  // max|S| of the state in buffer b (NaN is largest)
     uint32_t m = 0u;
 #pragma unroll
     for (int w = 0; w < kPassEpiThreads / 32; ++w) m = max(m, s_pmax[b][w]);
     return __uint_as_float(m);
   };
-  auto skip_chain = [&](float tau, float smax) { return !map_stored(tau) || smax <= tau; };
+  auto skip_chain = [&](float2 m, float bnd, float smax) {
+    return !map_stored(m.x) || certain_skip(m.x, bnd) || smax <= m.x;
+  };
 
   if (copy_warp) {
     // ---- copy warp (one lane) ----
@@ -1149,13 +1217,16 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
         tc::bulk_prefetch_l2(rec + kRecB + slice * (kVs * kHeadDim * 4), kVs * kHeadDim * 4);
         tc::bulk_prefetch_l2(rec + kRecOi + slice * (kVs * kChunk * 4), kVs * kChunk * 4);
       };
-      auto tau_ahead = [&](int cj) { return cj < nrun ? tau_of(cj) : 0.f; };
-      float ta0 = tau_ahead(0), ta1 = tau_ahead(1), ta2 = tau_ahead(2), ta3 = tau_ahead(3);  // chunks cj .. cj + 3
-      for (int cj = 1; cj < kPassL2Ahead && cj < nrun; ++cj) prefetch_record(cj, map_stored(cj == 1 ? ta1 : ta2));
+      auto meta_ahead = [&](int cj) { return cj < nrun ? meta_at(cj) : make_float2(0.f, 0.f); };
+      // chunks cj .. cj + 3, and the bound on chunk cj's start state
+      float2 ta0 = meta_ahead(0), ta1 = meta_ahead(1), ta2 = meta_ahead(2), ta3 = meta_ahead(3);
+      float bnd = s_bnd0;
+      for (int cj = 1; cj < kPassL2Ahead && cj < nrun; ++cj)
+        prefetch_record(cj, cj == 1 ? m_needed(ta1, bnd + ta0.y) : m_needed(ta2, (bnd + ta0.y) + ta1.y));
       int m_issued = 0, q_issued = 0;  // M_c and Q' copies issued
       bool abort = false;
       for (int cj = 0; cj < nrun && !abort; ++cj) {
-        if (map_stored(ta0)) {  // the M_c stage m_issued & 1 last held copy m_issued - 2
+        if (m_needed(ta0, bnd)) {  // the M_c stage m_issued & 1 last held copy m_issued - 2
           if (m_issued >= 2 && !tc::mbar_wait(&m_free[m_issued & 1], ((m_issued - 2) >> 1) & 1)) {
             abort = true;
             break;
@@ -1172,11 +1243,13 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
         tc::fence_async_smem();
         issue_copy(smb + (cj & 1) * kStageBytes + kStQ, rec_of(cj) + kRecQ, kStQBytes, &q_full[cj & 1]);
         ++q_issued;
-        if (cj + kPassL2Ahead < nrun) prefetch_record(cj + kPassL2Ahead, map_stored(ta3));
+        if (cj + kPassL2Ahead < nrun)
+          prefetch_record(cj + kPassL2Ahead, m_needed(ta3, ((bnd + ta0.y) + ta1.y) + ta2.y));
+        bnd = bnd + ta0.y;
         ta0 = ta1;
         ta1 = ta2;
         ta2 = ta3;
-        ta3 = tau_ahead(cj + 4);
+        ta3 = meta_ahead(cj + 4);
       }
       if (abort) {
         s_abort = 1;
@@ -1204,20 +1277,21 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
         }
         tc::mma_commit(&o_bar[cj % kOBufs]);
       };
-      float tau = tau_of(0);
-      int m_used = 0;  // M_c stages taken
+      float2 meta = meta_at(0);
+      float bnd = s_bnd0;  // bound on chunk ci's start state
+      int m_used = 0;      // M_c stages taken
       bool abort = false;
       for (int ci = 0; ci <= nrun && !abort; ++ci) {
         if (ci < nrun) {
-          const float tau_next = ci + 1 < nrun ? tau_of(ci + 1) : 0.f;
+          const float2 meta_next = ci + 1 < nrun ? meta_at(ci + 1) : make_float2(0.f, 0.f);
           const int b = ci % kSBufs;
           // state operand of chunk ci written (chunk 0's by the prologue)
           if (!tc::mbar_wait(&s_ready[b], (ci / kSBufs) & 1)) {
             abort = true;
             break;
           }
-          const bool skip = skip_chain(tau, state_max(b));
-          if (map_stored(tau)) {
+          const bool skip = skip_chain(meta, bnd, state_max(b));
+          if (m_needed(meta, bnd)) {
             if (!tc::mbar_wait(&m_full[m_used & 1], (m_used >> 1) & 1)) {
               abort = true;
               break;
@@ -1245,7 +1319,8 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
             }
             ++m_used;
           }
-          tau = tau_next;
+          bnd = bnd + meta.y;
+          meta = meta_next;
         }
         if (ci >= 1) {  // chunk ci - 1's output product, behind chunk ci's chain product
           if (!tc::mbar_wait(&q_full[(ci - 1) & 1], ((ci - 1) >> 1) & 1)) {
@@ -1340,7 +1415,8 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
     float4 bc0, bc1, pu0, pu1, pp0 = make_float4(0.f, 0.f, 0.f, 0.f), pp1 = pp0;  // pp: previous chunk's P Util
     load_bc(0, bc0, bc1);
     load_pu(0, pu0, pu1);
-    float tau = tau_of(0);
+    float2 meta = meta_at(0);
+    float bnd = s_bnd0;  // bound on the current chunk's start state
     publish_max(0);
     write_state_operand(0);
     write_intermediate(0);
@@ -1353,15 +1429,15 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
     for (int ci = 0; ci < nrun && ok; ++ci) {
       const bool more = ci + 1 < nrun;
       float4 nb0 = bc0, nb1 = bc1, nu0 = pu0, nu1 = pu1;
-      float ntau = tau;
+      float2 nmeta = meta;
       if (more) {  // next chunk's B_c, P Util and threshold, landing while this one finishes
         load_bc(ci + 1, nb0, nb1);
         load_pu(ci + 1, nu0, nu1);
-        ntau = tau_of(ci + 1);
+        nmeta = meta_at(ci + 1);
       }
       // S_{ci+1} = M_c S_ci + B_c, or B_c where the product cannot change it
       const float bb[8] = {bc0.x, bc0.y, bc0.z, bc0.w, bc1.x, bc1.y, bc1.z, bc1.w};
-      if (!skip_chain(tau, smax)) {
+      if (!skip_chain(meta, bnd, smax)) {
         if (!tc::mbar_wait(&ch_bar, nchain & 1)) ok = false;
         ++nchain;
         tc::tc_fence_after();
@@ -1393,7 +1469,8 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
       }
       pp0 = pu0; pp1 = pu1;
       bc0 = nb0; bc1 = nb1; pu0 = nu0; pu1 = nu1;
-      tau = ntau;
+      bnd = bnd + meta.y;
+      meta = nmeta;
     }
     if (ok && !output(nrun - 1, pp0, pp1)) ok = false;
     if (!ok) {
