@@ -303,16 +303,18 @@ def run_ours(args, rank, world, local_rank):
         flush.view(torch.int64).sum()
 
     phases = ["prefill", "decode", "verify_chain", "verify_tree", "commit", "verify_replay", "commit_replay",
-              "prefill_states"] + ([] if args.no_long else ["prefill_long", "prefill_long_calls"])
-    # The prefill's state pass of segment s overlaps the transform of segment
-    # s+1, so its stage events give the span of the transform launches (ev0 ->
-    # ev1, earlier segments' passes running alongside) and the exposed tail of
-    # the last pass segment (ev1 -> ev2).
-    kernels = ["prefill_transform", "prefill_pass_tail", "decode", "verify_chain", "verify_tree", "commit",
+              "prefill_states", "prefill_split"] + ([] if args.no_long else ["prefill_long", "prefill_long_calls"])
+    # The prefill's state pass is a dependent launch of its chunk transform
+    # (its CTAs start as the transform's leave), which an event between the
+    # two kernels would turn into an ordinary launch.  So the headline prefill
+    # phase has events around the call only, and "prefill_split" repeats the
+    # same call with a third event between the kernels: the transform's span
+    # (ev0 -> ev1) and the pass's (ev1 -> ev2).
+    kernels = ["prefill_transform", "prefill_pass", "decode", "verify_chain", "verify_tree", "commit",
                "verify_replay", "commit_replay"]
 
     def run_call(name, x):
-        if name == "prefill":
+        if name in ("prefill", "prefill_split"):
             kda.kda_prefill(D, gate, P["q"], P["k"], P["v"], P["g"], P["beta"], p_pool, p_idx, p_cu, 1,
                             p_o, workspace=ws)
         elif name == "decode":
@@ -350,13 +352,13 @@ def run_ours(args, rank, world, local_rank):
 
     def run_phase(name, ev=None):
         """One phase; with events, ev[0] is recorded right before the first
-        kernel and ev[2] right after the last (ev[1] between the two prefill
-        kernels), as graph nodes when captured."""
+        kernel and ev[2] right after the last (in "prefill_split" ev[1]
+        between the two prefill kernels), as graph nodes when captured."""
         cs = calls(name)
         for i, x in enumerate(cs):
             if ev is not None:
                 first, last = i == 0, i == len(cs) - 1
-                kda.kda_set_stage_events([ev[0] if first else None, ev[1] if first and last else None,
+                kda.kda_set_stage_events([ev[0] if first else None, ev[1] if name == "prefill_split" else None,
                                           ev[2] if last else None])
             run_call(name, x)
         kda.kda_set_stage_events(None)
@@ -428,8 +430,8 @@ def run_ours(args, rank, world, local_rank):
     ph_ms = {n: [r[n][0].elapsed_time(r[n][2]) / (1 if n.startswith("prefill") else len(calls(n)))
                  for r in records] for n in phases}
     k_ms = {
-        "prefill_transform": [r["prefill"][0].elapsed_time(r["prefill"][1]) for r in records],
-        "prefill_pass_tail": [r["prefill"][1].elapsed_time(r["prefill"][2]) for r in records],
+        "prefill_transform": [r["prefill_split"][0].elapsed_time(r["prefill_split"][1]) for r in records],
+        "prefill_pass": [r["prefill_split"][1].elapsed_time(r["prefill_split"][2]) for r in records],
         "decode": ph_ms["decode"], "verify_chain": ph_ms["verify_chain"],
         "verify_tree": ph_ms["verify_tree"], "commit": ph_ms["commit"],
         "verify_replay": ph_ms["verify_replay"], "commit_replay": ph_ms["commit_replay"],
@@ -438,7 +440,7 @@ def run_ours(args, rank, world, local_rank):
     tot = dict(zip(phases, max_over_ranks([tot[n] for n in phases], world, dev)))
     # a step is one pass over the hot path's phases; the chunk-state and long
     # prefills are reported on their own and kept out of ms_per_step
-    core = [n for n in phases if n not in ("prefill_states", "prefill_long", "prefill_long_calls")]
+    core = [n for n in phases if n not in ("prefill_states", "prefill_split", "prefill_long", "prefill_long_calls")]
 
     # ---- e2e: prefill through the C ABI with host buffers ----
     host = {n: torch.from_numpy(np.ascontiguousarray(pf[n])).pin_memory()
@@ -505,18 +507,14 @@ def run_ours(args, rank, world, local_rank):
     extras = {} if args.no_extras else run_extras(args, dev, stream, flush_l2, gate_seed=rank)
 
     hbm, bf16_tf, sm_max, peak_kind = _peaks()
-    # The library splits a single prefill of 256 chunks or more into four
-    # segments (a transform and a state-pass launch each) when 8 * heads fits
-    # in the SM count; same rule here, to count the launches.
-    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    # every prefill call here (bounded gate) is a chunk transform and a state pass
     def launches_of(T_):
-        seq_nch = (T_ + CHUNK - 1) // CHUNK
-        nseg = 4 if seq_nch >= 256 and 8 * H <= sms else 1
-        return 2 * nseg
+        return 2
 
     prefill_launches = launches_of(PREFILL_T)
-    extra_launches = prefill_launches + (0 if args.no_long else
-                                         launches_of(LONG_T) + LONG_CALLS * launches_of(LONG_T // LONG_CALLS))
+    # the chunk-state and split-timing prefills, and the long ones
+    extra_launches = 2 * prefill_launches + (0 if args.no_long else
+                                             launches_of(LONG_T) + LONG_CALLS * launches_of(LONG_T // LONG_CALLS))
     steps = args.steps
     prefill_s = tot["prefill"] / 1e3
     value = replica_throughput(PREFILL_T, steps, world, prefill_s)
@@ -525,11 +523,11 @@ def run_ours(args, rank, world, local_rank):
     # measured copy bandwidth (9.9 us at 1 x 4096) take far longer than its
     # algorithmic flops (2.2 GFLOP, hi/lo split passes not counted) at the
     # dense BF16 peak (1.2 us).  It is judged on those bytes over the span of
-    # its launches; its flop rate is reported beside.  The exposed pass tail
-    # has no roofline of its own.
+    # its launch; its flop rate is reported beside.  The state pass (its span
+    # after the transform) has no roofline of its own.
     work = {
         "prefill_transform": ("hbm", transform_bytes(PREFILL_T) / 1e9, hbm, "GB/s"),
-        "prefill_pass_tail": None,
+        "prefill_pass": None,
         "decode": ("hbm", decode_bytes(DECODE_B) / 1e9, hbm, "GB/s"),
         "verify_chain": ("hbm", verify_bytes(VERIFY_B, VERIFY_T) / 1e9, hbm, "GB/s"),
         "verify_tree": ("hbm", verify_bytes(VERIFY_B, VERIFY_T) / 1e9, hbm, "GB/s"),

@@ -163,18 +163,16 @@ size_t kda_prefill_workspace_size(kda_dims dims, int num_seqs, int64_t total_tok
  * device sets the kernels' shared-memory limits (cudaFuncSetAttribute); make
  * it before capturing calls into a CUDA graph.
  *
- * Schedule: when every sequence has the same length known on the host (one
- * sequence, or the fixed layout) and spans at least 256 chunks (16384
- * tokens), and 8 * HV * num_seqs does not exceed the SM count, the chunk
- * positions are cut into four segments.  Each segment's state pass runs on a second,
- * highest-priority stream owned by the library while the next segment's
- * transform runs on `stream`.  The state is carried in its pool slot.  That
- * stream and its events are created on the first such call made by each host
- * thread on each device; make that call before any capture too.  They are
- * forked from and joined back to `stream` with events, so ordering relative
- * to `stream` is unchanged: the call completes when `stream` passes it, and
- * under capture the fork and join become graph edges.  Results are bit-for-bit
- * those of the one-segment schedule.
+ * Schedule: everything runs on `stream`: the per-sequence decay check (given
+ * log-decays only), the chunk transform, then the state pass.  When
+ * 8 * HV * num_seqs does not exceed the SM count, each (sequence, head)
+ * chain of chunks runs as two CTAs per value slice; the second starts behind
+ * a chunk whose chain product is certainly left out (its map is zero, or too
+ * small for the bounded state to matter), which it finds within 32 chunks
+ * or else starts from the sequence's first chunk.  Results are bit for bit
+ * those of a single CTA per slice.  The pass is a programmatic dependent
+ * launch of the transform: its CTAs may start on SMs the transform has left
+ * and wait for the transform before reading its records.
  */
 kda_status kda_prefill(kda_dims dims, kda_gate gate, const kda_bf16 *q, const kda_bf16 *k,
                        const kda_bf16 *v, const kda_bf16 *g, const kda_bf16 *beta,

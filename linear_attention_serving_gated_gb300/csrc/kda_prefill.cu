@@ -121,10 +121,6 @@ struct PrefillArgs {
   const int32_t* seq_flags;   // [num_seqs] nonzero: sequence rejected (given decay
                               // out of range); nullptr when nothing is checked
   int32_t* err_flag;
-  // Position segment (seg_len > 0): this launch handles chunk positions
-  // [seg_pos0, seg_pos0 + seg_len) of every sequence, each of which has
-  // seq_nch chunks.  seg_len == 0: every chunk.
-  int seg_pos0, seg_len, seq_nch;
   int64_t tx_units;  // (chunk, head) units of this transform launch
   // Start states [num_seqs][HV][V][K] staged by the transform for a pass that
   // runs each chain in parts (nullptr: the pass reads the pool).  A later
@@ -300,22 +296,12 @@ __device__ __forceinline__ float4 exp_diff4(float4 a, float4 b) {
 __device__ ChunkLoc unit_loc(const PrefillArgs& a, int64_t u, int64_t* cid, int* h) {
   const int64_t cx = u / a.HV;
   *h = (int)(u % a.HV);
-  if (a.seg_len > 0) {  // (sequence, position) within the segment
-    const int n = (int)(cx / a.seg_len), pos = a.seg_pos0 + (int)(cx % a.seg_len);
-    const int64_t b = seq_begin(a, n) + (int64_t)pos * kChunk, e = seq_begin(a, n + 1);
-    *cid = (int64_t)n * a.seq_nch + pos;
-    return b < e ? ChunkLoc{n, b, (int)(e - b < kChunk ? e - b : kChunk)} : ChunkLoc{-1, 0, 0};
-  }
   *cid = cx;
   return locate_chunk(a, cx);
 }
 
 // Global chunk id of transform unit u (arithmetic only; see unit_loc).
-__device__ __forceinline__ int64_t unit_cid(const PrefillArgs& a, int64_t u) {
-  const int64_t cx = u / a.HV;
-  if (a.seg_len > 0) return (cx / a.seg_len) * a.seq_nch + a.seg_pos0 + cx % a.seg_len;
-  return cx;
-}
+__device__ __forceinline__ int64_t unit_cid(const PrefillArgs& a, int64_t u) { return u / a.HV; }
 
 // Persistent: CTA b takes units b, b + gridDim.x, ...  The next unit's q, k, v
 // and gate rows are copied into shared memory while this unit finishes.
@@ -1087,22 +1073,18 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
   __syncthreads();
   if (s_state == 2) return;
   const int64_t t0 = s_t0, t1 = s_t1;
-  // chunk positions [p0, p1) of this sequence in this launch
-  const int nch_seq = (int)((t1 - t0 + kChunk - 1) / kChunk);
-  const int p0 = a.seg_len > 0 ? (a.seg_pos0 < nch_seq ? a.seg_pos0 : nch_seq) : 0;
-  const int p1 = a.seg_len > 0 ? (p0 + a.seg_len < nch_seq ? p0 + a.seg_len : nch_seq) : nch_seq;
-  const int nch = p1 > p0 ? p1 - p0 : 0;  // chunks of this launch; chunk i of them is position p0 + i
+  const int nch = (int)((t1 - t0 + kChunk - 1) / kChunk);  // chunks of the sequence
   // this CTA's share of them: its outputs and chunk-start states, and the
   // final state for the last part
   const int own0 = (int)((int64_t)part * nch / parts), own1 = (int)((int64_t)(part + 1) * nch / parts);
   if (s_state == 1) {  // padding sequence: zero outputs
-    const int64_t ta = t0 + (int64_t)(p0 + own0) * kChunk;
-    const int64_t tb = t0 + (int64_t)(p0 + own1) * kChunk < t1 ? t0 + (int64_t)(p0 + own1) * kChunk : t1;
+    const int64_t ta = t0 + (int64_t)own0 * kChunk;
+    const int64_t tb = t0 + (int64_t)own1 * kChunk < t1 ? t0 + (int64_t)own1 * kChunk : t1;
     for (int64_t idx = tid; idx < (tb - ta) * kVs; idx += kPassThreads)
       a.o[((ta + idx / kVs) * HV + h) * V + v0 + idx % kVs] = 0;
     return;
   }
-  if (own0 >= own1) return;  // no chunk of this sequence in this segment, or none in this part
+  if (own0 >= own1) return;  // no chunk of this sequence in this part
   const int slot = a.state_idx[n];
   float* st = a.pool + ((size_t)slot * HV + h) * V * K;
   const size_t rec_stride = (size_t)HV * kRecBytes;
@@ -1120,9 +1102,9 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
   // L2-normalised keys, beta = sigmoid(raw) < 1 and g <= 0, every map has norm
   // <= 1, so ||S_{c+1}|| <= ||S_c|| + ||B_c|| (the records keep ||B_c||).
   const bool bounded = a.gate.use_qk_l2norm && a.gate.beta_is_raw && (!a.gate.A_log || a.gate.lower_bound <= 0.f);
-  const float* s_start = a.init_states ? a.init_states + ((size_t)n * HV + h) * V * K : st;  // the launch's
-  auto meta_of = [&](int j) -> float2 {  // {tau, ||B_c||} of chunk j of this launch, this slice
-    return __ldcg(reinterpret_cast<const float2*>(a.ws + ((size_t)(s_cbase + p0 + j) * HV + h) * kRecBytes +
+  const float* s_start = a.init_states ? a.init_states + ((size_t)n * HV + h) * V * K : st;  // the sequence's
+  auto meta_of = [&](int j) -> float2 {  // {tau, ||B_c||} of the sequence's chunk j, this slice
+    return __ldcg(reinterpret_cast<const float2*>(a.ws + ((size_t)(s_cbase + j) * HV + h) * kRecBytes +
                                                   kRecMeta) + slice);
   };
   if (bounded && warp < kPassEpiThreads / 32) {  // ||S_start[:, slice]||^2 by warp
@@ -1139,7 +1121,7 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
   // Part k > 0 starts at the latest chunk j + 1 <= own0 (j >= own0 - 32)
   // whose chain product is left out whatever S_j is -- an all-zero map, or
   // tau_j at least twice the bound on S_j -- so that S_{j+1} = B_j bit for
-  // bit; else at the launch's first chunk.  It runs the chunks before own0
+  // bit; else at the sequence's first chunk.  It runs the chunks before own0
   // again without writing their outputs.  Part 0 starts at own0 = 0.
   if (warp == 0) {
     float s0n = 0.f;
@@ -1174,9 +1156,9 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
   }
   __syncthreads();
   const int cs = s_cs;
-  const int nrun = own1 - cs;   // chunks run here, from position p0 + cs
+  const int nrun = own1 - cs;   // chunks run here, from chunk cs
   const int emit0 = own0 - cs;  // the first of them whose outputs are written
-  const uint8_t* ws_head = a.ws + ((size_t)(s_cbase + p0 + cs) * HV + h) * kRecBytes;
+  const uint8_t* ws_head = a.ws + ((size_t)(s_cbase + cs) * HV + h) * kRecBytes;
   const uint32_t tmem = tmem_base;
   const uint32_t dch = tmem;
   constexpr uint32_t idesc2 = tc::idesc_bf16_f32(128, 2 * kVs);
@@ -1350,7 +1332,7 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
       u0 = __ldcg(src);
       u1 = __ldcg(src + kChunk);
     };
-    if (cs == 0) {  // the launch's start state (staged by the transform when run in parts)
+    if (cs == 0) {  // the sequence's start state (staged by the transform when run in parts)
       const float* s0 = a.init_states ? a.init_states + ((size_t)n * HV + h) * V * K : st;
 #pragma unroll
       for (int jj = 0; jj < kColsPerThread; ++jj) S[jj] = s0[(size_t)(v0 + j0 + jj) * K + c];
@@ -1380,7 +1362,7 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
     };
     auto write_intermediate = [&](int ci) {  // S is the start state of chunk ci
       if (!a.intermediate || ci < emit0) return;
-      const int64_t cid = s_cbase + p0 + cs + ci;
+      const int64_t cid = s_cbase + cs + ci;
       if (cid < a.inter_chunks) {
         float* dst = a.intermediate + ((size_t)cid * HV + h) * V * K;
 #pragma unroll
@@ -1403,7 +1385,7 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
       float x[8];
 #pragma unroll
       for (int jj = 0; jj < kColsPerThread; ++jj) x[jj] = a.gate.scale * (dh[jj] + dl[jj] + oo[jj]);
-      const int64_t tcj = t0 + (int64_t)(p0 + cs + cj) * kChunk;
+      const int64_t tcj = t0 + (int64_t)(cs + cj) * kChunk;
       const int len = (int)(t1 - tcj < kChunk ? t1 - tcj : kChunk);
       if (lane < 16 && orow < len && cj >= emit0)
         *reinterpret_cast<uint4*>(a.o + ((tcj + orow) * HV + h) * V + v0 + j0) =
@@ -1569,49 +1551,6 @@ unsigned transform_grid(int64_t units, int dev) {
   return (unsigned)(units < g_num_sms[dev] ? units : g_num_sms[dev]);
 }
 
-// Segmented schedule.  When every sequence has the same number of chunks, at
-// least kSegmentMinChunks of them, and the state pass occupies at most half
-// of the SMs, the chunk positions are cut into kMaxSegments segments in the
-// ratio 12:10:7:3: the pass of segment s runs on a second stream while the
-// transform of segment s+1 runs on the caller's, so the pass (latency-bound,
-// a few SMs) hides under the transform (throughput-bound, all SMs), and the
-// last, unhidden pass segment is short.  The state is carried between pass
-// segments in its pool slot.  Shorter sequences run unsegmented: their pass
-// is short, and the segments' partial waves and the pass's SMs cost the
-// transform more than the overlap saves (1 x 4096 at 16 heads: 268 against
-// 280 us; 1 x 32768: 1731 unsegmented against 1916 us segmented).
-constexpr int kMaxSegments = 4;
-constexpr int kSegmentMinChunks = 256;
-constexpr int kSegmentWeights[kMaxSegments] = {12, 10, 7, 3};
-constexpr int kSegmentWeightSum = 32;
-
-// The second stream (highest priority, so the pass's CTAs are placed before
-// the transform's waiting ones) and its events: one set per host thread and
-// device, created on the first segmented call and kept for the process.
-struct PassStream {
-  cudaStream_t stream = nullptr;
-  cudaEvent_t fork = nullptr, join = nullptr, seg[kMaxSegments] = {};
-  bool ready = false;
-};
-thread_local PassStream t_pass[kMaxDevices];
-
-kda_status pass_stream(int dev, PassStream** out) {
-  PassStream& p = t_pass[dev];
-  if (!p.ready) {
-    int least = 0, greatest = 0;
-    if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess ||
-        cudaStreamCreateWithPriority(&p.stream, cudaStreamNonBlocking, greatest) != cudaSuccess ||
-        cudaEventCreateWithFlags(&p.fork, cudaEventDisableTiming) != cudaSuccess ||
-        cudaEventCreateWithFlags(&p.join, cudaEventDisableTiming) != cudaSuccess)
-      return KDA_ERR_CUDA;
-    for (int i = 0; i < kMaxSegments; ++i)
-      if (cudaEventCreateWithFlags(&p.seg[i], cudaEventDisableTiming) != cudaSuccess) return KDA_ERR_CUDA;
-    p.ready = true;
-  }
-  *out = &p;
-  return KDA_OK;
-}
-
 cudaEvent_t g_stage_events[3] = {nullptr, nullptr, nullptr};
 
 }  // namespace
@@ -1683,26 +1622,17 @@ extern "C" kda_status kda_prefill(kda_dims dims, kda_gate gate, const kda_bf16* 
   args.err_flag = err_flag;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
-  // Kernel shared-memory limits are set once per device, and the second
-  // stream of the segmented schedule is created once per host thread and
-  // device, on the first call made with that device current (so that first
-  // call should precede any stream capture).
+  // Kernel shared-memory limits are set once per device, on the first call
+  // made with that device current.
   int dev = 0;
   if ((s = ensure_kernel_attributes(&dev)) != KDA_OK) return s;
   const int64_t chunks = max_chunks(num_seqs, total_tokens);
-  const dim3 pass_grid(kSlices, dims.HV, num_seqs);
   uint8_t* const ws_states = args.ws + (size_t)chunks * dims.HV * kRecBytes;
   // the kernels for this call's 16-bit element type
   void (*const transform_kernel)(PrefillArgs) =
       dims.dtype == KDA_DTYPE_F16 ? chunk_transform_tc_kernel<true> : chunk_transform_tc_kernel<false>;
   void (*const pass_kernel)(PrefillArgs) =
       dims.dtype == KDA_DTYPE_F16 ? state_pass_kernel<true> : state_pass_kernel<false>;
-  int nseg = 1, seq_nch = 0;
-  if (total_tokens > 0 && (num_seqs == 1 || !cu_seqlens) &&
-      2 * (int64_t)kSlices * dims.HV * num_seqs <= g_num_sms[dev]) {
-    seq_nch = (int)((total_tokens / num_seqs + kChunk - 1) / kChunk);
-    nseg = seq_nch >= kSegmentMinChunks ? kMaxSegments : 1;
-  }
   record_stage(0, st);
   if (!gate.A_log && total_tokens > 0) {
     // given log-decays: flag the sequences the chunk form cannot take
@@ -1716,67 +1646,34 @@ extern "C" kda_status kda_prefill(kda_dims dims, kda_gate gate, const kda_bf16* 
     if ((s = launch_status()) != KDA_OK) return s;
     args.seq_flags = flags;
   }
-  if (nseg <= 1) {
-    // Each (sequence, head, slice) chain in two parts where the grid still
-    // fits the SMs: the second part restarts behind an all-zero map (see the
-    // pass), which halves the chain wherever the decay is strong.  The start
-    // states are then staged by the transform.
-    const int parts = total_tokens > 0 && 2 * (int64_t)kSlices * dims.HV * num_seqs <= g_num_sms[dev] ? 2 : 1;
-    if (parts > 1) args.init_states = reinterpret_cast<float*>(ws_states);
-    if (chunks > 0) {
-      args.tx_units = chunks * dims.HV;
-      transform_kernel<<<transform_grid(args.tx_units, dev), kTxThreads, kTransformTcSmem, st>>>(args);
-      if ((s = launch_status()) != KDA_OK) return s;
-    }
-    const dim3 grid(kSlices * parts, dims.HV, num_seqs);
-    if (g_stage_events[1]) {  // a stage event between the kernels: an ordinary launch
-      record_stage(1, st);
-      pass_kernel<<<grid, kPassThreads, kPassSmem, st>>>(args);
-      s = launch_status();
-    } else {  // dependent launch: the pass's CTAs start as the transform's leave
-      cudaLaunchAttribute attr[1];
-      attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-      attr[0].val.programmaticStreamSerializationAllowed = 1;
-      cudaLaunchConfig_t cfg = {};
-      cfg.gridDim = grid;
-      cfg.blockDim = dim3(kPassThreads);
-      cfg.dynamicSmemBytes = kPassSmem;
-      cfg.stream = st;
-      cfg.attrs = attr;
-      cfg.numAttrs = 1;
-      s = cudaLaunchKernelEx(&cfg, pass_kernel, args) == cudaSuccess ? launch_status() : KDA_ERR_CUDA;
-    }
-  } else {
-    PassStream* ps = nullptr;
-    if ((s = pass_stream(dev, &ps)) != KDA_OK) return s;
-    if (cudaEventRecord(ps->fork, st) != cudaSuccess ||
-        cudaStreamWaitEvent(ps->stream, ps->fork, 0) != cudaSuccess)
-      return KDA_ERR_CUDA;
-    int pos = 0;
-    for (int i = 0; i < nseg && pos < seq_nch && s == KDA_OK; ++i) {
-      PrefillArgs sa = args;
-      int want = (kSegmentWeights[i] * seq_nch + kSegmentWeightSum - 1) / kSegmentWeightSum;
-      if (i == nseg - 1 || pos + want > seq_nch) want = seq_nch - pos;
-      sa.seg_pos0 = pos;
-      sa.seg_len = want;
-      pos += want;
-      sa.seq_nch = seq_nch;
-      sa.tx_units = (int64_t)num_seqs * sa.seg_len * dims.HV;
-      transform_kernel<<<transform_grid(sa.tx_units, dev), kTxThreads, kTransformTcSmem, st>>>(sa);
-      if ((s = launch_status()) != KDA_OK) break;
-      if (cudaEventRecord(ps->seg[i], st) != cudaSuccess ||
-          cudaStreamWaitEvent(ps->stream, ps->seg[i], 0) != cudaSuccess) {
-        s = KDA_ERR_CUDA;
-        break;
-      }
-      pass_kernel<<<pass_grid, kPassThreads, kPassSmem, ps->stream>>>(sa);
-      s = launch_status();
-    }
+  // Each (sequence, head, slice) chain in two parts where the grid still
+  // fits the SMs: the second part restarts behind an all-zero map (see the
+  // pass), which halves the chain wherever the decay is strong.  The start
+  // states are then staged by the transform.
+  const int parts = total_tokens > 0 && 2 * (int64_t)kSlices * dims.HV * num_seqs <= g_num_sms[dev] ? 2 : 1;
+  if (parts > 1) args.init_states = reinterpret_cast<float*>(ws_states);
+  if (chunks > 0) {
+    args.tx_units = chunks * dims.HV;
+    transform_kernel<<<transform_grid(args.tx_units, dev), kTxThreads, kTransformTcSmem, st>>>(args);
+    if ((s = launch_status()) != KDA_OK) return s;
+  }
+  const dim3 grid(kSlices * parts, dims.HV, num_seqs);
+  if (g_stage_events[1]) {  // a stage event between the kernels: an ordinary launch
     record_stage(1, st);
-    // always join, so that a capture of `st` stays well formed
-    if (cudaEventRecord(ps->join, ps->stream) != cudaSuccess ||
-        cudaStreamWaitEvent(st, ps->join, 0) != cudaSuccess)
-      s = KDA_ERR_CUDA;
+    pass_kernel<<<grid, kPassThreads, kPassSmem, st>>>(args);
+    s = launch_status();
+  } else {  // dependent launch: the pass's CTAs start as the transform's leave
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kPassThreads);
+    cfg.dynamicSmemBytes = kPassSmem;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    s = cudaLaunchKernelEx(&cfg, pass_kernel, args) == cudaSuccess ? launch_status() : KDA_ERR_CUDA;
   }
   record_stage(2, st);
   return s;

@@ -6,9 +6,9 @@ parameters and state are its own.  The pages' packed-decode validator ("PR
 snippet) takes HV from the state shape and checks the gate input against
 HV*K while the q and k widths of a packed row follow H; the oracle follows
 the same reading and is pinned to its plain H == HV path (repeated q/k heads).
-Every phase is checked against the oracle: prefill (varlen and the segmented
-single-sequence schedule), decode, chain and tree verify with snapshots, their
-commit, and the ReplaySSM verify and commit.
+Every phase is checked against the oracle: prefill (varlen, and a long single
+sequence whose chains run in two parts), decode, chain and tree verify with
+snapshots, their commit, and the ReplaySSM verify and commit.
 """
 import numpy as np
 import pytest
@@ -53,8 +53,8 @@ def test_grouped_prefill_varlen_with_chunk_states():
     _prefill(d, 2, 4, intermediate=True)
 
 
-def test_grouped_prefill_single_sequence_segmented():
-    """16450 tokens (258 chunk positions) at 4 value heads: the segmented schedule."""
+def test_grouped_prefill_long_single_sequence():
+    """16450 tokens (258 chunks) at 4 value heads, the chains in two parts."""
     d = inputs.prefill_inputs(seed=502, lengths=[16450], H=1, HV=4, slots=3, state_idx=[2])
     _prefill(d, 1, 4)
 

@@ -177,23 +177,23 @@ def test_chunked_prefill_across_calls_matches_one_call():
     assert_s_close(pool[s], opool[s])
 
 
-# --- segmented schedule -----------------------------------------------------
-# A long single sequence (or equal-length fixed layout, 256 chunks or more)
-# whose state pass fits in half the SMs runs in four position segments, the
-# pass of segment s on a second stream alongside the transform of segment
-# s+1, the state carried in the pool slot.  These cases pin the segment edges
-# and the carry.
+# --- chains run in two parts ------------------------------------------------
+# When 8 * heads * sequences fits the SM count, each (sequence, head) chain of
+# chunks runs as two CTAs per value slice; the second restarts behind a chunk
+# whose chain product is certainly left out, or from the sequence's start.
+# These cases pin long sequences with ragged tails, padding sequences, the
+# bit-for-bit agreement with a single CTA per slice, and the dependent launch
+# under graph capture.
 
 @pytest.mark.parametrize("T", [16384 + 452, 16385])
-def test_segmented_prefill_ragged_tail_with_chunk_states(T):
-    """1 x T at 2 heads: 264 or 257 chunk positions cut into four
-    segments, the last chunk ragged (4 tokens, 1 token); chunk-start states
-    too."""
+def test_long_prefill_in_two_parts_ragged_tail_with_chunk_states(T):
+    """1 x T at 2 heads: 264 or 257 chunks in two parts, the last chunk
+    ragged (4 tokens, 1 token); chunk-start states too."""
     d = inputs.prefill_inputs(seed=T, lengths=[T], H=2, slots=3, state_idx=[2])
     check(run_both(d, 2, intermediate=True), d)
 
 
-def test_segmented_prefill_fixed_layout_with_padding_sequence():
+def test_long_prefill_in_two_parts_fixed_layout_with_padding_sequence():
     d = inputs.prefill_inputs(seed=70, lengths=[16400, 16400], H=2, slots=4, state_idx=[3, -1],
                               varlen=False)
     out = run_both(d, 2, varlen=False)
@@ -201,12 +201,13 @@ def test_segmented_prefill_fixed_layout_with_padding_sequence():
     assert torch.all(out["o"][16400:].float() == 0)
 
 
-def test_segmented_prefill_bitwise_equals_unsegmented_batch():
-    """Sequence A alone (one sequence: segmented) and the same tokens as the
-    first sequence of a varlen batch of two (not segmented) give identical
-    bits: the schedule does not change the arithmetic."""
-    H, TA, TB = 4, 16500, 100
-    d = inputs.prefill_inputs(seed=80, lengths=[TA, TB], H=H, slots=4, state_idx=[1, 3])
+def test_prefill_in_two_parts_bitwise_equals_one_part():
+    """Sequence A alone at 16 heads (its chains in two parts) and the same
+    tokens as the first sequence of a varlen batch of three (too many chains
+    to split: one part each) give identical bits: the split does not change
+    the arithmetic."""
+    H, TA, TB = 16, 16500, 100
+    d = inputs.prefill_inputs(seed=80, lengths=[TA, TB, TB], H=H, slots=4, state_idx=[1, 3, 0])
     og, gg = gates(d, H=H)
     x = {name: dev_bf16(d[name]) for name in ("q", "k", "v", "g", "beta")}
     pool0 = dev(d["pool"])
@@ -216,17 +217,17 @@ def test_segmented_prefill_bitwise_equals_unsegmented_batch():
     kda.kda_prefill(kda.dims(H), gg, *(x[n][:TA].contiguous() for n in ("q", "k", "v", "g", "beta")),
                     pool_a, dev(np.array([1], np.int32)), dev(np.array([0, TA], np.int32)), 1, o_a)
     pool_b = pool0.clone()
-    o_b = torch.zeros((TA + TB, H, K), dtype=torch.bfloat16, device="cuda")
+    o_b = torch.zeros((TA + 2 * TB, H, K), dtype=torch.bfloat16, device="cuda")
     kda.kda_prefill(kda.dims(H), gg, x["q"], x["k"], x["v"], x["g"], x["beta"], pool_b,
-                    dev(d["state_idx"]), dev(d["cu_seqlens"]), 2, o_b)
+                    dev(d["state_idx"]), dev(d["cu_seqlens"]), 3, o_b)
     torch.cuda.synchronize()
     assert torch.equal(o_a, o_b[:TA])
     assert torch.equal(pool_a[1], pool_b[1])
 
 
-def test_segmented_prefill_under_graph_capture_matches_eager():
-    """The fork to the pass stream and the join back are captured as graph
-    edges: a replay gives the eager result bit for bit."""
+def test_prefill_under_graph_capture_matches_eager():
+    """The pass's dependent launch is captured as a programmatic graph
+    edge: a replay gives the eager result bit for bit."""
     H, T = 4, 16448
     d = inputs.prefill_inputs(seed=90, lengths=[T], H=H, slots=2, state_idx=[1])
     og, gg = gates(d, H=H)
