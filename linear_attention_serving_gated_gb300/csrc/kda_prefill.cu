@@ -1184,9 +1184,8 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
     for (int w = 0; w < kPassEpiThreads / 32; ++w) m = max(m, s_pmax[b][w]);
     return __uint_as_float(m);
   };
-  auto skip_chain = [&](float2 m, float bnd, float smax) {
-    return !map_stored(m.x) || certain_skip(m.x, bnd) || smax <= m.x;
-  };
+  // The product is left out iff !m_needed, or else iff max|S| <= tau, where
+  // max|S| comes from the per-warp maxima the epilogue publishes only then.
 
   if (copy_warp) {
     // ---- copy warp (one lane) ----
@@ -1272,7 +1271,8 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
             abort = true;
             break;
           }
-          const bool skip = skip_chain(meta, bnd, state_max(b));
+          // the state's maximum is published (and read) only where it decides
+          const bool skip = !m_needed(meta, bnd) || state_max(b) <= meta.x;
           if (m_needed(meta, bnd)) {
             if (!tc::mbar_wait(&m_full[m_used & 1], (m_used >> 1) & 1)) {
               abort = true;
@@ -1419,7 +1419,7 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
       }
       // S_{ci+1} = M_c S_ci + B_c, or B_c where the product cannot change it
       const float bb[8] = {bc0.x, bc0.y, bc0.z, bc0.w, bc1.x, bc1.y, bc1.z, bc1.w};
-      if (!skip_chain(meta, bnd, smax)) {
+      if (m_needed(meta, bnd) && !(smax <= meta.x)) {
         if (!tc::mbar_wait(&ch_bar, nchain & 1)) ok = false;
         ++nchain;
         tc::tc_fence_after();
@@ -1433,10 +1433,12 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
         for (int jj = 0; jj < kColsPerThread; ++jj) S[jj] = bb[jj];
       }
       const int nb = (ci + 1) % kSBufs;
+      // does chunk ci + 1's decision need the maximum of S_{ci+1}?
+      const bool need_next = more && m_needed(nmeta, bnd + meta.y);
       if (more) {
         // its buffer's last readers, chunk ci - 2's products, finished before
         // chunk ci - 2's output product did, which this warp has waited for
-        publish_max(nb);
+        if (need_next) publish_max(nb);
         write_state_operand(nb);
         tc::fence_async_smem();
         tc::tc_fence_before();
@@ -1445,7 +1447,7 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
         write_intermediate(ci + 1);
       }
       if (ci >= 1 && !output(ci - 1, pp0, pp1)) ok = false;  // issued behind chunk ci's chain product
-      if (more) {  // every epilogue warp's maximum of S_{ci+1}
+      if (need_next) {  // every epilogue warp's maximum of S_{ci+1}
         if (!tc::mbar_wait(&s_ready[nb], ((ci + 1) / kSBufs) & 1)) ok = false;
         smax = state_max(nb);
       }
