@@ -60,9 +60,9 @@ LAYERS = 8  # default decode/verify/commit calls per timed replay (--layers)
 # traffic summary under profiles/).
 NCU_TRAFFIC = {
     # the transform launch of one 1x4096 prefill call, 16 heads: read
-    # 67,386,112 B (its inputs) + write 123,509,248 B (the part of the 180 MB
-    # of per-chunk records that leaves L2 before the state pass reads it)
-    "prefill_transform": {"bytes": 190895360, "src": "275e4328ea468af5"},
+    # 68,417,280 B (its inputs) + write 85,145,856 B (the part of its per-chunk
+    # records that leaves L2 before the state pass reads it)
+    "prefill_transform": {"bytes": 153563136, "src": "d7280e8a4bf13b4b"},
 }
 VERIFY_SWEEP = (1, 2, 4, 8, 12, 16, 24, 32, 48)  # requests x 6 draft tokens, chain and tree
 DECODE_SWEEP = (1, 16)  # besides the core step's 48
