@@ -26,6 +26,8 @@
 //     writes each snapshot straight from registers; a tree node whose parent
 //     is not the previous node reloads the parent's snapshot, which this same
 //     thread wrote (so it is visible to it without any barrier).
+#include <atomic>
+
 #include "kda_host.h"
 
 namespace kda {
@@ -91,12 +93,13 @@ struct FoldSmem {
 
 // CTAs per SM the register allocation must allow: 7 (72 registers) lets the
 // 1024 CTAs of a 16-request chain verify run as one wave; tree verify would
-// spill there and gets 5.
-template <int MODE>
-constexpr int kMinCtasPerSm = MODE == kTree ? 5 : 7;
+// spill there and gets 5.  Tree verify with four row groups (64-row CTAs,
+// up to 128 registers) runs 4 per SM.
+template <int MODE, int GROUPS>
+constexpr int kMinCtasPerSm = GROUPS == 4 ? 4 : MODE == kTree ? 5 : 7;
 
 template <int MODE, int GROUPS, bool F16>
-__global__ void __launch_bounds__(128, kMinCtasPerSm<MODE>) recurrent_kernel(const StepArgs args) {
+__global__ void __launch_bounds__(128, (kMinCtasPerSm<MODE, GROUPS>)) recurrent_kernel(const StepArgs args) {
   constexpr int K = kHeadDim, V = kHeadDim;
   __shared__ __align__(16) FoldSmem fs;
   __shared__ int tree_par[kTokBlock];  // tree: the parents of the first kTokBlock nodes
@@ -392,16 +395,40 @@ __global__ void __launch_bounds__(256) commit_kernel(const float* __restrict__ s
   }
 }
 
+// SMs of the current device (looked up once per device).
+int sm_count() {
+  static std::atomic<int> counts[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
+  int n = counts[dev].load(std::memory_order_relaxed);
+  if (n <= 0) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+    counts[dev].store(n, std::memory_order_relaxed);
+  }
+  return n;
+}
+
 template <int MODE>
 kda_status launch_recurrent(const StepArgs& a, cudaStream_t stream) {
   // Small batches use 16-row CTAs so that even one request spreads over 128
   // CTAs; larger batches use 32-row CTAs to halve the per-CTA fold work.
+  // Tree verify takes 64-row CTAs where their grid fits in one wave and the
+  // 32-row one does not (at 16 heads, 12 to 19 requests): its 96-register
+  // kernel runs 5 CTAs per SM, so 32-row CTAs need a second wave there.
   const int64_t units = (int64_t)a.B * a.HV;
+  const int sms = sm_count();
+  if (sms <= 0) return KDA_ERR_CUDA;
   record_stage(0, stream);
   const bool f16 = a.dtype == KDA_DTYPE_F16;
-  if (units * 8 <= 2 * 152) {
+  if (units * 8 <= 2 * (int64_t)sms) {
     dim3 grid(kHeadDim / 16, a.HV, a.B);
     (f16 ? recurrent_kernel<MODE, 1, true> : recurrent_kernel<MODE, 1, false>)<<<grid, 128, 0, stream>>>(a);
+  } else if (MODE == kTree && units * (kHeadDim / 32) > (int64_t)kMinCtasPerSm<MODE, 2> * sms &&
+             units * (kHeadDim / 64) <= (int64_t)kMinCtasPerSm<MODE, 4> * sms) {
+    if constexpr (MODE == kTree) {
+      dim3 grid(kHeadDim / 64, a.HV, a.B);
+      (f16 ? recurrent_kernel<MODE, 4, true> : recurrent_kernel<MODE, 4, false>)<<<grid, 128, 0, stream>>>(a);
+    }
   } else {
     dim3 grid(kHeadDim / 32, a.HV, a.B);
     (f16 ? recurrent_kernel<MODE, 2, true> : recurrent_kernel<MODE, 2, false>)<<<grid, 128, 0, stream>>>(a);
