@@ -87,6 +87,8 @@ struct FoldSmem {
   float k[kTokBlock][kHeadDim];    // k-hat
   float dec[kTokBlock][kHeadDim];  // exp(g)
   float v[kTokBlock][kHeadDim];
+  float gbias[kHeadDim];           // ReplaySSM verify: dt_bias of the head, and
+  float galog;                     // A_log, copied with the token rows
   float beta[kTokBlock];
   float red[kTokBlock][2][4];      // per-warp sums of squares of q and k
 };
@@ -166,14 +168,19 @@ __global__ void __launch_bounds__(128, (kMinCtasPerSm<MODE, GROUPS>)) recurrent_
   };
   if (MODE != kCommitReplay) request_raw(0, T < kTokBlock ? T : kTokBlock);
   // Gate parameters: loaded before the slot lookup so that their latency
-  // overlaps it, except in ReplaySSM verify, where the longer live range
-  // spills at its register budget.  exp(A_log) is taken after the state load.
+  // overlaps it.  ReplaySSM verify, where a longer live range spills at its
+  // register budget, copies them into shared memory with the token rows
+  // instead.  exp(A_log) is taken after the state load.
   constexpr bool kEarlyGate = MODE != kChainReplay;
   const GateArgs& ga = args.gate;
   float alog_early = 0.f, bias_early = 0.f;
   if constexpr (kEarlyGate) {
     alog_early = ga.A_log ? ga.A_log[h] : 0.f;
     bias_early = ga.dt_bias ? ga.dt_bias[h * K + tid] : 0.f;
+  } else {
+    if (ga.dt_bias && tid < kHeadDim / 4) cp_async16(&fs.gbias[tid * 4], ga.dt_bias + h * K + tid * 4);
+    if (ga.A_log && tid == kHeadDim / 4) cp_async4(&fs.galog, ga.A_log + h);
+    cp_async_commit();
   }
 
   const int slot = args.state_idx[r];
@@ -215,8 +222,9 @@ __global__ void __launch_bounds__(128, (kMinCtasPerSm<MODE, GROUPS>)) recurrent_
       S[gi][i] = *reinterpret_cast<const float4*>(root + (size_t)(row0 + gi * 4) * K + i * 32 +
                                                   lane_col);
 
-  const float exp_alog = ga.A_log ? __expf(kEarlyGate ? alog_early : ga.A_log[h]) : 0.f;
-  const float bias_c = kEarlyGate ? bias_early : (ga.dt_bias ? ga.dt_bias[h * K + tid] : 0.f);
+  // (ReplaySSM verify: set once its copies have landed, in the first fold)
+  float exp_alog = kEarlyGate && ga.A_log ? __expf(alog_early) : 0.f;
+  float bias_c = kEarlyGate ? bias_early : 0.f;
 
   for (int tb = 0; tb < T; tb += kTokBlock) {
     const int nt = T - tb < kTokBlock ? T - tb : kTokBlock;
@@ -225,6 +233,10 @@ __global__ void __launch_bounds__(128, (kMinCtasPerSm<MODE, GROUPS>)) recurrent_
     if (tb == 0 || MODE != kCommitReplay) {
       cp_async_wait_all();
       __syncthreads();
+    }
+    if (!kEarlyGate && tb == 0) {
+      exp_alog = ga.A_log ? __expf(fs.galog) : 0.f;
+      bias_c = ga.dt_bias ? fs.gbias[tid] : 0.f;
     }
     float sq[kTokBlock], sk[kTokBlock];
 #pragma unroll
