@@ -83,7 +83,7 @@ constexpr int kSlices = kHeadDim / kVs;
 constexpr uint32_t kRecM = 0;                                  // M_c hi, 128 x 128 (rows c', K = c)
 constexpr uint32_t kRecML = kRecM + 128 * 128 * 2;             // M_c lo
 constexpr uint32_t kRecQ = kRecML + 128 * 128 * 2;             // Q' (BF16), 64 x 128
-constexpr uint32_t kRecB = kRecQ + 64 * 128 * 2;               // B_c, FP32 [slice][quad][128][4]
+constexpr uint32_t kRecB = kRecQ + 64 * 128 * 2;               // B_c, FP32 [slice][32 columns][128 channels]
 constexpr uint32_t kRecOi = kRecB + kHeadDim * kHeadDim * 4;   // P Util, FP32 [slice][quad][64][4]
 constexpr uint32_t kRecMeta = kRecOi + kChunk * kHeadDim * 4;   // FP32 [slice] {tau, ||B_c||}
 constexpr uint32_t kRecBytes = kRecMeta + 128;
@@ -902,11 +902,10 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
 #pragma unroll
         for (int j = 0; j < 4; ++j)
           st_split8(Mh, Mh + 128 * 128 * 2, tc::sw128_offset(row, c0 + 8 * j, 128), d + 8 * j);
-      } else {  // B_c, value slice cg - 4 of row c' -> [slice][quad][128][4]
-        float4* dst = reinterpret_cast<float4*>(rec + kRecB) + (cg - 4) * (kVs / 4) * kHeadDim + row;
+      } else {  // B_c, value slice cg - 4 of row c' -> [slice][value column][128 channels]
+        float* dst = reinterpret_cast<float*>(rec + kRecB) + (size_t)(cg - 4) * kVs * kHeadDim + row;
 #pragma unroll
-        for (int qd = 0; qd < kVs / 4; ++qd)
-          dst[qd * kHeadDim] = make_float4(d[4 * qd], d[4 * qd + 1], d[4 * qd + 2], d[4 * qd + 3]);
+        for (int e = 0; e < kVs; ++e) dst[e * kHeadDim] = d[e];  // a warp: 128 consecutive bytes
         uint32_t mn = 0xffffffffu;  // min |B_c| of the slice as FP32 bits
 #pragma unroll
         for (int e = 0; e < 32; ++e) mn = min(mn, __float_as_uint(d[e]) & 0x7fffffffu);
@@ -1089,7 +1088,25 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
   float* st = a.pool + ((size_t)slot * HV + h) * V * K;
   const size_t rec_stride = (size_t)HV * kRecBytes;
   const int c = row;
-  float S[kColsPerThread];  // epilogue threads: S[c][v0 + j0 .. + 8)
+  // Epilogue threads hold the state in one of two ownerships, the same for
+  // the whole CTA: by channel (S[c][v0 + j0 .. + 8), c = the thread's TMEM
+  // lane), which a chain product's accumulator needs, or by column
+  // (S[cc0 .. + 8)[v0 + jc]), which writes the state operand with two 16-byte
+  // stores instead of sixteen 2-byte ones.  A chunk whose product is
+  // certainly left out (S_{i+1} = B_c) takes the second.
+  float S[kColsPerThread];
+  bool scol = true;  // S is held by column
+  const int jc = tid >> 4, cc0 = (tid & 15) * 8;
+  auto store_state = [&](float* dst) {  // S into a [V][K] FP32 state
+    if (scol) {
+      float4* d = reinterpret_cast<float4*>(dst + (size_t)(v0 + jc) * K + cc0);
+      d[0] = make_float4(S[0], S[1], S[2], S[3]);
+      d[1] = make_float4(S[4], S[5], S[6], S[7]);
+    } else {
+#pragma unroll
+      for (int jj = 0; jj < kColsPerThread; ++jj) dst[(size_t)(v0 + j0 + jj) * K + c] = S[jj];
+    }
+  };
 
   if (warp == 0) tc::tmem_alloc(&tmem_base, kTmemCols);
   tc::tc_fence_before();
@@ -1320,11 +1337,18 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
     }
   } else {
     // ---- epilogue warps ----
-    auto load_bc = [&](int ci, float4& b0, float4& b1) {  // B_c rows c, [slice][quad][128][4]
-      const float4* src = reinterpret_cast<const float4*>(ws_head + (int64_t)ci * (int64_t)rec_stride + kRecB) +
-                          (slice * (kVs / 4) + j0 / 4) * kHeadDim + row;
-      b0 = __ldcg(src);
-      b1 = __ldcg(src + kHeadDim);
+    auto load_b = [&](int ci, bool col, float (&b)[kColsPerThread]) {  // B_c, [slice][column][channel]
+      const float* src = reinterpret_cast<const float*>(ws_head + (int64_t)ci * (int64_t)rec_stride + kRecB) +
+                         slice * kVs * kHeadDim;
+      if (col) {
+        const float4 x = __ldcg(reinterpret_cast<const float4*>(src + jc * kHeadDim + cc0));
+        const float4 y = __ldcg(reinterpret_cast<const float4*>(src + jc * kHeadDim + cc0) + 1);
+        b[0] = x.x; b[1] = x.y; b[2] = x.z; b[3] = x.w;
+        b[4] = y.x; b[5] = y.y; b[6] = y.z; b[7] = y.w;
+      } else {
+#pragma unroll
+        for (int jj = 0; jj < kColsPerThread; ++jj) b[jj] = __ldcg(src + (j0 + jj) * kHeadDim + c);
+      }
     };
     auto load_pu = [&](int ci, float4& u0, float4& u1) {  // P Util rows t, [slice][quad][64][4]
       const float4* src = reinterpret_cast<const float4*>(ws_head + (size_t)ci * rec_stride + kRecOi) +
@@ -1333,14 +1357,12 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
       u1 = __ldcg(src + kChunk);
     };
     if (cs == 0) {  // the sequence's start state (staged by the transform when run in parts)
-      const float* s0 = a.init_states ? a.init_states + ((size_t)n * HV + h) * V * K : st;
-#pragma unroll
-      for (int jj = 0; jj < kColsPerThread; ++jj) S[jj] = s0[(size_t)(v0 + j0 + jj) * K + c];
-    } else {  // S_cs = B_{cs-1}: its map is all zero
-      float4 b0, b1;
-      load_bc(-1, b0, b1);
-      S[0] = b0.x; S[1] = b0.y; S[2] = b0.z; S[3] = b0.w;
-      S[4] = b1.x; S[5] = b1.y; S[6] = b1.z; S[7] = b1.w;
+      const float4* s0 = reinterpret_cast<const float4*>(s_start + (size_t)(v0 + jc) * K + cc0);
+      const float4 x = s0[0], y = s0[1];
+      S[0] = x.x; S[1] = x.y; S[2] = x.z; S[3] = x.w;
+      S[4] = y.x; S[5] = y.y; S[6] = y.z; S[7] = y.w;
+    } else {  // S_cs = B_{cs-1}: its product is left out whatever the state
+      load_b(-1, true, S);
     }
     auto publish_max = [&](int buf) {  // this warp's max|S| for buffer buf's state
       uint32_t m = 0u;
@@ -1350,23 +1372,28 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
       for (int o = 16; o; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
       if (lane == 0) s_pmax[buf][warp] = m;
     };
-    auto write_state_operand = [&](int buf) {
+    auto write_state_operand = [&](int buf) {  // rows j: S_hi[:, j]; rows 32 + j: S_lo[:, j]
       uint8_t* S2 = smb + kSmS + buf * kSmSBytes;
+      if (scol) {
+        uint4 hi, lo;
+        split8(S, hi, lo);
+        *reinterpret_cast<uint4*>(S2 + tc::sw128_offset(jc, cc0, 2 * kVs)) = hi;
+        *reinterpret_cast<uint4*>(S2 + tc::sw128_offset(kVs + jc, cc0, 2 * kVs)) = lo;
+      } else {
 #pragma unroll
-      for (int jj = 0; jj < kColsPerThread; ++jj) {
-        uint16_t hi, lo;
-        tc::split_bf16(S[jj], hi, lo);
-        *reinterpret_cast<uint16_t*>(S2 + tc::sw128_offset(j0 + jj, c, 2 * kVs)) = hi;
-        *reinterpret_cast<uint16_t*>(S2 + tc::sw128_offset(kVs + j0 + jj, c, 2 * kVs)) = lo;
+        for (int jj = 0; jj < kColsPerThread; ++jj) {
+          uint16_t hi, lo;
+          tc::split_bf16(S[jj], hi, lo);
+          *reinterpret_cast<uint16_t*>(S2 + tc::sw128_offset(j0 + jj, c, 2 * kVs)) = hi;
+          *reinterpret_cast<uint16_t*>(S2 + tc::sw128_offset(kVs + j0 + jj, c, 2 * kVs)) = lo;
+        }
       }
     };
     auto write_intermediate = [&](int ci) {  // S is the start state of chunk ci
       if (!a.intermediate || ci < emit0) return;
       const int64_t cid = s_cbase + cs + ci;
       if (cid < a.inter_chunks) {
-        float* dst = a.intermediate + ((size_t)cid * HV + h) * V * K;
-#pragma unroll
-        for (int jj = 0; jj < kColsPerThread; ++jj) dst[(size_t)(v0 + j0 + jj) * K + c] = S[jj];
+        store_state(a.intermediate + ((size_t)cid * HV + h) * V * K);
       } else if (tid == 0 && slice == 0) {
         set_error(a.err_flag, KDA_DEVERR_INTERMEDIATE);
       }
@@ -1394,11 +1421,14 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
       tc::tc_fence_before();
       return ok;
     };
-    float4 bc0, bc1, pu0, pu1, pp0 = make_float4(0.f, 0.f, 0.f, 0.f), pp1 = pp0;  // pp: previous chunk's P Util
-    load_bc(0, bc0, bc1);
-    load_pu(0, pu0, pu1);
-    float2 meta = meta_at(0);
+    auto meta_ahead = [&](int ci) { return ci < nrun ? meta_at(ci) : make_float2(0.f, 0.f); };
+    float4 pu0, pu1, pp0 = make_float4(0.f, 0.f, 0.f, 0.f), pp1 = pp0;  // pp: previous chunk's P Util
+    float bb[kColsPerThread];                                         // the current chunk's B_c
+    float2 meta = meta_at(0), meta1 = meta_ahead(1);  // the current and the next chunk's
     float bnd = s_bnd0;  // bound on the current chunk's start state
+    bool bcol = !m_needed(meta, bnd);  // B_c (and then S) by column: the product is certainly left out
+    load_b(0, bcol, bb);
+    load_pu(0, pu0, pu1);
     publish_max(0);
     write_state_operand(0);
     write_intermediate(0);
@@ -1410,15 +1440,19 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
     int nchain = 0;             // chain products so far
     for (int ci = 0; ci < nrun && ok; ++ci) {
       const bool more = ci + 1 < nrun;
-      float4 nb0 = bc0, nb1 = bc1, nu0 = pu0, nu1 = pu1;
-      float2 nmeta = meta;
-      if (more) {  // next chunk's B_c, P Util and threshold, landing while this one finishes
-        load_bc(ci + 1, nb0, nb1);
+      // the next chunk's B_c, P Util and the threshold after it, landing
+      // while this one finishes
+      const bool ncol = !m_needed(meta1, bnd + meta.y);
+      float nbb[kColsPerThread];
+      float4 nu0 = pu0, nu1 = pu1;
+      float2 meta2 = make_float2(0.f, 0.f);
+      if (more) {
+        load_b(ci + 1, ncol, nbb);
         load_pu(ci + 1, nu0, nu1);
-        nmeta = meta_at(ci + 1);
+        meta2 = meta_ahead(ci + 2);
       }
       // S_{ci+1} = M_c S_ci + B_c, or B_c where the product cannot change it
-      const float bb[8] = {bc0.x, bc0.y, bc0.z, bc0.w, bc1.x, bc1.y, bc1.z, bc1.w};
+      scol = bcol;
       if (m_needed(meta, bnd) && !(smax <= meta.x)) {
         if (!tc::mbar_wait(&ch_bar, nchain & 1)) ok = false;
         ++nchain;
@@ -1434,7 +1468,7 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
       }
       const int nb = (ci + 1) % kSBufs;
       // does chunk ci + 1's decision need the maximum of S_{ci+1}?
-      const bool need_next = more && m_needed(nmeta, bnd + meta.y);
+      const bool need_next = more && !ncol;
       if (more) {
         // its buffer's last readers, chunk ci - 2's products, finished before
         // chunk ci - 2's output product did, which this warp has waited for
@@ -1452,9 +1486,15 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
         smax = state_max(nb);
       }
       pp0 = pu0; pp1 = pu1;
-      bc0 = nb0; bc1 = nb1; pu0 = nu0; pu1 = nu1;
+      pu0 = nu0; pu1 = nu1;
+      if (more) {
+#pragma unroll
+        for (int jj = 0; jj < kColsPerThread; ++jj) bb[jj] = nbb[jj];
+      }
+      bcol = ncol;
       bnd = bnd + meta.y;
-      meta = nmeta;
+      meta = meta1;
+      meta1 = meta2;
     }
     if (ok && !output(nrun - 1, pp0, pp1)) ok = false;
     if (!ok) {
@@ -1463,10 +1503,7 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
     }
   }
   __syncthreads();
-  if (!s_abort && !mma_warp && !copy_warp && part == parts - 1) {
-#pragma unroll
-    for (int jj = 0; jj < kColsPerThread; ++jj) st[(size_t)(v0 + j0 + jj) * K + c] = S[jj];
-  }
+  if (!s_abort && !mma_warp && !copy_warp && part == parts - 1) store_state(st);
   tc::tc_fence_before();
   __syncthreads();
   if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
