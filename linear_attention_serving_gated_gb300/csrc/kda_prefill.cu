@@ -971,7 +971,7 @@ constexpr uint32_t kPassSmem = kSmS + kSBufs * kSmSBytes + 1024;  // + alignment
 // TMEM: the chain product in columns 0-63 (S_hi | S_lo halves), the output
 // product in 64-127 or 128-191 (two buffers)
 constexpr uint32_t kTmemCols = 256;
-constexpr int kOBufs = 2;  // output product buffers (TMEM columns, o_bar barriers)
+constexpr int kOBufs = 3;  // output product buffers (TMEM columns, o_bar barriers)
 static_assert(kStQ == kStM + kStMBytes && kRecQ == kRecM + kStMBytes, "the record's tiles in stage order");
 static_assert(kPassSmem <= 232448, "shared memory");
 // The output product is M = 64: its accumulator rows 16 q + l sit in TMEM
@@ -997,19 +997,20 @@ constexpr int kPassThreads = kPassEpiThreads + 64;  // + the MMA warp and the co
 constexpr int kColsPerThread = kVs / 4;
 
 // Per (sequence, head, 32 value columns), sequential over the sequence's
-// chunks.  Epilogue thread (lane quadrant, column group) owns S[c][v0 + j0 ..
-// + 8) for key channel c = its TMEM lane.  Per chunk i, with S_i its start
-// state:
+// chunks; the 16 epilogue warps own the slice of the state.  Per chunk i,
+// with S_i its start state:
 //   chain   D_ch = M_hi [S_hi | S_lo] + M_lo S_hi      (M=128 N=64, then N=32)
 //           S_{i+1} = D_ch[S_hi half] + D_ch[S_lo half] + B_c
 //   output  D_O  = Q' [S_hi | S_lo]                     (M=64 N=64)
 //           O    = scale (D_O[S_hi half] + D_O[S_lo half] + P Util)
-// Warp 16 issues the products: chunk i's chain product, then chunk i - 1's
-// output product, which thus runs while the epilogue warps turn chunk i's
-// chain product into S_{i+1}, and never delays a chain product.  Warp 17
-// issues the stage copies and L2 prefetches.  Neither blocks the epilogue
-// warps, which own the state; the state operand has three buffers (chunk
-// i - 1's output product may still read S_{i-1} while S_{i+1} is written).
+// Warp 16 issues the products as soon as S_i's operand is written: chunk i's
+// chain product, then its output product, which runs while the epilogue
+// warps turn the chain product into S_{i+1}.  The epilogue finishes chunk
+// i's output one chunk later (after writing S_{i+2}'s operand), so that it
+// never waits for a product just issued: the output has three TMEM buffers,
+// and the state operand three (chunk i's output product may still read S_i
+// while S_{i+1} and S_{i+2} are written).  Warp 17 issues the stage copies
+// and L2 prefetches.  Neither blocks the epilogue warps.
 template <bool F16>
 __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const PrefillArgs a) {
   extern __shared__ uint8_t smraw[];
@@ -1017,7 +1018,7 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
   // copied); Q' stage i & 1 holds chunk i's Q'.
   __shared__ uint64_t m_full[2], q_full[2];
   __shared__ uint64_t m_free[2];             // the M_c stage is free again
-  __shared__ uint64_t ch_bar, o_bar[kOBufs];  // chain product done; chunk i's output product done (i % 2)
+  __shared__ uint64_t ch_bar, o_bar[kOBufs];  // chain product done; chunk i's output product done (i % 3)
   __shared__ uint64_t s_ready[kSBufs];       // state operand buffer b written (per-warp arrivals)
   __shared__ uint32_t s_pmax[kSBufs][kPassEpiThreads / 32];  // per-warp max|S| (FP32 bits) of buffer b's state
   __shared__ uint32_t tmem_base;
@@ -1094,7 +1095,7 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
   // (S[cc0 .. + 8)[v0 + jc]), which writes the state operand with two 16-byte
   // stores instead of sixteen 2-byte ones.  A chunk whose product is
   // certainly left out (S_{i+1} = B_c) takes the second.
-  float S[kColsPerThread];
+  float S[kColsPerThread] = {};
   bool scol = true;  // S is held by column
   const int jc = tid >> 4, cc0 = (tid & 15) * 8;
   auto store_state = [&](float* dst) {  // S into a [V][K] FP32 state
@@ -1279,8 +1280,8 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
       float bnd = s_bnd0;  // bound on chunk ci's start state
       int m_used = 0;      // M_c stages taken
       bool abort = false;
-      for (int ci = 0; ci <= nrun && !abort; ++ci) {
-        if (ci < nrun) {
+      for (int ci = 0; ci < nrun && !abort; ++ci) {
+        {
           const float2 meta_next = ci + 1 < nrun ? meta_at(ci + 1) : make_float2(0.f, 0.f);
           const int b = ci % kSBufs;
           // state operand of chunk ci written (chunk 0's by the prologue)
@@ -1321,14 +1322,13 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
           bnd = bnd + meta.y;
           meta = meta_next;
         }
-        if (ci >= 1) {  // chunk ci - 1's output product, behind chunk ci's chain product
-          if (!tc::mbar_wait(&q_full[(ci - 1) & 1], ((ci - 1) >> 1) & 1)) {
-            abort = true;
-            break;
-          }
-          tc::tc_fence_after();
-          issue_output(ci - 1);
+        // chunk ci's output product, behind its chain product
+        if (!tc::mbar_wait(&q_full[ci & 1], (ci >> 1) & 1)) {
+          abort = true;
+          break;
         }
+        tc::tc_fence_after();
+        issue_output(ci);
       }
       if (abort) {
         s_abort = 1;
