@@ -62,6 +62,11 @@
 //                           are summed in the epilogues)
 //                           with S kept in FP32 registers (one key channel per
 //                           thread) and re-split into BF16 hi/lo operands.
+#include <cuda.h>  // CUtensorMap and its enums (the encoder is fetched at run time)
+#include <cudaTypedefs.h>
+
+#include <atomic>
+
 #include "kda_host.h"
 #include "kda_tc.cuh"
 
@@ -206,6 +211,26 @@ constexpr float kMinLogDecay = -5.5f;  // smallest per-token log-decay the windo
 constexpr int kLdB = 136;       // padded row stride (BF16 elements) of the raw q, k, v tiles
 constexpr int kTxThreads = 1024;
 constexpr int kTxWarps = kTxThreads / 32;
+// Tensor maps of the raw token rows, [T][heads][128] 16-bit elements, box =
+// 64 tokens of one head.  The q, k, v boxes are kLdB elements wide: the 8
+// elements past the row's 128 are outside the tensor and land as zeros, so
+// that the box fills the padded rows of Qs, Ks, Vs exactly.
+struct RowMaps {
+  CUtensorMap q, k, v, g;
+};
+constexpr int kRowThread = 32;  // issues the row copies (thread 0 issues the products)
+
+// 3-D tiled tensor copy global -> shared, completion on an mbarrier.  The
+// shared address is 128-byte aligned; coordinates are (element, head, token).
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int c0, int c1, int c2,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+      "[%5];" ::"r"(tc::smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(tc::smem_u32(bar))
+      : "memory");
+}
+constexpr uint32_t kRowBytes = 3u * kChunk * kLdB * 2 + kChunk * kHeadDim * 2;  // one unit's four boxes
 
 constexpr uint32_t kTxL = 0;                          // L: TF32 128 x 128
 constexpr uint32_t kTxR = kTxL + 128 * 128 * 4;       // R: TF32 64 x 128
@@ -226,6 +251,8 @@ constexpr uint32_t kTxEnd = kTxMisc + (3 * kChunk + 1536 + kHeadDim + 4 + kChunk
 constexpr int kDescBatch = 64;  // unit descriptors looked up together
 constexpr uint32_t kTransformTcSmem = kTxEnd + 1024;
 constexpr uint32_t kTxTmemCols = 512;  // M1, A2, M2: 0-255; the map product: 256-511
+static_assert(kTxQ % 128 == 0 && kTxK % 128 == 0 && kTxV % 128 == 0 && (kTxA2 + 128 * 64 * 2) % 128 == 0,
+              "tensor-copy destinations are 128-byte aligned");
 static_assert(2 * 256 * 64 * 2 <= kTxA2, "B2 fits in the L/R region");
 static_assert(kTxTf + kChunk * kLdT * 4 <= kTxR, "A and (I+A)^-1 stay below X in the R region");
 static_assert(kTxB3 + 2 * 256 * 64 * 2 <= kTxR && kTxMs + 2 * 128 * 128 * 2 <= kTxR,
@@ -306,7 +333,8 @@ __device__ __forceinline__ int64_t unit_cid(const PrefillArgs& a, int64_t u) { r
 // Persistent: CTA b takes units b, b + gridDim.x, ...  The next unit's q, k, v
 // and gate rows are copied into shared memory while this unit finishes.
 template <bool F16>
-__global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const PrefillArgs a) {
+__global__ void __launch_bounds__(kTxThreads, 1)
+    chunk_transform_tc_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ RowMaps rm) {
   extern __shared__ uint8_t smraw[];
   // Unit descriptor: first token and length of the unit's chunk, and whether
   // it is its sequence's first chunk; n < 0 marks a unit that is skipped (no
@@ -318,6 +346,7 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
   };
   static_assert(sizeof(UnitDesc) == 16, "descriptor size");
   __shared__ uint64_t mma_bar;
+  __shared__ uint64_t row_bar;  // a unit's q, k, v and gate input rows landed
   __shared__ uint32_t tmem_base;
   __shared__ UnitDesc s_desc[kDescBatch];
   __shared__ int s_abort, s_ok;
@@ -354,6 +383,7 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
     s_ok = seqlens_valid(a);
     if (!s_ok && blockIdx.x == 0) set_error(a.err_flag, KDA_DEVERR_SEQLENS);
     tc::mbar_init(&mma_bar, 1);
+    tc::mbar_init(&row_bar, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 0) tc::tmem_alloc(&tmem_base, kTxTmemCols);
@@ -375,20 +405,23 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
     return UnitDesc{l.t0, l.n, (int16_t)l.len, (int16_t)(l.t0 == seq_begin(a, l.n))};
   };
   // A unit's raw q, k, v rows into Qs, Ks, Vs and its gate input rows into Gs
-  // (16-byte asynchronous copies, one row piece per thread and tensor; rows
-  // past the chunk's end are zero-filled), dt_bias and A_log of its head into
-  // gbias and galog, and the raw beta of its tokens into braw (plain loads by
-  // threads 64-127, which have nothing else to do until the next barrier).
+  // (one tensor copy of 64 token rows per tensor, issued by thread
+  // kRowThread and completing on row_bar; rows past the last token land as
+  // zeros, rows of the next sequence are zeroed after landing), dt_bias and
+  // A_log of its head into gbias and galog, and the raw beta of its tokens
+  // into braw (plain loads by threads 64-127, which have nothing else to do
+  // until the next barrier).  Every issued batch is awaited once, at the fold
+  // of its unit.
   auto issue_rows = [&](const UnitDesc& ud, int hh) {
-    static_assert(kTxThreads == kChunk * 16, "one 16-byte piece of each row per thread");
-    const int hkk = hh / (a.HV / a.H), row = tid >> 4, piece = (tid & 15) * 8;
-    const bool live = row < ud.len;
-    const int64_t tok = ud.t0 + (live ? row : 0);
-    const uint32_t nb = live ? 16u : 0u;
-    cp_async16_zfill(Qs + (row * kLdB + piece) * 2, a.q + (tok * a.H + hkk) * kHeadDim + piece, nb);
-    cp_async16_zfill(Ks + (row * kLdB + piece) * 2, a.k + (tok * a.H + hkk) * kHeadDim + piece, nb);
-    cp_async16_zfill(Vs + (row * kLdB + piece) * 2, a.v + (tok * a.HV + hh) * kHeadDim + piece, nb);
-    cp_async16_zfill(Gs + (row * kHeadDim + piece) * 2, a.g + (tok * a.HV + hh) * kHeadDim + piece, nb);
+    if (tid == kRowThread) {
+      const int hkk = hh / (a.HV / a.H), t0 = (int)ud.t0;
+      tc::mbar_expect_tx(&row_bar, kRowBytes);
+      tc::fence_async_smem();  // the previous unit's reads of these rows come first
+      tma_load_3d(Qs, &rm.q, 0, hkk, t0, &row_bar);
+      tma_load_3d(Ks, &rm.k, 0, hkk, t0, &row_bar);
+      tma_load_3d(Vs, &rm.v, 0, hh, t0, &row_bar);
+      tma_load_3d(Gs, &rm.g, 0, hh, t0, &row_bar);
+    }
     if (tid < kHeadDim / 4 && a.gate.dt_bias) cp_async16(gbias + tid * 4, a.gate.dt_bias + hh * kHeadDim + tid * 4);
     if (tid == kHeadDim / 4 && a.gate.A_log) cp_async4(galog, a.gate.A_log + hh);
     cp_async_commit();
@@ -398,6 +431,7 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
     }
   };
   bool rows_ready = false;  // this unit's rows were copied during the previous unit
+  uint32_t row_phase = 0;   // row_bar's phase of the next batch awaited
   int it = 0;               // units of this CTA so far
   for (int64_t u = blockIdx.x; s_ok && u < a.tx_units; u += gridDim.x, ++it) {
     const int bi = it % kDescBatch;
@@ -443,6 +477,19 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
     }
     if (!rows_ready) issue_rows(ud, h);
     cp_async_wait_all();
+    if (!tc::mbar_wait(&row_bar, row_phase)) s_abort = 1;
+    row_phase ^= 1;
+    rows_ready = false;
+    if (len < kChunk) {  // rows past the chunk's end (the next sequence's, or zeros): zero
+      const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+      for (int i = tid; i < (kChunk - len) * 16; i += kTxThreads) {
+        const int r = len + (i >> 4), p = i & 15;
+        reinterpret_cast<uint4*>(Qs + r * kLdB * 2)[p] = z;
+        reinterpret_cast<uint4*>(Ks + r * kLdB * 2)[p] = z;
+        reinterpret_cast<uint4*>(Vs + r * kLdB * 2)[p] = z;
+        reinterpret_cast<uint4*>(Gs + r * kHeadDim * 2)[p] = z;
+      }
+    }
     __syncthreads();
     {
       constexpr int kTpw = kChunk / kTxWarps;  // tokens per warp
@@ -945,6 +992,7 @@ __global__ void __launch_bounds__(kTxThreads, 1) chunk_transform_tc_kernel(const
     }
   }  // units
   cp_async_wait_all();  // no copy into shared memory outlives the CTA
+  if (rows_ready) tc::mbar_wait(&row_bar, row_phase, 1u << 20);
   if (tid == 0) tc::bulk_wait_read();  // shared memory stays valid until read
   tc::tc_fence_before();
   __syncthreads();
@@ -1592,6 +1640,34 @@ unsigned transform_grid(int64_t units, int dev) {
 
 cudaEvent_t g_stage_events[3] = {nullptr, nullptr, nullptr};
 
+// The driver's tensor-map encoder, fetched once through the runtime.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static std::atomic<void*> fn{nullptr};
+  void* f = fn.load(std::memory_order_relaxed);
+  if (!f) {
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !f)
+      return nullptr;
+    fn.store(f, std::memory_order_relaxed);
+  }
+  return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+}
+
+// Tensor map of a [T][heads][128] 16-bit tensor, box (box0 elements, 1 head,
+// 64 tokens); elements outside the tensor land as zeros.
+bool encode_rows(CUtensorMap* m, const void* base, int64_t heads, int64_t T, uint32_t box0) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return false;
+  const cuuint64_t dim[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)heads, (cuuint64_t)T};
+  const cuuint64_t stride[2] = {(cuuint64_t)kHeadDim * 2, (cuuint64_t)heads * kHeadDim * 2};
+  const cuuint32_t box[3] = {box0, 1u, (cuuint32_t)kChunk};
+  const cuuint32_t estride[3] = {1u, 1u, 1u};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(base), dim, stride, box, estride,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 // Recorded as an external event node when the stream is being captured, so
@@ -1668,7 +1744,7 @@ extern "C" kda_status kda_prefill(kda_dims dims, kda_gate gate, const kda_bf16* 
   const int64_t chunks = max_chunks(num_seqs, total_tokens);
   uint8_t* const ws_states = args.ws + (size_t)chunks * dims.HV * kRecBytes;
   // the kernels for this call's 16-bit element type
-  void (*const transform_kernel)(PrefillArgs) =
+  void (*const transform_kernel)(PrefillArgs, RowMaps) =
       dims.dtype == KDA_DTYPE_F16 ? chunk_transform_tc_kernel<true> : chunk_transform_tc_kernel<false>;
   void (*const pass_kernel)(PrefillArgs) =
       dims.dtype == KDA_DTYPE_F16 ? state_pass_kernel<true> : state_pass_kernel<false>;
@@ -1691,9 +1767,13 @@ extern "C" kda_status kda_prefill(kda_dims dims, kda_gate gate, const kda_bf16* 
   // states are then staged by the transform.
   const int parts = total_tokens > 0 && 2 * (int64_t)kSlices * dims.HV * num_seqs <= g_num_sms[dev] ? 2 : 1;
   if (parts > 1) args.init_states = reinterpret_cast<float*>(ws_states);
-  if (chunks > 0) {
+  if (chunks > 0 && total_tokens > 0) {  // with no tokens every chunk is empty
     args.tx_units = chunks * dims.HV;
-    transform_kernel<<<transform_grid(args.tx_units, dev), kTxThreads, kTransformTcSmem, st>>>(args);
+    RowMaps maps;
+    if (!encode_rows(&maps.q, q, dims.H, total_tokens, kLdB) || !encode_rows(&maps.k, k, dims.H, total_tokens, kLdB) ||
+        !encode_rows(&maps.v, v, dims.HV, total_tokens, kLdB) || !encode_rows(&maps.g, g, dims.HV, total_tokens, kHeadDim))
+      return KDA_ERR_CUDA;
+    transform_kernel<<<transform_grid(args.tx_units, dev), kTxThreads, kTransformTcSmem, st>>>(args, maps);
     if ((s = launch_status()) != KDA_OK) return s;
   }
   const dim3 grid(kSlices * parts, dims.HV, num_seqs);
