@@ -465,8 +465,11 @@ __global__ void __launch_bounds__(kTxThreads, 1)
     // 1. fold.  The unit's rows are in shared memory (copied during the
     //    previous unit, or now).  Warp w owns tokens [2w, 2w+2), lane l
     //    channels [4l, 4l+4): every shared-memory access of a warp is one
-    //    whole row.  Per-token norms and beta, and Gam by warp-blocked prefix
-    //    (the running sum of a warp's last token is its total).  The previous
+    //    whole row.  Per-token norms and beta, and Gam by warp-blocked prefix:
+    //    each warp's running sum (its last token's is the warp's total), warp
+    //    0 turns the 32 totals into their prefix in place (in warp order, so
+    //    the sums associate as a sequential scan's would), and each warp adds
+    //    the total before it to its other token.  The previous
     //    unit's output staging (L/R and A2h regions) may still be read by its
     //    bulk stores: the fold writes none of it.
     if (a.init_states && ud.first) {  // the sequence's first chunk: stage its start state
@@ -519,16 +522,24 @@ __global__ void __launch_bounds__(kTxThreads, 1)
         f4(GM + t * kLd + c) = run;
       }
       __syncthreads();
-      float4 pre = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int w = 0; w < warp; ++w) {
-        const float4 x = f4(GM + (w * kTpw + kTpw - 1) * kLd + c);
-        pre = make_float4(pre.x + x.x, pre.y + x.y, pre.z + x.z, pre.w + x.w);
-      }
-      __syncthreads();  // every warp has read the totals it needs before any row changes
+      if (warp == 0) {  // the warps' totals -> their inclusive prefix, in place, in warp order
+        float4 acc = f4(GM + (kTpw - 1) * kLd + c);
 #pragma unroll
-      for (int u2 = 0; u2 < kTpw; ++u2) {
-        float4& gg = f4(GM + (warp * kTpw + u2) * kLd + c);
-        gg = make_float4(gg.x + pre.x, gg.y + pre.y, gg.z + pre.z, gg.w + pre.w);
+        for (int w = 1; w < kTxWarps; ++w) {
+          float4& x = f4(GM + (w * kTpw + kTpw - 1) * kLd + c);
+          const float4 y = x;
+          acc = make_float4(y.x + acc.x, y.y + acc.y, y.z + acc.z, y.w + acc.w);
+          x = acc;
+        }
+      }
+      __syncthreads();
+      if (warp > 0) {  // the warp's other tokens: + the total of the warps before it
+        const float4 pre = f4(GM + (warp * kTpw - 1) * kLd + c);
+#pragma unroll
+        for (int u2 = 0; u2 < kTpw - 1; ++u2) {
+          float4& gg = f4(GM + (warp * kTpw + u2) * kLd + c);
+          gg = make_float4(gg.x + pre.x, gg.y + pre.y, gg.z + pre.z, gg.w + pre.w);
+        }
       }
     }
     // the previous unit's output staging (A2 region, upper L/R region) is
