@@ -636,7 +636,8 @@ def run_extras(args, dev, stream, flush_l2, gate_seed=0):
     """Every other configuration of the workload, each timed on its own and
     reported beside the step (not in ms_per_step): the 1x128 prefill at 4
     heads, 1x8192 and 2x4096 at 16 heads, 8 varlen sequences in a 32768-row
-    bucket with garbage padding rows and a 240-slot pool, decode at 1 and 16
+    bucket with garbage padding rows and a 240-slot pool, 256 sequences of
+    128 tokens in one call, decode at 1 and 16
     requests, and chain and tree verify over the request sweep at 6 draft
     tokens.  Each is one CUDA graph (8 layer calls on disjoint buffers for the
     layer phases) replayed after an L2 flush, its kernels bracketed by events
@@ -693,6 +694,8 @@ def run_extras(args, dev, stream, flush_l2, gate_seed=0):
         ("prefill_2x4096_fixed", dict(seed=3, lengths=[4096, 4096], H=H, slots=16, varlen=False), False),
         ("prefill_varlen_8seq_32k_bucket", dict(seed=0, lengths=inputs.varlen_lengths(rng0), H=H, slots=240,
                                                 gb_rows=32768), True),
+        # a batch of many short prefills: 256 sequences x 128 tokens
+        ("prefill_256x128", dict(seed=5, lengths=[128] * 256, H=H, slots=256), True),
     ]
     for name, kw, varlen in prefills:
         d = inputs.prefill_inputs(**kw)
@@ -812,7 +815,7 @@ def main():
     ap.add_argument("--no-long", action="store_true",
                     help="skip the 32768-token prefill phases (about 1.4 GB less device memory, e.g. under ncu)")
     ap.add_argument("--no-extras", action="store_true",
-                    help="skip the other configurations (1x128 at 4 heads, 1x8192, 2x4096, varlen 32K bucket, "
+                    help="skip the other configurations (1x128 at 4 heads, 1x8192, 2x4096, varlen 32K bucket, 256x128, "
                          "decode 1/16, verify sweep)")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", 0))

@@ -152,7 +152,8 @@ size_t kda_prefill_workspace_size(kda_dims dims, int num_seqs, int64_t total_tok
  *   o             [total_tokens, HV, V] BF16 (round to nearest even)
  *   intermediate  NULL, or [sum_n ceil(T_n/64), HV, V, K] FP32: the state at
  *                 the start of every 64-token chunk of every sequence,
- *                 sequence-major.
+ *                 sequence-major.  The records of a padding sequence (slot
+ *                 -1) are not written.
  *   intermediate_chunks
  *                 the number of [HV, V, K] records `intermediate` holds
  *                 (ignored when it is NULL).  The chunk count depends on

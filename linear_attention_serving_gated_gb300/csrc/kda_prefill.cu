@@ -137,13 +137,28 @@ __device__ __forceinline__ int64_t seq_begin(const PrefillArgs& a, int n) {
   return a.cu_seqlens ? (int64_t)a.cu_seqlens[n] : a.total_tokens / a.num_seqs * n;
 }
 
-// Checks cu_seqlens (0 .. total_tokens, non-decreasing).  One thread.
-__device__ bool seqlens_valid(const PrefillArgs& a) {
+// Checks cu_seqlens (0 .. total_tokens, non-decreasing).  A whole warp,
+// 32 sequences per step; every lane gets the answer.
+__device__ bool seqlens_valid_warp(const PrefillArgs& a, int lane) {
   if (!a.cu_seqlens) return true;
   if (a.cu_seqlens[0] != 0 || a.cu_seqlens[a.num_seqs] != a.total_tokens) return false;
-  for (int n = 0; n < a.num_seqs; ++n)
-    if (a.cu_seqlens[n + 1] < a.cu_seqlens[n]) return false;
+  for (int n0 = 0; n0 < a.num_seqs; n0 += 32) {
+    const int n = n0 + lane;
+    if (__any_sync(0xffffffffu, n < a.num_seqs && a.cu_seqlens[n + 1] < a.cu_seqlens[n])) return false;
+  }
   return true;
+}
+
+// Chunks of the sequences before sequence n (the sequence-major chunk id of
+// its first chunk).  A whole warp, 32 sequences per step.
+__device__ int64_t chunk_base_warp(const PrefillArgs& a, int n, int lane) {
+  int64_t base = 0;
+  for (int m0 = 0; m0 < n; m0 += 32) {
+    const int m = m0 + lane;
+    const uint32_t c = m < n ? (uint32_t)((seq_begin(a, m + 1) - seq_begin(a, m) + kChunk - 1) / kChunk) : 0u;
+    base += __reduce_add_sync(0xffffffffu, c);
+  }
+  return base;
 }
 
 struct ChunkLoc {
@@ -152,19 +167,50 @@ struct ChunkLoc {
   int len;      // tokens in the chunk (1..64)
 };
 
-// Maps a global chunk id (sequence-major) to its sequence and token range.
-__device__ ChunkLoc locate_chunk(const PrefillArgs& a, int64_t cid) {
-  int64_t base = 0;
-  for (int n = 0; n < a.num_seqs; ++n) {
-    const int64_t b = seq_begin(a, n), e = seq_begin(a, n + 1);
-    const int64_t nch = (e - b + kChunk - 1) / kChunk;
-    if (cid < base + nch) {
-      const int64_t t0 = b + (cid - base) * kChunk;
-      return ChunkLoc{n, t0, (int)(e - t0 < kChunk ? e - t0 : kChunk)};
-    }
-    base += nch;
+// Maps sorted global chunk ids (sequence-major) to their sequences and token
+// ranges: lane l resolves cid[0] and cid[1] (-1: none), ascending over
+// (lane, 0) then (lane, 1) among the valid ones.  A whole warp walks the
+// sequences 32 at a time (one prefix sum of their chunk counts per step) and
+// stops past the largest id; each lane finds its ids' sequences among the
+// step's 32 by a binary search over the lanes' first chunk ids.
+__device__ void locate_chunks_warp(const PrefillArgs& a, const int64_t (&cid)[2], ChunkLoc (&out)[2], int lane) {
+  out[0] = out[1] = ChunkLoc{-1, 0, 0};
+  int64_t hi = cid[0] > cid[1] ? cid[0] : cid[1];
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    const int64_t y = __shfl_xor_sync(0xffffffffu, hi, o);
+    hi = y > hi ? y : hi;
   }
-  return ChunkLoc{-1, 0, 0};
+  int64_t base = 0;
+  for (int m0 = 0; m0 < a.num_seqs && base <= hi; m0 += 32) {
+    const int m = m0 + lane;
+    const int64_t b = m < a.num_seqs ? seq_begin(a, m) : 0, e = m < a.num_seqs ? seq_begin(a, m + 1) : 0;
+    const int64_t nch = (e - b + kChunk - 1) / kChunk;
+    int64_t incl = nch;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int64_t y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const int64_t lo = base + incl - nch;  // first chunk id of sequence m
+    const int64_t end = base + __shfl_sync(0xffffffffu, incl, 31);
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      int j = 0;  // the last lane whose first chunk id is <= cid[i]
+#pragma unroll
+      for (int step = 16; step; step >>= 1) {
+        const int64_t lj = __shfl_sync(0xffffffffu, lo, j + step);
+        if (cid[i] >= lj) j += step;
+      }
+      const int64_t lo_j = __shfl_sync(0xffffffffu, lo, j), b_j = __shfl_sync(0xffffffffu, b, j),
+                    e_j = __shfl_sync(0xffffffffu, e, j);
+      if (cid[i] >= base && cid[i] < end) {
+        const int64_t t0 = b_j + (cid[i] - lo_j) * kChunk;
+        out[i] = ChunkLoc{m0 + j, t0, (int)(e_j - t0 < kChunk ? e_j - t0 : kChunk)};
+      }
+    }
+    base = end;
+  }
 }
 
 __device__ __forceinline__ float warp_sum(float x) {
@@ -317,16 +363,6 @@ __device__ __forceinline__ float4 exp_diff4(float4 a, float4 b) {
                      decay_exp(a.w - b.w));
 }
 
-// Chunk of transform unit u (chunk-major: u = chunk slot * HV + head): its
-// sequence, first token and length (n = -1 if the slot holds no chunk), its
-// global chunk id and its head.
-__device__ ChunkLoc unit_loc(const PrefillArgs& a, int64_t u, int64_t* cid, int* h) {
-  const int64_t cx = u / a.HV;
-  *h = (int)(u % a.HV);
-  *cid = cx;
-  return locate_chunk(a, cx);
-}
-
 // Global chunk id of transform unit u (arithmetic only; see unit_loc).
 __device__ __forceinline__ int64_t unit_cid(const PrefillArgs& a, int64_t u) { return u / a.HV; }
 
@@ -378,10 +414,15 @@ __global__ void __launch_bounds__(kTxThreads, 1)
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   grid_dependency_launch();
+  if (warp == 1) {
+    const bool ok = seqlens_valid_warp(a, lane);
+    if (lane == 0) {
+      s_ok = ok;
+      if (!ok && blockIdx.x == 0) set_error(a.err_flag, KDA_DEVERR_SEQLENS);
+    }
+  }
   if (tid == 0) {
     s_abort = 0;
-    s_ok = seqlens_valid(a);
-    if (!s_ok && blockIdx.x == 0) set_error(a.err_flag, KDA_DEVERR_SEQLENS);
     tc::mbar_init(&mma_bar, 1);
     tc::mbar_init(&row_bar, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -392,17 +433,31 @@ __global__ void __launch_bounds__(kTxThreads, 1)
   tc::tc_fence_after();
   const uint32_t tmem = tmem_base;
   uint32_t phase = 0;
-  // Descriptors of this CTA's next kDescBatch units, one thread each, so that
-  // the slot lookups (dependent global reads) of a batch overlap.
-  auto describe = [&](int64_t uu) -> UnitDesc {
-    int64_t cid;
-    int hh;
-    const ChunkLoc l = unit_loc(a, uu, &cid, &hh);
-    if (l.n < 0) return UnitDesc{0, -1, 0, 0};
-    const int slot = a.state_idx[l.n];
-    if (slot < 0 || slot >= a.pool_slots) return UnitDesc{0, -1, 0, 0};  // padding / rejected
-    if (a.seq_flags && a.seq_flags[l.n]) return UnitDesc{0, -1, 0, 0};    // given decay out of range
-    return UnitDesc{l.t0, l.n, (int16_t)l.len, (int16_t)(l.t0 == seq_begin(a, l.n))};
+  // Descriptors of this CTA's next kDescBatch units (chunk-major: unit u is
+  // chunk u / HV, head u % HV), by warp 0: the batch's chunk ids ascend, so
+  // one walk over the sequences locates them all; then each lane checks its
+  // two units' slots.
+  static_assert(kDescBatch == 64, "two units per lane of warp 0");
+  auto describe_batch = [&](int64_t u0) {
+    int64_t cid[2];
+    ChunkLoc l[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int64_t uu = u0 + (int64_t)(lane + 32 * i) * gridDim.x;
+      cid[i] = uu < a.tx_units ? uu / a.HV : -1;
+    }
+    locate_chunks_warp(a, cid, l, lane);
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      UnitDesc d{0, -1, 0, 0};
+      if (l[i].n >= 0) {
+        const int slot = a.state_idx[l[i].n];
+        const bool live = slot >= 0 && slot < a.pool_slots &&        // else padding / rejected
+                          !(a.seq_flags && a.seq_flags[l[i].n]);  // given decay out of range
+        if (live) d = UnitDesc{l[i].t0, l[i].n, (int16_t)l[i].len, (int16_t)(l[i].t0 == seq_begin(a, l[i].n))};
+      }
+      s_desc[lane + 32 * i] = d;
+    }
   };
   // A unit's raw q, k, v rows into Qs, Ks, Vs and its gate input rows into Gs
   // (one tensor copy of 64 token rows per tensor, issued by thread
@@ -437,10 +492,7 @@ __global__ void __launch_bounds__(kTxThreads, 1)
     const int bi = it % kDescBatch;
     if (bi == 0) {
       __syncthreads();  // nobody reads the previous batch any more
-      if (tid < kDescBatch) {
-        const int64_t uu = u + (int64_t)tid * gridDim.x;
-        s_desc[tid] = uu < a.tx_units ? describe(uu) : UnitDesc{0, -1, 0, 0};
-      }
+      if (warp == 0) describe_batch(u);
     }
     __syncthreads();  // every thread is done with the previous unit's shared values
     if (tid == 0) {  // read by 9c, after several barriers
@@ -1096,38 +1148,39 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
   const int HV = a.HV, K = kHeadDim, V = kHeadDim;
   const bool reporter = slice == 0 && part == 0;
 
-  if (tid == 0) {
-    s_state = 0;
-    s_abort = 0;
-    if (!seqlens_valid(a)) {
-      s_state = 2;
-      if (reporter && h == 0 && n == 0) set_error(a.err_flag, KDA_DEVERR_SEQLENS);
-    } else {
-      const int slot = a.state_idx[n];
-      if (slot < -1 || slot >= a.pool_slots) {
-        s_state = 2;
-        if (reporter && h == 0) set_error(a.err_flag, KDA_DEVERR_SLOT);
-      } else if (slot == -1) {
-        s_state = 1;
-      } else if (a.seq_flags && a.seq_flags[n]) {
-        s_state = 2;  // given log-decay out of range: flagged by decay_check_kernel
-      }
-      int64_t base = 0;
-      for (int m = 0; m < n; ++m)
-        base += (seq_begin(a, m + 1) - seq_begin(a, m) + kChunk - 1) / kChunk;
+  if (warp == 0) {  // the chunks before sequence n, and the checks, by one warp
+    const bool valid = seqlens_valid_warp(a, lane);
+    const int64_t base = valid ? chunk_base_warp(a, n, lane) : 0;
+    if (lane == 0) {
       s_cbase = base;
-      s_t0 = seq_begin(a, n);
-      s_t1 = seq_begin(a, n + 1);
+      s_state = 0;
+      s_abort = 0;
+      if (!valid) {
+        s_state = 2;
+        if (reporter && h == 0 && n == 0) set_error(a.err_flag, KDA_DEVERR_SEQLENS);
+      } else {
+        const int slot = a.state_idx[n];
+        if (slot < -1 || slot >= a.pool_slots) {
+          s_state = 2;
+          if (reporter && h == 0) set_error(a.err_flag, KDA_DEVERR_SLOT);
+        } else if (slot == -1) {
+          s_state = 1;
+        } else if (a.seq_flags && a.seq_flags[n]) {
+          s_state = 2;  // given log-decay out of range: flagged by decay_check_kernel
+        }
+        s_t0 = seq_begin(a, n);
+        s_t1 = seq_begin(a, n + 1);
+      }
+      for (int i = 0; i < 2; ++i) {
+        tc::mbar_init(&m_full[i], 1);
+        tc::mbar_init(&q_full[i], 1);
+        tc::mbar_init(&m_free[i], 1);
+      }
+      tc::mbar_init(&ch_bar, 1);
+      for (int b = 0; b < kOBufs; ++b) tc::mbar_init(&o_bar[b], 1);
+      for (int b = 0; b < kSBufs; ++b) tc::mbar_init(&s_ready[b], kPassEpiThreads / 32);  // one arrival per epilogue warp
+      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    for (int i = 0; i < 2; ++i) {
-      tc::mbar_init(&m_full[i], 1);
-      tc::mbar_init(&q_full[i], 1);
-      tc::mbar_init(&m_free[i], 1);
-    }
-    tc::mbar_init(&ch_bar, 1);
-    for (int b = 0; b < kOBufs; ++b) tc::mbar_init(&o_bar[b], 1);
-    for (int b = 0; b < kSBufs; ++b) tc::mbar_init(&s_ready[b], kPassEpiThreads / 32);  // one arrival per epilogue warp
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
   if (s_state == 2) return;
