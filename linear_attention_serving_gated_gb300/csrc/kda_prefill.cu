@@ -137,25 +137,38 @@ __device__ __forceinline__ int64_t seq_begin(const PrefillArgs& a, int n) {
   return a.cu_seqlens ? (int64_t)a.cu_seqlens[n] : a.total_tokens / a.num_seqs * n;
 }
 
+// Sequences per lane per step of the warp walks below: their loads are all
+// in flight at once.
+constexpr int kWalkPerLane = 4;
+
 // Checks cu_seqlens (0 .. total_tokens, non-decreasing).  A whole warp,
-// 32 sequences per step; every lane gets the answer.
+// 128 sequences per step; every lane gets the answer.
 __device__ bool seqlens_valid_warp(const PrefillArgs& a, int lane) {
   if (!a.cu_seqlens) return true;
   if (a.cu_seqlens[0] != 0 || a.cu_seqlens[a.num_seqs] != a.total_tokens) return false;
-  for (int n0 = 0; n0 < a.num_seqs; n0 += 32) {
-    const int n = n0 + lane;
-    if (__any_sync(0xffffffffu, n < a.num_seqs && a.cu_seqlens[n + 1] < a.cu_seqlens[n])) return false;
+  for (int n0 = 0; n0 < a.num_seqs; n0 += 32 * kWalkPerLane) {
+    bool bad = false;
+#pragma unroll
+    for (int i = 0; i < kWalkPerLane; ++i) {
+      const int n = n0 + 32 * i + lane;
+      bad |= n < a.num_seqs && a.cu_seqlens[n + 1] < a.cu_seqlens[n];
+    }
+    if (__any_sync(0xffffffffu, bad)) return false;
   }
   return true;
 }
 
 // Chunks of the sequences before sequence n (the sequence-major chunk id of
-// its first chunk).  A whole warp, 32 sequences per step.
+// its first chunk).  A whole warp, 128 sequences per step.
 __device__ int64_t chunk_base_warp(const PrefillArgs& a, int n, int lane) {
   int64_t base = 0;
-  for (int m0 = 0; m0 < n; m0 += 32) {
-    const int m = m0 + lane;
-    const uint32_t c = m < n ? (uint32_t)((seq_begin(a, m + 1) - seq_begin(a, m) + kChunk - 1) / kChunk) : 0u;
+  for (int m0 = 0; m0 < n; m0 += 32 * kWalkPerLane) {
+    uint32_t c = 0u;
+#pragma unroll
+    for (int i = 0; i < kWalkPerLane; ++i) {
+      const int m = m0 + 32 * i + lane;
+      c += m < n ? (uint32_t)((seq_begin(a, m + 1) - seq_begin(a, m) + kChunk - 1) / kChunk) : 0u;
+    }
     base += __reduce_add_sync(0xffffffffu, c);
   }
   return base;
