@@ -23,12 +23,14 @@
 // Rows past the end of a sequence are q = k = v = 0, beta = 0, g = 0, which
 // leave every quantity above unchanged.  Writing O through Q' = Qtil - P W
 // moves the cancellation between Qtil S0 and P W S0 into the per-chunk FP32
-// transform.  Every state-dependent product splits both operands into BF16
-// hi + lo and sums three BF16 products (hi hi, hi lo, lo hi): [W; Q'] against
-// S and Khat^T against U.  With slow decay the state carries its errors over
-// many chunks, and a single BF16 rounding of W (2^-9 relative) already moves
-// the state by several 1e-3 of its RMS over 64 chunks; split, the state error
-// is set by the TF32 A and P products, a few 1e-4 of its RMS at g = 0.
+// transform.  The chunk's end state is affine in its start state,
+//   S_L = M_c S0 + B_c,  M_c = Diag(e^{Gam_L}) - Khat^T W,  B_c = Khat^T Util,
+// so the sequential part of the prefill is one product per chunk.  The
+// state-dependent products split both operands into BF16 hi + lo and sum
+// three BF16 products (hi hi, hi lo, lo hi): with slow decay the state
+// carries its errors over many chunks, and a single BF16 rounding of M_c
+// (2^-9 relative) would move it by several 1e-3 of its RMS over 64 chunks.
+// Q' (which only reaches o) is one BF16 operand against the split state.
 //
 // Decay factors inside A and P are split at a reference token r, the LAST
 // token of each 16-token block of i: e^{Gam_t-Gam_i} = e^{Gam_t-Gam_r} e^{Gam_r-Gam_i}.
@@ -38,30 +40,28 @@
 // lower bound -5 is inside that).  A left factor that underflows can only
 // drop terms that are smaller still.
 //
-// Two kernels:
-//   chunk_transform_tc_kernel  one CTA per (chunk, head), all chunks in
-//                           parallel: fold and cumulative decay on the CUDA
-//                           cores, A and P as tcgen05 products of decay-split
-//                           factors, (I+A)^-1 blocked on the CUDA cores, then
-//                           W, Util, P W, P Util as one more tcgen05 product;
-//                           Q' = Qtil - P W, Khat and gamma in the epilogue.
-//                           Writes one workspace record per (chunk, head)
-//                           already in the tensor-core operand layout.
-//   state_pass_kernel       one CTA per (sequence, head, 32 value columns),
-//                           sequential over the sequence's chunks, on tcgen05:
-//                           per chunk one bulk copy of the record's operand
-//                           tiles into shared memory (double-buffered, mbarrier
-//                           completion; Util and P Util are read straight into
-//                           registers), then
-//                             D1 = [W; Q']_hi [S_hi | S_lo] + [W; Q']_lo S_hi
-//                                                              (TMEM, M=128, N=2x32)
-//                             U  = Util - D1[0:64],  O = scale (D1[64:128] + P Util)
-//                             D2 = Khat_hi^T [U_hi | U_lo] + Khat_lo^T U_hi
-//                             S  = Diag(gamma) S + D2
-//                           (the hi and lo halves sit side by side along N and
-//                           are summed in the epilogues)
-//                           with S kept in FP32 registers (one key channel per
-//                           thread) and re-split into BF16 hi/lo operands.
+// Two kernels (a third checks given log-decays first):
+//   chunk_transform_tc_kernel  persistent, one CTA per SM looping over
+//                           (chunk, head) units, all chunks in parallel:
+//                           rows fed by TMA, fold and cumulative decay on the
+//                           CUDA cores, A and P as tcgen05 products of
+//                           decay-split factors, (I+A)^-1 blocked on the CUDA
+//                           cores, then W, Util, P W, P Util and the map
+//                           Khat^T [W | Util] as tcgen05 products.  Writes
+//                           one workspace record per (chunk, head): M_c (BF16
+//                           hi/lo, only where it is not all zero) and Q' in
+//                           the tensor-core operand layout, B_c and P Util in
+//                           FP32, and per value slice the threshold below
+//                           which M_c S cannot change an FP32 bit of S.
+//   state_pass_kernel       per (sequence, head, 32 value columns) chain,
+//                           sequential over the chunks, on tcgen05:
+//                             S_{i+1} = M_c S_i + B_c   (left out where the
+//                                       product cannot change the result)
+//                             O_i     = scale (Q' S_i + P Util)
+//                           with S in FP32 registers, re-split into a BF16
+//                           hi/lo operand each chunk.  Long chains run as two
+//                           CTAs, the second restarting behind a chunk whose
+//                           product is left out whatever its start state.
 #include <cuda.h>  // CUtensorMap and its enums (the encoder is fetched at run time)
 #include <cudaTypedefs.h>
 
@@ -127,6 +127,7 @@ struct PrefillArgs {
                               // out of range); nullptr when nothing is checked
   int32_t* err_flag;
   int64_t tx_units;  // (chunk, head) units of this transform launch
+  int parts;  // CTAs (items of the state pass) per (sequence, head, slice) chain
   // Start states [num_seqs][HV][V][K] staged by the transform for a pass that
   // runs each chain in parts (nullptr: the pass reads the pool).  A later
   // part writes the pool's final state, so no part may read the slot itself.
@@ -158,20 +159,19 @@ __device__ bool seqlens_valid_warp(const PrefillArgs& a, int lane) {
   return true;
 }
 
-// Chunks of the sequences before sequence n (the sequence-major chunk id of
-// its first chunk).  A whole warp, 128 sequences per step.
-__device__ int64_t chunk_base_warp(const PrefillArgs& a, int n, int lane) {
-  int64_t base = 0;
-  for (int m0 = 0; m0 < n; m0 += 32 * kWalkPerLane) {
+// Chunks of sequences [from, to).  A whole warp, 128 sequences per step.
+__device__ int64_t chunk_count_warp(const PrefillArgs& a, int from, int to, int lane) {
+  int64_t count = 0;
+  for (int m0 = from; m0 < to; m0 += 32 * kWalkPerLane) {
     uint32_t c = 0u;
 #pragma unroll
     for (int i = 0; i < kWalkPerLane; ++i) {
       const int m = m0 + 32 * i + lane;
-      c += m < n ? (uint32_t)((seq_begin(a, m + 1) - seq_begin(a, m) + kChunk - 1) / kChunk) : 0u;
+      c += m < to ? (uint32_t)((seq_begin(a, m + 1) - seq_begin(a, m) + kChunk - 1) / kChunk) : 0u;
     }
-    base += __reduce_add_sync(0xffffffffu, c);
+    count += __reduce_add_sync(0xffffffffu, c);
   }
-  return base;
+  return count;
 }
 
 struct ChunkLoc {
@@ -1135,7 +1135,9 @@ constexpr int kColsPerThread = kVs / 4;
 // and the state operand three (chunk i's output product may still read S_i
 // while S_{i+1} and S_{i+2} are written).  Warp 17 issues the stage copies
 // and L2 prefetches.  Neither blocks the epilogue warps.
-template <bool F16>
+// kMulti: a CTA may run several items (more items than SMs); without it each
+// CTA runs one, and the counters carried between items fold away.
+template <bool F16, bool kMulti>
 __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const PrefillArgs a) {
   extern __shared__ uint8_t smraw[];
   // M_c stage j & 1 holds the j-th M_c copied (maps that are all zero are not
@@ -1147,7 +1149,10 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
   __shared__ uint32_t s_pmax[kSBufs][kPassEpiThreads / 32];  // per-warp max|S| (FP32 bits) of buffer b's state
   __shared__ uint32_t tmem_base;
   __shared__ int64_t s_t0, s_t1, s_cbase;
-  __shared__ int s_state, s_abort, s_cs;
+  __shared__ int s_state, s_abort, s_cs, s_valid;
+  // counters of single roles that run on across items (see below)
+  __shared__ int s_m_issued, s_q_issued, s_m_used, s_wb_n;
+  __shared__ int64_t s_wb_base;
   __shared__ float s_bnd0, s_pn[kPassEpiThreads / 32];  // run start bound; per-warp sums
 
   uint8_t* smb = smraw + ((1024u - (tc::smem_u32(smraw) & 1023u)) & 1023u);
@@ -1156,22 +1161,75 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
   const int quad = warp & 3, cg = (warp >> 2) & 3;  // TMEM lane quadrant, column group
   const int row = quad * 32 + lane;                 // key channel c (chain) or output row
   const int j0 = cg * kColsPerThread;               // first of this thread's value columns
-  const int n = blockIdx.z, h = blockIdx.y, slice = blockIdx.x % kSlices, v0 = slice * kVs;
-  const int part = blockIdx.x / kSlices, parts = gridDim.x / kSlices;  // share of the chain
   const int HV = a.HV, K = kHeadDim, V = kHeadDim;
-  const bool reporter = slice == 0 && part == 0;
+  const int parts = a.parts;  // CTAs per chain
+  const int64_t n_items = (int64_t)kSlices * parts * HV * a.num_seqs;
 
-  if (warp == 0) {  // the chunks before sequence n, and the checks, by one warp
+  // Once per CTA: the cu_seqlens check, the barriers and TMEM.
+  if (warp == 0) {
     const bool valid = seqlens_valid_warp(a, lane);
-    const int64_t base = valid ? chunk_base_warp(a, n, lane) : 0;
     if (lane == 0) {
-      s_cbase = base;
-      s_state = 0;
+      s_valid = valid;
       s_abort = 0;
-      if (!valid) {
-        s_state = 2;
-        if (reporter && h == 0 && n == 0) set_error(a.err_flag, KDA_DEVERR_SEQLENS);
-      } else {
+      s_m_issued = s_q_issued = s_m_used = s_wb_n = 0;
+      s_wb_base = 0;
+      if (!valid && blockIdx.x == 0) set_error(a.err_flag, KDA_DEVERR_SEQLENS);
+      for (int i = 0; i < 2; ++i) {
+        tc::mbar_init(&m_full[i], 1);
+        tc::mbar_init(&q_full[i], 1);
+        tc::mbar_init(&m_free[i], 1);
+      }
+      tc::mbar_init(&ch_bar, 1);
+      for (int b = 0; b < kOBufs; ++b) tc::mbar_init(&o_bar[b], 1);
+      for (int b = 0; b < kSBufs; ++b) tc::mbar_init(&s_ready[b], kPassEpiThreads / 32);  // one arrival per epilogue warp
+      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+  }
+  if (warp == 0) tc::tmem_alloc(&tmem_base, kTmemCols);
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = tmem_base;
+  const uint32_t dch = tmem;
+  constexpr uint32_t idesc2 = tc::idesc_bf16_f32(128, 2 * kVs);
+  constexpr uint32_t idesc1 = tc::idesc_bf16_f32(128, kVs);
+  constexpr uint32_t idescO = tc::idesc_bf16_f32(kChunk, 2 * kVs);
+  const int c = row;
+  // Epilogue threads hold the state in one of two ownerships, the same for
+  // the whole CTA: by channel (S[c][v0 + j0 .. + 8), c = the thread's TMEM
+  // lane), which a chain product's accumulator needs, or by column
+  // (S[cc0 .. + 8)[v0 + jc]), which writes the state operand with two 16-byte
+  // stores instead of sixteen 2-byte ones.  A chunk whose product is
+  // certainly left out (S_{i+1} = B_c) takes the second.
+  float S[kColsPerThread] = {};
+  bool scol = true;  // S is held by column
+  const int jc = tid >> 4, cc0 = (tid & 15) * 8;
+  // Counters that run on across the CTA's items, so that ring positions and
+  // barrier phases continue from one item to the next: the chunks run before
+  // the current item (every role; chunk ci of an item is the CTA's chunk
+  // g0 + ci), the chain products waited for (epilogue), and in shared memory
+  // the M_c and Q' copies issued (copy warp), the M_c stages taken (MMA warp)
+  // and the chunks of sequences [0, s_wb_n), s_wb_base (warp 0).
+  int g0 = 0;
+  int nchain = 0;
+  // Items (sequence n, head h, part, 32-column slice), slices fastest; a CTA
+  // takes every gridDim.x-th, so its sequences ascend.  One CTA per item
+  // where they fit the SMs; otherwise each CTA runs several, which saves the
+  // set-up per item for many short sequences.
+  for (int64_t item = blockIdx.x; s_valid && item < n_items; item += gridDim.x) {
+    const int slice = (int)(item % kSlices), v0 = slice * kVs;
+    const int64_t rest = item / kSlices;
+    const int part = (int)(rest % parts), h = (int)(rest / parts % HV), n = (int)(rest / parts / HV);
+    const bool reporter = slice == 0 && part == 0;
+    __syncthreads();  // every thread is done with the previous item's shared values
+    if (warp == 0) {  // the chunks before sequence n (on from the previous item's), and the checks
+      const int64_t base = s_wb_base + chunk_count_warp(a, s_wb_n, n, lane);
+      __syncwarp();
+      if (lane == 0) {
+        s_wb_base = base;
+        s_wb_n = n;
+        s_cbase = base;
+        s_state = 0;
         const int slot = a.state_idx[n];
         if (slot < -1 || slot >= a.pool_slots) {
           s_state = 2;
@@ -1184,451 +1242,438 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
         s_t0 = seq_begin(a, n);
         s_t1 = seq_begin(a, n + 1);
       }
-      for (int i = 0; i < 2; ++i) {
-        tc::mbar_init(&m_full[i], 1);
-        tc::mbar_init(&q_full[i], 1);
-        tc::mbar_init(&m_free[i], 1);
+    }
+    __syncthreads();
+    if (s_abort) break;
+    if (s_state == 2) continue;
+    const int64_t t0 = s_t0, t1 = s_t1;
+    const int nch = (int)((t1 - t0 + kChunk - 1) / kChunk);  // chunks of the sequence
+    // this item's share of them: its outputs and chunk-start states, and the
+    // final state for the last part
+    const int own0 = (int)((int64_t)part * nch / parts), own1 = (int)((int64_t)(part + 1) * nch / parts);
+    if (s_state == 1) {  // padding sequence: zero outputs
+      const int64_t ta = t0 + (int64_t)own0 * kChunk;
+      const int64_t tb = t0 + (int64_t)own1 * kChunk < t1 ? t0 + (int64_t)own1 * kChunk : t1;
+      for (int64_t idx = tid; idx < (tb - ta) * kVs; idx += kPassThreads)
+        a.o[((ta + idx / kVs) * HV + h) * V + v0 + idx % kVs] = 0;
+      continue;
+    }
+    if (own0 >= own1) continue;  // no chunk of this sequence in this part
+    const int slot = a.state_idx[n];
+    float* st = a.pool + ((size_t)slot * HV + h) * V * K;
+    const size_t rec_stride = (size_t)HV * kRecBytes;
+    scol = true;
+    auto store_state = [&](float* dst) {  // S into a [V][K] FP32 state
+      if (scol) {
+        float4* d = reinterpret_cast<float4*>(dst + (size_t)(v0 + jc) * K + cc0);
+        d[0] = make_float4(S[0], S[1], S[2], S[3]);
+        d[1] = make_float4(S[4], S[5], S[6], S[7]);
+      } else {
+#pragma unroll
+        for (int jj = 0; jj < kColsPerThread; ++jj) dst[(size_t)(v0 + j0 + jj) * K + c] = S[jj];
       }
-      tc::mbar_init(&ch_bar, 1);
-      for (int b = 0; b < kOBufs; ++b) tc::mbar_init(&o_bar[b], 1);
-      for (int b = 0; b < kSBufs; ++b) tc::mbar_init(&s_ready[b], kPassEpiThreads / 32);  // one arrival per epilogue warp
-      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-  }
-  __syncthreads();
-  if (s_state == 2) return;
-  const int64_t t0 = s_t0, t1 = s_t1;
-  const int nch = (int)((t1 - t0 + kChunk - 1) / kChunk);  // chunks of the sequence
-  // this CTA's share of them: its outputs and chunk-start states, and the
-  // final state for the last part
-  const int own0 = (int)((int64_t)part * nch / parts), own1 = (int)((int64_t)(part + 1) * nch / parts);
-  if (s_state == 1) {  // padding sequence: zero outputs
-    const int64_t ta = t0 + (int64_t)own0 * kChunk;
-    const int64_t tb = t0 + (int64_t)own1 * kChunk < t1 ? t0 + (int64_t)own1 * kChunk : t1;
-    for (int64_t idx = tid; idx < (tb - ta) * kVs; idx += kPassThreads)
-      a.o[((ta + idx / kVs) * HV + h) * V + v0 + idx % kVs] = 0;
-    return;
-  }
-  if (own0 >= own1) return;  // no chunk of this sequence in this part
-  const int slot = a.state_idx[n];
-  float* st = a.pool + ((size_t)slot * HV + h) * V * K;
-  const size_t rec_stride = (size_t)HV * kRecBytes;
-  const int c = row;
-  // Epilogue threads hold the state in one of two ownerships, the same for
-  // the whole CTA: by channel (S[c][v0 + j0 .. + 8), c = the thread's TMEM
-  // lane), which a chain product's accumulator needs, or by column
-  // (S[cc0 .. + 8)[v0 + jc]), which writes the state operand with two 16-byte
-  // stores instead of sixteen 2-byte ones.  A chunk whose product is
-  // certainly left out (S_{i+1} = B_c) takes the second.
-  float S[kColsPerThread] = {};
-  bool scol = true;  // S is held by column
-  const int jc = tid >> 4, cc0 = (tid & 15) * 8;
-  auto store_state = [&](float* dst) {  // S into a [V][K] FP32 state
-    if (scol) {
-      float4* d = reinterpret_cast<float4*>(dst + (size_t)(v0 + jc) * K + cc0);
-      d[0] = make_float4(S[0], S[1], S[2], S[3]);
-      d[1] = make_float4(S[4], S[5], S[6], S[7]);
-    } else {
+    };
+    // Everything below reads the chunk transform's records: with a dependent
+    // launch, this is where the transform's completion is awaited (a no-op
+    // after the first item).
+    grid_dependency_wait();
+    // A bound on the slice's states before they are computed: with
+    // L2-normalised keys, beta = sigmoid(raw) < 1 and g <= 0, every map has norm
+    // <= 1, so ||S_{c+1}|| <= ||S_c|| + ||B_c|| (the records keep ||B_c||).
+    const bool bounded = a.gate.use_qk_l2norm && a.gate.beta_is_raw && (!a.gate.A_log || a.gate.lower_bound <= 0.f);
+    const float* s_start = a.init_states ? a.init_states + ((size_t)n * HV + h) * V * K : st;  // the sequence's
+    auto meta_of = [&](int j) -> float2 {  // {tau, ||B_c||} of the sequence's chunk j, this slice
+      return __ldcg(reinterpret_cast<const float2*>(a.ws + ((size_t)(s_cbase + j) * HV + h) * kRecBytes +
+                                                    kRecMeta) + slice);
+    };
+    if (bounded && warp < kPassEpiThreads / 32) {  // ||S_start[:, slice]||^2 by warp
+      float sq = 0.f;
 #pragma unroll
-      for (int jj = 0; jj < kColsPerThread; ++jj) dst[(size_t)(v0 + j0 + jj) * K + c] = S[jj];
+      for (int jj = 0; jj < kColsPerThread; ++jj) {
+        const float x = s_start[(size_t)(v0 + j0 + jj) * K + row];
+        sq += x * x;
+      }
+      sq = warp_sum(sq);
+      if (lane == 0) s_pn[warp] = sq;
     }
-  };
-
-  if (warp == 0) tc::tmem_alloc(&tmem_base, kTmemCols);
-  tc::tc_fence_before();
-  __syncthreads();
-  tc::tc_fence_after();
-  // Everything below reads the chunk transform's records: with a dependent
-  // launch, this is where the transform's completion is awaited.
-  grid_dependency_wait();
-  // A bound on the slice's states before they are computed: with
-  // L2-normalised keys, beta = sigmoid(raw) < 1 and g <= 0, every map has norm
-  // <= 1, so ||S_{c+1}|| <= ||S_c|| + ||B_c|| (the records keep ||B_c||).
-  const bool bounded = a.gate.use_qk_l2norm && a.gate.beta_is_raw && (!a.gate.A_log || a.gate.lower_bound <= 0.f);
-  const float* s_start = a.init_states ? a.init_states + ((size_t)n * HV + h) * V * K : st;  // the sequence's
-  auto meta_of = [&](int j) -> float2 {  // {tau, ||B_c||} of the sequence's chunk j, this slice
-    return __ldcg(reinterpret_cast<const float2*>(a.ws + ((size_t)(s_cbase + j) * HV + h) * kRecBytes +
-                                                  kRecMeta) + slice);
-  };
-  if (bounded && warp < kPassEpiThreads / 32) {  // ||S_start[:, slice]||^2 by warp
-    float sq = 0.f;
-#pragma unroll
-    for (int jj = 0; jj < kColsPerThread; ++jj) {
-      const float x = s_start[(size_t)(v0 + j0 + jj) * K + row];
-      sq += x * x;
-    }
-    sq = warp_sum(sq);
-    if (lane == 0) s_pn[warp] = sq;
-  }
-  __syncthreads();
-  // Part k > 0 starts at the latest chunk j + 1 <= own0 (j >= own0 - 32)
-  // whose chain product is left out whatever S_j is -- an all-zero map, or
-  // tau_j at least twice the bound on S_j -- so that S_{j+1} = B_j bit for
-  // bit; else at the sequence's first chunk.  It runs the chunks before own0
-  // again without writing their outputs.  Part 0 starts at own0 = 0.
-  if (warp == 0) {
-    float s0n = 0.f;
-    if (bounded) {
-      float t = 0.f;
-      for (int w = 0; w < kPassEpiThreads / 32; ++w) t += s_pn[w];
-      s0n = sqrtf(t) * kNormRoundUp;
-    }
-    int cs = 0;
-    float bnd0 = s0n;  // bound on the run's start state
-    if (own0 > 0) {
-      float pre = 0.f;  // sum of ||B_c|| over c < own0: with s0n, a bound on every S_j, j <= own0
+    __syncthreads();
+    // Part k > 0 starts at the latest chunk j + 1 <= own0 (j >= own0 - 32)
+    // whose chain product is left out whatever S_j is -- an all-zero map, or
+    // tau_j at least twice the bound on S_j -- so that S_{j+1} = B_j bit for
+    // bit; else at the sequence's first chunk.  It runs the chunks before own0
+    // again without writing their outputs.  Part 0 starts at own0 = 0.
+    if (warp == 0) {
+      float s0n = 0.f;
       if (bounded) {
-        for (int j = lane; j < own0; j += 32) pre += meta_of(j).y;
-        pre = warp_sum(pre);
+        float t = 0.f;
+        for (int w = 0; w < kPassEpiThreads / 32; ++w) t += s_pn[w];
+        s0n = sqrtf(t) * kNormRoundUp;
       }
-      const float bnd = (s0n + pre) * kNormRoundUp;
-      const int j = own0 - 1 - lane;
-      const float2 mj = j >= 0 ? meta_of(j) : make_float2(0.f, 0.f);
-      const bool cut = j >= 0 && (__float_as_uint(mj.x) == 0x7f800000u || (bounded && 2.f * bnd <= mj.x));
-      const uint32_t m = __ballot_sync(0xffffffffu, cut);
-      if (m) {
-        const int l = __ffs(m) - 1;
-        cs = own0 - l;
-        bnd0 = __shfl_sync(0xffffffffu, mj.y, l);  // S_cs = B_{cs-1}
+      int cs = 0;
+      float bnd0 = s0n;  // bound on the run's start state
+      if (own0 > 0) {
+        float pre = 0.f;  // sum of ||B_c|| over c < own0: with s0n, a bound on every S_j, j <= own0
+        if (bounded) {
+          for (int j = lane; j < own0; j += 32) pre += meta_of(j).y;
+          pre = warp_sum(pre);
+        }
+        const float bnd = (s0n + pre) * kNormRoundUp;
+        const int j = own0 - 1 - lane;
+        const float2 mj = j >= 0 ? meta_of(j) : make_float2(0.f, 0.f);
+        const bool cut = j >= 0 && (__float_as_uint(mj.x) == 0x7f800000u || (bounded && 2.f * bnd <= mj.x));
+        const uint32_t m = __ballot_sync(0xffffffffu, cut);
+        if (m) {
+          const int l = __ffs(m) - 1;
+          cs = own0 - l;
+          bnd0 = __shfl_sync(0xffffffffu, mj.y, l);  // S_cs = B_{cs-1}
+        }
+      }
+      if (lane == 0) {
+        s_cs = cs;
+        s_bnd0 = bnd0;
       }
     }
-    if (lane == 0) {
-      s_cs = cs;
-      s_bnd0 = bnd0;
-    }
-  }
-  __syncthreads();
-  const int cs = s_cs;
-  const int nrun = own1 - cs;   // chunks run here, from chunk cs
-  const int emit0 = own0 - cs;  // the first of them whose outputs are written
-  const uint8_t* ws_head = a.ws + ((size_t)(s_cbase + cs) * HV + h) * kRecBytes;
-  const uint32_t tmem = tmem_base;
-  const uint32_t dch = tmem;
-  constexpr uint32_t idesc2 = tc::idesc_bf16_f32(128, 2 * kVs);
-  constexpr uint32_t idesc1 = tc::idesc_bf16_f32(128, kVs);
-  constexpr uint32_t idescO = tc::idesc_bf16_f32(kChunk, 2 * kVs);
+    __syncthreads();
+    const int cs = s_cs;
+    const int nrun = own1 - cs;   // chunks run here, from chunk cs
+    const int emit0 = own0 - cs;  // the first of them whose outputs are written
+    const uint8_t* ws_head = a.ws + ((size_t)(s_cbase + cs) * HV + h) * kRecBytes;
 
-  // Chunk ci's {tau, ||B_c||} for this slice (tau = +inf: M_c is all zero and
-  // not stored), and the decisions every role takes the same way from them,
-  // from the running bound on the chunk's start state (s_bnd0 plus the
-  // ||B_c|| of the chunks before, added in order) and from the per-warp
-  // maxima of that state.
-  auto meta_at = [&](int ci) -> float2 {
-    return __ldcg(reinterpret_cast<const float2*>(ws_head + (size_t)ci * rec_stride + kRecMeta) + slice);
-  };
-  auto map_stored = [](float tau) { return __float_as_uint(tau) != 0x7f800000u; };
-  // left out whatever the state: the bound (doubled) is within tau
-  auto certain_skip = [&](float tau, float bnd) { return bounded && 2.f * bnd <= tau; };
-  // the M_c stage is copied and taken only for a product that may run
-  auto m_needed = [&](float2 m, float bnd) { return map_stored(m.x) && !certain_skip(m.x, bnd); };
-  auto state_max = [&](int b) -> float {  // max|S| of the state in buffer b (NaN is largest)
-    uint32_t m = 0u;
+    // Chunk ci's {tau, ||B_c||} for this slice (tau = +inf: M_c is all zero and
+    // not stored), and the decisions every role takes the same way from them,
+    // from the running bound on the chunk's start state (s_bnd0 plus the
+    // ||B_c|| of the chunks before, added in order) and from the per-warp
+    // maxima of that state.
+    auto meta_at = [&](int ci) -> float2 {
+      return __ldcg(reinterpret_cast<const float2*>(ws_head + (size_t)ci * rec_stride + kRecMeta) + slice);
+    };
+    auto map_stored = [](float tau) { return __float_as_uint(tau) != 0x7f800000u; };
+    // left out whatever the state: the bound (doubled) is within tau
+    auto certain_skip = [&](float tau, float bnd) { return bounded && 2.f * bnd <= tau; };
+    // the M_c stage is copied and taken only for a product that may run
+    auto m_needed = [&](float2 m, float bnd) { return map_stored(m.x) && !certain_skip(m.x, bnd); };
+    auto state_max = [&](int b) -> float {  // max|S| of the state in buffer b (NaN is largest)
+      uint32_t m = 0u;
 #pragma unroll
-    for (int w = 0; w < kPassEpiThreads / 32; ++w) m = max(m, s_pmax[b][w]);
-    return __uint_as_float(m);
-  };
-  // The product is left out iff !m_needed, or else iff max|S| <= tau, where
-  // max|S| comes from the per-warp maxima the epilogue publishes only then.
+      for (int w = 0; w < kPassEpiThreads / 32; ++w) m = max(m, s_pmax[b][w]);
+      return __uint_as_float(m);
+    };
+    // The product is left out iff !m_needed, or else iff max|S| <= tau, where
+    // max|S| comes from the per-warp maxima the epilogue publishes only then.
 
-  if (copy_warp) {
-    // ---- copy warp (one lane) ----
-    if (lane == 0) {
-      auto rec_of = [&](int cj) { return ws_head + (size_t)cj * rec_stride; };
-      auto prefetch_record = [&](int cj, bool with_m) {  // the operand tiles, this slice of B_c and P Util
-        const uint8_t* rec = rec_of(cj);
-        if (with_m) tc::bulk_prefetch_l2(rec + kRecM, kStMBytes);
-        tc::bulk_prefetch_l2(rec + kRecQ, kStQBytes);
-        tc::bulk_prefetch_l2(rec + kRecB + slice * (kVs * kHeadDim * 4), kVs * kHeadDim * 4);
-        tc::bulk_prefetch_l2(rec + kRecOi + slice * (kVs * kChunk * 4), kVs * kChunk * 4);
-      };
-      auto meta_ahead = [&](int cj) { return cj < nrun ? meta_at(cj) : make_float2(0.f, 0.f); };
-      // chunks cj .. cj + 3, and the bound on chunk cj's start state
-      float2 ta0 = meta_ahead(0), ta1 = meta_ahead(1), ta2 = meta_ahead(2), ta3 = meta_ahead(3);
-      float bnd = s_bnd0;
-      for (int cj = 1; cj < kPassL2Ahead && cj < nrun; ++cj)
-        prefetch_record(cj, cj == 1 ? m_needed(ta1, bnd + ta0.y) : m_needed(ta2, (bnd + ta0.y) + ta1.y));
-      int m_issued = 0, q_issued = 0;  // M_c and Q' copies issued
-      bool abort = false;
-      for (int cj = 0; cj < nrun && !abort; ++cj) {
-        if (m_needed(ta0, bnd)) {  // the M_c stage m_issued & 1 last held copy m_issued - 2
-          if (m_issued >= 2 && !tc::mbar_wait(&m_free[m_issued & 1], ((m_issued - 2) >> 1) & 1)) {
+    if (copy_warp) {
+      // ---- copy warp (one lane) ----
+      if (lane == 0) {
+        auto rec_of = [&](int cj) { return ws_head + (size_t)cj * rec_stride; };
+        auto prefetch_record = [&](int cj, bool with_m) {  // the operand tiles, this slice of B_c and P Util
+          const uint8_t* rec = rec_of(cj);
+          if (with_m) tc::bulk_prefetch_l2(rec + kRecM, kStMBytes);
+          tc::bulk_prefetch_l2(rec + kRecQ, kStQBytes);
+          tc::bulk_prefetch_l2(rec + kRecB + slice * (kVs * kHeadDim * 4), kVs * kHeadDim * 4);
+          tc::bulk_prefetch_l2(rec + kRecOi + slice * (kVs * kChunk * 4), kVs * kChunk * 4);
+        };
+        auto meta_ahead = [&](int cj) { return cj < nrun ? meta_at(cj) : make_float2(0.f, 0.f); };
+        // chunks cj .. cj + 3, and the bound on chunk cj's start state
+        float2 ta0 = meta_ahead(0), ta1 = meta_ahead(1), ta2 = meta_ahead(2), ta3 = meta_ahead(3);
+        float bnd = s_bnd0;
+        for (int cj = 1; cj < kPassL2Ahead && cj < nrun; ++cj)
+          prefetch_record(cj, cj == 1 ? m_needed(ta1, bnd + ta0.y) : m_needed(ta2, (bnd + ta0.y) + ta1.y));
+        int m_issued = s_m_issued, q_issued = s_q_issued;  // M_c and Q' copies issued by the CTA
+        bool abort = false;
+        for (int cj = 0; cj < nrun && !abort; ++cj) {
+          const int gj = g0 + cj;  // the CTA's chunk
+          if (m_needed(ta0, bnd)) {  // the M_c stage m_issued & 1 last held copy m_issued - 2
+            if (m_issued >= 2 && !tc::mbar_wait(&m_free[m_issued & 1], ((m_issued - 2) >> 1) & 1)) {
+              abort = true;
+              break;
+            }
+            tc::fence_async_smem();
+            issue_copy(smb + (m_issued & 1) * kStageBytes + kStM, rec_of(cj) + kRecM, kStMBytes, &m_full[m_issued & 1]);
+            ++m_issued;
+          }
+          // the Q' stage gj & 1 held chunk gj - 2's Q': free once its output product is done
+          if (gj >= 2 && !tc::mbar_wait(&o_bar[(gj - 2) % kOBufs], ((gj - 2) / kOBufs) & 1)) {
             abort = true;
             break;
           }
           tc::fence_async_smem();
-          issue_copy(smb + (m_issued & 1) * kStageBytes + kStM, rec_of(cj) + kRecM, kStMBytes, &m_full[m_issued & 1]);
-          ++m_issued;
+          issue_copy(smb + (gj & 1) * kStageBytes + kStQ, rec_of(cj) + kRecQ, kStQBytes, &q_full[gj & 1]);
+          ++q_issued;
+          if (cj + kPassL2Ahead < nrun)
+            prefetch_record(cj + kPassL2Ahead, m_needed(ta3, ((bnd + ta0.y) + ta1.y) + ta2.y));
+          bnd = bnd + ta0.y;
+          ta0 = ta1;
+          ta1 = ta2;
+          ta2 = ta3;
+          ta3 = meta_ahead(cj + 4);
         }
-        // the Q' stage cj & 1 held chunk cj - 2's Q': free once its output product is done
-        if (cj >= 2 && !tc::mbar_wait(&o_bar[(cj - 2) % kOBufs], ((cj - 2) / kOBufs) & 1)) {
-          abort = true;
-          break;
+        s_m_issued = m_issued;
+        s_q_issued = q_issued;
+        if (abort) {
+          s_abort = 1;
+          set_error(a.err_flag, KDA_DEVERR_TIMEOUT);
         }
-        tc::fence_async_smem();
-        issue_copy(smb + (cj & 1) * kStageBytes + kStQ, rec_of(cj) + kRecQ, kStQBytes, &q_full[cj & 1]);
-        ++q_issued;
-        if (cj + kPassL2Ahead < nrun)
-          prefetch_record(cj + kPassL2Ahead, m_needed(ta3, ((bnd + ta0.y) + ta1.y) + ta2.y));
-        bnd = bnd + ta0.y;
-        ta0 = ta1;
-        ta1 = ta2;
-        ta2 = ta3;
-        ta3 = meta_ahead(cj + 4);
       }
-      if (abort) {
-        s_abort = 1;
-        set_error(a.err_flag, KDA_DEVERR_TIMEOUT);
-      }
-      // no copy may outlive the CTA: the last two of each kind are the
-      // latest phases of their barriers
-      for (int j = m_issued - 2 > 0 ? m_issued - 2 : 0; j < m_issued; ++j)
-        tc::mbar_wait(&m_full[j & 1], (j >> 1) & 1, 1u << 20);
-      for (int j = q_issued - 2 > 0 ? q_issued - 2 : 0; j < q_issued; ++j)
-        tc::mbar_wait(&q_full[j & 1], (j >> 1) & 1, 1u << 20);
-    }
-  } else if (mma_warp) {
-    // ---- MMA warp (one lane) ----
-    if (lane == 0) {
-      auto issue_output = [&](int cj) {  // chunk cj's output product (Q' stage cj & 1, state buffer cj % 3)
-        const uint32_t qq = tc::smem_u32(smb + (cj & 1) * kStageBytes + kStQ);
-        const uint32_t sb2 = tc::smem_u32(smb + kSmS + (cj % kSBufs) * kSmSBytes);
-        const uint32_t dO = tmem + 64 + 64 * (cj % kOBufs);
+    } else if (mma_warp) {
+      // ---- MMA warp (one lane) ----
+      if (lane == 0) {
+        auto issue_output = [&](int cj) {  // the CTA's chunk cj: output product (Q' stage cj & 1, state buffer cj % 3)
+          const uint32_t qq = tc::smem_u32(smb + (cj & 1) * kStageBytes + kStQ);
+          const uint32_t sb2 = tc::smem_u32(smb + kSmS + (cj % kSBufs) * kSmSBytes);
+          const uint32_t dO = tmem + 64 + 64 * (cj % kOBufs);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {  // Q' [S_hi | S_lo]; Q' atom columns are 64 rows (8 KB) apart
-          const uint32_t koff = (k & 3) * 32;
-          tc::mma_bf16(dO, tc::sw128_desc(qq + (k >> 2) * (kChunk * 128) + koff),
-                       tc::sw128_desc(sb2 + (k >> 2) * (2 * kVs * 128) + koff), idescO, k > 0);
-        }
-        tc::mma_commit(&o_bar[cj % kOBufs]);
-      };
-      float2 meta = meta_at(0);
-      float bnd = s_bnd0;  // bound on chunk ci's start state
-      int m_used = 0;      // M_c stages taken
-      bool abort = false;
-      for (int ci = 0; ci < nrun && !abort; ++ci) {
-        {
-          const float2 meta_next = ci + 1 < nrun ? meta_at(ci + 1) : make_float2(0.f, 0.f);
-          const int b = ci % kSBufs;
-          // state operand of chunk ci written (chunk 0's by the prologue)
-          if (!tc::mbar_wait(&s_ready[b], (ci / kSBufs) & 1)) {
-            abort = true;
-            break;
+          for (int k = 0; k < 8; ++k) {  // Q' [S_hi | S_lo]; Q' atom columns are 64 rows (8 KB) apart
+            const uint32_t koff = (k & 3) * 32;
+            tc::mma_bf16(dO, tc::sw128_desc(qq + (k >> 2) * (kChunk * 128) + koff),
+                         tc::sw128_desc(sb2 + (k >> 2) * (2 * kVs * 128) + koff), idescO, k > 0);
           }
-          // the state's maximum is published (and read) only where it decides
-          const bool skip = !m_needed(meta, bnd) || state_max(b) <= meta.x;
-          if (m_needed(meta, bnd)) {
-            if (!tc::mbar_wait(&m_full[m_used & 1], (m_used >> 1) & 1)) {
+          tc::mma_commit(&o_bar[cj % kOBufs]);
+        };
+        float2 meta = meta_at(0);
+        float bnd = s_bnd0;       // bound on chunk ci's start state
+        int m_used = s_m_used;    // M_c stages taken by the CTA
+        bool abort = false;
+        for (int ci = 0; ci < nrun && !abort; ++ci) {
+          const int gi = g0 + ci;  // the CTA's chunk
+          {
+            const float2 meta_next = ci + 1 < nrun ? meta_at(ci + 1) : make_float2(0.f, 0.f);
+            const int b = gi % kSBufs;
+            // state operand of chunk ci written (the item's first by the prologue)
+            if (!tc::mbar_wait(&s_ready[b], (gi / kSBufs) & 1)) {
               abort = true;
               break;
             }
-            if (!skip) {
-              tc::tc_fence_after();
-              const uint32_t mh = tc::smem_u32(smb + (m_used & 1) * kStageBytes + kStM), ml = mh + 128 * 128 * 2;
-              const uint32_t sb2 = tc::smem_u32(smb + kSmS + b * kSmSBytes);
-#pragma unroll
-              for (int k = 0; k < 8; ++k) {  // M_hi [S_hi | S_lo]
-                const uint32_t koff = (k & 3) * 32;
-                tc::mma_bf16(dch, tc::sw128_desc(mh + (k >> 2) * (128 * 128) + koff),
-                             tc::sw128_desc(sb2 + (k >> 2) * (2 * kVs * 128) + koff), idesc2, k > 0);
+            // the state's maximum is published (and read) only where it decides
+            const bool skip = !m_needed(meta, bnd) || state_max(b) <= meta.x;
+            if (m_needed(meta, bnd)) {
+              if (!tc::mbar_wait(&m_full[m_used & 1], (m_used >> 1) & 1)) {
+                abort = true;
+                break;
               }
+              if (!skip) {
+                tc::tc_fence_after();
+                const uint32_t mh = tc::smem_u32(smb + (m_used & 1) * kStageBytes + kStM), ml = mh + 128 * 128 * 2;
+                const uint32_t sb2 = tc::smem_u32(smb + kSmS + b * kSmSBytes);
 #pragma unroll
-              for (int k = 0; k < 8; ++k) {  // + M_lo S_hi, into the S_lo half
-                const uint32_t koff = (k & 3) * 32;
-                tc::mma_bf16(dch + kVs, tc::sw128_desc(ml + (k >> 2) * (128 * 128) + koff),
-                             tc::sw128_desc(sb2 + (k >> 2) * (2 * kVs * 128) + koff), idesc1, true);
+                for (int k = 0; k < 8; ++k) {  // M_hi [S_hi | S_lo]
+                  const uint32_t koff = (k & 3) * 32;
+                  tc::mma_bf16(dch, tc::sw128_desc(mh + (k >> 2) * (128 * 128) + koff),
+                               tc::sw128_desc(sb2 + (k >> 2) * (2 * kVs * 128) + koff), idesc2, k > 0);
+                }
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {  // + M_lo S_hi, into the S_lo half
+                  const uint32_t koff = (k & 3) * 32;
+                  tc::mma_bf16(dch + kVs, tc::sw128_desc(ml + (k >> 2) * (128 * 128) + koff),
+                               tc::sw128_desc(sb2 + (k >> 2) * (2 * kVs * 128) + koff), idesc1, true);
+                }
+                tc::mma_commit(&ch_bar);
+                tc::mma_commit(&m_free[m_used & 1]);
+              } else {
+                mbar_arrive(&m_free[m_used & 1]);  // landed and not read
               }
-              tc::mma_commit(&ch_bar);
-              tc::mma_commit(&m_free[m_used & 1]);
-            } else {
-              mbar_arrive(&m_free[m_used & 1]);  // landed and not read
+              ++m_used;
             }
-            ++m_used;
+            bnd = bnd + meta.y;
+            meta = meta_next;
           }
-          bnd = bnd + meta.y;
-          meta = meta_next;
+          // chunk ci's output product, behind its chain product
+          if (!tc::mbar_wait(&q_full[gi & 1], (gi >> 1) & 1)) {
+            abort = true;
+            break;
+          }
+          tc::tc_fence_after();
+          issue_output(gi);
         }
-        // chunk ci's output product, behind its chain product
-        if (!tc::mbar_wait(&q_full[ci & 1], (ci >> 1) & 1)) {
-          abort = true;
-          break;
+        s_m_used = m_used;
+        if (abort) {
+          s_abort = 1;
+          set_error(a.err_flag, KDA_DEVERR_TIMEOUT);
         }
-        tc::tc_fence_after();
-        issue_output(ci);
       }
-      if (abort) {
+    } else {
+      // ---- epilogue warps ----
+      auto load_b = [&](int ci, bool col, float (&b)[kColsPerThread]) {  // B_c, [slice][column][channel]
+        const float* src = reinterpret_cast<const float*>(ws_head + (int64_t)ci * (int64_t)rec_stride + kRecB) +
+                           slice * kVs * kHeadDim;
+        if (col) {
+          const float4 x = __ldcg(reinterpret_cast<const float4*>(src + jc * kHeadDim + cc0));
+          const float4 y = __ldcg(reinterpret_cast<const float4*>(src + jc * kHeadDim + cc0) + 1);
+          b[0] = x.x; b[1] = x.y; b[2] = x.z; b[3] = x.w;
+          b[4] = y.x; b[5] = y.y; b[6] = y.z; b[7] = y.w;
+        } else {
+#pragma unroll
+          for (int jj = 0; jj < kColsPerThread; ++jj) b[jj] = __ldcg(src + (j0 + jj) * kHeadDim + c);
+        }
+      };
+      auto load_pu = [&](int ci, float4& u0, float4& u1) {  // P Util rows t, [slice][quad][64][4]
+        const float4* src = reinterpret_cast<const float4*>(ws_head + (size_t)ci * rec_stride + kRecOi) +
+                            (slice * (kVs / 4) + j0 / 4) * kChunk + (quad * 16 + (lane & 15));
+        u0 = __ldcg(src);
+        u1 = __ldcg(src + kChunk);
+      };
+      if (cs == 0) {  // the sequence's start state (staged by the transform when run in parts)
+        const float4* s0 = reinterpret_cast<const float4*>(s_start + (size_t)(v0 + jc) * K + cc0);
+        const float4 x = s0[0], y = s0[1];
+        S[0] = x.x; S[1] = x.y; S[2] = x.z; S[3] = x.w;
+        S[4] = y.x; S[5] = y.y; S[6] = y.z; S[7] = y.w;
+      } else {  // S_cs = B_{cs-1}: its product is left out whatever the state
+        load_b(-1, true, S);
+      }
+      auto publish_max = [&](int buf) {  // this warp's max|S| for buffer buf's state
+        uint32_t m = 0u;
+#pragma unroll
+        for (int jj = 0; jj < kColsPerThread; ++jj) m = max(m, __float_as_uint(S[jj]) & 0x7fffffffu);
+#pragma unroll
+        for (int o = 16; o; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if (lane == 0) s_pmax[buf][warp] = m;
+      };
+      auto write_state_operand = [&](int buf) {  // rows j: S_hi[:, j]; rows 32 + j: S_lo[:, j]
+        uint8_t* S2 = smb + kSmS + buf * kSmSBytes;
+        if (scol) {
+          uint4 hi, lo;
+          split8(S, hi, lo);
+          *reinterpret_cast<uint4*>(S2 + tc::sw128_offset(jc, cc0, 2 * kVs)) = hi;
+          *reinterpret_cast<uint4*>(S2 + tc::sw128_offset(kVs + jc, cc0, 2 * kVs)) = lo;
+        } else {
+#pragma unroll
+          for (int jj = 0; jj < kColsPerThread; ++jj) {
+            uint16_t hi, lo;
+            tc::split_bf16(S[jj], hi, lo);
+            *reinterpret_cast<uint16_t*>(S2 + tc::sw128_offset(j0 + jj, c, 2 * kVs)) = hi;
+            *reinterpret_cast<uint16_t*>(S2 + tc::sw128_offset(kVs + j0 + jj, c, 2 * kVs)) = lo;
+          }
+        }
+      };
+      auto write_intermediate = [&](int ci) {  // S is the start state of chunk ci
+        if (!a.intermediate || ci < emit0) return;
+        const int64_t cid = s_cbase + cs + ci;
+        if (cid < a.inter_chunks) {
+          store_state(a.intermediate + ((size_t)cid * HV + h) * V * K);
+        } else if (tid == 0 && slice == 0) {
+          set_error(a.err_flag, KDA_DEVERR_INTERMEDIATE);
+        }
+      };
+      const uint32_t lane_addr = (static_cast<uint32_t>(quad * 32) << 16) + j0;
+      // chunk cj's output: token 16 q + l is in TMEM lane 32 q + l (l < 16)
+      const int orow = quad * 16 + (lane & 15);
+      auto output = [&](int cj, const float4& u0, const float4& u1) -> bool {
+        const int gj = g0 + cj;  // the CTA's chunk
+        const bool ok = tc::mbar_wait(&o_bar[gj % kOBufs], (gj / kOBufs) & 1);
+        tc::tc_fence_after();
+        float dh[kColsPerThread], dl[kColsPerThread];
+        const uint32_t dO = tmem + 64 + 64 * (gj % kOBufs);
+        tc::tmem_ld8(dO + lane_addr, dh);
+        tc::tmem_ld8(dO + lane_addr + kVs, dl);
+        const float oo[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+        float x[8];
+#pragma unroll
+        for (int jj = 0; jj < kColsPerThread; ++jj) x[jj] = a.gate.scale * (dh[jj] + dl[jj] + oo[jj]);
+        const int64_t tcj = t0 + (int64_t)(cs + cj) * kChunk;
+        const int len = (int)(t1 - tcj < kChunk ? t1 - tcj : kChunk);
+        if (lane < 16 && orow < len && cj >= emit0)
+          *reinterpret_cast<uint4*>(a.o + ((tcj + orow) * HV + h) * V + v0 + j0) =
+              make_uint4(pack_out16x2<F16>(x[0], x[1]), pack_out16x2<F16>(x[2], x[3]),
+                         pack_out16x2<F16>(x[4], x[5]), pack_out16x2<F16>(x[6], x[7]));
+        tc::tc_fence_before();
+        return ok;
+      };
+      auto meta_ahead = [&](int ci) { return ci < nrun ? meta_at(ci) : make_float2(0.f, 0.f); };
+      float4 pu0, pu1, pp0 = make_float4(0.f, 0.f, 0.f, 0.f), pp1 = pp0;  // pp: previous chunk's P Util
+      float bb[kColsPerThread];                                         // the current chunk's B_c
+      float2 meta = meta_at(0), meta1 = meta_ahead(1);  // the current and the next chunk's
+      float bnd = s_bnd0;  // bound on the current chunk's start state
+      bool bcol = !m_needed(meta, bnd);  // B_c (and then S) by column: the product is certainly left out
+      load_b(0, bcol, bb);
+      load_pu(0, pu0, pu1);
+      // the buffer's last readers, the previous item's products, are done: this
+      // warp waited for every one of its outputs
+      const int b0 = g0 % kSBufs;
+      publish_max(b0);
+      write_state_operand(b0);
+      write_intermediate(0);
+      tc::fence_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_ready[b0]);
+      bool ok = tc::mbar_wait(&s_ready[b0], (g0 / kSBufs) & 1);
+      float smax = state_max(b0);  // max|S| of the current chunk's start state
+      for (int ci = 0; ci < nrun && ok; ++ci) {
+        const bool more = ci + 1 < nrun;
+        // the next chunk's B_c, P Util and the threshold after it, landing
+        // while this one finishes
+        const bool ncol = !m_needed(meta1, bnd + meta.y);
+        float nbb[kColsPerThread];
+        float4 nu0 = pu0, nu1 = pu1;
+        float2 meta2 = make_float2(0.f, 0.f);
+        if (more) {
+          load_b(ci + 1, ncol, nbb);
+          load_pu(ci + 1, nu0, nu1);
+          meta2 = meta_ahead(ci + 2);
+        }
+        // S_{ci+1} = M_c S_ci + B_c, or B_c where the product cannot change it
+        scol = bcol;
+        if (m_needed(meta, bnd) && !(smax <= meta.x)) {
+          if (!tc::mbar_wait(&ch_bar, nchain & 1)) ok = false;
+          ++nchain;
+          tc::tc_fence_after();
+          float dh[kColsPerThread], dl[kColsPerThread];
+          tc::tmem_ld8(dch + lane_addr, dh);
+          tc::tmem_ld8(dch + lane_addr + kVs, dl);
+#pragma unroll
+          for (int jj = 0; jj < kColsPerThread; ++jj) S[jj] = dh[jj] + dl[jj] + bb[jj];
+        } else {
+#pragma unroll
+          for (int jj = 0; jj < kColsPerThread; ++jj) S[jj] = bb[jj];
+        }
+        const int nb = (g0 + ci + 1) % kSBufs;
+        // does chunk ci + 1's decision need the maximum of S_{ci+1}?
+        const bool need_next = more && !ncol;
+        if (more) {
+          // its buffer's last readers, chunk ci - 2's products, finished before
+          // chunk ci - 2's output product did, which this warp has waited for
+          if (need_next) publish_max(nb);
+          write_state_operand(nb);
+          tc::fence_async_smem();
+          tc::tc_fence_before();
+          __syncwarp();  // the warp's operand writes (and TMEM reads) precede its arrival
+          if (lane == 0) mbar_arrive(&s_ready[nb]);  // the MMA warp may issue chunk ci + 1
+          write_intermediate(ci + 1);
+        }
+        if (ci >= 1 && !output(ci - 1, pp0, pp1)) ok = false;  // issued behind chunk ci's chain product
+        if (need_next) {  // every epilogue warp's maximum of S_{ci+1}
+          if (!tc::mbar_wait(&s_ready[nb], ((g0 + ci + 1) / kSBufs) & 1)) ok = false;
+          smax = state_max(nb);
+        }
+        pp0 = pu0; pp1 = pu1;
+        pu0 = nu0; pu1 = nu1;
+        if (more) {
+#pragma unroll
+          for (int jj = 0; jj < kColsPerThread; ++jj) bb[jj] = nbb[jj];
+        }
+        bcol = ncol;
+        bnd = bnd + meta.y;
+        meta = meta1;
+        meta1 = meta2;
+      }
+      if (ok && !output(nrun - 1, pp0, pp1)) ok = false;
+      if (!ok) {
         s_abort = 1;
         set_error(a.err_flag, KDA_DEVERR_TIMEOUT);
       }
     }
-  } else {
-    // ---- epilogue warps ----
-    auto load_b = [&](int ci, bool col, float (&b)[kColsPerThread]) {  // B_c, [slice][column][channel]
-      const float* src = reinterpret_cast<const float*>(ws_head + (int64_t)ci * (int64_t)rec_stride + kRecB) +
-                         slice * kVs * kHeadDim;
-      if (col) {
-        const float4 x = __ldcg(reinterpret_cast<const float4*>(src + jc * kHeadDim + cc0));
-        const float4 y = __ldcg(reinterpret_cast<const float4*>(src + jc * kHeadDim + cc0) + 1);
-        b[0] = x.x; b[1] = x.y; b[2] = x.z; b[3] = x.w;
-        b[4] = y.x; b[5] = y.y; b[6] = y.z; b[7] = y.w;
-      } else {
-#pragma unroll
-        for (int jj = 0; jj < kColsPerThread; ++jj) b[jj] = __ldcg(src + (j0 + jj) * kHeadDim + c);
-      }
-    };
-    auto load_pu = [&](int ci, float4& u0, float4& u1) {  // P Util rows t, [slice][quad][64][4]
-      const float4* src = reinterpret_cast<const float4*>(ws_head + (size_t)ci * rec_stride + kRecOi) +
-                          (slice * (kVs / 4) + j0 / 4) * kChunk + (quad * 16 + (lane & 15));
-      u0 = __ldcg(src);
-      u1 = __ldcg(src + kChunk);
-    };
-    if (cs == 0) {  // the sequence's start state (staged by the transform when run in parts)
-      const float4* s0 = reinterpret_cast<const float4*>(s_start + (size_t)(v0 + jc) * K + cc0);
-      const float4 x = s0[0], y = s0[1];
-      S[0] = x.x; S[1] = x.y; S[2] = x.z; S[3] = x.w;
-      S[4] = y.x; S[5] = y.y; S[6] = y.z; S[7] = y.w;
-    } else {  // S_cs = B_{cs-1}: its product is left out whatever the state
-      load_b(-1, true, S);
-    }
-    auto publish_max = [&](int buf) {  // this warp's max|S| for buffer buf's state
-      uint32_t m = 0u;
-#pragma unroll
-      for (int jj = 0; jj < kColsPerThread; ++jj) m = max(m, __float_as_uint(S[jj]) & 0x7fffffffu);
-#pragma unroll
-      for (int o = 16; o; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
-      if (lane == 0) s_pmax[buf][warp] = m;
-    };
-    auto write_state_operand = [&](int buf) {  // rows j: S_hi[:, j]; rows 32 + j: S_lo[:, j]
-      uint8_t* S2 = smb + kSmS + buf * kSmSBytes;
-      if (scol) {
-        uint4 hi, lo;
-        split8(S, hi, lo);
-        *reinterpret_cast<uint4*>(S2 + tc::sw128_offset(jc, cc0, 2 * kVs)) = hi;
-        *reinterpret_cast<uint4*>(S2 + tc::sw128_offset(kVs + jc, cc0, 2 * kVs)) = lo;
-      } else {
-#pragma unroll
-        for (int jj = 0; jj < kColsPerThread; ++jj) {
-          uint16_t hi, lo;
-          tc::split_bf16(S[jj], hi, lo);
-          *reinterpret_cast<uint16_t*>(S2 + tc::sw128_offset(j0 + jj, c, 2 * kVs)) = hi;
-          *reinterpret_cast<uint16_t*>(S2 + tc::sw128_offset(kVs + j0 + jj, c, 2 * kVs)) = lo;
-        }
-      }
-    };
-    auto write_intermediate = [&](int ci) {  // S is the start state of chunk ci
-      if (!a.intermediate || ci < emit0) return;
-      const int64_t cid = s_cbase + cs + ci;
-      if (cid < a.inter_chunks) {
-        store_state(a.intermediate + ((size_t)cid * HV + h) * V * K);
-      } else if (tid == 0 && slice == 0) {
-        set_error(a.err_flag, KDA_DEVERR_INTERMEDIATE);
-      }
-    };
-    const uint32_t lane_addr = (static_cast<uint32_t>(quad * 32) << 16) + j0;
-    // chunk cj's output: token 16 q + l is in TMEM lane 32 q + l (l < 16)
-    const int orow = quad * 16 + (lane & 15);
-    auto output = [&](int cj, const float4& u0, const float4& u1) -> bool {
-      const bool ok = tc::mbar_wait(&o_bar[cj % kOBufs], (cj / kOBufs) & 1);
-      tc::tc_fence_after();
-      float dh[kColsPerThread], dl[kColsPerThread];
-      const uint32_t dO = tmem + 64 + 64 * (cj % kOBufs);
-      tc::tmem_ld8(dO + lane_addr, dh);
-      tc::tmem_ld8(dO + lane_addr + kVs, dl);
-      const float oo[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-      float x[8];
-#pragma unroll
-      for (int jj = 0; jj < kColsPerThread; ++jj) x[jj] = a.gate.scale * (dh[jj] + dl[jj] + oo[jj]);
-      const int64_t tcj = t0 + (int64_t)(cs + cj) * kChunk;
-      const int len = (int)(t1 - tcj < kChunk ? t1 - tcj : kChunk);
-      if (lane < 16 && orow < len && cj >= emit0)
-        *reinterpret_cast<uint4*>(a.o + ((tcj + orow) * HV + h) * V + v0 + j0) =
-            make_uint4(pack_out16x2<F16>(x[0], x[1]), pack_out16x2<F16>(x[2], x[3]),
-                       pack_out16x2<F16>(x[4], x[5]), pack_out16x2<F16>(x[6], x[7]));
-      tc::tc_fence_before();
-      return ok;
-    };
-    auto meta_ahead = [&](int ci) { return ci < nrun ? meta_at(ci) : make_float2(0.f, 0.f); };
-    float4 pu0, pu1, pp0 = make_float4(0.f, 0.f, 0.f, 0.f), pp1 = pp0;  // pp: previous chunk's P Util
-    float bb[kColsPerThread];                                         // the current chunk's B_c
-    float2 meta = meta_at(0), meta1 = meta_ahead(1);  // the current and the next chunk's
-    float bnd = s_bnd0;  // bound on the current chunk's start state
-    bool bcol = !m_needed(meta, bnd);  // B_c (and then S) by column: the product is certainly left out
-    load_b(0, bcol, bb);
-    load_pu(0, pu0, pu1);
-    publish_max(0);
-    write_state_operand(0);
-    write_intermediate(0);
-    tc::fence_async_smem();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&s_ready[0]);
-    bool ok = tc::mbar_wait(&s_ready[0], 0);
-    float smax = state_max(0);  // max|S| of the current chunk's start state
-    int nchain = 0;             // chain products so far
-    for (int ci = 0; ci < nrun && ok; ++ci) {
-      const bool more = ci + 1 < nrun;
-      // the next chunk's B_c, P Util and the threshold after it, landing
-      // while this one finishes
-      const bool ncol = !m_needed(meta1, bnd + meta.y);
-      float nbb[kColsPerThread];
-      float4 nu0 = pu0, nu1 = pu1;
-      float2 meta2 = make_float2(0.f, 0.f);
-      if (more) {
-        load_b(ci + 1, ncol, nbb);
-        load_pu(ci + 1, nu0, nu1);
-        meta2 = meta_ahead(ci + 2);
-      }
-      // S_{ci+1} = M_c S_ci + B_c, or B_c where the product cannot change it
-      scol = bcol;
-      if (m_needed(meta, bnd) && !(smax <= meta.x)) {
-        if (!tc::mbar_wait(&ch_bar, nchain & 1)) ok = false;
-        ++nchain;
-        tc::tc_fence_after();
-        float dh[kColsPerThread], dl[kColsPerThread];
-        tc::tmem_ld8(dch + lane_addr, dh);
-        tc::tmem_ld8(dch + lane_addr + kVs, dl);
-#pragma unroll
-        for (int jj = 0; jj < kColsPerThread; ++jj) S[jj] = dh[jj] + dl[jj] + bb[jj];
-      } else {
-#pragma unroll
-        for (int jj = 0; jj < kColsPerThread; ++jj) S[jj] = bb[jj];
-      }
-      const int nb = (ci + 1) % kSBufs;
-      // does chunk ci + 1's decision need the maximum of S_{ci+1}?
-      const bool need_next = more && !ncol;
-      if (more) {
-        // its buffer's last readers, chunk ci - 2's products, finished before
-        // chunk ci - 2's output product did, which this warp has waited for
-        if (need_next) publish_max(nb);
-        write_state_operand(nb);
-        tc::fence_async_smem();
-        tc::tc_fence_before();
-        __syncwarp();  // the warp's operand writes (and TMEM reads) precede its arrival
-        if (lane == 0) mbar_arrive(&s_ready[nb]);  // the MMA warp may issue chunk ci + 1
-        write_intermediate(ci + 1);
-      }
-      if (ci >= 1 && !output(ci - 1, pp0, pp1)) ok = false;  // issued behind chunk ci's chain product
-      if (need_next) {  // every epilogue warp's maximum of S_{ci+1}
-        if (!tc::mbar_wait(&s_ready[nb], ((ci + 1) / kSBufs) & 1)) ok = false;
-        smax = state_max(nb);
-      }
-      pp0 = pu0; pp1 = pu1;
-      pu0 = nu0; pu1 = nu1;
-      if (more) {
-#pragma unroll
-        for (int jj = 0; jj < kColsPerThread; ++jj) bb[jj] = nbb[jj];
-      }
-      bcol = ncol;
-      bnd = bnd + meta.y;
-      meta = meta1;
-      meta1 = meta2;
-    }
-    if (ok && !output(nrun - 1, pp0, pp1)) ok = false;
-    if (!ok) {
-      s_abort = 1;
-      set_error(a.err_flag, KDA_DEVERR_TIMEOUT);
-    }
+    __syncthreads();
+    if (!s_abort && !mma_warp && !copy_warp && part == parts - 1) store_state(st);
+    g0 += nrun;
+    if constexpr (!kMulti) break;
+  }  // items
+  if (copy_warp && lane == 0) {
+    // no copy may outlive the CTA: the last two of each kind are the latest
+    // phases of their barriers
+    const int m_issued = s_m_issued, q_issued = s_q_issued;
+    for (int j = m_issued - 2 > 0 ? m_issued - 2 : 0; j < m_issued; ++j)
+      tc::mbar_wait(&m_full[j & 1], (j >> 1) & 1, 1u << 20);
+    for (int j = q_issued - 2 > 0 ? q_issued - 2 : 0; j < q_issued; ++j)
+      tc::mbar_wait(&q_full[j & 1], (j >> 1) & 1, 1u << 20);
   }
-  __syncthreads();
-  if (!s_abort && !mma_warp && !copy_warp && part == parts - 1) store_state(st);
   tc::tc_fence_before();
   __syncthreads();
   if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
@@ -1699,9 +1744,13 @@ kda_status ensure_kernel_attributes(int* dev_out) {
                            (int)kTransformTcSmem) != cudaSuccess ||
       cudaFuncSetAttribute(chunk_transform_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)kTransformTcSmem) != cudaSuccess ||
-      cudaFuncSetAttribute(state_pass_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      cudaFuncSetAttribute(state_pass_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)kPassSmem) != cudaSuccess ||
-      cudaFuncSetAttribute(state_pass_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      cudaFuncSetAttribute(state_pass_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)kPassSmem) != cudaSuccess ||
+      cudaFuncSetAttribute(state_pass_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)kPassSmem) != cudaSuccess ||
+      cudaFuncSetAttribute(state_pass_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)kPassSmem) != cudaSuccess ||
       cudaDeviceGetAttribute(&g_num_sms[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return KDA_ERR_CUDA;
@@ -1823,8 +1872,6 @@ extern "C" kda_status kda_prefill(kda_dims dims, kda_gate gate, const kda_bf16* 
   // the kernels for this call's 16-bit element type
   void (*const transform_kernel)(PrefillArgs, RowMaps) =
       dims.dtype == KDA_DTYPE_F16 ? chunk_transform_tc_kernel<true> : chunk_transform_tc_kernel<false>;
-  void (*const pass_kernel)(PrefillArgs) =
-      dims.dtype == KDA_DTYPE_F16 ? state_pass_kernel<true> : state_pass_kernel<false>;
   record_stage(0, st);
   if (!gate.A_log && total_tokens > 0) {
     // given log-decays: flag the sequences the chunk form cannot take
@@ -1853,7 +1900,15 @@ extern "C" kda_status kda_prefill(kda_dims dims, kda_gate gate, const kda_bf16* 
     transform_kernel<<<transform_grid(args.tx_units, dev), kTxThreads, kTransformTcSmem, st>>>(args, maps);
     if ((s = launch_status()) != KDA_OK) return s;
   }
-  const dim3 grid(kSlices * parts, dims.HV, num_seqs);
+  // one CTA per (sequence, head, slice, part) item where they fit the SMs,
+  // else as many CTAs as SMs, each looping over items
+  args.parts = parts;
+  const int64_t items = (int64_t)kSlices * parts * dims.HV * num_seqs;
+  const bool multi = items > g_num_sms[dev];
+  const dim3 grid((unsigned)(multi ? g_num_sms[dev] : (items > 0 ? items : 1)));
+  const bool f16 = dims.dtype == KDA_DTYPE_F16;
+  void (*const pass_kernel)(PrefillArgs) = multi ? (f16 ? state_pass_kernel<true, true> : state_pass_kernel<false, true>)
+                                                 : (f16 ? state_pass_kernel<true, false> : state_pass_kernel<false, false>);
   if (g_stage_events[1]) {  // a stage event between the kernels: an ordinary launch
     record_stage(1, st);
     pass_kernel<<<grid, kPassThreads, kPassSmem, st>>>(args);

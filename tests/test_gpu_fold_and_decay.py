@@ -174,6 +174,21 @@ def test_prefill_full_size_slow_decay(T, mode):
     _check_prefill(_prefill(d, 16, og, gg, intermediate=(T == 4096)), d)
 
 
+def test_prefill_many_sequences_slow_decay():
+    """40 sequences of 60-330 tokens at 4 heads with given log-decays in
+    [-0.02, 0]: every chain product runs, and with 640 (sequence, head,
+    slice) items against the SMs each state-pass CTA runs several of them,
+    so its copy rings, state buffers and barrier phases carry on from one
+    item to the next through the chain products."""
+    rng = np.random.default_rng(420)
+    lens = [int(x) for x in rng.integers(60, 331, size=40)]
+    T = sum(lens)
+    d = inputs.prefill_inputs(seed=421, lengths=lens, H=4, slots=48, gb_rows=T + 9)
+    d["g"][:T] = inputs.encode16(-0.02 * rng.random(d["g"][:T].shape))
+    og, gg = gates(d, H=4, given_decay=True)
+    _check_prefill(_prefill(d, 4, og, gg), d)
+
+
 # --- the prefill's decay range -------------------------------------------------
 
 def test_given_decay_outside_the_prefill_range_is_flagged_and_skipped():
