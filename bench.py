@@ -59,10 +59,10 @@ LAYERS = 8  # default decode/verify/commit calls per timed replay (--layers)
 # value (the figure is re-taken whenever they change; see the transform's ncu
 # traffic summary under profiles/).
 NCU_TRAFFIC = {
-    # the transform launch of one 1x4096 prefill call, 16 heads: read
-    # 68,417,280 B (its inputs) + write 85,145,856 B (the part of its per-chunk
-    # records that leaves L2 before the state pass reads it)
-    "prefill_transform": {"bytes": 153563136, "src": "d7280e8a4bf13b4b"},
+    # the transform launch of one 1x4096 prefill call, 16 heads, mean of two
+    # captured launches: read 68.47 MB (its inputs) + write 83.28 MB (the part
+    # of its per-chunk records that leaves L2 before the state pass reads it)
+    "prefill_transform": {"bytes": 151749504, "src": "186f04f11d42fd43"},
 }
 VERIFY_SWEEP = (1, 2, 4, 8, 12, 16, 24, 32, 48)  # requests x 6 draft tokens, chain and tree
 DECODE_SWEEP = (1, 16)  # besides the core step's 48
