@@ -94,11 +94,11 @@ struct FoldSmem {
 };
 
 // CTAs per SM the register allocation must allow: 7 (72 registers) lets the
-// 1024 CTAs of a 16-request chain verify run as one wave; tree verify would
-// spill there and gets 5.  Tree verify with four row groups (64-row CTAs,
-// up to 128 registers) runs 4 per SM.
+// 1024 CTAs of a 16-request verify run as one wave (tree verify fits there
+// with its row groups stepped together).  Tree verify with four row groups
+// (64-row CTAs, up to 128 registers) runs 4 per SM.
 template <int MODE, int GROUPS>
-constexpr int kMinCtasPerSm = GROUPS == 4 ? 4 : MODE == kTree ? 5 : 7;
+constexpr int kMinCtasPerSm = GROUPS == 4 ? 4 : 7;
 
 template <int MODE, int GROUPS, bool F16>
 __global__ void __launch_bounds__(128, (kMinCtasPerSm<MODE, GROUPS>)) recurrent_kernel(const StepArgs args) {
@@ -327,32 +327,81 @@ __global__ void __launch_bounds__(128, (kMinCtasPerSm<MODE, GROUPS>)) recurrent_
       float* snap = MODE == kChain || MODE == kTree
                         ? args.snapshots + (((size_t)r * T + t) * HV + h) * head_elems
                         : nullptr;
+      if constexpr (MODE == kTree) {
+        // X = Diag(exp g) S;  u = beta (v - X^T k);  S = X + k u^T;  o = scale S^T q.
+        // The row groups go through each step together, so that one group's
+        // dot, shuffle and update latencies overlap the others'.
+        float pk[GROUPS], po[GROUPS];
 #pragma unroll
-      for (int gi = 0; gi < GROUPS; ++gi) {
-        // X = Diag(exp g) S;  u = beta (v - X^T k);  S = X + k u^T;  o = scale S^T q
+        for (int gi = 0; gi < GROUPS; ++gi) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float2 lo = mul2(make_float2(S[gi][i].x, S[gi][i].y), make_float2(dec[i].x, dec[i].y));
-          const float2 hi = mul2(make_float2(S[gi][i].z, S[gi][i].w), make_float2(dec[i].z, dec[i].w));
-          S[gi][i] = make_float4(lo.x, lo.y, hi.x, hi.y);
+          for (int i = 0; i < 4; ++i) {
+            const float2 lo = mul2(make_float2(S[gi][i].x, S[gi][i].y), make_float2(dec[i].x, dec[i].y));
+            const float2 hi = mul2(make_float2(S[gi][i].z, S[gi][i].w), make_float2(dec[i].z, dec[i].w));
+            S[gi][i] = make_float4(lo.x, lo.y, hi.x, hi.y);
+          }
+          pk[gi] = dot16(S[gi], k);
         }
-        const int j = row0 + gi * 4;
-        const float uu = beta * (fs.v[u][j] - group_sum8(dot16(S[gi], k)));
-        const float2 u2 = make_float2(uu, uu);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float2 lo = fma2(make_float2(k[i].x, k[i].y), u2, make_float2(S[gi][i].x, S[gi][i].y));
-          const float2 hi = fma2(make_float2(k[i].z, k[i].w), u2, make_float2(S[gi][i].z, S[gi][i].w));
-          S[gi][i] = make_float4(lo.x, lo.y, hi.x, hi.y);
+        for (int m = 1; m < 8; m <<= 1)  // the 8-lane row group's sums, as group_sum8
+#pragma unroll
+          for (int gi = 0; gi < GROUPS; ++gi) pk[gi] += __shfl_xor_sync(0xffffffffu, pk[gi], m);
+#pragma unroll
+        for (int gi = 0; gi < GROUPS; ++gi) {
+          const float uu = beta * (fs.v[u][row0 + gi * 4] - pk[gi]);
+          const float2 u2 = make_float2(uu, uu);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float2 lo = fma2(make_float2(k[i].x, k[i].y), u2, make_float2(S[gi][i].x, S[gi][i].y));
+            const float2 hi = fma2(make_float2(k[i].z, k[i].w), u2, make_float2(S[gi][i].z, S[gi][i].w));
+            S[gi][i] = make_float4(lo.x, lo.y, hi.x, hi.y);
+          }
+          if (MODE != kCommitReplay) po[gi] = dot16(S[gi], q);
         }
         if (MODE == kCommitReplay) continue;  // the state is written once, after the last token
-        const float out = ga.scale * group_sum8(dot16(S[gi], q));
-        if (sub == 0) args.o[(row * HV + h) * V + j] = parents_ok ? float_to_out16<F16>(out) : 0;
-        if (MODE == kChainReplay) continue;  // no snapshots
-        if (MODE != kTree || parents_ok) {
-          float* dst = MODE == kDecode ? root + (size_t)j * K : snap + (size_t)j * K;
 #pragma unroll
-          for (int i = 0; i < 4; ++i) *reinterpret_cast<float4*>(dst + i * 32 + lane_col) = S[gi][i];
+        for (int m = 1; m < 8; m <<= 1)
+#pragma unroll
+          for (int gi = 0; gi < GROUPS; ++gi) po[gi] += __shfl_xor_sync(0xffffffffu, po[gi], m);
+#pragma unroll
+        for (int gi = 0; gi < GROUPS; ++gi) {
+          const int j = row0 + gi * 4;
+          const float out = ga.scale * po[gi];
+          if (sub == 0) args.o[(row * HV + h) * V + j] = parents_ok ? float_to_out16<F16>(out) : 0;
+          if (MODE != kChainReplay && (MODE != kTree || parents_ok)) {  // ReplaySSM verify keeps no snapshots
+            float* dst = MODE == kDecode ? root + (size_t)j * K : snap + (size_t)j * K;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) *reinterpret_cast<float4*>(dst + i * 32 + lane_col) = S[gi][i];
+          }
+        }
+      } else {
+#pragma unroll
+        for (int gi = 0; gi < GROUPS; ++gi) {
+          // X = Diag(exp g) S;  u = beta (v - X^T k);  S = X + k u^T;  o = scale S^T q
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float2 lo = mul2(make_float2(S[gi][i].x, S[gi][i].y), make_float2(dec[i].x, dec[i].y));
+            const float2 hi = mul2(make_float2(S[gi][i].z, S[gi][i].w), make_float2(dec[i].z, dec[i].w));
+            S[gi][i] = make_float4(lo.x, lo.y, hi.x, hi.y);
+          }
+          const int j = row0 + gi * 4;
+          const float uu = beta * (fs.v[u][j] - group_sum8(dot16(S[gi], k)));
+          const float2 u2 = make_float2(uu, uu);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float2 lo = fma2(make_float2(k[i].x, k[i].y), u2, make_float2(S[gi][i].x, S[gi][i].y));
+            const float2 hi = fma2(make_float2(k[i].z, k[i].w), u2, make_float2(S[gi][i].z, S[gi][i].w));
+            S[gi][i] = make_float4(lo.x, lo.y, hi.x, hi.y);
+          }
+          if (MODE == kCommitReplay) continue;  // the state is written once, after the last token
+          const float out = ga.scale * group_sum8(dot16(S[gi], q));
+          if (sub == 0) args.o[(row * HV + h) * V + j] = parents_ok ? float_to_out16<F16>(out) : 0;
+          if (MODE == kChainReplay) continue;  // no snapshots
+          if (MODE != kTree || parents_ok) {
+            float* dst = MODE == kDecode ? root + (size_t)j * K : snap + (size_t)j * K;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) *reinterpret_cast<float4*>(dst + i * 32 + lane_col) = S[gi][i];
+          }
         }
       }
     }
