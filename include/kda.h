@@ -171,9 +171,12 @@ size_t kda_prefill_workspace_size(kda_dims dims, int num_seqs, int64_t total_tok
  * a chunk whose chain product is certainly left out (its map is zero, or too
  * small for the bounded state to matter), which it finds within 32 chunks
  * or else starts from the sequence's first chunk.  Results are bit for bit
- * those of a single CTA per slice.  The pass is a programmatic dependent
- * launch of the transform: its CTAs may start on SMs the transform has left
- * and wait for the transform before reading its records.
+ * those of a single CTA per slice.  With more (sequence, head, slice) chains
+ * than SMs, the pass runs one CTA per SM, each looping over chains.  The
+ * pass is a programmatic dependent launch of the transform: its CTAs may
+ * start on SMs the transform has left and wait for the transform before
+ * reading its records.  The transform reads the token rows by TMA, through
+ * tensor maps encoded on the host for each call.
  */
 kda_status kda_prefill(kda_dims dims, kda_gate gate, const kda_bf16 *q, const kda_bf16 *k,
                        const kda_bf16 *v, const kda_bf16 *g, const kda_bf16 *beta,
