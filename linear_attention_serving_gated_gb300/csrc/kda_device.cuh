@@ -124,14 +124,6 @@ __device__ __forceinline__ void cp_async16(void* dst_smem, const void* src) {
                "l"(src)
                : "memory");
 }
-// As cp_async16, reading src_bytes (0 or 16) bytes and zero-filling the rest:
-// with 0 nothing is read from src.
-__device__ __forceinline__ void cp_async16_zfill(void* dst_smem, const void* src, uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
-                   static_cast<uint32_t>(__cvta_generic_to_shared(dst_smem))),
-               "l"(src), "r"(src_bytes)
-               : "memory");
-}
 __device__ __forceinline__ void cp_async4(void* dst_smem, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(
                    static_cast<uint32_t>(__cvta_generic_to_shared(dst_smem))),

@@ -269,14 +269,5 @@ __device__ __forceinline__ void st_tf32x4(uint8_t* tile, int row, int col, int r
       make_uint4(tf32_rna(x.x), tf32_rna(x.y), tf32_rna(x.z), tf32_rna(x.w));
 }
 
-// Eight consecutive values of row `row`, columns [col, col+8) (col a multiple
-// of 8), rounded to TF32 into a swizzled K-major 32-bit tile of `rows` rows.
-__device__ __forceinline__ void st_tf32x8(uint8_t* tile, int row, int col, int rows, const float* x) {
-  *reinterpret_cast<uint4*>(tile + sw128_offset_f32(row, col, rows)) =
-      make_uint4(tf32_rna(x[0]), tf32_rna(x[1]), tf32_rna(x[2]), tf32_rna(x[3]));
-  *reinterpret_cast<uint4*>(tile + sw128_offset_f32(row, col + 4, rows)) =
-      make_uint4(tf32_rna(x[4]), tf32_rna(x[5]), tf32_rna(x[6]), tf32_rna(x[7]));
-}
-
 }  // namespace tc
 }  // namespace kda
