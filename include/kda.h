@@ -82,9 +82,6 @@ typedef enum {
                                       records than the call's sequences have
                                       chunks; the states past its end were not
                                       written */
-#define KDA_DEVERR_DECAY 64   /* prefill with given log-decays (A_log NULL): a
-                                 value outside [-5.5, 0] or NaN; its sequence
-                                 was skipped (pool slot and o rows untouched) */
 
 /* element type of the token tensors (q, k, v, g, beta, mixed_qkv, a, b) and
  * of the output o: the "two precisions" of the pages' prefill sweep
@@ -132,13 +129,15 @@ size_t kda_prefill_workspace_size(kda_dims dims, int num_seqs, int64_t total_tok
  *   q, k          [total_tokens, H, K]    BF16
  *   v             [total_tokens, HV, V]   BF16
  *   g             [gb_rows, HV, K] BF16: gate input a (A_log given) or log-decay.
- *                 The chunk form needs per-token log-decays in [-5.5, 0]: a
- *                 bounded gate with lower_bound < -5.5 returns
- *                 KDA_ERR_UNSUPPORTED (the pages' gate uses -5).  Given
- *                 log-decays (A_log NULL) are checked on the device: a sequence
- *                 with any value outside [-5.5, 0] (or NaN) sets
- *                 KDA_DEVERR_DECAY and is skipped, its pool slot and o rows
- *                 left untouched.  Decode and verify take any log-decay.
+ *                 The chunk form needs per-token log-decays in [-5.5, 0].  A
+ *                 bounded gate with lower_bound < -5.5 (the pages' gate uses
+ *                 -5) runs every sequence token by token instead (one
+ *                 recurrent step per token, like decode; same outputs, far
+ *                 slower for long sequences).  Given log-decays (A_log NULL)
+ *                 are checked on the device: a sequence with any value
+ *                 outside [-5.5, 0] (or NaN) is left out of the chunk form
+ *                 and computed token by token after it.  Decode and verify
+ *                 take any log-decay.
  *   beta          [gb_rows, HV]    BF16: raw beta (beta_is_raw) or beta
  *   gb_rows       >= total_tokens (else KDA_ERR_SHAPE).  Rows past
  *                 total_tokens are CUDA-graph bucket padding and never read.

@@ -50,4 +50,29 @@ inline kda_status launch_status() {
 // stream if one is set.
 void record_stage(int i, cudaStream_t st);
 
+// The prefill's token-by-token path, for sequences whose log-decays the
+// chunk form's decay windows cannot take: one step per token like decode, the
+// state in registers, o and chunk-start states written per token and chunk,
+// the final state once.  seq_flags non-null: only the flagged sequences run.
+// chunk_base: device scratch of num_seqs int64 (written when intermediate is
+// set), stream-ordered after every earlier use of that memory.
+struct SeqPrefillArgs {
+  kda_dims dims;
+  GateArgs gate;
+  const kda_bf16 *q, *k, *v, *g, *beta;
+  float* pool;
+  int pool_slots;
+  const int32_t* state_idx;
+  const int32_t* cu_seqlens;
+  int num_seqs;
+  int64_t total_tokens;
+  const int32_t* seq_flags;
+  kda_bf16* o;
+  float* intermediate;
+  int64_t inter_chunks;
+  int64_t* chunk_base;
+  int32_t* err_flag;
+};
+kda_status launch_seq_prefill(const SeqPrefillArgs& p, cudaStream_t stream);
+
 }  // namespace kda

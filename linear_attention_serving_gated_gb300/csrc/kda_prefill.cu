@@ -1683,7 +1683,7 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
 // every per-token log-decay in [kMinLogDecay, 0].  Each thread checks eight
 // consecutive values of the real token rows (padding rows are never read); a
 // value outside the range, or NaN, flags its sequence, which the transform and
-// the state pass then skip, so that its pool slot is left as it was.
+// the state pass then skip and the token-by-token path computes.
 template <bool F16>
 __global__ void __launch_bounds__(256) decay_check_kernel(const PrefillArgs a, int32_t* flags) {
   const int64_t words_per_row = (int64_t)a.HV * kHeadDim / 8;
@@ -1714,7 +1714,6 @@ __global__ void __launch_bounds__(256) decay_check_kernel(const PrefillArgs a, i
         n = (int)(row / (a.total_tokens / a.num_seqs));
       }
       flags[n] = 1;
-      set_error(a.err_flag, KDA_DEVERR_DECAY);
     }
   }
 }
@@ -1835,8 +1834,9 @@ extern "C" kda_status kda_prefill(kda_dims dims, kda_gate gate, const kda_bf16* 
   s = check_gate(gate, &args.gate);
   if (s != KDA_OK) return s;
   // The chunk transform's decay-factor windows stay inside FP32 range for
-  // per-token log-decays >= kMinLogDecay; a bounded gate below it is refused.
-  if (gate.A_log && gate.lower_bound < kMinLogDecay) return KDA_ERR_UNSUPPORTED;
+  // per-token log-decays >= kMinLogDecay; a bounded gate that may go below it
+  // takes the token-by-token path for every sequence.
+  const bool token_path = gate.A_log && gate.lower_bound < kMinLogDecay;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(state_pool) ||
       !aligned16(o) || (intermediate && !aligned16(intermediate)))
     return KDA_ERR_ALIGNMENT;
@@ -1867,6 +1867,32 @@ extern "C" kda_status kda_prefill(kda_dims dims, kda_gate gate, const kda_bf16* 
   // made with that device current.
   int dev = 0;
   if ((s = ensure_kernel_attributes(&dev)) != KDA_OK) return s;
+  SeqPrefillArgs sp{};  // the token-by-token path's arguments
+  sp.dims = dims;
+  sp.gate = args.gate;
+  sp.q = q;
+  sp.k = k;
+  sp.v = v;
+  sp.g = g;
+  sp.beta = beta;
+  sp.pool = state_pool;
+  sp.pool_slots = pool_slots;
+  sp.state_idx = state_idx;
+  sp.cu_seqlens = cu_seqlens;
+  sp.num_seqs = num_seqs;
+  sp.total_tokens = total_tokens;
+  sp.o = o;
+  sp.intermediate = intermediate;
+  sp.inter_chunks = args.inter_chunks;
+  sp.chunk_base = reinterpret_cast<int64_t*>(args.ws);  // the records' space, unused by then
+  sp.err_flag = err_flag;
+  if (token_path) {
+    record_stage(0, st);
+    s = launch_seq_prefill(sp, st);
+    record_stage(1, st);
+    record_stage(2, st);
+    return s;
+  }
   const int64_t chunks = max_chunks(num_seqs, total_tokens);
   uint8_t* const ws_states = args.ws + (size_t)chunks * dims.HV * kRecBytes;
   // the kernels for this call's 16-bit element type
@@ -1925,6 +1951,10 @@ extern "C" kda_status kda_prefill(kda_dims dims, kda_gate gate, const kda_bf16* 
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     s = cudaLaunchKernelEx(&cfg, pass_kernel, args) == cudaSuccess ? launch_status() : KDA_ERR_CUDA;
+  }
+  if (s == KDA_OK && args.seq_flags) {  // given log-decays: the flagged sequences, token by token
+    sp.seq_flags = args.seq_flags;
+    s = launch_seq_prefill(sp, st);
   }
   record_stage(2, st);
   return s;

@@ -35,8 +35,11 @@ namespace {
 
 // kChainReplay: chain verify that keeps no snapshots; instead each draft
 // token's folded inputs go to a per-request ring.  kCommitReplay: replays the
-// accepted prefix from that ring onto the pool state.
-enum Mode { kDecode = 0, kChain = 1, kTree = 2, kChainReplay = 3, kCommitReplay = 4 };
+// accepted prefix from that ring onto the pool state.  kSeqPrefill: a
+// prefill's sequences token by token (o, chunk-start states, final state),
+// for log-decays the chunk form's decay windows cannot take.
+enum Mode { kDecode = 0, kChain = 1, kTree = 2, kChainReplay = 3, kCommitReplay = 4, kSeqPrefill = 5 };
+constexpr int kSeqChunk = 64;  // the prefill's chunk length (chunk-start states)
 
 // Ring record of one (request, token, head): k-hat [128], exp(g) [128],
 // v [128], beta, padding -- FP32, 16-byte aligned.
@@ -61,7 +64,22 @@ struct StepArgs {
   float* ring;                // replay modes
   const int32_t* accepted;    // kCommitReplay
   int32_t* err_flag;
+  // kSeqPrefill: q, k [T][H][K] and v [T][HV][V] (the gate input is a, beta
+  // is b), sequence bounds, which sequences run, chunk-start states
+  const kda_bf16 *sq, *sk, *sv;
+  const int32_t* cu_seqlens;
+  int num_seqs;
+  int64_t total_tokens;
+  const int32_t* seq_flags;  // non-null: only flagged sequences run
+  float* intermediate;
+  int64_t inter_chunks;
+  const int64_t* chunk_base;  // [num_seqs] chunk id of each sequence's first chunk
+  int seq0;                   // sequence of blockIdx.z == 0 (launches of at most 65535)
 };
+
+__device__ __forceinline__ int64_t seq_start(const StepArgs& a, int n) {
+  return a.cu_seqlens ? (int64_t)a.cu_seqlens[n] : a.total_tokens / a.num_seqs * n;
+}
 
 __device__ __forceinline__ float group_sum8(float x) {
   x += __shfl_xor_sync(0xffffffffu, x, 1);
@@ -96,9 +114,10 @@ struct FoldSmem {
 // CTAs per SM the register allocation must allow: 7 (72 registers) lets the
 // 1024 CTAs of a 16-request verify run as one wave (tree verify fits there
 // with its row groups stepped together).  Tree verify with four row groups
-// (64-row CTAs, up to 128 registers) runs 4 per SM.
+// (64-row CTAs, up to 128 registers) runs 4 per SM, and so does the
+// prefill's token-by-token path, which would spill at 72.
 template <int MODE, int GROUPS>
-constexpr int kMinCtasPerSm = GROUPS == 4 ? 4 : 7;
+constexpr int kMinCtasPerSm = GROUPS == 4 || MODE == kSeqPrefill ? 4 : 7;
 
 template <int MODE, int GROUPS, bool F16>
 __global__ void __launch_bounds__(128, (kMinCtasPerSm<MODE, GROUPS>)) recurrent_kernel(const StepArgs args) {
@@ -107,7 +126,7 @@ __global__ void __launch_bounds__(128, (kMinCtasPerSm<MODE, GROUPS>)) recurrent_
   __shared__ int tree_par[kTokBlock];  // tree: the parents of the first kTokBlock nodes
   // raw BF16 token rows of this head: q, k, v, gate input, per token of the block
   __shared__ __align__(16) uint16_t raw_s[kTokBlock][4][kHeadDim];
-  const int r = blockIdx.z, h = blockIdx.y;
+  const int r = blockIdx.z + (MODE == kSeqPrefill ? args.seq0 : 0), h = blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int sub = lane & 7;
   const int row0 = blockIdx.x * (16 * GROUPS) + warp * (4 * GROUPS) + (lane >> 3);
@@ -137,7 +156,26 @@ __global__ void __launch_bounds__(128, (kMinCtasPerSm<MODE, GROUPS>)) recurrent_
       return;  // acc < 0: nothing accepted, the pool keeps its state
     }
   }
-  const int T = MODE == kDecode ? 1 : MODE == kCommitReplay ? acc + 1 : args.T;
+  // kSeqPrefill: request r is sequence r, its tokens [sp_t0, sp_t0 + T)
+  int64_t sp_t0 = 0, sp_cbase = 0;
+  int sp_T = 0;
+  if constexpr (MODE == kSeqPrefill) {
+    if (args.seq_flags && !args.seq_flags[r]) return;  // this sequence took the chunk form
+    sp_t0 = seq_start(args, r);
+    const int64_t sp_t1 = seq_start(args, r + 1);
+    if (sp_t0 < 0 || sp_t1 < sp_t0 || sp_t1 > args.total_tokens) {  // no access outside the token rows
+      if (reporter) set_error(args.err_flag, KDA_DEVERR_SEQLENS);
+      return;
+    }
+    sp_T = (int)(sp_t1 - sp_t0);
+    if (sp_T == 0) return;  // keeps its state
+    if (args.intermediate) sp_cbase = args.chunk_base[r];
+  }
+  const int T = MODE == kDecode ? 1 : MODE == kCommitReplay ? acc + 1 : MODE == kSeqPrefill ? sp_T : args.T;
+  // the o row of token t
+  auto out_row = [&](int t) -> int64_t {
+    return MODE == kDecode ? r : MODE == kSeqPrefill ? sp_t0 + t : (int64_t)r * T + t;
+  };
 
   // Raw token rows of a block, copied 16 bytes at a time into raw_s.  The
   // first block's copies are issued before anything that waits on memory,
@@ -148,6 +186,7 @@ __global__ void __launch_bounds__(128, (kMinCtasPerSm<MODE, GROUPS>)) recurrent_
   // h / G.
   const int raw_m = (tid >> 4) & 3, raw_piece = (tid & 15) * 8;
   const int raw_off = MODE == kCommitReplay ? 0  // reads no token rows
+                    : MODE == kSeqPrefill ? raw_piece + (raw_m < 2 ? h / args.G : h) * kHeadDim  // separate tensors
                     : raw_piece + (raw_m == 0 ? (h / args.G) * kHeadDim
                                  : raw_m == 1 ? (args.H + h / args.G) * kHeadDim
                                  : raw_m == 2 ? (2 * args.H + h) * kHeadDim
@@ -155,14 +194,20 @@ __global__ void __launch_bounds__(128, (kMinCtasPerSm<MODE, GROUPS>)) recurrent_
   uint16_t b_raw = 0;  // thread u < nt: raw beta of token u of the block
   auto request_raw = [&](int tb, int nt) {
     for (int u = tid >> 6; u < nt; u += 2) {
-      const int64_t row = MODE == kDecode ? r : (int64_t)r * T + tb + u;
-      const kda_bf16* x = raw_m < 3 ? args.mixed_qkv + row * args.row_stride
-                                    : args.a + row * ((int64_t)args.HV * kHeadDim);
+      const int64_t row = out_row(tb + u);
+      const kda_bf16* x;
+      if constexpr (MODE == kSeqPrefill)
+        x = raw_m == 0 ? args.sq + row * ((int64_t)args.H * kHeadDim)
+          : raw_m == 1 ? args.sk + row * ((int64_t)args.H * kHeadDim)
+          : raw_m == 2 ? args.sv + row * ((int64_t)args.HV * kHeadDim)
+                       : args.a + row * ((int64_t)args.HV * kHeadDim);
+      else
+        x = raw_m < 3 ? args.mixed_qkv + row * args.row_stride : args.a + row * ((int64_t)args.HV * kHeadDim);
       cp_async16(&raw_s[u][raw_m][raw_piece], x + raw_off);
     }
     cp_async_commit();
     if (tid < nt) {  // kept in a register: its latency overlaps the slot lookup and state load
-      const int64_t row = MODE == kDecode ? r : (int64_t)r * T + tb + tid;
+      const int64_t row = out_row(tb + tid);
       b_raw = args.b[row * args.HV + h];
     }
   };
@@ -206,7 +251,7 @@ __global__ void __launch_bounds__(128, (kMinCtasPerSm<MODE, GROUPS>)) recurrent_
       for (int i = 0; i < T; ++i)
 #pragma unroll
         for (int gi = 0; gi < GROUPS; ++gi)
-          args.o[(((int64_t)r * T + i) * HV + h) * V + row0 + gi * 4] = 0;
+          args.o[(out_row(i) * HV + h) * V + row0 + gi * 4] = 0;
     return;
   }
 
@@ -315,7 +360,22 @@ __global__ void __launch_bounds__(128, (kMinCtasPerSm<MODE, GROUPS>)) recurrent_
                                                           i * 32 + lane_col);
         }
       }
-      const int64_t row = MODE == kDecode ? r : (int64_t)r * T + t;
+      const int64_t row = out_row(t);
+      if constexpr (MODE == kSeqPrefill) {  // the state at the start of each chunk
+        if (args.intermediate && t % kSeqChunk == 0) {
+          const int64_t cid = sp_cbase + t / kSeqChunk;
+          if (cid >= 0 && cid < args.inter_chunks) {
+            float* dst = args.intermediate + (size_t)(cid * HV + h) * head_elems;
+#pragma unroll
+            for (int gi = 0; gi < GROUPS; ++gi)
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                *reinterpret_cast<float4*>(dst + (size_t)(row0 + gi * 4) * K + i * 32 + lane_col) = S[gi][i];
+          } else if (reporter) {
+            set_error(args.err_flag, KDA_DEVERR_INTERMEDIATE);
+          }
+        }
+      }
       float4 q[4], k[4], dec[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
@@ -396,7 +456,7 @@ __global__ void __launch_bounds__(128, (kMinCtasPerSm<MODE, GROUPS>)) recurrent_
           if (MODE == kCommitReplay) continue;  // the state is written once, after the last token
           const float out = ga.scale * group_sum8(dot16(S[gi], q));
           if (sub == 0) args.o[(row * HV + h) * V + j] = parents_ok ? float_to_out16<F16>(out) : 0;
-          if (MODE == kChainReplay) continue;  // no snapshots
+          if (MODE == kChainReplay || MODE == kSeqPrefill) continue;  // no snapshots
           if (MODE != kTree || parents_ok) {
             float* dst = MODE == kDecode ? root + (size_t)j * K : snap + (size_t)j * K;
 #pragma unroll
@@ -407,7 +467,7 @@ __global__ void __launch_bounds__(128, (kMinCtasPerSm<MODE, GROUPS>)) recurrent_
     }
     if (tb + kTokBlock < T) __syncthreads();  // fold buffer reused by the next block
   }
-  if (MODE == kCommitReplay) {
+  if (MODE == kCommitReplay || MODE == kSeqPrefill) {  // the final state, once
 #pragma unroll
     for (int gi = 0; gi < GROUPS; ++gi)
 #pragma unroll
@@ -470,7 +530,7 @@ int sm_count() {
 }
 
 template <int MODE>
-kda_status launch_recurrent(const StepArgs& a, cudaStream_t stream) {
+kda_status launch_recurrent(const StepArgs& a, cudaStream_t stream, bool stages = true) {
   // Small batches use 16-row CTAs so that even one request spreads over 128
   // CTAs; larger batches use 32-row CTAs to halve the per-CTA fold work.
   // Tree verify takes 64-row CTAs where their grid fits in one wave and the
@@ -479,7 +539,7 @@ kda_status launch_recurrent(const StepArgs& a, cudaStream_t stream) {
   const int64_t units = (int64_t)a.B * a.HV;
   const int sms = sm_count();
   if (sms <= 0) return KDA_ERR_CUDA;
-  record_stage(0, stream);
+  if (stages) record_stage(0, stream);
   const bool f16 = a.dtype == KDA_DTYPE_F16;
   if (units * 8 <= 2 * (int64_t)sms) {
     dim3 grid(kHeadDim / 16, a.HV, a.B);
@@ -495,8 +555,10 @@ kda_status launch_recurrent(const StepArgs& a, cudaStream_t stream) {
     (f16 ? recurrent_kernel<MODE, 2, true> : recurrent_kernel<MODE, 2, false>)<<<grid, 128, 0, stream>>>(a);
   }
   const kda_status s = launch_status();
-  record_stage(1, stream);
-  record_stage(2, stream);
+  if (stages) {
+    record_stage(1, stream);
+    record_stage(2, stream);
+  }
   return s;
 }
 
@@ -529,7 +591,88 @@ kda_status check_packed(const kda_dims& dims, const kda_gate& gate, const kda_bf
   return KDA_OK;
 }
 
+// The chunk id of each sequence's first chunk: the exclusive prefix sum of
+// the per-sequence chunk counts, 1024 sequences per round with the running
+// total carried.  One CTA; empty or malformed sequences count 0 chunks (the
+// token path checks their bounds itself).
+__global__ void __launch_bounds__(1024) seq_chunk_base_kernel(const StepArgs a, int64_t* base) {
+  __shared__ int64_t warp_total[32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int64_t carry = 0;
+  for (int n0 = 0; n0 < a.num_seqs; n0 += 1024) {
+    const int n = n0 + tid;
+    int64_t c = 0;
+    if (n < a.num_seqs) {
+      const int64_t L = seq_start(a, n + 1) - seq_start(a, n);
+      c = L > 0 ? (L + kSeqChunk - 1) / kSeqChunk : 0;
+    }
+    int64_t x = c;  // inclusive scan within the warp
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int64_t y = __shfl_up_sync(0xffffffffu, x, d);
+      if (lane >= d) x += y;
+    }
+    if (lane == 31) warp_total[warp] = x;
+    __syncthreads();
+    if (warp == 0) {  // inclusive scan of the warp totals
+      int64_t w = warp_total[lane];
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int64_t y = __shfl_up_sync(0xffffffffu, w, d);
+        if (lane >= d) w += y;
+      }
+      warp_total[lane] = w;
+    }
+    __syncthreads();
+    if (n < a.num_seqs) base[n] = carry + (warp ? warp_total[warp - 1] : 0) + x - c;
+    carry += warp_total[31];
+    __syncthreads();  // warp_total is rewritten by the next round
+  }
+}
+
 }  // namespace
+
+// The prefill's token-by-token path (see kSeqPrefill).
+kda_status launch_seq_prefill(const SeqPrefillArgs& p, cudaStream_t stream) {
+  if (p.num_seqs <= 0 || p.total_tokens <= 0) return KDA_OK;
+  StepArgs a{};
+  a.gate = p.gate;
+  a.H = p.dims.H;
+  a.HV = p.dims.HV;
+  a.G = p.dims.HV / p.dims.H;
+  a.dtype = p.dims.dtype;
+  a.sq = p.q;
+  a.sk = p.k;
+  a.sv = p.v;
+  a.a = p.g;
+  a.b = p.beta;
+  a.B = p.num_seqs;
+  a.pool = p.pool;
+  a.pool_slots = p.pool_slots;
+  a.state_idx = p.state_idx;
+  a.o = p.o;
+  a.err_flag = p.err_flag;
+  a.cu_seqlens = p.cu_seqlens;
+  a.num_seqs = p.num_seqs;
+  a.total_tokens = p.total_tokens;
+  a.seq_flags = p.seq_flags;
+  a.intermediate = p.intermediate;
+  a.inter_chunks = p.inter_chunks;
+  a.chunk_base = p.chunk_base;
+  if (p.intermediate) {
+    seq_chunk_base_kernel<<<1, 1024, 0, stream>>>(a, p.chunk_base);
+    const kda_status s = launch_status();
+    if (s != KDA_OK) return s;
+  }
+  constexpr int kMaxGridZ = 65535;
+  for (int s0 = 0; s0 < p.num_seqs; s0 += kMaxGridZ) {
+    a.seq0 = s0;
+    a.B = p.num_seqs - s0 < kMaxGridZ ? p.num_seqs - s0 : kMaxGridZ;
+    const kda_status s = launch_recurrent<kSeqPrefill>(a, stream, false);
+    if (s != KDA_OK) return s;
+  }
+  return KDA_OK;
+}
 }  // namespace kda
 
 using namespace kda;

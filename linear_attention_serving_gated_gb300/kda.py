@@ -31,7 +31,6 @@ KDA_DEVERR_SEQLENS = 4
 KDA_DEVERR_ACCEPTED = 8
 KDA_DEVERR_TIMEOUT = 16
 KDA_DEVERR_INTERMEDIATE = 32
-KDA_DEVERR_DECAY = 64
 
 CHUNK = 64
 

@@ -89,8 +89,14 @@ def _check_prefill(r, d):
     others = [s for s in range(r["pool"].shape[0]) if s not in slots]
     if others:
         assert torch.equal(r["pool"][others], r["before"][others])
-    if r["inter"] is not None:
-        worst_s = max(worst_s, assert_s_close(r["inter"], r["inter_ref"], "chunk-start states"))
+    if r["inter"] is not None:  # records of padding sequences (slot -1) are not written
+        rows, base = [], 0
+        for L, slot in zip(d["lengths"], d["state_idx"]):
+            nch = (int(L) + 63) // 64
+            if slot >= 0:
+                rows.extend(range(base, base + nch))
+            base += nch
+        worst_s = max(worst_s, assert_s_close(r["inter"][rows], r["inter_ref"][rows], "chunk-start states"))
     return worst_o, worst_s
 
 
@@ -191,10 +197,11 @@ def test_prefill_many_sequences_slow_decay():
 
 # --- the prefill's decay range -------------------------------------------------
 
-def test_given_decay_outside_the_prefill_range_is_flagged_and_skipped():
-    """A_log absent: a sequence with a log-decay below -5.5 (here -8), above 0
-    or NaN is flagged with KDA_DEVERR_DECAY and skipped (its pool slot and o
-    rows untouched); the other sequences are computed as usual."""
+def test_given_decay_outside_the_chunk_range_takes_the_token_path():
+    """A_log absent: a sequence with a log-decay below -5.5 (here -8) or above
+    0 is flagged by the decay check, skipped by the chunk transform and the
+    state pass, and computed token by token instead; every sequence then
+    matches the oracle, with no error bit."""
     H, lens = 2, [70, 50, 90, 40]
     T = sum(lens)
     d = inputs.prefill_inputs(seed=310, lengths=lens, H=H, slots=6, gb_rows=T + 30)
@@ -204,32 +211,44 @@ def test_given_decay_outside_the_prefill_range_is_flagged_and_skipped():
     d["g"][120 + 89, 0, 127] = inputs.encode16(np.array([0.25]))[0]  # sequence 2 (its last row)
     d["g"][T + 3] = inputs.encode16(np.full((H, K), -50.0))           # padding row: never read
     og, gg = gates(d, H=H, given_decay=True)
-    x = {n: dev_bf16(d[n]) for n in ("q", "k", "v", "g", "beta")}
-    pool = dev(d["pool"])
-    before = pool.clone()
-    o = torch.full((T, H, K), 3.0, dtype=torch.bfloat16, device="cuda")
-    err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    kda.kda_prefill(kda.dims(H), gg, x["q"], x["k"], x["v"], x["g"], x["beta"], pool, dev(d["state_idx"]),
-                    dev(d["cu_seqlens"]), len(lens), o, err_flag=err)
-    torch.cuda.synchronize()
-    assert err.item() == kda.KDA_DEVERR_DECAY
-    slots = [int(s) for s in d["state_idx"]]
-    for n in (1, 2):
-        assert torch.equal(pool[slots[n]], before[slots[n]]), f"sequence {n} touched its slot"
-        a, b = int(d["cu_seqlens"][n]), int(d["cu_seqlens"][n + 1])
-        assert torch.all(o[a:b].float() == 3.0), f"sequence {n} wrote o"
-    # sequences 0 and 3 against the oracle run on them alone
-    for n in (0, 3):
-        a, b = int(d["cu_seqlens"][n]), int(d["cu_seqlens"][n + 1])
-        opool = d["pool"].astype(np.float64)
-        o_ref = ko.prefill(og, d["q"][a:b], d["k"][a:b], d["v"][a:b], d["g"][a:b], d["beta"][a:b], opool,
-                           d["state_idx"][n:n + 1], np.array([0, b - a], np.int32))
-        assert_o_close(o[a:b], o_ref, f"sequence {n} o")
-        assert_s_close(pool[slots[n]], opool[slots[n]], f"sequence {n} state")
-    # the same call at the range's edge (-5.5 and 0 exactly) is accepted
+    _check_prefill(_prefill(d, H, og, gg), d)
+    # the same call at the range's edge (-5.5 and 0 exactly) takes the chunk form
     d["g"][70 + 17, 1, 5] = inputs.encode16(np.array([-5.5]))[0]
     d["g"][120 + 89, 0, 127] = 0
     og, gg = gates(d, H=H, given_decay=True)
+    _check_prefill(_prefill(d, H, og, gg), d)
+
+
+def test_bounded_gate_below_the_chunk_range_takes_the_token_path():
+    """A bounded gate with lower_bound -8 (past the chunk form's -5.5): every
+    sequence runs token by token -- o, chunk-start states and final states
+    against the oracle, with a zero-length sequence (state unchanged) and a
+    padding sequence (zero outputs, no state) among them."""
+    H, lens = 2, [70, 0, 130, 1, 64, 20]
+    T = sum(lens)
+    idx = [3, 0, 5, -1, 1, 6]
+    d = inputs.prefill_inputs(seed=330, lengths=lens, H=H, slots=8, state_idx=idx, gb_rows=T + 11)
+    og, gg = gates(d, H=H, lower_bound=-8.0)
+    _check_prefill(_prefill(d, H, og, gg), d)
+
+
+def test_token_path_chunk_ids_past_1024_and_65535_sequences():
+    """The token path numbers its chunk-start records by a prefix sum of the
+    sequences' chunk counts, taken 1024 sequences at a time, and launches at
+    most 65535 sequences at a time: 66000 sequences, nearly all empty, with
+    real ones on both sides of each boundary."""
+    n, H = 66000, 2
+    lens = np.zeros(n, dtype=np.int64)
+    real = {3: 70, 1023: 5, 1024: 64, 1025: 1, 2047: 130, 65534: 65, 65535: 1, 65536: 64, 65999: 10}
+    for m, L in real.items():
+        lens[m] = L
+    idx = np.full(n, -1, dtype=np.int32)
+    for j, m in enumerate(sorted(real)):
+        idx[m] = j
+    idx[4], idx[65537] = 9, 10  # empty sequences with a slot: their states stay as they were
+    T = int(lens.sum())
+    d = inputs.prefill_inputs(seed=340, lengths=lens, H=H, slots=12, state_idx=idx, gb_rows=T + 3)
+    og, gg = gates(d, H=H, lower_bound=-8.0)
     _check_prefill(_prefill(d, H, og, gg), d)
 
 
