@@ -117,10 +117,10 @@ const char *kda_status_string(kda_status s);
 
 /* Bytes of device workspace kda_prefill needs for this call shape (an upper
  * bound over every cu_seqlens with this many sequences and tokens):
- *   align256(4 * num_seqs) + (total_tokens / 64 + num_seqs) * HV * 180352
+ *   align256(4 * num_seqs + 4) + (total_tokens / 64 + num_seqs) * HV * 180352
  *     + num_seqs * HV * 65536
- * (per-sequence flags, one record per (chunk, head), one staged start state
- * per (sequence, head)).  total_tokens above INT32_MAX (cu_seqlens are int32)
+ * (per-sequence flags and a counter, one record per (chunk, head), one
+ * staged start state per (sequence, head)).  total_tokens above INT32_MAX (cu_seqlens are int32)
  * gives SIZE_MAX. */
 size_t kda_prefill_workspace_size(kda_dims dims, int num_seqs, int64_t total_tokens);
 
@@ -171,7 +171,9 @@ size_t kda_prefill_workspace_size(kda_dims dims, int num_seqs, int64_t total_tok
  * small for the bounded state to matter), which it finds within 32 chunks
  * or else starts from the sequence's first chunk.  Results are bit for bit
  * those of a single CTA per slice.  With more (sequence, head, slice) chains
- * than SMs, the pass runs one CTA per SM, each looping over chains.  The
+ * than SMs, the pass runs one CTA per SM, each claiming the next chain from
+ * a counter in the workspace whenever it is free; there the chains run in
+ * two parts too when the sequences average 1024 tokens or more.  The
  * pass is a programmatic dependent launch of the transform: its CTAs may
  * start on SMs the transform has left and wait for the transform before
  * reading its records.  The transform reads the token rows by TMA, through
@@ -250,7 +252,7 @@ kda_status kda_commit(kda_dims dims, const float *snapshots, int B, int T,
  * until the process exits.  Calls whose workspace need
  * (kda_prefill_workspace_size) exceeds it return KDA_ERR_WORKSPACE and
  * launch nothing.  The rule is
- *   align256(4 * num_seqs) + (total_tokens / 64 + num_seqs) * HV * 180352
+ *   align256(4 * num_seqs + 4) + (total_tokens / 64 + num_seqs) * HV * 180352
  *       + num_seqs * HV * 65536 <= KDA_PREFILL_STATIC_SCRATCH_BYTES,
  * so one sequence at 16 heads takes at most 2943 tokens (46 records per
  * head); the 1 x 4096 shape at 16 heads needs 65 and is refused.

@@ -132,6 +132,7 @@ struct PrefillArgs {
   // runs each chain in parts (nullptr: the pass reads the pool).  A later
   // part writes the pool's final state, so no part may read the slot itself.
   float* init_states;
+  uint32_t* item_counter;  // the multi-item pass's claims (zeroed before the call's kernels)
 };
 
 __device__ __forceinline__ int64_t seq_begin(const PrefillArgs& a, int n) {
@@ -1112,6 +1113,10 @@ __device__ __forceinline__ void issue_copy(uint8_t* dst, const uint8_t* src, uin
 // Chunks ahead of the copies whose records are prefetched into L2.
 constexpr int kPassL2Ahead = 3;
 
+// With more pass items than SMs, chains run in two parts where the sequences
+// average this many tokens or more (shorter ones would mostly add items).
+constexpr int64_t kMultiPartTokens = 1024;
+
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(tc::smem_u32(bar)) : "memory");
 }
@@ -1152,7 +1157,7 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
   __shared__ int s_state, s_abort, s_cs, s_valid;
   // counters of single roles that run on across items (see below)
   __shared__ int s_m_issued, s_q_issued, s_m_used, s_wb_n;
-  __shared__ int64_t s_wb_base;
+  __shared__ int64_t s_wb_base, s_item;
   __shared__ float s_bnd0, s_pn[kPassEpiThreads / 32];  // run start bound; per-warp sums
 
   uint8_t* smb = smraw + ((1024u - (tc::smem_u32(smraw) & 1023u)) & 1023u);
@@ -1212,11 +1217,22 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
   // and the chunks of sequences [0, s_wb_n), s_wb_base (warp 0).
   int g0 = 0;
   int nchain = 0;
-  // Items (sequence n, head h, part, 32-column slice), slices fastest; a CTA
-  // takes every gridDim.x-th, so its sequences ascend.  One CTA per item
-  // where they fit the SMs; otherwise each CTA runs several, which saves the
-  // set-up per item for many short sequences.
-  for (int64_t item = blockIdx.x; s_valid && item < n_items; item += gridDim.x) {
+  // Items (sequence n, head h, part, 32-column slice), slices fastest.  One
+  // CTA per item where they fit the SMs; otherwise each CTA runs several,
+  // which saves the set-up per item for many short sequences: CTA b takes
+  // item b first, then claims the next unclaimed one from a counter whenever
+  // it is free, so that chains of different lengths spread over the CTAs.
+  // A CTA's claims ascend, and so do its sequences.
+  auto next_item = [&]() -> int64_t {
+    if constexpr (!kMulti) {
+      return n_items;
+    } else {
+      if (tid == 0) s_item = (int64_t)gridDim.x + atomicAdd(a.item_counter, 1u);
+      __syncthreads();  // rewritten only after the next item's barriers
+      return s_item;
+    }
+  };
+  for (int64_t item = blockIdx.x; s_valid && item < n_items; item = next_item()) {
     const int slice = (int)(item % kSlices), v0 = slice * kVs;
     const int64_t rest = item / kSlices;
     const int part = (int)(rest % parts), h = (int)(rest / parts % HV), n = (int)(rest / parts / HV);
@@ -1663,7 +1679,6 @@ __global__ void __launch_bounds__(kPassThreads, 1) state_pass_kernel(const Prefi
     __syncthreads();
     if (!s_abort && !mma_warp && !copy_warp && part == parts - 1) store_state(st);
     g0 += nrun;
-    if constexpr (!kMulti) break;
   }  // items
   if (copy_warp && lane == 0) {
     // no copy may outlive the CTA: the last two of each kind are the latest
@@ -1725,7 +1740,8 @@ int64_t max_chunks(int num_seqs, int64_t total_tokens) {
 // Workspace: the per-sequence flags of the given-decay check, then the
 // (chunk, head) records, 256-byte aligned, then one start state per
 // (sequence, head).
-size_t flags_bytes(int num_seqs) { return ((size_t)num_seqs * 4 + 255) & ~(size_t)255; }
+// per-sequence flags, then the multi-item pass's claim counter
+size_t flags_bytes(int num_seqs) { return ((size_t)num_seqs * 4 + 4 + 255) & ~(size_t)255; }
 constexpr size_t kStateBytes = (size_t)kHeadDim * kHeadDim * 4;
 
 constexpr int kMaxDevices = 64;
@@ -1899,10 +1915,26 @@ extern "C" kda_status kda_prefill(kda_dims dims, kda_gate gate, const kda_bf16* 
   void (*const transform_kernel)(PrefillArgs, RowMaps) =
       dims.dtype == KDA_DTYPE_F16 ? chunk_transform_tc_kernel<true> : chunk_transform_tc_kernel<false>;
   record_stage(0, st);
+  // Each (sequence, head, slice) chain in two parts where the grid still
+  // fits the SMs, or, with more items than SMs anyway, where the sequences
+  // average kMultiPartTokens tokens or more: the second part restarts behind
+  // an all-zero map (see the pass), which halves the chain wherever the decay
+  // is strong, and shorter items spread better over the CTAs.  The start
+  // states are then staged by the transform.
+  const int64_t items1 = (int64_t)kSlices * dims.HV * num_seqs;
+  const int parts = total_tokens > 0 && (2 * items1 <= g_num_sms[dev] ||
+                                         (items1 > g_num_sms[dev] && total_tokens >= (int64_t)num_seqs * kMultiPartTokens))
+                        ? 2 : 1;
+  // one CTA per (sequence, head, slice, part) item where they fit the SMs,
+  // else as many CTAs as SMs, each claiming items from a counter
+  const int64_t items = items1 * parts;
+  const bool multi = items > g_num_sms[dev];
+  args.item_counter = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(workspace) + (size_t)num_seqs * 4);
   if (!gate.A_log && total_tokens > 0) {
-    // given log-decays: flag the sequences the chunk form cannot take
+    // given log-decays: flag the sequences the chunk form cannot take (the
+    // claim counter, right behind the flags, is cleared with them)
     int32_t* flags = static_cast<int32_t*>(workspace);
-    if (cudaMemsetAsync(flags, 0, (size_t)num_seqs * 4, st) != cudaSuccess) return KDA_ERR_CUDA;
+    if (cudaMemsetAsync(flags, 0, (size_t)num_seqs * 4 + (multi ? 4 : 0), st) != cudaSuccess) return KDA_ERR_CUDA;
     const int64_t words = total_tokens * dims.HV * kHeadDim / 8;
     const int64_t want = (words + 255) / 256;
     const unsigned blocks = (unsigned)(want < 8LL * g_num_sms[dev] ? want : 8LL * g_num_sms[dev]);
@@ -1910,12 +1942,9 @@ extern "C" kda_status kda_prefill(kda_dims dims, kda_gate gate, const kda_bf16* 
         <<<blocks, 256, 0, st>>>(args, flags);
     if ((s = launch_status()) != KDA_OK) return s;
     args.seq_flags = flags;
+  } else if (multi && cudaMemsetAsync(args.item_counter, 0, 4, st) != cudaSuccess) {
+    return KDA_ERR_CUDA;
   }
-  // Each (sequence, head, slice) chain in two parts where the grid still
-  // fits the SMs: the second part restarts behind an all-zero map (see the
-  // pass), which halves the chain wherever the decay is strong.  The start
-  // states are then staged by the transform.
-  const int parts = total_tokens > 0 && 2 * (int64_t)kSlices * dims.HV * num_seqs <= g_num_sms[dev] ? 2 : 1;
   if (parts > 1) args.init_states = reinterpret_cast<float*>(ws_states);
   if (chunks > 0 && total_tokens > 0) {  // with no tokens every chunk is empty
     args.tx_units = chunks * dims.HV;
@@ -1926,11 +1955,7 @@ extern "C" kda_status kda_prefill(kda_dims dims, kda_gate gate, const kda_bf16* 
     transform_kernel<<<transform_grid(args.tx_units, dev), kTxThreads, kTransformTcSmem, st>>>(args, maps);
     if ((s = launch_status()) != KDA_OK) return s;
   }
-  // one CTA per (sequence, head, slice, part) item where they fit the SMs,
-  // else as many CTAs as SMs, each looping over items
   args.parts = parts;
-  const int64_t items = (int64_t)kSlices * parts * dims.HV * num_seqs;
-  const bool multi = items > g_num_sms[dev];
   const dim3 grid((unsigned)(multi ? g_num_sms[dev] : (items > 0 ? items : 1)));
   const bool f16 = dims.dtype == KDA_DTYPE_F16;
   void (*const pass_kernel)(PrefillArgs) = multi ? (f16 ? state_pass_kernel<true, true> : state_pass_kernel<false, true>)

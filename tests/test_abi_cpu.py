@@ -47,11 +47,11 @@ REC_BYTES = 180352  # one (chunk, head) record, as include/kda.h states
 
 
 def test_workspace_size_formula(lib):
-    """align256(4 num_seqs) + (T / 64 + num_seqs) HV 180352 + num_seqs HV
+    """align256(4 num_seqs + 4) + (T / 64 + num_seqs) HV 180352 + num_seqs HV
     65536 bytes, as kda.h states; sizes past int32 tokens give SIZE_MAX so
     that no check passes."""
-    for HV, n, T in ((16, 1, 64), (16, 1, 4096), (16, 8, 32768), (4, 3, 100), (2, 70, 0)):
-        want = ((4 * n + 255) // 256) * 256 + (T // 64 + n) * HV * REC_BYTES + n * HV * 65536
+    for HV, n, T in ((16, 1, 64), (16, 1, 4096), (16, 8, 32768), (4, 3, 100), (2, 70, 0), (16, 64, 4096)):
+        want = ((4 * n + 4 + 255) // 256) * 256 + (T // 64 + n) * HV * REC_BYTES + n * HV * 65536
         assert kda.kda_prefill_workspace_size(kda.dims(HV), n, T) == want
     assert kda.kda_prefill_workspace_size(kda.dims(16), 1, 2 ** 31) == 2 ** 64 - 1
     assert kda.kda_prefill_workspace_size(kda.dims(16), 1, 2 ** 31 - 1) < 2 ** 63
