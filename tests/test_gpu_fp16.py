@@ -22,8 +22,8 @@ K = 128
 F16 = kda.KDA_DTYPE_F16
 
 
-def _prefill(d, Hq, HV, intermediate=False):
-    og, gg = gates(d, H=Hq, HV=HV)
+def _prefill(d, Hq, HV, intermediate=False, lower_bound=-5.0):
+    og, gg = gates(d, H=Hq, HV=HV, lower_bound=lower_bound)
     lens = d["lengths"]
     T, n = int(lens.sum()), len(lens)
     x = {name: dev_in(d[name]) for name in ("q", "k", "v", "g", "beta")}
@@ -63,6 +63,14 @@ def test_fp16_prefill_single_sequence_16_heads():
 def test_fp16_grouped_heads_prefill():
     d = inputs.prefill_inputs(seed=603, lengths=[200, 33], H=2, HV=4, slots=5, dtype="f16")
     _prefill(d, 2, 4)
+
+
+def test_fp16_grouped_heads_prefill_token_path():
+    """A bounded gate below the chunk form's range (lower_bound -8): every
+    sequence runs token by token, here with FP16 rows and two value heads
+    per q/k head."""
+    d = inputs.prefill_inputs(seed=604, lengths=[130, 1, 64, 70], H=2, HV=4, slots=6, gb_rows=280, dtype="f16")
+    _prefill(d, 2, 4, intermediate=True, lower_bound=-8.0)
 
 
 def test_fp16_decode_chained_steps():
