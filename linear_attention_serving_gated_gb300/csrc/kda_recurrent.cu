@@ -113,9 +113,9 @@ struct FoldSmem {
 
 // CTAs per SM the register allocation must allow: 7 (72 registers) lets the
 // 1024 CTAs of a 16-request verify run as one wave (tree verify fits there
-// with its row groups stepped together).  Tree verify with four row groups
-// (64-row CTAs, up to 128 registers) runs 4 per SM, and so does the
-// prefill's token-by-token path, which would spill at 72.
+// with its row groups stepped together).  Four row groups (64-row CTAs of
+// tree and ReplaySSM verify, up to 128 registers) run 4 per SM, and so does
+// the prefill's token-by-token path, which would spill at 72.
 template <int MODE, int GROUPS>
 constexpr int kMinCtasPerSm = GROUPS == 4 || MODE == kSeqPrefill ? 4 : 7;
 
@@ -534,8 +534,10 @@ kda_status launch_recurrent(const StepArgs& a, cudaStream_t stream, bool stages 
   // Small batches use 16-row CTAs so that even one request spreads over 128
   // CTAs; larger batches use 32-row CTAs to halve the per-CTA fold work.
   // Tree verify takes 64-row CTAs where their grid fits in one wave and the
-  // 32-row one does not (at 16 heads, 12 to 19 requests): its 96-register
-  // kernel runs 5 CTAs per SM, so 32-row CTAs need a second wave there.
+  // 32-row one does not (at 16 heads, 17 to 19 requests).  ReplaySSM verify,
+  // bound by its per-token steps and the fold rather than by bytes, takes
+  // them wherever they fill the SMs in one wave (at 16 heads, 5 to 19
+  // requests): half as many CTAs fold each request's tokens.
   const int64_t units = (int64_t)a.B * a.HV;
   const int sms = sm_count();
   if (sms <= 0) return KDA_ERR_CUDA;
@@ -544,9 +546,11 @@ kda_status launch_recurrent(const StepArgs& a, cudaStream_t stream, bool stages 
   if (units * 8 <= 2 * (int64_t)sms) {
     dim3 grid(kHeadDim / 16, a.HV, a.B);
     (f16 ? recurrent_kernel<MODE, 1, true> : recurrent_kernel<MODE, 1, false>)<<<grid, 128, 0, stream>>>(a);
-  } else if (MODE == kTree && units * (kHeadDim / 32) > (int64_t)kMinCtasPerSm<MODE, 2> * sms &&
-             units * (kHeadDim / 64) <= (int64_t)kMinCtasPerSm<MODE, 4> * sms) {
-    if constexpr (MODE == kTree) {
+  } else if ((MODE == kTree && units * (kHeadDim / 32) > (int64_t)kMinCtasPerSm<MODE, 2> * sms &&
+              units * (kHeadDim / 64) <= (int64_t)kMinCtasPerSm<MODE, 4> * sms) ||
+             (MODE == kChainReplay && units * (kHeadDim / 64) >= sms &&
+              units * (kHeadDim / 64) <= (int64_t)kMinCtasPerSm<MODE, 4> * sms)) {
+    if constexpr (MODE == kTree || MODE == kChainReplay) {
       dim3 grid(kHeadDim / 64, a.HV, a.B);
       (f16 ? recurrent_kernel<MODE, 4, true> : recurrent_kernel<MODE, 4, false>)<<<grid, 128, 0, stream>>>(a);
     }
