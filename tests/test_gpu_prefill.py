@@ -20,10 +20,11 @@ pytestmark = pytest.mark.gpu
 K = 128
 
 
-def run_both(d, H, varlen=True, intermediate=False, num_seqs=None, oracle=True):
-    """Runs the CUDA prefill and the oracle on the same inputs.
+def run_both(d, H, varlen=True, intermediate=False, num_seqs=None, oracle=True, gate_kw=None):
+    """Runs the CUDA prefill and the oracle on the same inputs (gate_kw: the
+    gate's options, default the pages' bounded gate at -5).
     Returns a dict with device results and oracle results."""
-    og, gg = gates(d, H=H)
+    og, gg = gates(d, H=H, **(gate_kw or {}))
     lens = d["lengths"]
     n = len(lens) if num_seqs is None else num_seqs
     T = int(lens.sum())
@@ -113,6 +114,18 @@ def test_prefill_with_no_tokens_leaves_the_pool_unchanged():
 def test_prefill_fixed_layout_equal_lengths():
     d = inputs.prefill_inputs(seed=21, lengths=[96, 96, 96], H=2, slots=5, varlen=False)
     check(run_both(d, 2, varlen=False), d)
+
+
+def test_prefill_fixed_layout_token_path():
+    """The fixed layout (no cu_seqlens) on the token-by-token path: a bounded
+    gate at -8, and given log-decays with one sequence out of range."""
+    d = inputs.prefill_inputs(seed=22, lengths=[130, 130, 130], H=2, slots=5, varlen=False)
+    check(run_both(d, 2, varlen=False, intermediate=True, gate_kw=dict(lower_bound=-8.0)), d)
+    d = inputs.prefill_inputs(seed=23, lengths=[130, 130, 130], H=2, slots=5, varlen=False)
+    rng = np.random.default_rng(24)
+    d["g"][:] = inputs.encode16(-rng.uniform(0.0, 5.5, d["g"].shape))
+    d["g"][130 + 65, 1, 7] = inputs.encode16(np.array([-9.0]))[0]  # sequence 1 only
+    check(run_both(d, 2, varlen=False, intermediate=True, gate_kw=dict(given_decay=True)), d)
 
 
 def test_single_token_prefill_does_not_poison_later_shapes():
@@ -274,3 +287,48 @@ def test_prefill_under_graph_capture_matches_eager():
     torch.cuda.synchronize()
     assert torch.equal(o_g, o_e)
     assert torch.equal(pool_g, pool_e)
+
+
+@pytest.mark.parametrize("given_decay", [False, True])
+def test_multi_item_prefill_under_graph_replays_matches_eager(given_decay):
+    """More pass items than SMs (300 sequences at 2 heads): the pass's CTAs
+    claim items from a workspace counter that each call clears first.
+    Replayed twice from a graph (the pool reset between replays), the result
+    equals the eager call's bit for bit; with given log-decays the clearing
+    is the flags' memset, and one flagged sequence runs token by token."""
+    H = 2
+    lens = [int(x) for x in np.random.default_rng(91).integers(1, 200, size=300)]
+    T = sum(lens)
+    d = inputs.prefill_inputs(seed=92, lengths=lens, H=H, slots=310, gb_rows=T + 9)
+    if given_decay:
+        rng = np.random.default_rng(93)
+        d["g"][:T] = inputs.encode16(-rng.uniform(0.0, 5.5, d["g"][:T].shape))
+        d["g"][lens[0] + 3, 1, 9] = inputs.encode16(np.array([-7.0]))[0]  # sequence 1
+    og, gg = gates(d, H=H, given_decay=given_decay)
+    x = {name: dev_bf16(d[name]) for name in ("q", "k", "v", "g", "beta")}
+    idx, cu = dev(d["state_idx"]), dev(d["cu_seqlens"])
+    pool0 = dev(d["pool"])
+    n = len(lens)
+    ws = torch.empty(kda.kda_prefill_workspace_size(kda.dims(H), n, T), dtype=torch.uint8, device="cuda")
+    pool_e = pool0.clone()
+    o_e = torch.empty((T, H, K), dtype=torch.bfloat16, device="cuda")
+    kda.kda_prefill(kda.dims(H), gg, x["q"], x["k"], x["v"], x["g"], x["beta"], pool_e, idx, cu, n, o_e,
+                    workspace=ws)
+    torch.cuda.synchronize()
+    opool = d["pool"].astype(np.float64)
+    o_ref = ko.prefill(og, d["q"], d["k"], d["v"], d["g"], d["beta"], opool, d["state_idx"], d["cu_seqlens"])
+    assert_o_close(o_e, o_ref)
+
+    pool_g = pool0.clone()
+    o_g = torch.empty_like(o_e)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        kda.kda_prefill(kda.dims(H), gg, x["q"], x["k"], x["v"], x["g"], x["beta"], pool_g, idx, cu, n,
+                        o_g, workspace=ws)
+    for _ in range(2):
+        pool_g.copy_(pool0)
+        o_g.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(o_g, o_e)
+        assert torch.equal(pool_g, pool_e)
