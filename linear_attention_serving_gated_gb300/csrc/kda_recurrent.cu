@@ -25,7 +25,9 @@
 //   * verify keeps the state in registers across the T draft tokens and
 //     writes each snapshot straight from registers; a tree node whose parent
 //     is not the previous node reloads the parent's snapshot, which this same
-//     thread wrote (so it is visible to it without any barrier).
+//     thread wrote (so it is visible to it without any barrier); snapshots
+//     that will be reloaded are stored with L1 evict-last priority, the
+//     others without allocating in L1.
 #include <atomic>
 
 #include "kda_host.h"
@@ -88,6 +90,21 @@ __device__ __forceinline__ float group_sum8(float x) {
   return x;
 }
 
+// Tree verify's snapshot stores: a snapshot that a later node reloads (its
+// parent is not the node just before it) stays in L1 with evict-last
+// priority, so that the reload, by the same thread, finds it there; the
+// others are not allocated in L1, which keeps room for the kept ones.
+__device__ __forceinline__ void st_keep_l1(float* p, float4 v) {
+  asm volatile("st.global.L1::evict_last.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(v.x), "f"(v.y), "f"(v.z),
+               "f"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ void st_skip_l1(float* p, float4 v) {
+  asm volatile("st.global.L1::no_allocate.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(v.x), "f"(v.y), "f"(v.z),
+               "f"(v.w)
+               : "memory");
+}
+
 __device__ __forceinline__ float dot16(const float4 (&x)[4], const float4 (&y)[4]) {
   float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
@@ -124,6 +141,7 @@ __global__ void __launch_bounds__(128, (kMinCtasPerSm<MODE, GROUPS>)) recurrent_
   constexpr int K = kHeadDim, V = kHeadDim;
   __shared__ __align__(16) FoldSmem fs;
   __shared__ int tree_par[kTokBlock];  // tree: the parents of the first kTokBlock nodes
+  __shared__ uint32_t tree_keep;       // tree: bit i, node i's snapshot is reloaded by a later node
   // raw BF16 token rows of this head: q, k, v, gate input, per token of the block
   __shared__ __align__(16) uint16_t raw_s[kTokBlock][4][kHeadDim];
   const int r = blockIdx.z + (MODE == kSeqPrefill ? args.seq0 : 0), h = blockIdx.y;
@@ -243,6 +261,14 @@ __global__ void __launch_bounds__(128, (kMinCtasPerSm<MODE, GROUPS>)) recurrent_
     }
     if (tid < kTokBlock && tid < T) tree_par[tid] = args.parent[(int64_t)r * T + tid];
     parents_ok = !__syncthreads_or(bad);
+    if (tid == 0) {  // read after the fold's barriers; past kTokBlock nodes, every snapshot is kept
+      uint32_t keep = T > kTokBlock ? 0xffffffffu : 0u;
+      for (int i = 1; i < T && i < kTokBlock; ++i) {
+        const int p = tree_par[i];
+        if (p >= 0 && p != i - 1) keep |= 1u << p;
+      }
+      tree_keep = keep;
+    }
     if (!parents_ok && reporter) set_error(args.err_flag, KDA_DEVERR_PARENT);
   }
   if (!ok || slot < 0) {  // padding or rejected request: zero outputs, touch no state
@@ -430,8 +456,13 @@ __global__ void __launch_bounds__(128, (kMinCtasPerSm<MODE, GROUPS>)) recurrent_
           if (sub == 0) args.o[(row * HV + h) * V + j] = parents_ok ? float_to_out16<F16>(out) : 0;
           if (MODE != kChainReplay && (MODE != kTree || parents_ok)) {  // ReplaySSM verify keeps no snapshots
             float* dst = MODE == kDecode ? root + (size_t)j * K : snap + (size_t)j * K;
+            if (t >= 32 || (tree_keep >> t & 1u)) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) *reinterpret_cast<float4*>(dst + i * 32 + lane_col) = S[gi][i];
+              for (int i = 0; i < 4; ++i) st_keep_l1(dst + i * 32 + lane_col, S[gi][i]);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 4; ++i) st_skip_l1(dst + i * 32 + lane_col, S[gi][i]);
+            }
           }
         }
       } else {
