@@ -104,6 +104,15 @@ __device__ __forceinline__ void st_skip_l1(float* p, float4 v) {
                "f"(v.w)
                : "memory");
 }
+// The state of decode and ReplaySSM verify (CTAs of two or more row groups)
+// is read once and, for decode, written once: neither needs L1.
+__device__ __forceinline__ float4 ld_skip_l1(const float* p) {
+  float4 v;
+  asm volatile("ld.global.L1::no_allocate.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "l"(p));
+  return v;
+}
 
 __device__ __forceinline__ float dot16(const float4 (&x)[4], const float4 (&y)[4]) {
   float2 acc = make_float2(0.f, 0.f);
@@ -290,8 +299,9 @@ __global__ void __launch_bounds__(128, (kMinCtasPerSm<MODE, GROUPS>)) recurrent_
   for (int gi = 0; gi < GROUPS; ++gi)
 #pragma unroll
     for (int i = 0; i < 4; ++i)
-      S[gi][i] = *reinterpret_cast<const float4*>(root + (size_t)(row0 + gi * 4) * K + i * 32 +
-                                                  lane_col);
+      S[gi][i] = (MODE == kDecode || MODE == kChainReplay) && GROUPS >= 2
+                     ? ld_skip_l1(root + (size_t)(row0 + gi * 4) * K + i * 32 + lane_col)
+                     : *reinterpret_cast<const float4*>(root + (size_t)(row0 + gi * 4) * K + i * 32 + lane_col);
 
   // (ReplaySSM verify: set once its copies have landed, in the first fold)
   float exp_alog = kEarlyGate && ga.A_log ? __expf(alog_early) : 0.f;
@@ -490,8 +500,13 @@ __global__ void __launch_bounds__(128, (kMinCtasPerSm<MODE, GROUPS>)) recurrent_
           if (MODE == kChainReplay || MODE == kSeqPrefill) continue;  // no snapshots
           if (MODE != kTree || parents_ok) {
             float* dst = MODE == kDecode ? root + (size_t)j * K : snap + (size_t)j * K;
+            if (MODE == kDecode && GROUPS >= 2) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) *reinterpret_cast<float4*>(dst + i * 32 + lane_col) = S[gi][i];
+              for (int i = 0; i < 4; ++i) st_skip_l1(dst + i * 32 + lane_col, S[gi][i]);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 4; ++i) *reinterpret_cast<float4*>(dst + i * 32 + lane_col) = S[gi][i];
+            }
           }
         }
       }
