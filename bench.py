@@ -60,9 +60,9 @@ LAYERS = 8  # default decode/verify/commit calls per timed replay (--layers)
 # traffic summary under profiles/).
 NCU_TRAFFIC = {
     # the transform launch of one 1x4096 prefill call, 16 heads, mean of two
-    # captured launches: read 68.43 MB (its inputs) + write 83.36 MB (the part
+    # captured launches: read 68.45 MB (its inputs) + write 83.41 MB (the part
     # of its per-chunk records that leaves L2 before the state pass reads it)
-    "prefill_transform": {"bytes": 151794176, "src": "38a403dbceb26ef8"},
+    "prefill_transform": {"bytes": 151863552, "src": "b299d1e64a6576be"},
 }
 VERIFY_SWEEP = (1, 2, 4, 8, 12, 16, 24, 32, 48)  # requests x 6 draft tokens, chain and tree
 DECODE_SWEEP = (1, 16)  # besides the core step's 48
