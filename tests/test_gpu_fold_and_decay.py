@@ -11,12 +11,13 @@ through prefill, decode and chain/tree verify:
   * beta_is_raw = 0: beta is given in [0, 1];
   * use_qk_l2norm = 0: q and k are drawn with unit-order norms (raw N(0, 1)
     keys of norm ~11 make the update unstable by definition);
-  * bounded gates with lower bounds -1 and -5.5 (the prefill's limit).
+  * bounded gates with lower bounds -1 and -5.5 (the chunk form's limit);
+    below it, -8, the prefill runs token by token.
 Slow decay is where the prefill's state pass carries information over many
 chunks, and where its precision matters: full-size prefills at 16 heads with
 log-decays in [-0.02, 0] (given) or a bounded gate whose argument is pushed
-far negative (g ~ -5 e^-12).  Given log-decays outside the prefill's range
-are flagged and leave the pool untouched.
+far negative (g ~ -5 e^-12).  Given log-decays outside the chunk form's
+range flag their sequence, which is then computed token by token.
 """
 import numpy as np
 import pytest
